@@ -1,0 +1,237 @@
+/*
+ * sdt.h -- C ABI of the shape-driven-tile library (libsdt.so) for GB300 (sm_103a).
+ *
+ * Two compute calls and the tile-selection calls around them:
+ *
+ *   gemm_f16   C = A . B, fp16 in, fp32 accumulate, fp16 out, with the CTA tile
+ *              chosen from the problem shape.
+ *   gemv_m1    y = W . x for a single activation row (M = 1 decode), streaming a
+ *              K-major weight matrix, bf16 or q8 (int8 + one fp16 scale per 32).
+ *
+ * Conventions for every call in this header:
+ *  - Pointers named A, B, C, x, W, scales, y are DEVICE pointers owned by the
+ *    caller (typically PyTorch-allocated).  The library never frees, keeps or
+ *    allocates device memory for them; it allocates no device memory at all.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream) owned by the
+ *    caller.  Work is enqueued on it asynchronously; the library never
+ *    synchronises on the hot path.  Kernel faults surface on the caller's next
+ *    synchronising CUDA call, as with any CUDA kernel.
+ *  - Layouts are tight row-major: A is MxK (row stride K), B is KxN (row stride
+ *    N), C is MxN (row stride N).  W is [N][K] ("K-major": each output's K
+ *    weights are contiguous), scales are [N][K/32].
+ *  - Return value: SDT_OK (0) or a negative sdt_status.  Argument errors are
+ *    detected on the host before anything is enqueued; the message of the last
+ *    failure on the calling thread is available from sdt_last_error().
+ *
+ * Sources (the pages this library restates; cited by title and section):
+ *  [P1] "Beating hipBLASLt on a Gaming GPU" -- sections "The result" (the
+ *       pipelined fp16 GEMM) and "The part that actually mattered" (tile
+ *       geometry chosen from how many blocks the grid yields).
+ *  [P2] "mojo-baro" -- "Four rounds on the decode shape" (M=1, K=4096,
+ *       N=12288 decode; K-major weights; q8 with a scale per 32 weights;
+ *       several contiguous columns per thread with wide loads; an
+ *       M=1-specialised kernel).
+ *  [P3] FlyDSL pull request "Speed up the RDNA3 GEMM up to 1.85x by choosing
+ *       the tile from the shape" -- "Changes" (pick_tile over feasible_tiles,
+ *       opt-in measured sweep frozen into an artefact, k-loop start stagger with
+ *       mask wraparound for power-of-two k-tile counts) and the third commit
+ *       message (the K-scan that isolates power-of-two row strides).
+ */
+#ifndef SDT_H
+#define SDT_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; declared here so this header needs no CUDA headers. */
+typedef struct CUstream_st *sdt_stream_t;
+
+typedef enum sdt_status {
+    SDT_OK = 0,
+    SDT_ERR_NULL = -1,               /* a required pointer is NULL */
+    SDT_ERR_ALIGN = -2,              /* a pointer is not 16-byte aligned */
+    SDT_ERR_SHAPE = -3,              /* negative dims, no feasible tile, N or K not a multiple of 8,
+                                        q8 with K not a multiple of 32 */
+    SDT_ERR_UNSUPPORTED_DEVICE = -4, /* current device is not compute capability 10.3 (sm_103) */
+    SDT_ERR_LAUNCH = -5,             /* the kernel launch was rejected by the CUDA runtime */
+    SDT_ERR_TIMEOUT = -6,            /* a kernel gave up a bounded wait (read by sdt_check_device_status) */
+    SDT_ERR_TILE = -7,               /* unknown tile id, or the forced tile is infeasible for the shape */
+    SDT_ERR_TABLE = -8,              /* tune table could not be read or parsed */
+    SDT_ERR_CUDA = -9,               /* another CUDA runtime / driver call failed */
+    SDT_ERR_ARG = -10                /* another invalid argument (e.g. stagger value) */
+} sdt_status;
+
+/* ------------------------------------------------------------------------ */
+/* Core calls                                                                */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * gemm_f16 -- C[M][N] = A[M][K] . B[K][N]; fp16 (IEEE binary16) operands,
+ * fp32 accumulation on the tensor cores, C rounded to fp16 (nearest even).
+ * [P1 "The result"; P3 "Changes"].
+ *
+ * The tile is the tune-table entry for (M,N,K) when one is loaded and
+ * feasible, otherwise sdt_pick_tile(M,N,K).  With SDT_AUTOTUNE=1 in the
+ * environment, the first call for a shape times every feasible tile on
+ * `stream` (synchronising it) and remembers the fastest for later calls.
+ * The k-loop stagger follows SDT_STAGGER ("auto" (default), "0", "1").
+ *
+ * Requirements: A, B, C 16-byte aligned; M, N, K >= 0.  M == 0 or N == 0 is a
+ * no-op; K == 0 writes C = 0.  Otherwise some tile must divide the shape
+ * (M % 64, N % 64, K % 64 == 0 and K >= 128 at the least) or SDT_ERR_SHAPE is
+ * returned; shapes with ragged edges are not handled.
+ */
+int gemm_f16(int64_t M, int64_t N, int64_t K,
+             const void *A, const void *B, void *C, sdt_stream_t stream);
+
+/*
+ * gemv_m1 -- y[n] = sum_k x[k] * W[n][k] for n < N  (M = 1 decode).
+ * [P2 "Four rounds on the decode shape", rounds v1-v4].
+ *
+ *   x       bf16 [K]
+ *   W       scales == NULL: bf16 [N][K];  scales != NULL: int8 [N][K] (q8)
+ *   scales  NULL, or fp16 [N][K/32]: weight k of row n is
+ *           q[n][k] * scales[n][k/32]; the scale multiplies each group sum.
+ *   y       fp32 [N] (written, not accumulated into)
+ *
+ * Requirements: x, W, y 16-byte aligned (scales 2-byte aligned); K a
+ * multiple of 8 (bf16) or 32 (q8); K, N <= 2^30.  N == 0 is a no-op; K == 0
+ * writes y = 0.
+ */
+int gemv_m1(int64_t K, int64_t N, const void *x, const void *W,
+            const void *scales, float *y, sdt_stream_t stream);
+
+/* The two arms of gemv_m1 called explicitly (same contract; the q8 arm requires scales). */
+int gemv_m1_bf16(int64_t K, int64_t N, const void *x, const void *W, float *y,
+                 sdt_stream_t stream);
+int gemv_m1_q8(int64_t K, int64_t N, const void *x, const void *W,
+               const void *scales, float *y, sdt_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Tile ladder, feasibility and selection  [P3 "Changes"; P1 tile rule]      */
+/* ------------------------------------------------------------------------ */
+
+/* Static description of one tile of the ladder. */
+typedef struct sdt_tile_desc {
+    int id;           /* index into the ladder, 0 .. sdt_num_tiles()-1 */
+    int BM, BN, BK;   /* output rows x columns covered (by the CTA pair when cta_group == 2), k-depth */
+    int cta_group;    /* 1, or 2 for a two-CTA (cluster pair) tile */
+    int stages;       /* depth of the shared-memory TMA/MMA ring */
+    int threads;      /* threads per CTA */
+    int smem_bytes;   /* dynamic shared memory per CTA, including alignment slack */
+    int tmem_cols;    /* tensor-memory columns allocated per CTA */
+    char name[24];    /* e.g. "128x256", "2cta_256x128" */
+} sdt_tile_desc;
+
+int sdt_num_tiles(void);
+/* Fills *out for tile `tile_id`; SDT_ERR_TILE for an unknown id, SDT_ERR_NULL for out == NULL. */
+int sdt_tile_info(int tile_id, sdt_tile_desc *out);
+/* Static name of a tile, or NULL for an unknown id. */
+const char *sdt_tile_name(int tile_id);
+
+/*
+ * Feasible tiles for (M,N,K) [P3 "Changes"]: a tile is feasible when it
+ * (i) divides the shape (BM | M, BN | N, BK | K), (ii) can fill the pipeline
+ * (at least two k-tiles), (iii) fits on chip (its shared memory within
+ * `smem_limit` bytes per block, its accumulator within 512 TMEM columns).
+ * Writes up to `cap` tile ids in ladder order to `ids` (may be NULL when
+ * cap == 0) and returns how many tiles are feasible (which may exceed cap),
+ * or a negative status.  The `_for` form needs no GPU; the plain form uses
+ * the current device's opt-in shared-memory limit.
+ */
+int sdt_feasible_tiles_for(int64_t M, int64_t N, int64_t K, int smem_limit,
+                           int *ids, int cap);
+int sdt_feasible_tiles(int64_t M, int64_t N, int64_t K, int *ids, int cap);
+
+/*
+ * pick_tile [P3 "Changes"; P1 "The part that actually mattered"]: the
+ * heuristic tile for (M,N,K) on a GPU with `sm_count` SMs, chosen among the
+ * feasible tiles by how many CTAs each grid yields against the SM count and a
+ * per-tile throughput fitted to a measured sweep.  Needs no GPU and measures
+ * nothing.  Returns a tile id, or SDT_ERR_SHAPE when no tile is feasible.
+ * The plain form reads the current device's SM count and shared-memory limit.
+ */
+int sdt_pick_tile_for(int64_t M, int64_t N, int64_t K, int sm_count, int smem_limit);
+int sdt_pick_tile(int64_t M, int64_t N, int64_t K);
+
+/*
+ * The launcher rule of [P1 "The part that actually mattered"] as printed for
+ * a 96-unit card and scaled to `units`: count the 128x128-equivalent blocks
+ * (M/128)*(N/128); >= units -> the 128x128 tile, >= 2*units/3 -> 64x128,
+ * else 64x64.  Returns that tile's id (the seed the fitted heuristic grew
+ * from; kept for comparison).
+ */
+int sdt_seed_tile(int64_t M, int64_t N, int units);
+
+/*
+ * gemm_f16 with a forced tile (for sweeps).  `stagger`: -1 = as gemm_f16
+ * (SDT_STAGGER / auto), 0 = off, 1 = on when the k-tile count is a power of
+ * two (otherwise silently off) [P3 "Changes", third commit message].
+ * SDT_ERR_TILE if the tile is unknown or infeasible for the shape.
+ */
+int gemm_f16_with_tile(int64_t M, int64_t N, int64_t K,
+                       const void *A, const void *B, void *C, sdt_stream_t stream,
+                       int tile_id, int stagger);
+
+/*
+ * Frozen tune table [P3 "Changes": the measured sweep can be frozen into an
+ * offline artefact].  Text file, one entry per line: "M N K tile_name
+ * [stagger]"; '#' starts a comment.  Loading replaces the current table.
+ * Entries whose tile is infeasible for their shape are rejected
+ * (SDT_ERR_TABLE, table left unchanged).  The table named by the environment
+ * variable SDT_TUNE_TABLE is loaded on the first gemm_f16 call.
+ * sdt_tune_table_lookup returns the tile id for a shape or -1.
+ */
+int sdt_load_tune_table(const char *path);
+void sdt_clear_tune_table(void);
+int sdt_tune_table_size(void);
+int sdt_tune_table_lookup(int64_t M, int64_t N, int64_t K);
+
+/* ------------------------------------------------------------------------ */
+/* Diagnostics                                                               */
+/* ------------------------------------------------------------------------ */
+
+/* Message of the last failed call on this thread ("" if none).  Valid until the next call. */
+const char *sdt_last_error(void);
+
+/*
+ * Every mbarrier wait in the kernels is bounded (by default 2 s).  A kernel
+ * that gives up records a code in a device status word and returns without
+ * trapping.  This call synchronises `stream`, reads and clears the word for
+ * the current device, and returns SDT_OK or SDT_ERR_TIMEOUT (SDT_ERR_CUDA if
+ * the stream itself reports an error).  `where` (may be NULL) receives the
+ * recorded code: 1 producer, 2 MMA issuer, 3 epilogue, 4 drain, 5 probe.
+ */
+int sdt_check_device_status(sdt_stream_t stream, int *where);
+
+/*
+ * Test hook for the bounded waits: launches one CTA of the GEMM kernel's
+ * wait routine on an mbarrier nothing ever arrives at, with the given limit
+ * in microseconds (1 .. 10,000,000).  The kernel gives up, records code 5 and
+ * returns; read it with sdt_check_device_status.
+ */
+int sdt_debug_timeout_probe(sdt_stream_t stream, int64_t limit_us);
+
+/*
+ * Number of TMA tensor maps encoded so far by this process (misses of the
+ * tensor-map cache, whose key holds the base pointer, both extents, the row
+ * stride and the box).  For tests of the cache key.
+ */
+int64_t sdt_debug_tensor_map_encodes(void);
+
+/* SM count and opt-in shared memory per block of the current device. */
+int sdt_device_sm_count(void);
+int sdt_device_smem_optin(void);
+
+/* ABI version of this header (bumped on incompatible changes). */
+#define SDT_ABI_VERSION 1
+int sdt_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDT_H */

@@ -1,0 +1,189 @@
+"""Shape-driven fp16 GEMM and M=1 decode GEMV for GB300 (sm_103a).
+
+Thin binding over libsdt.so (C ABI in include/sdt.h): the functions below only
+check and marshal arguments (tensor pointers, shapes, the current CUDA stream)
+and call the C entry points of the same names.  Every step of the computation
+runs in the library's CUDA kernels; there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from ._lib import SdtError, check, lib, sdt_tile_desc
+
+__all__ = [
+    "SdtError", "gemm_f16", "gemm_f16_with_tile", "gemv_m1", "gemv_m1_bf16", "gemv_m1_q8",
+    "feasible_tiles", "pick_tile", "seed_tile", "tile_info", "tiles", "tile_id",
+    "load_tune_table", "clear_tune_table", "tune_table_lookup", "check_device_status",
+    "debug_timeout_probe", "device_sm_count", "lib",
+]
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _need(t, name, dtype, ndim):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must be {ndim}-D")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (tight row-major)")
+
+
+def _gemm_args(A, B, C):
+    _need(A, "A", torch.float16, 2)
+    _need(B, "B", torch.float16, 2)
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: A is {tuple(A.shape)}, B is {tuple(B.shape)}")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float16, device=A.device)
+    else:
+        _need(C, "C", torch.float16, 2)
+        if tuple(C.shape) != (M, N):
+            raise ValueError(f"C must be {(M, N)}, got {tuple(C.shape)}")
+    return M, N, K, C
+
+
+def gemm_f16(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, *, stream=None):
+    """C = A @ B (fp16 in, fp32 accumulate, fp16 out) with the tile chosen from the shape."""
+    M, N, K, C = _gemm_args(A, B, C)
+    check(lib().gemm_f16(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(), _stream(stream)))
+    return C
+
+
+def gemm_f16_with_tile(A, B, C=None, *, tile, stagger: int = -1, stream=None):
+    """gemm_f16 with a forced ladder tile (id or name); stagger -1 auto, 0 off, 1 on."""
+    M, N, K, C = _gemm_args(A, B, C)
+    tid = tile_id(tile) if isinstance(tile, str) else int(tile)
+    check(lib().gemm_f16_with_tile(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(),
+                                   _stream(stream), tid, int(stagger)))
+    return C
+
+
+def _gemv_args(x, W, y, wdtype):
+    _need(x, "x", torch.bfloat16, 1)
+    _need(W, "W", wdtype, 2)
+    N, K = W.shape
+    if x.shape[0] != K:
+        raise ValueError(f"x has length {x.shape[0]}, W is {tuple(W.shape)} (K-major [N, K])")
+    if y is None:
+        y = torch.empty(N, dtype=torch.float32, device=x.device)
+    else:
+        _need(y, "y", torch.float32, 1)
+        if y.shape[0] != N:
+            raise ValueError("y must have length N")
+    return K, N, y
+
+
+def gemv_m1_bf16(x, W, y=None, *, stream=None):
+    """y[n] = sum_k x[k] W[n, k]; x bf16 [K], W bf16 [N, K] (K-major), y fp32 [N]."""
+    K, N, y = _gemv_args(x, W, y, torch.bfloat16)
+    check(lib().gemv_m1_bf16(K, N, x.data_ptr(), W.data_ptr(), y.data_ptr(), _stream(stream)))
+    return y
+
+
+def gemv_m1_q8(x, q, scales, y=None, *, stream=None):
+    """q8 decode: W[n, k] = q[n, k] * scales[n, k // 32]; q int8 [N, K], scales fp16 [N, K/32]."""
+    K, N, y = _gemv_args(x, q, y, torch.int8)
+    _need(scales, "scales", torch.float16, 2)
+    if K % 32 or tuple(scales.shape) != (N, K // 32):
+        raise ValueError(f"scales must be {(N, K // 32)} with K % 32 == 0")
+    check(lib().gemv_m1_q8(K, N, x.data_ptr(), q.data_ptr(), scales.data_ptr(), y.data_ptr(),
+                           _stream(stream)))
+    return y
+
+
+def gemv_m1(x, W, scales=None, y=None, *, stream=None):
+    """M=1 decode GEMV: bf16 weights when scales is None, else q8 (int8 + fp16 scale per 32)."""
+    if scales is None:
+        return gemv_m1_bf16(x, W, y, stream=stream)
+    return gemv_m1_q8(x, W, scales, y, stream=stream)
+
+
+# ---- tiles ---------------------------------------------------------------------
+
+
+def tile_info(tile_id: int) -> dict:
+    d = sdt_tile_desc()
+    check(lib().sdt_tile_info(int(tile_id), ctypes.byref(d)))
+    return {f: (getattr(d, f).decode() if f == "name" else getattr(d, f)) for f, _ in d._fields_}
+
+
+def tiles() -> list[dict]:
+    return [tile_info(i) for i in range(lib().sdt_num_tiles())]
+
+
+def tile_id(name: str) -> int:
+    for t in tiles():
+        if t["name"] == name:
+            return t["id"]
+    raise KeyError(name)
+
+
+def feasible_tiles(M: int, N: int, K: int, smem_limit: int | None = None) -> list[int]:
+    cap = 64
+    ids = (ctypes.c_int * cap)()
+    if smem_limit is None:
+        n = check(lib().sdt_feasible_tiles(M, N, K, ids, cap))
+    else:
+        n = check(lib().sdt_feasible_tiles_for(M, N, K, int(smem_limit), ids, cap))
+    return list(ids[: min(n, cap)])
+
+
+def pick_tile(M: int, N: int, K: int, sm_count: int | None = None, smem_limit: int | None = None) -> int:
+    if sm_count is None:
+        return check(lib().sdt_pick_tile(M, N, K))
+    return check(lib().sdt_pick_tile_for(M, N, K, int(sm_count),
+                                         int(smem_limit) if smem_limit is not None else 232448))
+
+
+def seed_tile(M: int, N: int, units: int) -> int:
+    return check(lib().sdt_seed_tile(M, N, units))
+
+
+def load_tune_table(path: str) -> None:
+    check(lib().sdt_load_tune_table(str(path).encode()))
+
+
+def clear_tune_table() -> None:
+    lib().sdt_clear_tune_table()
+
+
+def tune_table_lookup(M: int, N: int, K: int) -> int:
+    return lib().sdt_tune_table_lookup(M, N, K)
+
+
+# ---- diagnostics ------------------------------------------------------------------
+
+
+def check_device_status(stream=None) -> int:
+    """Synchronise the stream; raise SdtError(SDT_ERR_TIMEOUT) if a kernel gave up a wait."""
+    where = ctypes.c_int(0)
+    rc = lib().sdt_check_device_status(_stream(stream), ctypes.byref(where))
+    if rc < 0:
+        err = SdtError(rc, (lib().sdt_last_error() or b"").decode())
+        err.where = where.value
+        raise err
+    return 0
+
+
+def debug_timeout_probe(limit_us: int, stream=None) -> None:
+    check(lib().sdt_debug_timeout_probe(_stream(stream), int(limit_us)))
+
+
+def device_sm_count() -> int:
+    return check(lib().sdt_device_sm_count())

@@ -1,0 +1,561 @@
+// gemm_host.cu -- host side of gemm_f16: the tile ladder, feasible_tiles,
+// pick_tile, the frozen tune table, the opt-in measured sweep, TMA tensor maps
+// and the C-ABI entry points.
+//
+// Tile selection follows the FlyDSL pull request "Speed up the RDNA3 GEMM up to
+// 1.85x by choosing the tile from the shape", section "Changes": a heuristic
+// (pick_tile) that needs no GPU and measures nothing chooses among the tiles that
+// feasible_tiles admits; an opt-in measured sweep (SDT_AUTOTUNE=1) times every
+// feasible tile, and a sweep's result can be frozen into a table
+// (SDT_TUNE_TABLE) that overrides the heuristic.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+
+#include "gemm_kernel.cuh"
+#include "host_common.cuh"
+
+namespace sdt {
+
+using LaunchFn = int (*)(const CUtensorMap &, const CUtensorMap &, const GemmArgs &, cudaStream_t);
+
+// One rung of the tile ladder.  kt_cycles / fixed_cycles feed pick_tile's cost
+// model: SM cycles one CTA of this tile spends per 64-deep k-tile when it has
+// the SM to itself, and its per-CTA fixed cost (TMEM allocation, pipeline fill,
+// epilogue).  They are fitted to the measured sweep of every feasible tile.
+struct LadderTile {
+    int BM, BN, cta_group, stages;
+    const char *name;
+    LaunchFn launch;
+    int smem_per_stage;
+    int smem_fixed;
+    int tmem_cols;
+    double kt_cycles;
+    double fixed_cycles;
+};
+
+#define SDT_TILE(BM_, BN_, STAGES_, NAME_, KT_, FIX_)                                              \
+    LadderTile {                                                                                   \
+        BM_, BN_, 1, STAGES_, NAME_, &launch_gemm_tile<BM_, BN_>, TileCfg<BM_, BN_>::STAGE_BYTES,  \
+            TileCfg<BM_, BN_>::ALIGN_SLACK + TileCfg<BM_, BN_>::CTRL_BYTES,                        \
+            TileCfg<BM_, BN_>::TMEM_COLS, KT_, FIX_                                                \
+    }
+
+static const LadderTile kLadder[] = {
+    SDT_TILE(64, 64, 6, "64x64", 160.0, 3000.0),
+    SDT_TILE(64, 128, 4, "64x128", 290.0, 3500.0),
+    SDT_TILE(128, 64, 4, "128x64", 200.0, 3500.0),
+    SDT_TILE(128, 128, 6, "128x128", 330.0, 4500.0),
+    SDT_TILE(128, 256, 4, "128x256", 580.0, 7000.0),
+};
+static constexpr int kNumTiles = sizeof(kLadder) / sizeof(kLadder[0]);
+static constexpr int kDefaultSmemLimit = 232448;  // opt-in shared memory per block on sm_100-class parts
+static constexpr int kMaxRing = 24;
+static constexpr int64_t kMaxDim = int64_t(1) << 30;
+
+static int tile_stages(const LadderTile &t, int smem_limit) {
+    int s = t.stages;
+    if (const char *e = getenv("SDT_STAGES")) {
+        int v = atoi(e);
+        if (v >= 2 && v <= kMaxRing) s = v;
+    }
+    while (s > 2 && t.smem_fixed + s * t.smem_per_stage > smem_limit) --s;
+    return s;
+}
+
+static int tile_smem(const LadderTile &t, int stages) { return t.smem_fixed + stages * t.smem_per_stage; }
+
+static bool feasible(const LadderTile &t, int64_t M, int64_t N, int64_t K, int smem_limit) {
+    if (M <= 0 || N <= 0 || K <= 0) return false;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return false;
+    if (M % t.BM || N % t.BN || K % kBK) return false;               // (i) divides the shape
+    if (K / kBK < 2) return false;                                   // (ii) fills the pipeline
+    if (tile_smem(t, t.stages) > smem_limit) return false;           // (iii) fits in shared memory
+    if (t.tmem_cols > 512) return false;                             //       and in tensor memory
+    return true;
+}
+
+static int ctas_per_sm(const LadderTile &t, int smem_per_sm) {
+    int by_smem = smem_per_sm / (tile_smem(t, t.stages) + 1024);
+    int by_tmem = 512 / t.tmem_cols;
+    int by_threads = 2048 / TileCfg<64, 64>::THREADS;
+    int occ = by_smem < by_tmem ? by_smem : by_tmem;
+    occ = occ < by_threads ? occ : by_threads;
+    return occ < 1 ? 1 : occ;
+}
+
+// Estimated makespan (SM cycles) of tile t on the shape: the tensor work of all
+// CTAs spread over the SMs in whole waves, plus fixed costs per round of
+// co-resident CTAs.
+static double model_cycles(const LadderTile &t, int64_t M, int64_t N, int64_t K, int sm_count,
+                           int smem_per_sm) {
+    const double ctas = double(M / t.BM) * double(N / t.BN);
+    const double nK = double(K / kBK);
+    const int occ = ctas_per_sm(t, smem_per_sm);
+    const double waves_1 = std::ceil(ctas / sm_count);
+    const double rounds = std::ceil(ctas / (double(sm_count) * occ));
+    return waves_1 * nK * t.kt_cycles + rounds * t.fixed_cycles;
+}
+
+static int pick_for(int64_t M, int64_t N, int64_t K, int sm_count, int smem_limit, int smem_per_sm) {
+    int best = -1;
+    double best_cost = 0.0;
+    for (int i = 0; i < kNumTiles; ++i) {
+        if (!feasible(kLadder[i], M, N, K, smem_limit)) continue;
+        double c = model_cycles(kLadder[i], M, N, K, sm_count, smem_per_sm);
+        if (best < 0 || c < best_cost * (1.0 - 1e-9)) {
+            best = i;
+            best_cost = c;
+        }
+    }
+    return best;
+}
+
+static int find_tile(const char *name) {
+    for (int i = 0; i < kNumTiles; ++i)
+        if (!strcmp(kLadder[i].name, name)) return i;
+    return -1;
+}
+
+static bool is_pow2(int64_t v) { return v > 0 && (v & (v - 1)) == 0; }
+
+// ---- frozen tune table ------------------------------------------------------
+
+struct TuneEntry {
+    int tile;
+    int stagger;  // -1 = auto
+};
+using ShapeKey = std::tuple<int64_t, int64_t, int64_t>;
+static std::mutex g_table_mu;
+static std::map<ShapeKey, TuneEntry> g_table;
+static std::once_flag g_env_table_once;
+
+static int load_table_file(const char *path, std::map<ShapeKey, TuneEntry> *out) {
+    FILE *f = fopen(path, "r");
+    if (!f) return fail(SDT_ERR_TABLE, "cannot open tune table '%s'", path);
+    char line[512];
+    int lineno = 0;
+    std::map<ShapeKey, TuneEntry> tab;
+    while (fgets(line, sizeof line, f)) {
+        ++lineno;
+        char *hash = strchr(line, '#');
+        if (hash) *hash = 0;
+        long long M, N, K;
+        char name[64];
+        int stagger = -1;
+        int n = sscanf(line, "%lld %lld %lld %63s %d", &M, &N, &K, name, &stagger);
+        if (n <= 0) {
+            bool blank = true;
+            for (char *c = line; *c; ++c)
+                if (*c != ' ' && *c != '\t' && *c != '\n' && *c != '\r') blank = false;
+            if (blank) continue;
+        }
+        if (n < 4) {
+            fclose(f);
+            return fail(SDT_ERR_TABLE, "%s:%d: expected 'M N K tile [stagger]'", path, lineno);
+        }
+        int id = find_tile(name);
+        if (id < 0) {
+            fclose(f);
+            return fail(SDT_ERR_TABLE, "%s:%d: unknown tile '%s'", path, lineno, name);
+        }
+        if (!feasible(kLadder[id], M, N, K, kDefaultSmemLimit)) {
+            fclose(f);
+            return fail(SDT_ERR_TABLE, "%s:%d: tile %s is infeasible for %lldx%lldx%lld", path, lineno, name,
+                        M, N, K);
+        }
+        if (n == 5 && stagger != 0 && stagger != 1 && stagger != -1) {
+            fclose(f);
+            return fail(SDT_ERR_TABLE, "%s:%d: stagger must be -1, 0 or 1", path, lineno);
+        }
+        tab[ShapeKey(M, N, K)] = TuneEntry{id, n == 5 ? stagger : -1};
+    }
+    fclose(f);
+    *out = std::move(tab);
+    return SDT_OK;
+}
+
+static void load_env_table() {
+    std::call_once(g_env_table_once, [] {
+        const char *p = getenv("SDT_TUNE_TABLE");
+        if (!p || !*p) return;
+        std::map<ShapeKey, TuneEntry> tab;
+        if (load_table_file(p, &tab) == SDT_OK) {
+            std::lock_guard<std::mutex> lock(g_table_mu);
+            g_table = std::move(tab);
+        } else {
+            fprintf(stderr, "libsdt: SDT_TUNE_TABLE ignored: %s\n", sdt_last_error());
+        }
+    });
+}
+
+static bool table_lookup(int64_t M, int64_t N, int64_t K, TuneEntry *e) {
+    std::lock_guard<std::mutex> lock(g_table_mu);
+    auto it = g_table.find(ShapeKey(M, N, K));
+    if (it == g_table.end()) return false;
+    *e = it->second;
+    return true;
+}
+
+// ---- TMA tensor maps ---------------------------------------------------------
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// Cache key of one 2-D fp16 tensor map.  The row stride is part of the key: two
+// operands of one shape but different pitch must never share a map.  The same
+// function builds the key for the lookup and for the insert.
+struct MapKey {
+    uintptr_t ptr;
+    uint64_t inner, outer, row_stride_bytes;
+    uint32_t box_inner, box_outer;
+    bool operator<(const MapKey &o) const {
+        return std::tie(ptr, inner, outer, row_stride_bytes, box_inner, box_outer) <
+               std::tie(o.ptr, o.inner, o.outer, o.row_stride_bytes, o.box_inner, o.box_outer);
+    }
+};
+
+static MapKey map_key(const void *ptr, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                      uint32_t box_inner, uint32_t box_outer) {
+    return MapKey{reinterpret_cast<uintptr_t>(ptr), inner, outer, row_stride_bytes, box_inner, box_outer};
+}
+
+static std::mutex g_map_mu;
+static std::map<MapKey, CUtensorMap> g_maps;
+static uint64_t g_map_encodes = 0;
+
+// 2-D fp16 tensor map, 128-byte swizzle, inner dimension contiguous.
+static int tensor_map_f16(const void *ptr, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                          uint32_t box_inner, uint32_t box_outer, CUtensorMap *out) {
+    const MapKey key = map_key(ptr, inner, outer, row_stride_bytes, box_inner, box_outer);
+    {
+        std::lock_guard<std::mutex> lock(g_map_mu);
+        auto it = g_maps.find(key);
+        if (it != g_maps.end()) {
+            *out = it->second;
+            return SDT_OK;
+        }
+    }
+    auto fn = encode_fn();
+    if (!fn) return fail(SDT_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    CUtensorMap m;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_stride_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(SDT_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", int(r));
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    if (g_maps.size() >= 4096) g_maps.clear();
+    g_maps[key] = m;
+    ++g_map_encodes;
+    *out = m;
+    return SDT_OK;
+}
+
+// ---- launch ----------------------------------------------------------------------
+
+__global__ void zero_fill_f16(__half *C, size_t n) {
+    size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x;
+    const size_t stride = size_t(gridDim.x) * blockDim.x;
+    for (; i < n; i += stride) C[i] = __ushort_as_half(0);
+}
+
+static int env_int(const char *name, int dflt, int lo, int hi) {
+    const char *s = getenv(name);
+    if (!s || !*s) return dflt;
+    int v = atoi(s);
+    return v < lo ? lo : (v > hi ? hi : v);
+}
+
+static int stagger_default() {
+    const char *s = getenv("SDT_STAGGER");
+    if (!s || !*s || !strcasecmp(s, "auto")) return 1;
+    if (!strcmp(s, "0") || !strcasecmp(s, "off")) return 0;
+    if (!strcmp(s, "1") || !strcasecmp(s, "on")) return 1;
+    return 1;
+}
+
+static int validate_common(int64_t M, int64_t N, int64_t K, const void *A, const void *B, void *C) {
+    if (M < 0 || N < 0 || K < 0) return fail(SDT_ERR_SHAPE, "negative dimension (M=%lld N=%lld K=%lld)",
+                                             (long long)M, (long long)N, (long long)K);
+    if (M == 0 || N == 0) return SDT_OK;
+    if (!C || (K > 0 && (!A || !B))) return fail(SDT_ERR_NULL, "NULL operand pointer");
+    if ((reinterpret_cast<uintptr_t>(C) & 15) || (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 15) ||
+                                                             (reinterpret_cast<uintptr_t>(B) & 15))))
+        return fail(SDT_ERR_ALIGN, "A, B and C must be 16-byte aligned");
+    return SDT_OK;
+}
+
+// Runs the forced tile; assumes arguments are validated and the shape is non-empty with K > 0.
+static int run_tile(int tile_id, int stagger_req, int64_t M, int64_t N, int64_t K, const void *A,
+                    const void *B, void *C, cudaStream_t stream, const DeviceInfo &dev) {
+    const LadderTile &t = kLadder[tile_id];
+    if (!feasible(t, M, N, K, dev.smem_optin))
+        return fail(SDT_ERR_TILE, "tile %s is infeasible for %lldx%lldx%lld", t.name, (long long)M,
+                    (long long)N, (long long)K);
+    CUtensorMap tmA, tmB;
+    int rc = tensor_map_f16(A, uint64_t(K), uint64_t(M), uint64_t(K) * 2, kBK, uint32_t(t.BM), &tmA);
+    if (rc) return rc;
+    rc = tensor_map_f16(B, uint64_t(N), uint64_t(K), uint64_t(N) * 2, 64, kBK, &tmB);
+    if (rc) return rc;
+    int *status = nullptr;
+    rc = status_word(&status);
+    if (rc) return rc;
+
+    GemmArgs a;
+    a.C = static_cast<__half *>(C);
+    a.M = int(M);
+    a.N = int(N);
+    a.K = int(K);
+    a.num_m_tiles = int(M / t.BM);
+    a.num_n_tiles = int(N / t.BN);
+    a.num_k_tiles = int(K / kBK);
+    a.stages = tile_stages(t, dev.smem_optin);
+    const int want_stagger = stagger_req < 0 ? stagger_default() : stagger_req;
+    a.stagger = (want_stagger && is_pow2(a.num_k_tiles)) ? 1 : 0;
+    a.stagger_stride = env_int("SDT_STAGGER_STRIDE", 1, 1, 1 << 20);
+    a.raster_group = env_int("SDT_RASTER_GROUP", 8, 1, 1 << 20);
+    a.timeout_ns = wait_timeout_ns();
+    a.status = status;
+    if (int64_t(a.num_m_tiles) * a.num_n_tiles > int64_t(0x7fffffff))
+        return fail(SDT_ERR_SHAPE, "grid too large");
+    int e = t.launch(tmA, tmB, a, stream);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(SDT_ERR_LAUNCH, "launch of tile %s failed: %s", t.name, cudaGetErrorString(cudaError_t(e)));
+    }
+    return SDT_OK;
+}
+
+// SDT_AUTOTUNE=1: time every feasible tile on the caller's stream (synchronising
+// it) and remember the fastest for this shape.
+static int autotune_shape(int64_t M, int64_t N, int64_t K, const void *A, const void *B, void *C,
+                          cudaStream_t stream, const DeviceInfo &dev, TuneEntry *out) {
+    cudaEvent_t e0, e1;
+    if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(SDT_ERR_CUDA, "cudaEventCreate failed during autotune");
+    }
+    int best = -1;
+    float best_ms = 0.f;
+    for (int i = 0; i < kNumTiles; ++i) {
+        if (!feasible(kLadder[i], M, N, K, dev.smem_optin)) continue;
+        int rc = run_tile(i, -1, M, N, K, A, B, C, stream, dev);
+        if (rc) break;
+        cudaEventRecord(e0, stream);
+        for (int r = 0; r < 5 && rc == SDT_OK; ++r) rc = run_tile(i, -1, M, N, K, A, B, C, stream, dev);
+        cudaEventRecord(e1, stream);
+        if (cudaEventSynchronize(e1) != cudaSuccess) {
+            cudaGetLastError();
+            rc = fail(SDT_ERR_CUDA, "autotune timing failed");
+        }
+        if (rc) {
+            cudaEventDestroy(e0);
+            cudaEventDestroy(e1);
+            return rc;
+        }
+        float ms = 0.f;
+        cudaEventElapsedTime(&ms, e0, e1);
+        if (best < 0 || ms < best_ms) {
+            best = i;
+            best_ms = ms;
+        }
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    if (best < 0) return fail(SDT_ERR_SHAPE, "no feasible tile to autotune");
+    *out = TuneEntry{best, -1};
+    std::lock_guard<std::mutex> lock(g_table_mu);
+    g_table[ShapeKey(M, N, K)] = *out;
+    return SDT_OK;
+}
+
+static int gemm_dispatch(int64_t M, int64_t N, int64_t K, const void *A, const void *B, void *C,
+                         sdt_stream_t stream_h, int tile_id, int stagger) {
+    clear_error();
+    int rc = validate_common(M, N, K, A, B, C);
+    if (rc) return rc;
+    if (M == 0 || N == 0) return SDT_OK;
+    if (stagger < -1 || stagger > 1) return fail(SDT_ERR_ARG, "stagger must be -1, 0 or 1");
+    if (tile_id != -1 && (tile_id < 0 || tile_id >= kNumTiles))
+        return fail(SDT_ERR_TILE, "unknown tile id %d", tile_id);
+    DeviceInfo dev;
+    rc = current_device(&dev);
+    if (rc) return rc;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_h);
+    if (K == 0) {
+        if (M > kMaxDim || N > kMaxDim) return fail(SDT_ERR_SHAPE, "dimension too large");
+        const size_t n = size_t(M) * size_t(N);
+        const unsigned blocks = unsigned(std::min<size_t>((n + 255) / 256, size_t(dev.sm_count) * 8));
+        zero_fill_f16<<<blocks, 256, 0, stream>>>(static_cast<__half *>(C), n);
+        cudaError_t e = cudaGetLastError();
+        return e == cudaSuccess ? SDT_OK : fail(SDT_ERR_LAUNCH, "zero fill failed: %s", cudaGetErrorString(e));
+    }
+    if (N % 8 || K % 8) return fail(SDT_ERR_SHAPE, "N and K must be multiples of 8");
+    if (tile_id >= 0) return run_tile(tile_id, stagger, M, N, K, A, B, C, stream, dev);
+
+    load_env_table();
+    TuneEntry te;
+    if (table_lookup(M, N, K, &te) && feasible(kLadder[te.tile], M, N, K, dev.smem_optin))
+        return run_tile(te.tile, stagger >= 0 ? stagger : te.stagger, M, N, K, A, B, C, stream, dev);
+    if (env_flag("SDT_AUTOTUNE")) {
+        rc = autotune_shape(M, N, K, A, B, C, stream, dev, &te);
+        if (rc) return rc;
+        return run_tile(te.tile, stagger, M, N, K, A, B, C, stream, dev);
+    }
+    const int id = pick_for(M, N, K, dev.sm_count, dev.smem_optin, dev.smem_per_sm);
+    if (id < 0)
+        return fail(SDT_ERR_SHAPE, "no feasible tile for %lldx%lldx%lld (need M,N,K multiples of 64 and K >= 128)",
+                    (long long)M, (long long)N, (long long)K);
+    return run_tile(id, stagger, M, N, K, A, B, C, stream, dev);
+}
+
+}  // namespace sdt
+
+using namespace sdt;
+
+extern "C" {
+
+int gemm_f16(int64_t M, int64_t N, int64_t K, const void *A, const void *B, void *C, sdt_stream_t stream) {
+    return gemm_dispatch(M, N, K, A, B, C, stream, -1, -1);
+}
+
+int gemm_f16_with_tile(int64_t M, int64_t N, int64_t K, const void *A, const void *B, void *C,
+                       sdt_stream_t stream, int tile_id, int stagger) {
+    if (tile_id < 0 || tile_id >= kNumTiles) {
+        clear_error();
+        return fail(SDT_ERR_TILE, "unknown tile id %d", tile_id);
+    }
+    return gemm_dispatch(M, N, K, A, B, C, stream, tile_id, stagger);
+}
+
+int sdt_num_tiles(void) { return kNumTiles; }
+
+int sdt_tile_info(int tile_id, sdt_tile_desc *out) {
+    clear_error();
+    if (!out) return fail(SDT_ERR_NULL, "out is NULL");
+    if (tile_id < 0 || tile_id >= kNumTiles) return fail(SDT_ERR_TILE, "unknown tile id %d", tile_id);
+    const LadderTile &t = kLadder[tile_id];
+    memset(out, 0, sizeof *out);
+    out->id = tile_id;
+    out->BM = t.BM;
+    out->BN = t.BN;
+    out->BK = kBK;
+    out->cta_group = t.cta_group;
+    out->stages = t.stages;
+    out->threads = TileCfg<64, 64>::THREADS;
+    out->smem_bytes = tile_smem(t, t.stages);
+    out->tmem_cols = t.tmem_cols;
+    snprintf(out->name, sizeof out->name, "%s", t.name);
+    return SDT_OK;
+}
+
+const char *sdt_tile_name(int tile_id) {
+    if (tile_id < 0 || tile_id >= kNumTiles) return nullptr;
+    return kLadder[tile_id].name;
+}
+
+int sdt_feasible_tiles_for(int64_t M, int64_t N, int64_t K, int smem_limit, int *ids, int cap) {
+    clear_error();
+    if (cap < 0 || (cap > 0 && !ids)) return fail(SDT_ERR_NULL, "ids is NULL with cap > 0");
+    int n = 0;
+    for (int i = 0; i < kNumTiles; ++i) {
+        if (!feasible(kLadder[i], M, N, K, smem_limit)) continue;
+        if (n < cap) ids[n] = i;
+        ++n;
+    }
+    return n;
+}
+
+int sdt_feasible_tiles(int64_t M, int64_t N, int64_t K, int *ids, int cap) {
+    DeviceInfo dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    return sdt_feasible_tiles_for(M, N, K, dev.smem_optin, ids, cap);
+}
+
+int sdt_pick_tile_for(int64_t M, int64_t N, int64_t K, int sm_count, int smem_limit) {
+    clear_error();
+    if (sm_count <= 0) return fail(SDT_ERR_ARG, "sm_count must be positive");
+    // Shared memory per SM on sm_100-class parts is 228 KiB.
+    const int id = pick_for(M, N, K, sm_count, smem_limit, 233472);
+    if (id < 0) return fail(SDT_ERR_SHAPE, "no feasible tile");
+    return id;
+}
+
+int sdt_pick_tile(int64_t M, int64_t N, int64_t K) {
+    DeviceInfo dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    clear_error();
+    const int id = pick_for(M, N, K, dev.sm_count, dev.smem_optin, dev.smem_per_sm);
+    if (id < 0) return fail(SDT_ERR_SHAPE, "no feasible tile");
+    return id;
+}
+
+int sdt_seed_tile(int64_t M, int64_t N, int units) {
+    clear_error();
+    if (units <= 0 || M < 0 || N < 0) return fail(SDT_ERR_ARG, "bad arguments");
+    const int64_t blocks = (M / 128) * (N / 128);
+    const char *name = blocks >= units ? "128x128" : (3 * blocks >= 2 * int64_t(units) ? "64x128" : "64x64");
+    return find_tile(name);
+}
+
+int sdt_load_tune_table(const char *path) {
+    clear_error();
+    if (!path) return fail(SDT_ERR_NULL, "path is NULL");
+    std::map<ShapeKey, TuneEntry> tab;
+    int rc = load_table_file(path, &tab);
+    if (rc) return rc;
+    std::lock_guard<std::mutex> lock(g_table_mu);
+    g_table = std::move(tab);
+    return SDT_OK;
+}
+
+void sdt_clear_tune_table(void) {
+    std::lock_guard<std::mutex> lock(g_table_mu);
+    g_table.clear();
+}
+
+int sdt_tune_table_size(void) {
+    std::lock_guard<std::mutex> lock(g_table_mu);
+    return int(g_table.size());
+}
+
+int sdt_tune_table_lookup(int64_t M, int64_t N, int64_t K) {
+    TuneEntry e;
+    return table_lookup(M, N, K, &e) ? e.tile : -1;
+}
+
+// Number of tensor maps encoded so far (cache misses); for the cache-key tests.
+int64_t sdt_debug_tensor_map_encodes(void) {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    return int64_t(g_map_encodes);
+}
+
+}  // extern "C"

@@ -1,0 +1,249 @@
+// gemm_kernel.cuh -- tcgen05 fp16 GEMM kernel template, one CTA per output tile.
+//
+// C[M][N] = A[M][K] . B[K][N]; fp16 operands, fp32 accumulation in tensor memory,
+// fp16 output.  The CTA tile BM x BN is a template parameter so that the host can
+// pick it from the problem shape ("Beating hipBLASLt on a Gaming GPU", section
+// "The part that actually mattered": tile shape as a compile-time kernel
+// parameter, one of several, chosen per launch).
+//
+// Roles inside a 128-thread CTA:
+//   warp 0, lane 0 : TMA producer.  Per k-tile: wait for the ring slot to be free,
+//                    arm its "full" barrier with the byte count, issue TMA loads of
+//                    A[BM x 64] (K-major, 128-byte swizzle) and B[64 x BN] (N
+//                    contiguous, 128-byte swizzle, one 64-column box at a time).
+//   warp 1, lane 0 : MMA issuer.  Per k-tile: wait "full", issue 4 x
+//                    tcgen05.mma (K = 16 each) into the TMEM accumulator, then
+//                    tcgen05.commit to the slot's "empty" barrier.  After the last
+//                    k-tile, commit to "acc_full".
+//   all 4 warps    : epilogue.  Wait "acc_full", tcgen05.ld 32 columns at a time
+//                    from the warp's TMEM lane quarter, round to fp16, store C.
+//
+// The k-loop start stagger (FlyDSL pull request "Speed up the RDNA3 GEMM up to
+// 1.85x by choosing the tile from the shape", "Changes" and third commit message)
+// starts CTA b at k-tile (b * stride) & (nK - 1) and wraps with the same mask; the
+// host enables it only when nK is a power of two.
+//
+// CTAs are rasterised in bands of `raster_group` m-tiles so that the A and B
+// panels in flight at any moment stay resident in L2.
+//
+// Every wait is bounded by a deadline; on expiry the kernel records a code in
+// the device status word, drains its own TMA copies (bounded again), frees its
+// TMEM and returns.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+
+namespace sdt {
+
+constexpr int kBK = 64;  // k-depth per ring slot: one 128-byte swizzle row of fp16
+
+struct GemmArgs {
+    __half *C;
+    int M, N, K;
+    int num_m_tiles, num_n_tiles, num_k_tiles;
+    int stages;           // ring depth used by this launch (<= the tile's maximum)
+    int stagger;          // 1: per-CTA k-loop start stagger (num_k_tiles is a power of two)
+    int stagger_stride;   // k-tiles between the start points of consecutive CTAs
+    int raster_group;     // m-tiles per raster band
+    unsigned long long timeout_ns;
+    int *status;          // device status word (first error code wins)
+};
+
+template <int BM, int BN>
+struct TileCfg {
+    static constexpr int A_BYTES = BM * kBK * 2;
+    static constexpr int B_BYTES = BN * kBK * 2;
+    static constexpr int B_BOX_BYTES = 64 * kBK * 2;  // one 64-column box of B
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int TMEM_COLS = BN;               // fp32 accumulator columns (power of two)
+    static constexpr int THREADS = 128;
+    static constexpr int ALIGN_SLACK = 1024;           // dynamic smem base rounded up to 1024 B
+    static constexpr int CTRL_BYTES = 512;             // barriers + TMEM address + flags
+    __host__ __device__ static constexpr int smem_bytes(int stages) {
+        return ALIGN_SLACK + stages * STAGE_BYTES + CTRL_BYTES;
+    }
+    static_assert(BM == 64 || BM == 128, "BM must be 64 or 128");
+    static_assert(BN == 64 || BN == 128 || BN == 256, "BN must be 64, 128 or 256");
+};
+
+__device__ __forceinline__ void record_status(int *status, int code) {
+    if (status) atomicCAS(status, 0, code);
+}
+
+template <int BM, int BN>
+__global__ void __launch_bounds__(128, 1)
+    gemm_f16_tile_kernel(const __grid_constant__ CUtensorMap tmA,
+                         const __grid_constant__ CUtensorMap tmB, const GemmArgs p) {
+    using Cfg = TileCfg<BM, BN>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+
+    const int S = p.stages;
+    uint8_t *smA = smem;
+    uint8_t *smB = smem + S * Cfg::A_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smB + S * Cfg::B_BYTES);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + S;
+    uint64_t *acc_full = bars + 2 * S;
+    volatile uint32_t *ctrl = reinterpret_cast<volatile uint32_t *>(bars + 2 * S + 1);
+    // ctrl[0]: TMEM base address   ctrl[1]: error flag   ctrl[2]: k-tiles issued by TMA
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // Output tile of this CTA (banded raster order).
+    const int lin = blockIdx.x;
+    const int per_band = p.raster_group * p.num_n_tiles;
+    const int band = lin / per_band;
+    const int first_m = band * p.raster_group;
+    const int band_m = min(p.num_m_tiles - first_m, p.raster_group);
+    const int in_band = lin - band * per_band;
+    const int m_tile = first_m + in_band % band_m;
+    const int n_tile = in_band / band_m;
+    const int m0 = m_tile * BM;
+    const int n0 = n_tile * BN;
+    const int nK = p.num_k_tiles;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        mbar_init(smem_u32(acc_full), 1);
+        ctrl[1] = 0;
+        ctrl[2] = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(const_cast<uint32_t *>(&ctrl[0])), Cfg::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_d = ctrl[0];
+
+    const uint64_t t_start = global_timer_ns();
+    const uint64_t deadline = t_start + p.timeout_ns;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer ----------------
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        const int start = p.stagger
+            ? static_cast<int>((static_cast<uint32_t>(lin) * static_cast<uint32_t>(p.stagger_stride)) &
+                               static_cast<uint32_t>(nK - 1))
+            : 0;
+        int s = 0;
+        uint32_t phase = 0;
+        for (int i = 0; i < nK; ++i) {
+            if (!mbar_wait(smem_u32(&empty[s]), phase ^ 1u, deadline)) {
+                record_status(p.status, kSiteProducer);
+                ctrl[1] = 1;
+                break;
+            }
+            if (ctrl[1]) break;
+            const int kt = p.stagger ? ((start + i) & (nK - 1)) : i;
+            const uint32_t fb = smem_u32(&full[s]);
+            mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
+            tma_load_2d(smem_u32(smA + s * Cfg::A_BYTES), &tmA, fb, kt * kBK, m0);
+#pragma unroll
+            for (int c = 0; c < BN / 64; ++c)
+                tma_load_2d(smem_u32(smB + s * Cfg::B_BYTES + c * Cfg::B_BOX_BYTES), &tmB, fb,
+                            n0 + c * 64, kt * kBK);
+            ctrl[2] = i + 1;
+            if (++s == S) { s = 0; phase ^= 1u; }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer ----------------
+        constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
+        int s = 0;
+        uint32_t phase = 0;
+        for (int i = 0; i < nK; ++i) {
+            if (!mbar_wait(smem_u32(&full[s]), phase, deadline)) {
+                record_status(p.status, kSiteMma);
+                ctrl[1] = 1;
+                break;
+            }
+            tc_fence_after();
+            // A: K-major, 128 B rows, 8-row groups 1024 B apart (SBO); +32 B per K=16 step.
+            // B: N-major, 64-column boxes BK*128 B apart (LBO), 8-row k groups 1024 B apart
+            //    (SBO); +2048 B per K=16 step.
+            const uint64_t a_desc = smem_desc_sw128(smem_u32(smA + s * Cfg::A_BYTES), 16, 1024);
+            const uint64_t b_desc =
+                smem_desc_sw128(smem_u32(smB + s * Cfg::B_BYTES), Cfg::B_BOX_BYTES, 1024);
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+                umma_f16(tmem_d, a_desc + 2ull * kk, b_desc + 128ull * kk, idesc,
+                         (i > 0 || kk > 0) ? 1u : 0u);
+            umma_commit(smem_u32(&empty[s]));
+            if (++s == S) { s = 0; phase ^= 1u; }
+        }
+        umma_commit(smem_u32(acc_full));
+    }
+    __syncwarp();
+
+    // ---------------- epilogue: TMEM -> registers -> fp16 -> global ----------------
+    const bool acc_ok = mbar_wait_sleepy(smem_u32(acc_full), 0, t_start + 3ull * p.timeout_ns);
+    if (!acc_ok) {
+        record_status(p.status, kSiteEpilogue);
+        ctrl[1] = 1;
+    }
+    tc_fence_after();
+    {
+        // Accumulator row r sits in TMEM lane r for M = 128; for M = 64 rows
+        // 16q .. 16q+15 sit in lanes 32q .. 32q+15 of lane quarter q.
+        const int row = (BM == 128) ? (warp * 32 + lane) : (warp * 16 + lane);
+        const bool row_valid = (BM == 128) || (lane < 16);
+        const uint32_t taddr_row = tmem_d + (static_cast<uint32_t>(warp * 32) << 16);
+        __half *crow = p.C + static_cast<size_t>(m0 + row) * p.N + n0;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr_row + c, r);
+            tmem_ld_wait();
+            if (row_valid && acc_ok) {
+                uint32_t h[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    __half2 v = __floats2half2_rn(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+                    h[j] = *reinterpret_cast<uint32_t *>(&v);
+                }
+                uint4 *dst = reinterpret_cast<uint4 *>(crow + c);
+                dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+                dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+                dst[2] = make_uint4(h[8], h[9], h[10], h[11]);
+                dst[3] = make_uint4(h[12], h[13], h[14], h[15]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+
+    if (threadIdx.x == 0 && ctrl[1]) {
+        // Drain: wait (bounded) for every TMA copy this CTA issued and may not have seen land.
+        const int issued = static_cast<int>(ctrl[2]);
+        const uint64_t drain_deadline = global_timer_ns() + p.timeout_ns;
+        for (int i = max(0, issued - S); i < issued; ++i) {
+            if (!mbar_wait(smem_u32(&full[i % S]), static_cast<uint32_t>((i / S) & 1), drain_deadline)) {
+                record_status(p.status, kSiteDrain);
+                break;
+            }
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem_d, Cfg::TMEM_COLS);
+    }
+}
+
+// Host-side launcher, one instantiation per ladder tile (defined in gemm_tiles.cu).
+template <int BM, int BN>
+int launch_gemm_tile(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args,
+                     cudaStream_t stream);
+
+}  // namespace sdt

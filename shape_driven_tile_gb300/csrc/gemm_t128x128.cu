@@ -1,0 +1,3 @@
+// Tile 128x128 of the GEMM ladder (one translation unit per tile).
+#include "gemm_launch.cuh"
+SDT_INSTANTIATE_GEMM_TILE(128, 128)

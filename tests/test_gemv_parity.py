@@ -1,0 +1,104 @@
+"""gemv_m1 (M=1 decode) on the GPU against the fp64 CPU oracle, through the C ABI."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import shape_driven_tile_gb300 as sdt
+from shape_driven_tile_gb300 import inputs
+from _parity import assert_close, u16
+
+pytestmark = pytest.mark.gpu
+
+K_DEC, N_DEC = 4096, 12288
+VARIANTS = ["1,4", "1,8", "2,2", "2,4", "4,2", "4,4"]
+
+
+@pytest.fixture
+def variant(request):
+    old = os.environ.get("SDT_GEMV_VARIANT")
+    os.environ["SDT_GEMV_VARIANT"] = request.param
+    yield request.param
+    if old is None:
+        del os.environ["SDT_GEMV_VARIANT"]
+    else:
+        os.environ["SDT_GEMV_VARIANT"] = old
+
+
+def bf16_case(K, N, seed):
+    x = inputs.uniform((K,), seed=seed, dtype=torch.bfloat16)
+    W = inputs.uniform((N, K), seed=seed + 1, dtype=torch.bfloat16)
+    return x, W
+
+
+@pytest.mark.parametrize("variant", VARIANTS, indirect=True)
+def test_decode_bf16_full(cuda_device, variant):
+    x, W = bf16_case(K_DEC, N_DEC, inputs.seed_for(3, 0))
+    y = torch.full((N_DEC,), float("nan"), device=cuda_device)
+    sdt.gemv_m1(x.to(cuda_device), W.to(cuda_device), y=y)
+    sdt.check_device_status()
+    assert_close(y.cpu().numpy(), oracle.gemv_bf16(u16(x), u16(W)), K_DEC, f"bf16 {variant}")
+
+
+@pytest.mark.parametrize("variant", VARIANTS, indirect=True)
+def test_decode_q8_full(cuda_device, variant):
+    x = inputs.uniform((K_DEC,), seed=inputs.seed_for(3, 0), dtype=torch.bfloat16)
+    q, s = inputs.q8_weights(N_DEC, K_DEC, seed=inputs.seed_for(3, 1))
+    y = torch.full((N_DEC,), float("nan"), device=cuda_device)
+    sdt.gemv_m1(x.to(cuda_device), q.to(cuda_device), s.to(cuda_device), y=y)
+    sdt.check_device_status()
+    ref = oracle.gemv_q8(u16(x), q.numpy(), u16(s))
+    # the q8 weights carry a scale of ~5e-3: the absolute bound is met with room to spare
+    assert_close(y.cpu().numpy(), ref, K_DEC, f"q8 {variant}")
+
+
+def test_decode_bf16_integer_exact(cuda_device):
+    x = inputs.integers((K_DEC,), seed=71, dtype=torch.bfloat16)
+    W = inputs.integers((N_DEC, K_DEC), seed=72, dtype=torch.bfloat16)
+    y = sdt.gemv_m1(x.to(cuda_device), W.to(cuda_device)).cpu().double().numpy()
+    assert np.array_equal(y, oracle.gemv_bf16(u16(x), u16(W)))
+
+
+def test_decode_q8_integer_exact(cuda_device):
+    x = inputs.integers((K_DEC,), seed=73, dtype=torch.bfloat16)
+    q, s = inputs.q8_weights_exact(N_DEC, K_DEC, seed=74)
+    y = sdt.gemv_m1(x.to(cuda_device), q.to(cuda_device), s.to(cuda_device)).cpu().double().numpy()
+    assert np.array_equal(y, oracle.gemv_q8(u16(x), q.numpy(), u16(s)))
+
+
+@pytest.mark.parametrize("K,N", [(8, 5), (40, 17), (256, 1), (4096, 12291), (4104, 333), (12288, 4096)])
+def test_ragged_bf16(cuda_device, K, N):
+    x, W = bf16_case(K, N, 81)
+    y = sdt.gemv_m1(x.to(cuda_device), W.to(cuda_device)).cpu().numpy()
+    assert_close(y, oracle.gemv_bf16(u16(x), u16(W)), K, f"bf16 K={K} N={N}")
+
+
+@pytest.mark.parametrize("K,N", [(32, 3), (96, 17), (4096, 12291), (4128, 65), (12288, 4096)])
+def test_ragged_q8(cuda_device, K, N):
+    x = inputs.uniform((K,), seed=91, dtype=torch.bfloat16)
+    q, s = inputs.q8_weights(N, K, seed=92)
+    y = sdt.gemv_m1(x.to(cuda_device), q.to(cuda_device), s.to(cuda_device)).cpu().numpy()
+    assert_close(y, oracle.gemv_q8(u16(x), q.numpy(), u16(s)), K, f"q8 K={K} N={N}")
+
+
+def test_zero_k_and_empty(cuda_device):
+    x = torch.empty(0, dtype=torch.bfloat16, device=cuda_device)
+    W = torch.empty((7, 0), dtype=torch.bfloat16, device=cuda_device)
+    y = torch.full((7,), float("nan"), device=cuda_device)
+    sdt.gemv_m1(x, W, y=y)
+    torch.cuda.synchronize()
+    assert bool((y == 0).all())
+    W = torch.empty((0, 64), dtype=torch.bfloat16, device=cuda_device)
+    assert sdt.gemv_m1(torch.zeros(64, dtype=torch.bfloat16, device=cuda_device), W).shape == (0,)
+
+
+def test_rotating_buffers_each_correct(cuda_device):
+    # The benchmark cycles through several weight buffers; each must give its own product.
+    x = inputs.uniform((K_DEC,), seed=101, dtype=torch.bfloat16)
+    xd = x.to(cuda_device)
+    for i in range(3):
+        W = inputs.uniform((2048, K_DEC), seed=102 + i, dtype=torch.bfloat16)
+        y = sdt.gemv_m1(xd, W.to(cuda_device)).cpu().numpy()
+        assert_close(y, oracle.gemv_bf16(u16(x), u16(W)), K_DEC, f"buffer {i}")

@@ -1,0 +1,133 @@
+"""Host-side tile logic of libsdt against the oracle's plain rules (no GPU).
+
+feasible_tiles is integer work, so it must agree with the oracle's three
+feasibility rules exactly; pick_tile must only return feasible tiles and keep
+the widest tile on deep grids; the seed rule must reproduce the pages' table.
+"""
+import itertools
+import os
+
+import pytest
+
+import shape_driven_tile_gb300 as sdt
+from oracle import tiles as otiles
+
+SMEM = 232448
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+SIZES = [0, 64, 128, 192, 256, 320, 512, 768, 1000, 1024, 1536, 1984, 2048, 2304, 4096, 8192]
+
+
+def ladder():
+    return sdt.tiles()
+
+
+@pytest.mark.parametrize("smem", [SMEM, 150_000, 100_000, 50_000])
+def test_feasible_tiles_match_oracle_rules(smem):
+    ts = ladder()
+    for M, N, K in itertools.product(SIZES, SIZES[:8], [0, 64, 128, 192, 1920, 2048]):
+        want = [t["id"] for t in ts if otiles.feasible(M, N, K, t, smem)]
+        assert sdt.feasible_tiles(M, N, K, smem_limit=smem) == want, (M, N, K, smem)
+
+
+def test_feasible_count_beyond_cap():
+    n = sdt.lib().sdt_feasible_tiles_for(256, 256, 256, SMEM, None, 0)
+    assert n == len(sdt.feasible_tiles(256, 256, 256, smem_limit=SMEM)) > 0
+
+
+@pytest.mark.parametrize("sm", [96, 148, 152])
+def test_pick_tile_is_always_feasible(sm):
+    for M, N, K in itertools.product(SIZES[1:], SIZES[1:], [128, 256, 2048, 4096]):
+        feas = sdt.feasible_tiles(M, N, K, smem_limit=SMEM)
+        if not feas:
+            with pytest.raises(sdt.SdtError):
+                sdt.pick_tile(M, N, K, sm_count=sm)
+            continue
+        assert sdt.pick_tile(M, N, K, sm_count=sm) in feas
+
+
+@pytest.mark.parametrize("sm", [148, 152])
+def test_pick_tile_keeps_wide_tile_on_deep_grids(sm):
+    # Once even the widest single-CTA tile cuts several waves of CTAs, there is no
+    # occupancy reason to move to a narrower one (the FlyDSL pull request's second
+    # safety property, restated for this ladder).
+    big = [t for t in ladder() if t["cta_group"] == 1 and t["BM"] * t["BN"] >= 128 * 256]
+    for n in (6144, 8192, 12288, 16384):
+        ctas = (n // 128) * (n // 256)
+        assert ctas >= 4 * sm
+        pick = sdt.tile_info(sdt.pick_tile(n, n, n, sm_count=sm))
+        assert pick["BM"] * pick["BN"] >= 128 * 128, (n, pick["name"])
+        assert big
+
+
+def test_pick_tile_uses_small_tiles_on_small_grids():
+    # 256^3 cuts only 4 CTAs of 128x128 (the pages' "cuts only 4 workgroups"): the pick
+    # must cut at least as many CTAs as 128x128 would, and more when it can.
+    t = sdt.tile_info(sdt.pick_tile(256, 256, 256, sm_count=148))
+    assert (256 // t["BM"]) * (256 // t["BN"]) >= 4
+    assert t["BM"] * t["BN"] <= 128 * 64
+
+
+def test_seed_rule_matches_oracle_and_golden():
+    for M, N in itertools.product(range(128, 4097, 128), [128, 512, 1024, 2048, 4096]):
+        for units in (96, 148, 152):
+            want = otiles.seed_tile(M, N, units)
+            assert sdt.tile_info(sdt.seed_tile(M, N, units))["name"] == want
+    with open(os.path.join(GOLDEN, "tile_rule_96cu.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                size, tile = line.split()[:2]
+                assert sdt.tile_info(sdt.seed_tile(int(size), int(size), 96))["name"] == tile
+
+
+def test_pick_tile_errors():
+    with pytest.raises(sdt.SdtError) as e:
+        sdt.pick_tile(100, 256, 256, sm_count=148)
+    assert e.value.status == "SDT_ERR_SHAPE"
+    with pytest.raises(sdt.SdtError):
+        sdt.pick_tile(256, 256, 256, sm_count=0)
+
+
+# ---- tune table ----------------------------------------------------------------------
+
+
+def test_tune_table_roundtrip(tmp_path):
+    p = tmp_path / "table.txt"
+    p.write_text("# frozen sweep\n256 256 256 64x64\n\n4096 4096 4096 128x256 1  # staggered\n")
+    sdt.load_tune_table(str(p))
+    try:
+        assert sdt.lib().sdt_tune_table_size() == 2
+        assert sdt.tile_info(sdt.tune_table_lookup(256, 256, 256))["name"] == "64x64"
+        assert sdt.tile_info(sdt.tune_table_lookup(4096, 4096, 4096))["name"] == "128x256"
+        assert sdt.tune_table_lookup(512, 512, 512) == -1
+    finally:
+        sdt.clear_tune_table()
+    assert sdt.lib().sdt_tune_table_size() == 0
+
+
+@pytest.mark.parametrize("body,needle", [
+    ("256 256 256 99x99\n", "unknown tile"),
+    ("192 256 256 128x128\n", "infeasible"),
+    ("256 256\n", "expected"),
+    ("256 256 256 64x64 7\n", "stagger"),
+])
+def test_tune_table_rejects_bad_entries(tmp_path, body, needle):
+    p = tmp_path / "bad.txt"
+    p.write_text("512 512 512 64x64\n" + body)
+    good = tmp_path / "good.txt"
+    good.write_text("1024 1024 1024 128x128\n")
+    sdt.load_tune_table(str(good))
+    try:
+        with pytest.raises(sdt.SdtError) as e:
+            sdt.load_tune_table(str(p))
+        assert e.value.status == "SDT_ERR_TABLE"
+        assert needle in str(e.value)
+        # a rejected table leaves the previous one in place
+        assert sdt.lib().sdt_tune_table_size() == 1
+    finally:
+        sdt.clear_tune_table()
+
+
+def test_tune_table_missing_file():
+    with pytest.raises(sdt.SdtError):
+        sdt.load_tune_table("/nonexistent/table.txt")
