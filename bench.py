@@ -1,0 +1,840 @@
+"""Benchmark of the shape-driven fp16 GEMM + M=1 decode GEMV on GB300.
+
+Default run (`python bench.py [--gpus N] [--steps K] [--warmup W]`):
+
+  one step = the whole hot path over one batch of synthetic input:
+    * fp16 GEMM C = A.B for every square size M=N=K in {256, 512, 768, 1024,
+      1536, 2048, 2560, 3072, 3584, 4096}, tile chosen by pick_tile;
+    * the M=1 decode GEMV, K=4096, N=12288, bf16 weights and q8 weights,
+      each from one of 8 rotating weight buffers (so every launch streams
+      its weights from HBM).
+  The step's working set (~1.6 GB) is far larger than the 129 MB L2, so no
+  explicit flush is needed between timed steps.
+
+  value = FLOPs of all timed steps on all ranks / the slowest rank's timed
+  wall time (CUDA events on the launching stream, barrier + synchronise on
+  both sides), in TFLOP/s.  Rank 0 prints one JSON line.
+
+Other modes (--mode): `sweep` times every feasible tile per square size and
+reports pick_tile's slowdown against the best; `kscan` the K-scan with the
+stagger on and off; `decode` the decode protocol (200 launches x 10
+repeats); `large` the 8192..16384 squares.  They print one JSON line each.
+
+`--impl reference` times the CPU oracle (the only implementation the pages'
+method has here) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fp16 GEMM TFLOP/s per size (% tensor peak); M=1 decode µs and HBM GB/s"
+SWEEP = [256, 512, 768, 1024, 1536, 2048, 2560, 3072, 3584, 4096]
+KSCAN = [1920, 1984, 2048, 2112, 2176, 2304]
+LARGE = [8192, 12288, 16384]
+DEC_K, DEC_N, DEC_BUFFERS = 4096, 12288, 8
+WORKLOAD = ("square fp16 GEMM sweep M=N=K in {256,512,768,1024,1536,2048,2560,3072,3584,4096} "
+            "(pick_tile) + M=1 decode GEMV K=4096 N=12288, bf16 and q8 arms, 8 rotating weight buffers")
+
+
+# ---------------------------------------------------------------------------------------------
+# workload arithmetic
+# ---------------------------------------------------------------------------------------------
+
+
+def gemm_flops(M, N, K):
+    return 2.0 * M * N * K
+
+
+def gemm_bytes(M, N, K):
+    """Compulsory DRAM bytes of one fp16 GEMM: read A and B once, write C once."""
+    return 2.0 * (M * K + K * N + M * N)
+
+
+def decode_bytes(K, N, fmt, scale_bytes=2, group=32):
+    """Bytes one decode GEMV must move: weights (+ scales), x (bf16) and y (fp32)."""
+    if fmt == "bf16":
+        w = 2 * K * N
+    else:
+        w = K * N + (K // group) * N * scale_bytes
+    return w + 2 * K + 4 * N
+
+
+def decode_weight_bytes(K, N, fmt, scale_bytes=2, group=32):
+    return 2 * K * N if fmt == "bf16" else K * N + (K // group) * N * scale_bytes
+
+
+def step_flops():
+    return sum(gemm_flops(n, n, n) for n in SWEEP) + 2 * (2.0 * DEC_K * DEC_N)
+
+
+# ---------------------------------------------------------------------------------------------
+# distributed bookkeeping (replicas only: no data-path collective)
+# ---------------------------------------------------------------------------------------------
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(backend):
+    import torch.distributed as dist
+
+    world, rank, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        os.environ.setdefault("MASTER_PORT", "29500")
+        dist.init_process_group(backend=backend, rank=rank, world_size=world)
+    return world, rank
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_value(units_per_rank_per_step: float, steps: int, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: units all ranks processed / the slowest rank's time."""
+    return units_per_rank_per_step * steps * world / max_seconds
+
+
+# ---------------------------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------------------------
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while the timed region runs."""
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu_index = gpu_index
+        self.period_ms = period_ms
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="sdt_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms), "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        return parse_clock_csv(open(self.path).read() if self.path and os.path.exists(self.path) else "")
+
+
+def parse_clock_csv(text: str):
+    rows = []
+    for line in text.splitlines():
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            rows.append(dict(sm=float(parts[1]), sm_max=float(parts[2]),
+                             power=float(parts[3]) if parts[3] not in ("[N/A]", "N/A") else None,
+                             active=parts[4], hw=parts[5], hw_thermal=parts[6], sw_thermal=parts[7],
+                             sw_power=parts[8]))
+        except ValueError:
+            continue
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    # samples "under load": the SM clock above half of its maximum
+    load = [r for r in rows if r["sm"] > 0.5 * r["sm_max"]] or rows
+    reasons = set()
+    for r in rows:
+        for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                          ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+            if r[key].lower() == "active":
+                reasons.add(name)
+    pw = [r["power"] for r in load if r["power"] is not None]
+    return {"sm_mhz": statistics.median(r["sm"] for r in load), "sm_max_mhz": max(r["sm_max"] for r in rows),
+            "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(load),
+            "power_w_max": max(pw) if pw else None}
+
+
+# ---------------------------------------------------------------------------------------------
+# peaks
+# ---------------------------------------------------------------------------------------------
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "tflops": p["bf16_tflops"],
+                "tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "tflops": 1900.0, "tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------------------------
+# CPU baseline: the oracle on a bounded sample (also the correctness gate for the sampled rows)
+# ---------------------------------------------------------------------------------------------
+
+
+def _u16(t):
+    import numpy as np
+    import torch
+
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def oracle_sample_plan(budget_flops: float):
+    """Rows of each sweep size the oracle computes, about budget_flops in total."""
+    per = budget_flops / len(SWEEP)
+    plan = []
+    for n in SWEEP:
+        rows = int(max(1, min(n, round(per / (2.0 * n * n)))))
+        plan.append((n, rows))
+    return plan
+
+
+def cpu_baseline_leg(host_inputs, gpu_outputs, budget_flops, check=True):
+    """Time the oracle on sampled rows of every GEMM and on one full decode of each arm.
+
+    host_inputs: {n: (A, B)} CPU fp16 tensors, plus "dec_bf16": (x, W), "dec_q8": (x, q, s)
+    gpu_outputs: {n: C (CPU fp16 tensor)}, "dec_bf16": y, "dec_q8": y (CPU fp32) or None
+    Returns (baseline dict, gate dict).
+    """
+    import numpy as np
+
+    import oracle
+
+    threads = oracle.max_threads()
+    flops = 0.0
+    seconds = 0.0
+    worst = 0.0
+    gate_ok = True
+    parts = []
+    for n, rows in oracle_sample_plan(budget_flops):
+        A, B = host_inputs[n]
+        sel = np.linspace(0, n - 1, rows).round().astype(np.int64) if rows < n else None
+        t0 = time.perf_counter()
+        ref = oracle.gemm(_u16(A), _u16(B), rows=sel)
+        seconds += time.perf_counter() - t0
+        flops += gemm_flops(ref.shape[0], n, n)
+        parts.append(f"{n}^3:{ref.shape[0]} rows")
+        if check and gpu_outputs is not None:
+            C = gpu_outputs[n].double().numpy()
+            got = C if sel is None else C[sel]
+            err = np.abs(got - ref).max()
+            rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300)
+            worst = max(worst, err / (1e-3 * math.sqrt(n)))
+            if not (np.isfinite(got).all() and err <= 1e-3 * math.sqrt(n) and rel <= 1e-3):
+                gate_ok = False
+    x, W = host_inputs["dec_bf16"]
+    t0 = time.perf_counter()
+    yb = oracle.gemv_bf16(_u16(x), _u16(W))
+    x, q, s = host_inputs["dec_q8"]
+    yq = oracle.gemv_q8(_u16(x), q.numpy(), _u16(s))
+    seconds += time.perf_counter() - t0
+    flops += 2 * 2.0 * DEC_K * DEC_N
+    parts.append("decode bf16+q8 full")
+    if check and gpu_outputs is not None:
+        for key, ref in (("dec_bf16", yb), ("dec_q8", yq)):
+            got = gpu_outputs[key].double().numpy()
+            err = np.abs(got - ref).max()
+            rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+            worst = max(worst, err / (1e-3 * math.sqrt(DEC_K)))
+            if not (np.isfinite(got).all() and err <= 1e-3 * math.sqrt(DEC_K) and rel <= 1e-3):
+                gate_ok = False
+    baseline = {"value": flops / seconds / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                "sample": "; ".join(parts) + f" ({flops / 1e9:.1f} GFLOP, {seconds:.1f} s, fp64 C oracle)"}
+    gate = {"passed": gate_ok, "worst_err_over_bound": worst} if check else None
+    return baseline, gate
+
+
+# ---------------------------------------------------------------------------------------------
+# the default step on the GPU
+# ---------------------------------------------------------------------------------------------
+
+
+def make_host_inputs(rank=0):
+    import torch
+
+    from shape_driven_tile_gb300 import inputs
+
+    host = {}
+    for n in SWEEP:
+        host[n] = (inputs.uniform((n, n), seed=inputs.seed_for(1, 0, base=1000 * rank)),
+                   inputs.uniform((n, n), seed=inputs.seed_for(1, 1, base=1000 * rank)))
+    x = inputs.uniform((DEC_K,), seed=inputs.seed_for(3, 0, base=1000 * rank), dtype=torch.bfloat16)
+    Wb = [inputs.uniform((DEC_N, DEC_K), seed=inputs.seed_for(3, 1, base=1000 * rank + 17 * i),
+                         dtype=torch.bfloat16) for i in range(DEC_BUFFERS)]
+    Q = [inputs.q8_weights(DEC_N, DEC_K, seed=inputs.seed_for(3, 1, base=1000 * rank + 17 * i + 5))
+         for i in range(DEC_BUFFERS)]
+    host["dec_bf16"] = (x, Wb[0])
+    host["dec_q8"] = (x, Q[0][0], Q[0][1])
+    return host, x, Wb, Q
+
+
+def run_default(args):
+    import torch
+
+    import shape_driven_tile_gb300 as sdt
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    world, rank = dist_init("nccl")
+    peaks = load_peaks()
+
+    host, x_h, Wb_h, Q_h = make_host_inputs(rank)
+    A = {n: host[n][0].to(dev) for n in SWEEP}
+    B = {n: host[n][1].to(dev) for n in SWEEP}
+    C = {n: torch.empty((n, n), dtype=torch.float16, device=dev) for n in SWEEP}
+    x = x_h.to(dev)
+    Wb = [w.to(dev) for w in Wb_h]
+    Wq = [q.to(dev) for q, _ in Q_h]
+    Sq = [s.to(dev) for _, s in Q_h]
+    yb = torch.empty(DEC_N, dtype=torch.float32, device=dev)
+    yq = torch.empty(DEC_N, dtype=torch.float32, device=dev)
+    tiles = {n: sdt.tile_info(sdt.pick_tile(n, n, n))["name"] for n in SWEEP}
+    stream = torch.cuda.current_stream()
+    # The timed loop calls the C ABI directly with the operands' device pointers, so that
+    # Python-side argument checks do not leave the GPU idle between the small GEMMs.
+    L = sdt.lib()
+    sp = stream.cuda_stream
+    gemm_args = [(n, n, n, A[n].data_ptr(), B[n].data_ptr(), C[n].data_ptr(), sp) for n in SWEEP]
+    pb = [(DEC_K, DEC_N, x.data_ptr(), w.data_ptr(), yb.data_ptr(), sp) for w in Wb]
+    pq = [(DEC_K, DEC_N, x.data_ptr(), q.data_ptr(), s_.data_ptr(), yq.data_ptr(), sp) for q, s_ in zip(Wq, Sq)]
+    gemm_c, gemv_b, gemv_q = L.gemm_f16, L.gemv_m1_bf16, L.gemv_m1_q8
+
+    def step(i, ev=None):
+        rc = 0
+        for j, a in enumerate(gemm_args):
+            if ev is not None:
+                ev[j].record(stream)
+            rc |= gemm_c(*a)
+        if ev is not None:
+            ev[len(SWEEP)].record(stream)
+        rc |= gemv_b(*pb[i % DEC_BUFFERS])
+        if ev is not None:
+            ev[len(SWEEP) + 1].record(stream)
+        rc |= gemv_q(*pq[i % DEC_BUFFERS])
+        if ev is not None:
+            ev[len(SWEEP) + 2].record(stream)
+        if rc:
+            raise sdt.SdtError(rc, (L.sdt_last_error() or b"").decode())
+
+    launches_per_step = len(SWEEP) + 2
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    sdt.check_device_status()
+
+    # correctness gate + CPU baseline (rank 0): results of one step vs the oracle on the sample
+    gate, baseline = None, None
+    if rank == 0:
+        step(0)
+        torch.cuda.synchronize()
+        outs = {n: C[n].cpu() for n in SWEEP}
+        outs["dec_bf16"] = yb.cpu()
+        outs["dec_q8"] = yq.cpu()
+        calib, _ = cpu_baseline_leg(host, None, budget_flops=2e9, check=False)
+        budget = min(args.cpu_budget_s * calib["value"] * 1e12, 400e9)
+        baseline, gate = cpu_baseline_leg(host, outs, budget_flops=budget)
+        if not gate["passed"]:
+            print(json.dumps({"metric": METRIC, "error": "correctness gate failed", "gate": gate}))
+            sys.exit(3)
+
+    # timed region
+    nev = launches_per_step + 1
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        for i in range(args.steps):
+            step(i, events[i])
+        stop.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    elapsed_s = start.elapsed_time(stop) / 1e3
+    sdt.check_device_status()
+    max_s = max_over_ranks(elapsed_s, device=dev)
+
+    # per-kernel durations from the events inside the timed region
+    per = {n: [] for n in SWEEP}
+    dec_b, dec_q = [], []
+    for ev in events:
+        for j, n in enumerate(SWEEP):
+            per[n].append(ev[j].elapsed_time(ev[j + 1]))
+        dec_b.append(ev[len(SWEEP)].elapsed_time(ev[len(SWEEP) + 1]))
+        dec_q.append(ev[len(SWEEP) + 1].elapsed_time(ev[len(SWEEP) + 2]))
+
+    # end to end through the public API with host buffers (pinned), copies inside the timed region
+    e2e = run_e2e(args, dev, host, Wb_h, Q_h, stream)
+
+    if rank != 0:
+        return
+    value = aggregate_value(step_flops(), args.steps, world, max_s) / 1e12
+    per_size = []
+    for n in SWEEP:
+        ms = statistics.mean(per[n])
+        tf = gemm_flops(n, n, n) / (ms / 1e3) / 1e12
+        per_size.append({"size": n, "tile": tiles[n], "us": round(ms * 1e3, 2), "tflops": round(tf, 1),
+                         "pct_peak": round(100 * tf / peaks["tflops"], 1)})
+    dec = {}
+    for name, lst, fmt in (("bf16", dec_b, "bf16"), ("q8", dec_q, "q8")):
+        us = statistics.mean(lst) * 1e3
+        gbs = decode_bytes(DEC_K, DEC_N, fmt) / (us / 1e6) / 1e9
+        dec[name] = {"us": round(us, 2), "us_min": round(min(lst) * 1e3, 2), "us_max": round(max(lst) * 1e3, 2),
+                     "gbs": round(gbs, 1), "pct_hbm": round(100 * gbs / peaks["hbm_gbs"], 1)}
+    # dominant kernel: the largest share of the step
+    shares = {n: statistics.mean(per[n]) for n in SWEEP}
+    dom = max(shares, key=shares.get)
+    dom_ms = shares[dom]
+    achieved = gemm_flops(dom, dom, dom) / (dom_ms / 1e3) / 1e12
+    traffic = load_traffic(f"gemm_{dom}")
+    clock = clocks.summary()
+    out = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(max_s * 1e3 / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "l2": "inputs larger than L2 (step working set %.0f MB, L2 129 MB)"
+                   % (step_working_set() / 1e6), "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "kernel": f"gemm_f16 {dom}^3 ({tiles[dom]})",
+                     "achieved": round(achieved, 1), "peak": peaks["tflops"], "unit": "TFLOP/s",
+                     "frac": round(achieved / peaks["tflops"], 4), "peak_source": peaks["source"] + " bf16 burst",
+                     "traffic": traffic},
+        "cpu_baseline": baseline,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clock,
+        "per_size": per_size,
+        "decode": dec,
+        "gate": gate,
+    }
+    print(json.dumps(out), flush=True)
+
+
+def step_working_set():
+    gemm = sum(3 * 2 * n * n for n in SWEEP)
+    dec = DEC_BUFFERS * (decode_weight_bytes(DEC_K, DEC_N, "bf16") + decode_weight_bytes(DEC_K, DEC_N, "q8"))
+    return gemm + dec
+
+
+def kernel_source_digest():
+    """Digest of the CUDA sources; recorded ncu traffic is stale once it changes."""
+    import hashlib
+
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "shape_driven_tile_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(kernel_key):
+    """DRAM bytes per launch from an ncu capture (profiles/traffic.json), or None when the
+    record is missing or was taken on different kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f)
+    e = t.get(kernel_key)
+    if not isinstance(e, dict) or e.get("source_digest") != kernel_source_digest():
+        return None
+    return e.get("bytes")
+
+
+def run_e2e(args, dev, host, Wb_h, Q_h, stream):
+    """Same metric through the public API with pinned host buffers: H2D of every step input,
+    the step, D2H of every result, all inside the timed region."""
+    import torch
+
+    import shape_driven_tile_gb300 as sdt
+
+    steps = max(3, min(args.steps, args.e2e_steps))
+    hA = {n: host[n][0].pin_memory() for n in SWEEP}
+    hB = {n: host[n][1].pin_memory() for n in SWEEP}
+    hC = {n: torch.empty((n, n), dtype=torch.float16).pin_memory() for n in SWEEP}
+    hx = host["dec_bf16"][0].pin_memory()
+    hW = [w.pin_memory() for w in Wb_h[:2]]
+    hQ = [(q.pin_memory(), s.pin_memory()) for q, s in Q_h[:2]]
+    hyb = torch.empty(DEC_N, dtype=torch.float32).pin_memory()
+    hyq = torch.empty(DEC_N, dtype=torch.float32).pin_memory()
+    dA = {n: torch.empty_like(hA[n], device=dev) for n in SWEEP}
+    dB = {n: torch.empty_like(hB[n], device=dev) for n in SWEEP}
+    dC = {n: torch.empty((n, n), dtype=torch.float16, device=dev) for n in SWEEP}
+    dx = torch.empty_like(hx, device=dev)
+    dW = torch.empty_like(hW[0], device=dev)
+    dq = torch.empty_like(hQ[0][0], device=dev)
+    ds = torch.empty_like(hQ[0][1], device=dev)
+    dyb = torch.empty(DEC_N, dtype=torch.float32, device=dev)
+    dyq = torch.empty(DEC_N, dtype=torch.float32, device=dev)
+    h2d = sum(hA[n].numel() * 2 + hB[n].numel() * 2 for n in SWEEP) + hx.numel() * 2 + hW[0].numel() * 2 \
+        + hQ[0][0].numel() + hQ[0][1].numel() * 2
+    d2h = sum(n * n * 2 for n in SWEEP) + 2 * DEC_N * 4
+
+    def e2e_step(i):
+        for n in SWEEP:
+            dA[n].copy_(hA[n], non_blocking=True)
+            dB[n].copy_(hB[n], non_blocking=True)
+        dx.copy_(hx, non_blocking=True)
+        dW.copy_(hW[i % 2], non_blocking=True)
+        dq.copy_(hQ[i % 2][0], non_blocking=True)
+        ds.copy_(hQ[i % 2][1], non_blocking=True)
+        for n in SWEEP:
+            sdt.gemm_f16(dA[n], dB[n], dC[n])
+            hC[n].copy_(dC[n], non_blocking=True)
+        sdt.gemv_m1(dx, dW, y=dyb)
+        sdt.gemv_m1(dx, dq, ds, y=dyq)
+        hyb.copy_(dyb, non_blocking=True)
+        hyq.copy_(dyq, non_blocking=True)
+
+    for i in range(2):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    secs = time.perf_counter() - t0
+    barrier()
+    world = dist_env()[0]
+    max_s = max_over_ranks(secs, device=dev)
+    return {"value": round(aggregate_value(step_flops(), steps, world, max_s) / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
+            "ms_per_step": round(max_s * 1e3 / steps, 3)}
+
+
+# ---------------------------------------------------------------------------------------------
+# reference arm: the oracle on the host cores
+# ---------------------------------------------------------------------------------------------
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    host, _, _, _ = make_host_inputs(0)
+    # size each step so that warmup + steps stay within about three minutes
+    calib_flops = 2e9
+    base, _ = cpu_baseline_leg(host, None, calib_flops, check=False)
+    per_step_s = min(2.0, 150.0 / max(1, args.steps + args.warmup))
+    budget = max(2e8, per_step_s * base["value"] * 1e12)
+    for _ in range(args.warmup):
+        cpu_baseline_leg(host, None, budget, check=False)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        b, _ = cpu_baseline_leg(host, None, budget, check=False)
+        vals.append(b)
+    secs = time.perf_counter() - t0
+    value = statistics.mean(b["value"] for b in vals)
+    out = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(secs * 1e3 / max(1, args.steps), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD + " -- oracle on a bounded sample per step"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": vals[0]["cores"], "kind": "oracle",
+                         "sample": vals[0]["sample"]},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+# ---------------------------------------------------------------------------------------------
+# measurement modes
+# ---------------------------------------------------------------------------------------------
+
+
+class L2Flush:
+    def __init__(self, dev, nbytes=512 << 20):
+        import torch
+
+        self.buf = torch.empty(nbytes // 4, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.buf.zero_()
+
+
+def time_cold(fn, reps, flush, stream):
+    """Mean device time of fn over reps launches, each after an L2 flush (events bracket fn only)."""
+    import torch
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for e0, e1 in evs:
+        flush()
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ts = [e0.elapsed_time(e1) for e0, e1 in evs]
+    return statistics.mean(ts), min(ts), max(ts)
+
+
+def run_sweep(args):
+    """Every feasible tile per square size (plus K-scan shapes); pick_tile's slowdown."""
+    import torch
+
+    import shape_driven_tile_gb300 as sdt
+
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    flush = L2Flush(dev)
+    peaks = load_peaks()
+    shapes = [(n, n, n) for n in (args.sizes or SWEEP)]
+    if args.with_kscan:
+        shapes += [(2048, 2048, k) for k in KSCAN if k != 2048]
+    rows = []
+    for (M, N, K) in shapes:
+        A = (torch.rand((M, K), device=dev) * 2 - 1).half()
+        B = (torch.rand((K, N), device=dev) * 2 - 1).half()
+        C = torch.empty((M, N), device=dev, dtype=torch.float16)
+        res = {}
+        for t in sdt.feasible_tiles(M, N, K):
+            name = sdt.tile_info(t)["name"]
+            for _ in range(3):
+                sdt.gemm_f16_with_tile(A, B, C, tile=t)
+            mean, lo, hi = time_cold(lambda: sdt.gemm_f16_with_tile(A, B, C, tile=t), args.reps, flush, stream)
+            res[name] = mean
+        pick = sdt.tile_info(sdt.pick_tile(M, N, K))["name"]
+        best = min(res, key=res.get)
+        fl = gemm_flops(M, N, K)
+        rows.append({"shape": [M, N, K], "pick": pick, "best": best,
+                     "slowdown": round(res[pick] / res[best] - 1, 4),
+                     "tflops": {k: round(fl / (v / 1e3) / 1e12, 1) for k, v in res.items()},
+                     "us": {k: round(v * 1e3, 2) for k, v in res.items()}})
+        print(json.dumps(rows[-1]), flush=True)
+        del A, B, C
+    sdt.check_device_status()
+    slow = [r["slowdown"] for r in rows]
+    print(json.dumps({"mode": "sweep", "shapes": len(rows), "pick_avg_slowdown": round(statistics.mean(slow), 4),
+                      "pick_worst_slowdown": round(max(slow), 4), "peak_tflops": peaks["tflops"],
+                      "timing": f"mean of {args.reps} launches, L2 flushed before each"}), flush=True)
+
+
+def run_kscan(args):
+    import torch
+
+    import shape_driven_tile_gb300 as sdt
+
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    flush = L2Flush(dev)
+    tile = sdt.tile_id(args.tile or "128x128")
+    out = []
+    for K in KSCAN:
+        A = (torch.rand((2048, K), device=dev) * 2 - 1).half()
+        B = (torch.rand((K, 2048), device=dev) * 2 - 1).half()
+        C = torch.empty((2048, 2048), device=dev, dtype=torch.float16)
+        row = {"K": K}
+        for st in (0, 1):
+            for _ in range(3):
+                sdt.gemm_f16_with_tile(A, B, C, tile=tile, stagger=st)
+            mean, lo, hi = time_cold(lambda: sdt.gemm_f16_with_tile(A, B, C, tile=tile, stagger=st),
+                                     args.reps, flush, stream)
+            row[f"stagger{st}_tflops"] = round(gemm_flops(2048, 2048, K) / (mean / 1e3) / 1e12, 1)
+        out.append(row)
+        print(json.dumps(row), flush=True)
+    sdt.check_device_status()
+    print(json.dumps({"mode": "kscan", "tile": sdt.tile_info(tile)["name"], "rows": out}), flush=True)
+
+
+def run_decode(args):
+    """The decode protocol: 8 rotating buffers, warm-up, 200 timed launches, repeated 10 times."""
+    import torch
+
+    import shape_driven_tile_gb300 as sdt
+
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    peaks = load_peaks()
+    x = (torch.rand(DEC_K, device=dev) * 2 - 1).bfloat16()
+    Wb = [(torch.rand((DEC_N, DEC_K), device=dev) * 2 - 1).bfloat16() for _ in range(DEC_BUFFERS)]
+    Wq = [torch.randint(-127, 128, (DEC_N, DEC_K), device=dev, dtype=torch.int8) for _ in range(DEC_BUFFERS)]
+    Sq = [(torch.rand((DEC_N, DEC_K // 32), device=dev) * 9e-3 + 1e-3).half() for _ in range(DEC_BUFFERS)]
+    y = torch.empty(DEC_N, device=dev)
+    res = {}
+    for arm in ("bf16", "q8"):
+        def launch(i):
+            if arm == "bf16":
+                sdt.gemv_m1(x, Wb[i % DEC_BUFFERS], y=y)
+            else:
+                sdt.gemv_m1(x, Wq[i % DEC_BUFFERS], Sq[i % DEC_BUFFERS], y=y)
+        t_end = time.time() + 1.0
+        i = 0
+        while time.time() < t_end:
+            launch(i)
+            i += 1
+        torch.cuda.synchronize()
+        reps = []
+        for r in range(10):
+            # captured graph of 200 launches cycling the 8 buffers (no host launch gaps)
+            g = torch.cuda.CUDAGraph()
+            s = torch.cuda.Stream()
+            s.wait_stream(stream)
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(g, stream=s):
+                    for j in range(200):
+                        launch(j)
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            reps.append(e0.elapsed_time(e1) * 1e3 / 200)
+        nbytes = decode_bytes(DEC_K, DEC_N, arm)
+        res[arm] = {"us_min": round(min(reps), 2), "us_max": round(max(reps), 2),
+                    "gbs_best": round(nbytes / (min(reps) / 1e6) / 1e9, 1),
+                    "pct_hbm_best": round(100 * nbytes / (min(reps) / 1e6) / 1e9 / peaks["hbm_gbs"], 1),
+                    "bytes": nbytes}
+    sdt.check_device_status()
+    print(json.dumps({"mode": "decode", "K": DEC_K, "N": DEC_N, "hbm_peak_gbs": peaks["hbm_gbs"],
+                      "protocol": "1 s warm, 200 graph-replayed launches x 10 repeats, 8 rotating buffers",
+                      **res}), flush=True)
+
+
+def run_large(args):
+    import torch
+
+    import shape_driven_tile_gb300 as sdt
+
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    flush = L2Flush(dev)
+    peaks = load_peaks()
+    rows = []
+    for n in (args.sizes or LARGE):
+        A = (torch.rand((n, n), device=dev) * 2 - 1).half()
+        B = (torch.rand((n, n), device=dev) * 2 - 1).half()
+        C = torch.empty((n, n), device=dev, dtype=torch.float16)
+        pick = sdt.pick_tile(n, n, n)
+        for _ in range(2):
+            sdt.gemm_f16(A, B, C)
+        mean, lo, hi = time_cold(lambda: sdt.gemm_f16(A, B, C), args.reps, flush, stream)
+        tf = gemm_flops(n, n, n) / (mean / 1e3) / 1e12
+        rows.append({"size": n, "tile": sdt.tile_info(pick)["name"], "ms": round(mean, 3), "tflops": round(tf, 1),
+                     "pct_peak": round(100 * tf / peaks["tflops"], 1)})
+        print(json.dumps(rows[-1]), flush=True)
+        del A, B, C
+    sdt.check_device_status()
+    print(json.dumps({"mode": "large", "rows": rows}), flush=True)
+
+
+def run_one(args):
+    """A few launches of one kernel (for profiler captures): a square GEMM with pick_tile,
+    or the decode GEMV (--gemv bf16|q8)."""
+    import torch
+
+    import shape_driven_tile_gb300 as sdt
+
+    dev = torch.device("cuda", 0)
+    if args.gemv:
+        x = (torch.rand(DEC_K, device=dev) * 2 - 1).bfloat16()
+        if args.gemv == "bf16":
+            Ws = [(torch.rand((DEC_N, DEC_K), device=dev) * 2 - 1).bfloat16() for _ in range(2)]
+            fn = lambda i: sdt.gemv_m1(x, Ws[i % 2])
+        else:
+            Ws = [torch.randint(-127, 128, (DEC_N, DEC_K), device=dev, dtype=torch.int8) for _ in range(2)]
+            Ss = [(torch.rand((DEC_N, DEC_K // 32), device=dev) * 9e-3 + 1e-3).half() for _ in range(2)]
+            fn = lambda i: sdt.gemv_m1(x, Ws[i % 2], Ss[i % 2])
+    else:
+        n = (args.sizes or [4096])[0]
+        A = (torch.rand((n, n), device=dev) * 2 - 1).half()
+        B = (torch.rand((n, n), device=dev) * 2 - 1).half()
+        C = torch.empty((n, n), device=dev, dtype=torch.float16)
+        if args.tile:
+            fn = lambda i: sdt.gemm_f16_with_tile(A, B, C, tile=args.tile)
+        else:
+            fn = lambda i: sdt.gemm_f16(A, B, C)
+    for i in range(args.warmup + args.reps):
+        fn(i)
+    torch.cuda.synchronize()
+    sdt.check_device_status()
+    print(json.dumps({"mode": "one", "launches": args.warmup + args.reps,
+                      "kernel": args.gemv or f"gemm {(args.sizes or [4096])[0]}^3 {args.tile or 'pick'}",
+                      "source_digest": kernel_source_digest()}), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["sdt", "reference"], default="sdt")
+    ap.add_argument("--mode", choices=["step", "sweep", "kscan", "decode", "large", "one"], default="step")
+    ap.add_argument("--gemv", choices=["bf16", "q8"])
+    ap.add_argument("--reps", type=int, default=20)
+    ap.add_argument("--sizes", type=int, nargs="*")
+    ap.add_argument("--tile")
+    ap.add_argument("--with-kscan", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    {"step": run_default, "sweep": run_sweep, "kscan": run_kscan, "decode": run_decode,
+     "large": run_large, "one": run_one}[args.mode](args)
+
+
+if __name__ == "__main__":
+    main()

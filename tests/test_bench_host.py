@@ -1,0 +1,89 @@
+"""Host logic of bench.py: clock parsing, workload arithmetic, and the multi-rank
+bookkeeping (barrier, max over ranks, whole-job aggregate) on two gloo ranks."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def test_workload_arithmetic_matches_pages():
+    # "mojo-baro", round v2: bf16 weights 100.7 MB, q8 with a 4-byte scale slot 56.6 MB,
+    # byte ratio 0.563 (round v1)
+    rows = {}
+    with open(os.path.join(os.path.dirname(__file__), "golden", "decode_bytes.txt")) as f:
+        for line in f:
+            p = line.split()
+            if p and not p[0].startswith("#") and p[0] != "ratio":
+                rows[p[2]] = (int(p[0]), int(p[1]), int(p[3]), float(p[4]))
+            elif p and p[0] == "ratio":
+                ratio = float(p[1])
+    K, N, _, mb = rows["bf16"]
+    assert round(bench.decode_weight_bytes(K, N, "bf16") / 1e6, 1) == mb
+    K, N, sb, mb = rows["q8"]
+    q8 = bench.decode_weight_bytes(K, N, "q8", scale_bytes=sb)
+    assert round(q8 / 1e6, 1) == mb
+    # printed to three places (0.5625 is printed as 0.563)
+    assert abs(q8 / bench.decode_weight_bytes(K, N, "bf16") - ratio) <= 5e-4 + 1e-12
+    assert bench.gemm_flops(4096, 4096, 4096) == 2 * 4096 ** 3
+
+
+def test_parse_clock_csv():
+    text = ("0, 1965, 2070, 900.5, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active\n"
+            "0, 1800, 2070, 1390.2, 0x0000000000000004, Not Active, Not Active, Not Active, Active\n"
+            "0, 300, 2070, 150.0, 0x0000000000000001, Not Active, Not Active, Not Active, Not Active\n"
+            "garbage line\n")
+    s = bench.parse_clock_csv(text)
+    assert s["sm_mhz"] == (1965 + 1800) / 2
+    assert s["sm_max_mhz"] == 2070
+    assert s["reasons"] == ["sw_power_cap"]
+    assert s["samples"] == 3 and s["samples_under_load"] == 2
+    assert bench.parse_clock_csv("")["samples"] == 0
+
+
+def test_oracle_sample_plan_bounds():
+    plan = bench.oracle_sample_plan(60e9)
+    assert [n for n, _ in plan] == bench.SWEEP
+    for n, rows in plan:
+        assert 1 <= rows <= n
+    assert sum(2.0 * r * n * n for n, r in plan) <= 66e9
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank),
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    import torch.distributed as dist
+
+    w, r = bench.dist_init("gloo")
+    bench.barrier()
+    mx = bench.max_over_ranks(1.5 + r)  # rank r "took" 1.5 + r seconds
+    val = bench.aggregate_value(100.0, 10, w, mx)
+    q.put((r, w, mx, val))
+    dist.destroy_process_group()
+
+
+def test_two_rank_bookkeeping_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for r, w, mx, val in out:
+        assert w == 2
+        assert mx == 2.5                  # the slowest rank's time
+        assert val == 100.0 * 10 * 2 / 2.5  # units of all ranks / slowest time
