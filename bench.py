@@ -640,6 +640,9 @@ def run_sweep(args):
     shapes = [(n, n, n) for n in (args.sizes or SWEEP)]
     if args.with_kscan:
         shapes += [(2048, 2048, k) for k in KSCAN if k != 2048]
+    for sh in args.shapes or []:
+        M, N, K = (int(v) for v in sh.lower().split("x"))
+        shapes.append((M, N, K))
     rows = []
     for (M, N, K) in shapes:
         A = (torch.rand((M, K), device=dev) * 2 - 1).half()
@@ -825,6 +828,7 @@ def main(argv=None):
     ap.add_argument("--sizes", type=int, nargs="*")
     ap.add_argument("--tile")
     ap.add_argument("--with-kscan", action="store_true")
+    ap.add_argument("--shapes", nargs="*", help="extra GEMM shapes MxNxK for --mode sweep")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--e2e-steps", type=int, default=20)
     args = ap.parse_args(argv)

@@ -203,7 +203,9 @@ const char *sdt_last_error(void);
  * trapping.  This call synchronises `stream`, reads and clears the word for
  * the current device, and returns SDT_OK or SDT_ERR_TIMEOUT (SDT_ERR_CUDA if
  * the stream itself reports an error).  `where` (may be NULL) receives the
- * recorded code: 1 producer, 2 MMA issuer, 3 epilogue, 4 drain, 5 probe.
+ * recorded code: its low 4 bits are the site (1 producer, 2 MMA issuer,
+ * 3 epilogue, 4 drain, 5 probe); the two-CTA kernels add the CTA's rank in the
+ * pair at bit 4 and the loop position from bit 8.
  */
 int sdt_check_device_status(sdt_stream_t stream, int *where);
 

@@ -22,6 +22,8 @@
 #include <tuple>
 
 #include "gemm_kernel.cuh"
+#include "gemm_persistent.cuh"
+#include "gemm_pair.cuh"
 #include "host_common.cuh"
 
 namespace sdt {
@@ -39,6 +41,8 @@ struct LadderTile {
     int smem_per_stage;
     int smem_fixed;
     int tmem_cols;
+    int threads;
+    bool persistent;  // one CTA per SM walking tiles; accumulator double-buffered in TMEM
     double kt_cycles;
     double fixed_cycles;
 };
@@ -47,7 +51,21 @@ struct LadderTile {
     LadderTile {                                                                                   \
         BM_, BN_, 1, STAGES_, NAME_, &launch_gemm_tile<BM_, BN_>, TileCfg<BM_, BN_>::STAGE_BYTES,  \
             TileCfg<BM_, BN_>::ALIGN_SLACK + TileCfg<BM_, BN_>::CTRL_BYTES,                        \
-            TileCfg<BM_, BN_>::TMEM_COLS, KT_, FIX_                                                \
+            TileCfg<BM_, BN_>::TMEM_COLS, TileCfg<BM_, BN_>::THREADS, false, KT_, FIX_             \
+    }
+
+#define SDT_PTILE(BN_, STAGES_, NAME_, KT_, FIX_)                                                  \
+    LadderTile {                                                                                   \
+        128, BN_, 1, STAGES_, NAME_, &launch_gemm_persistent<BN_>, PersistentCfg<BN_>::STAGE_BYTES, \
+            PersistentCfg<BN_>::ALIGN_SLACK + PersistentCfg<BN_>::CTRL_BYTES,                      \
+            PersistentCfg<BN_>::TMEM_COLS, PersistentCfg<BN_>::THREADS, true, KT_, FIX_            \
+    }
+
+#define SDT_PAIR(BN_, STAGES_, NAME_, KT_, FIX_)                                                   \
+    LadderTile {                                                                                   \
+        256, BN_, 2, STAGES_, NAME_, &launch_gemm_pair<BN_>, PairCfg<BN_>::STAGE_BYTES,            \
+            PairCfg<BN_>::ALIGN_SLACK + PairCfg<BN_>::CTRL_BYTES, PairCfg<BN_>::TMEM_COLS,         \
+            PairCfg<BN_>::THREADS, true, KT_, FIX_                                                 \
     }
 
 static const LadderTile kLadder[] = {
@@ -56,6 +74,10 @@ static const LadderTile kLadder[] = {
     SDT_TILE(128, 64, 4, "128x64", 200.0, 3500.0),
     SDT_TILE(128, 128, 6, "128x128", 330.0, 4500.0),
     SDT_TILE(128, 256, 4, "128x256", 580.0, 7000.0),
+    SDT_PTILE(128, 6, "p128x128", 330.0, 1500.0),
+    SDT_PTILE(256, 4, "p128x256", 580.0, 2000.0),
+    SDT_PAIR(128, 8, "2cta_256x128", 330.0, 2000.0),
+    SDT_PAIR(256, 6, "2cta_256x256", 580.0, 2500.0),
 };
 static constexpr int kNumTiles = sizeof(kLadder) / sizeof(kLadder[0]);
 static constexpr int kDefaultSmemLimit = 232448;  // opt-in shared memory per block on sm_100-class parts
@@ -87,7 +109,7 @@ static bool feasible(const LadderTile &t, int64_t M, int64_t N, int64_t K, int s
 static int ctas_per_sm(const LadderTile &t, int smem_per_sm) {
     int by_smem = smem_per_sm / (tile_smem(t, t.stages) + 1024);
     int by_tmem = 512 / t.tmem_cols;
-    int by_threads = 2048 / TileCfg<64, 64>::THREADS;
+    int by_threads = 2048 / t.threads;
     int occ = by_smem < by_tmem ? by_smem : by_tmem;
     occ = occ < by_threads ? occ : by_threads;
     return occ < 1 ? 1 : occ;
@@ -98,11 +120,17 @@ static int ctas_per_sm(const LadderTile &t, int smem_per_sm) {
 // co-resident CTAs.
 static double model_cycles(const LadderTile &t, int64_t M, int64_t N, int64_t K, int sm_count,
                            int smem_per_sm) {
-    const double ctas = double(M / t.BM) * double(N / t.BN);
+    const double tiles = double(M / t.BM) * double(N / t.BN);
     const double nK = double(K / kBK);
+    if (t.persistent) {
+        // one worker (CTA, or CTA pair) per SM (pair of SMs) walking its share of the tiles;
+        // epilogues overlap the next tile, the fixed cost is paid once
+        const double workers = t.cta_group == 2 ? double(sm_count / 2) : double(sm_count);
+        return std::ceil(tiles / workers) * nK * t.kt_cycles + t.fixed_cycles;
+    }
     const int occ = ctas_per_sm(t, smem_per_sm);
-    const double waves_1 = std::ceil(ctas / sm_count);
-    const double rounds = std::ceil(ctas / (double(sm_count) * occ));
+    const double waves_1 = std::ceil(tiles / sm_count);
+    const double rounds = std::ceil(tiles / (double(sm_count) * occ));
     return waves_1 * nK * t.kt_cycles + rounds * t.fixed_cycles;
 }
 
@@ -319,7 +347,10 @@ static int run_tile(int tile_id, int stagger_req, int64_t M, int64_t N, int64_t 
         return fail(SDT_ERR_TILE, "tile %s is infeasible for %lldx%lldx%lld", t.name, (long long)M,
                     (long long)N, (long long)K);
     CUtensorMap tmA, tmB;
-    int rc = tensor_map_f16(A, uint64_t(K), uint64_t(M), uint64_t(K) * 2, kBK, uint32_t(t.BM), &tmA);
+    // Each CTA stages BM / cta_group rows of A per k-tile (a pair tile splits its rows
+    // between the two CTAs); the box must match the bytes the kernel expects.
+    const uint32_t a_box_rows = uint32_t(t.BM / t.cta_group);
+    int rc = tensor_map_f16(A, uint64_t(K), uint64_t(M), uint64_t(K) * 2, kBK, a_box_rows, &tmA);
     if (rc) return rc;
     rc = tensor_map_f16(B, uint64_t(N), uint64_t(K), uint64_t(N) * 2, 64, kBK, &tmB);
     if (rc) return rc;
@@ -342,6 +373,7 @@ static int run_tile(int tile_id, int stagger_req, int64_t M, int64_t N, int64_t 
     a.raster_group = env_int("SDT_RASTER_GROUP", 8, 1, 1 << 20);
     a.timeout_ns = wait_timeout_ns();
     a.status = status;
+    a.max_ctas = dev.sm_count * ctas_per_sm(t, dev.smem_per_sm);
     if (int64_t(a.num_m_tiles) * a.num_n_tiles > int64_t(0x7fffffff))
         return fail(SDT_ERR_SHAPE, "grid too large");
     int e = t.launch(tmA, tmB, a, stream);
@@ -468,7 +500,7 @@ int sdt_tile_info(int tile_id, sdt_tile_desc *out) {
     out->BK = kBK;
     out->cta_group = t.cta_group;
     out->stages = t.stages;
-    out->threads = TileCfg<64, 64>::THREADS;
+    out->threads = t.threads;
     out->smem_bytes = tile_smem(t, t.stages);
     out->tmem_cols = t.tmem_cols;
     snprintf(out->name, sizeof out->name, "%s", t.name);

@@ -49,6 +49,7 @@ struct GemmArgs {
     int raster_group;     // m-tiles per raster band
     unsigned long long timeout_ns;
     int *status;          // device status word (first error code wins)
+    int max_ctas;         // persistent kernels: grid size cap (one CTA per SM); host-side only
 };
 
 template <int BM, int BN>

@@ -7,6 +7,8 @@
 #include <atomic>
 
 #include "gemm_kernel.cuh"
+#include "gemm_persistent.cuh"
+#include "gemm_pair.cuh"
 
 namespace sdt {
 
@@ -32,7 +34,72 @@ int launch_gemm_tile(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmA
     return cudaGetLastError();
 }
 
+template <int BN>
+int launch_gemm_persistent(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args,
+                           cudaStream_t stream) {
+    using Cfg = PersistentCfg<BN>;
+    auto kern = gemm_f16_persistent_kernel<BN>;
+    const int smem = Cfg::smem_bytes(args.stages);
+    static std::atomic<int> configured[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (configured[dev].load(std::memory_order_acquire) < smem) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        int prev = configured[dev].load();
+        while (prev < smem && !configured[dev].compare_exchange_weak(prev, smem)) {
+        }
+    }
+    const long long tiles = static_cast<long long>(args.num_m_tiles) * args.num_n_tiles;
+    const unsigned grid = static_cast<unsigned>(tiles < args.max_ctas ? tiles : args.max_ctas);
+    kern<<<grid, Cfg::THREADS, smem, stream>>>(tmA, tmB, args);
+    return cudaGetLastError();
+}
+
+template <int BN>
+int launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args, cudaStream_t stream) {
+    using Cfg = PairCfg<BN>;
+    auto kern = gemm_f16_pair_kernel<BN>;
+    const int smem = Cfg::smem_bytes(args.stages);
+    static std::atomic<int> configured[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (configured[dev].load(std::memory_order_acquire) < smem) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        int prev = configured[dev].load();
+        while (prev < smem && !configured[dev].compare_exchange_weak(prev, smem)) {
+        }
+    }
+    const long long tiles = static_cast<long long>(args.num_m_tiles) * args.num_n_tiles;
+    const long long pairs_cap = args.max_ctas / 2 > 0 ? args.max_ctas / 2 : 1;
+    const unsigned pairs = static_cast<unsigned>(tiles < pairs_cap ? tiles : pairs_cap);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * pairs, 1, 1);
+    cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, args);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
 }  // namespace sdt
+
+#define SDT_INSTANTIATE_GEMM_PAIR(BN)                                                              \
+    template int sdt::launch_gemm_pair<BN>(const CUtensorMap &, const CUtensorMap &, const sdt::GemmArgs &, \
+                                           cudaStream_t);
+
+#define SDT_INSTANTIATE_GEMM_PERSISTENT(BN)                                                        \
+    template int sdt::launch_gemm_persistent<BN>(const CUtensorMap &, const CUtensorMap &,         \
+                                                 const sdt::GemmArgs &, cudaStream_t);
 
 #define SDT_INSTANTIATE_GEMM_TILE(BM, BN)                                                          \
     template int sdt::launch_gemm_tile<BM, BN>(const CUtensorMap &, const CUtensorMap &,           \

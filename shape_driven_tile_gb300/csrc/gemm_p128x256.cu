@@ -1,0 +1,3 @@
+// Persistent tile 128x256 (double-buffered TMEM accumulator), one translation unit.
+#include "gemm_launch.cuh"
+SDT_INSTANTIATE_GEMM_PERSISTENT(256)

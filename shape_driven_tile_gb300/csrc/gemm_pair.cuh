@@ -1,0 +1,252 @@
+// gemm_pair.cuh -- persistent two-CTA (cta_group::2) tcgen05 fp16 GEMM.
+//
+// A cluster of two CTAs on neighbouring SMs computes one 256 x BN output tile
+// with a single stream of M=256 MMAs issued by the leader CTA (cluster rank 0):
+//   - each CTA stages, per k-tile, its own 128 rows of A and its own BN/2
+//     columns of B (same smem offsets in both CTAs); the MMA reads A rows and B
+//     columns from both SMs, so every operand byte is fetched from L2 once per
+//     pair instead of once per CTA -- a 256 x BN pair moves (128 + BN/2) x 64 x 2
+//     bytes per SM per k-tile against (128 + BN) x 64 x 2 for a 128 x BN CTA;
+//   - the accumulator of rows 0-127 lives in the leader's TMEM, rows 128-255 in
+//     the peer's, each 128 lanes x BN columns, double-buffered as in
+//     gemm_persistent.cuh;
+//   - both CTAs' TMA loads complete on the leader's "full" barrier (armed by the
+//     leader with both CTAs' bytes); the leader's commits arrive on the "empty"
+//     and "acc_full" barriers of both CTAs (multicast); both CTAs' epilogue warps
+//     arrive on the leader's "acc_empty" barrier.
+// Everything else (tile walk, ring, epilogue, bounded waits) follows
+// gemm_persistent.cuh.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "gemm_kernel.cuh"
+#include "gemm_persistent.cuh"
+#include "ptx.cuh"
+
+namespace sdt {
+
+template <int BN>
+struct PairCfg {
+    static constexpr int BM = 256;     // rows per pair tile
+    static constexpr int CTA_M = 128;  // rows staged and accumulated per CTA
+    static constexpr int B_HALF = BN / 2;
+    static constexpr int A_BYTES = CTA_M * kBK * 2;
+    static constexpr int B_BYTES = B_HALF * kBK * 2;
+    static constexpr int B_BOX_BYTES = 64 * kBK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // per CTA
+    static constexpr int ACC_BUFS = 2;
+    static constexpr int TMEM_COLS = ACC_BUFS * BN;
+    static constexpr int THREADS = 192;
+    static constexpr int EPI_WARPS = 4;
+    static constexpr int ALIGN_SLACK = 1024;
+    static constexpr int CTRL_BYTES = 512;
+    __host__ __device__ static constexpr int smem_bytes(int stages) {
+        return ALIGN_SLACK + stages * STAGE_BYTES + CTRL_BYTES;
+    }
+    static_assert(BN == 128 || BN == 256, "pair tiles use BN 128 or 256");
+    static_assert(TMEM_COLS <= 512, "two accumulators must fit in TMEM");
+};
+
+template <int BN>
+__global__ void __launch_bounds__(192, 1)
+    gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                         const GemmArgs p) {
+    using Cfg = PairCfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+
+    const int S = p.stages;
+    uint8_t *smA = smem;
+    uint8_t *smB = smem + S * Cfg::A_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smB + S * Cfg::B_BYTES);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + S;
+    uint64_t *acc_full = bars + 2 * S;
+    uint64_t *acc_empty = bars + 2 * S + 2;
+    uint64_t *mma_done = bars + 2 * S + 4;
+    volatile uint32_t *ctrl = reinterpret_cast<volatile uint32_t *>(bars + 2 * S + 5);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair = static_cast<int>(blockIdx.x >> 1);
+    const int num_pairs = static_cast<int>(gridDim.x >> 1);
+    const int num_tiles = p.num_m_tiles * p.num_n_tiles;  // pair tiles (256 rows each)
+    const int nK = p.num_k_tiles;
+    const uint64_t lim = p.timeout_ns;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&acc_full[b]), 1);
+            mbar_init(smem_u32(&acc_empty[b]), 2 * Cfg::EPI_WARPS);
+        }
+        mbar_init(smem_u32(mma_done), 1);
+        ctrl[1] = 0;
+        ctrl[2] = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(const_cast<uint32_t *>(&ctrl[0])), Cfg::TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();  // barriers of both CTAs initialised, TMEM allocated in both SMs
+    tc_fence_after();
+    const uint32_t tmem_base = ctrl[0];
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer (both CTAs) ----------------
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+            int s = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            bool stop = false;
+            for (int tile = pair; tile < num_tiles && !stop; tile += num_pairs) {
+                int m_tile, n_tile;
+                tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.raster_group, m_tile, n_tile);
+                const int m0 = m_tile * Cfg::BM + static_cast<int>(rank) * Cfg::CTA_M;
+                const int nb = n_tile * BN + static_cast<int>(rank) * Cfg::B_HALF;
+                const int start =
+                    p.stagger ? static_cast<int>((static_cast<uint32_t>(tile) * static_cast<uint32_t>(p.stagger_stride)) &
+                                                 static_cast<uint32_t>(nK - 1))
+                              : 0;
+                for (int i = 0; i < nK; ++i) {
+                    if (!mbar_wait_for(smem_u32(&empty[s]), phase ^ 1u, lim)) {
+                        record_status(p.status, kSiteProducer | static_cast<int>(rank << 4) | (issued << 8));
+                        ctrl[1] = 1;
+                        stop = true;
+                        break;
+                    }
+                    if (ctrl[1]) { stop = true; break; }
+                    const int kt = p.stagger ? ((start + i) & (nK - 1)) : i;
+                    const uint32_t fb_local = smem_u32(&full[s]);
+                    if (leader) mbar_arrive_expect_tx(fb_local, 2 * Cfg::STAGE_BYTES);
+                    const uint32_t fb = mapa_shared(fb_local, 0);
+                    tma_load_2d_pair(smem_u32(smA + s * Cfg::A_BYTES), &tmA, fb, kt * kBK, m0);
+#pragma unroll
+                    for (int c = 0; c < Cfg::B_HALF / 64; ++c)
+                        tma_load_2d_pair(smem_u32(smB + s * Cfg::B_BYTES + c * Cfg::B_BOX_BYTES), &tmB, fb,
+                                         nb + c * 64, kt * kBK);
+                    ctrl[2] = ++issued;
+                    if (++s == S) { s = 0; phase ^= 1u; }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            // ---------------- MMA issuer (leader only) ----------------
+            constexpr uint32_t idesc = idesc_f16_f32(Cfg::BM, BN);
+            int s = 0;
+            uint32_t phase = 0;
+            int j = 0;
+            bool stop = false;
+            for (int tile = pair; tile < num_tiles && !stop; tile += num_pairs, ++j) {
+                const int b = j & 1;
+                const uint32_t acc_phase = static_cast<uint32_t>((j >> 1) & 1);
+                if (!mbar_wait_cluster_for(smem_u32(&acc_empty[b]), acc_phase ^ 1u, lim)) {
+                    record_status(p.status, kSiteMma | 0x80 | (j << 8));
+                    ctrl[1] = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
+                for (int i = 0; i < nK; ++i) {
+                    if (!mbar_wait_for(smem_u32(&full[s]), phase, lim)) {
+                        record_status(p.status, kSiteMma | (((j << 12) | i) << 8));
+                        ctrl[1] = 1;
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t a_desc = smem_desc_sw128(smem_u32(smA + s * Cfg::A_BYTES), 16, 1024);
+                    const uint64_t b_desc =
+                        smem_desc_sw128(smem_u32(smB + s * Cfg::B_BYTES), Cfg::B_BOX_BYTES, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        umma_f16_pair(d_tmem, a_desc + 2ull * kk, b_desc + 128ull * kk, idesc,
+                                      (i > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit_pair(smem_u32(&empty[s]), 0x3);
+                    if (++s == S) { s = 0; phase ^= 1u; }
+                }
+                if (!stop) umma_commit_pair(smem_u32(&acc_full[b]), 0x3);
+            }
+            umma_commit_pair(smem_u32(mma_done), 0x1);
+            if (!mbar_wait_for(smem_u32(mma_done), 0, lim)) record_status(p.status, kSiteDrain);
+        }
+    } else {
+        // ---------------- epilogue warps (both CTAs) ----------------
+        const int q = warp & 3;
+        int j = 0;
+        for (int tile = pair; tile < num_tiles; tile += num_pairs, ++j) {
+            const int b = j & 1;
+            const uint32_t acc_phase = static_cast<uint32_t>((j >> 1) & 1);
+            if (!warp_wait(smem_u32(&acc_full[b]), acc_phase, 4 * lim, lane)) {
+                if (lane == 0) {
+                    record_status(p.status, kSiteEpilogue | static_cast<int>(rank << 4) | (j << 8));
+                    ctrl[1] = 1;
+                }
+                break;
+            }
+            tc_fence_after();
+            int m_tile, n_tile;
+            tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.raster_group, m_tile, n_tile);
+            const int row = m_tile * Cfg::BM + static_cast<int>(rank) * Cfg::CTA_M + q * 32 + lane;
+            __half *crow = p.C + static_cast<size_t>(row) * p.N + n_tile * BN;
+            const uint32_t taddr =
+                tmem_base + static_cast<uint32_t>(b * BN) + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(taddr + c, r);
+                tmem_ld_wait();
+                if (c == BN - 32) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[b]), 0));
+                }
+                uint32_t h[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    __half2 v = __floats2half2_rn(__uint_as_float(r[2 * t]), __uint_as_float(r[2 * t + 1]));
+                    h[t] = *reinterpret_cast<uint32_t *>(&v);
+                }
+                uint4 *dst = reinterpret_cast<uint4 *>(crow + c);
+                dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+                dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+                dst[2] = make_uint4(h[8], h[9], h[10], h[11]);
+                dst[3] = make_uint4(h[12], h[13], h[14], h[15]);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && leader && ctrl[1]) {
+        const int issued = static_cast<int>(ctrl[2]);
+        for (int i = max(0, issued - S); i < issued; ++i) {
+            if (!mbar_wait_for(smem_u32(&full[i % S]), static_cast<uint32_t>((i / S) & 1), lim)) {
+                record_status(p.status, kSiteDrain);
+                break;
+            }
+        }
+    }
+    cluster_sync();  // both CTAs done with each other's smem, barriers and TMEM
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+template <int BN>
+int launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args, cudaStream_t stream);
+
+}  // namespace sdt

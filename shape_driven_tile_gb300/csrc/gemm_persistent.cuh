@@ -1,0 +1,264 @@
+// gemm_persistent.cuh -- persistent, warp-specialised tcgen05 fp16 GEMM with a
+// double-buffered TMEM accumulator (one CTA per SM, BM = 128).
+//
+// Same arithmetic as gemm_kernel.cuh (fp16 operands, fp32 accumulation in
+// tensor memory, fp16 output) and the same TMA/descriptor layouts; what changes
+// is the schedule.  The grid is at most one CTA per SM and each CTA walks the
+// output tiles b, b + gridDim.x, b + 2*gridDim.x, ... (banded raster order), so
+//   - the smem ring keeps streaming across tile boundaries (no pipeline refill),
+//   - the accumulator alternates between two TMEM buffers: while the epilogue
+//     warps drain tile j from buffer j%2, the MMA warp already accumulates tile
+//     j+1 into the other buffer.
+//
+// Roles (192 threads):
+//   warp 0 lane 0 : TMA producer (ring slots: full/empty mbarriers)
+//   warp 1        : TMEM allocation; lane 0 issues tcgen05.mma and commits
+//   warps 2..5    : epilogue; warp w reads TMEM lane quarter w % 4
+// Accumulator hand-off: acc_full[b] (MMA commit -> epilogue) and acc_empty[b]
+// (one arrival per epilogue warp -> MMA).
+//
+// Every wait is bounded per wait (p.timeout_ns from the first failed poll); on
+// expiry the kernel records the site in the status word and unwinds: the
+// producer stops issuing, the MMA warp waits for its own MMAs, outstanding TMA
+// copies are drained, TMEM is freed.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "gemm_kernel.cuh"
+#include "ptx.cuh"
+
+namespace sdt {
+
+template <int BN>
+struct PersistentCfg {
+    static constexpr int BM = 128;
+    static constexpr int A_BYTES = BM * kBK * 2;
+    static constexpr int B_BYTES = BN * kBK * 2;
+    static constexpr int B_BOX_BYTES = 64 * kBK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int ACC_BUFS = 2;
+    static constexpr int TMEM_COLS = ACC_BUFS * BN;
+    static constexpr int THREADS = 192;
+    static constexpr int EPI_WARPS = 4;
+    static constexpr int ALIGN_SLACK = 1024;
+    static constexpr int CTRL_BYTES = 512;
+    __host__ __device__ static constexpr int smem_bytes(int stages) {
+        return ALIGN_SLACK + stages * STAGE_BYTES + CTRL_BYTES;
+    }
+    static_assert(BN == 128 || BN == 256, "persistent tiles use BN 128 or 256");
+    static_assert(TMEM_COLS <= 512, "two accumulators must fit in TMEM");
+};
+
+// Banded raster: tile index -> (m_tile, n_tile); bands of `group` m-tiles, m fastest.
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int group, int &m_tile,
+                                            int &n_tile) {
+    const int per_band = group * num_n;
+    const int band = tile / per_band;
+    const int first_m = band * group;
+    const int band_m = min(num_m - first_m, group);
+    const int in_band = tile - band * per_band;
+    m_tile = first_m + in_band % band_m;
+    n_tile = in_band / band_m;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(192, 1)
+    gemm_f16_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
+                               const __grid_constant__ CUtensorMap tmB, const GemmArgs p) {
+    using Cfg = PersistentCfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+
+    const int S = p.stages;
+    uint8_t *smA = smem;
+    uint8_t *smB = smem + S * Cfg::A_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smB + S * Cfg::B_BYTES);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + S;
+    uint64_t *acc_full = bars + 2 * S;       // [2]
+    uint64_t *acc_empty = bars + 2 * S + 2;  // [2]
+    uint64_t *mma_done = bars + 2 * S + 4;
+    volatile uint32_t *ctrl = reinterpret_cast<volatile uint32_t *>(bars + 2 * S + 5);
+    // ctrl[0]: TMEM base   ctrl[1]: error flag   ctrl[2]: k-tiles issued by TMA
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int num_tiles = p.num_m_tiles * p.num_n_tiles;
+    const int nK = p.num_k_tiles;
+    const uint64_t lim = p.timeout_ns;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&acc_full[b]), 1);
+            mbar_init(smem_u32(&acc_empty[b]), Cfg::EPI_WARPS);
+        }
+        mbar_init(smem_u32(mma_done), 1);
+        ctrl[1] = 0;
+        ctrl[2] = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(const_cast<uint32_t *>(&ctrl[0])), Cfg::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = ctrl[0];
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer ----------------
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+            int s = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+                int m_tile, n_tile;
+                tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.raster_group, m_tile, n_tile);
+                const int m0 = m_tile * Cfg::BM, n0 = n_tile * BN;
+                const int start =
+                    p.stagger ? static_cast<int>((static_cast<uint32_t>(tile) * static_cast<uint32_t>(p.stagger_stride)) &
+                                                 static_cast<uint32_t>(nK - 1))
+                              : 0;
+                bool stop = false;
+                for (int i = 0; i < nK; ++i) {
+                    if (!mbar_wait_for(smem_u32(&empty[s]), phase ^ 1u, lim)) {
+                        record_status(p.status, kSiteProducer);
+                        ctrl[1] = 1;
+                        stop = true;
+                        break;
+                    }
+                    if (ctrl[1]) { stop = true; break; }
+                    const int kt = p.stagger ? ((start + i) & (nK - 1)) : i;
+                    const uint32_t fb = smem_u32(&full[s]);
+                    mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
+                    tma_load_2d(smem_u32(smA + s * Cfg::A_BYTES), &tmA, fb, kt * kBK, m0);
+#pragma unroll
+                    for (int c = 0; c < BN / 64; ++c)
+                        tma_load_2d(smem_u32(smB + s * Cfg::B_BYTES + c * Cfg::B_BOX_BYTES), &tmB, fb,
+                                    n0 + c * 64, kt * kBK);
+                    ctrl[2] = ++issued;
+                    if (++s == S) { s = 0; phase ^= 1u; }
+                }
+                if (stop) break;
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer ----------------
+            constexpr uint32_t idesc = idesc_f16_f32(Cfg::BM, BN);
+            int s = 0;
+            uint32_t phase = 0;
+            int j = 0;
+            bool stop = false;
+            for (int tile = blockIdx.x; tile < num_tiles && !stop; tile += gridDim.x, ++j) {
+                const int b = j & 1;
+                const uint32_t acc_phase = static_cast<uint32_t>((j >> 1) & 1);
+                if (!mbar_wait_for(smem_u32(&acc_empty[b]), acc_phase ^ 1u, lim)) {
+                    record_status(p.status, kSiteMma);
+                    ctrl[1] = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
+                for (int i = 0; i < nK; ++i) {
+                    if (!mbar_wait_for(smem_u32(&full[s]), phase, lim)) {
+                        record_status(p.status, kSiteMma);
+                        ctrl[1] = 1;
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t a_desc = smem_desc_sw128(smem_u32(smA + s * Cfg::A_BYTES), 16, 1024);
+                    const uint64_t b_desc =
+                        smem_desc_sw128(smem_u32(smB + s * Cfg::B_BYTES), Cfg::B_BOX_BYTES, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        umma_f16(d_tmem, a_desc + 2ull * kk, b_desc + 128ull * kk, idesc,
+                                 (i > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit(smem_u32(&empty[s]));
+                    if (++s == S) { s = 0; phase ^= 1u; }
+                }
+                if (!stop) umma_commit(smem_u32(&acc_full[b]));
+            }
+            // all MMAs this thread issued have completed once mma_done flips
+            umma_commit(smem_u32(mma_done));
+            if (!mbar_wait_for(smem_u32(mma_done), 0, lim)) record_status(p.status, kSiteDrain);
+        }
+    } else {
+        // ---------------- epilogue warps ----------------
+        const int q = warp & 3;
+        int j = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++j) {
+            const int b = j & 1;
+            const uint32_t acc_phase = static_cast<uint32_t>((j >> 1) & 1);
+            if (!warp_wait(smem_u32(&acc_full[b]), acc_phase, lim, lane)) {
+                if (lane == 0) {
+                    record_status(p.status, kSiteEpilogue);
+                    ctrl[1] = 1;
+                }
+                break;
+            }
+            tc_fence_after();
+            int m_tile, n_tile;
+            tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.raster_group, m_tile, n_tile);
+            const int row = m_tile * Cfg::BM + q * 32 + lane;
+            __half *crow = p.C + static_cast<size_t>(row) * p.N + n_tile * BN;
+            const uint32_t taddr = tmem_base + static_cast<uint32_t>(b * BN) + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(taddr + c, r);
+                tmem_ld_wait();
+                if (c == BN - 32) {
+                    // the whole accumulator of this tile is in registers: hand the buffer back
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&acc_empty[b]));
+                }
+                uint32_t h[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    __half2 v = __floats2half2_rn(__uint_as_float(r[2 * t]), __uint_as_float(r[2 * t + 1]));
+                    h[t] = *reinterpret_cast<uint32_t *>(&v);
+                }
+                uint4 *dst = reinterpret_cast<uint4 *>(crow + c);
+                dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+                dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+                dst[2] = make_uint4(h[8], h[9], h[10], h[11]);
+                dst[3] = make_uint4(h[12], h[13], h[14], h[15]);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && ctrl[1]) {
+        const int issued = static_cast<int>(ctrl[2]);
+        for (int i = max(0, issued - S); i < issued; ++i) {
+            if (!mbar_wait_for(smem_u32(&full[i % S]), static_cast<uint32_t>((i / S) & 1), lim)) {
+                record_status(p.status, kSiteDrain);
+                break;
+            }
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+template <int BN>
+int launch_gemm_persistent(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args,
+                           cudaStream_t stream);
+
+}  // namespace sdt

@@ -15,21 +15,24 @@
 // butterfly of warp shuffles at the end of each row block.
 //
 //  bf16: a bf16 is the top half of an fp32, so conversion is a shift or a mask;
-//        each product is exact in fp32 and is accumulated with FMA.
+//        each product is exact in fp32 and is accumulated with packed (f32x2)
+//        FMA into two partial sums per lane.
 //  q8  : int8 weights are turned into exact fp32 values by placing the byte
-//        (offset to unsigned) in the mantissa of 2^23 and subtracting 2^23+128;
-//        a 16-byte chunk is half of one 32-weight group, so the group's fp16
-//        scale multiplies the chunk's partial sum once.
+//        (offset to unsigned) in the mantissa of 2^23 and subtracting 2^23+128
+//        (packed f32x2 add); a 16-byte chunk is half of one 32-weight group, so
+//        the group's fp16 scale multiplies the chunk's partial sum once.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
 
 #include "host_common.cuh"
+#include "ptx.cuh"
 
 namespace sdt {
 
@@ -41,20 +44,6 @@ __device__ __forceinline__ uint4 ld_stream_v4(const uint4 *p) {
     return v;
 }
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-__device__ __forceinline__ float dot8_bf16(const uint4 &w, const uint4 &x, float acc) {
-    acc = fmaf(bf16_lo(w.x), bf16_lo(x.x), acc);
-    acc = fmaf(bf16_hi(w.x), bf16_hi(x.x), acc);
-    acc = fmaf(bf16_lo(w.y), bf16_lo(x.y), acc);
-    acc = fmaf(bf16_hi(w.y), bf16_hi(x.y), acc);
-    acc = fmaf(bf16_lo(w.z), bf16_lo(x.z), acc);
-    acc = fmaf(bf16_hi(w.z), bf16_hi(x.z), acc);
-    acc = fmaf(bf16_lo(w.w), bf16_lo(x.w), acc);
-    acc = fmaf(bf16_hi(w.w), bf16_hi(x.w), acc);
-    return acc;
-}
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -62,24 +51,56 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// Four int8 weights of one 32-bit word (already xor-ed with 0x80808080) times four
-// bf16 activations (two words), accumulated into acc.
-__device__ __forceinline__ float dot4_q8(uint32_t qw, uint32_t x01, uint32_t x23, float acc) {
-    const uint32_t magic = 0x4B000000u;  // 2^23
-    const float off = 8388736.0f;        // 2^23 + 128
-    const float q0 = __uint_as_float(__byte_perm(qw, magic, 0x7540)) - off;
-    const float q1 = __uint_as_float(__byte_perm(qw, magic, 0x7541)) - off;
-    const float q2 = __uint_as_float(__byte_perm(qw, magic, 0x7542)) - off;
-    const float q3 = __uint_as_float(__byte_perm(qw, magic, 0x7543)) - off;
-    acc = fmaf(q0, bf16_lo(x01), acc);
-    acc = fmaf(q1, bf16_hi(x01), acc);
-    acc = fmaf(q2, bf16_lo(x23), acc);
-    acc = fmaf(q3, bf16_hi(x23), acc);
+// Packed pairs of fp32 (sm_100-class f32x2 arithmetic): a 64-bit register holds
+// two floats, low word first.
+__device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ float sum2(uint64_t a) {
+    return __uint_as_float(static_cast<uint32_t>(a)) + __uint_as_float(static_cast<uint32_t>(a >> 32));
+}
+
+// A bf16 pair word -> the two fp32 values, packed.
+__device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) { return pack2(w << 16, w & 0xFFFF0000u); }
+
+// Four int8 weights of one word (already xor-ed with 0x80808080, i.e. biased to
+// unsigned) times four activations (two packed pairs), accumulated into a packed pair.
+// Each byte u is placed in the mantissa of 2^23, so the float is exactly 2^23 + u;
+// subtracting 2^23 + 128 gives the signed weight exactly.
+__device__ __forceinline__ uint64_t dot4_q8(uint32_t qw, uint64_t x01, uint64_t x23, uint64_t acc) {
+    const uint32_t magic = 0x4B000000u;                  // 2^23
+    const uint32_t off = 0xCB000080u;                    // -(2^23 + 128)
+    const uint64_t neg_off = pack2(off, off);
+    const uint64_t q01 = add2(pack2(__byte_perm(qw, magic, 0x7540), __byte_perm(qw, magic, 0x7541)), neg_off);
+    const uint64_t q23 = add2(pack2(__byte_perm(qw, magic, 0x7542), __byte_perm(qw, magic, 0x7543)), neg_off);
+    acc = fma2(q01, x01, acc);
+    acc = fma2(q23, x23, acc);
     return acc;
 }
 
 constexpr int kGemvThreads = 256;
 constexpr int kGemvWarps = kGemvThreads / 32;
+
+// Eight bf16 weights times eight activations (packed pairs), accumulated into a packed pair.
+__device__ __forceinline__ uint64_t dot8_bf16(const uint4 &w, const uint64_t (&xp)[4], uint64_t acc) {
+    acc = fma2(bf16x2_to_f32x2(w.x), xp[0], acc);
+    acc = fma2(bf16x2_to_f32x2(w.y), xp[1], acc);
+    acc = fma2(bf16x2_to_f32x2(w.z), xp[2], acc);
+    acc = fma2(bf16x2_to_f32x2(w.w), xp[3], acc);
+    return acc;
+}
 
 template <int ROWS, int U>
 __global__ void __launch_bounds__(kGemvThreads)
@@ -89,9 +110,9 @@ __global__ void __launch_bounds__(kGemvThreads)
     const int gwarp = blockIdx.x * kGemvWarps + (threadIdx.x >> 5);
     const int nwarps = gridDim.x * kGemvWarps;
     for (int n0 = gwarp * ROWS; n0 < N; n0 += nwarps * ROWS) {
-        float acc[ROWS];
+        uint64_t acc[ROWS];
 #pragma unroll
-        for (int r = 0; r < ROWS; ++r) acc[r] = 0.f;
+        for (int r = 0; r < ROWS; ++r) acc[r] = 0;
         for (int c0 = lane; c0 < K8; c0 += 32 * U) {
             uint4 w[ROWS][U];
             uint4 xv[U];
@@ -106,13 +127,16 @@ __global__ void __launch_bounds__(kGemvThreads)
                 xv[u] = in ? __ldg(x + c) : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
-            for (int u = 0; u < U; ++u)
+            for (int u = 0; u < U; ++u) {
+                const uint64_t xp[4] = {bf16x2_to_f32x2(xv[u].x), bf16x2_to_f32x2(xv[u].y),
+                                        bf16x2_to_f32x2(xv[u].z), bf16x2_to_f32x2(xv[u].w)};
 #pragma unroll
-                for (int r = 0; r < ROWS; ++r) acc[r] = dot8_bf16(w[r][u], xv[u], acc[r]);
+                for (int r = 0; r < ROWS; ++r) acc[r] = dot8_bf16(w[r][u], xp, acc[r]);
+            }
         }
 #pragma unroll
         for (int r = 0; r < ROWS; ++r) {
-            const float v = warp_sum(acc[r]);
+            const float v = warp_sum(sum2(acc[r]));
             if (lane == 0 && n0 + r < N) y[n0 + r] = v;
         }
     }
@@ -151,16 +175,19 @@ __global__ void __launch_bounds__(kGemvThreads)
                 const bool in = c < K16;
                 const uint4 xa = in ? __ldg(x + 2 * c) : make_uint4(0, 0, 0, 0);
                 const uint4 xb = in ? __ldg(x + 2 * c + 1) : make_uint4(0, 0, 0, 0);
+                // the chunk's 16 activations as 8 packed fp32 pairs, shared by the ROWS rows
+                const uint64_t x0 = bf16x2_to_f32x2(xa.x), x1 = bf16x2_to_f32x2(xa.y);
+                const uint64_t x2 = bf16x2_to_f32x2(xa.z), x3 = bf16x2_to_f32x2(xa.w);
+                const uint64_t x4 = bf16x2_to_f32x2(xb.x), x5 = bf16x2_to_f32x2(xb.y);
+                const uint64_t x6 = bf16x2_to_f32x2(xb.z), x7 = bf16x2_to_f32x2(xb.w);
 #pragma unroll
                 for (int r = 0; r < ROWS; ++r) {
-                    const uint4 q = make_uint4(w[r][u].x ^ 0x80808080u, w[r][u].y ^ 0x80808080u,
-                                               w[r][u].z ^ 0x80808080u, w[r][u].w ^ 0x80808080u);
-                    float part = 0.f;
-                    part = dot4_q8(q.x, xa.x, xa.y, part);
-                    part = dot4_q8(q.y, xa.z, xa.w, part);
-                    part = dot4_q8(q.z, xb.x, xb.y, part);
-                    part = dot4_q8(q.w, xb.z, xb.w, part);
-                    acc[r] = fmaf(sc[r][u], part, acc[r]);
+                    uint64_t part = 0;
+                    part = dot4_q8(w[r][u].x ^ 0x80808080u, x0, x1, part);
+                    part = dot4_q8(w[r][u].y ^ 0x80808080u, x2, x3, part);
+                    part = dot4_q8(w[r][u].z ^ 0x80808080u, x4, x5, part);
+                    part = dot4_q8(w[r][u].w ^ 0x80808080u, x6, x7, part);
+                    acc[r] = fmaf(sc[r][u], sum2(part), acc[r]);
                 }
             }
         }
@@ -172,23 +199,288 @@ __global__ void __launch_bounds__(kGemvThreads)
     }
 }
 
+// ---------------------------------------------------------------------------------
+// Streaming variant: weights (and q8 scales) staged through shared memory by bulk
+// copies.
+//
+// One CTA per SM owns a contiguous slice of rows (a multiple of RS rows).  A
+// producer thread streams the slice RS rows at a time -- one contiguous block of
+// RS * row_bytes since W is row-major, plus the matching RS * K/16 bytes of q8
+// scales -- into a ring of shared-memory stages with cp.async.bulk + mbarrier
+// complete_tx, so the copy engine keeps many kilobytes in flight per SM
+// independently of the consumers' arithmetic.  The activations are converted
+// once per CTA to fp32 in shared memory.  NW consumer warps work on each stage:
+// H warps per row (RS = NW / H rows), lane l of a warp reading 16-byte chunks
+// h*32 + l, h*32 + l + 32*H, ... of its row, so all operands of the inner loop
+// come from shared memory.  Partial sums stay in packed fp32 pairs; the H
+// warps of a row combine through shared-memory atomics (no barrier between
+// warps, so a warp that gives up a bounded wait cannot stall its partner).
+// ---------------------------------------------------------------------------------
+
+constexpr int kStreamConsumers = 16;
+constexpr int kStreamThreads = (kStreamConsumers + 1) * 32;
+constexpr int kStreamSmemBudget = 220 * 1024;
+
+struct StreamArgs {
+    const uint4 *x;        // bf16 activations [K]
+    const uint8_t *W;      // [N][row_bytes]
+    const uint8_t *scales; // q8: fp16 [N][K/32]
+    float *y;
+    int K, N;
+    int row_bytes;
+    int scale_row_bytes;   // q8: K/16; bf16: 0
+    int stages;
+    int rows_per_cta;      // multiple of the rows per stage
+    unsigned long long timeout_ns;
+    int *status;
+};
+
+template <bool Q8, int H>
+__global__ void __launch_bounds__(kStreamThreads, 1) gemv_stream_kernel(const StreamArgs a) {
+    constexpr int RS = kStreamConsumers / H;  // rows per stage
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw + 127u) & ~127u) - raw);
+    const int S = a.stages;
+    const int w_bytes = RS * a.row_bytes;
+    const int sc_bytes = RS * a.scale_row_bytes;
+    const int stage_bytes = w_bytes + sc_bytes;
+    // Activations as fp32 pairs in a transposed layout: pair p of chunk c at xs2[p * nchunk + c],
+    // so the 32 lanes of a warp (consecutive chunks) read 32 consecutive 8-byte words.
+    uint2 *xs2 = reinterpret_cast<uint2 *>(smem + S * stage_bytes);  // K/2 pairs
+    float *partial = reinterpret_cast<float *>(xs2 + (a.K >> 1));    // [S][RS] row sums (H > 1)
+    uint32_t *arrived = reinterpret_cast<uint32_t *>(partial + S * RS);  // [S][RS] warps done
+    uint64_t *full = reinterpret_cast<uint64_t *>(arrived + S * RS);
+    uint64_t *empty = full + S;
+    volatile uint32_t *ctrl = reinterpret_cast<volatile uint32_t *>(empty + S);  // [0] error, [1] issued
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int r_begin = blockIdx.x * a.rows_per_cta;
+    const int r_end = min(a.N, r_begin + a.rows_per_cta);
+    const int n_st = r_end > r_begin ? (r_end - r_begin + RS - 1) / RS : 0;
+    const uint64_t lim = a.timeout_ns;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(smem_u32(&full[i]), 1);
+            mbar_init(smem_u32(&empty[i]), kStreamConsumers);
+        }
+        ctrl[0] = 0;
+        ctrl[1] = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kStreamConsumers) {
+        if (lane == 0) {
+            int s = 0;
+            uint32_t phase = 0;
+            for (int st = 0; st < n_st; ++st) {
+                if (!mbar_wait_for(smem_u32(&empty[s]), phase ^ 1u, lim)) {
+                    if (a.status) atomicCAS(a.status, 0, static_cast<int>(kSiteProducer));
+                    ctrl[0] = 1;
+                    break;
+                }
+                if (ctrl[0]) break;
+                const int r = r_begin + st * RS;
+                const int nrows = min(RS, r_end - r);
+                const uint32_t fb = smem_u32(&full[s]);
+                uint8_t *dst = smem + s * stage_bytes;
+                mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nrows * (a.row_bytes + a.scale_row_bytes)));
+                bulk_load(smem_u32(dst), a.W + static_cast<size_t>(r) * a.row_bytes,
+                          static_cast<uint32_t>(nrows * a.row_bytes), fb);
+                if (Q8)
+                    bulk_load(smem_u32(dst + w_bytes), a.scales + static_cast<size_t>(r) * a.scale_row_bytes,
+                              static_cast<uint32_t>(nrows * a.scale_row_bytes), fb);
+                ctrl[1] = static_cast<uint32_t>(st + 1);
+                if (++s == S) { s = 0; phase ^= 1u; }
+            }
+        }
+    } else {
+        for (int i = threadIdx.x; i < S * RS; i += kStreamConsumers * 32) {
+            partial[i] = 0.f;
+            arrived[i] = 0u;
+        }
+        const int nchunk = a.K >> (Q8 ? 4 : 3);  // 16-byte weight chunks per row
+        // activations -> fp32 pairs in shared memory (consumer warps only; the producer is
+        // already streaming).  x word i holds elements 8i .. 8i+7: chunk 8i / E, pairs from
+        // (8i % E) / 2, with E = 16 (q8) or 8 (bf16) elements per chunk.
+        for (int i = threadIdx.x; i < (a.K >> 3); i += kStreamConsumers * 32) {
+            const uint4 v = __ldg(a.x + i);
+            const int c = Q8 ? (i >> 1) : i;
+            const int p0 = Q8 ? (i & 1) * 4 : 0;
+            xs2[(p0 + 0) * nchunk + c] = make_uint2(v.x << 16, v.x & 0xFFFF0000u);
+            xs2[(p0 + 1) * nchunk + c] = make_uint2(v.y << 16, v.y & 0xFFFF0000u);
+            xs2[(p0 + 2) * nchunk + c] = make_uint2(v.z << 16, v.z & 0xFFFF0000u);
+            xs2[(p0 + 3) * nchunk + c] = make_uint2(v.w << 16, v.w & 0xFFFF0000u);
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kStreamConsumers * 32) : "memory");
+
+        const int row_in_stage = warp / H;
+        const int h = warp % H;
+        int s = 0;
+        uint32_t phase = 0;
+        for (int st = 0; st < n_st; ++st) {
+            if (!warp_wait(smem_u32(&full[s]), phase, lim, lane)) {
+                if (lane == 0) {
+                    if (a.status) atomicCAS(a.status, 0, static_cast<int>(kSiteEpilogue));
+                    ctrl[0] = 1;
+                }
+                break;
+            }
+            const int row = r_begin + st * RS + row_in_stage;
+            const uint8_t *wrow = smem + s * stage_bytes + row_in_stage * a.row_bytes;
+            const __half *srow = reinterpret_cast<const __half *>(smem + s * stage_bytes + w_bytes +
+                                                                 row_in_stage * a.scale_row_bytes);
+            float v = 0.f;
+            if (row < r_end) {
+                uint64_t acc = 0;
+                float accf = 0.f;
+#pragma unroll 4
+                for (int c = h * 32 + lane; c < nchunk; c += 32 * H) {
+                    const uint4 w = *reinterpret_cast<const uint4 *>(wrow + c * 16);
+                    if (Q8) {
+                        const uint2 *xp = xs2 + c;
+                        uint64_t part = 0;
+                        const uint2 p0 = xp[0], p1 = xp[nchunk], p2 = xp[2 * nchunk], p3 = xp[3 * nchunk];
+                        const uint2 p4 = xp[4 * nchunk], p5 = xp[5 * nchunk], p6 = xp[6 * nchunk],
+                                    p7 = xp[7 * nchunk];
+                        part = dot4_q8(w.x ^ 0x80808080u, pack2(p0.x, p0.y), pack2(p1.x, p1.y), part);
+                        part = dot4_q8(w.y ^ 0x80808080u, pack2(p2.x, p2.y), pack2(p3.x, p3.y), part);
+                        part = dot4_q8(w.z ^ 0x80808080u, pack2(p4.x, p4.y), pack2(p5.x, p5.y), part);
+                        part = dot4_q8(w.w ^ 0x80808080u, pack2(p6.x, p6.y), pack2(p7.x, p7.y), part);
+                        accf = fmaf(__half2float(srow[c >> 1]), sum2(part), accf);
+                    } else {
+                        const uint2 *xp = xs2 + c;
+                        const uint2 p0 = xp[0], p1 = xp[nchunk], p2 = xp[2 * nchunk], p3 = xp[3 * nchunk];
+                        acc = fma2(bf16x2_to_f32x2(w.x), pack2(p0.x, p0.y), acc);
+                        acc = fma2(bf16x2_to_f32x2(w.y), pack2(p1.x, p1.y), acc);
+                        acc = fma2(bf16x2_to_f32x2(w.z), pack2(p2.x, p2.y), acc);
+                        acc = fma2(bf16x2_to_f32x2(w.w), pack2(p3.x, p3.y), acc);
+                    }
+                }
+                v = warp_sum(Q8 ? accf : sum2(acc));
+            }
+            if (lane == 0) {
+                if (H == 1) {
+                    if (row < r_end) a.y[row] = v;
+                } else {
+                    // The H warps of a row add into the stage slot's sum; the last to arrive
+                    // writes y and clears the slot.  The slot is reused only after this stage's
+                    // empty barrier (which needs every warp's arrival below) has completed.
+                    // With H = 2 the sum 0 + a + b is the same in either arrival order.
+                    float *sum = &partial[s * RS + row_in_stage];
+                    uint32_t *cnt = &arrived[s * RS + row_in_stage];
+                    atomicAdd(sum, v);
+                    __threadfence_block();
+                    if (atomicAdd(cnt, 1u) == H - 1) {
+                        __threadfence_block();
+                        const float t = atomicExch(sum, 0.f);
+                        atomicExch(cnt, 0u);
+                        if (row < r_end) a.y[row] = t;
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&empty[s]));  // this warp is done with the stage
+            if (++s == S) { s = 0; phase ^= 1u; }
+        }
+    }
+
+    __syncthreads();
+    if (threadIdx.x == kStreamConsumers * 32 && ctrl[0]) {
+        // drain: wait (bounded) for bulk copies this CTA issued and may not have seen land
+        const int issued = static_cast<int>(ctrl[1]);
+        for (int i = max(0, issued - S); i < issued; ++i)
+            if (!mbar_wait_for(smem_u32(&full[i % S]), static_cast<uint32_t>((i / S) & 1), lim)) {
+                if (a.status) atomicCAS(a.status, 0, static_cast<int>(kSiteDrain));
+                break;
+            }
+    }
+}
+
 __global__ void zero_fill_f32(float *y, int64_t n) {
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x)
         y[i] = 0.f;
 }
 
 struct GemvVariant {
-    int rows, unroll;
+    int rows, unroll;  // register-path kernel: rows per warp, chunks in flight per row
+    int stream_h;      // > 0: streaming kernel with this many consumer warps per row
 };
 
-// Variant selection (rows per warp, chunks in flight per row); SDT_GEMV_VARIANT="R,U" overrides.
+// Variant selection.  Default: the register kernel with 2 rows per warp and 4
+// chunks in flight per row (fastest measured on GB300 at K=4096, N=12288).
+// SDT_GEMV_VARIANT overrides: "stream1" / "stream2" (streaming kernel, warps per
+// row), "stream" (its default split), or "R,U" for the register kernel.
 static GemvVariant gemv_variant(bool q8) {
-    GemvVariant v = q8 ? GemvVariant{2, 4} : GemvVariant{2, 4};
+    GemvVariant v{2, 4, 0};
     if (const char *s = getenv("SDT_GEMV_VARIANT")) {
         int r = 0, u = 0;
-        if (sscanf(s, "%d,%d", &r, &u) == 2) v = GemvVariant{r, u};
+        if (!strcmp(s, "stream1")) v.stream_h = 1;
+        else if (!strcmp(s, "stream2")) v.stream_h = 2;
+        else if (!strcmp(s, "stream")) v.stream_h = q8 ? 1 : 2;
+        else if (sscanf(s, "%d,%d", &r, &u) == 2) v = GemvVariant{r, u, 0};
     }
     return v;
+}
+
+template <bool Q8, int H>
+static cudaError_t launch_stream(const StreamArgs &a, int grid, int smem, cudaStream_t s) {
+    auto kern = gemv_stream_kernel<Q8, H>;
+    static std::atomic<int> configured[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (configured[dev].load() < smem) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured[dev].store(smem);
+    }
+    kern<<<grid, kStreamThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+// Streams W through shared memory when a ring of at least two stages fits (with the
+// fp32 activations); returns false to ask for the register kernel.
+static bool try_stream(bool q8, int H, int64_t K, int64_t N, const void *x, const void *W, const void *scales,
+                       float *y, cudaStream_t s, const DeviceInfo &dev, int *status, cudaError_t *err) {
+    if (H != 1 && H != 2) return false;
+    // every bulk copy must be a multiple of 16 bytes: q8 scale rows (K/16 bytes) need K % 256 == 0
+    if (q8 && K % 256) return false;
+    const int64_t RS = kStreamConsumers / H;
+    const int64_t row_bytes = q8 ? K : 2 * K;
+    const int64_t scale_row_bytes = q8 ? K / 16 : 0;
+    const int64_t stage_bytes = RS * (row_bytes + scale_row_bytes);
+    // per stage: the weights + scales, two 8-byte barriers, RS row sums and RS counters
+    const int64_t per_stage = stage_bytes + 16 + 8 * RS;
+    const int64_t fixed = 128 + 4 * K + 8;
+    const int64_t budget = std::min<int64_t>(kStreamSmemBudget, dev.smem_optin);
+    int64_t stages = (budget - fixed) / per_stage;
+    if (stages > 8) stages = 8;
+    if (stages < 2) return false;
+    const int64_t min_rows = RS;
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(dev.sm_count, (N + min_rows - 1) / min_rows));
+    int64_t rows_per_cta = (N + grid - 1) / grid;
+    rows_per_cta = (rows_per_cta + RS - 1) / RS * RS;  // whole stages (16-byte aligned scale copies)
+    const int64_t ctas = (N + rows_per_cta - 1) / rows_per_cta;
+    StreamArgs a;
+    a.x = static_cast<const uint4 *>(x);
+    a.W = static_cast<const uint8_t *>(W);
+    a.scales = static_cast<const uint8_t *>(scales);
+    a.y = y;
+    a.K = int(K);
+    a.N = int(N);
+    a.row_bytes = int(row_bytes);
+    a.scale_row_bytes = int(scale_row_bytes);
+    a.stages = int(stages);
+    a.rows_per_cta = int(rows_per_cta);
+    a.timeout_ns = wait_timeout_ns();
+    a.status = status;
+    const int smem = int(fixed + stages * per_stage);
+    if (q8) *err = H == 1 ? launch_stream<true, 1>(a, int(ctas), smem, s) : launch_stream<true, 2>(a, int(ctas), smem, s);
+    else *err = H == 1 ? launch_stream<false, 1>(a, int(ctas), smem, s) : launch_stream<false, 2>(a, int(ctas), smem, s);
+    return true;
 }
 
 template <int R, int U>
@@ -239,17 +531,22 @@ static int gemv_impl(int64_t K, int64_t N, const void *x, const void *W, const v
     int rc = current_device(&dev);
     if (rc) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream_h);
+    cudaError_t e = cudaSuccess;
     if (K == 0) {
         const int blocks = int(std::min<int64_t>((N + 255) / 256, int64_t(dev.sm_count) * 4));
         zero_fill_f32<<<blocks, 256, 0, s>>>(y, N);
-    } else if (!q8) {
-        const GemvVariant v = gemv_variant(false);
-        SDT_GEMV_DISPATCH(launch_bf16, v, int(K / 8), int(N), x, W, y, s);
+        e = cudaGetLastError();
     } else {
-        const GemvVariant v = gemv_variant(true);
-        SDT_GEMV_DISPATCH(launch_q8, v, int(K / 16), int(N), x, W, scales, y, s);
+        const GemvVariant v = gemv_variant(q8);
+        int *status = nullptr;
+        rc = status_word(&status);
+        if (rc) return rc;
+        if (!try_stream(q8, v.stream_h, K, N, x, W, scales, y, s, dev, status, &e)) {
+            if (!q8) SDT_GEMV_DISPATCH(launch_bf16, v, int(K / 8), int(N), x, W, y, s);
+            else SDT_GEMV_DISPATCH(launch_q8, v, int(K / 16), int(N), x, W, scales, y, s);
+            e = cudaGetLastError();
+        }
     }
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(SDT_ERR_LAUNCH, "gemv launch failed: %s", cudaGetErrorString(e));
     return SDT_OK;
 }

@@ -15,7 +15,7 @@ def test_timeout_probe_reports_and_clears(cuda_device):
     with pytest.raises(sdt.SdtError) as e:
         sdt.check_device_status()
     assert e.value.status == "SDT_ERR_TIMEOUT"
-    assert e.value.where == 5
+    assert e.value.where & 0xF == 5
     sdt.check_device_status()  # the word was cleared by the read
     # the context is still usable
     A = inputs.integers((256, 256), seed=1).to(cuda_device)

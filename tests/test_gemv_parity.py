@@ -13,7 +13,7 @@ from _parity import assert_close, u16
 pytestmark = pytest.mark.gpu
 
 K_DEC, N_DEC = 4096, 12288
-VARIANTS = ["1,4", "1,8", "2,2", "2,4", "4,2", "4,4"]
+VARIANTS = ["stream", "stream1", "stream2", "1,4", "2,4", "4,4"]
 
 
 @pytest.fixture
