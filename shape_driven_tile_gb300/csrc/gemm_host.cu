@@ -43,41 +43,49 @@ struct LadderTile {
     int tmem_cols;
     int threads;
     bool persistent;  // one CTA per SM walking tiles; accumulator double-buffered in TMEM
-    double kt_cycles;
-    double fixed_cycles;
+    // pick_tile cost model, fitted to the measured sweep of every feasible tile (us):
+    //   fixed  -- per launch (persistent) or per round of co-resident CTAs
+    //   kt     -- per k-tile per round of tiles on one worker (CTA, or CTA pair)
+    //   per_mb -- per MB of operand tiles the whole grid streams from L2
+    double fixed_us;
+    double kt_us;
+    double per_mb_us;
+    bool candidate;   // considered by pick_tile (tiles dominated everywhere in the sweep are not)
 };
 
-#define SDT_TILE(BM_, BN_, STAGES_, NAME_, KT_, FIX_)                                              \
+#define SDT_TILE(BM_, BN_, STAGES_, NAME_, FIX_, KT_, MB_, CAND_)                                  \
     LadderTile {                                                                                   \
         BM_, BN_, 1, STAGES_, NAME_, &launch_gemm_tile<BM_, BN_>, TileCfg<BM_, BN_>::STAGE_BYTES,  \
             TileCfg<BM_, BN_>::ALIGN_SLACK + TileCfg<BM_, BN_>::CTRL_BYTES,                        \
-            TileCfg<BM_, BN_>::TMEM_COLS, TileCfg<BM_, BN_>::THREADS, false, KT_, FIX_             \
+            TileCfg<BM_, BN_>::TMEM_COLS, TileCfg<BM_, BN_>::THREADS, false, FIX_, KT_, MB_, CAND_ \
     }
 
-#define SDT_PTILE(BN_, STAGES_, NAME_, KT_, FIX_)                                                  \
+#define SDT_PTILE(BN_, STAGES_, NAME_, FIX_, KT_, MB_, CAND_)                                       \
     LadderTile {                                                                                   \
         128, BN_, 1, STAGES_, NAME_, &launch_gemm_persistent<BN_>, PersistentCfg<BN_>::STAGE_BYTES, \
             PersistentCfg<BN_>::ALIGN_SLACK + PersistentCfg<BN_>::CTRL_BYTES,                      \
-            PersistentCfg<BN_>::TMEM_COLS, PersistentCfg<BN_>::THREADS, true, KT_, FIX_            \
+            PersistentCfg<BN_>::TMEM_COLS, PersistentCfg<BN_>::THREADS, true, FIX_, KT_, MB_, CAND_ \
     }
 
-#define SDT_PAIR(BN_, STAGES_, NAME_, KT_, FIX_)                                                   \
+#define SDT_PAIR(BN_, STAGES_, NAME_, FIX_, KT_, MB_, CAND_)                                        \
     LadderTile {                                                                                   \
         256, BN_, 2, STAGES_, NAME_, &launch_gemm_pair<BN_>, PairCfg<BN_>::STAGE_BYTES,            \
             PairCfg<BN_>::ALIGN_SLACK + PairCfg<BN_>::CTRL_BYTES, PairCfg<BN_>::TMEM_COLS,         \
-            PairCfg<BN_>::THREADS, true, KT_, FIX_                                                 \
+            PairCfg<BN_>::THREADS, true, FIX_, KT_, MB_, CAND_                                     \
     }
 
+// Cost-model constants fitted on GB300 (152 SMs) to the cold-L2 sweep of every
+// feasible tile over square, K-scan and rectangular shapes (bench.py --mode sweep).
 static const LadderTile kLadder[] = {
-    SDT_TILE(64, 64, 6, "64x64", 160.0, 3000.0),
-    SDT_TILE(64, 128, 4, "64x128", 290.0, 3500.0),
-    SDT_TILE(128, 64, 4, "128x64", 200.0, 3500.0),
-    SDT_TILE(128, 128, 6, "128x128", 330.0, 4500.0),
-    SDT_TILE(128, 256, 4, "128x256", 580.0, 7000.0),
-    SDT_PTILE(128, 6, "p128x128", 330.0, 1500.0),
-    SDT_PTILE(256, 4, "p128x256", 580.0, 2000.0),
-    SDT_PAIR(128, 8, "2cta_256x128", 330.0, 2000.0),
-    SDT_PAIR(256, 6, "2cta_256x256", 580.0, 2500.0),
+    SDT_TILE(64, 64, 6, "64x64", 5.587, 0.12525, 0.00000, true),
+    SDT_TILE(64, 128, 4, "64x128", 7.070, 0.14383, 0.00000, true),
+    SDT_TILE(128, 64, 4, "128x64", 6.966, 0.14082, 0.00000, true),
+    SDT_TILE(128, 128, 6, "128x128", 6.446, 0.28298, 0.00000, true),
+    SDT_TILE(128, 256, 4, "128x256", 8.098, 0.38408, 0.00000, false),
+    SDT_PTILE(128, 6, "p128x128", 9.033, 0.21035, 0.01685, true),
+    SDT_PTILE(256, 4, "p128x256", 9.761, 0.32421, 0.01203, true),
+    SDT_PAIR(128, 8, "2cta_256x128", 10.814, 0.26226, 0.01143, false),
+    SDT_PAIR(256, 6, "2cta_256x256", 11.818, 0.26476, 0.01995, true),
 };
 static constexpr int kNumTiles = sizeof(kLadder) / sizeof(kLadder[0]);
 static constexpr int kDefaultSmemLimit = 232448;  // opt-in shared memory per block on sm_100-class parts
@@ -115,37 +123,38 @@ static int ctas_per_sm(const LadderTile &t, int smem_per_sm) {
     return occ < 1 ? 1 : occ;
 }
 
-// Estimated makespan (SM cycles) of tile t on the shape: the tensor work of all
-// CTAs spread over the SMs in whole waves, plus fixed costs per round of
-// co-resident CTAs.
-static double model_cycles(const LadderTile &t, int64_t M, int64_t N, int64_t K, int sm_count,
-                           int smem_per_sm) {
+// Estimated run time (us) of tile t on the shape.  Persistent tiles: one worker
+// (CTA or CTA pair) per SM (pair of SMs) walking ceil(tiles / workers) tiles,
+// fixed cost once.  Other tiles: whole waves of CTAs, fixed cost per round of
+// co-resident CTAs.  Both pay for the operand bytes the grid streams from L2.
+static double model_us(const LadderTile &t, int64_t M, int64_t N, int64_t K, int sm_count, int smem_per_sm) {
     const double tiles = double(M / t.BM) * double(N / t.BN);
     const double nK = double(K / kBK);
+    const double mb = tiles * nK * double(t.BM + t.BN) * kBK * 2.0 / 1e6;
     if (t.persistent) {
-        // one worker (CTA, or CTA pair) per SM (pair of SMs) walking its share of the tiles;
-        // epilogues overlap the next tile, the fixed cost is paid once
         const double workers = t.cta_group == 2 ? double(sm_count / 2) : double(sm_count);
-        return std::ceil(tiles / workers) * nK * t.kt_cycles + t.fixed_cycles;
+        return t.fixed_us + std::ceil(tiles / workers) * nK * t.kt_us + mb * t.per_mb_us;
     }
     const int occ = ctas_per_sm(t, smem_per_sm);
-    const double waves_1 = std::ceil(tiles / sm_count);
     const double rounds = std::ceil(tiles / (double(sm_count) * occ));
-    return waves_1 * nK * t.kt_cycles + rounds * t.fixed_cycles;
+    const double waves_1 = std::ceil(tiles / sm_count);
+    return rounds * t.fixed_us + waves_1 * nK * t.kt_us + mb * t.per_mb_us;
 }
 
 static int pick_for(int64_t M, int64_t N, int64_t K, int sm_count, int smem_limit, int smem_per_sm) {
-    int best = -1;
+    int best = -1, fallback = -1;
     double best_cost = 0.0;
     for (int i = 0; i < kNumTiles; ++i) {
         if (!feasible(kLadder[i], M, N, K, smem_limit)) continue;
-        double c = model_cycles(kLadder[i], M, N, K, sm_count, smem_per_sm);
+        if (fallback < 0) fallback = i;
+        if (!kLadder[i].candidate) continue;
+        const double c = model_us(kLadder[i], M, N, K, sm_count, smem_per_sm);
         if (best < 0 || c < best_cost * (1.0 - 1e-9)) {
             best = i;
             best_cost = c;
         }
     }
-    return best;
+    return best >= 0 ? best : fallback;
 }
 
 static int find_tile(const char *name) {
