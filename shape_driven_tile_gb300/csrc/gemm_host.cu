@@ -44,9 +44,12 @@ struct LadderTile {
     int threads;
     bool persistent;  // one CTA per SM walking tiles; accumulator double-buffered in TMEM
     // pick_tile cost model, fitted to the measured sweep of every feasible tile (us):
-    //   fixed  -- per launch (persistent) or per round of co-resident CTAs
-    //   kt     -- per k-tile per round of tiles on one worker (CTA, or CTA pair)
-    //   per_mb -- per MB of operand tiles the whole grid streams from L2
+    //   fixed  -- per launch (persistent) or per round of co-resident CTAs; it
+    //             covers the launch, the pipeline fill and the first `stages` k-tiles
+    //             (issued as one burst), and the exposed epilogue
+    //   kt     -- per further k-tile per round of tiles on one worker (CTA or pair)
+    //   per_mb -- per MB of operand tiles the whole grid streams from L2 (fits to 0
+    //             on GB300; kept so the model can express bandwidth-bound ladders)
     double fixed_us;
     double kt_us;
     double per_mb_us;
@@ -74,18 +77,19 @@ struct LadderTile {
             PairCfg<BN_>::THREADS, true, FIX_, KT_, MB_, CAND_                                     \
     }
 
-// Cost-model constants fitted on GB300 (152 SMs) to the cold-L2 sweep of every
-// feasible tile over square, K-scan and rectangular shapes (bench.py --mode sweep).
+// Cost-model constants fitted on GB300 (152 SMs) by one least-squares fit over
+// the cold-L2 sweep of every feasible tile on 43 shapes: the square sizes, the
+// K-scan, rectangular and deep-K shapes (bench.py --mode sweep).
 static const LadderTile kLadder[] = {
-    SDT_TILE(64, 64, 6, "64x64", 5.587, 0.12525, 0.00000, true),
-    SDT_TILE(64, 128, 4, "64x128", 7.070, 0.14383, 0.00000, true),
-    SDT_TILE(128, 64, 4, "128x64", 6.966, 0.14082, 0.00000, true),
-    SDT_TILE(128, 128, 6, "128x128", 6.446, 0.28298, 0.00000, true),
-    SDT_TILE(128, 256, 4, "128x256", 8.098, 0.38408, 0.00000, false),
-    SDT_PTILE(128, 6, "p128x128", 9.033, 0.21035, 0.01685, true),
-    SDT_PTILE(256, 4, "p128x256", 9.761, 0.32421, 0.01203, true),
-    SDT_PAIR(128, 8, "2cta_256x128", 10.814, 0.26226, 0.01143, false),
-    SDT_PAIR(256, 6, "2cta_256x256", 11.818, 0.26476, 0.01995, true),
+    SDT_TILE(64, 64, 6, "64x64", 6.174, 0.28066, 0.00000, true),
+    SDT_TILE(64, 128, 4, "64x128", 7.399, 0.32058, 0.00000, true),
+    SDT_TILE(128, 64, 4, "128x64", 7.378, 0.31033, 0.00000, true),
+    SDT_TILE(128, 128, 6, "128x128", 8.030, 0.30361, 0.00000, true),
+    SDT_TILE(128, 256, 4, "128x256", 9.910, 0.37718, 0.00000, false),
+    SDT_PTILE(128, 6, "p128x128", 10.442, 0.27964, 0.00000, true),
+    SDT_PTILE(256, 4, "p128x256", 11.265, 0.37733, 0.00000, true),
+    SDT_PAIR(128, 8, "2cta_256x128", 12.888, 0.29877, 0.00000, false),
+    SDT_PAIR(256, 6, "2cta_256x256", 13.532, 0.32647, 0.00000, true),
 };
 static constexpr int kNumTiles = sizeof(kLadder) / sizeof(kLadder[0]);
 static constexpr int kDefaultSmemLimit = 232448;  // opt-in shared memory per block on sm_100-class parts
@@ -133,12 +137,12 @@ static double model_us(const LadderTile &t, int64_t M, int64_t N, int64_t K, int
     const double mb = tiles * nK * double(t.BM + t.BN) * kBK * 2.0 / 1e6;
     if (t.persistent) {
         const double workers = t.cta_group == 2 ? double(sm_count / 2) : double(sm_count);
-        return t.fixed_us + std::ceil(tiles / workers) * nK * t.kt_us + mb * t.per_mb_us;
+        const double ktiles = std::max(0.0, std::ceil(tiles / workers) * nK - t.stages);
+        return t.fixed_us + ktiles * t.kt_us + mb * t.per_mb_us;
     }
     const int occ = ctas_per_sm(t, smem_per_sm);
     const double rounds = std::ceil(tiles / (double(sm_count) * occ));
-    const double waves_1 = std::ceil(tiles / sm_count);
-    return rounds * t.fixed_us + waves_1 * nK * t.kt_us + mb * t.per_mb_us;
+    return rounds * (t.fixed_us + std::max(0.0, nK - t.stages) * t.kt_us) + mb * t.per_mb_us;
 }
 
 static int pick_for(int64_t M, int64_t N, int64_t K, int sm_count, int smem_limit, int smem_per_sm) {
