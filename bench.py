@@ -781,6 +781,50 @@ def run_large(args):
     print(json.dumps({"mode": "large", "rows": rows}), flush=True)
 
 
+def run_splitk(args):
+    """Split-K against the best unsplit tile on small-grid shapes (cold L2)."""
+    import torch
+
+    import shape_driven_tile_gb300 as sdt
+
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    flush = L2Flush(dev)
+    shapes = [tuple(int(v) for v in s.lower().split("x")) for s in (args.shapes or [])] or [
+        (256, 256, 8192), (512, 512, 8192), (1024, 1024, 8192), (256, 4096, 4096), (2048, 512, 8192),
+        (1024, 2048, 8192), (512, 512, 4096), (1024, 1024, 4096), (256, 256, 256), (512, 512, 512),
+        (1024, 1024, 1024), (768, 768, 768)]
+    for (M, N, K) in shapes:
+        A = (torch.rand((M, K), device=dev) * 2 - 1).half()
+        B = (torch.rand((K, N), device=dev) * 2 - 1).half()
+        C = torch.empty((M, N), device=dev, dtype=torch.float16)
+        base = {}
+        for t in sdt.feasible_tiles(M, N, K):
+            for _ in range(3):
+                sdt.gemm_f16_with_tile(A, B, C, tile=t)
+            base[sdt.tile_info(t)["name"]] = time_cold(lambda: sdt.gemm_f16_with_tile(A, B, C, tile=t),
+                                                       args.reps, flush, stream)[0]
+        tid, sp = sdt.pick_splitk(M, N, K, sm_count=sdt.device_sm_count())
+        res = {}
+        for algo in (sdt.SPLITK_REDUCE_KERNEL, sdt.SPLITK_IN_KERNEL):
+            for splits in sorted({2, 4, 8, 16, sp}):
+                if splits > K // 64 or sdt.splitk_workspace_bytes(M, N, K, tid, splits) == 0:
+                    continue
+                ws = sdt.splitk_workspace(M, N, K, tid, splits, device=dev)
+                fn = lambda: sdt.gemm_f16_splitk(A, B, C, workspace=ws, tile=tid, splits=splits, algo=algo)
+                for _ in range(3):
+                    fn()
+                res[f"{'ik' if algo else 'rk'}x{splits}"] = time_cold(fn, args.reps, flush, stream)[0]
+        best_base = min(base, key=base.get)
+        best_split = min(res, key=res.get) if res else None
+        print(json.dumps({"shape": [M, N, K], "split_tile": sdt.tile_info(tid)["name"], "picked_splits": sp,
+                          "best_unsplit": best_base, "best_unsplit_us": round(base[best_base] * 1e3, 2),
+                          "split_us": {k: round(v * 1e3, 2) for k, v in res.items()},
+                          "speedup_best_split": round(base[best_base] / res[best_split], 3) if res else None}),
+              flush=True)
+    sdt.check_device_status()
+
+
 def run_one(args):
     """A few launches of one kernel (for profiler captures): a square GEMM with pick_tile,
     or the decode GEMV (--gemv bf16|q8)."""
@@ -822,7 +866,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["sdt", "reference"], default="sdt")
-    ap.add_argument("--mode", choices=["step", "sweep", "kscan", "decode", "large", "one"], default="step")
+    ap.add_argument("--mode", choices=["step", "sweep", "kscan", "decode", "large", "one", "splitk"], default="step")
     ap.add_argument("--gemv", choices=["bf16", "q8"])
     ap.add_argument("--reps", type=int, default=20)
     ap.add_argument("--sizes", type=int, nargs="*")
@@ -837,7 +881,7 @@ def main(argv=None):
     if args.impl == "reference":
         return run_reference(args)
     {"step": run_default, "sweep": run_sweep, "kscan": run_kscan, "decode": run_decode,
-     "large": run_large, "one": run_one}[args.mode](args)
+     "large": run_large, "one": run_one, "splitk": run_splitk}[args.mode](args)
 
 
 if __name__ == "__main__":

@@ -36,10 +36,13 @@
  *       opt-in measured sweep frozen into an artefact, k-loop start stagger with
  *       mask wraparound for power-of-two k-tile counts) and the third commit
  *       message (the K-scan that isolates power-of-two row strides).
+ *  [P4] "Iteratively Tuning hipBLASLt TensileLite Kernels" -- "The Six Rounds"
+ *       (split-K with a choice of reduction algorithm; workgroup mapping).
  */
 #ifndef SDT_H
 #define SDT_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -175,6 +178,54 @@ int sdt_seed_tile(int64_t M, int64_t N, int units);
 int gemm_f16_with_tile(int64_t M, int64_t N, int64_t K,
                        const void *A, const void *B, void *C, sdt_stream_t stream,
                        int tile_id, int stagger);
+
+/*
+ * Split-K [P4 "The Six Rounds", round 2 "Split-K": the contraction is split
+ * across CTAs and the partial results are reduced; the page distinguishes a
+ * reduction in a separate pass from one inside the single kernel].
+ *
+ * Output tile t of a one-CTA-per-tile ladder rung (64x64, 64x128, 128x64,
+ * 128x128, 128x256) is computed by `splits` CTAs, CTA s accumulating k-tiles
+ * [s*ceil(nK/splits), ...) (nK = K/64) and writing an fp32 partial tile to the
+ * caller's workspace; the partials are summed in split order (independent of
+ * arrival order) and rounded once to fp16:
+ *   SDT_SPLITK_REDUCE_KERNEL  a second kernel sums the partials;
+ *   SDT_SPLITK_IN_KERNEL      the last CTA of each tile to finish (per-tile
+ *                             arrival counter in the workspace) sums them and
+ *                             resets its counter to zero.
+ * `splits` is rounded down to the count that leaves no split empty.
+ * tile_id < 0 picks tile and splits with sdt_pick_splitk_for (then splits <= 0
+ * takes the picked count).  The k-loop stagger is not applied.
+ *
+ * Workspace: device memory owned by the caller, 256-byte aligned, at least
+ * sdt_splitk_workspace_bytes(M,N,K,tile_id,splits) bytes: fp32 partials
+ * [splits][M][N] (padded to 256 B) then one u32 counter per output tile.  The
+ * counters must be zero before the first SDT_SPLITK_IN_KERNEL call on a
+ * workspace (sdt_splitk_workspace_init zeroes a workspace on `stream`); every
+ * completed call leaves them zero again.  Calls that share a workspace must not
+ * overlap on the GPU.  Same operand requirements as gemm_f16 (tight row-major,
+ * 16-byte aligned; tile dims divide M, N; K % 64 == 0).
+ * Errors: SDT_ERR_TILE (tile without split-K form or not dividing the shape),
+ * SDT_ERR_ARG (splits out of 1..nK, unknown algo, workspace too small),
+ * SDT_ERR_ALIGN, SDT_ERR_NULL, as well as gemm_f16's.
+ */
+#define SDT_SPLITK_REDUCE_KERNEL 0
+#define SDT_SPLITK_IN_KERNEL 1
+int gemm_f16_splitk(int64_t M, int64_t N, int64_t K, const void *A, const void *B, void *C,
+                    void *workspace, size_t workspace_bytes, int tile_id, int splits, int algo,
+                    sdt_stream_t stream);
+/* Bytes of workspace gemm_f16_splitk needs (0 for an invalid combination). */
+size_t sdt_splitk_workspace_bytes(int64_t M, int64_t N, int64_t K, int tile_id, int splits);
+/* Zero a split-K workspace on `stream` (its counters must start at zero). */
+int sdt_splitk_workspace_init(void *workspace, size_t workspace_bytes, sdt_stream_t stream);
+/*
+ * Heuristic (tile, splits) for split-K on a GPU with `sm_count` SMs: the
+ * pick_tile cost model with K shared among the splits plus the reduction's
+ * fp32 traffic, minimised over the split-K tiles and 1..32 splits.  splits == 1
+ * means splitting does not pay.  Needs no GPU.
+ */
+int sdt_pick_splitk_for(int64_t M, int64_t N, int64_t K, int sm_count, int smem_limit,
+                        int *tile_id, int *splits);
 
 /*
  * Frozen tune table [P3 "Changes": the measured sweep can be frozen into an

@@ -17,7 +17,8 @@ __all__ = [
     "SdtError", "gemm_f16", "gemm_f16_with_tile", "gemv_m1", "gemv_m1_bf16", "gemv_m1_q8",
     "feasible_tiles", "pick_tile", "seed_tile", "tile_info", "tiles", "tile_id",
     "load_tune_table", "clear_tune_table", "tune_table_lookup", "check_device_status",
-    "debug_timeout_probe", "device_sm_count", "lib",
+    "debug_timeout_probe", "device_sm_count", "lib", "gemm_f16_splitk", "splitk_workspace",
+    "splitk_workspace_bytes", "pick_splitk", "SPLITK_REDUCE_KERNEL", "SPLITK_IN_KERNEL",
 ]
 
 
@@ -112,6 +113,46 @@ def gemv_m1(x, W, scales=None, y=None, *, stream=None):
     if scales is None:
         return gemv_m1_bf16(x, W, y, stream=stream)
     return gemv_m1_q8(x, W, scales, y, stream=stream)
+
+
+SPLITK_REDUCE_KERNEL = 0
+SPLITK_IN_KERNEL = 1
+
+
+def splitk_workspace_bytes(M: int, N: int, K: int, tile, splits: int) -> int:
+    tid = tile_id(tile) if isinstance(tile, str) else int(tile)
+    return int(lib().sdt_splitk_workspace_bytes(M, N, K, tid, int(splits)))
+
+
+def splitk_workspace(M: int, N: int, K: int, tile, splits: int, device=None) -> torch.Tensor:
+    """A zeroed workspace tensor for gemm_f16_splitk (allocated by torch, owned by the caller)."""
+    nbytes = splitk_workspace_bytes(M, N, K, tile, splits)
+    if nbytes == 0:
+        raise ValueError("invalid split-K combination")
+    ws = torch.empty(nbytes + 256, dtype=torch.uint8, device=device or "cuda")
+    off = (-ws.data_ptr()) % 256
+    ws = ws[off:off + nbytes]
+    check(lib().sdt_splitk_workspace_init(ws.data_ptr(), nbytes, _stream(None)))
+    return ws
+
+
+def gemm_f16_splitk(A, B, C=None, *, workspace, tile=-1, splits: int = 0,
+                    algo: int = SPLITK_REDUCE_KERNEL, stream=None):
+    """Split-K GEMM with a caller-owned workspace (see sdt.h); tile -1 picks tile and splits."""
+    M, N, K, C = _gemm_args(A, B, C)
+    tid = tile_id(tile) if isinstance(tile, str) else int(tile)
+    if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda:
+        raise TypeError("workspace must be a CUDA tensor")
+    nbytes = workspace.numel() * workspace.element_size()
+    check(lib().gemm_f16_splitk(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(), workspace.data_ptr(), nbytes,
+                                tid, int(splits), int(algo), _stream(stream)))
+    return C
+
+
+def pick_splitk(M: int, N: int, K: int, sm_count: int = 152, smem_limit: int = 232448):
+    t, sp = ctypes.c_int(0), ctypes.c_int(0)
+    check(lib().sdt_pick_splitk_for(M, N, K, int(sm_count), int(smem_limit), ctypes.byref(t), ctypes.byref(sp)))
+    return t.value, sp.value
 
 
 # ---- tiles ---------------------------------------------------------------------

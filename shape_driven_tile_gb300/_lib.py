@@ -50,6 +50,10 @@ SIGNATURES = {
     "sdt_device_sm_count": (cint, []),
     "sdt_device_smem_optin": (cint, []),
     "sdt_abi_version": (cint, []),
+    "gemm_f16_splitk": (cint, [i64, i64, i64, vp, vp, vp, vp, ctypes.c_size_t, cint, cint, cint, vp]),
+    "sdt_splitk_workspace_bytes": (ctypes.c_size_t, [i64, i64, i64, cint, cint]),
+    "sdt_splitk_workspace_init": (cint, [vp, ctypes.c_size_t, vp]),
+    "sdt_pick_splitk_for": (cint, [i64, i64, i64, cint, cint, ctypes.POINTER(cint), ctypes.POINTER(cint)]),
 }
 
 STATUS = {

@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -29,6 +30,11 @@
 namespace sdt {
 
 using LaunchFn = int (*)(const CUtensorMap &, const CUtensorMap &, const GemmArgs &, cudaStream_t);
+
+// Split-K launchers of the one-CTA-per-tile ladder rungs, in ladder order (null: no split-K form).
+static const LaunchFn kSplitLaunch[] = {
+    &launch_gemm_tile_split<64, 64>, &launch_gemm_tile_split<64, 128>, &launch_gemm_tile_split<128, 64>,
+    &launch_gemm_tile_split<128, 128>, &launch_gemm_tile_split<128, 256>, nullptr, nullptr, nullptr, nullptr};
 
 // One rung of the tile ladder.  kt_cycles / fixed_cycles feed pick_tile's cost
 // model: SM cycles one CTA of this tile spends per 64-deep k-tile when it has
@@ -318,7 +324,34 @@ static int tensor_map_f16(const void *ptr, uint64_t inner, uint64_t outer, uint6
     return SDT_OK;
 }
 
+static_assert(sizeof(kSplitLaunch) / sizeof(kSplitLaunch[0]) == kNumTiles, "one split entry per ladder tile");
+
 // ---- launch ----------------------------------------------------------------------
+
+__global__ void splitk_reduce_kernel(const float *__restrict__ partials, __half *__restrict__ C, size_t elems,
+                                     int splits) {
+    const size_t stride = size_t(gridDim.x) * blockDim.x * 8;
+    for (size_t i = (size_t(blockIdx.x) * blockDim.x + threadIdx.x) * 8; i < elems; i += stride) {
+        float4 a0 = __ldg(reinterpret_cast<const float4 *>(partials + i));
+        float4 a1 = __ldg(reinterpret_cast<const float4 *>(partials + i + 4));
+        for (int sp = 1; sp < splits; ++sp) {
+            const float4 b0 = __ldg(reinterpret_cast<const float4 *>(partials + sp * elems + i));
+            const float4 b1 = __ldg(reinterpret_cast<const float4 *>(partials + sp * elems + i + 4));
+            a0.x += b0.x; a0.y += b0.y; a0.z += b0.z; a0.w += b0.w;
+            a1.x += b1.x; a1.y += b1.y; a1.z += b1.z; a1.w += b1.w;
+        }
+        __half2 h0 = __floats2half2_rn(a0.x, a0.y), h1 = __floats2half2_rn(a0.z, a0.w);
+        __half2 h2 = __floats2half2_rn(a1.x, a1.y), h3 = __floats2half2_rn(a1.z, a1.w);
+        *reinterpret_cast<uint4 *>(C + i) =
+            make_uint4(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1),
+                       *reinterpret_cast<uint32_t *>(&h2), *reinterpret_cast<uint32_t *>(&h3));
+    }
+}
+
+__global__ void zero_fill_u32(unsigned *p, size_t n) {
+    for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += size_t(gridDim.x) * blockDim.x)
+        p[i] = 0u;
+}
 
 __global__ void zero_fill_f16(__half *C, size_t n) {
     size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x;
@@ -480,6 +513,143 @@ static int gemm_dispatch(int64_t M, int64_t N, int64_t K, const void *A, const v
     return run_tile(id, stagger, M, N, K, A, B, C, stream, dev);
 }
 
+// ---- split-K ----------------------------------------------------------------------
+
+static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Workspace layout: fp32 partials [splits][M][N], padded to 256 bytes, then one
+// u32 arrival counter per output tile.
+static size_t splitk_partials_bytes(int64_t M, int64_t N, int splits) {
+    return (size_t(splits) * size_t(M) * size_t(N) * 4 + 255) / 256 * 256;
+}
+
+static int splitk_effective(int64_t nK, int splits) {
+    const int64_t kps = ceil_div(nK, splits);
+    return int(ceil_div(nK, kps));
+}
+
+static bool splitk_tile_ok(int tile_id) {
+    return tile_id >= 0 && tile_id < kNumTiles && kSplitLaunch[tile_id] != nullptr;
+}
+
+static bool splitk_feasible(const LadderTile &t, int64_t M, int64_t N, int64_t K, int smem_limit) {
+    if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return false;
+    if (M % t.BM || N % t.BN || K % kBK) return false;
+    return tile_smem(t, t.stages) <= smem_limit && t.tmem_cols <= 512;
+}
+
+// Cost model for (tile, splits): the tile model with K divided among the splits,
+// CTAs = tiles x splits, plus the reduction's fp32 traffic (written once, read once).
+static double splitk_model_us(const LadderTile &t, int64_t M, int64_t N, int64_t K, int splits, int sm_count,
+                              int smem_per_sm) {
+    const double tiles = double(M / t.BM) * double(N / t.BN) * splits;
+    const double kps = double(ceil_div(K / kBK, splits));
+    const int occ = ctas_per_sm(t, smem_per_sm);
+    const double rounds = std::ceil(tiles / (double(sm_count) * occ));
+    double us = rounds * (t.fixed_us + std::max(0.0, kps - t.stages) * t.kt_us);
+    if (splits > 1) us += 1.0 + double(M) * double(N) * (8.0 * splits + 2.0) / 4.0e6;  // ~4 TB/s through L2
+    return us;
+}
+
+static int pick_splitk_for(int64_t M, int64_t N, int64_t K, int sm_count, int smem_limit, int smem_per_sm,
+                           int *tile_out, int *splits_out) {
+    double best = 0.0;
+    int bt = -1, bs = 1;
+    const int64_t nK = K / kBK;
+    for (int i = 0; i < kNumTiles; ++i) {
+        if (!splitk_tile_ok(i) || !kLadder[i].candidate) continue;
+        if (!splitk_feasible(kLadder[i], M, N, K, smem_limit)) continue;
+        for (int sp = 1; sp <= 32 && sp <= nK; ++sp) {
+            if (splitk_effective(nK, sp) != sp) continue;
+            const double c = splitk_model_us(kLadder[i], M, N, K, sp, sm_count, smem_per_sm);
+            if (bt < 0 || c < best * (1.0 - 1e-9)) {
+                best = c;
+                bt = i;
+                bs = sp;
+            }
+        }
+    }
+    if (bt < 0) return fail(SDT_ERR_SHAPE, "no tile divides %lldx%lldx%lld", (long long)M, (long long)N, (long long)K);
+    *tile_out = bt;
+    *splits_out = bs;
+    return SDT_OK;
+}
+
+static int splitk_run(int64_t M, int64_t N, int64_t K, const void *A, const void *B, void *C, void *ws,
+                      size_t ws_bytes, int tile_id, int splits, int algo, cudaStream_t stream) {
+    int rc = validate_common(M, N, K, A, B, C);
+    if (rc) return rc;
+    if (M == 0 || N == 0) return SDT_OK;
+    if (algo != SDT_SPLITK_REDUCE_KERNEL && algo != SDT_SPLITK_IN_KERNEL)
+        return fail(SDT_ERR_ARG, "unknown split-K algorithm %d", algo);
+    DeviceInfo dev;
+    rc = current_device(&dev);
+    if (rc) return rc;
+    if (K == 0) return gemm_dispatch(M, N, K, A, B, C, reinterpret_cast<sdt_stream_t>(stream), -1, -1);
+    if (tile_id < 0) {
+        int sp = 1;
+        rc = pick_splitk_for(M, N, K, dev.sm_count, dev.smem_optin, dev.smem_per_sm, &tile_id, &sp);
+        if (rc) return rc;
+        if (splits <= 0) splits = sp;
+    }
+    if (!splitk_tile_ok(tile_id)) return fail(SDT_ERR_TILE, "tile %d has no split-K form", tile_id);
+    const LadderTile &t = kLadder[tile_id];
+    if (!splitk_feasible(t, M, N, K, dev.smem_optin))
+        return fail(SDT_ERR_TILE, "tile %s does not divide %lldx%lldx%lld", t.name, (long long)M, (long long)N,
+                    (long long)K);
+    const int64_t nK = K / kBK;
+    if (splits < 1 || splits > nK) return fail(SDT_ERR_ARG, "splits must be in 1..%lld", (long long)nK);
+    splits = splitk_effective(nK, splits);
+    const int64_t tiles = (M / t.BM) * (N / t.BN);
+    const size_t need = splitk_partials_bytes(M, N, splits) + size_t(tiles) * 4;
+    if (!ws) return fail(SDT_ERR_NULL, "split-K needs a workspace");
+    if (reinterpret_cast<uintptr_t>(ws) & 255) return fail(SDT_ERR_ALIGN, "the workspace must be 256-byte aligned");
+    if (ws_bytes < need)
+        return fail(SDT_ERR_ARG, "workspace of %zu bytes is smaller than the %zu bytes needed", ws_bytes, need);
+    CUtensorMap tmA, tmB;
+    rc = tensor_map_f16(A, uint64_t(K), uint64_t(M), uint64_t(K) * 2, kBK, uint32_t(t.BM), &tmA);
+    if (rc) return rc;
+    rc = tensor_map_f16(B, uint64_t(N), uint64_t(K), uint64_t(N) * 2, 64, kBK, &tmB);
+    if (rc) return rc;
+    int *status = nullptr;
+    rc = status_word(&status);
+    if (rc) return rc;
+    GemmArgs a;
+    memset(&a, 0, sizeof a);
+    a.C = static_cast<__half *>(C);
+    a.M = int(M);
+    a.N = int(N);
+    a.K = int(K);
+    a.num_m_tiles = int(M / t.BM);
+    a.num_n_tiles = int(N / t.BN);
+    a.num_k_tiles = int(nK);
+    a.stages = tile_stages(t, dev.smem_optin);
+    a.stagger = 0;
+    a.stagger_stride = 1;
+    a.raster_group = env_int("SDT_RASTER_GROUP", 8, 1, 1 << 20);
+    a.timeout_ns = wait_timeout_ns();
+    a.status = status;
+    a.max_ctas = dev.sm_count * ctas_per_sm(t, dev.smem_per_sm);
+    a.splits = splits;
+    a.k_per_split = int(ceil_div(nK, splits));
+    a.splitk_reduce_in_kernel = algo == SDT_SPLITK_IN_KERNEL ? 1 : 0;
+    a.partials = static_cast<float *>(ws);
+    a.counters = reinterpret_cast<unsigned *>(static_cast<char *>(ws) + splitk_partials_bytes(M, N, splits));
+    int e = kSplitLaunch[tile_id](tmA, tmB, a, stream);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(SDT_ERR_LAUNCH, "split-K launch of tile %s failed: %s", t.name, cudaGetErrorString(cudaError_t(e)));
+    }
+    if (algo == SDT_SPLITK_REDUCE_KERNEL) {
+        const size_t elems = size_t(M) * size_t(N);
+        const unsigned blocks = unsigned(std::min<size_t>((elems / 8 + 255) / 256, size_t(dev.sm_count) * 8));
+        splitk_reduce_kernel<<<blocks, 256, 0, stream>>>(a.partials, a.C, elems, splits);
+        cudaError_t e2 = cudaGetLastError();
+        if (e2 != cudaSuccess) return fail(SDT_ERR_LAUNCH, "split-K reduction launch failed: %s", cudaGetErrorString(e2));
+    }
+    return SDT_OK;
+}
+
 }  // namespace sdt
 
 using namespace sdt;
@@ -595,6 +765,44 @@ int sdt_tune_table_size(void) {
 int sdt_tune_table_lookup(int64_t M, int64_t N, int64_t K) {
     TuneEntry e;
     return table_lookup(M, N, K, &e) ? e.tile : -1;
+}
+
+size_t sdt_splitk_workspace_bytes(int64_t M, int64_t N, int64_t K, int tile_id, int splits) {
+    clear_error();
+    if (M <= 0 || N <= 0 || K <= 0 || !splitk_tile_ok(tile_id) || splits < 1) return 0;
+    const LadderTile &t = kLadder[tile_id];
+    if (M % t.BM || N % t.BN || K % kBK || splits > K / kBK) return 0;
+    const int sp = splitk_effective(K / kBK, splits);
+    return splitk_partials_bytes(M, N, sp) + size_t((M / t.BM) * (N / t.BN)) * 4;
+}
+
+int sdt_splitk_workspace_init(void *workspace, size_t workspace_bytes, sdt_stream_t stream) {
+    clear_error();
+    if (!workspace) return fail(SDT_ERR_NULL, "workspace is NULL");
+    if (reinterpret_cast<uintptr_t>(workspace) & 255) return fail(SDT_ERR_ALIGN, "the workspace must be 256-byte aligned");
+    DeviceInfo dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    const size_t n = workspace_bytes / 4;
+    if (n == 0) return SDT_OK;
+    const unsigned blocks = unsigned(std::min<size_t>((n + 255) / 256, size_t(dev.sm_count) * 8));
+    zero_fill_u32<<<blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(static_cast<unsigned *>(workspace), n);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? SDT_OK : fail(SDT_ERR_LAUNCH, "workspace init failed: %s", cudaGetErrorString(e));
+}
+
+int sdt_pick_splitk_for(int64_t M, int64_t N, int64_t K, int sm_count, int smem_limit, int *tile_id, int *splits) {
+    clear_error();
+    if (!tile_id || !splits) return fail(SDT_ERR_NULL, "tile_id and splits must not be NULL");
+    if (sm_count <= 0) return fail(SDT_ERR_ARG, "sm_count must be positive");
+    return pick_splitk_for(M, N, K, sm_count, smem_limit, 233472, tile_id, splits);
+}
+
+int gemm_f16_splitk(int64_t M, int64_t N, int64_t K, const void *A, const void *B, void *C, void *workspace,
+                    size_t workspace_bytes, int tile_id, int splits, int algo, sdt_stream_t stream) {
+    clear_error();
+    return splitk_run(M, N, K, A, B, C, workspace, workspace_bytes, tile_id, splits, algo,
+                      reinterpret_cast<cudaStream_t>(stream));
 }
 
 // Number of tensor maps encoded so far (cache misses); for the cache-key tests.

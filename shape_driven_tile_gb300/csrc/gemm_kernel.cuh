@@ -50,6 +50,12 @@ struct GemmArgs {
     unsigned long long timeout_ns;
     int *status;          // device status word (first error code wins)
     int max_ctas;         // persistent kernels: grid size cap (one CTA per SM); host-side only
+    // split-K (blockIdx.y = split): k-tiles [split*k_per_split, ...) of each output tile
+    int splits;
+    int k_per_split;
+    int splitk_reduce_in_kernel;  // 1: the last CTA of a tile sums the partials and writes C
+    float *partials;      // [splits][M][N] fp32
+    unsigned *counters;   // [num_m_tiles * num_n_tiles], zero between calls
 };
 
 template <int BM, int BN>
@@ -73,7 +79,11 @@ __device__ __forceinline__ void record_status(int *status, int code) {
     if (status) atomicCAS(status, 0, code);
 }
 
-template <int BM, int BN>
+// SPLIT: the CTA accumulates only its split's k-tiles and writes an fp32 partial
+// tile to p.partials[split]; with p.splitk_reduce_in_kernel the last CTA of the
+// output tile to finish (per-tile arrival counter) sums all partials in split
+// order and writes the fp16 tile, then resets the counter to zero.
+template <int BM, int BN, bool SPLIT = false>
 __global__ void __launch_bounds__(128, 1)
     gemm_f16_tile_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB, const GemmArgs p) {
@@ -91,6 +101,7 @@ __global__ void __launch_bounds__(128, 1)
     uint64_t *acc_full = bars + 2 * S;
     volatile uint32_t *ctrl = reinterpret_cast<volatile uint32_t *>(bars + 2 * S + 1);
     // ctrl[0]: TMEM base address   ctrl[1]: error flag   ctrl[2]: k-tiles issued by TMA
+    // ctrl[3]: split-K, this CTA is the last of its tile
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -106,7 +117,9 @@ __global__ void __launch_bounds__(128, 1)
     const int n_tile = in_band / band_m;
     const int m0 = m_tile * BM;
     const int n0 = n_tile * BN;
-    const int nK = p.num_k_tiles;
+    const int split = SPLIT ? static_cast<int>(blockIdx.y) : 0;
+    const int k_first = SPLIT ? split * p.k_per_split : 0;
+    const int nK = SPLIT ? min(p.k_per_split, p.num_k_tiles - k_first) : p.num_k_tiles;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -134,7 +147,8 @@ __global__ void __launch_bounds__(128, 1)
         // ---------------- TMA producer ----------------
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
-        const int start = p.stagger
+        const bool stagger = !SPLIT && p.stagger;
+        const int start = stagger
             ? static_cast<int>((static_cast<uint32_t>(lin) * static_cast<uint32_t>(p.stagger_stride)) &
                                static_cast<uint32_t>(nK - 1))
             : 0;
@@ -147,7 +161,7 @@ __global__ void __launch_bounds__(128, 1)
                 break;
             }
             if (ctrl[1]) break;
-            const int kt = p.stagger ? ((start + i) & (nK - 1)) : i;
+            const int kt = k_first + (stagger ? ((start + i) & (nK - 1)) : i);
             const uint32_t fb = smem_u32(&full[s]);
             mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
             tma_load_2d(smem_u32(smA + s * Cfg::A_BYTES), &tmA, fb, kt * kBK, m0);
@@ -201,11 +215,20 @@ __global__ void __launch_bounds__(128, 1)
         const bool row_valid = (BM == 128) || (lane < 16);
         const uint32_t taddr_row = tmem_d + (static_cast<uint32_t>(warp * 32) << 16);
         __half *crow = p.C + static_cast<size_t>(m0 + row) * p.N + n0;
+        float *prow = SPLIT ? p.partials + (static_cast<size_t>(split) * p.M + m0 + row) * p.N + n0 : nullptr;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
             uint32_t r[32];
             tmem_ld_32x32b_x32(taddr_row + c, r);
             tmem_ld_wait();
+            if (SPLIT) {
+                if (row_valid && acc_ok) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(prow + c);
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) dst[t] = make_uint4(r[4 * t], r[4 * t + 1], r[4 * t + 2], r[4 * t + 3]);
+                }
+                continue;
+            }
             if (row_valid && acc_ok) {
                 uint32_t h[16];
 #pragma unroll
@@ -222,6 +245,44 @@ __global__ void __launch_bounds__(128, 1)
         }
     }
     tc_fence_before();
+    if (SPLIT && p.splitk_reduce_in_kernel) {
+        // Publish this split's partial, then count arrivals on the tile; the last CTA
+        // to arrive sums every split's partial in split order (so the result does not
+        // depend on arrival order), writes C, and resets the counter for the next call.
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const unsigned prev = atomicAdd(&p.counters[lin], 1u);
+            ctrl[3] = (prev == static_cast<unsigned>(p.splits - 1)) ? 1u : 0u;
+        }
+        __syncthreads();
+        if (ctrl[3]) {
+            __threadfence();
+            const int row = (BM == 128) ? (warp * 32 + lane) : (warp * 16 + lane);
+            if ((BM == 128 || lane < 16) && !ctrl[1]) {
+                const size_t plane = static_cast<size_t>(p.M) * p.N;
+                const float *src = p.partials + static_cast<size_t>(m0 + row) * p.N + n0;
+                __half *crow = p.C + static_cast<size_t>(m0 + row) * p.N + n0;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 8) {
+                    float4 a0 = __ldcg(reinterpret_cast<const float4 *>(src + c));
+                    float4 a1 = __ldcg(reinterpret_cast<const float4 *>(src + c + 4));
+                    for (int sp = 1; sp < p.splits; ++sp) {
+                        const float4 b0 = __ldcg(reinterpret_cast<const float4 *>(src + sp * plane + c));
+                        const float4 b1 = __ldcg(reinterpret_cast<const float4 *>(src + sp * plane + c + 4));
+                        a0.x += b0.x; a0.y += b0.y; a0.z += b0.z; a0.w += b0.w;
+                        a1.x += b1.x; a1.y += b1.y; a1.z += b1.z; a1.w += b1.w;
+                    }
+                    __half2 h0 = __floats2half2_rn(a0.x, a0.y), h1 = __floats2half2_rn(a0.z, a0.w);
+                    __half2 h2 = __floats2half2_rn(a1.x, a1.y), h3 = __floats2half2_rn(a1.z, a1.w);
+                    *reinterpret_cast<uint4 *>(crow + c) =
+                        make_uint4(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1),
+                                   *reinterpret_cast<uint32_t *>(&h2), *reinterpret_cast<uint32_t *>(&h3));
+                }
+            }
+            if (threadIdx.x == 0) atomicExch(&p.counters[lin], 0u);
+        }
+    }
     __syncthreads();
 
     if (threadIdx.x == 0 && ctrl[1]) {
@@ -242,9 +303,17 @@ __global__ void __launch_bounds__(128, 1)
     }
 }
 
-// Host-side launcher, one instantiation per ladder tile (defined in gemm_tiles.cu).
+// Sums the fp32 partials [splits][M][N] in split order and writes fp16 C (the
+// separate-kernel reduction of split-K); each thread handles 8 consecutive columns.
+__global__ void splitk_reduce_kernel(const float *__restrict__ partials, __half *__restrict__ C, size_t elems,
+                                     int splits);
+
+// Host-side launchers, one instantiation per ladder tile (gemm_t*.cu).
 template <int BM, int BN>
 int launch_gemm_tile(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args,
                      cudaStream_t stream);
+template <int BM, int BN>
+int launch_gemm_tile_split(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args,
+                           cudaStream_t stream);
 
 }  // namespace sdt

@@ -34,6 +34,28 @@ int launch_gemm_tile(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmA
     return cudaGetLastError();
 }
 
+template <int BM, int BN>
+int launch_gemm_tile_split(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args,
+                           cudaStream_t stream) {
+    using Cfg = TileCfg<BM, BN>;
+    auto kern = gemm_f16_tile_kernel<BM, BN, true>;
+    const int smem = Cfg::smem_bytes(args.stages);
+    static std::atomic<int> configured[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (configured[dev].load(std::memory_order_acquire) < smem) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        int prev = configured[dev].load();
+        while (prev < smem && !configured[dev].compare_exchange_weak(prev, smem)) {
+        }
+    }
+    const dim3 grid(static_cast<unsigned>(args.num_m_tiles) * static_cast<unsigned>(args.num_n_tiles),
+                    static_cast<unsigned>(args.splits), 1);
+    kern<<<grid, Cfg::THREADS, smem, stream>>>(tmA, tmB, args);
+    return cudaGetLastError();
+}
+
 template <int BN>
 int launch_gemm_persistent(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args,
                            cudaStream_t stream) {
@@ -103,4 +125,6 @@ int launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmA
 
 #define SDT_INSTANTIATE_GEMM_TILE(BM, BN)                                                          \
     template int sdt::launch_gemm_tile<BM, BN>(const CUtensorMap &, const CUtensorMap &,           \
-                                               const sdt::GemmArgs &, cudaStream_t);
+                                               const sdt::GemmArgs &, cudaStream_t);               \
+    template int sdt::launch_gemm_tile_split<BM, BN>(const CUtensorMap &, const CUtensorMap &,     \
+                                                     const sdt::GemmArgs &, cudaStream_t);
