@@ -228,6 +228,29 @@ int sdt_pick_splitk_for(int64_t M, int64_t N, int64_t K, int sm_count, int smem_
                         int *tile_id, int *splits);
 
 /*
+ * gemm_f16_splitk_noalloc -- gemm_f16_splitk (SDT_SPLITK_REDUCE_KERNEL) with its
+ * workspace in a fixed 16 MiB array that the library holds in device memory,
+ * so the call allocates nothing.  The pages have no counterpart; this is an
+ * interface for callers that cannot allocate device memory where they
+ * multiply: code that must not synchronise the device (cudaMalloc and
+ * cudaFree can), plugin hosts that give a kernel library a fixed memory
+ * budget and no allocator, latency-critical loops that forbid allocator calls.
+ *
+ * Arguments as gemm_f16_splitk, minus the workspace and the algorithm
+ * (tile_id < 0 picks tile and splits).  Shapes whose partials
+ * (sdt_splitk_workspace_bytes) exceed 16 MiB are rejected with SDT_ERR_ARG
+ * and a message naming the sizes.  The first call on each device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.  Every GPU on which the
+ * library's module holding the array is loaded keeps the 16 MiB until the
+ * process exits.  All calls share the array: nothing in it has to start at
+ * zero (each call overwrites the partials it reads), but calls that overlap
+ * on the GPU race on it and corrupt each other's results.
+ */
+int gemm_f16_splitk_noalloc(int64_t M, int64_t N, int64_t K, const void *A, const void *B, void *C,
+                            int tile_id, int splits, sdt_stream_t stream);
+
+/*
  * Frozen tune table [P3 "Changes": the measured sweep can be frozen into an
  * offline artefact].  Text file, one entry per line: "M N K tile_name
  * [stagger]"; '#' starts a comment.  Loading replaces the current table.

@@ -54,6 +54,7 @@ SIGNATURES = {
     "sdt_splitk_workspace_bytes": (ctypes.c_size_t, [i64, i64, i64, cint, cint]),
     "sdt_splitk_workspace_init": (cint, [vp, ctypes.c_size_t, vp]),
     "sdt_pick_splitk_for": (cint, [i64, i64, i64, cint, cint, ctypes.POINTER(cint), ctypes.POINTER(cint)]),
+    "gemm_f16_splitk_noalloc": (cint, [i64, i64, i64, vp, vp, vp, cint, cint, vp]),
 }
 
 STATUS = {

@@ -650,6 +650,13 @@ static int splitk_run(int64_t M, int64_t N, int64_t K, const void *A, const void
     return SDT_OK;
 }
 
+// Entry for other translation units of the library (the no-allocation variant):
+// the same validation and launches as gemm_f16_splitk on a given workspace.
+int splitk_launch(int64_t M, int64_t N, int64_t K, const void *A, const void *B, void *C, void *ws,
+                  size_t ws_bytes, int tile_id, int splits, int algo, cudaStream_t stream) {
+    return splitk_run(M, N, K, A, B, C, ws, ws_bytes, tile_id, splits, algo, stream);
+}
+
 }  // namespace sdt
 
 using namespace sdt;
