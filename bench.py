@@ -345,12 +345,22 @@ def run_default(args):
     pq = [(DEC_K, DEC_N, x.data_ptr(), q.data_ptr(), s_.data_ptr(), yq.data_ptr(), sp) for q, s_ in zip(Wq, Sq)]
     gemm_c, gemv_b, gemv_q = L.gemm_f16, L.gemv_m1_bf16, L.gemv_m1_q8
 
-    def step(i, ev=None):
+    dom_j = len(SWEEP) - 1  # the 4096^3 launch: largest share of the step
+
+    def step(i, ev=None, dom=None):
+        # ev: events around every launch (instrumented step); dom: events around the
+        # dominant launch only.  Any event between two launches stops the second from
+        # overlapping its set-up with the first (programmatic dependent launch), so
+        # most timed steps carry only the two events around the dominant launch.
         rc = 0
         for j, a in enumerate(gemm_args):
             if ev is not None:
                 ev[j].record(stream)
+            elif dom is not None and j == dom_j:
+                dom[0].record(stream)
             rc |= gemm_c(*a)
+            if ev is None and dom is not None and j == dom_j:
+                dom[1].record(stream)
         if ev is not None:
             ev[len(SWEEP)].record(stream)
         rc |= gemv_b(*pb[i % DEC_BUFFERS])
@@ -383,9 +393,13 @@ def run_default(args):
             print(json.dumps({"metric": METRIC, "error": "correctness gate failed", "gate": gate}))
             sys.exit(3)
 
-    # timed region
+    # timed region: every INSTR-th step is instrumented around every launch
+    INSTR = 10
     nev = launches_per_step + 1
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    inst_idx = [i for i in range(args.steps) if i % INSTR == 0]
+    events = {i: [torch.cuda.Event(enable_timing=True) for _ in range(nev)] for i in inst_idx}
+    dom_events = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for i in range(args.steps) if i not in events}
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
     barrier()
@@ -393,7 +407,7 @@ def run_default(args):
     with ClockSampler(local) as clocks:
         start.record(stream)
         for i in range(args.steps):
-            step(i, events[i])
+            step(i, events.get(i), dom_events.get(i))
         stop.record(stream)
         torch.cuda.synchronize()
         barrier()
@@ -404,11 +418,12 @@ def run_default(args):
     # per-kernel durations from the events inside the timed region
     per = {n: [] for n in SWEEP}
     dec_b, dec_q = [], []
-    for ev in events:
+    for ev in events.values():
         for j, n in enumerate(SWEEP):
             per[n].append(ev[j].elapsed_time(ev[j + 1]))
         dec_b.append(ev[len(SWEEP)].elapsed_time(ev[len(SWEEP) + 1]))
         dec_q.append(ev[len(SWEEP) + 1].elapsed_time(ev[len(SWEEP) + 2]))
+    dom_ms = [e0.elapsed_time(e1) for e0, e1 in dom_events.values()] + per[SWEEP[dom_j]]
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     e2e = run_e2e(args, dev, host, Wb_h, Q_h, stream)
@@ -428,11 +443,11 @@ def run_default(args):
         gbs = decode_bytes(DEC_K, DEC_N, fmt) / (us / 1e6) / 1e9
         dec[name] = {"us": round(us, 2), "us_min": round(min(lst) * 1e3, 2), "us_max": round(max(lst) * 1e3, 2),
                      "gbs": round(gbs, 1), "pct_hbm": round(100 * gbs / peaks["hbm_gbs"], 1)}
-    # dominant kernel: the largest share of the step
+    # dominant kernel: the largest share of the step, timed in every step
     shares = {n: statistics.mean(per[n]) for n in SWEEP}
-    dom = max(shares, key=shares.get)
-    dom_ms = shares[dom]
-    achieved = gemm_flops(dom, dom, dom) / (dom_ms / 1e3) / 1e12
+    dom = SWEEP[dom_j]
+    assert dom == max(shares, key=shares.get)
+    achieved = gemm_flops(dom, dom, dom) / (statistics.mean(dom_ms) / 1e3) / 1e12
     traffic = load_traffic(f"gemm_{dom}")
     clock = clocks.summary()
     out = {
@@ -450,6 +465,8 @@ def run_default(args):
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "l2": "inputs larger than L2 (step working set %.0f MB, L2 129 MB)"
                    % (step_working_set() / 1e6), "parallelism": f"replicas x{world}"},
+        "timing": {"per_size_and_decode": f"instrumented steps (every {INSTR}th, events around every launch)",
+                   "roofline": "events around the 4096^3 launch in every timed step"},
         "roofline": {"bound": "tensor", "kernel": f"gemm_f16 {dom}^3 ({tiles[dom]})",
                      "achieved": round(achieved, 1), "peak": peaks["tflops"], "unit": "TFLOP/s",
                      "frac": round(achieved / peaks["tflops"], 4), "peak_source": peaks["source"] + " bf16 burst",
@@ -825,6 +842,37 @@ def run_splitk(args):
     sdt.check_device_status()
 
 
+def run_chain(args):
+    """Back-to-back launches of one GEMM (or decode GEMV) between two events: the
+    per-launch time a stream of dependent-free launches sees (launch overlap included)."""
+    import torch
+
+    import shape_driven_tile_gb300 as sdt
+
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    out = {}
+    for n in (args.sizes or [256, 512, 768, 1024, 1536, 2048]):
+        A = (torch.rand((n, n), device=dev) * 2 - 1).half()
+        B = (torch.rand((n, n), device=dev) * 2 - 1).half()
+        C = torch.empty((n, n), device=dev, dtype=torch.float16)
+        L = sdt.lib()
+        a = (n, n, n, A.data_ptr(), B.data_ptr(), C.data_ptr(), stream.cuda_stream)
+        for _ in range(10):
+            L.gemm_f16(*a)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = args.reps
+        e0.record(stream)
+        for _ in range(reps):
+            L.gemm_f16(*a)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out[n] = round(e0.elapsed_time(e1) * 1e3 / reps, 2)
+    sdt.check_device_status()
+    print(json.dumps({"mode": "chain", "pdl": os.environ.get("SDT_PDL", "1"), "us_per_launch": out}), flush=True)
+
+
 def run_one(args):
     """A few launches of one kernel (for profiler captures): a square GEMM with pick_tile,
     or the decode GEMV (--gemv bf16|q8)."""
@@ -866,7 +914,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["sdt", "reference"], default="sdt")
-    ap.add_argument("--mode", choices=["step", "sweep", "kscan", "decode", "large", "one", "splitk"], default="step")
+    ap.add_argument("--mode", choices=["step", "sweep", "kscan", "decode", "large", "one", "splitk", "chain"],
+                    default="step")
     ap.add_argument("--gemv", choices=["bf16", "q8"])
     ap.add_argument("--reps", type=int, default=20)
     ap.add_argument("--sizes", type=int, nargs="*")
@@ -881,7 +930,7 @@ def main(argv=None):
     if args.impl == "reference":
         return run_reference(args)
     {"step": run_default, "sweep": run_sweep, "kscan": run_kscan, "decode": run_decode,
-     "large": run_large, "one": run_one, "splitk": run_splitk}[args.mode](args)
+     "large": run_large, "one": run_one, "splitk": run_splitk, "chain": run_chain}[args.mode](args)
 
 
 if __name__ == "__main__":

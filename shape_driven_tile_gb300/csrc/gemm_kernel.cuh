@@ -139,6 +139,8 @@ __global__ void __launch_bounds__(128, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_d = ctrl[0];
+    griddep_launch_dependents();
+    griddep_wait();  // the previous kernel's writes (A, B, C) are visible from here on
 
     const uint64_t t_start = global_timer_ns();
     const uint64_t deadline = t_start + p.timeout_ns;

@@ -9,6 +9,7 @@
 #include "gemm_kernel.cuh"
 #include "gemm_persistent.cuh"
 #include "gemm_pair.cuh"
+#include "launch.cuh"
 
 namespace sdt {
 
@@ -30,8 +31,7 @@ int launch_gemm_tile(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmA
         }
     }
     const unsigned grid = static_cast<unsigned>(args.num_m_tiles) * static_cast<unsigned>(args.num_n_tiles);
-    kern<<<grid, Cfg::THREADS, smem, stream>>>(tmA, tmB, args);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3(grid), dim3(Cfg::THREADS), size_t(smem), stream, 1, tmA, tmB, args);
 }
 
 template <int BM, int BN>
@@ -52,8 +52,7 @@ int launch_gemm_tile_split(const CUtensorMap &tmA, const CUtensorMap &tmB, const
     }
     const dim3 grid(static_cast<unsigned>(args.num_m_tiles) * static_cast<unsigned>(args.num_n_tiles),
                     static_cast<unsigned>(args.splits), 1);
-    kern<<<grid, Cfg::THREADS, smem, stream>>>(tmA, tmB, args);
-    return cudaGetLastError();
+    return launch_kernel(kern, grid, dim3(Cfg::THREADS), size_t(smem), stream, 1, tmA, tmB, args);
 }
 
 template <int BN>
@@ -74,8 +73,7 @@ int launch_gemm_persistent(const CUtensorMap &tmA, const CUtensorMap &tmB, const
     }
     const long long tiles = static_cast<long long>(args.num_m_tiles) * args.num_n_tiles;
     const unsigned grid = static_cast<unsigned>(tiles < args.max_ctas ? tiles : args.max_ctas);
-    kern<<<grid, Cfg::THREADS, smem, stream>>>(tmA, tmB, args);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3(grid), dim3(Cfg::THREADS), size_t(smem), stream, 1, tmA, tmB, args);
 }
 
 template <int BN>
@@ -96,21 +94,7 @@ int launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmA
     const long long tiles = static_cast<long long>(args.num_m_tiles) * args.num_n_tiles;
     const long long pairs_cap = args.max_ctas / 2 > 0 ? args.max_ctas / 2 : 1;
     const unsigned pairs = static_cast<unsigned>(tiles < pairs_cap ? tiles : pairs_cap);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * pairs, 1, 1);
-    cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, args);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3(2 * pairs), dim3(Cfg::THREADS), size_t(smem), stream, 2, tmA, tmB, args);
 }
 
 }  // namespace sdt

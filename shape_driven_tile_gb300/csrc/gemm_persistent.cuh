@@ -111,6 +111,8 @@ __global__ void __launch_bounds__(192, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = ctrl[0];
+    griddep_launch_dependents();
+    griddep_wait();  // the previous kernel's writes (A, B, C) are visible from here on
 
     if (warp == 0) {
         if (lane == 0) {

@@ -32,6 +32,7 @@
 #include <cstring>
 
 #include "host_common.cuh"
+#include "launch.cuh"
 #include "ptx.cuh"
 
 namespace sdt {
@@ -106,6 +107,8 @@ template <int ROWS, int U>
 __global__ void __launch_bounds__(kGemvThreads)
     gemv_bf16_kernel(int K8, int N, const uint4 *__restrict__ x, const uint4 *__restrict__ W,
                      float *__restrict__ y) {
+    griddep_launch_dependents();
+    griddep_wait();  // x and W may come from the previous kernel
     const int lane = threadIdx.x & 31;
     const int gwarp = blockIdx.x * kGemvWarps + (threadIdx.x >> 5);
     const int nwarps = gridDim.x * kGemvWarps;
@@ -147,6 +150,8 @@ template <int ROWS, int U>
 __global__ void __launch_bounds__(kGemvThreads)
     gemv_q8_kernel(int K16, int N, const uint4 *__restrict__ x, const uint4 *__restrict__ W,
                    const __half *__restrict__ scales, float *__restrict__ y) {
+    griddep_launch_dependents();
+    griddep_wait();  // x and W may come from the previous kernel
     const int lane = threadIdx.x & 31;
     const int gwarp = blockIdx.x * kGemvWarps + (threadIdx.x >> 5);
     const int nwarps = gridDim.x * kGemvWarps;
@@ -271,6 +276,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) gemv_stream_kernel(const St
         fence_mbar_init();
     }
     __syncthreads();
+    griddep_launch_dependents();
+    griddep_wait();  // x and W may come from the previous kernel
 
     if (warp == kStreamConsumers) {
         if (lane == 0) {
@@ -437,8 +444,7 @@ static cudaError_t launch_stream(const StreamArgs &a, int grid, int smem, cudaSt
         if (e != cudaSuccess) return e;
         configured[dev].store(smem);
     }
-    kern<<<grid, kStreamThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3(grid), dim3(kStreamThreads), size_t(smem), s, 1, a);
 }
 
 // Streams W through shared memory when a ring of at least two stages fits (with the
@@ -484,31 +490,30 @@ static bool try_stream(bool q8, int H, int64_t K, int64_t N, const void *x, cons
 }
 
 template <int R, int U>
-static void launch_bf16(int K8, int N, const void *x, const void *W, float *y, cudaStream_t s) {
+static cudaError_t launch_bf16(int K8, int N, const void *x, const void *W, float *y, cudaStream_t s) {
     const int rows_per_block = kGemvWarps * R;
     const int blocks = (N + rows_per_block - 1) / rows_per_block;
-    gemv_bf16_kernel<R, U><<<blocks, kGemvThreads, 0, s>>>(K8, N, static_cast<const uint4 *>(x),
-                                                            static_cast<const uint4 *>(W), y);
+    return launch_kernel(gemv_bf16_kernel<R, U>, dim3(blocks), dim3(kGemvThreads), 0, s, 1, K8, N,
+                  static_cast<const uint4 *>(x), static_cast<const uint4 *>(W), y);
 }
 
 template <int R, int U>
-static void launch_q8(int K16, int N, const void *x, const void *W, const void *sc, float *y,
-                      cudaStream_t s) {
+static cudaError_t launch_q8(int K16, int N, const void *x, const void *W, const void *sc, float *y,
+                             cudaStream_t s) {
     const int rows_per_block = kGemvWarps * R;
     const int blocks = (N + rows_per_block - 1) / rows_per_block;
-    gemv_q8_kernel<R, U><<<blocks, kGemvThreads, 0, s>>>(K16, N, static_cast<const uint4 *>(x),
-                                                          static_cast<const uint4 *>(W),
-                                                          static_cast<const __half *>(sc), y);
+    return launch_kernel(gemv_q8_kernel<R, U>, dim3(blocks), dim3(kGemvThreads), 0, s, 1, K16, N,
+                  static_cast<const uint4 *>(x), static_cast<const uint4 *>(W), static_cast<const __half *>(sc), y);
 }
 
-#define SDT_GEMV_DISPATCH(FN, V, ...)                                                              \
+#define SDT_GEMV_DISPATCH(E, FN, V, ...)                                                           \
     do {                                                                                           \
-        if (V.rows == 1 && V.unroll == 4) FN<1, 4>(__VA_ARGS__);                                   \
-        else if (V.rows == 1 && V.unroll == 8) FN<1, 8>(__VA_ARGS__);                              \
-        else if (V.rows == 2 && V.unroll == 2) FN<2, 2>(__VA_ARGS__);                              \
-        else if (V.rows == 4 && V.unroll == 2) FN<4, 2>(__VA_ARGS__);                              \
-        else if (V.rows == 4 && V.unroll == 4) FN<4, 4>(__VA_ARGS__);                              \
-        else FN<2, 4>(__VA_ARGS__);                                                                \
+        if (V.rows == 1 && V.unroll == 4) E = FN<1, 4>(__VA_ARGS__);                               \
+        else if (V.rows == 1 && V.unroll == 8) E = FN<1, 8>(__VA_ARGS__);                          \
+        else if (V.rows == 2 && V.unroll == 2) E = FN<2, 2>(__VA_ARGS__);                          \
+        else if (V.rows == 4 && V.unroll == 2) E = FN<4, 2>(__VA_ARGS__);                          \
+        else if (V.rows == 4 && V.unroll == 4) E = FN<4, 4>(__VA_ARGS__);                          \
+        else E = FN<2, 4>(__VA_ARGS__);                                                            \
     } while (0)
 
 static constexpr int64_t kGemvMaxDim = int64_t(1) << 30;
@@ -542,9 +547,8 @@ static int gemv_impl(int64_t K, int64_t N, const void *x, const void *W, const v
         rc = status_word(&status);
         if (rc) return rc;
         if (!try_stream(q8, v.stream_h, K, N, x, W, scales, y, s, dev, status, &e)) {
-            if (!q8) SDT_GEMV_DISPATCH(launch_bf16, v, int(K / 8), int(N), x, W, y, s);
-            else SDT_GEMV_DISPATCH(launch_q8, v, int(K / 16), int(N), x, W, scales, y, s);
-            e = cudaGetLastError();
+            if (!q8) SDT_GEMV_DISPATCH(e, launch_bf16, v, int(K / 8), int(N), x, W, y, s);
+            else SDT_GEMV_DISPATCH(e, launch_q8, v, int(K / 16), int(N), x, W, scales, y, s);
         }
     }
     if (e != cudaSuccess) return fail(SDT_ERR_LAUNCH, "gemv launch failed: %s", cudaGetErrorString(e));

@@ -23,6 +23,17 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// ---- programmatic dependent launch ---------------------------------------------
+// launch_dependents: this CTA no longer holds back the launch of the next kernel in
+// the stream (its set-up may overlap our run).  wait: block until the previous
+// kernel in the stream has completed and its memory is visible.  Both are no-ops
+// when the kernel was launched without programmatic stream serialisation.
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- mbarrier --------------------------------------------------------------
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
