@@ -143,7 +143,13 @@ static double model_us(const LadderTile &t, int64_t M, int64_t N, int64_t K, int
     const double mb = tiles * nK * double(t.BM + t.BN) * kBK * 2.0 / 1e6;
     if (t.persistent) {
         const double workers = t.cta_group == 2 ? double(sm_count / 2) : double(sm_count);
-        const double ktiles = std::max(0.0, std::ceil(tiles / workers) * nK - t.stages);
+        double rounds = std::ceil(tiles / workers);
+        if (t.cta_group == 2 && t.BN == 256) {
+            // a tail of at most half the workers runs as half-width items in half a round
+            const double tail = tiles - std::floor(tiles / workers) * workers;
+            if (tail > 0 && 2 * tail <= workers) rounds -= 0.5;
+        }
+        const double ktiles = std::max(0.0, rounds * nK - t.stages);
         return t.fixed_us + ktiles * t.kt_us + mb * t.per_mb_us;
     }
     const int occ = ctas_per_sm(t, smem_per_sm);
@@ -405,6 +411,7 @@ static int run_tile(int tile_id, int stagger_req, int64_t M, int64_t N, int64_t 
     if (rc) return rc;
 
     GemmArgs a;
+    memset(&a, 0, sizeof a);
     a.C = static_cast<__half *>(C);
     a.M = int(M);
     a.N = int(N);
@@ -420,8 +427,19 @@ static int run_tile(int tile_id, int stagger_req, int64_t M, int64_t N, int64_t 
     a.timeout_ns = wait_timeout_ns();
     a.status = status;
     a.max_ctas = dev.sm_count * ctas_per_sm(t, dev.smem_per_sm);
-    if (int64_t(a.num_m_tiles) * a.num_n_tiles > int64_t(0x7fffffff))
+    if (int64_t(a.num_m_tiles) * a.num_n_tiles > int64_t(0x3fffffff))
         return fail(SDT_ERR_SHAPE, "grid too large");
+    const int tiles = a.num_m_tiles * a.num_n_tiles;
+    a.tail_start = tiles;
+    a.num_items = tiles;
+    if (t.cta_group == 2 && t.BN == 256 && env_int("SDT_TAIL_SPLIT", 1, 0, 1)) {
+        const int workers = std::max(1, a.max_ctas / 2);
+        const int tail = tiles % workers;
+        if (tail > 0 && 2 * tail <= workers) {
+            a.tail_start = tiles - tail;
+            a.num_items = a.tail_start + 2 * tail;
+        }
+    }
     int e = t.launch(tmA, tmB, a, stream);
     if (e != cudaSuccess) {
         cudaGetLastError();

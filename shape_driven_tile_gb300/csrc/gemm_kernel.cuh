@@ -56,6 +56,10 @@ struct GemmArgs {
     int splitk_reduce_in_kernel;  // 1: the last CTA of a tile sums the partials and writes C
     float *partials;      // [splits][M][N] fp32
     unsigned *counters;   // [num_m_tiles * num_n_tiles], zero between calls
+    // two-CTA tiles: work items [0, tail_start) are whole tiles, items
+    // [tail_start, num_items) are column halves of tiles tail_start ... (two per tile)
+    int tail_start;
+    int num_items;
 };
 
 template <int BM, int BN>

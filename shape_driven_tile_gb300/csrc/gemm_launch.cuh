@@ -91,9 +91,9 @@ int launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmA
         while (prev < smem && !configured[dev].compare_exchange_weak(prev, smem)) {
         }
     }
-    const long long tiles = static_cast<long long>(args.num_m_tiles) * args.num_n_tiles;
+    const long long items = args.num_items;
     const long long pairs_cap = args.max_ctas / 2 > 0 ? args.max_ctas / 2 : 1;
-    const unsigned pairs = static_cast<unsigned>(tiles < pairs_cap ? tiles : pairs_cap);
+    const unsigned pairs = static_cast<unsigned>(items < pairs_cap ? items : pairs_cap);
     return launch_kernel(kern, dim3(2 * pairs), dim3(Cfg::THREADS), size_t(smem), stream, 2, tmA, tmB, args);
 }
 

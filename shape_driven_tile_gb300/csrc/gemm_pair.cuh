@@ -48,6 +48,25 @@ struct PairCfg {
     static_assert(TMEM_COLS <= 512, "two accumulators must fit in TMEM");
 };
 
+// Work item -> output tile, column offset and width.  When the last round of whole
+// tiles would leave at least half of the pairs idle, the host makes each of those
+// tail tiles two half-width items instead, so the tail takes half a round.
+template <int BN>
+__device__ __forceinline__ void pair_item(int item, const GemmArgs &p, int &tile, int &m_tile, int &n_tile,
+                                          int &n_off, int &width) {
+    if (item < p.tail_start) {
+        tile = item;
+        n_off = 0;
+        width = BN;
+    } else {
+        const int h = item - p.tail_start;
+        tile = p.tail_start + (h >> 1);
+        n_off = (h & 1) * (BN / 2);
+        width = BN / 2;
+    }
+    tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.raster_group, m_tile, n_tile);
+}
+
 template <int BN>
 __global__ void __launch_bounds__(192, 1)
     gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -74,7 +93,7 @@ __global__ void __launch_bounds__(192, 1)
     const bool leader = rank == 0;
     const int pair = static_cast<int>(blockIdx.x >> 1);
     const int num_pairs = static_cast<int>(gridDim.x >> 1);
-    const int num_tiles = p.num_m_tiles * p.num_n_tiles;  // pair tiles (256 rows each)
+    const int num_items = p.num_items;  // whole tiles (256 rows each) and tail halves
     const int nK = p.num_k_tiles;
     const uint64_t lim = p.timeout_ns;
 
@@ -112,11 +131,13 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t phase = 0;
             int issued = 0;
             bool stop = false;
-            for (int tile = pair; tile < num_tiles && !stop; tile += num_pairs) {
-                int m_tile, n_tile;
-                tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.raster_group, m_tile, n_tile);
+            for (int item = pair; item < num_items && !stop; item += num_pairs) {
+                int tile, m_tile, n_tile, n_off, width;
+                pair_item<BN>(item, p, tile, m_tile, n_tile, n_off, width);
                 const int m0 = m_tile * Cfg::BM + static_cast<int>(rank) * Cfg::CTA_M;
-                const int nb = n_tile * BN + static_cast<int>(rank) * Cfg::B_HALF;
+                const int nb = n_tile * BN + n_off + static_cast<int>(rank) * (width / 2);
+                const int boxes = width / 128;  // 64-column B boxes per CTA
+                const uint32_t pair_bytes = 2u * static_cast<uint32_t>(Cfg::A_BYTES + boxes * Cfg::B_BOX_BYTES);
                 const int start =
                     p.stagger ? static_cast<int>((static_cast<uint32_t>(tile) * static_cast<uint32_t>(p.stagger_stride)) &
                                                  static_cast<uint32_t>(nK - 1))
@@ -131,11 +152,10 @@ __global__ void __launch_bounds__(192, 1)
                     if (ctrl[1]) { stop = true; break; }
                     const int kt = p.stagger ? ((start + i) & (nK - 1)) : i;
                     const uint32_t fb_local = smem_u32(&full[s]);
-                    if (leader) mbar_arrive_expect_tx(fb_local, 2 * Cfg::STAGE_BYTES);
+                    if (leader) mbar_arrive_expect_tx(fb_local, pair_bytes);
                     const uint32_t fb = mapa_shared(fb_local, 0);
                     tma_load_2d_pair(smem_u32(smA + s * Cfg::A_BYTES), &tmA, fb, kt * kBK, m0);
-#pragma unroll
-                    for (int c = 0; c < Cfg::B_HALF / 64; ++c)
+                    for (int c = 0; c < boxes; ++c)
                         tma_load_2d_pair(smem_u32(smB + s * Cfg::B_BYTES + c * Cfg::B_BOX_BYTES), &tmB, fb,
                                          nb + c * 64, kt * kBK);
                     ctrl[2] = ++issued;
@@ -146,12 +166,14 @@ __global__ void __launch_bounds__(192, 1)
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             // ---------------- MMA issuer (leader only) ----------------
-            constexpr uint32_t idesc = idesc_f16_f32(Cfg::BM, BN);
+            constexpr uint32_t idesc_full = idesc_f16_f32(Cfg::BM, BN);
+            constexpr uint32_t idesc_half = idesc_f16_f32(Cfg::BM, BN / 2);
             int s = 0;
             uint32_t phase = 0;
             int j = 0;
             bool stop = false;
-            for (int tile = pair; tile < num_tiles && !stop; tile += num_pairs, ++j) {
+            for (int item = pair; item < num_items && !stop; item += num_pairs, ++j) {
+                const uint32_t idesc = item < p.tail_start ? idesc_full : idesc_half;
                 const int b = j & 1;
                 const uint32_t acc_phase = static_cast<uint32_t>((j >> 1) & 1);
                 if (!mbar_wait_cluster_for(smem_u32(&acc_empty[b]), acc_phase ^ 1u, lim)) {
@@ -188,7 +210,7 @@ __global__ void __launch_bounds__(192, 1)
         // ---------------- epilogue warps (both CTAs) ----------------
         const int q = warp & 3;
         int j = 0;
-        for (int tile = pair; tile < num_tiles; tile += num_pairs, ++j) {
+        for (int item = pair; item < num_items; item += num_pairs, ++j) {
             const int b = j & 1;
             const uint32_t acc_phase = static_cast<uint32_t>((j >> 1) & 1);
             if (!warp_wait(smem_u32(&acc_full[b]), acc_phase, 4 * lim, lane)) {
@@ -199,18 +221,18 @@ __global__ void __launch_bounds__(192, 1)
                 break;
             }
             tc_fence_after();
-            int m_tile, n_tile;
-            tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.raster_group, m_tile, n_tile);
+            int tile, m_tile, n_tile, n_off, width;
+            pair_item<BN>(item, p, tile, m_tile, n_tile, n_off, width);
             const int row = m_tile * Cfg::BM + static_cast<int>(rank) * Cfg::CTA_M + q * 32 + lane;
-            __half *crow = p.C + static_cast<size_t>(row) * p.N + n_tile * BN;
+            __half *crow = p.C + static_cast<size_t>(row) * p.N + n_tile * BN + n_off;
             const uint32_t taddr =
                 tmem_base + static_cast<uint32_t>(b * BN) + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
+            for (int c = 0; c < width; c += 32) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(taddr + c, r);
                 tmem_ld_wait();
-                if (c == BN - 32) {
+                if (c == width - 32) {
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[b]), 0));
