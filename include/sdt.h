@@ -180,6 +180,35 @@ int gemm_f16_with_tile(int64_t M, int64_t N, int64_t K,
                        int tile_id, int stagger);
 
 /*
+ * gemm_ex -- the general form: caller row strides, transposed operands, bf16,
+ * and shapes no tile divides [P3 "Changes": the row strides are taken from the
+ * caller's tensors; the measured layouts are TN and NN; P3 "Performance" runs
+ * bf16].  C[M][N] (row stride ldc) = op(A) . op(B) with fp32 accumulation:
+ *   op(A): layout without SDT_LAYOUT_A_T: A is M x K row-major (lda >= K);
+ *          with it, A is stored K x M (lda >= M), i.e. A^T is given.
+ *   op(B): without SDT_LAYOUT_B_T: B is K x N row-major (ldb >= N);
+ *          with it, B is stored N x K (ldb >= K), i.e. B^T is given ("TN" is
+ *          SDT_LAYOUT_B_T: C = A . (B^T)^T).
+ *   dtype: SDT_DTYPE_F16 or SDT_DTYPE_BF16 for A, B and C alike.
+ * Any M, K >= 0; N a multiple of 8; lda, ldb, ldc multiples of 8 (16-byte
+ * rows) at least the row lengths above; pointers 16-byte aligned.  Tiles
+ * overhang ragged edges: the TMA reads zeros outside the operands and the
+ * epilogue writes only inside C.  tile_id -1 picks with sdt_pick_tile_any_for's
+ * model; a forced tile needs only to fit on chip.  The k-loop stagger follows
+ * SDT_STAGGER as in gemm_f16.  Errors: SDT_ERR_SHAPE (N % 8, dims > 2^30),
+ * SDT_ERR_ARG (strides, dtype, layout), SDT_ERR_ALIGN, SDT_ERR_NULL,
+ * SDT_ERR_TILE.
+ */
+#define SDT_DTYPE_F16 0
+#define SDT_DTYPE_BF16 1
+#define SDT_LAYOUT_A_T 1
+#define SDT_LAYOUT_B_T 2
+int gemm_ex(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
+            void *C, int64_t ldc, int dtype, int layout, int tile_id, sdt_stream_t stream);
+/* pick_tile's cost model over every tile for any shape (tiles may overhang); needs no GPU. */
+int sdt_pick_tile_any_for(int64_t M, int64_t N, int64_t K, int sm_count, int smem_limit);
+
+/*
  * Split-K [P4 "The Six Rounds", round 2 "Split-K": the contraction is split
  * across CTAs and the partial results are reduced; the page distinguishes a
  * reduction in a separate pass from one inside the single kernel].

@@ -14,7 +14,7 @@ Every entry cites the passage it follows in ``oracle.c``.  Summary:
   ("Beating hipBLASLt on a Gaming GPU", section "The result").
 * ``gemv_bf16(x, W)``, ``gemv_q8(x, q, s)`` -- the M=1 decode products of
   "mojo-baro", section "Four rounds on the decode shape" (rounds v1/v2).
-* ``f16_to_f64``, ``bf16_to_f64``, ``f64_to_f16`` -- format conversions from
+* ``f16_to_f64``, ``bf16_to_f64``, ``f64_to_f16``, ``f64_to_bf16`` -- format conversions from
   the IEEE 754 binary16 / bfloat16 definitions.
 * ``tiles`` submodule -- the tile-feasibility rules and the block-count tile
   rule of the pages, as plain integer functions.
@@ -51,6 +51,9 @@ def _bind(lib):
     i64, p = ctypes.c_int64, ctypes.c_void_p
     lib.sdt_oracle_gemm_rows.argtypes = [i64, i64, i64, p, p, p, i64, p, ctypes.c_int]
     lib.sdt_oracle_gemm_rows.restype = ctypes.c_int
+    lib.sdt_oracle_gemm_rows_t.argtypes = [i64, i64, i64, p, p, p, i64, p, ctypes.c_int, ctypes.c_int]
+    lib.sdt_oracle_gemm_rows_t.restype = ctypes.c_int
+    lib.sdt_oracle_f64_array_to_bf16.argtypes = [p, p, i64]
     lib.sdt_oracle_gemv_bf16.argtypes = [i64, i64, p, p, p, ctypes.c_int]
     lib.sdt_oracle_gemv_bf16.restype = ctypes.c_int
     lib.sdt_oracle_gemv_q8.argtypes = [i64, i64, p, p, p, p, ctypes.c_int]
@@ -96,8 +99,8 @@ def max_threads() -> int:
     return int(_load().sdt_oracle_max_threads())
 
 
-def gemm(A, B, rows=None, threads: int = 0) -> np.ndarray:
-    """fp64 C (or the selected rows of C) for fp16 bit patterns A [M,K], B [K,N]."""
+def gemm(A, B, rows=None, threads: int = 0, dtype: str = "f16") -> np.ndarray:
+    """fp64 C (or the selected rows of C) for 16-bit patterns A [M,K], B [K,N] (dtype f16 or bf16)."""
     A, B = _u16(A), _u16(B)
     M, K = A.shape
     K2, N = B.shape
@@ -110,9 +113,11 @@ def gemm(A, B, rows=None, threads: int = 0) -> np.ndarray:
         r = np.ascontiguousarray(rows, dtype=np.int64)
         n_rows = r.size
     C = np.empty((n_rows, N), dtype=np.float64)
-    rc = _load().sdt_oracle_gemm_rows(M, N, K, _ptr(A), _ptr(B),
-                                      None if r is None else _ptr(r), n_rows,
-                                      _ptr(C), threads)
+    if dtype not in ("f16", "bf16"):
+        raise ValueError("dtype must be f16 or bf16")
+    rc = _load().sdt_oracle_gemm_rows_t(M, N, K, _ptr(A), _ptr(B),
+                                        None if r is None else _ptr(r), n_rows,
+                                        _ptr(C), threads, 1 if dtype == "bf16" else 0)
     if rc != 0:
         raise ValueError("oracle gemm rejected its arguments")
     return C
@@ -156,6 +161,14 @@ def bf16_to_f64(h) -> np.ndarray:
     h = _u16(h)
     out = np.empty(h.shape, dtype=np.float64)
     _load().sdt_oracle_bf16_array_to_f64(_ptr(h), _ptr(out), h.size)
+    return out
+
+
+def f64_to_bf16(x) -> np.ndarray:
+    """Round fp64 values to bfloat16 bit patterns, nearest, ties to even."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(x.shape, dtype=np.uint16)
+    _load().sdt_oracle_f64_array_to_bf16(_ptr(x), _ptr(out), x.size)
     return out
 
 

@@ -27,10 +27,14 @@
  *      (row, group), stored [N][K/32].  The group sum is formed first and then
  *      scaled, which is the order the description reads in.
  *
- *  - fp16 and bf16 decoding and an fp64 -> fp16 round-to-nearest-even
- *    encoder, written from the IEEE 754 binary16 definition; they are used to
- *    compare against the GPU's fp16 output bit for bit on integer-valued
- *    inputs.
+ *  - The same GEMM on bfloat16 operands (the FlyDSL pull request "Speed up
+ *    the RDNA3 GEMM up to 1.85x by choosing the tile from the shape",
+ *    section "Performance", measures bf16).
+ *
+ *  - fp16 and bf16 decoding and fp64 -> fp16 / bf16 round-to-nearest-even
+ *    encoders, written from the IEEE 754 binary16 and the bfloat16
+ *    definitions; they are used to compare against the GPU's 16-bit output bit
+ *    for bit on integer-valued inputs.
  *
  * Build: plain C99 with OpenMP across output rows (which does not change the
  * order of any single output's sum).  Compile with -ffp-contract=off so that
@@ -95,6 +99,34 @@ uint16_t sdt_oracle_f64_to_f16(double x)
     return (uint16_t)(sign | (uint16_t)((E + 15) << 10) | (uint16_t)((int)q - 1024));
 }
 
+/* Round an fp64 value to the nearest bfloat16 (8 significant bits, binary32
+ * exponent range), ties to even.  Written from the format's definition: the
+ * significand is rounded to 8 bits at the value's binary exponent; below the
+ * smallest normal (2^-126) the quantum is fixed at 2^-133. */
+uint16_t sdt_oracle_f64_to_bf16(double x)
+{
+    uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    double a = fabs(x);
+    if (isnan(x)) return 0x7fc0u;
+    if (isinf(x)) return (uint16_t)(sign | 0x7f80u);
+    if (a < ldexp(1.0, -126)) {
+        double q = nearbyint(ldexp(a, 133));      /* subnormal quantum 2^-133 */
+        return (uint16_t)(sign | (uint16_t)q);    /* q == 128 is the smallest normal */
+    }
+    int e2;
+    frexp(a, &e2);
+    int E = e2 - 1;                               /* a in [2^E, 2^(E+1)) */
+    double q = nearbyint(ldexp(a, 7 - E));        /* significand in [128, 256] */
+    if (q == 256.0) { q = 128.0; E += 1; }
+    if (E > 127) return (uint16_t)(sign | 0x7f80u);
+    return (uint16_t)(sign | (uint16_t)((E + 127) << 7) | (uint16_t)((int)q - 128));
+}
+
+void sdt_oracle_f64_array_to_bf16(const double *x, uint16_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = sdt_oracle_f64_to_bf16(x[i]);
+}
+
 void sdt_oracle_f16_array_to_f64(const uint16_t *h, double *out, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i) out[i] = sdt_oracle_f16_to_f64(h[i]);
@@ -119,17 +151,23 @@ void sdt_oracle_f64_array_to_f16(const double *x, uint16_t *out, int64_t n)
  * threads <= 0 uses the OpenMP default.  Returns 0, or -1 on bad arguments or
  * allocation failure.
  */
-int sdt_oracle_gemm_rows(int64_t M, int64_t N, int64_t K,
-                         const uint16_t *A, const uint16_t *B,
-                         const int64_t *rows, int64_t n_rows,
-                         double *C, int threads)
+/* dtype 0: A and B hold IEEE binary16 patterns; dtype 1: bfloat16 patterns. */
+static double sdt_oracle_decode(uint16_t v, int dtype)
 {
-    if (M < 0 || N < 0 || K < 0 || n_rows < 0) return -1;
+    return dtype ? sdt_oracle_bf16_to_f64(v) : sdt_oracle_f16_to_f64(v);
+}
+
+int sdt_oracle_gemm_rows_t(int64_t M, int64_t N, int64_t K,
+                           const uint16_t *A, const uint16_t *B,
+                           const int64_t *rows, int64_t n_rows,
+                           double *C, int threads, int dtype)
+{
+    if (M < 0 || N < 0 || K < 0 || n_rows < 0 || (dtype != 0 && dtype != 1)) return -1;
     if (n_rows == 0 || N == 0) return 0;
     if (!A || !B || !C) return -1;
     double *Bd = (double *)malloc((size_t)(K * N > 0 ? K * N : 1) * sizeof(double));
     if (!Bd) return -1;
-    for (int64_t t = 0; t < K * N; ++t) Bd[t] = sdt_oracle_f16_to_f64(B[t]);
+    for (int64_t t = 0; t < K * N; ++t) Bd[t] = sdt_oracle_decode(B[t], dtype);
     int bad = 0;
 #ifdef _OPENMP
     if (threads > 0) omp_set_num_threads(threads);
@@ -141,13 +179,21 @@ int sdt_oracle_gemm_rows(int64_t M, int64_t N, int64_t K,
         double *acc = C + r * N;
         for (int64_t j = 0; j < N; ++j) acc[j] = 0.0;
         for (int64_t k = 0; k < K; ++k) {
-            double a = sdt_oracle_f16_to_f64(A[i * K + k]);
+            double a = sdt_oracle_decode(A[i * K + k], dtype);
             const double *brow = Bd + k * N;
             for (int64_t j = 0; j < N; ++j) acc[j] += a * brow[j];
         }
     }
     free(Bd);
     return bad ? -1 : 0;
+}
+
+int sdt_oracle_gemm_rows(int64_t M, int64_t N, int64_t K,
+                         const uint16_t *A, const uint16_t *B,
+                         const int64_t *rows, int64_t n_rows,
+                         double *C, int threads)
+{
+    return sdt_oracle_gemm_rows_t(M, N, K, A, B, rows, n_rows, C, threads, 0);
 }
 
 int sdt_oracle_gemm(int64_t M, int64_t N, int64_t K,

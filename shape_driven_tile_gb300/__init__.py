@@ -18,7 +18,7 @@ __all__ = [
     "feasible_tiles", "pick_tile", "seed_tile", "tile_info", "tiles", "tile_id",
     "load_tune_table", "clear_tune_table", "tune_table_lookup", "check_device_status",
     "debug_timeout_probe", "device_sm_count", "lib", "gemm_f16_splitk", "splitk_workspace",
-    "splitk_workspace_bytes", "pick_splitk", "SPLITK_REDUCE_KERNEL", "SPLITK_IN_KERNEL",
+    "splitk_workspace_bytes", "pick_splitk", "SPLITK_REDUCE_KERNEL", "SPLITK_IN_KERNEL", "gemm_ex",
 ]
 
 
@@ -113,6 +113,49 @@ def gemv_m1(x, W, scales=None, y=None, *, stream=None):
     if scales is None:
         return gemv_m1_bf16(x, W, y, stream=stream)
     return gemv_m1_q8(x, W, scales, y, stream=stream)
+
+
+DTYPE_CODES = {torch.float16: 0, torch.bfloat16: 1}
+LAYOUT_A_T, LAYOUT_B_T = 1, 2
+
+
+def _layout_of(T, name):
+    """(stored transposed?, leading dimension) of a 2-D view: row-major or a transposed row-major view."""
+    if T.dim() != 2:
+        raise ValueError(f"{name} must be 2-D")
+    r, c = T.shape
+    s0, s1 = T.stride()
+    up8 = lambda v: (max(v, 1) + 7) // 8 * 8  # a single stored row never steps: any legal stride works
+    if s1 == 1 or c == 1:
+        return False, (s0 if r > 1 else up8(max(s0, c)))
+    if s0 == 1 or r == 1:
+        return True, (s1 if c > 1 else up8(max(s1, r)))
+    raise ValueError(f"{name} needs unit stride in one dimension (row-major or transposed row-major)")
+
+
+def gemm_ex(A, B, C=None, *, tile=-1, stream=None):
+    """C = A @ B for fp16 or bf16 views of any shape: A [M, K] and B [K, N] may be row-major
+    (padded rows allowed) or transposed views (e.g. X.t()); C [M, N] row-major, padding allowed."""
+    if A.dtype not in DTYPE_CODES or B.dtype != A.dtype:
+        raise TypeError("A and B must both be float16 or both bfloat16")
+    if not (A.is_cuda and B.is_cuda):
+        raise ValueError("A and B must be CUDA tensors")
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: {tuple(A.shape)} @ {tuple(B.shape)}")
+    a_t, lda = _layout_of(A, "A")
+    b_t, ldb = _layout_of(B, "B")
+    if C is None:
+        C = torch.empty((M, N), dtype=A.dtype, device=A.device)
+    elif C.dtype != A.dtype or tuple(C.shape) != (M, N) or (C.stride(1) != 1 and N > 1):
+        raise ValueError(f"C must be a row-major {A.dtype} [{M}, {N}] view")
+    ldc = C.stride(0) if M > 1 else max(C.stride(0), N)
+    tid = tile_id(tile) if isinstance(tile, str) else int(tile)
+    layout = (LAYOUT_A_T if a_t else 0) | (LAYOUT_B_T if b_t else 0)
+    check(lib().gemm_ex(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, C.data_ptr(), ldc, DTYPE_CODES[A.dtype],
+                        layout, tid, _stream(stream)))
+    return C
 
 
 SPLITK_REDUCE_KERNEL = 0

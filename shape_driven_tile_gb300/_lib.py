@@ -55,6 +55,8 @@ SIGNATURES = {
     "sdt_splitk_workspace_init": (cint, [vp, ctypes.c_size_t, vp]),
     "sdt_pick_splitk_for": (cint, [i64, i64, i64, cint, cint, ctypes.POINTER(cint), ctypes.POINTER(cint)]),
     "gemm_f16_splitk_noalloc": (cint, [i64, i64, i64, vp, vp, vp, cint, cint, vp]),
+    "gemm_ex": (cint, [i64, i64, i64, vp, i64, vp, i64, vp, i64, cint, cint, cint, vp]),
+    "sdt_pick_tile_any_for": (cint, [i64, i64, i64, cint, cint]),
 }
 
 STATUS = {

@@ -43,7 +43,7 @@ static const LaunchFn kSplitLaunch[] = {
 struct LadderTile {
     int BM, BN, cta_group, stages;
     const char *name;
-    LaunchFn launch;
+    LaunchFn launch[4];  // per operand layout (bit 0: A transposed, bit 1: B transposed)
     int smem_per_stage;
     int smem_fixed;
     int tmem_cols;
@@ -62,23 +62,25 @@ struct LadderTile {
     bool candidate;   // considered by pick_tile (tiles dominated everywhere in the sweep are not)
 };
 
+#define SDT_LAUNCH4_(FN, ...) {&FN<__VA_ARGS__, 0>, &FN<__VA_ARGS__, 1>, &FN<__VA_ARGS__, 2>, &FN<__VA_ARGS__, 3>}
+
 #define SDT_TILE(BM_, BN_, STAGES_, NAME_, FIX_, KT_, MB_, CAND_)                                  \
     LadderTile {                                                                                   \
-        BM_, BN_, 1, STAGES_, NAME_, &launch_gemm_tile<BM_, BN_>, TileCfg<BM_, BN_>::STAGE_BYTES,  \
-            TileCfg<BM_, BN_>::ALIGN_SLACK + TileCfg<BM_, BN_>::CTRL_BYTES,                        \
+        BM_, BN_, 1, STAGES_, NAME_, SDT_LAUNCH4_(launch_gemm_tile, BM_, BN_),                     \
+            TileCfg<BM_, BN_>::STAGE_BYTES, TileCfg<BM_, BN_>::ALIGN_SLACK + TileCfg<BM_, BN_>::CTRL_BYTES, \
             TileCfg<BM_, BN_>::TMEM_COLS, TileCfg<BM_, BN_>::THREADS, false, FIX_, KT_, MB_, CAND_ \
     }
 
 #define SDT_PTILE(BN_, STAGES_, NAME_, FIX_, KT_, MB_, CAND_)                                       \
     LadderTile {                                                                                   \
-        128, BN_, 1, STAGES_, NAME_, &launch_gemm_persistent<BN_>, PersistentCfg<BN_>::STAGE_BYTES, \
-            PersistentCfg<BN_>::ALIGN_SLACK + PersistentCfg<BN_>::CTRL_BYTES,                      \
+        128, BN_, 1, STAGES_, NAME_, SDT_LAUNCH4_(launch_gemm_persistent, BN_),                    \
+            PersistentCfg<BN_>::STAGE_BYTES, PersistentCfg<BN_>::ALIGN_SLACK + PersistentCfg<BN_>::CTRL_BYTES, \
             PersistentCfg<BN_>::TMEM_COLS, PersistentCfg<BN_>::THREADS, true, FIX_, KT_, MB_, CAND_ \
     }
 
 #define SDT_PAIR(BN_, STAGES_, NAME_, FIX_, KT_, MB_, CAND_)                                        \
     LadderTile {                                                                                   \
-        256, BN_, 2, STAGES_, NAME_, &launch_gemm_pair<BN_>, PairCfg<BN_>::STAGE_BYTES,            \
+        256, BN_, 2, STAGES_, NAME_, SDT_LAUNCH4_(launch_gemm_pair, BN_), PairCfg<BN_>::STAGE_BYTES, \
             PairCfg<BN_>::ALIGN_SLACK + PairCfg<BN_>::CTRL_BYTES, PairCfg<BN_>::TMEM_COLS,         \
             PairCfg<BN_>::THREADS, true, FIX_, KT_, MB_, CAND_                                     \
     }
@@ -138,8 +140,8 @@ static int ctas_per_sm(const LadderTile &t, int smem_per_sm) {
 // fixed cost once.  Other tiles: whole waves of CTAs, fixed cost per round of
 // co-resident CTAs.  Both pay for the operand bytes the grid streams from L2.
 static double model_us(const LadderTile &t, int64_t M, int64_t N, int64_t K, int sm_count, int smem_per_sm) {
-    const double tiles = double(M / t.BM) * double(N / t.BN);
-    const double nK = double(K / kBK);
+    const double tiles = double((M + t.BM - 1) / t.BM) * double((N + t.BN - 1) / t.BN);
+    const double nK = double((K + kBK - 1) / kBK);
     const double mb = tiles * nK * double(t.BM + t.BN) * kBK * 2.0 / 1e6;
     if (t.persistent) {
         const double workers = t.cta_group == 2 ? double(sm_count / 2) : double(sm_count);
@@ -171,6 +173,25 @@ static int pick_for(int64_t M, int64_t N, int64_t K, int sm_count, int smem_limi
         }
     }
     return best >= 0 ? best : fallback;
+}
+
+// Tiles usable on any shape (they overhang ragged edges): only the on-chip limits apply.
+static bool fits_chip(const LadderTile &t, int smem_limit) {
+    return tile_smem(t, t.stages) <= smem_limit && t.tmem_cols <= 512;
+}
+
+static int pick_any(int64_t M, int64_t N, int64_t K, int sm_count, int smem_limit, int smem_per_sm) {
+    int best = -1;
+    double best_cost = 0.0;
+    for (int i = 0; i < kNumTiles; ++i) {
+        if (!kLadder[i].candidate || !fits_chip(kLadder[i], smem_limit)) continue;
+        const double c = model_us(kLadder[i], M, N, K, sm_count, smem_per_sm);
+        if (best < 0 || c < best_cost * (1.0 - 1e-9)) {
+            best = i;
+            best_cost = c;
+        }
+    }
+    return best;
 }
 
 static int find_tile(const char *name) {
@@ -277,32 +298,35 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// Cache key of one 2-D fp16 tensor map.  The row stride is part of the key: two
+// Cache key of one 2-D tensor map.  The row stride is part of the key: two
 // operands of one shape but different pitch must never share a map.  The same
 // function builds the key for the lookup and for the insert.
 struct MapKey {
     uintptr_t ptr;
     uint64_t inner, outer, row_stride_bytes;
-    uint32_t box_inner, box_outer;
+    int dtype, box_outer;
     bool operator<(const MapKey &o) const {
-        return std::tie(ptr, inner, outer, row_stride_bytes, box_inner, box_outer) <
-               std::tie(o.ptr, o.inner, o.outer, o.row_stride_bytes, o.box_inner, o.box_outer);
+        return std::tie(ptr, inner, outer, row_stride_bytes, dtype, box_outer) <
+               std::tie(o.ptr, o.inner, o.outer, o.row_stride_bytes, o.dtype, o.box_outer);
     }
 };
 
-static MapKey map_key(const void *ptr, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
-                      uint32_t box_inner, uint32_t box_outer) {
-    return MapKey{reinterpret_cast<uintptr_t>(ptr), inner, outer, row_stride_bytes, box_inner, box_outer};
+static MapKey map_key(const void *ptr, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes, int dtype,
+                      int box_outer) {
+    return MapKey{reinterpret_cast<uintptr_t>(ptr), inner, outer, row_stride_bytes, dtype, box_outer};
 }
 
 static std::mutex g_map_mu;
 static std::map<MapKey, CUtensorMap> g_maps;
 static uint64_t g_map_encodes = 0;
 
-// 2-D fp16 tensor map, 128-byte swizzle, inner dimension contiguous.
-static int tensor_map_f16(const void *ptr, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
-                          uint32_t box_inner, uint32_t box_outer, CUtensorMap *out) {
-    const MapKey key = map_key(ptr, inner, outer, row_stride_bytes, box_inner, box_outer);
+// 2-D 16-bit tensor map (fp16 or bf16) with a box of 64 contiguous elements by
+// `box_outer` rows and 128-byte swizzle; `inner` is the contiguous dimension.
+// Elements outside [0, inner) x [0, outer) read as zero, which is what lets tiles
+// overhang ragged edges.
+static int tensor_map_2d(const void *ptr, int dtype, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                         int box_outer, CUtensorMap *out) {
+    const MapKey key = map_key(ptr, inner, outer, row_stride_bytes, dtype, box_outer);
     {
         std::lock_guard<std::mutex> lock(g_map_mu);
         auto it = g_maps.find(key);
@@ -316,11 +340,12 @@ static int tensor_map_f16(const void *ptr, uint64_t inner, uint64_t outer, uint6
     CUtensorMap m;
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {row_stride_bytes};
-    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t box[2] = {64, cuuint32_t(box_outer)};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const CUtensorMapDataType dt =
+        dtype == SDT_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUresult r = fn(&m, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(SDT_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", int(r));
     std::lock_guard<std::mutex> lock(g_map_mu);
     if (g_maps.size() >= 4096) g_maps.clear();
@@ -330,7 +355,28 @@ static int tensor_map_f16(const void *ptr, uint64_t inner, uint64_t outer, uint6
     return SDT_OK;
 }
 
-static_assert(sizeof(kSplitLaunch) / sizeof(kSplitLaunch[0]) == kNumTiles, "one split entry per ladder tile");
+// Operand maps for the layouts: A is M x K (K contiguous) or, transposed, K x M;
+// B is K x N (N contiguous) or, transposed, N x K.  A row-major A tile is one box
+// of a_rows (the rows one CTA stages) x 64; every other operand tile is loaded as
+// 64 x 64 boxes.
+static int operand_maps(const void *A, int64_t lda, const void *B, int64_t ldb, int64_t M, int64_t N, int64_t K,
+                        int dtype, int layout, int a_rows, CUtensorMap *tmA, CUtensorMap *tmB) {
+    const bool a_t = layout & SDT_LAYOUT_A_T, b_t = layout & SDT_LAYOUT_B_T;
+    int rc = a_t ? tensor_map_2d(A, dtype, uint64_t(M), uint64_t(K), uint64_t(lda) * 2, 64, tmA)
+                 : tensor_map_2d(A, dtype, uint64_t(K), uint64_t(M), uint64_t(lda) * 2, a_rows, tmA);
+    if (rc) return rc;
+    return b_t ? tensor_map_2d(B, dtype, uint64_t(K), uint64_t(N), uint64_t(ldb) * 2, 64, tmB)
+               : tensor_map_2d(B, dtype, uint64_t(N), uint64_t(K), uint64_t(ldb) * 2, 64, tmB);
+}
+
+// Instruction-descriptor bits for the types and majors: fp32 accumulator (bit 4),
+// A/B type f16 = 0 / bf16 = 1 (bits 7 and 10), A MN-major (bit 15), B MN-major (bit 16).
+static uint32_t idesc_flags_for(int dtype, int layout) {
+    const uint32_t dt = dtype == SDT_DTYPE_BF16 ? 1u : 0u;
+    const uint32_t a_mn = (layout & SDT_LAYOUT_A_T) ? 1u : 0u;
+    const uint32_t b_mn = (layout & SDT_LAYOUT_B_T) ? 0u : 1u;
+    return (1u << 4) | (dt << 7) | (dt << 10) | (a_mn << 15) | (b_mn << 16);
+}
 
 // ---- launch ----------------------------------------------------------------------
 
@@ -357,6 +403,13 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ partials, __half 
 __global__ void zero_fill_u32(unsigned *p, size_t n) {
     for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += size_t(gridDim.x) * blockDim.x)
         p[i] = 0u;
+}
+
+// C[r][0..N) = 0 for r < M with row stride ldc (N, ldc multiples of 8).
+__global__ void zero_fill_2d(uint16_t *C, int64_t M, int64_t N, int64_t ldc) {
+    const int64_t vecs = N / 8, total = M * vecs;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x)
+        *reinterpret_cast<uint4 *>(C + (i / vecs) * ldc + (i % vecs) * 8) = make_uint4(0, 0, 0, 0);
 }
 
 __global__ void zero_fill_f16(__half *C, size_t n) {
@@ -391,20 +444,14 @@ static int validate_common(int64_t M, int64_t N, int64_t K, const void *A, const
     return SDT_OK;
 }
 
-// Runs the forced tile; assumes arguments are validated and the shape is non-empty with K > 0.
-static int run_tile(int tile_id, int stagger_req, int64_t M, int64_t N, int64_t K, const void *A,
-                    const void *B, void *C, cudaStream_t stream, const DeviceInfo &dev) {
+// Launches ladder tile `tile_id` on validated, non-empty arguments with K > 0
+// (any shape: tiles overhang ragged edges; layouts and type per the flags).
+static int run_tile_ex(int tile_id, int stagger_req, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
+                       const void *B, int64_t ldb, void *C, int64_t ldc, int dtype, int layout, cudaStream_t stream,
+                       const DeviceInfo &dev) {
     const LadderTile &t = kLadder[tile_id];
-    if (!feasible(t, M, N, K, dev.smem_optin))
-        return fail(SDT_ERR_TILE, "tile %s is infeasible for %lldx%lldx%lld", t.name, (long long)M,
-                    (long long)N, (long long)K);
     CUtensorMap tmA, tmB;
-    // Each CTA stages BM / cta_group rows of A per k-tile (a pair tile splits its rows
-    // between the two CTAs); the box must match the bytes the kernel expects.
-    const uint32_t a_box_rows = uint32_t(t.BM / t.cta_group);
-    int rc = tensor_map_f16(A, uint64_t(K), uint64_t(M), uint64_t(K) * 2, kBK, a_box_rows, &tmA);
-    if (rc) return rc;
-    rc = tensor_map_f16(B, uint64_t(N), uint64_t(K), uint64_t(N) * 2, 64, kBK, &tmB);
+    int rc = operand_maps(A, lda, B, ldb, M, N, K, dtype, layout, t.BM / t.cta_group, &tmA, &tmB);
     if (rc) return rc;
     int *status = nullptr;
     rc = status_word(&status);
@@ -416,9 +463,9 @@ static int run_tile(int tile_id, int stagger_req, int64_t M, int64_t N, int64_t 
     a.M = int(M);
     a.N = int(N);
     a.K = int(K);
-    a.num_m_tiles = int(M / t.BM);
-    a.num_n_tiles = int(N / t.BN);
-    a.num_k_tiles = int(K / kBK);
+    a.num_m_tiles = int((M + t.BM - 1) / t.BM);
+    a.num_n_tiles = int((N + t.BN - 1) / t.BN);
+    a.num_k_tiles = int((K + kBK - 1) / kBK);
     a.stages = tile_stages(t, dev.smem_optin);
     const int want_stagger = stagger_req < 0 ? stagger_default() : stagger_req;
     a.stagger = (want_stagger && is_pow2(a.num_k_tiles)) ? 1 : 0;
@@ -427,6 +474,8 @@ static int run_tile(int tile_id, int stagger_req, int64_t M, int64_t N, int64_t 
     a.timeout_ns = wait_timeout_ns();
     a.status = status;
     a.max_ctas = dev.sm_count * ctas_per_sm(t, dev.smem_per_sm);
+    a.ldc = int(ldc);
+    a.idesc_flags = idesc_flags_for(dtype, layout);
     if (int64_t(a.num_m_tiles) * a.num_n_tiles > int64_t(0x3fffffff))
         return fail(SDT_ERR_SHAPE, "grid too large");
     const int tiles = a.num_m_tiles * a.num_n_tiles;
@@ -440,12 +489,22 @@ static int run_tile(int tile_id, int stagger_req, int64_t M, int64_t N, int64_t 
             a.num_items = a.tail_start + 2 * tail;
         }
     }
-    int e = t.launch(tmA, tmB, a, stream);
+    int e = t.launch[layout & 3](tmA, tmB, a, stream);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return fail(SDT_ERR_LAUNCH, "launch of tile %s failed: %s", t.name, cudaGetErrorString(cudaError_t(e)));
     }
     return SDT_OK;
+}
+
+// gemm_f16's forced tile: tight row-major fp16, the tile must divide the shape.
+static int run_tile(int tile_id, int stagger_req, int64_t M, int64_t N, int64_t K, const void *A,
+                    const void *B, void *C, cudaStream_t stream, const DeviceInfo &dev) {
+    const LadderTile &t = kLadder[tile_id];
+    if (!feasible(t, M, N, K, dev.smem_optin))
+        return fail(SDT_ERR_TILE, "tile %s is infeasible for %lldx%lldx%lld", t.name, (long long)M,
+                    (long long)N, (long long)K);
+    return run_tile_ex(tile_id, stagger_req, M, N, K, A, K, B, N, C, N, SDT_DTYPE_F16, 0, stream, dev);
 }
 
 // SDT_AUTOTUNE=1: time every feasible tile on the caller's stream (synchronising
@@ -625,15 +684,15 @@ static int splitk_run(int64_t M, int64_t N, int64_t K, const void *A, const void
     if (ws_bytes < need)
         return fail(SDT_ERR_ARG, "workspace of %zu bytes is smaller than the %zu bytes needed", ws_bytes, need);
     CUtensorMap tmA, tmB;
-    rc = tensor_map_f16(A, uint64_t(K), uint64_t(M), uint64_t(K) * 2, kBK, uint32_t(t.BM), &tmA);
-    if (rc) return rc;
-    rc = tensor_map_f16(B, uint64_t(N), uint64_t(K), uint64_t(N) * 2, 64, kBK, &tmB);
+    rc = operand_maps(A, K, B, N, M, N, K, SDT_DTYPE_F16, 0, t.BM, &tmA, &tmB);
     if (rc) return rc;
     int *status = nullptr;
     rc = status_word(&status);
     if (rc) return rc;
     GemmArgs a;
     memset(&a, 0, sizeof a);
+    a.ldc = int(N);
+    a.idesc_flags = idesc_flags_for(SDT_DTYPE_F16, 0);
     a.C = static_cast<__half *>(C);
     a.M = int(M);
     a.N = int(N);
@@ -666,6 +725,44 @@ static int splitk_run(int64_t M, int64_t N, int64_t K, const void *A, const void
         if (e2 != cudaSuccess) return fail(SDT_ERR_LAUNCH, "split-K reduction launch failed: %s", cudaGetErrorString(e2));
     }
     return SDT_OK;
+}
+
+static int gemm_ex_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
+                        void *C, int64_t ldc, int dtype, int layout, int tile_id, cudaStream_t stream) {
+    if (M < 0 || N < 0 || K < 0)
+        return fail(SDT_ERR_SHAPE, "negative dimension (M=%lld N=%lld K=%lld)", (long long)M, (long long)N,
+                    (long long)K);
+    if (dtype != SDT_DTYPE_F16 && dtype != SDT_DTYPE_BF16) return fail(SDT_ERR_ARG, "unknown dtype %d", dtype);
+    if (layout & ~(SDT_LAYOUT_A_T | SDT_LAYOUT_B_T)) return fail(SDT_ERR_ARG, "unknown layout flags %d", layout);
+    if (M == 0 || N == 0) return SDT_OK;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return fail(SDT_ERR_SHAPE, "dimension above 2^30");
+    if (!C || (K > 0 && (!A || !B))) return fail(SDT_ERR_NULL, "NULL operand pointer");
+    if ((reinterpret_cast<uintptr_t>(C) & 15) ||
+        (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15))))
+        return fail(SDT_ERR_ALIGN, "A, B and C must be 16-byte aligned");
+    if (N % 8) return fail(SDT_ERR_SHAPE, "N must be a multiple of 8 (C rows are written 16 bytes at a time)");
+    if (ldc < N || ldc % 8) return fail(SDT_ERR_ARG, "ldc must be >= N and a multiple of 8");
+    if (K > 0) {
+        const int64_t a_inner = (layout & SDT_LAYOUT_A_T) ? M : K;
+        const int64_t b_inner = (layout & SDT_LAYOUT_B_T) ? K : N;
+        if (lda < a_inner || lda % 8) return fail(SDT_ERR_ARG, "lda must be >= %lld and a multiple of 8", (long long)a_inner);
+        if (ldb < b_inner || ldb % 8) return fail(SDT_ERR_ARG, "ldb must be >= %lld and a multiple of 8", (long long)b_inner);
+    }
+    if (tile_id < -1 || tile_id >= kNumTiles) return fail(SDT_ERR_TILE, "unknown tile id %d", tile_id);
+    DeviceInfo dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    if (K == 0) {
+        const int64_t total = M * (N / 8);
+        const unsigned blocks = unsigned(std::min<int64_t>((total + 255) / 256, int64_t(dev.sm_count) * 8));
+        zero_fill_2d<<<blocks, 256, 0, stream>>>(static_cast<uint16_t *>(C), M, N, ldc);
+        cudaError_t e = cudaGetLastError();
+        return e == cudaSuccess ? SDT_OK : fail(SDT_ERR_LAUNCH, "zero fill failed: %s", cudaGetErrorString(e));
+    }
+    if (tile_id < 0) tile_id = pick_any(M, N, K, dev.sm_count, dev.smem_optin, dev.smem_per_sm);
+    if (tile_id < 0 || !fits_chip(kLadder[tile_id], dev.smem_optin))
+        return fail(SDT_ERR_TILE, "no tile fits this device");
+    return run_tile_ex(tile_id, -1, M, N, K, A, lda, B, ldb, C, ldc, dtype, layout, stream, dev);
 }
 
 // Entry for other translation units of the library (the no-allocation variant):
@@ -790,6 +887,19 @@ int sdt_tune_table_size(void) {
 int sdt_tune_table_lookup(int64_t M, int64_t N, int64_t K) {
     TuneEntry e;
     return table_lookup(M, N, K, &e) ? e.tile : -1;
+}
+
+int gemm_ex(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb, void *C,
+            int64_t ldc, int dtype, int layout, int tile_id, sdt_stream_t stream) {
+    clear_error();
+    return gemm_ex_impl(M, N, K, A, lda, B, ldb, C, ldc, dtype, layout, tile_id, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sdt_pick_tile_any_for(int64_t M, int64_t N, int64_t K, int sm_count, int smem_limit) {
+    clear_error();
+    if (sm_count <= 0 || M <= 0 || N <= 0 || K <= 0) return fail(SDT_ERR_ARG, "dimensions and sm_count must be positive");
+    const int id = pick_any(M, N, K, sm_count, smem_limit, 233472);
+    return id >= 0 ? id : fail(SDT_ERR_SHAPE, "no tile fits");
 }
 
 size_t sdt_splitk_workspace_bytes(int64_t M, int64_t N, int64_t K, int tile_id, int splits) {

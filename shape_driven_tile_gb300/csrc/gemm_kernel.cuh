@@ -31,6 +31,7 @@
 // TMEM and returns.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "ptx.cuh"
@@ -60,7 +61,81 @@ struct GemmArgs {
     // [tail_start, num_items) are column halves of tiles tail_start ... (two per tile)
     int tail_start;
     int num_items;
+    int ldc;                // row stride of C in elements
+    uint32_t idesc_flags;   // instruction-descriptor bits: accumulator, operand types, operand majors
 };
+
+// Operand layouts, a template parameter of every GEMM kernel: bit 0 set means A is
+// stored K x M (M contiguous, "transposed A"); bit 1 set means B is stored N x K
+// (K contiguous, "transposed B").  LAYOUT 0 is row-major A (M x K) and B (K x N).
+template <int LAYOUT>
+struct OperandLayout {
+    static constexpr bool A_MN = (LAYOUT & 1) != 0;  // A tile is MN-major in shared memory
+    static constexpr bool B_MN = (LAYOUT & 2) == 0;  // B tile is MN-major in shared memory
+};
+
+// One operand tile of ROWS rows (M or N) x 64 K-elements for k-tile kt.
+// MN-major operand (rows contiguous in memory): ROWS/64 TMA boxes of 64 x 64, box c
+// covering rows r0+64c .. +63 and landing at dst + 8 KB * c as 64 k-rows of 128 B
+// (canonical MN-major 128 B swizzle: 64-element chunks 8 KB apart).  K-major operand
+// (K contiguous): ROWS/KBOX boxes of 64 x KBOX (KBOX = ROWS when the whole tile is one
+// box), landing as consecutive 128-byte rows (canonical K-major 128 B swizzle: 8-row
+// groups 1024 B apart).
+template <bool PAIR, bool MN, int ROWS, int KBOX>
+__device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap *map, uint32_t bar, int kt, int r0) {
+    if constexpr (MN) {
+#pragma unroll
+        for (int c = 0; c < ROWS / 64; ++c) {
+            if (PAIR) tma_load_2d_pair(dst + c * 8192, map, bar, r0 + 64 * c, kt * kBK);
+            else tma_load_2d(dst + c * 8192, map, bar, r0 + 64 * c, kt * kBK);
+        }
+    } else {
+        static_assert(ROWS % KBOX == 0, "K-major tile must be whole boxes");
+#pragma unroll
+        for (int c = 0; c < ROWS / KBOX; ++c) {
+            if (PAIR) tma_load_2d_pair(dst + c * KBOX * 128, map, bar, kt * kBK, r0 + KBOX * c);
+            else tma_load_2d(dst + c * KBOX * 128, map, bar, kt * kBK, r0 + KBOX * c);
+        }
+    }
+}
+
+// Shared-memory matrix descriptor of a staged operand tile and its advance (in
+// 16-byte units) per K = 16 MMA step: +32 B along a K-major row, +2 KB (16 k-rows)
+// for an MN-major tile.
+template <bool MN>
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base) {
+    return MN ? smem_desc_sw128(base, 8192, 1024) : smem_desc_sw128(base, 16, 1024);
+}
+template <bool MN>
+__host__ __device__ constexpr uint64_t operand_k_step() {
+    return MN ? 128ull : 2ull;
+}
+
+// Instruction descriptor for an M x N MMA with the runtime type/major bits.
+__device__ __forceinline__ uint32_t idesc_for(uint32_t flags, int M, int N) {
+    return flags | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Stores 32 fp32 accumulator columns of one C row as fp16/bf16, 16 bytes at a time,
+// skipping vectors at or beyond column limit `ncols` (a multiple of 8).
+__device__ __forceinline__ void store_row32(void *crow, const uint32_t (&r)[32], int ncols, bool bf16) {
+    uint32_t h[16];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+        const float lo = __uint_as_float(r[2 * t]), hi = __uint_as_float(r[2 * t + 1]);
+        if (bf16) {
+            __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+            h[t] = *reinterpret_cast<uint32_t *>(&v);
+        } else {
+            __half2 v = __floats2half2_rn(lo, hi);
+            h[t] = *reinterpret_cast<uint32_t *>(&v);
+        }
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(crow);
+#pragma unroll
+    for (int v = 0; v < 4; ++v)
+        if (8 * v + 8 <= ncols) dst[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
+}
 
 template <int BM, int BN>
 struct TileCfg {
@@ -87,11 +162,12 @@ __device__ __forceinline__ void record_status(int *status, int code) {
 // tile to p.partials[split]; with p.splitk_reduce_in_kernel the last CTA of the
 // output tile to finish (per-tile arrival counter) sums all partials in split
 // order and writes the fp16 tile, then resets the counter to zero.
-template <int BM, int BN, bool SPLIT = false>
+template <int BM, int BN, bool SPLIT, int LAYOUT>
 __global__ void __launch_bounds__(128, 1)
     gemm_f16_tile_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB, const GemmArgs p) {
     using Cfg = TileCfg<BM, BN>;
+    using L = OperandLayout<LAYOUT>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -170,17 +246,15 @@ __global__ void __launch_bounds__(128, 1)
             const int kt = k_first + (stagger ? ((start + i) & (nK - 1)) : i);
             const uint32_t fb = smem_u32(&full[s]);
             mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
-            tma_load_2d(smem_u32(smA + s * Cfg::A_BYTES), &tmA, fb, kt * kBK, m0);
-#pragma unroll
-            for (int c = 0; c < BN / 64; ++c)
-                tma_load_2d(smem_u32(smB + s * Cfg::B_BYTES + c * Cfg::B_BOX_BYTES), &tmB, fb,
-                            n0 + c * 64, kt * kBK);
+            load_operand<false, L::A_MN, BM, BM>(smem_u32(smA + s * Cfg::A_BYTES), &tmA, fb, kt, m0);
+            load_operand<false, L::B_MN, BN, 64>(smem_u32(smB + s * Cfg::B_BYTES), &tmB, fb, kt, n0);
             ctrl[2] = i + 1;
             if (++s == S) { s = 0; phase ^= 1u; }
         }
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer ----------------
-        constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
+        const uint32_t idesc = idesc_for(p.idesc_flags, BM, BN);
+        constexpr uint64_t a_step = operand_k_step<L::A_MN>(), b_step = operand_k_step<L::B_MN>();
         int s = 0;
         uint32_t phase = 0;
         for (int i = 0; i < nK; ++i) {
@@ -190,16 +264,11 @@ __global__ void __launch_bounds__(128, 1)
                 break;
             }
             tc_fence_after();
-            // A: K-major, 128 B rows, 8-row groups 1024 B apart (SBO); +32 B per K=16 step.
-            // B: N-major, 64-column boxes BK*128 B apart (LBO), 8-row k groups 1024 B apart
-            //    (SBO); +2048 B per K=16 step.
-            const uint64_t a_desc = smem_desc_sw128(smem_u32(smA + s * Cfg::A_BYTES), 16, 1024);
-            const uint64_t b_desc =
-                smem_desc_sw128(smem_u32(smB + s * Cfg::B_BYTES), Cfg::B_BOX_BYTES, 1024);
+            const uint64_t a_desc = operand_desc<L::A_MN>(smem_u32(smA + s * Cfg::A_BYTES));
+            const uint64_t b_desc = operand_desc<L::B_MN>(smem_u32(smB + s * Cfg::B_BYTES));
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk)
-                umma_f16(tmem_d, a_desc + 2ull * kk, b_desc + 128ull * kk, idesc,
-                         (i > 0 || kk > 0) ? 1u : 0u);
+                umma_f16(tmem_d, a_desc + a_step * kk, b_desc + b_step * kk, idesc, (i > 0 || kk > 0) ? 1u : 0u);
             umma_commit(smem_u32(&empty[s]));
             if (++s == S) { s = 0; phase ^= 1u; }
         }
@@ -218,9 +287,10 @@ __global__ void __launch_bounds__(128, 1)
         // Accumulator row r sits in TMEM lane r for M = 128; for M = 64 rows
         // 16q .. 16q+15 sit in lanes 32q .. 32q+15 of lane quarter q.
         const int row = (BM == 128) ? (warp * 32 + lane) : (warp * 16 + lane);
-        const bool row_valid = (BM == 128) || (lane < 16);
+        const bool row_valid = ((BM == 128) || (lane < 16)) && (m0 + row < p.M);
         const uint32_t taddr_row = tmem_d + (static_cast<uint32_t>(warp * 32) << 16);
-        __half *crow = p.C + static_cast<size_t>(m0 + row) * p.N + n0;
+        const bool bf16 = ((p.idesc_flags >> 7) & 7u) == 1u;
+        uint16_t *crow = reinterpret_cast<uint16_t *>(p.C) + static_cast<size_t>(m0 + row) * p.ldc + n0;
         float *prow = SPLIT ? p.partials + (static_cast<size_t>(split) * p.M + m0 + row) * p.N + n0 : nullptr;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
@@ -235,19 +305,7 @@ __global__ void __launch_bounds__(128, 1)
                 }
                 continue;
             }
-            if (row_valid && acc_ok) {
-                uint32_t h[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    __half2 v = __floats2half2_rn(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-                    h[j] = *reinterpret_cast<uint32_t *>(&v);
-                }
-                uint4 *dst = reinterpret_cast<uint4 *>(crow + c);
-                dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
-                dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
-                dst[2] = make_uint4(h[8], h[9], h[10], h[11]);
-                dst[3] = make_uint4(h[12], h[13], h[14], h[15]);
-            }
+            if (row_valid && acc_ok) store_row32(crow + c, r, p.N - (n0 + c), bf16);
         }
     }
     tc_fence_before();
@@ -314,8 +372,8 @@ __global__ void __launch_bounds__(128, 1)
 __global__ void splitk_reduce_kernel(const float *__restrict__ partials, __half *__restrict__ C, size_t elems,
                                      int splits);
 
-// Host-side launchers, one instantiation per ladder tile (gemm_t*.cu).
-template <int BM, int BN>
+// Host-side launchers, instantiated per ladder tile and layout (gemm_t*.cu).
+template <int BM, int BN, int LAYOUT>
 int launch_gemm_tile(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args,
                      cudaStream_t stream);
 template <int BM, int BN>

@@ -13,14 +13,10 @@
 
 namespace sdt {
 
-template <int BM, int BN>
-int launch_gemm_tile(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args,
-                     cudaStream_t stream) {
-    using Cfg = TileCfg<BM, BN>;
-    auto kern = gemm_f16_tile_kernel<BM, BN>;
-    const int smem = Cfg::smem_bytes(args.stages);
-    // Raise the dynamic shared-memory cap once per device to the largest this launch needs.
-    static std::atomic<int> configured[64];
+// Raise a kernel's dynamic shared-memory cap once per device (and kernel) to the
+// largest size a launch has asked for.
+template <typename Kern>
+int ensure_smem(Kern kern, int smem, std::atomic<int> *configured) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (configured[dev].load(std::memory_order_acquire) < smem) {
@@ -30,67 +26,55 @@ int launch_gemm_tile(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmA
         while (prev < smem && !configured[dev].compare_exchange_weak(prev, smem)) {
         }
     }
+    return cudaSuccess;
+}
+
+template <int BM, int BN, int LAYOUT>
+int launch_gemm_tile(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args,
+                     cudaStream_t stream) {
+    using Cfg = TileCfg<BM, BN>;
+    auto kern = gemm_f16_tile_kernel<BM, BN, false, LAYOUT>;
+    const int smem = Cfg::smem_bytes(args.stages);
+    static std::atomic<int> configured[64];
+    if (int e = ensure_smem(kern, smem, configured)) return e;
     const unsigned grid = static_cast<unsigned>(args.num_m_tiles) * static_cast<unsigned>(args.num_n_tiles);
     return launch_kernel(kern, dim3(grid), dim3(Cfg::THREADS), size_t(smem), stream, 1, tmA, tmB, args);
 }
 
+// Split-K form (row-major A and B only).
 template <int BM, int BN>
 int launch_gemm_tile_split(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args,
                            cudaStream_t stream) {
     using Cfg = TileCfg<BM, BN>;
-    auto kern = gemm_f16_tile_kernel<BM, BN, true>;
+    auto kern = gemm_f16_tile_kernel<BM, BN, true, 0>;
     const int smem = Cfg::smem_bytes(args.stages);
     static std::atomic<int> configured[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (configured[dev].load(std::memory_order_acquire) < smem) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        int prev = configured[dev].load();
-        while (prev < smem && !configured[dev].compare_exchange_weak(prev, smem)) {
-        }
-    }
+    if (int e = ensure_smem(kern, smem, configured)) return e;
     const dim3 grid(static_cast<unsigned>(args.num_m_tiles) * static_cast<unsigned>(args.num_n_tiles),
                     static_cast<unsigned>(args.splits), 1);
     return launch_kernel(kern, grid, dim3(Cfg::THREADS), size_t(smem), stream, 1, tmA, tmB, args);
 }
 
-template <int BN>
+template <int BN, int LAYOUT>
 int launch_gemm_persistent(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args,
                            cudaStream_t stream) {
     using Cfg = PersistentCfg<BN>;
-    auto kern = gemm_f16_persistent_kernel<BN>;
+    auto kern = gemm_f16_persistent_kernel<BN, LAYOUT>;
     const int smem = Cfg::smem_bytes(args.stages);
     static std::atomic<int> configured[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (configured[dev].load(std::memory_order_acquire) < smem) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        int prev = configured[dev].load();
-        while (prev < smem && !configured[dev].compare_exchange_weak(prev, smem)) {
-        }
-    }
+    if (int e = ensure_smem(kern, smem, configured)) return e;
     const long long tiles = static_cast<long long>(args.num_m_tiles) * args.num_n_tiles;
     const unsigned grid = static_cast<unsigned>(tiles < args.max_ctas ? tiles : args.max_ctas);
     return launch_kernel(kern, dim3(grid), dim3(Cfg::THREADS), size_t(smem), stream, 1, tmA, tmB, args);
 }
 
-template <int BN>
+template <int BN, int LAYOUT>
 int launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args, cudaStream_t stream) {
     using Cfg = PairCfg<BN>;
-    auto kern = gemm_f16_pair_kernel<BN>;
+    auto kern = gemm_f16_pair_kernel<BN, LAYOUT>;
     const int smem = Cfg::smem_bytes(args.stages);
     static std::atomic<int> configured[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (configured[dev].load(std::memory_order_acquire) < smem) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        int prev = configured[dev].load();
-        while (prev < smem && !configured[dev].compare_exchange_weak(prev, smem)) {
-        }
-    }
+    if (int e = ensure_smem(kern, smem, configured)) return e;
     const long long items = args.num_items;
     const long long pairs_cap = args.max_ctas / 2 > 0 ? args.max_ctas / 2 : 1;
     const unsigned pairs = static_cast<unsigned>(items < pairs_cap ? items : pairs_cap);
@@ -99,16 +83,23 @@ int launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmA
 
 }  // namespace sdt
 
-#define SDT_INSTANTIATE_GEMM_PAIR(BN)                                                              \
-    template int sdt::launch_gemm_pair<BN>(const CUtensorMap &, const CUtensorMap &, const sdt::GemmArgs &, \
-                                           cudaStream_t);
+// Each macro instantiates one ladder tile for the four operand layouts.
+#define SDT_LAYOUTS_(X, ...) X(__VA_ARGS__, 0) X(__VA_ARGS__, 1) X(__VA_ARGS__, 2) X(__VA_ARGS__, 3)
 
-#define SDT_INSTANTIATE_GEMM_PERSISTENT(BN)                                                        \
-    template int sdt::launch_gemm_persistent<BN>(const CUtensorMap &, const CUtensorMap &,         \
-                                                 const sdt::GemmArgs &, cudaStream_t);
+#define SDT_PAIR_ONE_(BN, L)                                                                         \
+    template int sdt::launch_gemm_pair<BN, L>(const CUtensorMap &, const CUtensorMap &, const sdt::GemmArgs &, \
+                                              cudaStream_t);
+#define SDT_INSTANTIATE_GEMM_PAIR(BN) SDT_LAYOUTS_(SDT_PAIR_ONE_, BN)
 
-#define SDT_INSTANTIATE_GEMM_TILE(BM, BN)                                                          \
-    template int sdt::launch_gemm_tile<BM, BN>(const CUtensorMap &, const CUtensorMap &,           \
-                                               const sdt::GemmArgs &, cudaStream_t);               \
-    template int sdt::launch_gemm_tile_split<BM, BN>(const CUtensorMap &, const CUtensorMap &,     \
+#define SDT_PERSISTENT_ONE_(BN, L)                                                                   \
+    template int sdt::launch_gemm_persistent<BN, L>(const CUtensorMap &, const CUtensorMap &,        \
+                                                    const sdt::GemmArgs &, cudaStream_t);
+#define SDT_INSTANTIATE_GEMM_PERSISTENT(BN) SDT_LAYOUTS_(SDT_PERSISTENT_ONE_, BN)
+
+#define SDT_TILE_ONE_(BM, BN, L)                                                                     \
+    template int sdt::launch_gemm_tile<BM, BN, L>(const CUtensorMap &, const CUtensorMap &,          \
+                                                  const sdt::GemmArgs &, cudaStream_t);
+#define SDT_INSTANTIATE_GEMM_TILE(BM, BN)                                                            \
+    SDT_LAYOUTS_(SDT_TILE_ONE_, BM, BN)                                                              \
+    template int sdt::launch_gemm_tile_split<BM, BN>(const CUtensorMap &, const CUtensorMap &,       \
                                                      const sdt::GemmArgs &, cudaStream_t);

@@ -67,11 +67,12 @@ __device__ __forceinline__ void pair_item(int item, const GemmArgs &p, int &tile
     tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.raster_group, m_tile, n_tile);
 }
 
-template <int BN>
+template <int BN, int LAYOUT>
 __global__ void __launch_bounds__(192, 1)
     gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const GemmArgs p) {
     using Cfg = PairCfg<BN>;
+    using L = OperandLayout<LAYOUT>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -136,8 +137,9 @@ __global__ void __launch_bounds__(192, 1)
                 pair_item<BN>(item, p, tile, m_tile, n_tile, n_off, width);
                 const int m0 = m_tile * Cfg::BM + static_cast<int>(rank) * Cfg::CTA_M;
                 const int nb = n_tile * BN + n_off + static_cast<int>(rank) * (width / 2);
-                const int boxes = width / 128;  // 64-column B boxes per CTA
-                const uint32_t pair_bytes = 2u * static_cast<uint32_t>(Cfg::A_BYTES + boxes * Cfg::B_BOX_BYTES);
+                const bool whole = width == BN;  // whole tile, else a tail half (BN/4 B rows per CTA)
+                const uint32_t pair_bytes =
+                    2u * static_cast<uint32_t>(Cfg::A_BYTES + (whole ? Cfg::B_HALF : Cfg::B_HALF / 2) * kBK * 2);
                 const int start =
                     p.stagger ? static_cast<int>((static_cast<uint32_t>(tile) * static_cast<uint32_t>(p.stagger_stride)) &
                                                  static_cast<uint32_t>(nK - 1))
@@ -154,10 +156,18 @@ __global__ void __launch_bounds__(192, 1)
                     const uint32_t fb_local = smem_u32(&full[s]);
                     if (leader) mbar_arrive_expect_tx(fb_local, pair_bytes);
                     const uint32_t fb = mapa_shared(fb_local, 0);
-                    tma_load_2d_pair(smem_u32(smA + s * Cfg::A_BYTES), &tmA, fb, kt * kBK, m0);
-                    for (int c = 0; c < boxes; ++c)
-                        tma_load_2d_pair(smem_u32(smB + s * Cfg::B_BYTES + c * Cfg::B_BOX_BYTES), &tmB, fb,
-                                         nb + c * 64, kt * kBK);
+                    load_operand<true, L::A_MN, Cfg::CTA_M, Cfg::CTA_M>(smem_u32(smA + s * Cfg::A_BYTES), &tmA, fb,
+                                                                         kt, m0);
+                    if constexpr (Cfg::B_HALF >= 128) {
+                        if (whole)
+                            load_operand<true, L::B_MN, Cfg::B_HALF, 64>(smem_u32(smB + s * Cfg::B_BYTES), &tmB, fb, kt,
+                                                                         nb);
+                        else
+                            load_operand<true, L::B_MN, Cfg::B_HALF / 2, 64>(smem_u32(smB + s * Cfg::B_BYTES), &tmB, fb,
+                                                                             kt, nb);
+                    } else {  // tail halves need B_HALF / 2 >= 64 (the host only splits BN = 256 tails)
+                        load_operand<true, L::B_MN, Cfg::B_HALF, 64>(smem_u32(smB + s * Cfg::B_BYTES), &tmB, fb, kt, nb);
+                    }
                     ctrl[2] = ++issued;
                     if (++s == S) { s = 0; phase ^= 1u; }
                 }
@@ -166,8 +176,9 @@ __global__ void __launch_bounds__(192, 1)
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             // ---------------- MMA issuer (leader only) ----------------
-            constexpr uint32_t idesc_full = idesc_f16_f32(Cfg::BM, BN);
-            constexpr uint32_t idesc_half = idesc_f16_f32(Cfg::BM, BN / 2);
+            const uint32_t idesc_full = idesc_for(p.idesc_flags, Cfg::BM, BN);
+            const uint32_t idesc_half = idesc_for(p.idesc_flags, Cfg::BM, BN / 2);
+            constexpr uint64_t a_step = operand_k_step<L::A_MN>(), b_step = operand_k_step<L::B_MN>();
             int s = 0;
             uint32_t phase = 0;
             int j = 0;
@@ -191,12 +202,11 @@ __global__ void __launch_bounds__(192, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t a_desc = smem_desc_sw128(smem_u32(smA + s * Cfg::A_BYTES), 16, 1024);
-                    const uint64_t b_desc =
-                        smem_desc_sw128(smem_u32(smB + s * Cfg::B_BYTES), Cfg::B_BOX_BYTES, 1024);
+                    const uint64_t a_desc = operand_desc<L::A_MN>(smem_u32(smA + s * Cfg::A_BYTES));
+                    const uint64_t b_desc = operand_desc<L::B_MN>(smem_u32(smB + s * Cfg::B_BYTES));
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
-                        umma_f16_pair(d_tmem, a_desc + 2ull * kk, b_desc + 128ull * kk, idesc,
+                        umma_f16_pair(d_tmem, a_desc + a_step * kk, b_desc + b_step * kk, idesc,
                                       (i > 0 || kk > 0) ? 1u : 0u);
                     umma_commit_pair(smem_u32(&empty[s]), 0x3);
                     if (++s == S) { s = 0; phase ^= 1u; }
@@ -224,7 +234,10 @@ __global__ void __launch_bounds__(192, 1)
             int tile, m_tile, n_tile, n_off, width;
             pair_item<BN>(item, p, tile, m_tile, n_tile, n_off, width);
             const int row = m_tile * Cfg::BM + static_cast<int>(rank) * Cfg::CTA_M + q * 32 + lane;
-            __half *crow = p.C + static_cast<size_t>(row) * p.N + n_tile * BN + n_off;
+            const int n0 = n_tile * BN + n_off;
+            const bool row_valid = row < p.M;
+            const bool bf16 = ((p.idesc_flags >> 7) & 7u) == 1u;
+            uint16_t *crow = reinterpret_cast<uint16_t *>(p.C) + static_cast<size_t>(row) * p.ldc + n0;
             const uint32_t taddr =
                 tmem_base + static_cast<uint32_t>(b * BN) + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll 1
@@ -237,17 +250,7 @@ __global__ void __launch_bounds__(192, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[b]), 0));
                 }
-                uint32_t h[16];
-#pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    __half2 v = __floats2half2_rn(__uint_as_float(r[2 * t]), __uint_as_float(r[2 * t + 1]));
-                    h[t] = *reinterpret_cast<uint32_t *>(&v);
-                }
-                uint4 *dst = reinterpret_cast<uint4 *>(crow + c);
-                dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
-                dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
-                dst[2] = make_uint4(h[8], h[9], h[10], h[11]);
-                dst[3] = make_uint4(h[12], h[13], h[14], h[15]);
+                if (row_valid) store_row32(crow + c, r, p.N - (n0 + c), bf16);
             }
         }
     }
@@ -270,7 +273,7 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
-template <int BN>
+template <int BN, int LAYOUT>
 int launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args, cudaStream_t stream);
 
 }  // namespace sdt

@@ -62,11 +62,12 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int 
     n_tile = in_band / band_m;
 }
 
-template <int BN>
+template <int BN, int LAYOUT>
 __global__ void __launch_bounds__(192, 1)
     gemm_f16_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
                                const __grid_constant__ CUtensorMap tmB, const GemmArgs p) {
     using Cfg = PersistentCfg<BN>;
+    using L = OperandLayout<LAYOUT>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -142,11 +143,8 @@ __global__ void __launch_bounds__(192, 1)
                     const int kt = p.stagger ? ((start + i) & (nK - 1)) : i;
                     const uint32_t fb = smem_u32(&full[s]);
                     mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
-                    tma_load_2d(smem_u32(smA + s * Cfg::A_BYTES), &tmA, fb, kt * kBK, m0);
-#pragma unroll
-                    for (int c = 0; c < BN / 64; ++c)
-                        tma_load_2d(smem_u32(smB + s * Cfg::B_BYTES + c * Cfg::B_BOX_BYTES), &tmB, fb,
-                                    n0 + c * 64, kt * kBK);
+                    load_operand<false, L::A_MN, Cfg::BM, Cfg::BM>(smem_u32(smA + s * Cfg::A_BYTES), &tmA, fb, kt, m0);
+                    load_operand<false, L::B_MN, BN, 64>(smem_u32(smB + s * Cfg::B_BYTES), &tmB, fb, kt, n0);
                     ctrl[2] = ++issued;
                     if (++s == S) { s = 0; phase ^= 1u; }
                 }
@@ -156,7 +154,8 @@ __global__ void __launch_bounds__(192, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------- MMA issuer ----------------
-            constexpr uint32_t idesc = idesc_f16_f32(Cfg::BM, BN);
+            const uint32_t idesc = idesc_for(p.idesc_flags, Cfg::BM, BN);
+            constexpr uint64_t a_step = operand_k_step<L::A_MN>(), b_step = operand_k_step<L::B_MN>();
             int s = 0;
             uint32_t phase = 0;
             int j = 0;
@@ -179,12 +178,11 @@ __global__ void __launch_bounds__(192, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t a_desc = smem_desc_sw128(smem_u32(smA + s * Cfg::A_BYTES), 16, 1024);
-                    const uint64_t b_desc =
-                        smem_desc_sw128(smem_u32(smB + s * Cfg::B_BYTES), Cfg::B_BOX_BYTES, 1024);
+                    const uint64_t a_desc = operand_desc<L::A_MN>(smem_u32(smA + s * Cfg::A_BYTES));
+                    const uint64_t b_desc = operand_desc<L::B_MN>(smem_u32(smB + s * Cfg::B_BYTES));
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
-                        umma_f16(d_tmem, a_desc + 2ull * kk, b_desc + 128ull * kk, idesc,
+                        umma_f16(d_tmem, a_desc + a_step * kk, b_desc + b_step * kk, idesc,
                                  (i > 0 || kk > 0) ? 1u : 0u);
                     umma_commit(smem_u32(&empty[s]));
                     if (++s == S) { s = 0; phase ^= 1u; }
@@ -213,7 +211,10 @@ __global__ void __launch_bounds__(192, 1)
             int m_tile, n_tile;
             tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.raster_group, m_tile, n_tile);
             const int row = m_tile * Cfg::BM + q * 32 + lane;
-            __half *crow = p.C + static_cast<size_t>(row) * p.N + n_tile * BN;
+            const int n0 = n_tile * BN;
+            const bool row_valid = row < p.M;
+            const bool bf16 = ((p.idesc_flags >> 7) & 7u) == 1u;
+            uint16_t *crow = reinterpret_cast<uint16_t *>(p.C) + static_cast<size_t>(row) * p.ldc + n0;
             const uint32_t taddr = tmem_base + static_cast<uint32_t>(b * BN) + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll 1
             for (int c = 0; c < BN; c += 32) {
@@ -226,17 +227,7 @@ __global__ void __launch_bounds__(192, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&acc_empty[b]));
                 }
-                uint32_t h[16];
-#pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    __half2 v = __floats2half2_rn(__uint_as_float(r[2 * t]), __uint_as_float(r[2 * t + 1]));
-                    h[t] = *reinterpret_cast<uint32_t *>(&v);
-                }
-                uint4 *dst = reinterpret_cast<uint4 *>(crow + c);
-                dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
-                dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
-                dst[2] = make_uint4(h[8], h[9], h[10], h[11]);
-                dst[3] = make_uint4(h[12], h[13], h[14], h[15]);
+                if (row_valid) store_row32(crow + c, r, p.N - (n0 + c), bf16);
             }
         }
     }
@@ -259,7 +250,7 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
-template <int BN>
+template <int BN, int LAYOUT>
 int launch_gemm_persistent(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args,
                            cudaStream_t stream);
 

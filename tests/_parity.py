@@ -52,3 +52,27 @@ def boundary_rows(M: int, step: int = 64, extra: int = 8, seed: int = 0) -> np.n
 
 def nan_like(shape, device, dtype=torch.float16):
     return torch.full(shape, float("nan"), dtype=dtype, device=device)
+
+
+def assert_close_bf16(got, ref, K, what=""):
+    """bf16 output: the fp32 accumulation bound 1e-3*sqrt(K) plus half a bf16 ulp of the
+    result (2^-8 relative), and a relative Frobenius error within 2^-8 (the bf16
+    rounding of C alone is up to 2^-8 relative)."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    bound = 1e-3 * np.sqrt(max(K, 1)) + 2.0 ** -8 * np.abs(ref)
+    excess = np.abs(got - ref) - bound
+    assert excess.max() <= 0, f"{what}: error exceeds bound by {excess.max():.3e}"
+    nref = float(np.linalg.norm(ref))
+    if nref > 0:
+        rel = float(np.linalg.norm(got - ref)) / nref
+        assert rel <= 2.0 ** -8, f"{what}: relative Frobenius error {rel:.3e} > 2^-8"
+
+
+def assert_bit_exact_bf16(got_bf16, ref_f64, what=""):
+    want = oracle.f64_to_bf16(ref_f64)
+    got = u16(got_bf16)
+    bad = got != want
+    assert not bad.any(), f"{what}: {int(bad.sum())} of {bad.size} bf16 results differ from the oracle"

@@ -250,3 +250,38 @@ def test_gemv_q8_one_hot_positions():
 def test_gemv_q8_rejects_ragged_group():
     with pytest.raises(ValueError):
         oracle.gemv_q8(np.zeros(40, np.uint16), np.zeros((2, 40), np.int8), np.zeros((2, 1), np.uint16))
+
+
+# ---- bf16 ----------------------------------------------------------------
+
+
+def test_bf16_encode_roundtrip_ties_and_random():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = bf16_vals(bits)
+    finite = np.isfinite(vals)
+    assert np.array_equal(oracle.f64_to_bf16(vals[finite]), bits[finite])
+    # Midpoints between consecutive positive finite bf16 values and random values,
+    # against torch's conversion (nearest, ties to even).  torch converts float64
+    # through float32, so every input here is exactly representable in float32:
+    # then its result is a single rounding to bf16.
+    pos = np.unique(vals[finite & (vals >= 0)])
+    mids = (pos[:-1] + pos[1:]) / 2.0
+    rnd = (RNG.standard_normal(50000) * 10.0 ** RNG.integers(-40, 38, 50000)).astype(np.float32)
+    x = np.concatenate([mids, -mids, rnd[np.isfinite(rnd)].astype(np.float64),
+                        np.array([3.3895313892515355e38, float(np.float32(3.4e38)), 2.0 ** -149, 2.0 ** -134,
+                                  3 * 2.0 ** -135, 0.0, -0.0])])
+    assert np.array_equal(x.astype(np.float32).astype(np.float64), x)
+    want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.f64_to_bf16(x), want)
+
+
+def test_gemm_bf16_matches_library_matmul_and_integers():
+    M, N, K = 19, 31, 53
+    A = bf16_bits(RNG.uniform(-1, 1, (M, K)))
+    B = bf16_bits(RNG.uniform(-1, 1, (K, N)))
+    want = bf16_vals(A) @ bf16_vals(B)
+    assert np.allclose(oracle.gemm(A, B, dtype="bf16"), want, rtol=0, atol=1e-12)
+    Ai = RNG.integers(-2, 3, (M, K))
+    Bi = RNG.integers(-2, 3, (K, N))
+    got = oracle.gemm(bf16_bits(Ai), bf16_bits(Bi), dtype="bf16")
+    assert np.array_equal(got, (Ai @ Bi).astype(np.float64))

@@ -28,6 +28,10 @@ FORMAT_PINS = [
     pins.test_f16_encode_roundtrip_and_ties,
     pins.test_f16_encode_random_and_edges,
 ]
+BF16_PINS = [
+    pins.test_bf16_encode_roundtrip_ties_and_random,
+    pins.test_gemm_bf16_matches_library_matmul_and_integers,
+]
 GEMV_PINS = [
     pins.test_gemv_bf16_matches_library_dot,
     pins.test_gemv_bf16_integer_exact_and_layout,
@@ -36,13 +40,18 @@ GEMV_PINS = [
 ]
 
 MUTANTS = {
+    "bf16_round_down": ("double q = nearbyint(ldexp(a, 7 - E));", "double q = floor(ldexp(a, 7 - E));", BF16_PINS),
+    "bf16_bias": ("return (uint16_t)(sign | (uint16_t)((E + 127) << 7) | (uint16_t)((int)q - 128));",
+                  "return (uint16_t)(sign | (uint16_t)((E + 126) << 7) | (uint16_t)((int)q - 128));", BF16_PINS),
+    "gemm_decodes_bf16_as_f16": ("return dtype ? sdt_oracle_bf16_to_f64(v) : sdt_oracle_f16_to_f64(v);",
+                                 "return sdt_oracle_f16_to_f64(v);", BF16_PINS),
     "gemm_drops_last_k": ("for (int64_t k = 0; k < K; ++k) {",
                           "for (int64_t k = 0; k < K - 1; ++k) {", GEMM_PINS),
     "gemm_sign": ("acc[j] += a * brow[j];", "acc[j] -= a * brow[j];", GEMM_PINS),
     "gemm_b_row_index": ("const double *brow = Bd + k * N;",
                          "const double *brow = Bd + (K - 1 - k) * N;", GEMM_PINS),
-    "gemm_a_col_index": ("double a = sdt_oracle_f16_to_f64(A[i * K + k]);",
-                         "double a = sdt_oracle_f16_to_f64(A[i * K + (K - 1 - k)]);", GEMM_PINS),
+    "gemm_a_col_index": ("double a = sdt_oracle_decode(A[i * K + k], dtype);",
+                         "double a = sdt_oracle_decode(A[i * K + (K - 1 - k)], dtype);", GEMM_PINS),
     "f16_bias": ("v = ldexp((double)(f + 1024), e - 25);",
                  "v = ldexp((double)(f + 1024), e - 24);", FORMAT_PINS),
     "f16_subnormal": ("v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);", FORMAT_PINS),
