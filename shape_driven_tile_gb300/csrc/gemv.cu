@@ -20,7 +20,9 @@
 //  q8  : int8 weights are turned into exact fp32 values by placing the byte
 //        (offset to unsigned) in the mantissa of 2^23 and subtracting 2^23+128
 //        (packed f32x2 add); a 16-byte chunk is half of one 32-weight group, so
-//        the group's fp16 scale multiplies the chunk's partial sum once.
+//        the group's fp16 scale multiplies the chunk's partial sum once.  The
+//        default q8 path is the integer kernel further down (gemv_q8_dp2a_kernel),
+//        which multiplies in int16 x int8 dot products instead.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -407,6 +409,272 @@ __global__ void __launch_bounds__(kStreamThreads, 1) gemv_stream_kernel(const St
     }
 }
 
+// ---------------------------------------------------------------------------------
+// q8 on integer dot products (dp2a).
+//
+// The weights are integers, so the multiply-accumulate of a group of 32 can run
+// in integer arithmetic once the activations are integers too.  Each group's 32
+// activations are multiplied by the power of two 2^(14 - e) that puts the largest
+// magnitude (binary exponent e) in [2^14, 2^15) and rounded to int16.  A bf16
+// value within a factor 2^7 of the group's largest converts exactly (so do all
+// integer inputs); a smaller one is off by at most 2^-15 of the group's largest.
+// Then
+//     y[n] = sum_g s[n,g] * 2^(e_g - 14) * sum_{k in g} xi[k] * q[n,k],
+// where the inner sum is exact in int32 (|sum| < 32 * 2^15 * 2^7 = 2^27) and
+// takes 16 dp2a instructions per group (each: two int16 x int8 products added
+// to an int32), with no per-weight conversion at all.  The fp32 path above
+// spends about four instructions per weight on conversion and packed FMA, and
+// its byte permutes issue at a quarter of the FMA rate on this GPU, while dp2a
+// issues at half rate: two per four weights.
+//
+// Work split: thread t of a CTA owns groups t, t + T, ... (GT of them) of every
+// row, so its packed int16 activations stay in registers for the whole kernel.
+// A CTA owns a contiguous, balanced range of rows and walks it RB rows at a time:
+// one 32-byte load per row and group per thread (a warp reads 1 KB of one row per
+// instruction), double-buffered so that the next RB rows are in flight while the
+// current ones are summed.  Each row's partial sums are combined by a transposed
+// butterfly within the warp and then across warps through shared memory, in a
+// fixed order: results are deterministic.
+//
+// Launch-to-launch overlap: in a stream of decode kernels the device idles
+// between the end of one kernel and the first loads of the next.  Each CTA
+// therefore asks L2 for the first pf_bytes of its rows before waiting on the
+// previous kernel (programmatic dependent launch lets it start as soon as an SM
+// has room), and the kernel's own weight loads are marked evict-first in L2 so
+// that its stream does not push those prefetched lines out.
+constexpr int kDpMaxThreads = 256;
+
+// Read-only 16-byte load kept in program order with the weight loads around it.
+__device__ __forceinline__ uint4 ld_nc_v4(const uint4 *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void ld_stream_v8(const uint8_t *p, uint32_t (&w)[8]) {
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
+                   "=r"(w[7])
+                 : "l"(p));
+}
+
+// The same 32-byte load with an L2 eviction-priority policy (from createpolicy).
+__device__ __forceinline__ void ld_stream_v8_hint(const uint8_t *p, uint64_t pol, uint32_t (&w)[8]) {
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
+                   "=r"(w[7])
+                 : "l"(p), "l"(pol));
+}
+
+// c + a.lo16 * b.byte0 + a.hi16 * b.byte1 (lo) or bytes 2, 3 (hi); all signed.
+__device__ __forceinline__ int dp2a_lo(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.lo.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp2a_hi(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.hi.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Sum RB per-lane values (one per row) over the warp.  Each round halves the
+// values a lane holds: the lower lane of a pair keeps the lower half of the rows
+// and receives its partner's copy of them, the upper lane the upper half.  After
+// log2(RB) such rounds the remaining rounds are plain butterflies; lane l then
+// holds the warp's sum for row l / (32 / RB).
+template <int RB>
+__device__ __forceinline__ float reduce_rows(float (&v)[RB], int lane) {
+    int off = 16;
+#pragma unroll
+    for (int h = RB / 2; h >= 1; h /= 2) {
+        const bool upper = lane & off;
+#pragma unroll
+        for (int i = 0; i < h; ++i) {
+            const float send = upper ? v[i] : v[i + h];
+            const float keep = upper ? v[i + h] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+        off >>= 1;
+    }
+    float r = v[0];
+#pragma unroll
+    for (; off >= 1; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
+    return r;
+}
+
+template <int GT, int RB>
+struct DpBatch {
+    uint32_t w[RB][GT][8];  // 32 int8 weights per (row, group)
+    float s[RB][GT];        // that group's scale
+};
+
+template <bool EF, int GT, int RB>
+__device__ __forceinline__ void dp_load(DpBatch<GT, RB> &b, int n0, int r_end, int K, int G, const int (&g)[GT],
+                                        const uint8_t *__restrict__ W, const __half *__restrict__ scales,
+                                        uint64_t pol) {
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+        const int n = n0 + r;
+#pragma unroll
+        for (int i = 0; i < GT; ++i) {
+            if (n < r_end && g[i] < G) {
+                // (a run-time choice here would merge the two loads' registers and wait for each)
+                if (EF) ld_stream_v8_hint(W + size_t(n) * K + size_t(g[i]) * 32, pol, b.w[r][i]);
+                else ld_stream_v8(W + size_t(n) * K + size_t(g[i]) * 32, b.w[r][i]);
+                b.s[r][i] = __half2float(scales[size_t(n) * G + g[i]]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) b.w[r][i][j] = 0u;
+                b.s[r][i] = 0.f;
+            }
+        }
+    }
+}
+
+// Thread 0 asks L2 for rows [r0, r1) of W and of the scales (clipped to 16-byte
+// boundaries inside the range).  These requests need no registers, so they add to
+// the bytes in flight per SM beyond the two register batches; the branch on the
+// thread index also keeps the compiler from sinking the batch loads issued just
+// before it into the arithmetic that follows.
+__device__ __forceinline__ void dp_prefetch_rows(int r0, int r1, int K, int G, const uint8_t *W,
+                                                 const __half *scales) {
+    if (threadIdx.x == 0 && r1 > r0) {
+        const size_t w0 = size_t(r0) * K, wb = size_t(r1 - r0) * K;  // K % 32 == 0
+        for (size_t o = 0; o < wb; o += 32768) bulk_prefetch_l2(W + w0 + o, uint32_t(wb - o < 32768 ? wb - o : 32768));
+        const size_t s0 = (size_t(r0) * G * 2 + 15) & ~size_t(15), s1 = (size_t(r1) * G * 2) & ~size_t(15);
+        if (s1 > s0 && (reinterpret_cast<uintptr_t>(scales) & 15) == 0)
+            bulk_prefetch_l2(reinterpret_cast<const uint8_t *>(scales) + s0, uint32_t(s1 - s0));
+    }
+}
+
+template <int GT, int RB>
+__device__ __forceinline__ void dp_finish(const DpBatch<GT, RB> &b, int n0, int r_end, const uint32_t (&xi)[GT][16],
+                                          const float (&xf)[GT], float *red, float *__restrict__ y) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float p[RB];
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+        p[r] = 0.f;
+#pragma unroll
+        for (int i = 0; i < GT; ++i) {
+            int acc = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                acc = dp2a_lo(xi[i][2 * j], b.w[r][i][j], acc);
+                acc = dp2a_hi(xi[i][2 * j + 1], b.w[r][i][j], acc);
+            }
+            p[r] = fmaf(float(acc), b.s[r][i] * xf[i], p[r]);
+        }
+    }
+    const float v = reduce_rows<RB>(p, lane);
+    constexpr int kLanesPerRow = 32 / RB;
+    if (lane % kLanesPerRow == 0) red[warp * RB + lane / kLanesPerRow] = v;
+    __syncthreads();
+    if (int(threadIdx.x) < RB && n0 + int(threadIdx.x) < r_end) {
+        float t = 0.f;
+        for (int w = 0; w < int(blockDim.x >> 5); ++w) t += red[w * RB + threadIdx.x];
+        y[n0 + threadIdx.x] = t;
+    }
+}
+
+template <int GT, int RB, bool EF, int MINB = 1>
+__global__ void __launch_bounds__(kDpMaxThreads, MINB)
+    gemv_q8_dp2a_kernel(int K, int N, const uint4 *__restrict__ x, const uint8_t *__restrict__ W,
+                        const __half *__restrict__ scales, float *__restrict__ y, uint32_t pf_bytes,
+                        int ahead) {
+    __shared__ float red[2][(kDpMaxThreads / 32) * RB];  // per-warp row sums, by batch parity
+    griddep_launch_dependents();
+    uint64_t pol = 0;
+    if (EF) asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    const int G = K >> 5;
+    const int T = blockDim.x;
+    const int r_begin = int(int64_t(N) * blockIdx.x / gridDim.x);
+    const int r_end = int(int64_t(N) * (blockIdx.x + 1) / gridDim.x);
+    int g[GT];
+#pragma unroll
+    for (int i = 0; i < GT; ++i) g[i] = threadIdx.x + i * T;
+    if (pf_bytes && threadIdx.x == 0 && r_end > r_begin) {
+        // Ask L2 for the first pf_bytes of this CTA's weight rows (and their scales) while
+        // the previous kernel in the stream may still be running.  L2 is where global
+        // memory is coherent, so a line fetched now and written by that kernel later is
+        // updated in place: the loads after the wait below still see its results.
+        const size_t slice = size_t(r_end - r_begin) * K;
+        const size_t wb = slice < pf_bytes ? slice : size_t(pf_bytes);  // multiples of 16
+        const uint8_t *wp = W + size_t(r_begin) * K;
+        for (size_t o = 0; o < wb; o += 32768) bulk_prefetch_l2(wp + o, uint32_t(wb - o < 32768 ? wb - o : 32768));
+        const size_t s0 = (size_t(r_begin) * G * 2 + 15) & ~size_t(15);  // inside this CTA's scale rows
+        const size_t s1 = (size_t(r_begin) * G * 2 + (wb / K + 1) * G * 2) & ~size_t(15);
+        const size_t s2 = (size_t(r_end) * G * 2) & ~size_t(15);
+        const size_t s_end = s1 < s2 ? s1 : s2;
+        const uint8_t *sp = reinterpret_cast<const uint8_t *>(scales);
+        if (s_end > s0 && (reinterpret_cast<uintptr_t>(sp) & 15) == 0) bulk_prefetch_l2(sp + s0, uint32_t(s_end - s0));
+    }
+    griddep_wait();  // x and W may come from the previous kernel
+
+    // Issue order: the activations first (an L2 hit, so they return while the weights
+    // are still on their way), then the first two batches of weights, then the
+    // conversion, which waits only for the activations.
+    uint32_t xw[GT][16];
+#pragma unroll
+    for (int i = 0; i < GT; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 v = g[i] < G ? ld_nc_v4(x + size_t(g[i]) * 4 + j) : make_uint4(0, 0, 0, 0);
+            xw[i][4 * j] = v.x;
+            xw[i][4 * j + 1] = v.y;
+            xw[i][4 * j + 2] = v.z;
+            xw[i][4 * j + 3] = v.w;
+        }
+    DpBatch<GT, RB> ba, bb;
+    dp_load<EF>(ba, r_begin, r_end, K, G, g, W, scales, pol);
+    dp_load<EF>(bb, r_begin + RB, r_end, K, G, g, W, scales, pol);
+    // rows loaded into registers later are asked of L2 `ahead` rows in advance
+    if (ahead) dp_prefetch_rows(r_begin + 2 * RB, min(r_begin + 2 * RB + ahead, r_end), K, G, W, scales);
+
+    // this thread's groups of activations -> packed int16 pairs and the factor undoing the scaling
+    uint32_t xi[GT][16];
+    float xf[GT];
+#pragma unroll
+    for (int i = 0; i < GT; ++i) {
+        uint32_t e2 = 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) e2 = __vmaxu2(e2, xw[i][j] & 0x7F807F80u);  // exponent fields
+        const uint32_t e_raw = max(e2 & 0xFFFFu, e2 >> 16) >> 7;
+        // clamp tiny groups so both factors stay normal floats (values below 2^-111 are
+        // rounded to multiples of 2^-125, far below any tolerance)
+        const uint32_t e = max(e_raw, 16u);
+        const float up = __uint_as_float((268u - e) << 23);  // 2^(14 - (e - 127))
+        xf[i] = e_raw == 255u ? __uint_as_float(0x7FC00000u)  // Inf or NaN among the activations
+                              : __uint_as_float((e - 14u) << 23);  // 2^((e - 127) - 14)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int lo = __float2int_rn(__uint_as_float(xw[i][j] << 16) * up);
+            const int hi = __float2int_rn(__uint_as_float(xw[i][j] & 0xFFFF0000u) * up);
+            xi[i][j] = (uint32_t(lo) & 0xFFFFu) | (uint32_t(hi) << 16);
+        }
+    }
+
+    // batch pipeline: while one register set is summed, the other is in flight
+    int n0 = r_begin, parity = 0;
+    while (n0 < r_end) {
+        dp_finish(ba, n0, r_end, xi, xf, red[parity], y);
+        parity ^= 1;
+        if (n0 + 2 * RB < r_end) {
+            dp_load<EF>(ba, n0 + 2 * RB, r_end, K, G, g, W, scales, pol);
+            if (ahead) dp_prefetch_rows(n0 + 2 * RB + ahead, min(n0 + 3 * RB + ahead, r_end), K, G, W, scales);
+        }
+        if (n0 + RB >= r_end) break;
+        dp_finish(bb, n0 + RB, r_end, xi, xf, red[parity], y);
+        parity ^= 1;
+        if (n0 + 3 * RB < r_end) {
+            dp_load<EF>(bb, n0 + 3 * RB, r_end, K, G, g, W, scales, pol);
+            if (ahead) dp_prefetch_rows(n0 + 3 * RB + ahead, min(n0 + 4 * RB + ahead, r_end), K, G, W, scales);
+        }
+        n0 += 2 * RB;
+    }
+}
+
 __global__ void zero_fill_f32(float *y, int64_t n) {
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x)
         y[i] = 0.f;
@@ -415,22 +683,108 @@ __global__ void zero_fill_f32(float *y, int64_t n) {
 struct GemvVariant {
     int rows, unroll;  // register-path kernel: rows per warp, chunks in flight per row
     int stream_h;      // > 0: streaming kernel with this many consumer warps per row
+    int dp_rows;       // q8, > 0: the integer dot-product kernel with this many rows per batch
 };
 
-// Variant selection.  Default: the register kernel with 2 rows per warp and 4
-// chunks in flight per row (fastest measured on GB300 at K=4096, N=12288).
-// SDT_GEMV_VARIANT overrides: "stream1" / "stream2" (streaming kernel, warps per
-// row), "stream" (its default split), or "R,U" for the register kernel.
+// Variant selection.  Default: q8 on the integer dot-product kernel (2 rows per
+// batch) where its conditions hold, bf16 on the register kernel with 2 rows per
+// warp and 4 chunks in flight per row (fastest measured on GB300 at K=4096,
+// N=12288).  SDT_GEMV_VARIANT overrides: "dp2" / "dp4" / "dp8" (integer kernel,
+// rows per batch), "stream1" / "stream2" (streaming kernel, warps per row),
+// "stream" (its default split), or "R,U" for the register kernel.
 static GemvVariant gemv_variant(bool q8) {
-    GemvVariant v{2, 4, 0};
+    GemvVariant v{2, 4, 0, q8 ? 2 : 0};
     if (const char *s = getenv("SDT_GEMV_VARIANT")) {
         int r = 0, u = 0;
-        if (!strcmp(s, "stream1")) v.stream_h = 1;
-        else if (!strcmp(s, "stream2")) v.stream_h = 2;
-        else if (!strcmp(s, "stream")) v.stream_h = q8 ? 1 : 2;
-        else if (sscanf(s, "%d,%d", &r, &u) == 2) v = GemvVariant{r, u, 0};
+        if (!strcmp(s, "dp2")) v.dp_rows = q8 ? 2 : 0;
+        else if (!strcmp(s, "dp4")) v.dp_rows = q8 ? 4 : 0;
+        else if (!strcmp(s, "dp8")) v.dp_rows = q8 ? 8 : 0;
+        else if (!strcmp(s, "stream1")) v = GemvVariant{2, 4, 1, 0};
+        else if (!strcmp(s, "stream2")) v = GemvVariant{2, 4, 2, 0};
+        else if (!strcmp(s, "stream")) v = GemvVariant{2, 4, q8 ? 1 : 2, 0};
+        else if (sscanf(s, "%d,%d", &r, &u) == 2) v = GemvVariant{r, u, 0, 0};
     }
     return v;
+}
+
+// Bytes of its weight rows each decode CTA asks L2 for before waiting on the
+// previous kernel (SDT_GEMV_L2_PREFETCH_KB, default 8; 0 turns the prefetch off).
+// 8 KB per CTA (7 MB over the grid at K=4096) measured best on GB300: larger
+// prefetches compete with the previous kernel's last loads.
+static uint32_t gemv_l2_prefetch_bytes() {
+    if (const char *s = getenv("SDT_GEMV_L2_PREFETCH_KB")) {
+        const long kb = strtol(s, nullptr, 10);
+        return kb > 0 ? uint32_t(std::min<long>(kb, 1 << 20) * 1024) : 0u;
+    }
+    return 8u * 1024;
+}
+
+// How many rows ahead of its register loads a decode CTA asks L2 for rows
+// (SDT_GEMV_L2_AHEAD_ROWS, default one batch; rounded up to whole batches, 0 =
+// none).  Measured on GB300 at K=4096, N=12288: one batch ahead is best; more
+// only adds requests that compete with the register loads.
+static int gemv_l2_ahead_rows(int rb) {
+    int rows = rb;
+    if (const char *s = getenv("SDT_GEMV_L2_AHEAD_ROWS")) rows = std::max(0, atoi(s));
+    return (rows + rb - 1) / rb * rb;
+}
+
+// Launches the integer dot-product q8 kernel: T = ceil(G / GT) threads rounded up
+// to a warp, one CTA per resident slot on every SM (balanced row ranges).
+template <int GT, int RB, bool EF, int MINB = 1>
+static cudaError_t launch_q8_dp(int K, int N, const void *x, const void *W, const void *sc, float *y,
+                                cudaStream_t s, const DeviceInfo &dev) {
+    auto kern = gemv_q8_dp2a_kernel<GT, RB, EF, MINB>;
+    const int G = K / 32;
+    const int T = ((G + GT - 1) / GT + 31) / 32 * 32;
+    static std::atomic<int> occ_cache[64][kDpMaxThreads / 32];  // resident CTAs per SM, by device and T
+    if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+    std::atomic<int> &slot = occ_cache[dev.device][T / 32 - 1];
+    int occ = slot.load();
+    if (occ <= 0) {
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, T, 0);
+        if (e != cudaSuccess) return e;
+        if (occ < 1) occ = 1;
+        slot.store(occ);
+    }
+    const int grid = int(std::min<int64_t>(int64_t(occ) * dev.sm_count, N));
+    return launch_kernel(kern, dim3(grid), dim3(T), 0, s, 1, K, N, static_cast<const uint4 *>(x),
+                         static_cast<const uint8_t *>(W), static_cast<const __half *>(sc), y,
+                         gemv_l2_prefetch_bytes(), gemv_l2_ahead_rows(RB));
+}
+
+// The integer kernel takes up to 256 threads of 1 or 2 groups each (K <= 16384)
+// and 32-byte aligned weights (its loads are 32 bytes); returns false to ask for
+// another kernel.  Two rows per batch with registers capped at 64 (8 CTAs of 128
+// threads per SM) keeps the most bytes in flight and measured fastest; the weight
+// loads are marked evict-first in L2 (SDT_GEMV_EVICT_FIRST=0 turns that off) so
+// they do not displace the next kernel's prefetched rows.
+static bool try_q8_dp(int rows, int64_t K, int64_t N, const void *x, const void *W, const void *scales, float *y,
+                      cudaStream_t s, const DeviceInfo &dev, cudaError_t *err) {
+    if (rows != 2 && rows != 4 && rows != 8) return false;
+    if (reinterpret_cast<uintptr_t>(W) & 31) return false;
+    const int64_t G = K / 32;
+    const char *ef_env = getenv("SDT_GEMV_EVICT_FIRST");
+    const bool ef = !(ef_env && (!strcmp(ef_env, "0") || !strcmp(ef_env, "off")));
+    const int k = int(K), n = int(N);
+    if (G <= kDpMaxThreads) {
+        if (rows == 2)
+            *err = ef ? launch_q8_dp<1, 2, true, 4>(k, n, x, W, scales, y, s, dev)
+                      : launch_q8_dp<1, 2, false, 4>(k, n, x, W, scales, y, s, dev);
+        else if (rows == 4)
+            *err = ef ? launch_q8_dp<1, 4, true>(k, n, x, W, scales, y, s, dev)
+                      : launch_q8_dp<1, 4, false>(k, n, x, W, scales, y, s, dev);
+        else
+            *err = ef ? launch_q8_dp<1, 8, true>(k, n, x, W, scales, y, s, dev)
+                      : launch_q8_dp<1, 8, false>(k, n, x, W, scales, y, s, dev);
+        return true;
+    }
+    if (G <= 2 * kDpMaxThreads) {
+        *err = ef ? launch_q8_dp<2, 4, true>(k, n, x, W, scales, y, s, dev)
+                  : launch_q8_dp<2, 4, false>(k, n, x, W, scales, y, s, dev);
+        return true;
+    }
+    return false;
 }
 
 template <bool Q8, int H>
@@ -546,7 +900,8 @@ static int gemv_impl(int64_t K, int64_t N, const void *x, const void *W, const v
         int *status = nullptr;
         rc = status_word(&status);
         if (rc) return rc;
-        if (!try_stream(q8, v.stream_h, K, N, x, W, scales, y, s, dev, status, &e)) {
+        if (!(q8 && try_q8_dp(v.dp_rows, K, N, x, W, scales, y, s, dev, &e)) &&
+            !try_stream(q8, v.stream_h, K, N, x, W, scales, y, s, dev, status, &e)) {
             if (!q8) SDT_GEMV_DISPATCH(e, launch_bf16, v, int(K / 8), int(N), x, W, y, s);
             else SDT_GEMV_DISPATCH(e, launch_q8, v, int(K / 16), int(N), x, W, scales, y, s);
         }

@@ -146,6 +146,13 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
         : "memory");
 }
 
+// Hint: bring `bytes` of global memory at `src` into L2 (no data returned, no
+// completion to wait for).  16-byte aligned address, size a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+                 : "memory");
+}
+
 // ---- tcgen05: tensor memory -------------------------------------------------
 
 // Allocate `ncols` TMEM columns (power of two, 32..512); the base address is written to smem at `dst`.

@@ -13,7 +13,7 @@ from _parity import assert_close, u16
 pytestmark = pytest.mark.gpu
 
 K_DEC, N_DEC = 4096, 12288
-VARIANTS = ["stream", "stream1", "stream2", "1,4", "2,4", "4,4"]
+VARIANTS = ["stream", "stream1", "stream2", "1,4", "2,4", "4,4", "dp2", "dp4", "dp8"]
 
 
 @pytest.fixture
@@ -102,3 +102,58 @@ def test_rotating_buffers_each_correct(cuda_device):
         W = inputs.uniform((2048, K_DEC), seed=102 + i, dtype=torch.bfloat16)
         y = sdt.gemv_m1(xd, W.to(cuda_device)).cpu().numpy()
         assert_close(y, oracle.gemv_bf16(u16(x), u16(W)), K_DEC, f"buffer {i}")
+
+
+@pytest.mark.parametrize("variant", ["dp2", "dp4", "dp8"], indirect=True)
+@pytest.mark.parametrize("K,N", [(32, 3), (4096, 12291), (4128, 65), (8192, 300), (12288, 4096), (16384, 77)])
+def test_ragged_q8_integer_kernel(cuda_device, variant, K, N):
+    # K = 32 (one group), a ragged group count, one and two groups per thread
+    x = inputs.uniform((K,), seed=93, dtype=torch.bfloat16)
+    q, s = inputs.q8_weights(N, K, seed=94)
+    y = sdt.gemv_m1(x.to(cuda_device), q.to(cuda_device), s.to(cuda_device)).cpu().numpy()
+    assert_close(y, oracle.gemv_q8(u16(x), q.numpy(), u16(s)), K, f"q8 {variant} K={K} N={N}")
+
+
+def test_q8_integer_exact_large_k(cuda_device):
+    # two groups per thread: still bit-exact on integer activations and power-of-two scales
+    K, N = 12288, 1000
+    x = inputs.integers((K,), seed=95, dtype=torch.bfloat16)
+    q, s = inputs.q8_weights_exact(N, K, seed=96)
+    y = sdt.gemv_m1(x.to(cuda_device), q.to(cuda_device), s.to(cuda_device)).cpu().double().numpy()
+    assert np.array_equal(y, oracle.gemv_q8(u16(x), q.numpy(), u16(s)))
+
+
+def test_q8_wide_dynamic_range(cuda_device):
+    # activations spread over 2^-24 .. 2^24: each group is rescaled by its own power of two
+    K, N = 4096, 2048
+    g = torch.Generator().manual_seed(97)
+    mag = torch.exp2(torch.randint(-24, 25, (K,), generator=g).to(torch.float32))
+    x = ((torch.rand(K, generator=g) * 2 - 1) * mag).to(torch.bfloat16)
+    q, s = inputs.q8_weights(N, K, seed=98)
+    y = sdt.gemv_m1(x.to(cuda_device), q.to(cuda_device), s.to(cuda_device)).cpu().numpy()
+    ref = oracle.gemv_q8(u16(x), q.numpy(), u16(s))
+    err = np.abs(y - ref)
+    assert np.linalg.norm(y - ref) <= 1e-3 * np.linalg.norm(ref)
+    assert err.max() <= 1e-3 * np.abs(ref).max()
+
+
+def test_q8_weights_16_byte_aligned(cuda_device):
+    # weights 16- but not 32-byte aligned take the fp32 register kernel; same result
+    K, N = 4096, 513
+    x = inputs.uniform((K,), seed=99, dtype=torch.bfloat16)
+    q, s = inputs.q8_weights(N, K, seed=100)
+    buf = torch.empty(N * K + 16, dtype=torch.int8, device=cuda_device)
+    Wd = buf[16:].view(N, K)
+    Wd.copy_(q.to(cuda_device))
+    assert Wd.data_ptr() % 32 == 16
+    y = sdt.gemv_m1(x.to(cuda_device), Wd, s.to(cuda_device)).cpu().numpy()
+    assert_close(y, oracle.gemv_q8(u16(x), q.numpy(), u16(s)), K, "q8 16-byte aligned W")
+
+
+def test_q8_nonfinite_activation_gives_nan(cuda_device):
+    K, N = 4096, 64
+    x = inputs.uniform((K,), seed=101, dtype=torch.bfloat16)
+    x[1000] = float("inf")
+    q, s = inputs.q8_weights(N, K, seed=102)
+    y = sdt.gemv_m1(x.to(cuda_device), q.to(cuda_device), s.to(cuda_device)).cpu().numpy()
+    assert not np.isfinite(y).any()
