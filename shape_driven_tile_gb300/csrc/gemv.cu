@@ -7,7 +7,16 @@
 // (round v4); q8 (int8 with a scale per 32 weights, round v2) halves the bytes
 // but only pays if dequantisation stays off the critical path.
 //
-// Design here: one warp owns ROWS consecutive output rows at a time.  Lane l
+// Two designs live here.  The default one (further down: gemv_q8_dp2a_kernel and
+// gemv_bf16_rows_kernel) gives each CTA a balanced contiguous range of rows and
+// its threads fixed 32-byte slices of every row, with the activations kept in
+// registers, two batches of rows in flight, L2 prefetches that start before the
+// previous kernel in the stream has finished, and q8 multiplied in int16 x int8
+// dot products.  The first one, kept as a fallback for shapes the default does
+// not take (K not a multiple of 16, K above 8192 for bf16 or 16384 for q8,
+// weights only 16-byte aligned):
+//
+// One warp owns ROWS consecutive output rows at a time.  Lane l
 // reads 16-byte chunks l, l+32, l+64, ... of each row, so every load instruction
 // of the warp covers 512 contiguous bytes of one row.  U chunks per row are
 // issued before any arithmetic so that ROWS*U 16-byte loads per lane are in
@@ -20,9 +29,7 @@
 //  q8  : int8 weights are turned into exact fp32 values by placing the byte
 //        (offset to unsigned) in the mantissa of 2^23 and subtracting 2^23+128
 //        (packed f32x2 add); a 16-byte chunk is half of one 32-weight group, so
-//        the group's fp16 scale multiplies the chunk's partial sum once.  The
-//        default q8 path is the integer kernel further down (gemv_q8_dp2a_kernel),
-//        which multiplies in int16 x int8 dot products instead.
+//        the group's fp16 scale multiplies the chunk's partial sum once.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -548,10 +555,26 @@ __device__ __forceinline__ void dp_prefetch_rows(int r0, int r1, int K, int G, c
     }
 }
 
+// The CTA's partial sums p[r] of rows n0 + r -> y: warp butterfly, then the warps'
+// sums added in warp order by threads 0..RB-1 (one barrier; `red` alternates
+// between two buffers by batch, so the next batch's writes cannot race the reads).
+template <int RB>
+__device__ __forceinline__ void store_rows(float (&p)[RB], int n0, int r_end, float *red, float *__restrict__ y) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float v = reduce_rows<RB>(p, lane);
+    constexpr int kLanesPerRow = 32 / RB;
+    if (lane % kLanesPerRow == 0) red[warp * RB + lane / kLanesPerRow] = v;
+    __syncthreads();
+    if (int(threadIdx.x) < RB && n0 + int(threadIdx.x) < r_end) {
+        float t = 0.f;
+        for (int w = 0; w < int(blockDim.x >> 5); ++w) t += red[w * RB + threadIdx.x];
+        y[n0 + threadIdx.x] = t;
+    }
+}
+
 template <int GT, int RB>
 __device__ __forceinline__ void dp_finish(const DpBatch<GT, RB> &b, int n0, int r_end, const uint32_t (&xi)[GT][16],
                                           const float (&xf)[GT], float *red, float *__restrict__ y) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     float p[RB];
 #pragma unroll
     for (int r = 0; r < RB; ++r) {
@@ -567,15 +590,7 @@ __device__ __forceinline__ void dp_finish(const DpBatch<GT, RB> &b, int n0, int 
             p[r] = fmaf(float(acc), b.s[r][i] * xf[i], p[r]);
         }
     }
-    const float v = reduce_rows<RB>(p, lane);
-    constexpr int kLanesPerRow = 32 / RB;
-    if (lane % kLanesPerRow == 0) red[warp * RB + lane / kLanesPerRow] = v;
-    __syncthreads();
-    if (int(threadIdx.x) < RB && n0 + int(threadIdx.x) < r_end) {
-        float t = 0.f;
-        for (int w = 0; w < int(blockDim.x >> 5); ++w) t += red[w * RB + threadIdx.x];
-        y[n0 + threadIdx.x] = t;
-    }
+    store_rows<RB>(p, n0, r_end, red, y);
 }
 
 template <int GT, int RB, bool EF, int MINB = 1>
@@ -675,6 +690,124 @@ __global__ void __launch_bounds__(kDpMaxThreads, MINB)
     }
 }
 
+// ---------------------------------------------------------------------------------
+// bf16 decode on the same row-range skeleton.  Thread t owns the 32-byte units
+// (16 weights) t, t + T, ... of every row and holds their activations in
+// registers as fp32 pairs; per unit: one 32-byte load, 8 bf16 -> fp32 pair
+// conversions (shift and mask) and 8 packed f32x2 FMAs.  Balanced row ranges,
+// two register batches in flight, the L2 prefetch before the wait and one batch
+// ahead, evict-first weight loads and the fixed-order reduction are as in the q8
+// kernel above.
+template <int GT, int RB>
+struct BfBatch {
+    uint32_t w[RB][GT][8];  // 16 bf16 weights per (row, unit)
+};
+
+template <bool EF, int GT, int RB>
+__device__ __forceinline__ void bf_load(BfBatch<GT, RB> &b, int n0, int r_end, int K, int U, const int (&u)[GT],
+                                        const uint8_t *__restrict__ W, uint64_t pol) {
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+        const int n = n0 + r;
+#pragma unroll
+        for (int i = 0; i < GT; ++i) {
+            if (n < r_end && u[i] < U) {
+                const uint8_t *p = W + size_t(n) * 2 * K + size_t(u[i]) * 32;
+                if (EF) ld_stream_v8_hint(p, pol, b.w[r][i]);
+                else ld_stream_v8(p, b.w[r][i]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) b.w[r][i][j] = 0u;
+            }
+        }
+    }
+}
+
+// Thread 0 asks L2 for rows [r0, r1) of a bf16 W (row bytes 2K, a multiple of 32).
+__device__ __forceinline__ void bf_prefetch_rows(int r0, int r1, int K, const uint8_t *W) {
+    if (threadIdx.x == 0 && r1 > r0) {
+        const size_t w0 = size_t(r0) * 2 * K, wb = size_t(r1 - r0) * 2 * K;
+        for (size_t o = 0; o < wb; o += 32768) bulk_prefetch_l2(W + w0 + o, uint32_t(wb - o < 32768 ? wb - o : 32768));
+    }
+}
+
+template <int GT, int RB>
+__device__ __forceinline__ void bf_finish(const BfBatch<GT, RB> &b, int n0, int r_end, const uint64_t (&xp)[GT][8],
+                                          float *red, float *__restrict__ y) {
+    float p[RB];
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+        uint64_t acc = 0;
+#pragma unroll
+        for (int i = 0; i < GT; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc = fma2(bf16x2_to_f32x2(b.w[r][i][j]), xp[i][j], acc);
+        p[r] = sum2(acc);
+    }
+    store_rows<RB>(p, n0, r_end, red, y);
+}
+
+template <int GT, int RB, bool EF, int MINB = 1>
+__global__ void __launch_bounds__(kDpMaxThreads, MINB)
+    gemv_bf16_rows_kernel(int K, int N, const uint4 *__restrict__ x, const uint8_t *__restrict__ W,
+                          float *__restrict__ y, uint32_t pf_bytes, int ahead) {
+    __shared__ float red[2][(kDpMaxThreads / 32) * RB];  // per-warp row sums, by batch parity
+    griddep_launch_dependents();
+    uint64_t pol = 0;
+    if (EF) asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    const int U = K >> 4;  // 32-byte units per row
+    const int T = blockDim.x;
+    const int r_begin = int(int64_t(N) * blockIdx.x / gridDim.x);
+    const int r_end = int(int64_t(N) * (blockIdx.x + 1) / gridDim.x);
+    int u[GT];
+#pragma unroll
+    for (int i = 0; i < GT; ++i) u[i] = threadIdx.x + i * T;
+    if (pf_bytes && threadIdx.x == 0 && r_end > r_begin) {
+        // as in the q8 kernel: only moves bytes of this CTA's rows into L2 early
+        const size_t slice = size_t(r_end - r_begin) * 2 * K;
+        const size_t wb = slice < pf_bytes ? slice : size_t(pf_bytes);
+        const uint8_t *wp = W + size_t(r_begin) * 2 * K;
+        for (size_t o = 0; o < wb; o += 32768) bulk_prefetch_l2(wp + o, uint32_t(wb - o < 32768 ? wb - o : 32768));
+    }
+    griddep_wait();  // x and W may come from the previous kernel
+
+    uint32_t xw[GT][8];
+#pragma unroll
+    for (int i = 0; i < GT; ++i) {
+        const uint4 v0 = u[i] < U ? ld_nc_v4(x + size_t(u[i]) * 2) : make_uint4(0, 0, 0, 0);
+        const uint4 v1 = u[i] < U ? ld_nc_v4(x + size_t(u[i]) * 2 + 1) : make_uint4(0, 0, 0, 0);
+        xw[i][0] = v0.x; xw[i][1] = v0.y; xw[i][2] = v0.z; xw[i][3] = v0.w;
+        xw[i][4] = v1.x; xw[i][5] = v1.y; xw[i][6] = v1.z; xw[i][7] = v1.w;
+    }
+    BfBatch<GT, RB> ba, bb;
+    bf_load<EF>(ba, r_begin, r_end, K, U, u, W, pol);
+    bf_load<EF>(bb, r_begin + RB, r_end, K, U, u, W, pol);
+    if (ahead) bf_prefetch_rows(r_begin + 2 * RB, min(r_begin + 2 * RB + ahead, r_end), K, W);
+    uint64_t xp[GT][8];
+#pragma unroll
+    for (int i = 0; i < GT; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) xp[i][j] = bf16x2_to_f32x2(xw[i][j]);
+
+    int n0 = r_begin, parity = 0;
+    while (n0 < r_end) {
+        bf_finish(ba, n0, r_end, xp, red[parity], y);
+        parity ^= 1;
+        if (n0 + 2 * RB < r_end) {
+            bf_load<EF>(ba, n0 + 2 * RB, r_end, K, U, u, W, pol);
+            if (ahead) bf_prefetch_rows(n0 + 2 * RB + ahead, min(n0 + 3 * RB + ahead, r_end), K, W);
+        }
+        if (n0 + RB >= r_end) break;
+        bf_finish(bb, n0 + RB, r_end, xp, red[parity], y);
+        parity ^= 1;
+        if (n0 + 3 * RB < r_end) {
+            bf_load<EF>(bb, n0 + 3 * RB, r_end, K, U, u, W, pol);
+            if (ahead) bf_prefetch_rows(n0 + 3 * RB + ahead, min(n0 + 4 * RB + ahead, r_end), K, W);
+        }
+        n0 += 2 * RB;
+    }
+}
+
 __global__ void zero_fill_f32(float *y, int64_t n) {
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x)
         y[i] = 0.f;
@@ -683,22 +816,23 @@ __global__ void zero_fill_f32(float *y, int64_t n) {
 struct GemvVariant {
     int rows, unroll;  // register-path kernel: rows per warp, chunks in flight per row
     int stream_h;      // > 0: streaming kernel with this many consumer warps per row
-    int dp_rows;       // q8, > 0: the integer dot-product kernel with this many rows per batch
+    int rr_rows;       // > 0: the row-range kernel (q8: integer dot products) with this many rows per batch
 };
 
-// Variant selection.  Default: q8 on the integer dot-product kernel (2 rows per
-// batch) where its conditions hold, bf16 on the register kernel with 2 rows per
-// warp and 4 chunks in flight per row (fastest measured on GB300 at K=4096,
-// N=12288).  SDT_GEMV_VARIANT overrides: "dp2" / "dp4" / "dp8" (integer kernel,
-// rows per batch), "stream1" / "stream2" (streaming kernel, warps per row),
-// "stream" (its default split), or "R,U" for the register kernel.
+// Variant selection.  Default: the row-range kernels with 2 rows per batch (q8 on
+// integer dot products, bf16 on packed fp32 FMA) where their conditions hold,
+// else the register kernel with 2 rows per warp and 4 chunks in flight per row
+// (fastest measured on GB300 at K=4096, N=12288).  SDT_GEMV_VARIANT overrides: "dp2" (row-range kernel, 2 rows per
+// batch, either format), "dp4" / "dp8" (q8 integer kernel, rows per batch),
+// "stream1" / "stream2" (streaming kernel, warps per row), "stream" (its default
+// split), or "R,U" for the register kernel.
 static GemvVariant gemv_variant(bool q8) {
-    GemvVariant v{2, 4, 0, q8 ? 2 : 0};
+    GemvVariant v{2, 4, 0, 2};
     if (const char *s = getenv("SDT_GEMV_VARIANT")) {
         int r = 0, u = 0;
-        if (!strcmp(s, "dp2")) v.dp_rows = q8 ? 2 : 0;
-        else if (!strcmp(s, "dp4")) v.dp_rows = q8 ? 4 : 0;
-        else if (!strcmp(s, "dp8")) v.dp_rows = q8 ? 8 : 0;
+        if (!strcmp(s, "dp2")) v.rr_rows = 2;
+        else if (!strcmp(s, "dp4")) v.rr_rows = q8 ? 4 : 0;
+        else if (!strcmp(s, "dp8")) v.rr_rows = q8 ? 8 : 0;
         else if (!strcmp(s, "stream1")) v = GemvVariant{2, 4, 1, 0};
         else if (!strcmp(s, "stream2")) v = GemvVariant{2, 4, 2, 0};
         else if (!strcmp(s, "stream")) v = GemvVariant{2, 4, q8 ? 1 : 2, 0};
@@ -708,15 +842,15 @@ static GemvVariant gemv_variant(bool q8) {
 }
 
 // Bytes of its weight rows each decode CTA asks L2 for before waiting on the
-// previous kernel (SDT_GEMV_L2_PREFETCH_KB, default 8; 0 turns the prefetch off).
-// 8 KB per CTA (7 MB over the grid at K=4096) measured best on GB300: larger
-// prefetches compete with the previous kernel's last loads.
-static uint32_t gemv_l2_prefetch_bytes() {
+// previous kernel (SDT_GEMV_L2_PREFETCH_KB overrides; 0 turns the prefetch off).
+// Measured best on GB300 at K=4096, N=12288: 8 KB (two rows) for q8, 32 KB (four
+// rows) for bf16; larger prefetches compete with the previous kernel's last loads.
+static uint32_t gemv_l2_prefetch_bytes(uint32_t default_kb) {
     if (const char *s = getenv("SDT_GEMV_L2_PREFETCH_KB")) {
         const long kb = strtol(s, nullptr, 10);
         return kb > 0 ? uint32_t(std::min<long>(kb, 1 << 20) * 1024) : 0u;
     }
-    return 8u * 1024;
+    return default_kb * 1024;
 }
 
 // How many rows ahead of its register loads a decode CTA asks L2 for rows
@@ -750,7 +884,53 @@ static cudaError_t launch_q8_dp(int K, int N, const void *x, const void *W, cons
     const int grid = int(std::min<int64_t>(int64_t(occ) * dev.sm_count, N));
     return launch_kernel(kern, dim3(grid), dim3(T), 0, s, 1, K, N, static_cast<const uint4 *>(x),
                          static_cast<const uint8_t *>(W), static_cast<const __half *>(sc), y,
-                         gemv_l2_prefetch_bytes(), gemv_l2_ahead_rows(RB));
+                         gemv_l2_prefetch_bytes(8), gemv_l2_ahead_rows(RB));
+}
+
+// Launches the bf16 row-range kernel: T = ceil(U / GT) threads (U = K/16 units of
+// 32 bytes per row) rounded up to a warp, one CTA per resident slot on every SM.
+template <int GT, int RB, bool EF, int MINB>
+static cudaError_t launch_bf16_rows(int K, int N, const void *x, const void *W, float *y, cudaStream_t s,
+                                   const DeviceInfo &dev) {
+    auto kern = gemv_bf16_rows_kernel<GT, RB, EF, MINB>;
+    const int U = K / 16;
+    const int T = ((U + GT - 1) / GT + 31) / 32 * 32;
+    static std::atomic<int> occ_cache[64][kDpMaxThreads / 32];  // resident CTAs per SM, by device and T
+    if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+    std::atomic<int> &slot = occ_cache[dev.device][T / 32 - 1];
+    int occ = slot.load();
+    if (occ <= 0) {
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, T, 0);
+        if (e != cudaSuccess) return e;
+        if (occ < 1) occ = 1;
+        slot.store(occ);
+    }
+    const int grid = int(std::min<int64_t>(int64_t(occ) * dev.sm_count, N));
+    return launch_kernel(kern, dim3(grid), dim3(T), 0, s, 1, K, N, static_cast<const uint4 *>(x),
+                         static_cast<const uint8_t *>(W), y, gemv_l2_prefetch_bytes(32), gemv_l2_ahead_rows(RB));
+}
+
+// The bf16 row-range kernel takes K % 16 == 0 (whole 32-byte units), K <= 8192
+// (one or two units per thread) and 32-byte aligned weights; returns false to ask
+// for another kernel.
+static bool try_bf16_rows(int rows, int64_t K, int64_t N, const void *x, const void *W, float *y, cudaStream_t s,
+                          const DeviceInfo &dev, cudaError_t *err) {
+    if (rows != 2 || K % 16 || (reinterpret_cast<uintptr_t>(W) & 31)) return false;
+    const char *ef_env = getenv("SDT_GEMV_EVICT_FIRST");
+    const bool ef = !(ef_env && (!strcmp(ef_env, "0") || !strcmp(ef_env, "off")));
+    const int64_t U = K / 16;
+    const int k = int(K), n = int(N);
+    if (U <= kDpMaxThreads) {
+        *err = ef ? launch_bf16_rows<1, 2, true, 4>(k, n, x, W, y, s, dev)
+                  : launch_bf16_rows<1, 2, false, 4>(k, n, x, W, y, s, dev);
+        return true;
+    }
+    if (U <= 2 * kDpMaxThreads) {
+        *err = ef ? launch_bf16_rows<2, 2, true, 2>(k, n, x, W, y, s, dev)
+                  : launch_bf16_rows<2, 2, false, 2>(k, n, x, W, y, s, dev);
+        return true;
+    }
+    return false;
 }
 
 // The integer kernel takes up to 256 threads of 1 or 2 groups each (K <= 16384)
@@ -900,7 +1080,8 @@ static int gemv_impl(int64_t K, int64_t N, const void *x, const void *W, const v
         int *status = nullptr;
         rc = status_word(&status);
         if (rc) return rc;
-        if (!(q8 && try_q8_dp(v.dp_rows, K, N, x, W, scales, y, s, dev, &e)) &&
+        if (!(q8 && try_q8_dp(v.rr_rows, K, N, x, W, scales, y, s, dev, &e)) &&
+            !(!q8 && try_bf16_rows(v.rr_rows, K, N, x, W, y, s, dev, &e)) &&
             !try_stream(q8, v.stream_h, K, N, x, W, scales, y, s, dev, status, &e)) {
             if (!q8) SDT_GEMV_DISPATCH(e, launch_bf16, v, int(K / 8), int(N), x, W, y, s);
             else SDT_GEMV_DISPATCH(e, launch_q8, v, int(K / 16), int(N), x, W, scales, y, s);

@@ -157,3 +157,21 @@ def test_q8_nonfinite_activation_gives_nan(cuda_device):
     q, s = inputs.q8_weights(N, K, seed=102)
     y = sdt.gemv_m1(x.to(cuda_device), q.to(cuda_device), s.to(cuda_device)).cpu().numpy()
     assert not np.isfinite(y).any()
+
+
+@pytest.mark.parametrize("variant", ["dp2"], indirect=True)
+@pytest.mark.parametrize("K,N", [(16, 3), (48, 17), (4096, 12291), (4112, 65), (8192, 300), (4104, 33)])
+def test_ragged_bf16_row_range_kernel(cuda_device, variant, K, N):
+    # one unit, a ragged unit count, one and two units per thread; K % 16 != 0 falls back
+    x, W = bf16_case(K, N, 111)
+    y = sdt.gemv_m1(x.to(cuda_device), W.to(cuda_device)).cpu().numpy()
+    assert_close(y, oracle.gemv_bf16(u16(x), u16(W)), K, f"bf16 {variant} K={K} N={N}")
+
+
+@pytest.mark.parametrize("variant", ["dp2"], indirect=True)
+def test_bf16_row_range_integer_exact(cuda_device, variant):
+    K, N = 8192, 1000
+    x = inputs.integers((K,), seed=113, dtype=torch.bfloat16)
+    W = inputs.integers((N, K), seed=114, dtype=torch.bfloat16)
+    y = sdt.gemv_m1(x.to(cuda_device), W.to(cuda_device)).cpu().double().numpy()
+    assert np.array_equal(y, oracle.gemv_bf16(u16(x), u16(W)))
