@@ -428,6 +428,9 @@ def run_default(args):
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     e2e = run_e2e(args, dev, host, Wb_h, Q_h, stream)
 
+    # the decode protocol (after the timed region): 200 back-to-back launches x 10 repeats
+    dec_proto = decode_protocol(x, Wb, Wq, Sq, yb, peaks, stream) if rank == 0 else None
+
     if rank != 0:
         return
     value = aggregate_value(step_flops(), args.steps, world, max_s) / 1e12
@@ -446,7 +449,7 @@ def run_default(args):
     # dominant kernel: the largest share of the step, timed in every step
     shares = {n: statistics.mean(per[n]) for n in SWEEP}
     dom = SWEEP[dom_j]
-    assert dom == max(shares, key=shares.get)
+    largest_share = max(shares, key=shares.get)  # 4096 in every unprofiled run so far
     achieved = gemm_flops(dom, dom, dom) / (statistics.mean(dom_ms) / 1e3) / 1e12
     traffic = load_traffic(f"gemm_{dom}")
     clock = clocks.summary()
@@ -465,9 +468,11 @@ def run_default(args):
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "l2": "inputs larger than L2 (step working set %.0f MB, L2 129 MB)"
                    % (step_working_set() / 1e6), "parallelism": f"replicas x{world}"},
-        "timing": {"per_size_and_decode": f"instrumented steps (every {INSTR}th, events around every launch)",
+        "timing": {"per_size_and_decode": f"instrumented steps (every {INSTR}th, events around every launch; "
+                   "a decode launch there follows the GEMMs, so it cannot overlap a previous decode)",
                    "roofline": "events around the 4096^3 launch in every timed step"},
         "roofline": {"bound": "tensor", "kernel": f"gemm_f16 {dom}^3 ({tiles[dom]})",
+                     "largest_share_in_step": f"gemm_f16 {largest_share}^3",
                      "achieved": round(achieved, 1), "peak": peaks["tflops"], "unit": "TFLOP/s",
                      "frac": round(achieved / peaks["tflops"], 4), "peak_source": peaks["source"] + " bf16 burst",
                      "traffic": traffic},
@@ -475,8 +480,16 @@ def run_default(args):
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clock,
+        "roofline_decode": {
+            "bound": "hbm", "kernel": "gemv_m1 bf16 and q8, K=4096 N=12288 (decode protocol, best repeat)",
+            "achieved": {a: dec_proto[a]["gbs_best"] for a in ("bf16", "q8")}, "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": {a: round(dec_proto[a]["gbs_best"] / peaks["hbm_gbs"], 4) for a in ("bf16", "q8")},
+            "peak_source": peaks["source"] + " copy bandwidth",
+            "traffic": {a: load_traffic(f"gemv_{a}") for a in ("bf16", "q8")}},
         "per_size": per_size,
         "decode": dec,
+        "decode_protocol": dict(dec_proto, protocol="1 s warm, 200 graph-replayed launches x 10 repeats, "
+                                "8 rotating buffers, after the timed region"),
         "gate": gate,
     }
     print(json.dumps(out), flush=True)
@@ -488,31 +501,72 @@ def step_working_set():
     return gemm + dec
 
 
-def kernel_source_digest():
-    """Digest of the CUDA sources; recorded ncu traffic is stale once it changes."""
+SOURCES = {  # the CUDA sources each recorded kernel is built from
+    "gemm": lambda name: name.startswith("gemm") or name in ("ptx.cuh", "launch.cuh"),
+    "gemv": lambda name: name in ("gemv.cu", "ptx.cuh", "launch.cuh"),
+}
+
+
+def kernel_source_digest(kind="gemm"):
+    """Digest of the CUDA sources of one kernel family; recorded ncu traffic is stale once it changes."""
     import hashlib
 
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "shape_driven_tile_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
+        if name.endswith((".cu", ".cuh")) and SOURCES[kind](name):
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
+TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+
+
 def load_traffic(kernel_key):
     """DRAM bytes per launch from an ncu capture (profiles/traffic.json), or None when the
     record is missing or was taken on different kernel sources."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(path):
+    if not os.path.exists(TRAFFIC):
         return None
-    with open(path) as f:
+    with open(TRAFFIC) as f:
         t = json.load(f)
     e = t.get(kernel_key)
-    if not isinstance(e, dict) or e.get("source_digest") != kernel_source_digest():
+    kind = kernel_key.split("_")[0]
+    if not isinstance(e, dict) or kind not in SOURCES or e.get("source_digest") != kernel_source_digest(kind):
         return None
     return e.get("bytes")
+
+
+def record_traffic(args):
+    """Store the DRAM bytes of one launch from an ncu CSV (--metrics dram__bytes_read.sum,
+    dram__bytes_write.sum, one captured launch) under --key in profiles/traffic.json, with
+    the digest of the sources the kernel was built from."""
+    import csv
+
+    with open(args.ncu_csv) as f:
+        lines = [ln for ln in f if ln.startswith('"')]
+    rows = list(csv.DictReader(lines))
+    vals, kernel = {}, None
+    for r in rows:
+        name, unit, v = r.get("Metric Name"), r.get("Metric Unit", ""), r.get("Metric Value", "")
+        if name in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}.get(unit, 1)
+            vals[name] = float(v.replace(",", "")) * scale
+            kernel = r.get("Kernel Name")
+    if len(vals) != 2:
+        raise SystemExit(f"{args.ncu_csv}: no dram__bytes_read/write.sum rows")
+    t = {}
+    if os.path.exists(TRAFFIC):
+        with open(TRAFFIC) as f:
+            t = json.load(f)
+    kind = args.key.split("_")[0]
+    t[args.key] = {"bytes": int(round(vals["dram__bytes_read.sum"] + vals["dram__bytes_write.sum"])),
+                   "read": int(round(vals["dram__bytes_read.sum"])), "write": int(round(vals["dram__bytes_write.sum"])),
+                   "kernel": (kernel or "")[:120], "source_digest": kernel_source_digest(kind),
+                   "how": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one launch: " + args.ncu_csv}
+    with open(TRAFFIC, "w") as f:
+        json.dump(t, f, indent=1)
+    print(json.dumps({"mode": "record-traffic", args.key: t[args.key]}))
 
 
 def run_e2e(args, dev, host, Wb_h, Q_h, stream):
@@ -715,6 +769,55 @@ def run_kscan(args):
     print(json.dumps({"mode": "kscan", "tile": sdt.tile_info(tile)["name"], "rows": out}), flush=True)
 
 
+def decode_protocol(x, Wb, Wq, Sq, y, peaks, stream, warm_s=1.0, reps=10, launches=200):
+    """The decode protocol of the pages' workload: a warm-up of warm_s seconds, then `reps`
+    repeats of `launches` back-to-back launches (captured in a CUDA graph, cycling the
+    rotating weight buffers so every launch streams its weights from HBM), timed with
+    events on the launching stream.  Returns per arm the min/max per-launch time."""
+    import torch
+
+    import shape_driven_tile_gb300 as sdt
+
+    nb = len(Wb)
+    res = {}
+    for arm in ("bf16", "q8"):
+        def launch(i):
+            if arm == "bf16":
+                sdt.gemv_m1(x, Wb[i % nb], y=y)
+            else:
+                sdt.gemv_m1(x, Wq[i % nb], Sq[i % nb], y=y)
+        t_end = time.time() + warm_s
+        i = 0
+        while time.time() < t_end:
+            launch(i)
+            i += 1
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(stream)
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                for j in range(launches):
+                    launch(j)
+        torch.cuda.synchronize()
+        times = []
+        for r in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e3 / launches)
+        del g
+        nbytes = decode_bytes(DEC_K, DEC_N, arm)
+        res[arm] = {"us_min": round(min(times), 2), "us_max": round(max(times), 2),
+                    "gbs_best": round(nbytes / (min(times) / 1e6) / 1e9, 1),
+                    "pct_hbm_best": round(100 * nbytes / (min(times) / 1e6) / 1e9 / peaks["hbm_gbs"], 1),
+                    "bytes": nbytes}
+    return res
+
+
 def run_decode(args):
     """The decode protocol: 8 rotating buffers, warm-up, 200 timed launches, repeated 10 times."""
     import torch
@@ -729,42 +832,7 @@ def run_decode(args):
     Wq = [torch.randint(-127, 128, (DEC_N, DEC_K), device=dev, dtype=torch.int8) for _ in range(DEC_BUFFERS)]
     Sq = [(torch.rand((DEC_N, DEC_K // 32), device=dev) * 9e-3 + 1e-3).half() for _ in range(DEC_BUFFERS)]
     y = torch.empty(DEC_N, device=dev)
-    res = {}
-    for arm in ("bf16", "q8"):
-        def launch(i):
-            if arm == "bf16":
-                sdt.gemv_m1(x, Wb[i % DEC_BUFFERS], y=y)
-            else:
-                sdt.gemv_m1(x, Wq[i % DEC_BUFFERS], Sq[i % DEC_BUFFERS], y=y)
-        t_end = time.time() + 1.0
-        i = 0
-        while time.time() < t_end:
-            launch(i)
-            i += 1
-        torch.cuda.synchronize()
-        reps = []
-        for r in range(10):
-            # captured graph of 200 launches cycling the 8 buffers (no host launch gaps)
-            g = torch.cuda.CUDAGraph()
-            s = torch.cuda.Stream()
-            s.wait_stream(stream)
-            with torch.cuda.stream(s):
-                with torch.cuda.graph(g, stream=s):
-                    for j in range(200):
-                        launch(j)
-            torch.cuda.synchronize()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            g.replay()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            reps.append(e0.elapsed_time(e1) * 1e3 / 200)
-        nbytes = decode_bytes(DEC_K, DEC_N, arm)
-        res[arm] = {"us_min": round(min(reps), 2), "us_max": round(max(reps), 2),
-                    "gbs_best": round(nbytes / (min(reps) / 1e6) / 1e9, 1),
-                    "pct_hbm_best": round(100 * nbytes / (min(reps) / 1e6) / 1e9 / peaks["hbm_gbs"], 1),
-                    "bytes": nbytes}
+    res = decode_protocol(x, Wb, Wq, Sq, y, peaks, stream)
     sdt.check_device_status()
     print(json.dumps({"mode": "decode", "K": DEC_K, "N": DEC_N, "hbm_peak_gbs": peaks["hbm_gbs"],
                       "protocol": "1 s warm, 200 graph-replayed launches x 10 repeats, 8 rotating buffers",
@@ -905,7 +973,7 @@ def run_one(args):
     sdt.check_device_status()
     print(json.dumps({"mode": "one", "launches": args.warmup + args.reps,
                       "kernel": args.gemv or f"gemm {(args.sizes or [4096])[0]}^3 {args.tile or 'pick'}",
-                      "source_digest": kernel_source_digest()}), flush=True)
+                      "source_digest": kernel_source_digest("gemv" if args.gemv else "gemm")}), flush=True)
 
 
 def main(argv=None):
@@ -914,8 +982,10 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["sdt", "reference"], default="sdt")
-    ap.add_argument("--mode", choices=["step", "sweep", "kscan", "decode", "large", "one", "splitk", "chain"],
-                    default="step")
+    ap.add_argument("--mode", choices=["step", "sweep", "kscan", "decode", "large", "one", "splitk", "chain",
+                                       "record-traffic"], default="step")
+    ap.add_argument("--ncu-csv", help="record-traffic: ncu --csv log of one launch")
+    ap.add_argument("--key", help="record-traffic: gemm_4096, gemv_bf16 or gemv_q8")
     ap.add_argument("--gemv", choices=["bf16", "q8"])
     ap.add_argument("--reps", type=int, default=20)
     ap.add_argument("--sizes", type=int, nargs="*")
@@ -929,6 +999,8 @@ def main(argv=None):
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.mode == "record-traffic":
+        return record_traffic(args)
     {"step": run_default, "sweep": run_sweep, "kscan": run_kscan, "decode": run_decode,
      "large": run_large, "one": run_one, "splitk": run_splitk, "chain": run_chain}[args.mode](args)
 

@@ -103,6 +103,15 @@ int gemm_f16(int64_t M, int64_t N, int64_t K,
  * Requirements: x, W, y 16-byte aligned (scales 2-byte aligned); K a
  * multiple of 8 (bf16) or 32 (q8); K, N <= 2^30.  N == 0 is a no-op; K == 0
  * writes y = 0.
+ *
+ * Launched with programmatic dependent launch, the kernel may start while the
+ * previous kernel in `stream` is still running; before it waits for that
+ * kernel it only asks L2 for the first rows of W (a prefetch, which cannot
+ * observe stale data: L2 is where device memory is coherent), so results still
+ * reflect everything the previous kernel wrote to x, W and scales.  q8 sums
+ * each group exactly in int32 after scaling the group's activations to int16
+ * by a power of two (exact for activations within a factor 2^7 of the group's
+ * largest; otherwise off by at most 2^-15 of it).
  */
 int gemv_m1(int64_t K, int64_t N, const void *x, const void *W,
             const void *scales, float *y, sdt_stream_t stream);

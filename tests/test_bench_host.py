@@ -2,6 +2,7 @@
 bookkeeping (barrier, max over ranks, whole-job aggregate) on two gloo ranks."""
 import os
 import socket
+import types
 
 import pytest
 import torch.multiprocessing as mp
@@ -87,3 +88,22 @@ def test_two_rank_bookkeeping_gloo():
         assert w == 2
         assert mx == 2.5                  # the slowest rank's time
         assert val == 100.0 * 10 * 2 / 2.5  # units of all ranks / slowest time
+
+
+def test_record_traffic_and_staleness(tmp_path, monkeypatch):
+    # an ncu --csv log of one launch -> bytes per launch, tied to the kernel family's sources
+    csv_path = tmp_path / "t.csv"
+    csv_path.write_text(
+        "==PROF== Connected to process 1\n"
+        '"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream","Block Size",'
+        '"Grid Size","Device","CC","Section Name","Metric Name","Metric Unit","Metric Value"\n'
+        '"0","1","p","h","gemv_q8_dp2a_kernel","1","7","(128, 1, 1)","(1216, 1, 1)","0","10.3","s",'
+        '"dram__bytes_read.sum","Mbyte","53.51"\n'
+        '"0","1","p","h","gemv_q8_dp2a_kernel","1","7","(128, 1, 1)","(1216, 1, 1)","0","10.3","s",'
+        '"dram__bytes_write.sum","Kbyte","49.15"\n')
+    monkeypatch.setattr(bench, "TRAFFIC", str(tmp_path / "traffic.json"))
+    bench.record_traffic(types.SimpleNamespace(ncu_csv=str(csv_path), key="gemv_q8"))
+    assert bench.load_traffic("gemv_q8") == 53510000 + 49150
+    # a record taken on other sources is not used
+    monkeypatch.setattr(bench, "kernel_source_digest", lambda kind="gemm": "0" * 16)
+    assert bench.load_traffic("gemv_q8") is None
