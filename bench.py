@@ -848,6 +848,73 @@ def run_decode(args):
                       **res}), flush=True)
 
 
+def run_p4(args):
+    """The GEMM problem matrix of "Iteratively Tuning hipBLASLt TensileLite Kernels"
+    ("Experiment Setup": 24 shapes x fp16/bf16 x NN/TN) through gemm_ex with the
+    library's pick (one JSON line per problem: latency, tile, roofline fraction);
+    with --tune, the monotone coordinate descent of shape_driven_tile_gb300.tune from
+    that pick, the latency after every round (the page's Table 2 columns for this
+    library's rounds) and the per-round speedups (its Table 3)."""
+    import torch
+
+    import shape_driven_tile_gb300 as sdt
+    from shape_driven_tile_gb300 import inputs, tune
+
+    dev = torch.device("cuda", 0)
+    peaks = load_peaks()
+    names = set(args.shapes or [])
+    rows = []
+    for si, (name, M, N, K) in enumerate(inputs.P4_SHAPES):
+        if names and name not in names:
+            continue
+        for dtype in (torch.float16, torch.bfloat16):
+            for layout in ("NN", "TN"):
+                A_h, B_h = inputs.p4_operands(M, N, K, layout, seed=inputs.seed_for(6 + si, 0), dtype=dtype)
+                A = A_h.to(dev)
+                B = B_h.to(dev) if layout == "NN" else B_h.to(dev).t()
+                C = torch.empty((M, N), dtype=dtype, device=dev)
+                prob = tune.GemmProblem(A, B, C, reps=args.reps)
+                start = prob.start()
+                row = {"shape": name, "M": M, "N": N, "K": K, "dtype": "f16" if dtype == torch.float16 else "bf16",
+                       "layout": layout, "pick": sdt.tile_info(start["tile"])["name"]}
+                if args.tune:
+                    held, traj = prob.tune()
+                    row["rounds"] = {t["round"]: round(t["us"], 2) for t in traj}
+                    row["tuned"] = dict(held, tile=sdt.tile_info(held["tile"])["name"])
+                    row["speedup"] = round(traj[0]["us"] / traj[-1]["us"], 3)
+                    us = traj[-1]["us"]
+                else:
+                    us = prob.measure(start)
+                flops = gemm_flops(M, N, K)
+                nbytes = 2 * (M * K + K * N + M * N)
+                bound_us = max(flops / (peaks["tflops"] * 1e12), nbytes / (peaks["hbm_gbs"] * 1e9)) * 1e6
+                row.update({"us": round(us, 2), "tflops": round(flops / (us / 1e6) / 1e12, 1),
+                            "roofline_bound": "tensor" if flops / (peaks["tflops"] * 1e12) >= nbytes / (peaks["hbm_gbs"] * 1e9) else "hbm",
+                            "roofline_frac": round(bound_us / us, 3)})
+                rows.append(row)
+                print(json.dumps(row), flush=True)
+                del A, B, C, prob
+                torch.cuda.empty_cache()
+    sdt.check_device_status()
+    out = {"mode": "p4", "problems": len(rows), "timing": f"mean of {args.reps} launches, L2 flushed before each",
+           "roofline_frac_median": round(statistics.median(r["roofline_frac"] for r in rows), 3)}
+    if args.tune:
+        names_r = [k for k in rows[0]["rounds"] if k != "base"]
+        per_round = {}
+        for i, rn in enumerate(names_r):
+            prev = "base" if i == 0 else names_r[i - 1]
+            sp = [r["rounds"][prev] / r["rounds"][rn] for r in rows]
+            per_round[rn] = {"mean": round(statistics.mean(sp), 3), "median": round(statistics.median(sp), 3),
+                             "max": round(max(sp), 3)}
+        out["per_round_speedup"] = per_round
+        out["overall_speedup"] = {"mean": round(statistics.mean(r["speedup"] for r in rows), 3),
+                                  "median": round(statistics.median(r["speedup"] for r in rows), 3),
+                                  "max": round(max(r["speedup"] for r in rows), 3)}
+        out["monotone"] = all(all(b <= a for a, b in zip(list(r["rounds"].values()),
+                                                         list(r["rounds"].values())[1:])) for r in rows)
+    print(json.dumps(out), flush=True)
+
+
 def run_large(args):
     import torch
 
@@ -992,7 +1059,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["sdt", "reference"], default="sdt")
     ap.add_argument("--mode", choices=["step", "sweep", "kscan", "decode", "large", "one", "splitk", "chain",
-                                       "record-traffic"], default="step")
+                                       "record-traffic", "p4"], default="step")
+    ap.add_argument("--tune", action="store_true", help="p4: run the coordinate-descent tuner per problem")
     ap.add_argument("--ncu-csv", help="record-traffic: ncu --csv log of one launch")
     ap.add_argument("--key", help="record-traffic: gemm_4096, gemv_bf16 or gemv_q8")
     ap.add_argument("--gemv", choices=["bf16", "q8"])
@@ -1000,7 +1068,7 @@ def main(argv=None):
     ap.add_argument("--sizes", type=int, nargs="*")
     ap.add_argument("--tile")
     ap.add_argument("--with-kscan", action="store_true")
-    ap.add_argument("--shapes", nargs="*", help="extra GEMM shapes MxNxK for --mode sweep")
+    ap.add_argument("--shapes", nargs="*", help="extra GEMM shapes MxNxK for --mode sweep; shape names for --mode p4")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--e2e-steps", type=int, default=20)
     args = ap.parse_args(argv)
@@ -1011,7 +1079,7 @@ def main(argv=None):
     if args.mode == "record-traffic":
         return record_traffic(args)
     {"step": run_default, "sweep": run_sweep, "kscan": run_kscan, "decode": run_decode,
-     "large": run_large, "one": run_one, "splitk": run_splitk, "chain": run_chain}[args.mode](args)
+     "large": run_large, "one": run_one, "splitk": run_splitk, "chain": run_chain, "p4": run_p4}[args.mode](args)
 
 
 if __name__ == "__main__":

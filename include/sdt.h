@@ -266,6 +266,29 @@ int sdt_pick_splitk_for(int64_t M, int64_t N, int64_t K, int sm_count, int smem_
                         int *tile_id, int *splits);
 
 /*
+ * gemm_ex_splitk -- split-K in gemm_ex's general form [P4 "The Six Rounds",
+ * round 2, with the operands of P3 "Changes"]: caller row strides, either
+ * transposed operand, fp16 or bf16, and shapes no tile divides.  Arguments and
+ * requirements as gemm_ex, plus the split-K arguments of gemm_f16_splitk.
+ * The partial planes cover whole tiles: [splits][ceil(M/BM)*BM][ceil(N/BN)*BN]
+ * fp32, then one u32 counter per output tile; the workspace must hold
+ * sdt_splitk_ex_workspace_bytes(M,N,K,tile_id,splits) bytes (256-byte
+ * aligned; counters zero before the first SDT_SPLITK_IN_KERNEL call, as for
+ * gemm_f16_splitk).  The reduction writes only inside C (row stride ldc), in
+ * the operands' type.  tile_id < 0 picks with sdt_pick_splitk_any_for (then
+ * splits <= 0 takes the picked count).  Errors as gemm_ex and gemm_f16_splitk.
+ */
+int gemm_ex_splitk(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
+                   void *C, int64_t ldc, int dtype, int layout, void *workspace, size_t workspace_bytes,
+                   int tile_id, int splits, int algo, sdt_stream_t stream);
+/* Bytes of workspace gemm_ex_splitk needs for any shape (0 for a tile without split-K form,
+ * splits outside 1..ceil(K/64), or a non-positive dimension). */
+size_t sdt_splitk_ex_workspace_bytes(int64_t M, int64_t N, int64_t K, int tile_id, int splits);
+/* sdt_pick_splitk_for's model over the split-K tiles for any shape (tiles may overhang). */
+int sdt_pick_splitk_any_for(int64_t M, int64_t N, int64_t K, int sm_count, int smem_limit,
+                            int *tile_id, int *splits);
+
+/*
  * gemm_f16_splitk_noalloc -- gemm_f16_splitk (SDT_SPLITK_REDUCE_KERNEL) with its
  * workspace in a fixed 16 MiB array that the library holds in device memory,
  * so the call allocates nothing.  The pages have no counterpart; this is an

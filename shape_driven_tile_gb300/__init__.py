@@ -18,7 +18,8 @@ __all__ = [
     "feasible_tiles", "pick_tile", "seed_tile", "tile_info", "tiles", "tile_id",
     "load_tune_table", "clear_tune_table", "tune_table_lookup", "check_device_status",
     "debug_timeout_probe", "device_sm_count", "lib", "gemm_f16_splitk", "splitk_workspace",
-    "splitk_workspace_bytes", "pick_splitk", "SPLITK_REDUCE_KERNEL", "SPLITK_IN_KERNEL", "gemm_ex",
+    "splitk_workspace_bytes", "pick_splitk", "pick_tile_any", "gemm_ex_splitk",
+    "splitk_ex_workspace_bytes", "pick_splitk_any", "SPLITK_REDUCE_KERNEL", "SPLITK_IN_KERNEL", "gemm_ex",
 ]
 
 
@@ -133,9 +134,8 @@ def _layout_of(T, name):
     raise ValueError(f"{name} needs unit stride in one dimension (row-major or transposed row-major)")
 
 
-def gemm_ex(A, B, C=None, *, tile=-1, stream=None):
-    """C = A @ B for fp16 or bf16 views of any shape: A [M, K] and B [K, N] may be row-major
-    (padded rows allowed) or transposed views (e.g. X.t()); C [M, N] row-major, padding allowed."""
+def _ex_args(A, B, C):
+    """(M, N, K, lda, ldb, ldc, layout, C) of gemm_ex-style views."""
     if A.dtype not in DTYPE_CODES or B.dtype != A.dtype:
         raise TypeError("A and B must both be float16 or both bfloat16")
     if not (A.is_cuda and B.is_cuda):
@@ -151,8 +151,15 @@ def gemm_ex(A, B, C=None, *, tile=-1, stream=None):
     elif C.dtype != A.dtype or tuple(C.shape) != (M, N) or (C.stride(1) != 1 and N > 1):
         raise ValueError(f"C must be a row-major {A.dtype} [{M}, {N}] view")
     ldc = C.stride(0) if M > 1 else max(C.stride(0), N)
-    tid = tile_id(tile) if isinstance(tile, str) else int(tile)
     layout = (LAYOUT_A_T if a_t else 0) | (LAYOUT_B_T if b_t else 0)
+    return M, N, K, lda, ldb, ldc, layout, C
+
+
+def gemm_ex(A, B, C=None, *, tile=-1, stream=None):
+    """C = A @ B for fp16 or bf16 views of any shape: A [M, K] and B [K, N] may be row-major
+    (padded rows allowed) or transposed views (e.g. X.t()); C [M, N] row-major, padding allowed."""
+    M, N, K, lda, ldb, ldc, layout, C = _ex_args(A, B, C)
+    tid = tile_id(tile) if isinstance(tile, str) else int(tile)
     check(lib().gemm_ex(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, C.data_ptr(), ldc, DTYPE_CODES[A.dtype],
                         layout, tid, _stream(stream)))
     return C
@@ -190,6 +197,33 @@ def gemm_f16_splitk(A, B, C=None, *, workspace, tile=-1, splits: int = 0,
     check(lib().gemm_f16_splitk(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(), workspace.data_ptr(), nbytes,
                                 tid, int(splits), int(algo), _stream(stream)))
     return C
+
+
+def splitk_ex_workspace_bytes(M: int, N: int, K: int, tile, splits: int) -> int:
+    tid = tile_id(tile) if isinstance(tile, str) else int(tile)
+    return int(lib().sdt_splitk_ex_workspace_bytes(M, N, K, tid, int(splits)))
+
+
+def gemm_ex_splitk(A, B, C=None, *, workspace, tile=-1, splits: int = 0, algo: int = SPLITK_REDUCE_KERNEL,
+                   stream=None):
+    """Split-K form of gemm_ex (same views); `workspace` as for gemm_f16_splitk, sized by
+    splitk_ex_workspace_bytes."""
+    M, N, K, lda, ldb, ldc, layout, C = _ex_args(A, B, C)
+    tid = tile_id(tile) if isinstance(tile, str) else int(tile)
+    if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda:
+        raise TypeError("workspace must be a CUDA tensor")
+    nbytes = workspace.numel() * workspace.element_size()
+    check(lib().gemm_ex_splitk(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, C.data_ptr(), ldc,
+                               DTYPE_CODES[A.dtype], layout, workspace.data_ptr(), nbytes, tid, int(splits),
+                               int(algo), _stream(stream)))
+    return C
+
+
+def pick_splitk_any(M: int, N: int, K: int, sm_count: int = 152, smem_limit: int = 232448):
+    t, sp = ctypes.c_int(0), ctypes.c_int(0)
+    check(lib().sdt_pick_splitk_any_for(M, N, K, int(sm_count), int(smem_limit), ctypes.byref(t),
+                                        ctypes.byref(sp)))
+    return t.value, sp.value
 
 
 def pick_splitk(M: int, N: int, K: int, sm_count: int = 152, smem_limit: int = 232448):
@@ -233,6 +267,14 @@ def pick_tile(M: int, N: int, K: int, sm_count: int | None = None, smem_limit: i
         return check(lib().sdt_pick_tile(M, N, K))
     return check(lib().sdt_pick_tile_for(M, N, K, int(sm_count),
                                          int(smem_limit) if smem_limit is not None else 232448))
+
+
+def pick_tile_any(M: int, N: int, K: int, sm_count: int | None = None, smem_limit: int | None = None) -> int:
+    """The tile gemm_ex picks for any shape (tiles may overhang ragged edges)."""
+    if sm_count is None:
+        sm_count, smem_limit = device_sm_count(), lib().sdt_device_smem_optin()
+    return check(lib().sdt_pick_tile_any_for(M, N, K, int(sm_count),
+                                             int(smem_limit) if smem_limit is not None else 232448))
 
 
 def seed_tile(M: int, N: int, units: int) -> int:

@@ -31,10 +31,15 @@ namespace sdt {
 
 using LaunchFn = int (*)(const CUtensorMap &, const CUtensorMap &, const GemmArgs &, cudaStream_t);
 
-// Split-K launchers of the one-CTA-per-tile ladder rungs, in ladder order (null: no split-K form).
-static const LaunchFn kSplitLaunch[] = {
-    &launch_gemm_tile_split<64, 64>, &launch_gemm_tile_split<64, 128>, &launch_gemm_tile_split<128, 64>,
-    &launch_gemm_tile_split<128, 128>, &launch_gemm_tile_split<128, 256>, nullptr, nullptr, nullptr, nullptr};
+// Split-K launchers of the one-CTA-per-tile ladder rungs, in ladder order, per operand
+// layout (null: no split-K form).
+#define SDT_SPLIT4_(BM, BN)                                                                        \
+    {&launch_gemm_tile_split<BM, BN, 0>, &launch_gemm_tile_split<BM, BN, 1>,                       \
+     &launch_gemm_tile_split<BM, BN, 2>, &launch_gemm_tile_split<BM, BN, 3>}
+static const LaunchFn kSplitLaunch[][4] = {
+    SDT_SPLIT4_(64, 64),   SDT_SPLIT4_(64, 128),  SDT_SPLIT4_(128, 64),  SDT_SPLIT4_(128, 128),
+    SDT_SPLIT4_(128, 256), {nullptr, nullptr, nullptr, nullptr},     {nullptr, nullptr, nullptr, nullptr},
+    {nullptr, nullptr, nullptr, nullptr},         {nullptr, nullptr, nullptr, nullptr}};
 
 // One rung of the tile ladder.  kt_cycles / fixed_cycles feed pick_tile's cost
 // model: SM cycles one CTA of this tile spends per 64-deep k-tile when it has
@@ -146,8 +151,10 @@ static double model_us(const LadderTile &t, int64_t M, int64_t N, int64_t K, int
     if (t.persistent) {
         const double workers = t.cta_group == 2 ? double(sm_count / 2) : double(sm_count);
         double rounds = std::ceil(tiles / workers);
-        if (t.cta_group == 2 && t.BN == 256) {
+        if (t.cta_group == 2 && t.BN == 256 && tiles >= workers) {
             // a tail of at most half the workers runs as half-width items in half a round
+            // (after at least one full round: a grid that is all tail keeps the full
+            // k-loop per item, which the fit does not cover)
             const double tail = tiles - std::floor(tiles / workers) * workers;
             if (tail > 0 && 2 * tail <= workers) rounds -= 0.5;
         }
@@ -380,23 +387,21 @@ static uint32_t idesc_flags_for(int dtype, int layout) {
 
 // ---- launch ----------------------------------------------------------------------
 
-__global__ void splitk_reduce_kernel(const float *__restrict__ partials, __half *__restrict__ C, size_t elems,
-                                     int splits) {
-    const size_t stride = size_t(gridDim.x) * blockDim.x * 8;
-    for (size_t i = (size_t(blockIdx.x) * blockDim.x + threadIdx.x) * 8; i < elems; i += stride) {
-        float4 a0 = __ldg(reinterpret_cast<const float4 *>(partials + i));
-        float4 a1 = __ldg(reinterpret_cast<const float4 *>(partials + i + 4));
+__global__ void splitk_reduce_kernel(const float *__restrict__ partials, uint16_t *__restrict__ C, int64_t M,
+                                     int64_t N, int64_t Mp, int64_t Np, int64_t ldc, int splits, int bf16) {
+    const int64_t vecs = N / 8, total = M * vecs, plane = Mp * Np;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t r = i / vecs, c = (i % vecs) * 8;
+        const float *src = partials + r * Np + c;
+        float4 a0 = __ldg(reinterpret_cast<const float4 *>(src));
+        float4 a1 = __ldg(reinterpret_cast<const float4 *>(src + 4));
         for (int sp = 1; sp < splits; ++sp) {
-            const float4 b0 = __ldg(reinterpret_cast<const float4 *>(partials + sp * elems + i));
-            const float4 b1 = __ldg(reinterpret_cast<const float4 *>(partials + sp * elems + i + 4));
+            const float4 b0 = __ldg(reinterpret_cast<const float4 *>(src + sp * plane));
+            const float4 b1 = __ldg(reinterpret_cast<const float4 *>(src + sp * plane + 4));
             a0.x += b0.x; a0.y += b0.y; a0.z += b0.z; a0.w += b0.w;
             a1.x += b1.x; a1.y += b1.y; a1.z += b1.z; a1.w += b1.w;
         }
-        __half2 h0 = __floats2half2_rn(a0.x, a0.y), h1 = __floats2half2_rn(a0.z, a0.w);
-        __half2 h2 = __floats2half2_rn(a1.x, a1.y), h3 = __floats2half2_rn(a1.z, a1.w);
-        *reinterpret_cast<uint4 *>(C + i) =
-            make_uint4(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1),
-                       *reinterpret_cast<uint32_t *>(&h2), *reinterpret_cast<uint32_t *>(&h3));
+        *reinterpret_cast<uint4 *>(C + r * ldc + c) = pack8_f32(a0, a1, bf16 != 0);
     }
 }
 
@@ -594,10 +599,10 @@ static int gemm_dispatch(int64_t M, int64_t N, int64_t K, const void *A, const v
 
 static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Workspace layout: fp32 partials [splits][M][N], padded to 256 bytes, then one
-// u32 arrival counter per output tile.
-static size_t splitk_partials_bytes(int64_t M, int64_t N, int splits) {
-    return (size_t(splits) * size_t(M) * size_t(N) * 4 + 255) / 256 * 256;
+// Workspace layout: fp32 partials [splits][Mp][Np] (M and N rounded up to whole
+// tiles), padded to 256 bytes, then one u32 arrival counter per output tile.
+static size_t splitk_partials_bytes(int64_t Mp, int64_t Np, int splits) {
+    return (size_t(splits) * size_t(Mp) * size_t(Np) * 4 + 255) / 256 * 256;
 }
 
 static int splitk_effective(int64_t nK, int splits) {
@@ -606,7 +611,15 @@ static int splitk_effective(int64_t nK, int splits) {
 }
 
 static bool splitk_tile_ok(int tile_id) {
-    return tile_id >= 0 && tile_id < kNumTiles && kSplitLaunch[tile_id] != nullptr;
+    return tile_id >= 0 && tile_id < kNumTiles && kSplitLaunch[tile_id][0] != nullptr;
+}
+
+// Workspace bytes of split-K with tile t on any shape (0 for an invalid combination).
+static size_t splitk_ws_bytes(const LadderTile &t, int64_t M, int64_t N, int64_t K, int splits) {
+    const int64_t nK = ceil_div(K, kBK);
+    if (M <= 0 || N <= 0 || K <= 0 || splits < 1 || splits > nK) return 0;
+    const int64_t mt = ceil_div(M, t.BM), nt = ceil_div(N, t.BN);
+    return splitk_partials_bytes(mt * t.BM, nt * t.BN, splitk_effective(nK, splits)) + size_t(mt * nt) * 4;
 }
 
 static bool splitk_feasible(const LadderTile &t, int64_t M, int64_t N, int64_t K, int smem_limit) {
@@ -619,8 +632,8 @@ static bool splitk_feasible(const LadderTile &t, int64_t M, int64_t N, int64_t K
 // CTAs = tiles x splits, plus the reduction's fp32 traffic (written once, read once).
 static double splitk_model_us(const LadderTile &t, int64_t M, int64_t N, int64_t K, int splits, int sm_count,
                               int smem_per_sm) {
-    const double tiles = double(M / t.BM) * double(N / t.BN) * splits;
-    const double kps = double(ceil_div(K / kBK, splits));
+    const double tiles = double(ceil_div(M, t.BM)) * double(ceil_div(N, t.BN)) * splits;
+    const double kps = double(ceil_div(ceil_div(K, kBK), splits));
     const int occ = ctas_per_sm(t, smem_per_sm);
     const double rounds = std::ceil(tiles / (double(sm_count) * occ));
     double us = rounds * (t.fixed_us + std::max(0.0, kps - t.stages) * t.kt_us);
@@ -652,6 +665,71 @@ static int pick_splitk_for(int64_t M, int64_t N, int64_t K, int sm_count, int sm
     return SDT_OK;
 }
 
+// Launches split-K with tile `tile_id` (which has a split-K form and fits on chip)
+// on validated, non-empty operands with K > 0; any shape (tiles overhang ragged
+// edges: the TMA reads zeros outside the operands, the partial planes are whole
+// tiles, the reduction writes only inside C), either layout bit, fp16 or bf16.
+static int splitk_launch_ex(int tile_id, int splits, int algo, int64_t M, int64_t N, int64_t K, const void *A,
+                            int64_t lda, const void *B, int64_t ldb, void *C, int64_t ldc, int dtype, int layout,
+                            void *ws, size_t ws_bytes, cudaStream_t stream, const DeviceInfo &dev) {
+    const LadderTile &t = kLadder[tile_id];
+    const int64_t nK = ceil_div(K, kBK);
+    if (splits < 1 || splits > nK) return fail(SDT_ERR_ARG, "splits must be in 1..%lld", (long long)nK);
+    splits = splitk_effective(nK, splits);
+    const int64_t mt = ceil_div(M, t.BM), nt = ceil_div(N, t.BN);
+    if (mt * nt > int64_t(0x3fffffff)) return fail(SDT_ERR_SHAPE, "grid too large");
+    const size_t need = splitk_ws_bytes(t, M, N, K, splits);
+    if (!ws) return fail(SDT_ERR_NULL, "split-K needs a workspace");
+    if (reinterpret_cast<uintptr_t>(ws) & 255) return fail(SDT_ERR_ALIGN, "the workspace must be 256-byte aligned");
+    if (ws_bytes < need)
+        return fail(SDT_ERR_ARG, "workspace of %zu bytes is smaller than the %zu bytes needed", ws_bytes, need);
+    CUtensorMap tmA, tmB;
+    int rc = operand_maps(A, lda, B, ldb, M, N, K, dtype, layout, t.BM, &tmA, &tmB);
+    if (rc) return rc;
+    int *status = nullptr;
+    rc = status_word(&status);
+    if (rc) return rc;
+    GemmArgs a;
+    memset(&a, 0, sizeof a);
+    a.ldc = int(ldc);
+    a.idesc_flags = idesc_flags_for(dtype, layout);
+    a.C = static_cast<__half *>(C);
+    a.M = int(M);
+    a.N = int(N);
+    a.K = int(K);
+    a.num_m_tiles = int(mt);
+    a.num_n_tiles = int(nt);
+    a.num_k_tiles = int(nK);
+    a.stages = tile_stages(t, dev.smem_optin);
+    a.stagger = 0;
+    a.stagger_stride = 1;
+    a.raster_group = env_int("SDT_RASTER_GROUP", 8, 1, 1 << 20);
+    a.timeout_ns = wait_timeout_ns();
+    a.status = status;
+    a.max_ctas = dev.sm_count * ctas_per_sm(t, dev.smem_per_sm);
+    a.splits = splits;
+    a.k_per_split = int(ceil_div(nK, splits));
+    a.splitk_reduce_in_kernel = algo == SDT_SPLITK_IN_KERNEL ? 1 : 0;
+    a.partials = static_cast<float *>(ws);
+    a.counters = reinterpret_cast<unsigned *>(static_cast<char *>(ws) +
+                                              splitk_partials_bytes(mt * t.BM, nt * t.BN, splits));
+    int e = kSplitLaunch[tile_id][layout & 3](tmA, tmB, a, stream);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(SDT_ERR_LAUNCH, "split-K launch of tile %s failed: %s", t.name, cudaGetErrorString(cudaError_t(e)));
+    }
+    if (algo == SDT_SPLITK_REDUCE_KERNEL) {
+        const int64_t total = M * (N / 8);
+        const unsigned blocks = unsigned(std::min<int64_t>((total + 255) / 256, int64_t(dev.sm_count) * 8));
+        splitk_reduce_kernel<<<blocks, 256, 0, stream>>>(a.partials, static_cast<uint16_t *>(C), M, N, mt * t.BM,
+                                                         nt * t.BN, ldc, splits, dtype == SDT_DTYPE_BF16 ? 1 : 0);
+        cudaError_t e2 = cudaGetLastError();
+        if (e2 != cudaSuccess) return fail(SDT_ERR_LAUNCH, "split-K reduction launch failed: %s", cudaGetErrorString(e2));
+    }
+    return SDT_OK;
+}
+
+// gemm_f16_splitk: tight row-major fp16, the tile must divide the shape.
 static int splitk_run(int64_t M, int64_t N, int64_t K, const void *A, const void *B, void *C, void *ws,
                       size_t ws_bytes, int tile_id, int splits, int algo, cudaStream_t stream) {
     int rc = validate_common(M, N, K, A, B, C);
@@ -674,61 +752,38 @@ static int splitk_run(int64_t M, int64_t N, int64_t K, const void *A, const void
     if (!splitk_feasible(t, M, N, K, dev.smem_optin))
         return fail(SDT_ERR_TILE, "tile %s does not divide %lldx%lldx%lld", t.name, (long long)M, (long long)N,
                     (long long)K);
-    const int64_t nK = K / kBK;
-    if (splits < 1 || splits > nK) return fail(SDT_ERR_ARG, "splits must be in 1..%lld", (long long)nK);
-    splits = splitk_effective(nK, splits);
-    const int64_t tiles = (M / t.BM) * (N / t.BN);
-    const size_t need = splitk_partials_bytes(M, N, splits) + size_t(tiles) * 4;
-    if (!ws) return fail(SDT_ERR_NULL, "split-K needs a workspace");
-    if (reinterpret_cast<uintptr_t>(ws) & 255) return fail(SDT_ERR_ALIGN, "the workspace must be 256-byte aligned");
-    if (ws_bytes < need)
-        return fail(SDT_ERR_ARG, "workspace of %zu bytes is smaller than the %zu bytes needed", ws_bytes, need);
-    CUtensorMap tmA, tmB;
-    rc = operand_maps(A, K, B, N, M, N, K, SDT_DTYPE_F16, 0, t.BM, &tmA, &tmB);
-    if (rc) return rc;
-    int *status = nullptr;
-    rc = status_word(&status);
-    if (rc) return rc;
-    GemmArgs a;
-    memset(&a, 0, sizeof a);
-    a.ldc = int(N);
-    a.idesc_flags = idesc_flags_for(SDT_DTYPE_F16, 0);
-    a.C = static_cast<__half *>(C);
-    a.M = int(M);
-    a.N = int(N);
-    a.K = int(K);
-    a.num_m_tiles = int(M / t.BM);
-    a.num_n_tiles = int(N / t.BN);
-    a.num_k_tiles = int(nK);
-    a.stages = tile_stages(t, dev.smem_optin);
-    a.stagger = 0;
-    a.stagger_stride = 1;
-    a.raster_group = env_int("SDT_RASTER_GROUP", 8, 1, 1 << 20);
-    a.timeout_ns = wait_timeout_ns();
-    a.status = status;
-    a.max_ctas = dev.sm_count * ctas_per_sm(t, dev.smem_per_sm);
-    a.splits = splits;
-    a.k_per_split = int(ceil_div(nK, splits));
-    a.splitk_reduce_in_kernel = algo == SDT_SPLITK_IN_KERNEL ? 1 : 0;
-    a.partials = static_cast<float *>(ws);
-    a.counters = reinterpret_cast<unsigned *>(static_cast<char *>(ws) + splitk_partials_bytes(M, N, splits));
-    int e = kSplitLaunch[tile_id](tmA, tmB, a, stream);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return fail(SDT_ERR_LAUNCH, "split-K launch of tile %s failed: %s", t.name, cudaGetErrorString(cudaError_t(e)));
+    return splitk_launch_ex(tile_id, splits, algo, M, N, K, A, K, B, N, C, N, SDT_DTYPE_F16, 0, ws, ws_bytes, stream,
+                            dev);
+}
+
+// (tile, splits) for split-K on any shape: the split-K cost model over the tiles
+// with a split-K form that fit on chip (tiles may overhang ragged edges).
+static int pick_splitk_any(int64_t M, int64_t N, int64_t K, int sm_count, int smem_limit, int smem_per_sm,
+                           int *tile_out, int *splits_out) {
+    double best = 0.0;
+    int bt = -1, bs = 1;
+    const int64_t nK = ceil_div(K, kBK);
+    for (int i = 0; i < kNumTiles; ++i) {
+        if (!splitk_tile_ok(i) || !kLadder[i].candidate || !fits_chip(kLadder[i], smem_limit)) continue;
+        for (int sp = 1; sp <= 32 && sp <= nK; ++sp) {
+            if (splitk_effective(nK, sp) != sp) continue;
+            const double c = splitk_model_us(kLadder[i], M, N, K, sp, sm_count, smem_per_sm);
+            if (bt < 0 || c < best * (1.0 - 1e-9)) {
+                best = c;
+                bt = i;
+                bs = sp;
+            }
+        }
     }
-    if (algo == SDT_SPLITK_REDUCE_KERNEL) {
-        const size_t elems = size_t(M) * size_t(N);
-        const unsigned blocks = unsigned(std::min<size_t>((elems / 8 + 255) / 256, size_t(dev.sm_count) * 8));
-        splitk_reduce_kernel<<<blocks, 256, 0, stream>>>(a.partials, a.C, elems, splits);
-        cudaError_t e2 = cudaGetLastError();
-        if (e2 != cudaSuccess) return fail(SDT_ERR_LAUNCH, "split-K reduction launch failed: %s", cudaGetErrorString(e2));
-    }
+    if (bt < 0) return fail(SDT_ERR_TILE, "no split-K tile fits this device");
+    *tile_out = bt;
+    *splits_out = bs;
     return SDT_OK;
 }
 
-static int gemm_ex_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
-                        void *C, int64_t ldc, int dtype, int layout, int tile_id, cudaStream_t stream) {
+// Argument checks of gemm_ex and gemm_ex_splitk (SDT_OK also for empty shapes).
+static int validate_ex(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
+                       void *C, int64_t ldc, int dtype, int layout) {
     if (M < 0 || N < 0 || K < 0)
         return fail(SDT_ERR_SHAPE, "negative dimension (M=%lld N=%lld K=%lld)", (long long)M, (long long)N,
                     (long long)K);
@@ -748,21 +803,55 @@ static int gemm_ex_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t 
         if (lda < a_inner || lda % 8) return fail(SDT_ERR_ARG, "lda must be >= %lld and a multiple of 8", (long long)a_inner);
         if (ldb < b_inner || ldb % 8) return fail(SDT_ERR_ARG, "ldb must be >= %lld and a multiple of 8", (long long)b_inner);
     }
+    return SDT_OK;
+}
+
+// C = 0 for K == 0 (the empty sum), row stride ldc.
+static int zero_c(int64_t M, int64_t N, void *C, int64_t ldc, cudaStream_t stream, const DeviceInfo &dev) {
+    const int64_t total = M * (N / 8);
+    const unsigned blocks = unsigned(std::min<int64_t>((total + 255) / 256, int64_t(dev.sm_count) * 8));
+    zero_fill_2d<<<blocks, 256, 0, stream>>>(static_cast<uint16_t *>(C), M, N, ldc);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? SDT_OK : fail(SDT_ERR_LAUNCH, "zero fill failed: %s", cudaGetErrorString(e));
+}
+
+static int gemm_ex_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
+                        void *C, int64_t ldc, int dtype, int layout, int tile_id, cudaStream_t stream) {
+    int rc = validate_ex(M, N, K, A, lda, B, ldb, C, ldc, dtype, layout);
+    if (rc || M == 0 || N == 0) return rc;
     if (tile_id < -1 || tile_id >= kNumTiles) return fail(SDT_ERR_TILE, "unknown tile id %d", tile_id);
     DeviceInfo dev;
-    int rc = current_device(&dev);
+    rc = current_device(&dev);
     if (rc) return rc;
-    if (K == 0) {
-        const int64_t total = M * (N / 8);
-        const unsigned blocks = unsigned(std::min<int64_t>((total + 255) / 256, int64_t(dev.sm_count) * 8));
-        zero_fill_2d<<<blocks, 256, 0, stream>>>(static_cast<uint16_t *>(C), M, N, ldc);
-        cudaError_t e = cudaGetLastError();
-        return e == cudaSuccess ? SDT_OK : fail(SDT_ERR_LAUNCH, "zero fill failed: %s", cudaGetErrorString(e));
-    }
+    if (K == 0) return zero_c(M, N, C, ldc, stream, dev);
     if (tile_id < 0) tile_id = pick_any(M, N, K, dev.sm_count, dev.smem_optin, dev.smem_per_sm);
     if (tile_id < 0 || !fits_chip(kLadder[tile_id], dev.smem_optin))
         return fail(SDT_ERR_TILE, "no tile fits this device");
     return run_tile_ex(tile_id, -1, M, N, K, A, lda, B, ldb, C, ldc, dtype, layout, stream, dev);
+}
+
+static int gemm_ex_splitk_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+                               int64_t ldb, void *C, int64_t ldc, int dtype, int layout, void *ws, size_t ws_bytes,
+                               int tile_id, int splits, int algo, cudaStream_t stream) {
+    int rc = validate_ex(M, N, K, A, lda, B, ldb, C, ldc, dtype, layout);
+    if (rc || M == 0 || N == 0) return rc;
+    if (algo != SDT_SPLITK_REDUCE_KERNEL && algo != SDT_SPLITK_IN_KERNEL)
+        return fail(SDT_ERR_ARG, "unknown split-K algorithm %d", algo);
+    if (tile_id < -1 || tile_id >= kNumTiles) return fail(SDT_ERR_TILE, "unknown tile id %d", tile_id);
+    DeviceInfo dev;
+    rc = current_device(&dev);
+    if (rc) return rc;
+    if (K == 0) return zero_c(M, N, C, ldc, stream, dev);
+    if (tile_id < 0) {
+        int sp = 1;
+        rc = pick_splitk_any(M, N, K, dev.sm_count, dev.smem_optin, dev.smem_per_sm, &tile_id, &sp);
+        if (rc) return rc;
+        if (splits <= 0) splits = sp;
+    }
+    if (!splitk_tile_ok(tile_id)) return fail(SDT_ERR_TILE, "tile %d has no split-K form", tile_id);
+    if (!fits_chip(kLadder[tile_id], dev.smem_optin)) return fail(SDT_ERR_TILE, "tile %d does not fit", tile_id);
+    return splitk_launch_ex(tile_id, splits, algo, M, N, K, A, lda, B, ldb, C, ldc, dtype, layout, ws, ws_bytes,
+                            stream, dev);
 }
 
 // Entry for other translation units of the library (the no-allocation variant):
@@ -931,6 +1020,28 @@ int sdt_pick_splitk_for(int64_t M, int64_t N, int64_t K, int sm_count, int smem_
     if (!tile_id || !splits) return fail(SDT_ERR_NULL, "tile_id and splits must not be NULL");
     if (sm_count <= 0) return fail(SDT_ERR_ARG, "sm_count must be positive");
     return pick_splitk_for(M, N, K, sm_count, smem_limit, 233472, tile_id, splits);
+}
+
+int gemm_ex_splitk(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb, void *C,
+                   int64_t ldc, int dtype, int layout, void *workspace, size_t workspace_bytes, int tile_id, int splits,
+                   int algo, sdt_stream_t stream) {
+    clear_error();
+    return gemm_ex_splitk_impl(M, N, K, A, lda, B, ldb, C, ldc, dtype, layout, workspace, workspace_bytes, tile_id,
+                               splits, algo, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t sdt_splitk_ex_workspace_bytes(int64_t M, int64_t N, int64_t K, int tile_id, int splits) {
+    clear_error();
+    if (!splitk_tile_ok(tile_id)) return 0;
+    return splitk_ws_bytes(kLadder[tile_id], M, N, K, splits);
+}
+
+int sdt_pick_splitk_any_for(int64_t M, int64_t N, int64_t K, int sm_count, int smem_limit, int *tile_id,
+                            int *splits) {
+    clear_error();
+    if (!tile_id || !splits) return fail(SDT_ERR_NULL, "tile_id and splits must not be NULL");
+    if (sm_count <= 0 || M <= 0 || N <= 0 || K <= 0) return fail(SDT_ERR_ARG, "dimensions and sm_count must be positive");
+    return pick_splitk_any(M, N, K, sm_count, smem_limit, 233472, tile_id, splits);
 }
 
 int gemm_f16_splitk(int64_t M, int64_t N, int64_t K, const void *A, const void *B, void *C, void *workspace,

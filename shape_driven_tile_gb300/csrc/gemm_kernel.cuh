@@ -55,7 +55,7 @@ struct GemmArgs {
     int splits;
     int k_per_split;
     int splitk_reduce_in_kernel;  // 1: the last CTA of a tile sums the partials and writes C
-    float *partials;      // [splits][M][N] fp32
+    float *partials;      // [splits][num_m_tiles*BM][num_n_tiles*BN] fp32
     unsigned *counters;   // [num_m_tiles * num_n_tiles], zero between calls
     // two-CTA tiles: work items [0, tail_start) are whole tiles, items
     // [tail_start, num_items) are column halves of tiles tail_start ... (two per tile)
@@ -135,6 +135,23 @@ __device__ __forceinline__ void store_row32(void *crow, const uint32_t (&r)[32],
 #pragma unroll
     for (int v = 0; v < 4; ++v)
         if (8 * v + 8 <= ncols) dst[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
+}
+
+// Eight fp32 values -> eight fp16 or bf16 (round to nearest even), packed for one 16-byte store.
+__device__ __forceinline__ uint4 pack8_f32(const float4 &a, const float4 &b, bool bf16) {
+    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t h[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        if (bf16) {
+            __nv_bfloat162 x = __floats2bfloat162_rn(v[2 * t], v[2 * t + 1]);
+            h[t] = *reinterpret_cast<uint32_t *>(&x);
+        } else {
+            __half2 x = __floats2half2_rn(v[2 * t], v[2 * t + 1]);
+            h[t] = *reinterpret_cast<uint32_t *>(&x);
+        }
+    }
+    return make_uint4(h[0], h[1], h[2], h[3]);
 }
 
 template <int BM, int BN>
@@ -291,7 +308,10 @@ __global__ void __launch_bounds__(128, 1)
         const uint32_t taddr_row = tmem_d + (static_cast<uint32_t>(warp * 32) << 16);
         const bool bf16 = ((p.idesc_flags >> 7) & 7u) == 1u;
         uint16_t *crow = reinterpret_cast<uint16_t *>(p.C) + static_cast<size_t>(m0 + row) * p.ldc + n0;
-        float *prow = SPLIT ? p.partials + (static_cast<size_t>(split) * p.M + m0 + row) * p.N + n0 : nullptr;
+        // partial planes are [splits][num_m_tiles*BM][num_n_tiles*BN]: whole tiles, so the
+        // 32-column stores below need no column mask on ragged shapes
+        const size_t Mp = static_cast<size_t>(p.num_m_tiles) * BM, Np = static_cast<size_t>(p.num_n_tiles) * BN;
+        float *prow = SPLIT ? p.partials + (static_cast<size_t>(split) * Mp + m0 + row) * Np + n0 : nullptr;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
             uint32_t r[32];
@@ -323,12 +343,15 @@ __global__ void __launch_bounds__(128, 1)
         if (ctrl[3]) {
             __threadfence();
             const int row = (BM == 128) ? (warp * 32 + lane) : (warp * 16 + lane);
-            if ((BM == 128 || lane < 16) && !ctrl[1]) {
-                const size_t plane = static_cast<size_t>(p.M) * p.N;
-                const float *src = p.partials + static_cast<size_t>(m0 + row) * p.N + n0;
-                __half *crow = p.C + static_cast<size_t>(m0 + row) * p.N + n0;
+            if ((BM == 128 || lane < 16) && m0 + row < p.M && !ctrl[1]) {
+                const size_t Mp = static_cast<size_t>(p.num_m_tiles) * BM;
+                const size_t Np = static_cast<size_t>(p.num_n_tiles) * BN;
+                const size_t plane = Mp * Np;
+                const float *src = p.partials + static_cast<size_t>(m0 + row) * Np + n0;
+                uint16_t *crow = reinterpret_cast<uint16_t *>(p.C) + static_cast<size_t>(m0 + row) * p.ldc + n0;
+                const bool bf16 = ((p.idesc_flags >> 7) & 7u) == 1u;
 #pragma unroll 1
-                for (int c = 0; c < BN; c += 8) {
+                for (int c = 0; c < BN && n0 + c < p.N; c += 8) {  // N % 8 == 0: whole 8-column vectors
                     float4 a0 = __ldcg(reinterpret_cast<const float4 *>(src + c));
                     float4 a1 = __ldcg(reinterpret_cast<const float4 *>(src + c + 4));
                     for (int sp = 1; sp < p.splits; ++sp) {
@@ -337,11 +360,7 @@ __global__ void __launch_bounds__(128, 1)
                         a0.x += b0.x; a0.y += b0.y; a0.z += b0.z; a0.w += b0.w;
                         a1.x += b1.x; a1.y += b1.y; a1.z += b1.z; a1.w += b1.w;
                     }
-                    __half2 h0 = __floats2half2_rn(a0.x, a0.y), h1 = __floats2half2_rn(a0.z, a0.w);
-                    __half2 h2 = __floats2half2_rn(a1.x, a1.y), h3 = __floats2half2_rn(a1.z, a1.w);
-                    *reinterpret_cast<uint4 *>(crow + c) =
-                        make_uint4(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1),
-                                   *reinterpret_cast<uint32_t *>(&h2), *reinterpret_cast<uint32_t *>(&h3));
+                    *reinterpret_cast<uint4 *>(crow + c) = pack8_f32(a0, a1, bf16);
                 }
             }
             if (threadIdx.x == 0) atomicExch(&p.counters[lin], 0u);
@@ -367,16 +386,17 @@ __global__ void __launch_bounds__(128, 1)
     }
 }
 
-// Sums the fp32 partials [splits][M][N] in split order and writes fp16 C (the
-// separate-kernel reduction of split-K); each thread handles 8 consecutive columns.
-__global__ void splitk_reduce_kernel(const float *__restrict__ partials, __half *__restrict__ C, size_t elems,
-                                     int splits);
+// Sums the fp32 partials [splits][Mp][Np] in split order and writes C [M][N] (row
+// stride ldc, fp16 or bf16): the separate-kernel reduction of split-K; each thread
+// handles 8 consecutive columns of one row.
+__global__ void splitk_reduce_kernel(const float *__restrict__ partials, uint16_t *__restrict__ C, int64_t M,
+                                     int64_t N, int64_t Mp, int64_t Np, int64_t ldc, int splits, int bf16);
 
 // Host-side launchers, instantiated per ladder tile and layout (gemm_t*.cu).
 template <int BM, int BN, int LAYOUT>
 int launch_gemm_tile(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args,
                      cudaStream_t stream);
-template <int BM, int BN>
+template <int BM, int BN, int LAYOUT>
 int launch_gemm_tile_split(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args,
                            cudaStream_t stream);
 

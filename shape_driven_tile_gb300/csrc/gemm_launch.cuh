@@ -41,12 +41,12 @@ int launch_gemm_tile(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmA
     return launch_kernel(kern, dim3(grid), dim3(Cfg::THREADS), size_t(smem), stream, 1, tmA, tmB, args);
 }
 
-// Split-K form (row-major A and B only).
-template <int BM, int BN>
+// Split-K form.
+template <int BM, int BN, int LAYOUT>
 int launch_gemm_tile_split(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args,
                            cudaStream_t stream) {
     using Cfg = TileCfg<BM, BN>;
-    auto kern = gemm_f16_tile_kernel<BM, BN, true, 0>;
+    auto kern = gemm_f16_tile_kernel<BM, BN, true, LAYOUT>;
     const int smem = Cfg::smem_bytes(args.stages);
     static std::atomic<int> configured[64];
     if (int e = ensure_smem(kern, smem, configured)) return e;
@@ -99,7 +99,9 @@ int launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmA
 #define SDT_TILE_ONE_(BM, BN, L)                                                                     \
     template int sdt::launch_gemm_tile<BM, BN, L>(const CUtensorMap &, const CUtensorMap &,          \
                                                   const sdt::GemmArgs &, cudaStream_t);
+#define SDT_TILE_SPLIT_ONE_(BM, BN, L)                                                               \
+    template int sdt::launch_gemm_tile_split<BM, BN, L>(const CUtensorMap &, const CUtensorMap &,    \
+                                                        const sdt::GemmArgs &, cudaStream_t);
 #define SDT_INSTANTIATE_GEMM_TILE(BM, BN)                                                            \
     SDT_LAYOUTS_(SDT_TILE_ONE_, BM, BN)                                                              \
-    template int sdt::launch_gemm_tile_split<BM, BN>(const CUtensorMap &, const CUtensorMap &,       \
-                                                     const sdt::GemmArgs &, cudaStream_t);
+    SDT_LAYOUTS_(SDT_TILE_SPLIT_ONE_, BM, BN)

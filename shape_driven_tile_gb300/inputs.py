@@ -61,3 +61,46 @@ def q8_weights_exact(N: int, K: int, seed: int, group: int = 32):
     e = torch.randint(7, 11, (N, K // group), generator=g, dtype=torch.int32)
     s = torch.pow(2.0, -e.to(torch.float64)).to(torch.float16)
     return q, s
+
+
+# The GEMM shapes of "Iteratively Tuning hipBLASLt TensileLite Kernels", section
+# "Experiment Setup" (problem matrix: six geometric probes and eighteen
+# LLM-serving shapes) as printed in its Table 2: (name, M, N, K).
+P4_SHAPES = [
+    ("sn_16_dec", 16, 16, 4096),
+    ("sn_16_pf", 8192, 16, 2048),
+    ("sn_32_dec", 16, 32, 8192),
+    ("sn_64_pf", 4096, 64, 4096),
+    ("sn_128_dec", 16, 128, 4096),
+    ("sn_256_pf", 4096, 256, 8192),
+    ("sqS", 512, 512, 512),
+    ("sqL", 2048, 2048, 2048),
+    ("fatK", 1024, 1024, 8192),
+    ("thinK", 4096, 4096, 512),
+    ("tallM", 8192, 1024, 2048),
+    ("wideN", 1024, 8192, 2048),
+    ("d4k_qkv_dec", 16, 8192, 4096),
+    ("d4k_qkv_pf", 4096, 8192, 4096),
+    ("d4k_ffn_dec", 16, 16384, 4096),
+    ("d4k_ffn_pf", 4096, 16384, 4096),
+    ("d4k_down_dec", 16, 4096, 16384),
+    ("d4k_down_pf", 4096, 4096, 16384),
+    ("d8k_qkv_dec", 16, 16384, 8192),
+    ("d8k_qkv_pf", 2048, 16384, 8192),
+    ("d8k_ffn_pf", 2048, 32768, 8192),
+    ("d8k_down_pf", 2048, 8192, 32768),
+    ("moe_up_pf", 4096, 2048, 8192),
+    ("moe_down_pf", 4096, 8192, 2048),
+]
+
+
+def p4_operands(M: int, N: int, K: int, layout: str, seed: int, dtype=torch.float16):
+    """Uniform [-1, 1] operands of one problem of that matrix, on the CPU: A [M, K]
+    row-major, and B as the logical [K, N] matrix stored row-major ("NN") or as its
+    transpose [N, K] ("TN": both operands K-contiguous).  Returns (A, B_stored)."""
+    A = uniform((M, K), seed=seed, dtype=dtype)
+    if layout == "NN":
+        return A, uniform((K, N), seed=seed + 1, dtype=dtype)
+    if layout == "TN":
+        return A, uniform((N, K), seed=seed + 1, dtype=dtype)
+    raise ValueError("layout must be NN or TN")

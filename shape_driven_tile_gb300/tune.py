@@ -1,0 +1,221 @@
+"""Monotone coordinate-descent tuning of one GEMM problem.
+
+"Iteratively Tuning hipBLASLt TensileLite Kernels", sections "The Iteration:
+Principle and Design" and "The Six Rounds": the search opens one group of
+parameters at a time while every other parameter stays pinned at the running
+best, puts the running best into every round's candidate list, and adopts a
+round's winner only when it is strictly faster, so the latency after each round
+can only stay or fall; the groups run in order of impact, with the tail
+handling last.  The starting point is the library's own choice (the page's warm
+start from the kernel already in hand; here pick_tile's tile).
+
+Groups for this library's kernels:
+
+  1. ``tile``     -- the ladder tile (any tile that fits on chip; gemm_ex lets
+                     tiles overhang ragged edges)
+  2. ``split-K``  -- split count and reduction algorithm with the tile pinned
+                     (gemm_ex_splitk, a form of the one-CTA tiles only: when the
+                     held tile is persistent or a CTA pair, the round opens the
+                     split-capable tiles too; candidates the library rejects are
+                     dropped before timing, as the page's legality filter drops
+                     configurations that cannot be generated)
+  3. ``mapping``  -- how CTAs land on the output: the raster band height (m-tiles
+                     per band) and the k-loop start stagger
+  4. ``tail``     -- the two-CTA 256x256 tile's tail as half-width items or not
+
+The descent itself (``descend``) is pure host logic over a ``measure`` callable;
+``GemmProblem`` supplies candidates and GPU timings for a problem.
+"""
+from __future__ import annotations
+
+import os
+from typing import Callable, Iterable
+
+import torch
+
+import shape_driven_tile_gb300 as sdt
+
+SPLITS = (2, 3, 4, 6, 8, 12, 16)
+RASTER = (1, 2, 4, 8, 16, 32)
+DEFAULTS = {"tile": -1, "splits": 1, "algo": 0, "raster": 8, "stagger": 1, "tail": 1}
+
+
+def _key(cfg: dict) -> tuple:
+    return tuple(sorted(cfg.items()))
+
+
+def descend(rounds, start: dict, measure: Callable[[dict], float | None]):
+    """Run the rounds from `start`.
+
+    rounds  : sequence of (name, propose) where propose(held) yields candidate configs
+    measure : config -> latency (any unit, lower is better) or None when the
+              configuration is illegal for the problem
+    Returns (held, trajectory).  trajectory[0] is the start ("base"); entry r > 0
+    records the round's name, the latency held after it, the configuration held,
+    and how many candidates were enumerated and how many were legal.  The held
+    latency is always a measurement of the held configuration: the incumbent is
+    timed again in every round with the challengers (keeping its best time), and
+    a challenger replaces it only when its time is strictly lower.  So the held
+    latency never rises from one round to the next, whatever the ranges or the
+    noise, and the worst a round can do is keep what it started from.
+    """
+    held = dict(start)
+    t_held = measure(held)
+    if t_held is None:
+        raise ValueError("the starting configuration is not legal for the problem")
+    traj = [{"round": "base", "us": t_held, "cfg": dict(held), "enumerated": 1, "legal": 1}]
+    for name, propose in rounds:
+        cands, seen = [], set()
+        for c in [dict(held)] + list(propose(dict(held))):  # union the incumbent
+            k = _key(c)
+            if k not in seen:
+                seen.add(k)
+                cands.append(dict(c))
+        results = []
+        for c in cands:
+            t = measure(c)
+            if t is not None:
+                results.append((t, c))
+        if not results:
+            traj.append({"round": name, "us": t_held, "cfg": dict(held), "enumerated": len(cands), "legal": 0})
+            continue
+        for t, c in results:
+            if _key(c) == _key(held):
+                t_held = min(t_held, t)
+        best_t, best_c = min(results, key=lambda r: r[0])
+        if best_t < t_held and _key(best_c) != _key(held):
+            held, t_held = best_c, best_t
+        traj.append({"round": name, "us": t_held, "cfg": dict(held), "enumerated": len(cands),
+                     "legal": len(results)})
+    return held, traj
+
+
+class _Env:
+    """Sets the library's per-call environment knobs for one launch and restores them."""
+
+    NAMES = {"raster": "SDT_RASTER_GROUP", "stagger": "SDT_STAGGER", "tail": "SDT_TAIL_SPLIT"}
+
+    def __init__(self, cfg: dict):
+        self.vals = {self.NAMES[k]: str(int(cfg[k])) for k in self.NAMES}
+
+    def __enter__(self):
+        self.old = {k: os.environ.get(k) for k in self.vals}
+        os.environ.update(self.vals)
+
+    def __exit__(self, *exc):
+        for k, v in self.old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+
+
+class GemmProblem:
+    """One problem C = op(A) . op(B) on the GPU and the candidates of each round.
+
+    A is [M, K] row-major; B is the logical [K, N] operand as a view (row-major, or
+    the transpose of a row-major [N, K] tensor); C is [M, N] row-major.  Latency of
+    a configuration: mean device time of `reps` launches, each after writing a
+    buffer larger than L2 (CUDA events on the current stream around the launch).
+    """
+
+    def __init__(self, A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, reps: int = 10,
+                 flush_bytes: int = 512 << 20):
+        self.A, self.B, self.C, self.reps = A, B, C, reps
+        self.M, self.K = A.shape
+        self.N = B.shape[1]
+        self.dtype = A.dtype
+        self.flush = torch.empty(flush_bytes // 4, dtype=torch.float32, device=A.device)
+        self.ws = None
+        self.ntiles = len(sdt.tiles())
+
+    # -- launching ----------------------------------------------------------------------
+    def _workspace(self, nbytes: int) -> torch.Tensor:
+        if self.ws is None or self.ws.numel() < nbytes:
+            ws = torch.empty(max(nbytes, 256) + 256, dtype=torch.uint8, device=self.A.device)
+            off = (-ws.data_ptr()) % 256
+            self.ws = ws[off:off + max(nbytes, 256)]
+            sdt.lib().sdt_splitk_workspace_init(self.ws.data_ptr(), self.ws.numel(),
+                                                torch.cuda.current_stream().cuda_stream)
+        return self.ws
+
+    def launcher(self, cfg: dict):
+        """A no-argument callable that launches cfg, or None when cfg is illegal here."""
+        if cfg["splits"] > 1:
+            nbytes = sdt.splitk_ex_workspace_bytes(self.M, self.N, self.K, cfg["tile"], cfg["splits"])
+            if nbytes == 0:
+                return None
+            ws = self._workspace(nbytes)
+
+            def run():
+                with _Env(cfg):
+                    sdt.gemm_ex_splitk(self.A, self.B, self.C, workspace=ws, tile=cfg["tile"],
+                                       splits=cfg["splits"], algo=cfg["algo"])
+            return run
+
+        def run():
+            with _Env(cfg):
+                sdt.gemm_ex(self.A, self.B, self.C, tile=cfg["tile"])
+        return run
+
+    def measure(self, cfg: dict) -> float | None:
+        run = self.launcher(cfg)
+        if run is None:
+            return None
+        try:
+            run()  # also rejects configurations the library refuses (tile/shape/split rules)
+            torch.cuda.synchronize()
+        except sdt.SdtError:
+            return None
+        stream = torch.cuda.current_stream()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(self.reps)]
+        for e0, e1 in evs:
+            self.flush.zero_()
+            e0.record(stream)
+            run()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return 1e3 * sum(e0.elapsed_time(e1) for e0, e1 in evs) / self.reps
+
+    # -- rounds -------------------------------------------------------------------------
+    def start(self) -> dict:
+        cfg = dict(DEFAULTS)
+        cfg["tile"] = sdt.pick_tile_any(self.M, self.N, self.K)
+        return cfg
+
+    def rounds(self):
+        def tiles(held):
+            for t in range(self.ntiles):
+                yield dict(held, tile=t, splits=1, algo=0)
+
+        def split(held):
+            # The page opens the split with the tile pinned.  Here split-K is a form of the
+            # one-CTA tiles only, so when the held tile is persistent or a CTA pair the round
+            # opens the split-capable tiles with it; the held configuration stays a
+            # candidate either way.  Candidates without a split-K form for the shape are
+            # dropped by measure()'s legality check.
+            if held["splits"] > 1:
+                return
+            own = sdt.splitk_ex_workspace_bytes(self.M, self.N, self.K, held["tile"], 2) > 0
+            tiles = [held["tile"]] if own else range(self.ntiles)
+            for t in tiles:
+                for s in SPLITS:
+                    for a in (sdt.SPLITK_REDUCE_KERNEL, sdt.SPLITK_IN_KERNEL):
+                        yield dict(held, tile=t, splits=s, algo=a)
+
+        def mapping(held):
+            for r in RASTER:
+                for st in (0, 1):
+                    yield dict(held, raster=r, stagger=st)
+
+        def tail(held):
+            info = sdt.tile_info(held["tile"])
+            if info["cta_group"] == 2 and info["BN"] == 256 and held["splits"] == 1:
+                for t in (0, 1):
+                    yield dict(held, tail=t)
+
+        return [("tile", tiles), ("split-K", split), ("mapping", mapping), ("tail", tail)]
+
+    def tune(self):
+        return descend(self.rounds(), self.start(), self.measure)

@@ -45,3 +45,33 @@ def test_splitk_argument_errors_without_gpu():
     assert L.gemm_f16_splitk(256, 256, 256, 0x1000, 0x2000, 0x3000, None, 0, 0, 2, 9, None) == -10
     assert L.gemm_f16_splitk(256, 256, 256, 0x1000, 0x2008, 0x3000, 0x4000, 1 << 20, 0, 2, 1, None) == -2
     assert L.gemm_f16_splitk(0, 256, 256, None, None, None, None, 0, 0, 2, 1, None) == 0
+
+
+@pytest.mark.parametrize("name", SPLIT_TILES)
+def test_ex_workspace_bytes_cover_whole_tiles(name):
+    # gemm_ex_splitk: partial planes are whole tiles, so ragged shapes round up
+    t = sdt.tile_info(sdt.tile_id(name))
+    for M, N, K in [(16, 4096, 4096), (300, 136, 1000), (512, 768, 4096), (1, 8, 65)]:
+        Mp, Np = -(-M // t["BM"]) * t["BM"], -(-N // t["BN"]) * t["BN"]
+        nk = -(-K // 64)
+        for splits in (1, 2, 3, 7):
+            if splits > nk:
+                assert sdt.splitk_ex_workspace_bytes(M, N, K, name, splits) == 0
+                continue
+            kps = -(-nk // splits)
+            eff = -(-nk // kps)
+            tiles = (Mp // t["BM"]) * (Np // t["BN"])
+            want = -(-(eff * Mp * Np * 4) // 256) * 256 + tiles * 4
+            assert sdt.splitk_ex_workspace_bytes(M, N, K, name, splits) == want
+        # on shapes the tile divides, the same bytes as gemm_f16_splitk's workspace
+        if M % t["BM"] == 0 and N % t["BN"] == 0 and K % 64 == 0:
+            assert sdt.splitk_ex_workspace_bytes(M, N, K, name, 3) == sdt.splitk_workspace_bytes(M, N, K, name, 3)
+
+
+def test_ex_workspace_bytes_invalid_and_pick():
+    assert sdt.splitk_ex_workspace_bytes(512, 512, 4096, "p128x256", 2) == 0    # no split form
+    assert sdt.splitk_ex_workspace_bytes(0, 512, 4096, "64x64", 2) == 0
+    tid, sp = sdt.pick_splitk_any(16, 16384, 4096)
+    assert sdt.tile_info(tid)["name"] in SPLIT_TILES and sdt.splitk_ex_workspace_bytes(16, 16384, 4096, tid, sp) > 0
+    tid, sp = sdt.pick_splitk_any(16, 16, 4096)
+    assert sp > 1                       # one output tile, 64 k-tiles: splitting pays
