@@ -12,7 +12,9 @@ start from the kernel already in hand; here pick_tile's tile).
 Groups for this library's kernels:
 
   1. ``tile``     -- the ladder tile (any tile that fits on chip; gemm_ex lets
-                     tiles overhang ragged edges)
+                     tiles overhang ragged edges) with its ring depth (the
+                     page opens DepthU in this round; 0 = the tile's own depth,
+                     deeper rings are clamped to what fits in shared memory)
   2. ``split-K``  -- split count and reduction algorithm with the tile pinned
                      (gemm_ex_splitk, a form of the one-CTA tiles only: when the
                      held tile is persistent or a CTA pair, the round opens the
@@ -36,8 +38,9 @@ import torch
 import shape_driven_tile_gb300 as sdt
 
 SPLITS = (2, 3, 4, 6, 8, 12, 16)
+DEPTHS = (0, 3, 4, 6, 8, 12)
 RASTER = (1, 2, 4, 8, 16, 32)
-DEFAULTS = {"tile": -1, "splits": 1, "algo": 0, "raster": 8, "stagger": 1, "tail": 1}
+DEFAULTS = {"tile": -1, "stages": 0, "splits": 1, "algo": 0, "raster": 8, "stagger": 1, "tail": 1}
 
 
 def _key(cfg: dict) -> tuple:
@@ -93,7 +96,7 @@ def descend(rounds, start: dict, measure: Callable[[dict], float | None]):
 class _Env:
     """Sets the library's per-call environment knobs for one launch and restores them."""
 
-    NAMES = {"raster": "SDT_RASTER_GROUP", "stagger": "SDT_STAGGER", "tail": "SDT_TAIL_SPLIT"}
+    NAMES = {"raster": "SDT_RASTER_GROUP", "stagger": "SDT_STAGGER", "tail": "SDT_TAIL_SPLIT", "stages": "SDT_STAGES"}
 
     def __init__(self, cfg: dict):
         self.vals = {self.NAMES[k]: str(int(cfg[k])) for k in self.NAMES}
@@ -187,7 +190,8 @@ class GemmProblem:
     def rounds(self):
         def tiles(held):
             for t in range(self.ntiles):
-                yield dict(held, tile=t, splits=1, algo=0)
+                for d in DEPTHS:
+                    yield dict(held, tile=t, stages=d, splits=1, algo=0)
 
         def split(held):
             # The page opens the split with the tile pinned.  Here split-K is a form of the
