@@ -745,6 +745,8 @@ def run_sweep(args):
         print(json.dumps(rows[-1]), flush=True)
         del A, B, C
     sdt.check_device_status()
+    if args.table_out:
+        write_tune_table(args.table_out, [(*r["shape"], {"tile": r["best"]}) for r in rows], "the tile sweep")
     slow = [r["slowdown"] for r in rows]
     print(json.dumps({"mode": "sweep", "shapes": len(rows), "pick_avg_slowdown": round(statistics.mean(slow), 4),
                       "pick_worst_slowdown": round(max(slow), 4), "peak_tflops": peaks["tflops"],
@@ -912,7 +914,29 @@ def run_p4(args):
                                   "max": round(max(r["speedup"] for r in rows), 3)}
         out["monotone"] = all(all(b <= a for a, b in zip(list(r["rounds"].values()),
                                                          list(r["rounds"].values())[1:])) for r in rows)
+        if args.table_out:
+            out["table"] = write_tune_table(args.table_out, [
+                (r["M"], r["N"], r["K"], r["tuned"]) for r in rows
+                if r["dtype"] == "f16" and r["layout"] == "NN" and r["tuned"]["splits"] == 1],
+                "coordinate descent, bench.py --mode p4 --tune")
     print(json.dumps(out), flush=True)
+
+
+def write_tune_table(path, entries, how):
+    """Freeze tuned configurations for gemm_f16 ("M N K tile stagger raster stages" lines;
+    see sdt_load_tune_table); shapes gemm_f16 cannot run with that tile are left out."""
+    import shape_driven_tile_gb300 as sdt
+
+    lines = [f"# frozen by {how}; GB300, {time.strftime('%Y-%m-%d')}"]
+    for M, N, K, cfg in entries:
+        tid = sdt.tile_id(cfg["tile"]) if isinstance(cfg["tile"], str) else cfg["tile"]
+        if tid not in sdt.feasible_tiles(M, N, K, smem_limit=232448):
+            continue
+        lines.append(f"{M} {N} {K} {sdt.tile_info(tid)['name']} {cfg.get('stagger', -1)} "
+                     f"{cfg.get('raster', 0)} {cfg.get('stages', 0)}")
+    with open(path, "w") as f:
+        f.write("\n".join(lines) + "\n")
+    return {"path": path, "entries": len(lines) - 1}
 
 
 def run_large(args):
@@ -1061,6 +1085,7 @@ def main(argv=None):
     ap.add_argument("--mode", choices=["step", "sweep", "kscan", "decode", "large", "one", "splitk", "chain",
                                        "record-traffic", "p4"], default="step")
     ap.add_argument("--tune", action="store_true", help="p4: run the coordinate-descent tuner per problem")
+    ap.add_argument("--table-out", help="p4 --tune / sweep: write the winners as a gemm_f16 tune table")
     ap.add_argument("--ncu-csv", help="record-traffic: ncu --csv log of one launch")
     ap.add_argument("--key", help="record-traffic: gemm_4096, gemv_bf16 or gemv_q8")
     ap.add_argument("--gemv", choices=["bf16", "q8"])

@@ -80,7 +80,10 @@ typedef enum sdt_status {
  * feasible, otherwise sdt_pick_tile(M,N,K).  With SDT_AUTOTUNE=1 in the
  * environment, the first call for a shape times every feasible tile on
  * `stream` (synchronising it) and remembers the fastest for later calls.
- * The k-loop stagger follows SDT_STAGGER ("auto" (default), "0", "1").
+ * The k-loop stagger follows SDT_STAGGER: "auto" (default) staggers the
+ * one-CTA tiles when the k-tile count is a power of two and leaves the
+ * persistent and two-CTA tiles unstaggered (measured faster on GB300); "0" and
+ * "1" force it off or on.
  *
  * Requirements: A, B, C 16-byte aligned; M, N, K >= 0.  M == 0 or N == 0 is a
  * no-op; K == 0 writes C = 0.  Otherwise some tile must divide the shape

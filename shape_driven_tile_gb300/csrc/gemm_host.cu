@@ -109,9 +109,13 @@ static constexpr int kDefaultSmemLimit = 232448;  // opt-in shared memory per bl
 static constexpr int kMaxRing = 24;
 static constexpr int64_t kMaxDim = int64_t(1) << 30;
 
-static int tile_stages(const LadderTile &t, int smem_limit) {
+// Ring depth of a launch: `req` when in 2..kMaxRing, else SDT_STAGES when set, else
+// the tile's own depth; lowered until the ring fits in shared memory.
+static int tile_stages(const LadderTile &t, int smem_limit, int req = 0) {
     int s = t.stages;
-    if (const char *e = getenv("SDT_STAGES")) {
+    if (req >= 2 && req <= kMaxRing) {
+        s = req;
+    } else if (const char *e = getenv("SDT_STAGES")) {
         int v = atoi(e);
         if (v >= 2 && v <= kMaxRing) s = v;
     }
@@ -214,6 +218,8 @@ static bool is_pow2(int64_t v) { return v > 0 && (v & (v - 1)) == 0; }
 struct TuneEntry {
     int tile;
     int stagger;  // -1 = auto
+    int raster;   // m-tiles per raster band, 0 = default
+    int stages;   // ring depth, 0 = the tile's own
 };
 using ShapeKey = std::tuple<int64_t, int64_t, int64_t>;
 static std::mutex g_table_mu;
@@ -232,8 +238,8 @@ static int load_table_file(const char *path, std::map<ShapeKey, TuneEntry> *out)
         if (hash) *hash = 0;
         long long M, N, K;
         char name[64];
-        int stagger = -1;
-        int n = sscanf(line, "%lld %lld %lld %63s %d", &M, &N, &K, name, &stagger);
+        int stagger = -1, raster = 0, stages = 0;
+        int n = sscanf(line, "%lld %lld %lld %63s %d %d %d", &M, &N, &K, name, &stagger, &raster, &stages);
         if (n <= 0) {
             bool blank = true;
             for (char *c = line; *c; ++c)
@@ -242,7 +248,7 @@ static int load_table_file(const char *path, std::map<ShapeKey, TuneEntry> *out)
         }
         if (n < 4) {
             fclose(f);
-            return fail(SDT_ERR_TABLE, "%s:%d: expected 'M N K tile [stagger]'", path, lineno);
+            return fail(SDT_ERR_TABLE, "%s:%d: expected 'M N K tile [stagger [raster [stages]]]'", path, lineno);
         }
         int id = find_tile(name);
         if (id < 0) {
@@ -254,11 +260,19 @@ static int load_table_file(const char *path, std::map<ShapeKey, TuneEntry> *out)
             return fail(SDT_ERR_TABLE, "%s:%d: tile %s is infeasible for %lldx%lldx%lld", path, lineno, name,
                         M, N, K);
         }
-        if (n == 5 && stagger != 0 && stagger != 1 && stagger != -1) {
+        if (n >= 5 && stagger != 0 && stagger != 1 && stagger != -1) {
             fclose(f);
             return fail(SDT_ERR_TABLE, "%s:%d: stagger must be -1, 0 or 1", path, lineno);
         }
-        tab[ShapeKey(M, N, K)] = TuneEntry{id, n == 5 ? stagger : -1};
+        if (n >= 6 && (raster < 0 || raster > (1 << 20))) {
+            fclose(f);
+            return fail(SDT_ERR_TABLE, "%s:%d: raster must be 0 (default) or a positive band height", path, lineno);
+        }
+        if (n >= 7 && stages != 0 && (stages < 2 || stages > kMaxRing)) {
+            fclose(f);
+            return fail(SDT_ERR_TABLE, "%s:%d: stages must be 0 (the tile's own) or 2..%d", path, lineno, kMaxRing);
+        }
+        tab[ShapeKey(M, N, K)] = TuneEntry{id, n >= 5 ? stagger : -1, n >= 6 ? raster : 0, n >= 7 ? stages : 0};
     }
     fclose(f);
     *out = std::move(tab);
@@ -430,12 +444,16 @@ static int env_int(const char *name, int dflt, int lo, int hi) {
     return v < lo ? lo : (v > hi ? hi : v);
 }
 
-static int stagger_default() {
+// SDT_STAGGER: "0"/"off", "1"/"on", or "auto" (default): on for the one-CTA tiles,
+// off for the persistent and two-CTA kernels.  Those keep a whole grid of tiles in
+// flight on the same k-slices, which L2 then serves once; staggering their k-loops
+// measured 3-5 % slower on GB300 at 2048^3 and 4096^3 and no faster at 8192^3 and
+// 12288^3 (alternating processes on one GPU); on the one-CTA tiles it is neutral.
+static int stagger_default(const LadderTile &t) {
     const char *s = getenv("SDT_STAGGER");
-    if (!s || !*s || !strcasecmp(s, "auto")) return 1;
-    if (!strcmp(s, "0") || !strcasecmp(s, "off")) return 0;
-    if (!strcmp(s, "1") || !strcasecmp(s, "on")) return 1;
-    return 1;
+    if (s && (!strcmp(s, "0") || !strcasecmp(s, "off"))) return 0;
+    if (s && (!strcmp(s, "1") || !strcasecmp(s, "on"))) return 1;
+    return t.persistent ? 0 : 1;
 }
 
 static int validate_common(int64_t M, int64_t N, int64_t K, const void *A, const void *B, void *C) {
@@ -453,7 +471,7 @@ static int validate_common(int64_t M, int64_t N, int64_t K, const void *A, const
 // (any shape: tiles overhang ragged edges; layouts and type per the flags).
 static int run_tile_ex(int tile_id, int stagger_req, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
                        const void *B, int64_t ldb, void *C, int64_t ldc, int dtype, int layout, cudaStream_t stream,
-                       const DeviceInfo &dev) {
+                       const DeviceInfo &dev, int raster_req = 0, int stages_req = 0) {
     const LadderTile &t = kLadder[tile_id];
     CUtensorMap tmA, tmB;
     int rc = operand_maps(A, lda, B, ldb, M, N, K, dtype, layout, t.BM / t.cta_group, &tmA, &tmB);
@@ -471,11 +489,11 @@ static int run_tile_ex(int tile_id, int stagger_req, int64_t M, int64_t N, int64
     a.num_m_tiles = int((M + t.BM - 1) / t.BM);
     a.num_n_tiles = int((N + t.BN - 1) / t.BN);
     a.num_k_tiles = int((K + kBK - 1) / kBK);
-    a.stages = tile_stages(t, dev.smem_optin);
-    const int want_stagger = stagger_req < 0 ? stagger_default() : stagger_req;
+    a.stages = tile_stages(t, dev.smem_optin, stages_req);
+    const int want_stagger = stagger_req < 0 ? stagger_default(t) : stagger_req;
     a.stagger = (want_stagger && is_pow2(a.num_k_tiles)) ? 1 : 0;
     a.stagger_stride = env_int("SDT_STAGGER_STRIDE", 1, 1, 1 << 20);
-    a.raster_group = env_int("SDT_RASTER_GROUP", 8, 1, 1 << 20);
+    a.raster_group = raster_req > 0 ? raster_req : env_int("SDT_RASTER_GROUP", 8, 1, 1 << 20);
     a.timeout_ns = wait_timeout_ns();
     a.status = status;
     a.max_ctas = dev.sm_count * ctas_per_sm(t, dev.smem_per_sm);
@@ -504,12 +522,14 @@ static int run_tile_ex(int tile_id, int stagger_req, int64_t M, int64_t N, int64
 
 // gemm_f16's forced tile: tight row-major fp16, the tile must divide the shape.
 static int run_tile(int tile_id, int stagger_req, int64_t M, int64_t N, int64_t K, const void *A,
-                    const void *B, void *C, cudaStream_t stream, const DeviceInfo &dev) {
+                    const void *B, void *C, cudaStream_t stream, const DeviceInfo &dev, int raster_req = 0,
+                    int stages_req = 0) {
     const LadderTile &t = kLadder[tile_id];
     if (!feasible(t, M, N, K, dev.smem_optin))
         return fail(SDT_ERR_TILE, "tile %s is infeasible for %lldx%lldx%lld", t.name, (long long)M,
                     (long long)N, (long long)K);
-    return run_tile_ex(tile_id, stagger_req, M, N, K, A, K, B, N, C, N, SDT_DTYPE_F16, 0, stream, dev);
+    return run_tile_ex(tile_id, stagger_req, M, N, K, A, K, B, N, C, N, SDT_DTYPE_F16, 0, stream, dev, raster_req,
+                       stages_req);
 }
 
 // SDT_AUTOTUNE=1: time every feasible tile on the caller's stream (synchronising
@@ -549,7 +569,7 @@ static int autotune_shape(int64_t M, int64_t N, int64_t K, const void *A, const 
     cudaEventDestroy(e0);
     cudaEventDestroy(e1);
     if (best < 0) return fail(SDT_ERR_SHAPE, "no feasible tile to autotune");
-    *out = TuneEntry{best, -1};
+    *out = TuneEntry{best, -1, 0, 0};
     std::lock_guard<std::mutex> lock(g_table_mu);
     g_table[ShapeKey(M, N, K)] = *out;
     return SDT_OK;
@@ -582,7 +602,8 @@ static int gemm_dispatch(int64_t M, int64_t N, int64_t K, const void *A, const v
     load_env_table();
     TuneEntry te;
     if (table_lookup(M, N, K, &te) && feasible(kLadder[te.tile], M, N, K, dev.smem_optin))
-        return run_tile(te.tile, stagger >= 0 ? stagger : te.stagger, M, N, K, A, B, C, stream, dev);
+        return run_tile(te.tile, stagger >= 0 ? stagger : te.stagger, M, N, K, A, B, C, stream, dev, te.raster,
+                        te.stages);
     if (env_flag("SDT_AUTOTUNE")) {
         rc = autotune_shape(M, N, K, A, B, C, stream, dev, &te);
         if (rc) return rc;

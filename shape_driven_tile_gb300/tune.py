@@ -31,6 +31,7 @@ The descent itself (``descend``) is pure host logic over a ``measure`` callable;
 from __future__ import annotations
 
 import os
+import random
 from typing import Callable, Iterable
 
 import torch
@@ -40,19 +41,24 @@ import shape_driven_tile_gb300 as sdt
 SPLITS = (2, 3, 4, 6, 8, 12, 16)
 DEPTHS = (0, 3, 4, 6, 8, 12)
 RASTER = (1, 2, 4, 8, 16, 32)
-DEFAULTS = {"tile": -1, "stages": 0, "splits": 1, "algo": 0, "raster": 8, "stagger": 1, "tail": 1}
+# 0 / -1 leave the library's own default for that knob (raster band, stagger "auto", ring depth)
+DEFAULTS = {"tile": -1, "stages": 0, "splits": 1, "algo": 0, "raster": 0, "stagger": -1, "tail": 1}
 
 
 def _key(cfg: dict) -> tuple:
     return tuple(sorted(cfg.items()))
 
 
-def descend(rounds, start: dict, measure: Callable[[dict], float | None]):
+def descend(rounds, start: dict, measure: Callable[[dict], float | None], passes: int = 1, seed: int = 0):
     """Run the rounds from `start`.
 
     rounds  : sequence of (name, propose) where propose(held) yields candidate configs
     measure : config -> latency (any unit, lower is better) or None when the
               configuration is illegal for the problem
+    passes  : each round times its candidates `passes` times, every pass in a fresh
+              shuffled order, and keeps each candidate's best time -- so a slow drift
+              of the device (clocks, temperature) does not favour whichever candidate
+              is always timed first
     Returns (held, trajectory).  trajectory[0] is the start ("base"); entry r > 0
     records the round's name, the latency held after it, the configuration held,
     and how many candidates were enumerated and how many were legal.  The held
@@ -62,6 +68,7 @@ def descend(rounds, start: dict, measure: Callable[[dict], float | None]):
     latency never rises from one round to the next, whatever the ranges or the
     noise, and the worst a round can do is keep what it started from.
     """
+    rng = random.Random(seed)
     held = dict(start)
     t_held = measure(held)
     if t_held is None:
@@ -74,11 +81,17 @@ def descend(rounds, start: dict, measure: Callable[[dict], float | None]):
             if k not in seen:
                 seen.add(k)
                 cands.append(dict(c))
-        results = []
-        for c in cands:
-            t = measure(c)
-            if t is not None:
-                results.append((t, c))
+        best_of = {}
+        order = list(range(len(cands)))
+        for _ in range(max(1, passes)):
+            rng.shuffle(order)
+            for i in order:
+                k = _key(cands[i])
+                if best_of.get(k, 0.0) is None:
+                    continue  # illegal: not timed again
+                t = measure(cands[i])
+                best_of[k] = None if t is None else min(t, best_of.get(k) or t)
+        results = [(best_of[_key(c)], c) for c in cands if best_of[_key(c)] is not None]
         if not results:
             traj.append({"round": name, "us": t_held, "cfg": dict(held), "enumerated": len(cands), "legal": 0})
             continue
@@ -94,16 +107,23 @@ def descend(rounds, start: dict, measure: Callable[[dict], float | None]):
 
 
 class _Env:
-    """Sets the library's per-call environment knobs for one launch and restores them."""
+    """Sets the library's per-call environment knobs for one launch and restores them
+    (a knob at its "library default" value is removed from the environment)."""
 
     NAMES = {"raster": "SDT_RASTER_GROUP", "stagger": "SDT_STAGGER", "tail": "SDT_TAIL_SPLIT", "stages": "SDT_STAGES"}
+    LIBRARY_DEFAULT = {"raster": 0, "stagger": -1, "stages": 0}
 
     def __init__(self, cfg: dict):
-        self.vals = {self.NAMES[k]: str(int(cfg[k])) for k in self.NAMES}
+        self.vals = {self.NAMES[k]: (None if self.LIBRARY_DEFAULT.get(k) == cfg[k] else str(int(cfg[k])))
+                     for k in self.NAMES}
 
     def __enter__(self):
         self.old = {k: os.environ.get(k) for k in self.vals}
-        os.environ.update(self.vals)
+        for k, v in self.vals.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
 
     def __exit__(self, *exc):
         for k, v in self.old.items():
@@ -210,7 +230,7 @@ class GemmProblem:
 
         def mapping(held):
             for r in RASTER:
-                for st in (0, 1):
+                for st in (-1, 0, 1):
                     yield dict(held, raster=r, stagger=st)
 
         def tail(held):
@@ -221,5 +241,5 @@ class GemmProblem:
 
         return [("tile", tiles), ("split-K", split), ("mapping", mapping), ("tail", tail)]
 
-    def tune(self):
-        return descend(self.rounds(), self.start(), self.measure)
+    def tune(self, passes: int = 2):
+        return descend(self.rounds(), self.start(), self.measure, passes=passes)

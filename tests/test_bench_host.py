@@ -107,3 +107,20 @@ def test_record_traffic_and_staleness(tmp_path, monkeypatch):
     # a record taken on other sources is not used
     monkeypatch.setattr(bench, "kernel_source_digest", lambda kind="gemm": "0" * 16)
     assert bench.load_traffic("gemv_q8") is None
+
+
+def test_tuned_configurations_freeze_into_a_loadable_table(tmp_path):
+    import shape_driven_tile_gb300 as sdt
+    p = tmp_path / "tuned.txt"
+    out = bench.write_tune_table(str(p), [
+        (4096, 4096, 4096, {"tile": "2cta_256x256", "stagger": 0, "raster": 1, "stages": 6}),
+        (16, 16384, 4096, {"tile": "64x64"}),            # gemm_f16 cannot run this shape: left out
+        (1024, 1024, 1024, {"tile": "64x64", "stagger": -1, "raster": 0, "stages": 0})], "a test")
+    assert out["entries"] == 2
+    sdt.load_tune_table(str(p))
+    try:
+        assert sdt.lib().sdt_tune_table_size() == 2
+        assert sdt.tile_info(sdt.tune_table_lookup(4096, 4096, 4096))["name"] == "2cta_256x256"
+        assert sdt.tune_table_lookup(16, 16384, 4096) == -1
+    finally:
+        sdt.clear_tune_table()

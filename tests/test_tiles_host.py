@@ -104,11 +104,26 @@ def test_tune_table_roundtrip(tmp_path):
     assert sdt.lib().sdt_tune_table_size() == 0
 
 
+def test_tune_table_takes_raster_and_depth(tmp_path):
+    # the coordinate-descent tuner freezes tile, stagger, raster band and ring depth
+    p = tmp_path / "table.txt"
+    p.write_text("4096 4096 4096 2cta_256x256 0 1 6  # tuned\n2048 2048 2048 p128x256 -1 0 0\n")
+    sdt.load_tune_table(str(p))
+    try:
+        assert sdt.lib().sdt_tune_table_size() == 2
+        assert sdt.tile_info(sdt.tune_table_lookup(4096, 4096, 4096))["name"] == "2cta_256x256"
+    finally:
+        sdt.clear_tune_table()
+
+
 @pytest.mark.parametrize("body,needle", [
     ("256 256 256 99x99\n", "unknown tile"),
     ("192 256 256 128x128\n", "infeasible"),
     ("256 256\n", "expected"),
     ("256 256 256 64x64 7\n", "stagger"),
+    ("256 256 256 64x64 0 -2\n", "raster"),
+    ("256 256 256 64x64 0 4 1\n", "stages"),
+    ("256 256 256 64x64 0 4 99\n", "stages"),
 ])
 def test_tune_table_rejects_bad_entries(tmp_path, body, needle):
     p = tmp_path / "bad.txt"

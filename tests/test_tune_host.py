@@ -84,3 +84,31 @@ def test_p4_shape_list_matches_the_page():
     assert d["d4k_down_pf"] == (4096, 4096, 16384) and d["sn_64_pf"] == (4096, 64, 4096)
     assert d["d4k_ffn_dec"] == (16, 16384, 4096) and d["fatK"] == (1024, 1024, 8192)
     assert all(n % 8 == 0 for _, _, n, _ in P4_SHAPES)  # gemm_ex's only shape rule
+
+
+def test_passes_shuffle_order_and_keep_best():
+    # a device that slows down as it is used: with one fixed order the first candidate
+    # would always look fastest; shuffled passes keep each candidate's best time
+    clock = [0]
+    order_seen = []
+
+    def drifting(c):
+        clock[0] += 1
+        order_seen.append(c["a"])
+        return 10.0 + c["a"] * 0.01 + clock[0] * 0.1
+
+    held, traj = descend([("a", lambda h: (dict(h, a=v) for v in range(4)))], {"a": 3}, drifting, passes=3, seed=1)
+    firsts = [order_seen[1 + 4 * p] for p in range(3)]  # first candidate timed in each pass
+    assert len(set(firsts)) > 1                         # the order changes between passes
+    assert len(order_seen) == 1 + 4 * 3
+
+
+def test_passes_skip_illegal_after_first_pass():
+    calls = []
+
+    def measure(c):
+        calls.append(c["a"])
+        return None if c["a"] == 1 else 5.0 - c["a"]
+
+    descend([("a", lambda h: (dict(h, a=v) for v in range(3)))], {"a": 0}, measure, passes=3)
+    assert calls.count(1) == 1
