@@ -239,12 +239,14 @@ int sdt_pick_tile_any_for(int64_t M, int64_t N, int64_t K, int sm_count, int sme
  * takes the picked count).  The k-loop stagger is not applied.
  *
  * Workspace: device memory owned by the caller, 256-byte aligned, at least
- * sdt_splitk_workspace_bytes(M,N,K,tile_id,splits) bytes: fp32 partials
- * [splits][M][N] (padded to 256 B) then one u32 counter per output tile.  The
+ * sdt_splitk_workspace_bytes(M,N,K,tile_id,splits) bytes: one u32 counter per
+ * output tile (padded to 256 B), then fp32 partials [splits][M][N].  The
  * counters must be zero before the first SDT_SPLITK_IN_KERNEL call on a
  * workspace (sdt_splitk_workspace_init zeroes a workspace on `stream`); every
- * completed call leaves them zero again.  Calls that share a workspace must not
- * overlap on the GPU.  Same operand requirements as gemm_f16 (tight row-major,
+ * completed call leaves them zero again and writes partials only after the
+ * counter region, so a workspace zeroed once serves any sequence of split-K
+ * calls (any shape, tile, split count or algorithm) that fit in it.  Calls that
+ * share a workspace must not overlap on the GPU.  Same operand requirements as gemm_f16 (tight row-major,
  * 16-byte aligned; tile dims divide M, N; K % 64 == 0).
  * Errors: SDT_ERR_TILE (tile without split-K form or not dividing the shape),
  * SDT_ERR_ARG (splits out of 1..nK, unknown algo, workspace too small),
@@ -273,8 +275,9 @@ int sdt_pick_splitk_for(int64_t M, int64_t N, int64_t K, int sm_count, int smem_
  * round 2, with the operands of P3 "Changes"]: caller row strides, either
  * transposed operand, fp16 or bf16, and shapes no tile divides.  Arguments and
  * requirements as gemm_ex, plus the split-K arguments of gemm_f16_splitk.
- * The partial planes cover whole tiles: [splits][ceil(M/BM)*BM][ceil(N/BN)*BN]
- * fp32, then one u32 counter per output tile; the workspace must hold
+ * The partial planes cover whole tiles: one u32 counter per output tile
+ * (padded to 256 B), then [splits][ceil(M/BM)*BM][ceil(N/BN)*BN] fp32; the
+ * workspace (shareable with gemm_f16_splitk calls) must hold
  * sdt_splitk_ex_workspace_bytes(M,N,K,tile_id,splits) bytes (256-byte
  * aligned; counters zero before the first SDT_SPLITK_IN_KERNEL call, as for
  * gemm_f16_splitk).  The reduction writes only inside C (row stride ldc), in

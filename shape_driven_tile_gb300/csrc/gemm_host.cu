@@ -620,10 +620,15 @@ static int gemm_dispatch(int64_t M, int64_t N, int64_t K, const void *A, const v
 
 static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Workspace layout: fp32 partials [splits][Mp][Np] (M and N rounded up to whole
-// tiles), padded to 256 bytes, then one u32 arrival counter per output tile.
+// Workspace layout: one u32 arrival counter per output tile, padded to 256 bytes,
+// then the fp32 partials [splits][Mp][Np] (M and N rounded up to whole tiles).
+// The counters come first so that every configuration finds counter t at the same
+// place: a completed call leaves its counters at zero and never writes partials
+// over another configuration's counters, so a workspace zeroed once serves any
+// sequence of calls (any tile, split count or algorithm) that do not overlap.
+static size_t splitk_counter_bytes(int64_t tiles) { return (size_t(tiles) * 4 + 255) / 256 * 256; }
 static size_t splitk_partials_bytes(int64_t Mp, int64_t Np, int splits) {
-    return (size_t(splits) * size_t(Mp) * size_t(Np) * 4 + 255) / 256 * 256;
+    return size_t(splits) * size_t(Mp) * size_t(Np) * 4;
 }
 
 static int splitk_effective(int64_t nK, int splits) {
@@ -640,7 +645,7 @@ static size_t splitk_ws_bytes(const LadderTile &t, int64_t M, int64_t N, int64_t
     const int64_t nK = ceil_div(K, kBK);
     if (M <= 0 || N <= 0 || K <= 0 || splits < 1 || splits > nK) return 0;
     const int64_t mt = ceil_div(M, t.BM), nt = ceil_div(N, t.BN);
-    return splitk_partials_bytes(mt * t.BM, nt * t.BN, splitk_effective(nK, splits)) + size_t(mt * nt) * 4;
+    return splitk_counter_bytes(mt * nt) + splitk_partials_bytes(mt * t.BM, nt * t.BN, splitk_effective(nK, splits));
 }
 
 static bool splitk_feasible(const LadderTile &t, int64_t M, int64_t N, int64_t K, int smem_limit) {
@@ -731,9 +736,8 @@ static int splitk_launch_ex(int tile_id, int splits, int algo, int64_t M, int64_
     a.splits = splits;
     a.k_per_split = int(ceil_div(nK, splits));
     a.splitk_reduce_in_kernel = algo == SDT_SPLITK_IN_KERNEL ? 1 : 0;
-    a.partials = static_cast<float *>(ws);
-    a.counters = reinterpret_cast<unsigned *>(static_cast<char *>(ws) +
-                                              splitk_partials_bytes(mt * t.BM, nt * t.BN, splits));
+    a.counters = static_cast<unsigned *>(ws);
+    a.partials = reinterpret_cast<float *>(static_cast<char *>(ws) + splitk_counter_bytes(mt * nt));
     int e = kSplitLaunch[tile_id][layout & 3](tmA, tmB, a, stream);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -1017,8 +1021,7 @@ size_t sdt_splitk_workspace_bytes(int64_t M, int64_t N, int64_t K, int tile_id, 
     if (M <= 0 || N <= 0 || K <= 0 || !splitk_tile_ok(tile_id) || splits < 1) return 0;
     const LadderTile &t = kLadder[tile_id];
     if (M % t.BM || N % t.BN || K % kBK || splits > K / kBK) return 0;
-    const int sp = splitk_effective(K / kBK, splits);
-    return splitk_partials_bytes(M, N, sp) + size_t((M / t.BM) * (N / t.BN)) * 4;
+    return splitk_ws_bytes(t, M, N, K, splits);
 }
 
 int sdt_splitk_workspace_init(void *workspace, size_t workspace_bytes, sdt_stream_t stream) {

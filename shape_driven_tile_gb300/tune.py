@@ -154,6 +154,8 @@ class GemmProblem:
 
     # -- launching ----------------------------------------------------------------------
     def _workspace(self, nbytes: int) -> torch.Tensor:
+        """One workspace for every split candidate, zeroed when it is (re)allocated: the
+        library keeps a zeroed workspace valid across tiles, split counts and algorithms."""
         if self.ws is None or self.ws.numel() < nbytes:
             ws = torch.empty(max(nbytes, 256) + 256, dtype=torch.uint8, device=self.A.device)
             off = (-ws.data_ptr()) % 256

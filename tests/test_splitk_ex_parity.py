@@ -101,3 +101,23 @@ def test_errors(cuda_device):
     with pytest.raises(sdt.SdtError) as e:
         sdt.gemm_ex_splitk(A, B, workspace=ws[:64], tile="64x64", splits=1)
     assert e.value.status == "SDT_ERR_ARG"
+
+
+def test_one_workspace_serves_any_sequence_of_configurations(cuda_device):
+    # zeroed once, then in-kernel reductions with different tiles and split counts in turn
+    # (each configuration's partial planes must never land on another's counters)
+    M, N, K = 256, 384, 2048
+    A, Av = operand(M, K, False, torch.float16, 541, True, cuda_device)
+    B, Bv = operand(K, N, False, torch.float16, 542, True, cuda_device)
+    ref = ref_of(Av, Bv, torch.float16)
+    cfgs = [("64x64", 2), ("128x128", 5), ("64x128", 3), ("64x64", 7), ("128x64", 2), ("128x256", 4)]
+    need = max(sdt.splitk_ex_workspace_bytes(M, N, K, t, s) for t, s in cfgs)
+    ws = torch.zeros(need + 256, dtype=torch.uint8, device=cuda_device)
+    ws = ws[(-ws.data_ptr()) % 256:][:need]
+    for rep in range(2):
+        for tile, splits in cfgs:
+            for algo in (sdt.SPLITK_IN_KERNEL, sdt.SPLITK_REDUCE_KERNEL):
+                C = torch.full((M, N), float("nan"), dtype=torch.float16, device=cuda_device)
+                sdt.gemm_ex_splitk(A, B, C, workspace=ws, tile=tile, splits=splits, algo=algo)
+                sdt.check_device_status()
+                assert_bit_exact_f16(C, ref, f"{tile} s{splits} a{algo} rep{rep}")

@@ -14,7 +14,7 @@ def test_workspace_bytes(name):
         nk = K // 64
         kps = -(-nk // splits)
         eff = -(-nk // kps)
-        want = -(-(eff * M * N * 4) // 256) * 256 + (M // t["BM"]) * (N // t["BN"]) * 4
+        want = -(-((M // t["BM"]) * (N // t["BN"]) * 4) // 256) * 256 + eff * M * N * 4
         assert sdt.splitk_workspace_bytes(M, N, K, name, splits) == want
 
 
@@ -61,7 +61,7 @@ def test_ex_workspace_bytes_cover_whole_tiles(name):
             kps = -(-nk // splits)
             eff = -(-nk // kps)
             tiles = (Mp // t["BM"]) * (Np // t["BN"])
-            want = -(-(eff * Mp * Np * 4) // 256) * 256 + tiles * 4
+            want = -(-(tiles * 4) // 256) * 256 + eff * Mp * Np * 4
             assert sdt.splitk_ex_workspace_bytes(M, N, K, name, splits) == want
         # on shapes the tile divides, the same bytes as gemm_f16_splitk's workspace
         if M % t["BM"] == 0 and N % t["BN"] == 0 and K % 64 == 0:
