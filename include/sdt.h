@@ -141,6 +141,12 @@ typedef struct sdt_tile_desc {
     char name[24];    /* e.g. "128x256", "2cta_256x128" */
 } sdt_tile_desc;
 
+/* The ladder also holds "skinny" tiles, named s<BM>x<BN> (s128x16, s128x32), for
+ * problems with few rows (M up to a few tens): gemm_ex and gemm_ex_splitk run
+ * them on C^T = op(B)^T . op(A)^T so that the many output columns fill the MMA's
+ * 128 rows, and write C back transposed.  They need A stored M x K (K
+ * contiguous); sdt_feasible_tiles, pick_tile, gemm_f16, gemm_f16_splitk and the
+ * tune table never use them. */
 int sdt_num_tiles(void);
 /* Fills *out for tile `tile_id`; SDT_ERR_TILE for an unknown id, SDT_ERR_NULL for out == NULL. */
 int sdt_tile_info(int tile_id, sdt_tile_desc *out);

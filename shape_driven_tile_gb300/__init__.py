@@ -236,9 +236,13 @@ def pick_splitk(M: int, N: int, K: int, sm_count: int = 152, smem_limit: int = 2
 
 
 def tile_info(tile_id: int) -> dict:
+    """The ladder tile's description; "skinny" marks the tiles (named s<BM>x<BN>) that
+    gemm_ex and gemm_ex_splitk run with swapped operands and gemm_f16 never uses."""
     d = sdt_tile_desc()
     check(lib().sdt_tile_info(int(tile_id), ctypes.byref(d)))
-    return {f: (getattr(d, f).decode() if f == "name" else getattr(d, f)) for f, _ in d._fields_}
+    info = {f: (getattr(d, f).decode() if f == "name" else getattr(d, f)) for f, _ in d._fields_}
+    info["skinny"] = info["name"].startswith("s")
+    return info
 
 
 def tiles() -> list[dict]:

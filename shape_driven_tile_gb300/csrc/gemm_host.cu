@@ -39,7 +39,8 @@ using LaunchFn = int (*)(const CUtensorMap &, const CUtensorMap &, const GemmArg
 static const LaunchFn kSplitLaunch[][4] = {
     SDT_SPLIT4_(64, 64),   SDT_SPLIT4_(64, 128),  SDT_SPLIT4_(128, 64),  SDT_SPLIT4_(128, 128),
     SDT_SPLIT4_(128, 256), {nullptr, nullptr, nullptr, nullptr},     {nullptr, nullptr, nullptr, nullptr},
-    {nullptr, nullptr, nullptr, nullptr},         {nullptr, nullptr, nullptr, nullptr}};
+    {nullptr, nullptr, nullptr, nullptr},         {nullptr, nullptr, nullptr, nullptr},
+    SDT_SPLIT4_(128, 16),  SDT_SPLIT4_(128, 32)};
 
 // One rung of the tile ladder.  kt_cycles / fixed_cycles feed pick_tile's cost
 // model: SM cycles one CTA of this tile spends per 64-deep k-tile when it has
@@ -65,6 +66,7 @@ struct LadderTile {
     double kt_us;
     double per_mb_us;
     bool candidate;   // considered by pick_tile (tiles dominated everywhere in the sweep are not)
+    bool swap = false;  // skinny tile: runs C^T = op(B)^T . op(A)^T (gemm_ex forms only)
 };
 
 #define SDT_LAUNCH4_(FN, ...) {&FN<__VA_ARGS__, 0>, &FN<__VA_ARGS__, 1>, &FN<__VA_ARGS__, 2>, &FN<__VA_ARGS__, 3>}
@@ -81,6 +83,13 @@ struct LadderTile {
         128, BN_, 1, STAGES_, NAME_, SDT_LAUNCH4_(launch_gemm_persistent, BN_),                    \
             PersistentCfg<BN_>::STAGE_BYTES, PersistentCfg<BN_>::ALIGN_SLACK + PersistentCfg<BN_>::CTRL_BYTES, \
             PersistentCfg<BN_>::TMEM_COLS, PersistentCfg<BN_>::THREADS, true, FIX_, KT_, MB_, CAND_ \
+    }
+
+#define SDT_STILE(BN_, STAGES_, NAME_, FIX_, KT_, MB_)                                              \
+    LadderTile {                                                                                   \
+        128, BN_, 1, STAGES_, NAME_, SDT_LAUNCH4_(launch_gemm_tile, 128, BN_),                     \
+            TileCfg<128, BN_>::STAGE_BYTES, TileCfg<128, BN_>::ALIGN_SLACK + TileCfg<128, BN_>::CTRL_BYTES, \
+            TileCfg<128, BN_>::TMEM_COLS, TileCfg<128, BN_>::THREADS, false, FIX_, KT_, MB_, false, true \
     }
 
 #define SDT_PAIR(BN_, STAGES_, NAME_, FIX_, KT_, MB_, CAND_)                                        \
@@ -103,8 +112,16 @@ static const LadderTile kLadder[] = {
     SDT_PTILE(256, 4, "p128x256", 11.265, 0.37733, 0.00000, true),
     SDT_PAIR(128, 8, "2cta_256x128", 12.888, 0.29877, 0.00000, false),
     SDT_PAIR(256, 6, "2cta_256x256", 13.532, 0.32647, 0.00000, true),
+    // Skinny tiles for few-row problems (M up to a few tens, e.g. decode rows): the
+    // operands are swapped so that the many output columns fill the 128 MMA rows and
+    // the M rows become a 16- or 32-wide MMA N; the weights stream through a deep ring
+    // (18 / 20 KB per stage) and C is written transposed back.  gemm_ex and
+    // gemm_ex_splitk only; A must be stored M x K (K contiguous).
+    SDT_STILE(16, 12, "s128x16", 7.0, 0.25, 0.00000),
+    SDT_STILE(32, 11, "s128x32", 7.0, 0.25, 0.00000),
 };
 static constexpr int kNumTiles = sizeof(kLadder) / sizeof(kLadder[0]);
+static_assert(sizeof(kSplitLaunch) / sizeof(kSplitLaunch[0]) == kNumTiles, "one split-K row per ladder tile");
 static constexpr int kDefaultSmemLimit = 232448;  // opt-in shared memory per block on sm_100-class parts
 static constexpr int kMaxRing = 24;
 static constexpr int64_t kMaxDim = int64_t(1) << 30;
@@ -126,6 +143,7 @@ static int tile_stages(const LadderTile &t, int smem_limit, int req = 0) {
 static int tile_smem(const LadderTile &t, int stages) { return t.smem_fixed + stages * t.smem_per_stage; }
 
 static bool feasible(const LadderTile &t, int64_t M, int64_t N, int64_t K, int smem_limit) {
+    if (t.swap) return false;  // gemm_ex forms only
     if (M <= 0 || N <= 0 || K <= 0) return false;
     if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return false;
     if (M % t.BM || N % t.BN || K % kBK) return false;               // (i) divides the shape
@@ -381,13 +399,40 @@ static int tensor_map_2d(const void *ptr, int dtype, uint64_t inner, uint64_t ou
 // of a_rows (the rows one CTA stages) x 64; every other operand tile is loaded as
 // 64 x 64 boxes.
 static int operand_maps(const void *A, int64_t lda, const void *B, int64_t ldb, int64_t M, int64_t N, int64_t K,
-                        int dtype, int layout, int a_rows, CUtensorMap *tmA, CUtensorMap *tmB) {
+                        int dtype, int layout, int a_rows, CUtensorMap *tmA, CUtensorMap *tmB, int b_rows = 64) {
     const bool a_t = layout & SDT_LAYOUT_A_T, b_t = layout & SDT_LAYOUT_B_T;
     int rc = a_t ? tensor_map_2d(A, dtype, uint64_t(M), uint64_t(K), uint64_t(lda) * 2, 64, tmA)
                  : tensor_map_2d(A, dtype, uint64_t(K), uint64_t(M), uint64_t(lda) * 2, a_rows, tmA);
     if (rc) return rc;
-    return b_t ? tensor_map_2d(B, dtype, uint64_t(K), uint64_t(N), uint64_t(ldb) * 2, 64, tmB)
+    return b_t ? tensor_map_2d(B, dtype, uint64_t(K), uint64_t(N), uint64_t(ldb) * 2, b_rows, tmB)
                : tensor_map_2d(B, dtype, uint64_t(N), uint64_t(K), uint64_t(ldb) * 2, 64, tmB);
+}
+
+// A gemm_ex problem as the kernels see it.  Skinny (swap) tiles compute
+// C^T = op(B)^T . op(A)^T: the new A is op(B)^T (stored as B is, with the
+// transposed bit flipped), the new B is op(A)^T (A stored M x K becomes a
+// K-contiguous [M][K] operand of N = M columns), and C is written transposed.
+struct ExProblem {
+    int64_t M, N, K;
+    const void *A;
+    int64_t lda;
+    const void *B;
+    int64_t ldb;
+    int layout;
+    int c_trans;
+};
+
+static int ex_problem(const LadderTile &t, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
+                      const void *B, int64_t ldb, int layout, ExProblem *out) {
+    if (!t.swap) {
+        *out = ExProblem{M, N, K, A, lda, B, ldb, layout, 0};
+        return SDT_OK;
+    }
+    if (layout & SDT_LAYOUT_A_T)
+        return fail(SDT_ERR_TILE, "skinny tile %s needs A stored M x K (K contiguous)", t.name);
+    const int new_layout = ((layout & SDT_LAYOUT_B_T) ? 0 : SDT_LAYOUT_A_T) | SDT_LAYOUT_B_T;
+    *out = ExProblem{N, M, K, B, ldb, A, lda, new_layout, 1};
+    return SDT_OK;
 }
 
 // Instruction-descriptor bits for the types and majors: fp32 accumulator (bit 4),
@@ -416,6 +461,19 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ partials, uint16_
             a1.x += b1.x; a1.y += b1.y; a1.z += b1.z; a1.w += b1.w;
         }
         *reinterpret_cast<uint4 *>(C + r * ldc + c) = pack8_f32(a0, a1, bf16 != 0);
+    }
+}
+
+__global__ void splitk_reduce_trans_kernel(const float *__restrict__ partials, uint16_t *__restrict__ C,
+                                           int64_t M, int64_t N, int64_t Mp, int64_t Np, int64_t ldc, int splits,
+                                           int bf16) {
+    const int64_t total = M * N, plane = Mp * Np;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t r = i % M, c = i / M;
+        const float *src = partials + r * Np + c;
+        float a = src[0];
+        for (int sp = 1; sp < splits; ++sp) a += src[sp * plane];
+        C[c * ldc + r] = f32_to_16(a, bf16 != 0);
     }
 }
 
@@ -469,12 +527,18 @@ static int validate_common(int64_t M, int64_t N, int64_t K, const void *A, const
 
 // Launches ladder tile `tile_id` on validated, non-empty arguments with K > 0
 // (any shape: tiles overhang ragged edges; layouts and type per the flags).
-static int run_tile_ex(int tile_id, int stagger_req, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
-                       const void *B, int64_t ldb, void *C, int64_t ldc, int dtype, int layout, cudaStream_t stream,
-                       const DeviceInfo &dev, int raster_req = 0, int stages_req = 0) {
+static int run_tile_ex(int tile_id, int stagger_req, int64_t M0, int64_t N0, int64_t K0, const void *A0,
+                       int64_t lda0, const void *B0, int64_t ldb0, void *C, int64_t ldc, int dtype, int layout0,
+                       cudaStream_t stream, const DeviceInfo &dev, int raster_req = 0, int stages_req = 0) {
     const LadderTile &t = kLadder[tile_id];
+    ExProblem ex;
+    int rc = ex_problem(t, M0, N0, K0, A0, lda0, B0, ldb0, layout0, &ex);
+    if (rc) return rc;
+    const int64_t M = ex.M, N = ex.N, K = ex.K, lda = ex.lda, ldb = ex.ldb;
+    const void *A = ex.A, *B = ex.B;
+    const int layout = ex.layout;
     CUtensorMap tmA, tmB;
-    int rc = operand_maps(A, lda, B, ldb, M, N, K, dtype, layout, t.BM / t.cta_group, &tmA, &tmB);
+    rc = operand_maps(A, lda, B, ldb, M, N, K, dtype, layout, t.BM / t.cta_group, &tmA, &tmB, t.BN < 64 ? t.BN : 64);
     if (rc) return rc;
     int *status = nullptr;
     rc = status_word(&status);
@@ -499,6 +563,7 @@ static int run_tile_ex(int tile_id, int stagger_req, int64_t M, int64_t N, int64
     a.max_ctas = dev.sm_count * ctas_per_sm(t, dev.smem_per_sm);
     a.ldc = int(ldc);
     a.idesc_flags = idesc_flags_for(dtype, layout);
+    a.c_trans = ex.c_trans;
     if (int64_t(a.num_m_tiles) * a.num_n_tiles > int64_t(0x3fffffff))
         return fail(SDT_ERR_SHAPE, "grid too large");
     const int tiles = a.num_m_tiles * a.num_n_tiles;
@@ -649,6 +714,7 @@ static size_t splitk_ws_bytes(const LadderTile &t, int64_t M, int64_t N, int64_t
 }
 
 static bool splitk_feasible(const LadderTile &t, int64_t M, int64_t N, int64_t K, int smem_limit) {
+    if (t.swap) return false;  // gemm_ex_splitk only
     if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return false;
     if (M % t.BM || N % t.BN || K % kBK) return false;
     return tile_smem(t, t.stages) <= smem_limit && t.tmem_cols <= 512;
@@ -695,10 +761,16 @@ static int pick_splitk_for(int64_t M, int64_t N, int64_t K, int sm_count, int sm
 // on validated, non-empty operands with K > 0; any shape (tiles overhang ragged
 // edges: the TMA reads zeros outside the operands, the partial planes are whole
 // tiles, the reduction writes only inside C), either layout bit, fp16 or bf16.
-static int splitk_launch_ex(int tile_id, int splits, int algo, int64_t M, int64_t N, int64_t K, const void *A,
-                            int64_t lda, const void *B, int64_t ldb, void *C, int64_t ldc, int dtype, int layout,
+static int splitk_launch_ex(int tile_id, int splits, int algo, int64_t M0, int64_t N0, int64_t K0, const void *A0,
+                            int64_t lda0, const void *B0, int64_t ldb0, void *C, int64_t ldc, int dtype, int layout0,
                             void *ws, size_t ws_bytes, cudaStream_t stream, const DeviceInfo &dev) {
     const LadderTile &t = kLadder[tile_id];
+    ExProblem ex;
+    int rc0 = ex_problem(t, M0, N0, K0, A0, lda0, B0, ldb0, layout0, &ex);
+    if (rc0) return rc0;
+    const int64_t M = ex.M, N = ex.N, K = ex.K, lda = ex.lda, ldb = ex.ldb;
+    const void *A = ex.A, *B = ex.B;
+    const int layout = ex.layout;
     const int64_t nK = ceil_div(K, kBK);
     if (splits < 1 || splits > nK) return fail(SDT_ERR_ARG, "splits must be in 1..%lld", (long long)nK);
     splits = splitk_effective(nK, splits);
@@ -710,7 +782,7 @@ static int splitk_launch_ex(int tile_id, int splits, int algo, int64_t M, int64_
     if (ws_bytes < need)
         return fail(SDT_ERR_ARG, "workspace of %zu bytes is smaller than the %zu bytes needed", ws_bytes, need);
     CUtensorMap tmA, tmB;
-    int rc = operand_maps(A, lda, B, ldb, M, N, K, dtype, layout, t.BM, &tmA, &tmB);
+    int rc = operand_maps(A, lda, B, ldb, M, N, K, dtype, layout, t.BM, &tmA, &tmB, t.BN < 64 ? t.BN : 64);
     if (rc) return rc;
     int *status = nullptr;
     rc = status_word(&status);
@@ -719,6 +791,7 @@ static int splitk_launch_ex(int tile_id, int splits, int algo, int64_t M, int64_
     memset(&a, 0, sizeof a);
     a.ldc = int(ldc);
     a.idesc_flags = idesc_flags_for(dtype, layout);
+    a.c_trans = ex.c_trans;
     a.C = static_cast<__half *>(C);
     a.M = int(M);
     a.N = int(N);
@@ -744,10 +817,15 @@ static int splitk_launch_ex(int tile_id, int splits, int algo, int64_t M, int64_
         return fail(SDT_ERR_LAUNCH, "split-K launch of tile %s failed: %s", t.name, cudaGetErrorString(cudaError_t(e)));
     }
     if (algo == SDT_SPLITK_REDUCE_KERNEL) {
-        const int64_t total = M * (N / 8);
+        const int64_t total = ex.c_trans ? M * N : M * (N / 8);
         const unsigned blocks = unsigned(std::min<int64_t>((total + 255) / 256, int64_t(dev.sm_count) * 8));
-        splitk_reduce_kernel<<<blocks, 256, 0, stream>>>(a.partials, static_cast<uint16_t *>(C), M, N, mt * t.BM,
-                                                         nt * t.BN, ldc, splits, dtype == SDT_DTYPE_BF16 ? 1 : 0);
+        if (ex.c_trans)
+            splitk_reduce_trans_kernel<<<blocks, 256, 0, stream>>>(a.partials, static_cast<uint16_t *>(C), M, N,
+                                                                   mt * t.BM, nt * t.BN, ldc, splits,
+                                                                   dtype == SDT_DTYPE_BF16 ? 1 : 0);
+        else
+            splitk_reduce_kernel<<<blocks, 256, 0, stream>>>(a.partials, static_cast<uint16_t *>(C), M, N, mt * t.BM,
+                                                             nt * t.BN, ldc, splits, dtype == SDT_DTYPE_BF16 ? 1 : 0);
         cudaError_t e2 = cudaGetLastError();
         if (e2 != cudaSuccess) return fail(SDT_ERR_LAUNCH, "split-K reduction launch failed: %s", cudaGetErrorString(e2));
     }
@@ -1020,7 +1098,7 @@ size_t sdt_splitk_workspace_bytes(int64_t M, int64_t N, int64_t K, int tile_id, 
     clear_error();
     if (M <= 0 || N <= 0 || K <= 0 || !splitk_tile_ok(tile_id) || splits < 1) return 0;
     const LadderTile &t = kLadder[tile_id];
-    if (M % t.BM || N % t.BN || K % kBK || splits > K / kBK) return 0;
+    if (t.swap || M % t.BM || N % t.BN || K % kBK || splits > K / kBK) return 0;
     return splitk_ws_bytes(t, M, N, K, splits);
 }
 
@@ -1057,7 +1135,8 @@ int gemm_ex_splitk(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, 
 size_t sdt_splitk_ex_workspace_bytes(int64_t M, int64_t N, int64_t K, int tile_id, int splits) {
     clear_error();
     if (!splitk_tile_ok(tile_id)) return 0;
-    return splitk_ws_bytes(kLadder[tile_id], M, N, K, splits);
+    const LadderTile &t = kLadder[tile_id];
+    return t.swap ? splitk_ws_bytes(t, N, M, K, splits) : splitk_ws_bytes(t, M, N, K, splits);
 }
 
 int sdt_pick_splitk_any_for(int64_t M, int64_t N, int64_t K, int sm_count, int smem_limit, int *tile_id,

@@ -63,6 +63,7 @@ struct GemmArgs {
     int num_items;
     int ldc;                // row stride of C in elements
     uint32_t idesc_flags;   // instruction-descriptor bits: accumulator, operand types, operand majors
+    int c_trans;            // 1: element (r, c) of this problem is C[c * ldc + r] (operands swapped)
 };
 
 // Operand layouts, a template parameter of every GEMM kernel: bit 0 set means A is
@@ -137,6 +138,11 @@ __device__ __forceinline__ void store_row32(void *crow, const uint32_t (&r)[32],
         if (8 * v + 8 <= ncols) dst[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
 }
 
+// One fp32 value -> fp16 or bf16 bits (round to nearest even).
+__device__ __forceinline__ uint16_t f32_to_16(float v, bool bf16) {
+    return bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(v)) : __half_as_ushort(__float2half_rn(v));
+}
+
 // Eight fp32 values -> eight fp16 or bf16 (round to nearest even), packed for one 16-byte store.
 __device__ __forceinline__ uint4 pack8_f32(const float4 &a, const float4 &b, bool bf16) {
     const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
@@ -160,7 +166,7 @@ struct TileCfg {
     static constexpr int B_BYTES = BN * kBK * 2;
     static constexpr int B_BOX_BYTES = 64 * kBK * 2;  // one 64-column box of B
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int TMEM_COLS = BN;               // fp32 accumulator columns (power of two)
+    static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;  // fp32 accumulator columns (power of two, >= 32)
     static constexpr int THREADS = 128;
     static constexpr int ALIGN_SLACK = 1024;           // dynamic smem base rounded up to 1024 B
     static constexpr int CTRL_BYTES = 512;             // barriers + TMEM address + flags
@@ -168,7 +174,7 @@ struct TileCfg {
         return ALIGN_SLACK + stages * STAGE_BYTES + CTRL_BYTES;
     }
     static_assert(BM == 64 || BM == 128, "BM must be 64 or 128");
-    static_assert(BN == 64 || BN == 128 || BN == 256, "BN must be 64, 128 or 256");
+    static_assert(BN == 16 || BN == 32 || BN == 64 || BN == 128 || BN == 256, "BN must be 16 .. 256");
 };
 
 __device__ __forceinline__ void record_status(int *status, int code) {
@@ -264,7 +270,8 @@ __global__ void __launch_bounds__(128, 1)
             const uint32_t fb = smem_u32(&full[s]);
             mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
             load_operand<false, L::A_MN, BM, BM>(smem_u32(smA + s * Cfg::A_BYTES), &tmA, fb, kt, m0);
-            load_operand<false, L::B_MN, BN, 64>(smem_u32(smB + s * Cfg::B_BYTES), &tmB, fb, kt, n0);
+            // (tiles narrower than 64 columns take K-major B only: boxes of BN rows)
+            load_operand<false, L::B_MN, BN, (BN < 64 ? BN : 64)>(smem_u32(smB + s * Cfg::B_BYTES), &tmB, fb, kt, n0);
             ctrl[2] = i + 1;
             if (++s == S) { s = 0; phase ^= 1u; }
         }
@@ -312,20 +319,33 @@ __global__ void __launch_bounds__(128, 1)
         // 32-column stores below need no column mask on ragged shapes
         const size_t Mp = static_cast<size_t>(p.num_m_tiles) * BM, Np = static_cast<size_t>(p.num_n_tiles) * BN;
         float *prow = SPLIT ? p.partials + (static_cast<size_t>(split) * Mp + m0 + row) * Np + n0 : nullptr;
+        constexpr int CH = BN < 32 ? BN : 32;  // accumulator columns per TMEM load
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = 0; c < BN; c += CH) {
             uint32_t r[32];
-            tmem_ld_32x32b_x32(taddr_row + c, r);
+            if (CH == 32) tmem_ld_32x32b_x32(taddr_row + c, r);
+            else tmem_ld_32x32b_x16(taddr_row + c, r);
             tmem_ld_wait();
             if (SPLIT) {
                 if (row_valid && acc_ok) {
                     uint4 *dst = reinterpret_cast<uint4 *>(prow + c);
 #pragma unroll
-                    for (int t = 0; t < 8; ++t) dst[t] = make_uint4(r[4 * t], r[4 * t + 1], r[4 * t + 2], r[4 * t + 3]);
+                    for (int t = 0; t < CH / 4; ++t) dst[t] = make_uint4(r[4 * t], r[4 * t + 1], r[4 * t + 2], r[4 * t + 3]);
                 }
                 continue;
             }
-            if (row_valid && acc_ok) store_row32(crow + c, r, p.N - (n0 + c), bf16);
+            if (!(row_valid && acc_ok)) continue;
+            if (p.c_trans) {
+                // swapped operands: this accumulator row is column m0 + row of C; lanes hold
+                // consecutive rows, so each store instruction writes 32 neighbouring elements
+                uint16_t *ccol = reinterpret_cast<uint16_t *>(p.C) + m0 + row;
+#pragma unroll
+                for (int t = 0; t < CH; ++t)
+                    if (n0 + c + t < p.N)
+                        ccol[static_cast<size_t>(n0 + c + t) * p.ldc] = f32_to_16(__uint_as_float(r[t]), bf16);
+            } else {
+                store_row32(crow + c, r, p.N - (n0 + c), bf16);
+            }
         }
     }
     tc_fence_before();
@@ -351,7 +371,7 @@ __global__ void __launch_bounds__(128, 1)
                 uint16_t *crow = reinterpret_cast<uint16_t *>(p.C) + static_cast<size_t>(m0 + row) * p.ldc + n0;
                 const bool bf16 = ((p.idesc_flags >> 7) & 7u) == 1u;
 #pragma unroll 1
-                for (int c = 0; c < BN && n0 + c < p.N; c += 8) {  // N % 8 == 0: whole 8-column vectors
+                for (int c = 0; c < BN && n0 + c < p.N; c += 8) {  // N % 8 == 0 unless transposed
                     float4 a0 = __ldcg(reinterpret_cast<const float4 *>(src + c));
                     float4 a1 = __ldcg(reinterpret_cast<const float4 *>(src + c + 4));
                     for (int sp = 1; sp < p.splits; ++sp) {
@@ -360,7 +380,15 @@ __global__ void __launch_bounds__(128, 1)
                         a0.x += b0.x; a0.y += b0.y; a0.z += b0.z; a0.w += b0.w;
                         a1.x += b1.x; a1.y += b1.y; a1.z += b1.z; a1.w += b1.w;
                     }
-                    *reinterpret_cast<uint4 *>(crow + c) = pack8_f32(a0, a1, bf16);
+                    if (p.c_trans) {
+                        const float v[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                        uint16_t *ccol = reinterpret_cast<uint16_t *>(p.C) + m0 + row;
+#pragma unroll
+                        for (int t = 0; t < 8; ++t)
+                            if (n0 + c + t < p.N) ccol[static_cast<size_t>(n0 + c + t) * p.ldc] = f32_to_16(v[t], bf16);
+                    } else {
+                        *reinterpret_cast<uint4 *>(crow + c) = pack8_f32(a0, a1, bf16);
+                    }
                 }
             }
             if (threadIdx.x == 0) atomicExch(&p.counters[lin], 0u);
@@ -391,6 +419,11 @@ __global__ void __launch_bounds__(128, 1)
 // handles 8 consecutive columns of one row.
 __global__ void splitk_reduce_kernel(const float *__restrict__ partials, uint16_t *__restrict__ C, int64_t M,
                                      int64_t N, int64_t Mp, int64_t Np, int64_t ldc, int splits, int bf16);
+// The same for swapped operands: element (r, c) of the problem goes to C[c * ldc + r];
+// one element per thread, consecutive threads on consecutive r (coalesced stores).
+__global__ void splitk_reduce_trans_kernel(const float *__restrict__ partials, uint16_t *__restrict__ C,
+                                           int64_t M, int64_t N, int64_t Mp, int64_t Np, int64_t ldc, int splits,
+                                           int bf16);
 
 // Host-side launchers, instantiated per ladder tile and layout (gemm_t*.cu).
 template <int BM, int BN, int LAYOUT>

@@ -19,7 +19,7 @@ SIZES = [0, 64, 128, 192, 256, 320, 512, 768, 1000, 1024, 1536, 1984, 2048, 2304
 
 
 def ladder():
-    return sdt.tiles()
+    return [t for t in sdt.tiles() if not t["skinny"]]  # the skinny tiles are gemm_ex-only
 
 
 @pytest.mark.parametrize("smem", [SMEM, 150_000, 100_000, 50_000])
@@ -145,3 +145,16 @@ def test_tune_table_rejects_bad_entries(tmp_path, body, needle):
 def test_tune_table_missing_file():
     with pytest.raises(sdt.SdtError):
         sdt.load_tune_table("/nonexistent/table.txt")
+
+
+def test_skinny_tiles_are_never_feasible_for_gemm_f16():
+    skinny = [t["id"] for t in sdt.tiles() if t["skinny"]]
+    assert len(skinny) == 2
+    for M, N, K in [(128, 16, 128), (256, 32, 4096), (256, 64, 4096), (4096, 4096, 4096)]:
+        feas = sdt.feasible_tiles(M, N, K, smem_limit=232448)
+        assert not set(skinny) & set(feas)
+        if feas:
+            assert sdt.pick_tile(M, N, K, sm_count=152) not in skinny
+    for t in skinny:
+        assert sdt.splitk_workspace_bytes(256, 32, 4096, t, 2) == 0        # not gemm_f16_splitk
+        assert sdt.splitk_ex_workspace_bytes(16, 4096, 4096, t, 2) > 0     # gemm_ex_splitk
