@@ -674,14 +674,11 @@ def run_reference(args):
 # ---------------------------------------------------------------------------------------------
 
 
-class L2Flush:
-    def __init__(self, dev, nbytes=512 << 20):
-        import torch
+def L2Flush(dev):
+    """A read of 4x the L2 size before each timed launch (shape_driven_tile_gb300.tune.L2Flush)."""
+    from shape_driven_tile_gb300 import tune
 
-        self.buf = torch.empty(nbytes // 4, dtype=torch.float32, device=dev)
-
-    def __call__(self):
-        self.buf.zero_()
+    return tune.L2Flush(dev)
 
 
 def time_cold(fn, reps, flush, stream):

@@ -133,13 +133,30 @@ class _Env:
                 os.environ[k] = v
 
 
+class L2Flush:
+    """Leaves L2 holding clean lines of an unrelated buffer: a read of 4x the L2 size.
+
+    A flush by writing (zeroing a large buffer) leaves L2 full of dirty lines, and
+    the next kernel then pays for their write-back inside its timed region -- up to
+    the whole L2 (~129 MB) of extra DRAM writes, which on a memory-bound launch of
+    tens of microseconds inflates its time by a fifth or more.  A read pass evicts
+    the previous launch's operands just the same and leaves nothing to write back.
+    """
+
+    def __init__(self, device, nbytes: int = 512 << 20):
+        self.buf = torch.ones(nbytes // 4, dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.buf.sum()
+
+
 class GemmProblem:
     """One problem C = op(A) . op(B) on the GPU and the candidates of each round.
 
     A is [M, K] row-major; B is the logical [K, N] operand as a view (row-major, or
     the transpose of a row-major [N, K] tensor); C is [M, N] row-major.  Latency of
-    a configuration: mean device time of `reps` launches, each after writing a
-    buffer larger than L2 (CUDA events on the current stream around the launch).
+    a configuration: mean device time of `reps` launches, each after an L2 flush
+    (``L2Flush``; CUDA events on the current stream around the launch).
     """
 
     def __init__(self, A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, reps: int = 10,
@@ -148,7 +165,7 @@ class GemmProblem:
         self.M, self.K = A.shape
         self.N = B.shape[1]
         self.dtype = A.dtype
-        self.flush = torch.empty(flush_bytes // 4, dtype=torch.float32, device=A.device)
+        self.flush = L2Flush(A.device, flush_bytes)
         self.ws = None
         self.ntiles = len(sdt.tiles())
 
@@ -196,7 +213,7 @@ class GemmProblem:
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(self.reps)]
         for e0, e1 in evs:
-            self.flush.zero_()
+            self.flush()
             e0.record(stream)
             run()
             e1.record(stream)
