@@ -245,9 +245,11 @@ int sdt_pick_tile_any_for(int64_t M, int64_t N, int64_t K, int sm_count, int sme
  * takes the picked count).  The k-loop stagger is not applied.
  *
  * Workspace: device memory owned by the caller, 256-byte aligned, at least
- * sdt_splitk_workspace_bytes(M,N,K,tile_id,splits) bytes: one u32 counter per
- * output tile (padded to 256 B), then fp32 partials [splits][M][N].  The
- * counters must be zero before the first SDT_SPLITK_IN_KERNEL call on a
+ * sdt_splitk_workspace_bytes(M,N,K,tile_id,splits) bytes: a fixed 1 MiB region
+ * of u32 counters (the in-kernel reduction uses one per output tile, at most
+ * 262144 tiles; stream-K one per tile and TMEM lane quarter), then fp32
+ * partials [splits][M][N].  The counter region has the same place and size in
+ * every configuration.  The counters must be zero before the first SDT_SPLITK_IN_KERNEL call on a
  * workspace (sdt_splitk_workspace_init zeroes a workspace on `stream`); every
  * completed call leaves them zero again and writes partials only after the
  * counter region, so a workspace zeroed once serves any sequence of split-K
@@ -260,6 +262,7 @@ int sdt_pick_tile_any_for(int64_t M, int64_t N, int64_t K, int sm_count, int sme
  */
 #define SDT_SPLITK_REDUCE_KERNEL 0
 #define SDT_SPLITK_IN_KERNEL 1
+#define SDT_SPLITK_STREAM 2 /* stream-K; see sdt_streamk_workspace_bytes */
 int gemm_f16_splitk(int64_t M, int64_t N, int64_t K, const void *A, const void *B, void *C,
                     void *workspace, size_t workspace_bytes, int tile_id, int splits, int algo,
                     sdt_stream_t stream);
@@ -281,8 +284,7 @@ int sdt_pick_splitk_for(int64_t M, int64_t N, int64_t K, int sm_count, int smem_
  * round 2, with the operands of P3 "Changes"]: caller row strides, either
  * transposed operand, fp16 or bf16, and shapes no tile divides.  Arguments and
  * requirements as gemm_ex, plus the split-K arguments of gemm_f16_splitk.
- * The partial planes cover whole tiles: one u32 counter per output tile
- * (padded to 256 B), then [splits][ceil(M/BM)*BM][ceil(N/BN)*BN] fp32; the
+ * The partial planes cover whole tiles: the 1 MiB counter region, then [splits][ceil(M/BM)*BM][ceil(N/BN)*BN] fp32; the
  * workspace (shareable with gemm_f16_splitk calls) must hold
  * sdt_splitk_ex_workspace_bytes(M,N,K,tile_id,splits) bytes (256-byte
  * aligned; counters zero before the first SDT_SPLITK_IN_KERNEL call, as for
@@ -296,6 +298,32 @@ int gemm_ex_splitk(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, 
 /* Bytes of workspace gemm_ex_splitk needs for any shape (0 for a tile without split-K form,
  * splits outside 1..ceil(K/64), or a non-positive dimension). */
 size_t sdt_splitk_ex_workspace_bytes(int64_t M, int64_t N, int64_t K, int tile_id, int splits);
+/*
+ * Stream-K [P4 "The Six Rounds", round 2: a fixed number of workgroups share the
+ * whole iteration space, a workgroup's share may end inside an output tile, and
+ * the partial tiles are fixed up afterwards].  algo = SDT_SPLITK_STREAM in
+ * gemm_f16_splitk / gemm_ex_splitk, with `splits` read as the CTA count G
+ * (<= 0: one CTA per SM slot, sdt_streamk_ctas; lowered to the unit count when
+ * larger).  The units are (output tile, 64-deep k-tile) pairs, tiles in banded
+ * raster order and k-tiles in order; CTA g takes units
+ * [floor(g*U/G), floor((g+1)*U/G)).  Whole tiles are stored directly; a CTA's
+ * first and last tile may be partial: it writes an fp32 partial tile to its
+ * slots (2g, 2g+1) and counts its arrival on per-(tile, TMEM lane quarter)
+ * counters; the last CTA to arrive sums the tile's partials in CTA order,
+ * writes C and zeroes the counter.  Same tiles as split-K (the one-CTA rungs
+ * and the skinny tiles), any shape and layout gemm_ex takes.
+ * Workspace: the 1 MiB counter region shared with split-K (zero before the
+ * first call, left zero by every completed call), then 2*G fp32 tiles of
+ * BM x BN: sdt_streamk_workspace_bytes(M,N,K,tile_id,G) bytes (G >= 1, taken
+ * as at most the unit count; 0 for
+ * a tile without stream-K form, a non-positive dimension, more than 65536
+ * output tiles or more than 2^20 CTAs).
+ */
+size_t sdt_streamk_workspace_bytes(int64_t M, int64_t N, int64_t K, int tile_id, int ctas);
+/* Default stream-K CTA count of a tile: SMs x CTAs of its kernel per SM (needs no GPU). */
+int sdt_streamk_ctas_for(int tile_id, int sm_count, int smem_limit);
+/* The same on the current device. */
+int sdt_streamk_ctas(int tile_id);
 /* sdt_pick_splitk_for's model over the split-K tiles for any shape (tiles may overhang). */
 int sdt_pick_splitk_any_for(int64_t M, int64_t N, int64_t K, int sm_count, int smem_limit,
                             int *tile_id, int *splits);

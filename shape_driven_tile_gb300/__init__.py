@@ -20,6 +20,7 @@ __all__ = [
     "debug_timeout_probe", "device_sm_count", "lib", "gemm_f16_splitk", "splitk_workspace",
     "splitk_workspace_bytes", "pick_splitk", "pick_tile_any", "gemm_ex_splitk",
     "splitk_ex_workspace_bytes", "pick_splitk_any", "SPLITK_REDUCE_KERNEL", "SPLITK_IN_KERNEL", "gemm_ex",
+    "SPLITK_STREAM", "streamk_ctas", "streamk_workspace_bytes",
 ]
 
 
@@ -167,6 +168,7 @@ def gemm_ex(A, B, C=None, *, tile=-1, stream=None):
 
 SPLITK_REDUCE_KERNEL = 0
 SPLITK_IN_KERNEL = 1
+SPLITK_STREAM = 2  # stream-K: `splits` is the CTA count (<= 0: one per SM slot)
 
 
 def splitk_workspace_bytes(M: int, N: int, K: int, tile, splits: int) -> int:
@@ -217,6 +219,23 @@ def gemm_ex_splitk(A, B, C=None, *, workspace, tile=-1, splits: int = 0, algo: i
                                DTYPE_CODES[A.dtype], layout, workspace.data_ptr(), nbytes, tid, int(splits),
                                int(algo), _stream(stream)))
     return C
+
+
+def streamk_ctas(tile, sm_count: int | None = None, smem_limit: int = 232448) -> int:
+    """Default stream-K CTA count of a tile (SMs x CTAs per SM); current device when sm_count is None."""
+    tid = tile_id(tile) if isinstance(tile, str) else int(tile)
+    if sm_count is None:
+        return check(lib().sdt_streamk_ctas(tid))
+    return check(lib().sdt_streamk_ctas_for(tid, int(sm_count), int(smem_limit)))
+
+
+def streamk_workspace_bytes(M: int, N: int, K: int, tile, ctas: int | None = None) -> int:
+    """Workspace bytes of gemm_ex_splitk / gemm_f16_splitk with algo=SPLITK_STREAM and `ctas`
+    CTAs (None: the tile's default count on the current device)."""
+    tid = tile_id(tile) if isinstance(tile, str) else int(tile)
+    if ctas is None or ctas <= 0:
+        ctas = streamk_ctas(tid)
+    return int(lib().sdt_streamk_workspace_bytes(M, N, K, tid, int(ctas)))
 
 
 def pick_splitk_any(M: int, N: int, K: int, sm_count: int = 152, smem_limit: int = 232448):

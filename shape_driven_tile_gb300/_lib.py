@@ -61,6 +61,9 @@ SIGNATURES = {
                               cint, vp]),
     "sdt_splitk_ex_workspace_bytes": (ctypes.c_size_t, [i64, i64, i64, cint, cint]),
     "sdt_pick_splitk_any_for": (cint, [i64, i64, i64, cint, cint, ctypes.POINTER(cint), ctypes.POINTER(cint)]),
+    "sdt_streamk_workspace_bytes": (ctypes.c_size_t, [i64, i64, i64, cint, cint]),
+    "sdt_streamk_ctas_for": (cint, [cint, cint, cint]),
+    "sdt_streamk_ctas": (cint, [cint]),
 }
 
 STATUS = {

@@ -25,6 +25,7 @@
 #include "gemm_kernel.cuh"
 #include "gemm_persistent.cuh"
 #include "gemm_pair.cuh"
+#include "gemm_streamk.cuh"
 #include "host_common.cuh"
 
 namespace sdt {
@@ -41,6 +42,16 @@ static const LaunchFn kSplitLaunch[][4] = {
     SDT_SPLIT4_(128, 256), {nullptr, nullptr, nullptr, nullptr},     {nullptr, nullptr, nullptr, nullptr},
     {nullptr, nullptr, nullptr, nullptr},         {nullptr, nullptr, nullptr, nullptr},
     SDT_SPLIT4_(128, 16),  SDT_SPLIT4_(128, 32)};
+
+// Stream-K launchers of the same rungs (null: no stream-K form).
+#define SDT_STREAM4_(BM, BN)                                                                       \
+    {&launch_gemm_streamk<BM, BN, 0>, &launch_gemm_streamk<BM, BN, 1>, &launch_gemm_streamk<BM, BN, 2>, \
+     &launch_gemm_streamk<BM, BN, 3>}
+static const LaunchFn kStreamLaunch[][4] = {
+    SDT_STREAM4_(64, 64),   SDT_STREAM4_(64, 128),  SDT_STREAM4_(128, 64),  SDT_STREAM4_(128, 128),
+    SDT_STREAM4_(128, 256), {nullptr, nullptr, nullptr, nullptr},       {nullptr, nullptr, nullptr, nullptr},
+    {nullptr, nullptr, nullptr, nullptr},           {nullptr, nullptr, nullptr, nullptr},
+    SDT_STREAM4_(128, 16),  SDT_STREAM4_(128, 32)};
 
 // One rung of the tile ladder.  kt_cycles / fixed_cycles feed pick_tile's cost
 // model: SM cycles one CTA of this tile spends per 64-deep k-tile when it has
@@ -122,6 +133,7 @@ static const LadderTile kLadder[] = {
 };
 static constexpr int kNumTiles = sizeof(kLadder) / sizeof(kLadder[0]);
 static_assert(sizeof(kSplitLaunch) / sizeof(kSplitLaunch[0]) == kNumTiles, "one split-K row per ladder tile");
+static_assert(sizeof(kStreamLaunch) / sizeof(kStreamLaunch[0]) == kNumTiles, "one stream-K row per ladder tile");
 static constexpr int kDefaultSmemLimit = 232448;  // opt-in shared memory per block on sm_100-class parts
 static constexpr int kMaxRing = 24;
 static constexpr int64_t kMaxDim = int64_t(1) << 30;
@@ -685,13 +697,15 @@ static int gemm_dispatch(int64_t M, int64_t N, int64_t K, const void *A, const v
 
 static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Workspace layout: one u32 arrival counter per output tile, padded to 256 bytes,
-// then the fp32 partials [splits][Mp][Np] (M and N rounded up to whole tiles).
-// The counters come first so that every configuration finds counter t at the same
-// place: a completed call leaves its counters at zero and never writes partials
-// over another configuration's counters, so a workspace zeroed once serves any
-// sequence of calls (any tile, split count or algorithm) that do not overlap.
-static size_t splitk_counter_bytes(int64_t tiles) { return (size_t(tiles) * 4 + 255) / 256 * 256; }
+// Workspace layout: a fixed 1 MiB region of u32 arrival counters (split-K in-kernel:
+// one per output tile; stream-K: one per output tile and TMEM lane quarter), then the
+// fp32 partials.  The counter region has the same place and size for every shape,
+// tile, split count and algorithm: a completed call leaves its counters at zero and
+// writes partials only past the region, so a workspace zeroed once serves any
+// sequence of calls that do not overlap on the GPU.
+static constexpr size_t kCounterRegionBytes = size_t(1) << 20;
+static constexpr int64_t kMaxCounters = int64_t(kCounterRegionBytes / 4);
+static size_t splitk_counter_bytes(int64_t) { return kCounterRegionBytes; }
 static size_t splitk_partials_bytes(int64_t Mp, int64_t Np, int splits) {
     return size_t(splits) * size_t(Mp) * size_t(Np) * 4;
 }
@@ -776,6 +790,8 @@ static int splitk_launch_ex(int tile_id, int splits, int algo, int64_t M0, int64
     splits = splitk_effective(nK, splits);
     const int64_t mt = ceil_div(M, t.BM), nt = ceil_div(N, t.BN);
     if (mt * nt > int64_t(0x3fffffff)) return fail(SDT_ERR_SHAPE, "grid too large");
+    if (algo == SDT_SPLITK_IN_KERNEL && mt * nt > kMaxCounters)
+        return fail(SDT_ERR_SHAPE, "the in-kernel reduction counts at most %lld output tiles", (long long)kMaxCounters);
     const size_t need = splitk_ws_bytes(t, M, N, K, splits);
     if (!ws) return fail(SDT_ERR_NULL, "split-K needs a workspace");
     if (reinterpret_cast<uintptr_t>(ws) & 255) return fail(SDT_ERR_ALIGN, "the workspace must be 256-byte aligned");
@@ -832,14 +848,107 @@ static int splitk_launch_ex(int tile_id, int splits, int algo, int64_t M0, int64
     return SDT_OK;
 }
 
+// ---- stream-K ---------------------------------------------------------------------
+
+static constexpr int64_t kMaxStreamUnits = int64_t(1) << 40;  // keeps (u + 1) * G within 64 bits
+static constexpr int64_t kMaxStreamCtas = int64_t(1) << 20;
+
+static bool streamk_tile_ok(int tile_id) {
+    return tile_id >= 0 && tile_id < kNumTiles && kStreamLaunch[tile_id][0] != nullptr;
+}
+
+// CTAs of tile t's stream-K kernel that fit on one SM: shared memory at the ring depth
+// the launch uses, two TMEM accumulators of BN columns, 192 threads.
+static int streamk_ctas_per_sm(const LadderTile &t, int smem_limit, int smem_per_sm) {
+    const int by_smem = smem_per_sm / (tile_smem(t, tile_stages(t, smem_limit)) + 1024);
+    const int tmem = 2 * t.BN < 32 ? 32 : 2 * t.BN;
+    int occ = std::min(by_smem, 512 / tmem);
+    occ = std::min(occ, 2048 / 192);
+    return occ < 1 ? 1 : occ;
+}
+
+// Workspace bytes of stream-K with tile t and `ctas` CTAs (lowered to the unit count)
+// on an M x N x K problem as the kernel sees it (swapped for a skinny tile), 0 for an
+// invalid combination: the counter region, then two fp32 BM x BN partial tiles per CTA.
+static size_t streamk_ws_bytes(const LadderTile &t, int64_t M, int64_t N, int64_t K, int64_t ctas) {
+    if (M <= 0 || N <= 0 || K <= 0 || ctas < 1 || ctas > kMaxStreamCtas) return 0;
+    const int64_t tiles = ceil_div(M, t.BM) * ceil_div(N, t.BN);
+    const int64_t units = tiles * ceil_div(K, kBK);
+    if (4 * tiles > kMaxCounters || units > kMaxStreamUnits) return 0;
+    return kCounterRegionBytes + size_t(2 * std::min(ctas, units)) * size_t(t.BM) * size_t(t.BN) * 4;
+}
+
+// Launches stream-K with tile `tile_id` (which has a stream-K form and fits on chip) on
+// validated, non-empty operands with K > 0; ctas <= 0 takes one CTA per SM slot.  The
+// CTA count is lowered to the number of (tile, k-tile) units when it is larger.
+static int streamk_launch_ex(int tile_id, int64_t ctas, int64_t M0, int64_t N0, int64_t K0, const void *A0,
+                             int64_t lda0, const void *B0, int64_t ldb0, void *C, int64_t ldc, int dtype, int layout0,
+                             void *ws, size_t ws_bytes, cudaStream_t stream, const DeviceInfo &dev) {
+    const LadderTile &t = kLadder[tile_id];
+    ExProblem ex;
+    int rc = ex_problem(t, M0, N0, K0, A0, lda0, B0, ldb0, layout0, &ex);
+    if (rc) return rc;
+    const int64_t M = ex.M, N = ex.N, K = ex.K;
+    const int64_t nK = ceil_div(K, kBK);
+    const int64_t mt = ceil_div(M, t.BM), nt = ceil_div(N, t.BN);
+    if (4 * mt * nt > kMaxCounters)
+        return fail(SDT_ERR_SHAPE, "stream-K counts at most %lld output tiles", (long long)(kMaxCounters / 4));
+    const int64_t units = mt * nt * nK;
+    if (units > kMaxStreamUnits) return fail(SDT_ERR_SHAPE, "too many (tile, k-tile) units for stream-K");
+    if (ctas <= 0) ctas = int64_t(dev.sm_count) * streamk_ctas_per_sm(t, dev.smem_optin, dev.smem_per_sm);
+    if (ctas > kMaxStreamCtas) return fail(SDT_ERR_ARG, "stream-K takes at most %lld CTAs", (long long)kMaxStreamCtas);
+    ctas = std::min(ctas, units);
+    const size_t need = streamk_ws_bytes(t, M, N, K, ctas);
+    if (!ws) return fail(SDT_ERR_NULL, "stream-K needs a workspace");
+    if (reinterpret_cast<uintptr_t>(ws) & 255) return fail(SDT_ERR_ALIGN, "the workspace must be 256-byte aligned");
+    if (ws_bytes < need)
+        return fail(SDT_ERR_ARG, "workspace of %zu bytes is smaller than the %zu bytes needed", ws_bytes, need);
+    CUtensorMap tmA, tmB;
+    rc = operand_maps(ex.A, ex.lda, ex.B, ex.ldb, M, N, K, dtype, ex.layout, t.BM, &tmA, &tmB, t.BN < 64 ? t.BN : 64);
+    if (rc) return rc;
+    int *status = nullptr;
+    rc = status_word(&status);
+    if (rc) return rc;
+    GemmArgs a;
+    memset(&a, 0, sizeof a);
+    a.ldc = int(ldc);
+    a.idesc_flags = idesc_flags_for(dtype, ex.layout);
+    a.c_trans = ex.c_trans;
+    a.C = static_cast<__half *>(C);
+    a.M = int(M);
+    a.N = int(N);
+    a.K = int(K);
+    a.num_m_tiles = int(mt);
+    a.num_n_tiles = int(nt);
+    a.num_k_tiles = int(nK);
+    a.stages = tile_stages(t, dev.smem_optin);
+    a.stagger_stride = 1;
+    a.raster_group = env_int("SDT_RASTER_GROUP", 8, 1, 1 << 20);
+    a.timeout_ns = wait_timeout_ns();
+    a.status = status;
+    a.max_ctas = int(ctas);
+    a.splits = int(ctas);
+    a.counters = static_cast<unsigned *>(ws);
+    a.partials = reinterpret_cast<float *>(static_cast<char *>(ws) + kCounterRegionBytes);
+    int e = kStreamLaunch[tile_id][ex.layout & 3](tmA, tmB, a, stream);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(SDT_ERR_LAUNCH, "stream-K launch of tile %s failed: %s", t.name, cudaGetErrorString(cudaError_t(e)));
+    }
+    return SDT_OK;
+}
+
+static bool splitk_algo_ok(int algo) {
+    return algo == SDT_SPLITK_REDUCE_KERNEL || algo == SDT_SPLITK_IN_KERNEL || algo == SDT_SPLITK_STREAM;
+}
+
 // gemm_f16_splitk: tight row-major fp16, the tile must divide the shape.
 static int splitk_run(int64_t M, int64_t N, int64_t K, const void *A, const void *B, void *C, void *ws,
                       size_t ws_bytes, int tile_id, int splits, int algo, cudaStream_t stream) {
     int rc = validate_common(M, N, K, A, B, C);
     if (rc) return rc;
     if (M == 0 || N == 0) return SDT_OK;
-    if (algo != SDT_SPLITK_REDUCE_KERNEL && algo != SDT_SPLITK_IN_KERNEL)
-        return fail(SDT_ERR_ARG, "unknown split-K algorithm %d", algo);
+    if (!splitk_algo_ok(algo)) return fail(SDT_ERR_ARG, "unknown split-K algorithm %d", algo);
     DeviceInfo dev;
     rc = current_device(&dev);
     if (rc) return rc;
@@ -848,13 +957,16 @@ static int splitk_run(int64_t M, int64_t N, int64_t K, const void *A, const void
         int sp = 1;
         rc = pick_splitk_for(M, N, K, dev.sm_count, dev.smem_optin, dev.smem_per_sm, &tile_id, &sp);
         if (rc) return rc;
-        if (splits <= 0) splits = sp;
+        if (splits <= 0 && algo != SDT_SPLITK_STREAM) splits = sp;
     }
     if (!splitk_tile_ok(tile_id)) return fail(SDT_ERR_TILE, "tile %d has no split-K form", tile_id);
     const LadderTile &t = kLadder[tile_id];
     if (!splitk_feasible(t, M, N, K, dev.smem_optin))
         return fail(SDT_ERR_TILE, "tile %s does not divide %lldx%lldx%lld", t.name, (long long)M, (long long)N,
                     (long long)K);
+    if (algo == SDT_SPLITK_STREAM)
+        return streamk_launch_ex(tile_id, splits, M, N, K, A, K, B, N, C, N, SDT_DTYPE_F16, 0, ws, ws_bytes, stream,
+                                 dev);
     return splitk_launch_ex(tile_id, splits, algo, M, N, K, A, K, B, N, C, N, SDT_DTYPE_F16, 0, ws, ws_bytes, stream,
                             dev);
 }
@@ -938,8 +1050,7 @@ static int gemm_ex_splitk_impl(int64_t M, int64_t N, int64_t K, const void *A, i
                                int tile_id, int splits, int algo, cudaStream_t stream) {
     int rc = validate_ex(M, N, K, A, lda, B, ldb, C, ldc, dtype, layout);
     if (rc || M == 0 || N == 0) return rc;
-    if (algo != SDT_SPLITK_REDUCE_KERNEL && algo != SDT_SPLITK_IN_KERNEL)
-        return fail(SDT_ERR_ARG, "unknown split-K algorithm %d", algo);
+    if (!splitk_algo_ok(algo)) return fail(SDT_ERR_ARG, "unknown split-K algorithm %d", algo);
     if (tile_id < -1 || tile_id >= kNumTiles) return fail(SDT_ERR_TILE, "unknown tile id %d", tile_id);
     DeviceInfo dev;
     rc = current_device(&dev);
@@ -949,10 +1060,13 @@ static int gemm_ex_splitk_impl(int64_t M, int64_t N, int64_t K, const void *A, i
         int sp = 1;
         rc = pick_splitk_any(M, N, K, dev.sm_count, dev.smem_optin, dev.smem_per_sm, &tile_id, &sp);
         if (rc) return rc;
-        if (splits <= 0) splits = sp;
+        if (splits <= 0 && algo != SDT_SPLITK_STREAM) splits = sp;
     }
     if (!splitk_tile_ok(tile_id)) return fail(SDT_ERR_TILE, "tile %d has no split-K form", tile_id);
     if (!fits_chip(kLadder[tile_id], dev.smem_optin)) return fail(SDT_ERR_TILE, "tile %d does not fit", tile_id);
+    if (algo == SDT_SPLITK_STREAM)
+        return streamk_launch_ex(tile_id, splits, M, N, K, A, lda, B, ldb, C, ldc, dtype, layout, ws, ws_bytes,
+                                 stream, dev);
     return splitk_launch_ex(tile_id, splits, algo, M, N, K, A, lda, B, ldb, C, ldc, dtype, layout, ws, ws_bytes,
                             stream, dev);
 }
@@ -1139,6 +1253,26 @@ size_t sdt_splitk_ex_workspace_bytes(int64_t M, int64_t N, int64_t K, int tile_i
     return t.swap ? splitk_ws_bytes(t, N, M, K, splits) : splitk_ws_bytes(t, M, N, K, splits);
 }
 
+size_t sdt_streamk_workspace_bytes(int64_t M, int64_t N, int64_t K, int tile_id, int ctas) {
+    clear_error();
+    if (!streamk_tile_ok(tile_id)) return 0;
+    const LadderTile &t = kLadder[tile_id];
+    return t.swap ? streamk_ws_bytes(t, N, M, K, ctas) : streamk_ws_bytes(t, M, N, K, ctas);
+}
+int sdt_streamk_ctas_for(int tile_id, int sm_count, int smem_limit) {
+    clear_error();
+    if (!streamk_tile_ok(tile_id)) return fail(SDT_ERR_TILE, "tile %d has no stream-K form", tile_id);
+    if (sm_count <= 0 || smem_limit <= 0) return fail(SDT_ERR_ARG, "sm_count and smem_limit must be positive");
+    return sm_count * streamk_ctas_per_sm(kLadder[tile_id], smem_limit, 233472);
+}
+int sdt_streamk_ctas(int tile_id) {
+    clear_error();
+    if (!streamk_tile_ok(tile_id)) return fail(SDT_ERR_TILE, "tile %d has no stream-K form", tile_id);
+    DeviceInfo dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    return dev.sm_count * streamk_ctas_per_sm(kLadder[tile_id], dev.smem_optin, dev.smem_per_sm);
+}
 int sdt_pick_splitk_any_for(int64_t M, int64_t N, int64_t K, int sm_count, int smem_limit, int *tile_id,
                             int *splits) {
     clear_error();

@@ -9,6 +9,7 @@
 #include "gemm_kernel.cuh"
 #include "gemm_persistent.cuh"
 #include "gemm_pair.cuh"
+#include "gemm_streamk.cuh"
 #include "launch.cuh"
 
 namespace sdt {
@@ -53,6 +54,19 @@ int launch_gemm_tile_split(const CUtensorMap &tmA, const CUtensorMap &tmB, const
     const dim3 grid(static_cast<unsigned>(args.num_m_tiles) * static_cast<unsigned>(args.num_n_tiles),
                     static_cast<unsigned>(args.splits), 1);
     return launch_kernel(kern, grid, dim3(Cfg::THREADS), size_t(smem), stream, 1, tmA, tmB, args);
+}
+
+// Stream-K form: args.splits CTAs share the (tile, k-tile) units.
+template <int BM, int BN, int LAYOUT>
+int launch_gemm_streamk(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args,
+                        cudaStream_t stream) {
+    using Cfg = StreamCfg<BM, BN>;
+    auto kern = gemm_streamk_kernel<BM, BN, LAYOUT>;
+    const int smem = Cfg::smem_bytes(args.stages);
+    static std::atomic<int> configured[64];
+    if (int e = ensure_smem(kern, smem, configured)) return e;
+    return launch_kernel(kern, dim3(static_cast<unsigned>(args.splits)), dim3(Cfg::THREADS), size_t(smem), stream, 1,
+                         tmA, tmB, args);
 }
 
 template <int BN, int LAYOUT>
@@ -102,6 +116,10 @@ int launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmA
 #define SDT_TILE_SPLIT_ONE_(BM, BN, L)                                                               \
     template int sdt::launch_gemm_tile_split<BM, BN, L>(const CUtensorMap &, const CUtensorMap &,    \
                                                         const sdt::GemmArgs &, cudaStream_t);
+#define SDT_TILE_STREAM_ONE_(BM, BN, L)                                                              \
+    template int sdt::launch_gemm_streamk<BM, BN, L>(const CUtensorMap &, const CUtensorMap &,       \
+                                                     const sdt::GemmArgs &, cudaStream_t);
 #define SDT_INSTANTIATE_GEMM_TILE(BM, BN)                                                            \
     SDT_LAYOUTS_(SDT_TILE_ONE_, BM, BN)                                                              \
-    SDT_LAYOUTS_(SDT_TILE_SPLIT_ONE_, BM, BN)
+    SDT_LAYOUTS_(SDT_TILE_SPLIT_ONE_, BM, BN)                                                        \
+    SDT_LAYOUTS_(SDT_TILE_STREAM_ONE_, BM, BN)
