@@ -925,7 +925,8 @@ def run_p4(args):
         if args.table_out:
             out["table"] = write_tune_table(args.table_out, [
                 (r["M"], r["N"], r["K"], r["tuned"]) for r in rows
-                if r["dtype"] == "f16" and r["layout"] == "NN" and r["tuned"]["splits"] == 1],
+                if r["dtype"] == "f16" and r["layout"] == "NN" and r["tuned"]["splits"] == 1
+                and r["tuned"]["algo"] != sdt.SPLITK_STREAM],
                 "coordinate descent, bench.py --mode p4 --tune")
     print(json.dumps(out), flush=True)
 

@@ -362,32 +362,60 @@ __global__ void __launch_bounds__(128, 1)
         __syncthreads();
         if (ctrl[3]) {
             __threadfence();
-            const int row = (BM == 128) ? (warp * 32 + lane) : (warp * 16 + lane);
-            if ((BM == 128 || lane < 16) && m0 + row < p.M && !ctrl[1]) {
-                const size_t Mp = static_cast<size_t>(p.num_m_tiles) * BM;
+            const int vrows = min(BM, p.M - m0);  // rows of the tile inside C
+            if (vrows > 0 && !ctrl[1]) {
+                // The tile's rows inside C, 8 consecutive columns per thread and step (a
+                // warp reads whole sectors of a partial row), up to four steps per pass:
+                // every load of a split in a pass is issued before any of it is used.
                 const size_t Np = static_cast<size_t>(p.num_n_tiles) * BN;
-                const size_t plane = Mp * Np;
-                const float *src = p.partials + static_cast<size_t>(m0 + row) * Np + n0;
-                uint16_t *crow = reinterpret_cast<uint16_t *>(p.C) + static_cast<size_t>(m0 + row) * p.ldc + n0;
+                const size_t plane = static_cast<size_t>(p.num_m_tiles) * BM * Np;
+                const float *src0 = p.partials + static_cast<size_t>(m0) * Np + n0;
                 const bool bf16 = ((p.idesc_flags >> 7) & 7u) == 1u;
+                const int total = vrows * BN;
+                constexpr int STEP = Cfg::THREADS * 8;
 #pragma unroll 1
-                for (int c = 0; c < BN && n0 + c < p.N; c += 8) {  // N % 8 == 0 unless transposed
-                    float4 a0 = __ldcg(reinterpret_cast<const float4 *>(src + c));
-                    float4 a1 = __ldcg(reinterpret_cast<const float4 *>(src + c + 4));
-                    for (int sp = 1; sp < p.splits; ++sp) {
-                        const float4 b0 = __ldcg(reinterpret_cast<const float4 *>(src + sp * plane + c));
-                        const float4 b1 = __ldcg(reinterpret_cast<const float4 *>(src + sp * plane + c + 4));
-                        a0.x += b0.x; a0.y += b0.y; a0.z += b0.z; a0.w += b0.w;
-                        a1.x += b1.x; a1.y += b1.y; a1.z += b1.z; a1.w += b1.w;
-                    }
-                    if (p.c_trans) {
-                        const float v[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                        uint16_t *ccol = reinterpret_cast<uint16_t *>(p.C) + m0 + row;
+                for (int e0 = static_cast<int>(threadIdx.x) * 8; e0 < total; e0 += 4 * STEP) {
+                    float4 acc[8];
+#pragma unroll 2
+                    for (int sp = 0; sp < p.splits; ++sp) {
+                        float4 x[8];
 #pragma unroll
-                        for (int t = 0; t < 8; ++t)
-                            if (n0 + c + t < p.N) ccol[static_cast<size_t>(n0 + c + t) * p.ldc] = f32_to_16(v[t], bf16);
-                    } else {
-                        *reinterpret_cast<uint4 *>(crow + c) = pack8_f32(a0, a1, bf16);
+                        for (int i = 0; i < 4; ++i) {
+                            const int e = e0 + i * STEP;
+                            const float *src = src0 + sp * plane + static_cast<size_t>(e / BN) * Np + (e % BN);
+                            if (e < total) {
+                                x[2 * i] = __ldcg(reinterpret_cast<const float4 *>(src));
+                                x[2 * i + 1] = __ldcg(reinterpret_cast<const float4 *>(src + 4));
+                            } else {
+                                x[2 * i] = x[2 * i + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            }
+                        }
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            if (sp == 0) {
+                                acc[i] = x[i];
+                            } else {
+                                acc[i].x += x[i].x; acc[i].y += x[i].y; acc[i].z += x[i].z; acc[i].w += x[i].w;
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int e = e0 + i * STEP;
+                        if (e >= total) continue;
+                        const int r = e / BN, c = e % BN;
+                        if (n0 + c >= p.N) continue;
+                        if (p.c_trans) {
+                            const float v[8] = {acc[2 * i].x, acc[2 * i].y, acc[2 * i].z, acc[2 * i].w,
+                                                acc[2 * i + 1].x, acc[2 * i + 1].y, acc[2 * i + 1].z, acc[2 * i + 1].w};
+                            uint16_t *ccol = reinterpret_cast<uint16_t *>(p.C) + m0 + r;
+#pragma unroll
+                            for (int t = 0; t < 8; ++t)
+                                if (n0 + c + t < p.N) ccol[static_cast<size_t>(n0 + c + t) * p.ldc] = f32_to_16(v[t], bf16);
+                        } else {  // N % 8 == 0 unless transposed
+                            uint16_t *crow = reinterpret_cast<uint16_t *>(p.C) + static_cast<size_t>(m0 + r) * p.ldc + n0;
+                            *reinterpret_cast<uint4 *>(crow + c) = pack8_f32(acc[2 * i], acc[2 * i + 1], bf16);
+                        }
                     }
                 }
             }

@@ -285,7 +285,10 @@ __global__ void __launch_bounds__(192, 1)
                     }
                 }
             }
-            if (!whole) {
+            // A quarter with no row inside C takes no part in the fix-up (every CTA of
+            // the tile skips it alike, so its counter stays untouched).
+            const int row0 = BM == 128 ? q * 32 : q * 16;
+            if (!whole && m0 + row0 < p.M) {
                 // Publish this quarter's partial rows, then count the arrival on the
                 // (tile, quarter) counter; the last of the tile's CTAs to arrive sums.
                 __threadfence();
@@ -300,21 +303,53 @@ __global__ void __launch_bounds__(192, 1)
                 last = __shfl_sync(0xffffffffu, last, 0);
                 if (last) {
                     __threadfence();
-                    if (row_ok) {
-                        // slot of CTA g for this tile: 2g when the tile is g's first, else 2g+1
-                        const int lo_slot = 2 * g_lo + (sk_first_unit(g_lo, G, U) / nK == tile ? 0 : 1);
+                    // The quarter's rows (32, or 16 for BM = 64) x BN columns, 256 elements
+                    // per step: lane l takes 8 consecutive columns, so each load of the
+                    // warp reads whole 32-byte sectors of a slot row and each store
+                    // writes 16 bytes of a C row.  Partial rows beyond M were never
+                    // written and are not stored.
+                    constexpr int R = BM == 128 ? 32 : 16;
+                    static_assert((R * BN) % 1024 == 0 || R * BN == 256 || R * BN == 512, "whole steps");
+                    const int vrows = min(R, p.M - m0 - row0);      // rows of the quarter inside C
+                    const int steps = (vrows * BN + 255) / 256;      // 256 elements per step
+                    // slot of CTA g for this tile: 2g when the tile is g's first, else 2g+1
+                    const int lo_slot = 2 * g_lo + (sk_first_unit(g_lo, G, U) / nK == tile ? 0 : 1);
+                    // Up to four steps at a time: for each CTA in order, all of its loads of
+                    // those steps are issued before any is used; the sum starts from the
+                    // first CTA's partial and adds the others in CTA order.
 #pragma unroll 1
-                        for (int c = 0; c < BN; c += 8) {
-                            float4 a = make_float4(0.f, 0.f, 0.f, 0.f), bq = a;
-                            for (int g = g_lo; g <= g_hi; ++g) {
-                                const int sl = g == g_lo ? lo_slot : 2 * g;
-                                const float *src = p.partials + (static_cast<size_t>(sl) * BM + r) * BN + c;
-                                const float4 x0 = __ldcg(reinterpret_cast<const float4 *>(src));
-                                const float4 x1 = __ldcg(reinterpret_cast<const float4 *>(src + 4));
-                                a.x += x0.x; a.y += x0.y; a.z += x0.z; a.w += x0.w;
-                                bq.x += x1.x; bq.y += x1.y; bq.z += x1.z; bq.w += x1.w;
+                    for (int st0 = 0; st0 < steps; st0 += 4) {
+                        float4 acc[8];
+#pragma unroll 2
+                        for (int g = g_lo; g <= g_hi; ++g) {
+                            const int sl = g == g_lo ? lo_slot : 2 * g;
+                            const float *slot_base = p.partials + static_cast<size_t>(sl) * BM * BN;
+                            float4 x[8];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int e = (st0 + i) * 256 + lane * 8;
+                                const float *src = slot_base + static_cast<size_t>(row0) * BN + e;
+                                if (st0 + i < steps) {
+                                    x[2 * i] = __ldcg(reinterpret_cast<const float4 *>(src));
+                                    x[2 * i + 1] = __ldcg(reinterpret_cast<const float4 *>(src + 4));
+                                } else {
+                                    x[2 * i] = x[2 * i + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                                }
                             }
-                            sk_store8(p, m0 + r, n0 + c, a, bq, bf16);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                if (g == g_lo) {
+                                    acc[i] = x[i];
+                                } else {
+                                    acc[i].x += x[i].x; acc[i].y += x[i].y; acc[i].z += x[i].z; acc[i].w += x[i].w;
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int e = (st0 + i) * 256 + lane * 8;
+                            const int rr = row0 + e / BN, cc = e % BN;
+                            if (st0 + i < steps && rr - row0 < vrows) sk_store8(p, m0 + rr, n0 + cc, acc[2 * i], acc[2 * i + 1], bf16);
                         }
                     }
                     __syncwarp();

@@ -15,12 +15,14 @@ Groups for this library's kernels:
                      tiles overhang ragged edges) with its ring depth (the
                      page opens DepthU in this round; 0 = the tile's own depth,
                      deeper rings are clamped to what fits in shared memory)
-  2. ``split-K``  -- split count and reduction algorithm with the tile pinned
-                     (gemm_ex_splitk, a form of the one-CTA tiles only: when the
-                     held tile is persistent or a CTA pair, the round opens the
-                     split-capable tiles too; candidates the library rejects are
-                     dropped before timing, as the page's legality filter drops
-                     configurations that cannot be generated)
+  2. ``split-K``  -- split count and reduction algorithm with the tile pinned,
+                     and stream-K (the page's other choice in this round) with
+                     one CTA per SM slot or one per SM (gemm_ex_splitk, forms of
+                     the one-CTA tiles only: when the held tile is persistent or
+                     a CTA pair, the round opens the split-capable tiles too;
+                     candidates the library rejects are dropped before timing, as
+                     the page's legality filter drops configurations that cannot
+                     be generated)
   3. ``mapping``  -- how CTAs land on the output: the raster band height (m-tiles
                      per band) and the k-loop start stagger
   4. ``tail``     -- the two-CTA 256x256 tile's tail as half-width items or not
@@ -183,8 +185,13 @@ class GemmProblem:
 
     def launcher(self, cfg: dict):
         """A no-argument callable that launches cfg, or None when cfg is illegal here."""
-        if cfg["splits"] > 1:
-            nbytes = sdt.splitk_ex_workspace_bytes(self.M, self.N, self.K, cfg["tile"], cfg["splits"])
+        if cfg["algo"] == sdt.SPLITK_STREAM or cfg["splits"] > 1:
+            if cfg["algo"] == sdt.SPLITK_STREAM:
+                if sdt.lib().sdt_streamk_workspace_bytes(self.M, self.N, self.K, cfg["tile"], 1) == 0:
+                    return None  # no stream-K form
+                nbytes = sdt.streamk_workspace_bytes(self.M, self.N, self.K, cfg["tile"], cfg["splits"] or None)
+            else:
+                nbytes = sdt.splitk_ex_workspace_bytes(self.M, self.N, self.K, cfg["tile"], cfg["splits"])
             if nbytes == 0:
                 return None
             ws = self._workspace(nbytes)
@@ -238,14 +245,18 @@ class GemmProblem:
             # opens the split-capable tiles with it; the held configuration stays a
             # candidate either way.  Candidates without a split-K form for the shape are
             # dropped by measure()'s legality check.
-            if held["splits"] > 1:
+            if held["splits"] > 1 or held["algo"] == sdt.SPLITK_STREAM:
                 return
             own = sdt.splitk_ex_workspace_bytes(self.M, self.N, self.K, held["tile"], 2) > 0
             tiles = [held["tile"]] if own else range(self.ntiles)
+            sms = sdt.device_sm_count()
             for t in tiles:
                 for s in SPLITS:
                     for a in (sdt.SPLITK_REDUCE_KERNEL, sdt.SPLITK_IN_KERNEL):
                         yield dict(held, tile=t, splits=s, algo=a)
+                # stream-K: one CTA per SM slot (0), and one per SM
+                for g in (0, sms):
+                    yield dict(held, tile=t, splits=g, algo=sdt.SPLITK_STREAM)
 
         def mapping(held):
             for r in RASTER:
