@@ -878,15 +878,23 @@ def run_p4(args):
         if names and name not in names:
             continue
         for dtype in (torch.float16, torch.bfloat16):
+            if args.dtypes and ("f16" if dtype == torch.float16 else "bf16") not in args.dtypes:
+                continue
             for layout in ("NN", "TN"):
+                if args.layouts and layout not in args.layouts:
+                    continue
                 A_h, B_h = inputs.p4_operands(M, N, K, layout, seed=inputs.seed_for(6 + si, 0), dtype=dtype)
                 A = A_h.to(dev)
                 B = B_h.to(dev) if layout == "NN" else B_h.to(dev).t()
                 C = torch.empty((M, N), dtype=dtype, device=dev)
                 prob = tune.GemmProblem(A, B, C, reps=args.reps)
                 start = prob.start()
+                if args.tile:  # a given configuration instead of the library's pick
+                    start = dict(tune.DEFAULTS, tile=sdt.tile_id(args.tile), splits=args.splits, algo=args.algo)
                 row = {"shape": name, "M": M, "N": N, "K": K, "dtype": "f16" if dtype == torch.float16 else "bf16",
                        "layout": layout, "pick": sdt.tile_info(start["tile"])["name"]}
+                if args.tile:
+                    row["config"] = {"tile": args.tile, "splits": args.splits, "algo": args.algo}
                 if args.tune:
                     held, traj = prob.tune()
                     row["rounds"] = {t["round"]: round(t["us"], 2) for t in traj}
@@ -895,6 +903,8 @@ def run_p4(args):
                     us = traj[-1]["us"]
                 else:
                     us = prob.measure(start)
+                    if us is None:
+                        raise SystemExit(f"configuration {start} is not legal for {name}")
                 flops = gemm_flops(M, N, K)
                 nbytes = 2 * (M * K + K * N + M * N)
                 bound_us = max(flops / (peaks["tflops"] * 1e12), nbytes / (peaks["hbm_gbs"] * 1e9)) * 1e6
@@ -1100,7 +1110,11 @@ def main(argv=None):
     ap.add_argument("--gemv", choices=["bf16", "q8"])
     ap.add_argument("--reps", type=int, default=20)
     ap.add_argument("--sizes", type=int, nargs="*")
-    ap.add_argument("--tile")
+    ap.add_argument("--tile", help="one/kscan/sweep: the tile; p4: time this tile instead of the pick")
+    ap.add_argument("--splits", type=int, default=1, help="p4 with --tile: split count (stream-K: CTA count, 0 = default)")
+    ap.add_argument("--algo", type=int, default=0, help="p4 with --tile: 0/1 split-K reduction, 2 stream-K")
+    ap.add_argument("--dtypes", nargs="*", choices=["f16", "bf16"], help="p4: operand types to run (default both)")
+    ap.add_argument("--layouts", nargs="*", choices=["NN", "TN"], help="p4: layouts to run (default both)")
     ap.add_argument("--with-kscan", action="store_true")
     ap.add_argument("--shapes", nargs="*", help="extra GEMM shapes MxNxK for --mode sweep; shape names for --mode p4")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
