@@ -227,7 +227,7 @@ int gemm_ex(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const v
 int sdt_pick_tile_any_for(int64_t M, int64_t N, int64_t K, int sm_count, int smem_limit);
 
 /*
- * Split-K [P4 "The Six Rounds", round 2 "Split-K": the contraction is split
+ * Split-K [P4 "The Six Rounds", the "Split-K" step: the contraction is split
  * across CTAs and the partial results are reduced; the page distinguishes a
  * reduction in a separate pass from one inside the single kernel].
  *
@@ -281,7 +281,7 @@ int sdt_pick_splitk_for(int64_t M, int64_t N, int64_t K, int sm_count, int smem_
 
 /*
  * gemm_ex_splitk -- split-K in gemm_ex's general form [P4 "The Six Rounds",
- * round 2, with the operands of P3 "Changes"]: caller row strides, either
+ * the split-K step, with the operands of P3 "Changes"]: caller row strides, either
  * transposed operand, fp16 or bf16, and shapes no tile divides.  Arguments and
  * requirements as gemm_ex, plus the split-K arguments of gemm_f16_splitk.
  * The partial planes cover whole tiles: the 1 MiB counter region, then [splits][ceil(M/BM)*BM][ceil(N/BN)*BN] fp32; the
@@ -299,7 +299,7 @@ int gemm_ex_splitk(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, 
  * splits outside 1..ceil(K/64), or a non-positive dimension). */
 size_t sdt_splitk_ex_workspace_bytes(int64_t M, int64_t N, int64_t K, int tile_id, int splits);
 /*
- * Stream-K [P4 "The Six Rounds", round 2: a fixed number of workgroups share the
+ * Stream-K [P4 "The Six Rounds", the split-K step: a fixed number of workgroups share the
  * whole iteration space, a workgroup's share may end inside an output tile, and
  * the partial tiles are fixed up afterwards].  algo = SDT_SPLITK_STREAM in
  * gemm_f16_splitk / gemm_ex_splitk, with `splits` read as the CTA count G

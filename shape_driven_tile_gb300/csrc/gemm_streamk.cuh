@@ -1,7 +1,7 @@
 // gemm_streamk.cuh -- stream-K form of the one-CTA ladder tiles.
 //
 // "Iteratively Tuning hipBLASLt TensileLite Kernels", section "The Six Rounds",
-// round 2: besides splitting K into equal slices per output tile, the page's
+// the split-K step: besides splitting K into equal slices per output tile, the page's
 // kernels can run "Stream-K", where a fixed number of workgroups share the whole
 // iteration space and a workgroup's slice may end part-way through an output
 // tile, the partial tiles being fixed up afterwards.  Here the iteration space is

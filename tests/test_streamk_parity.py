@@ -67,7 +67,7 @@ def test_cta_counts(cuda_device, tile, ctas):
 
 @pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("M,N,K", [(1, 8, 64), (16, 16, 4096), (16, 4096, 16384), (16, 8192, 4096), (3, 200, 65),
-                                   (33, 1000, 3000), (1, 4096, 64)])
+                                   (33, 1000, 3000), (1, 4096, 64), (5, 40, 17), (130, 136, 1), (64, 64, 63)])
 def test_decode_and_tiny_shapes(cuda_device, tile, M, N, K):
     for dt in DTYPES.values():
         A, Av = operand(M, K, False, dt, 721, True, cuda_device)
