@@ -374,9 +374,11 @@ def run_default(args):
             raise sdt.SdtError(rc, (L.sdt_last_error() or b"").decode())
 
     launches_per_step = len(SWEEP) + 2
+    t_warm = time.perf_counter()
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
+    warmup_s = time.perf_counter() - t_warm
     sdt.check_device_status()
 
     # correctness gate + CPU baseline (rank 0): results of one step vs the oracle on the sample
@@ -492,8 +494,29 @@ def run_default(args):
         "decode_protocol": dict(dec_proto, protocol="1 s warm, 200 graph-replayed launches x 10 repeats, "
                                 "8 rotating buffers, after the timed region"),
         "gate": gate,
+        "receipt": receipt(dev, warmup_s),
     }
     print(json.dumps(out), flush=True)
+
+
+def receipt(dev, warmup_s):
+    """What the numbers were measured on: device, driver, runtime, library sources."""
+    import torch
+
+    import shape_driven_tile_gb300 as sdt
+
+    props = torch.cuda.get_device_properties(dev)
+    driver = None
+    try:
+        r = subprocess.run(["nvidia-smi", "--query-gpu=driver_version", "--format=csv,noheader",
+                            f"--id={dev.index or 0}"], capture_output=True, text=True, timeout=20)
+        driver = r.stdout.strip() or None
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return {"gpu": props.name, "sm_count": sdt.device_sm_count(), "driver": driver,
+            "cuda_runtime": torch.version.cuda, "torch": torch.__version__,
+            "kernel_sources": {k: kernel_source_digest(k) for k in SOURCES},
+            "warmup_s": round(warmup_s, 3), "host_cores": len(os.sched_getaffinity(0))}
 
 
 def step_working_set():

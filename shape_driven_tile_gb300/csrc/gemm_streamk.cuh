@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t acc_phase = static_cast<uint32_t>((j >> 1) & 1);
             const int slot = 2 * static_cast<int>(blockIdx.x) + (j == 0 ? 0 : 1);
             ++j;
-            if (!warp_wait(smem_u32(&acc_full[b]), acc_phase, lim, lane)) {
+            if (!warp_wait(smem_u32(&acc_full[b]), acc_phase, 4 * lim, lane)) {
                 if (lane == 0) {
                     record_status(p.status, kSiteEpilogue);
                     ctrl[1] = 1;
