@@ -138,3 +138,23 @@ def test_tight_entry_and_errors(cuda_device):
     with pytest.raises(sdt.SdtError) as e:  # workspace too small for 8 CTAs
         sdt.gemm_ex_splitk(A, B, workspace=small, tile="128x128", splits=8, algo=sdt.SPLITK_STREAM)
     assert e.value.status == "SDT_ERR_ARG"
+
+
+def test_empty_and_refused_cases(cuda_device):
+    # K = 0: the empty sum, C = 0; M = 0: nothing to do; skinny tiles refuse A stored K x M
+    ws = workspace(sdt.streamk_workspace_bytes(64, 64, 64, "128x128", 4), cuda_device)
+    A = torch.empty((40, 0), dtype=torch.float16, device=cuda_device)
+    B = torch.empty((0, 24), dtype=torch.float16, device=cuda_device)
+    C = torch.full((40, 24), 3.0, dtype=torch.float16, device=cuda_device)
+    sdt.gemm_ex_splitk(A, B, C, workspace=ws, tile="128x128", splits=4, algo=sdt.SPLITK_STREAM)
+    sdt.check_device_status()
+    assert bool((C == 0).all())
+    A0 = torch.empty((0, 64), dtype=torch.float16, device=cuda_device)
+    B0 = torch.ones((64, 16), dtype=torch.float16, device=cuda_device)
+    C0 = sdt.gemm_ex_splitk(A0, B0, workspace=ws, tile="128x128", splits=4, algo=sdt.SPLITK_STREAM)
+    assert C0.shape == (0, 16)
+    At, _ = operand(16, 256, True, torch.float16, 771, True, cuda_device)
+    Bn, _ = operand(256, 64, False, torch.float16, 772, True, cuda_device)
+    with pytest.raises(sdt.SdtError) as e:
+        sdt.gemm_ex_splitk(At, Bn, workspace=ws, tile="s128x16", splits=4, algo=sdt.SPLITK_STREAM)
+    assert e.value.status == "SDT_ERR_TILE"
