@@ -744,8 +744,11 @@ def run_sweep(args):
             sdt.gemm_f16(W, W, Wc)
         torch.cuda.synchronize()
     del W, Wc
-    rows = []
+    rows = load_resume(args.resume, shapes)
+    done = {tuple(r["shape"]) for r in rows}
     for (M, N, K) in shapes:
+        if (M, N, K) in done:
+            continue
         A = (torch.rand((M, K), device=dev) * 2 - 1).half()
         B = (torch.rand((K, N), device=dev) * 2 - 1).half()
         C = torch.empty((M, N), device=dev, dtype=torch.float16)
@@ -773,6 +776,7 @@ def run_sweep(args):
                      "tflops": {k: round(fl / (v / 1e3) / 1e12, 1) for k, v in res.items()},
                      "us": {k: round(v * 1e3, 2) for k, v in res.items()}})
         print(json.dumps(rows[-1]), flush=True)
+        append_resume(args.resume, rows[-1])
         del A, B, C
     sdt.check_device_status()
     if args.table_out:
@@ -782,6 +786,35 @@ def run_sweep(args):
                       "pick_worst_slowdown": round(max(slow), 4), "peak_tflops": peaks["tflops"],
                       "timing": f"best of 3 shuffled passes, each the mean of {max(1, args.reps // 3)} launches "
                                 "with L2 flushed before each"}), flush=True)
+
+
+def load_resume(path, shapes):
+    """Rows of an interrupted sweep (one JSON object per line, as the sweep prints them)
+    for the shapes still asked for; a missing file is an empty start."""
+    rows = []
+    if not path or not os.path.exists(path):
+        return rows
+    want = {tuple(sh) for sh in shapes}
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if not line:
+                continue
+            try:
+                r = json.loads(line)
+            except json.JSONDecodeError:
+                continue  # a line cut short when the run stopped
+            if isinstance(r, dict) and tuple(r.get("shape", ())) in want and "us" in r:
+                rows.append(r)
+    return rows
+
+
+def append_resume(path, row):
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(row) + "\n")
+            f.flush()
+            os.fsync(f.fileno())
 
 
 def run_kscan(args):
@@ -1139,6 +1172,7 @@ def main(argv=None):
     ap.add_argument("--dtypes", nargs="*", choices=["f16", "bf16"], help="p4: operand types to run (default both)")
     ap.add_argument("--layouts", nargs="*", choices=["NN", "TN"], help="p4: layouts to run (default both)")
     ap.add_argument("--with-kscan", action="store_true")
+    ap.add_argument("--resume", help="sweep: append each shape's row to this file and skip shapes already in it")
     ap.add_argument("--shapes", nargs="*", help="extra GEMM shapes MxNxK for --mode sweep; shape names for --mode p4")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--e2e-steps", type=int, default=20)

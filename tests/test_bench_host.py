@@ -124,3 +124,18 @@ def test_tuned_configurations_freeze_into_a_loadable_table(tmp_path):
         assert sdt.tune_table_lookup(16, 16384, 4096) == -1
     finally:
         sdt.clear_tune_table()
+
+
+def test_sweep_resume_file(tmp_path):
+    # an interrupted sweep keeps its finished shapes; a torn last line is ignored
+    path = tmp_path / "sweep.jsonl"
+    bench.append_resume(str(path), {"shape": [256, 256, 256], "pick": "64x64", "best": "64x64", "slowdown": 0.0,
+                                    "us": {"64x64": 8.0}})
+    bench.append_resume(str(path), {"shape": [512, 512, 512], "pick": "64x64", "best": "64x64", "slowdown": 0.0,
+                                    "us": {"64x64": 9.0}})
+    with open(path, "a") as f:
+        f.write('{"shape": [768, 768, 7')
+    rows = bench.load_resume(str(path), [(256, 256, 256), (768, 768, 768)])
+    assert [r["shape"] for r in rows] == [[256, 256, 256]]
+    assert bench.load_resume(str(tmp_path / "missing.jsonl"), [(256, 256, 256)]) == []
+    assert bench.load_resume(None, [(256, 256, 256)]) == []
