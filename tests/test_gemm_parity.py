@@ -277,3 +277,18 @@ def test_nondefault_stream(cuda_device):
         C = sdt.gemm_f16(Ad, Bd)
     s.synchronize()
     assert_bit_exact_f16(C, oracle.gemm(u16(A), u16(B)), "side stream")
+
+
+@pytest.mark.parametrize("tile", tile_ids(), ids=tile_name)
+def test_pipeline_phase_edges(cuda_device, tile):
+    # k-tile counts around the ring depth: the first reuse of slot 0, the phase flip at
+    # the ring's end, and one and two full turns of the ring, on one output tile
+    info = sdt.tile_info(tile)
+    S = info["stages"]
+    M, N = info["BM"], info["BN"]
+    for nk in sorted({2, S - 1, S, S + 1, 2 * S, 2 * S + 1} - {0, 1}):
+        K = 64 * nk
+        A = inputs.integers((M, K), seed=inputs.seed_for(90 + nk, 0))
+        B = inputs.integers((K, N), seed=inputs.seed_for(90 + nk, 1))
+        C = run(A.to(cuda_device), B.to(cuda_device), cuda_device, tile=tile)
+        assert_bit_exact_f16(C, oracle.gemm(u16(A), u16(B)), f"{tile_name(tile)} nK={nk}")
