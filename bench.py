@@ -594,8 +594,11 @@ def record_traffic(args):
 
 
 def run_e2e(args, dev, host, Wb_h, Q_h, stream):
-    """Same metric through the public API with pinned host buffers: H2D of every step input,
-    the step, D2H of every result, all inside the timed region."""
+    """Same metric through the public API with pinned host buffers: every step copies its
+    inputs host -> device, runs the step and copies every result device -> host, all inside
+    the timed region.  The copies of neighbouring steps overlap the compute on three streams
+    (inputs of step i+1 in, step i computed, results of step i-1 out), each with two buffer
+    sets ordered by events, as a serving loop would run it."""
     import torch
 
     import shape_driven_tile_gb300 as sdt
@@ -603,40 +606,59 @@ def run_e2e(args, dev, host, Wb_h, Q_h, stream):
     steps = max(3, min(args.steps, args.e2e_steps))
     hA = {n: host[n][0].pin_memory() for n in SWEEP}
     hB = {n: host[n][1].pin_memory() for n in SWEEP}
-    hC = {n: torch.empty((n, n), dtype=torch.float16).pin_memory() for n in SWEEP}
     hx = host["dec_bf16"][0].pin_memory()
     hW = [w.pin_memory() for w in Wb_h[:2]]
     hQ = [(q.pin_memory(), s.pin_memory()) for q, s in Q_h[:2]]
-    hyb = torch.empty(DEC_N, dtype=torch.float32).pin_memory()
-    hyq = torch.empty(DEC_N, dtype=torch.float32).pin_memory()
-    dA = {n: torch.empty_like(hA[n], device=dev) for n in SWEEP}
-    dB = {n: torch.empty_like(hB[n], device=dev) for n in SWEEP}
-    dC = {n: torch.empty((n, n), dtype=torch.float16, device=dev) for n in SWEEP}
-    dx = torch.empty_like(hx, device=dev)
-    dW = torch.empty_like(hW[0], device=dev)
-    dq = torch.empty_like(hQ[0][0], device=dev)
-    ds = torch.empty_like(hQ[0][1], device=dev)
-    dyb = torch.empty(DEC_N, dtype=torch.float32, device=dev)
-    dyq = torch.empty(DEC_N, dtype=torch.float32, device=dev)
+    sets = []
+    for _ in range(2):
+        sets.append({
+            "hC": {n: torch.empty((n, n), dtype=torch.float16).pin_memory() for n in SWEEP},
+            "hyb": torch.empty(DEC_N, dtype=torch.float32).pin_memory(),
+            "hyq": torch.empty(DEC_N, dtype=torch.float32).pin_memory(),
+            "dA": {n: torch.empty_like(hA[n], device=dev) for n in SWEEP},
+            "dB": {n: torch.empty_like(hB[n], device=dev) for n in SWEEP},
+            "dC": {n: torch.empty((n, n), dtype=torch.float16, device=dev) for n in SWEEP},
+            "dx": torch.empty_like(hx, device=dev),
+            "dW": torch.empty_like(hW[0], device=dev),
+            "dq": torch.empty_like(hQ[0][0], device=dev),
+            "ds": torch.empty_like(hQ[0][1], device=dev),
+            "dyb": torch.empty(DEC_N, dtype=torch.float32, device=dev),
+            "dyq": torch.empty(DEC_N, dtype=torch.float32, device=dev),
+            # step i's input copies done / compute done / result copies done
+            "in": torch.cuda.Event(), "comp": torch.cuda.Event(), "out": torch.cuda.Event(),
+        })
     h2d = sum(hA[n].numel() * 2 + hB[n].numel() * 2 for n in SWEEP) + hx.numel() * 2 + hW[0].numel() * 2 \
         + hQ[0][0].numel() + hQ[0][1].numel() * 2
     d2h = sum(n * n * 2 for n in SWEEP) + 2 * DEC_N * 4
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    s_c = stream
 
     def e2e_step(i):
+        b = sets[i % 2]
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(b["comp"])  # step i-2 no longer reads this set's inputs
+            for n in SWEEP:
+                b["dA"][n].copy_(hA[n], non_blocking=True)
+                b["dB"][n].copy_(hB[n], non_blocking=True)
+            b["dx"].copy_(hx, non_blocking=True)
+            b["dW"].copy_(hW[i % 2], non_blocking=True)
+            b["dq"].copy_(hQ[i % 2][0], non_blocking=True)
+            b["ds"].copy_(hQ[i % 2][1], non_blocking=True)
+            b["in"].record(s_in)
+        s_c.wait_event(b["in"])
+        s_c.wait_event(b["out"])  # step i-2's results have left this set's outputs
         for n in SWEEP:
-            dA[n].copy_(hA[n], non_blocking=True)
-            dB[n].copy_(hB[n], non_blocking=True)
-        dx.copy_(hx, non_blocking=True)
-        dW.copy_(hW[i % 2], non_blocking=True)
-        dq.copy_(hQ[i % 2][0], non_blocking=True)
-        ds.copy_(hQ[i % 2][1], non_blocking=True)
-        for n in SWEEP:
-            sdt.gemm_f16(dA[n], dB[n], dC[n])
-            hC[n].copy_(dC[n], non_blocking=True)
-        sdt.gemv_m1(dx, dW, y=dyb)
-        sdt.gemv_m1(dx, dq, ds, y=dyq)
-        hyb.copy_(dyb, non_blocking=True)
-        hyq.copy_(dyq, non_blocking=True)
+            sdt.gemm_f16(b["dA"][n], b["dB"][n], b["dC"][n], stream=s_c)
+        sdt.gemv_m1(b["dx"], b["dW"], y=b["dyb"], stream=s_c)
+        sdt.gemv_m1(b["dx"], b["dq"], b["ds"], y=b["dyq"], stream=s_c)
+        b["comp"].record(s_c)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(b["comp"])
+            for n in SWEEP:
+                b["hC"][n].copy_(b["dC"][n], non_blocking=True)
+            b["hyb"].copy_(b["dyb"], non_blocking=True)
+            b["hyq"].copy_(b["dyq"], non_blocking=True)
+            b["out"].record(s_out)
 
     for i in range(2):
         e2e_step(i)
@@ -648,11 +670,19 @@ def run_e2e(args, dev, host, Wb_h, Q_h, stream):
     torch.cuda.synchronize()
     secs = time.perf_counter() - t0
     barrier()
+    # the last step's results against a device-only run of the same step
+    last = sets[(steps - 1) % 2]
+    ref = {n: torch.empty((n, n), dtype=torch.float16, device=dev) for n in SWEEP}
+    for n in SWEEP:
+        sdt.gemm_f16(last["dA"][n], last["dB"][n], ref[n])
+    torch.cuda.synchronize()
+    ok = all(torch.equal(last["hC"][n], ref[n].cpu()) for n in SWEEP)
     world = dist_env()[0]
     max_s = max_over_ranks(secs, device=dev)
     return {"value": round(aggregate_value(step_flops(), steps, world, max_s) / 1e12, 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
-            "ms_per_step": round(max_s * 1e3 / steps, 3)}
+            "ms_per_step": round(max_s * 1e3 / steps, 3), "results_match_device_run": ok,
+            "overlap": "inputs of step i+1 in, step i computed, results of step i-1 out, on three streams"}
 
 
 # ---------------------------------------------------------------------------------------------
