@@ -208,8 +208,10 @@ def splitk_ex_workspace_bytes(M: int, N: int, K: int, tile, splits: int) -> int:
 
 def gemm_ex_splitk(A, B, C=None, *, workspace, tile=-1, splits: int = 0, algo: int = SPLITK_REDUCE_KERNEL,
                    stream=None):
-    """Split-K form of gemm_ex (same views); `workspace` as for gemm_f16_splitk, sized by
-    splitk_ex_workspace_bytes."""
+    """Split-K / Stream-K form of gemm_ex (same views); `workspace` as for gemm_f16_splitk,
+    sized by splitk_ex_workspace_bytes (algo 0 and 1: `splits` k-slices per output tile) or
+    streamk_workspace_bytes (algo SPLITK_STREAM: `splits` is the CTA count, 0 = one per SM
+    slot)."""
     M, N, K, lda, ldb, ldc, layout, C = _ex_args(A, B, C)
     tid = tile_id(tile) if isinstance(tile, str) else int(tile)
     if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda:
