@@ -299,9 +299,10 @@ int gemm_ex_splitk(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, 
  * splits outside 1..ceil(K/64), or a non-positive dimension). */
 size_t sdt_splitk_ex_workspace_bytes(int64_t M, int64_t N, int64_t K, int tile_id, int splits);
 /*
- * Stream-K [P4 "The Six Rounds", the split-K step: a fixed number of workgroups share the
- * whole iteration space, a workgroup's share may end inside an output tile, and
- * the partial tiles are fixed up afterwards].  algo = SDT_SPLITK_STREAM in
+ * Stream-K [P4 "The Six Rounds", the last round "Stream-K": a fixed grid of
+ * workgroups shares the whole iteration space instead of the contraction being
+ * split per tile; a workgroup's share may end inside an output tile, and the
+ * partial tiles are fixed up afterwards].  algo = SDT_SPLITK_STREAM in
  * gemm_f16_splitk / gemm_ex_splitk, with `splits` read as the CTA count G
  * (<= 0: one CTA per SM slot, sdt_streamk_ctas; lowered to the unit count when
  * larger).  The units are (output tile, 64-deep k-tile) pairs, tiles in banded

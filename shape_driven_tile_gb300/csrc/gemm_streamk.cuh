@@ -1,10 +1,10 @@
 // gemm_streamk.cuh -- stream-K form of the one-CTA ladder tiles.
 //
 // "Iteratively Tuning hipBLASLt TensileLite Kernels", section "The Six Rounds",
-// the split-K step: besides splitting K into equal slices per output tile, the page's
-// kernels can run "Stream-K", where a fixed number of workgroups share the whole
-// iteration space and a workgroup's slice may end part-way through an output
-// tile, the partial tiles being fixed up afterwards.  Here the iteration space is
+// the last round ("Stream-K"): instead of splitting K into equal slices per output
+// tile, a fixed grid of workgroups shares the whole iteration space, so the work is
+// spread evenly whatever the tile count; a workgroup's share may end part-way
+// through an output tile, and the partial tiles are fixed up afterwards.  Here the iteration space is
 // the list of (output tile, 64-deep k-tile) units, tiles in banded raster order
 // and k-tiles in order within a tile; CTA g of G owns the contiguous units
 // [floor(g*U/G), floor((g+1)*U/G)), so every CTA gets the same number of k-tiles

@@ -15,17 +15,21 @@ Groups for this library's kernels:
                      tiles overhang ragged edges) with its ring depth (the
                      page opens DepthU in this round; 0 = the tile's own depth,
                      deeper rings are clamped to what fits in shared memory)
-  2. ``split-K``  -- split count and reduction algorithm with the tile pinned,
-                     and stream-K (the page's other choice in this round) with
-                     one CTA per SM slot or one per SM (gemm_ex_splitk, forms of
-                     the one-CTA tiles only: when the held tile is persistent or
-                     a CTA pair, the round opens the split-capable tiles too;
-                     candidates the library rejects are dropped before timing, as
-                     the page's legality filter drops configurations that cannot
-                     be generated)
+  2. ``split-K``  -- split count and reduction algorithm with the tile pinned
+                     (gemm_ex_splitk, a form of the one-CTA tiles only: when the
+                     held tile is persistent or a CTA pair, the round opens the
+                     split-capable tiles too; candidates the library rejects are
+                     dropped before timing, as the page's legality filter drops
+                     configurations that cannot be generated)
   3. ``mapping``  -- how CTAs land on the output: the raster band height (m-tiles
                      per band) and the k-loop start stagger
   4. ``tail``     -- the two-CTA 256x256 tile's tail as half-width items or not
+  5. ``stream-K`` -- the page's terminal branch ("Stream-K"): the split count is
+                     set aside and Stream-K opened instead, with one CTA per SM
+                     slot or one per SM, on the held tile (or, when it has no
+                     stream-K form, on the tiles that have one); being a strict-
+                     win round it keeps the split-K best when Stream-K loses,
+                     which is the page's try-and-fallback
 
 The descent itself (``descend``) is pure host logic over a ``measure`` callable;
 ``GemmProblem`` supplies candidates and GPU timings for a problem.
@@ -249,14 +253,10 @@ class GemmProblem:
                 return
             own = sdt.splitk_ex_workspace_bytes(self.M, self.N, self.K, held["tile"], 2) > 0
             tiles = [held["tile"]] if own else range(self.ntiles)
-            sms = sdt.device_sm_count()
             for t in tiles:
                 for s in SPLITS:
                     for a in (sdt.SPLITK_REDUCE_KERNEL, sdt.SPLITK_IN_KERNEL):
                         yield dict(held, tile=t, splits=s, algo=a)
-                # stream-K: one CTA per SM slot (0), and one per SM
-                for g in (0, sms):
-                    yield dict(held, tile=t, splits=g, algo=sdt.SPLITK_STREAM)
 
         def mapping(held):
             for r in RASTER:
@@ -269,7 +269,17 @@ class GemmProblem:
                 for t in (0, 1):
                     yield dict(held, tail=t)
 
-        return [("tile", tiles), ("split-K", split), ("mapping", mapping), ("tail", tail)]
+        def stream(held):
+            def has_form(t):
+                return sdt.lib().sdt_streamk_workspace_bytes(self.M, self.N, self.K, t, 1) > 0
+
+            tiles = [held["tile"]] if has_form(held["tile"]) else [t for t in range(self.ntiles) if has_form(t)]
+            sms = sdt.device_sm_count()
+            for t in tiles:
+                for g in (0, sms):  # one CTA per SM slot (0), and one per SM
+                    yield dict(held, tile=t, splits=g, algo=sdt.SPLITK_STREAM, tail=1)
+
+        return [("tile", tiles), ("split-K", split), ("mapping", mapping), ("tail", tail), ("stream-K", stream)]
 
     def tune(self, passes: int = 2):
         return descend(self.rounds(), self.start(), self.measure, passes=passes)
