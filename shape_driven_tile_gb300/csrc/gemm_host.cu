@@ -41,7 +41,7 @@ static const LaunchFn kSplitLaunch[][4] = {
     SDT_SPLIT4_(64, 64),   SDT_SPLIT4_(64, 128),  SDT_SPLIT4_(128, 64),  SDT_SPLIT4_(128, 128),
     SDT_SPLIT4_(128, 256), {nullptr, nullptr, nullptr, nullptr},     {nullptr, nullptr, nullptr, nullptr},
     {nullptr, nullptr, nullptr, nullptr},         {nullptr, nullptr, nullptr, nullptr},
-    SDT_SPLIT4_(128, 16),  SDT_SPLIT4_(128, 32)};
+    {nullptr, nullptr, nullptr, nullptr},         SDT_SPLIT4_(128, 16),  SDT_SPLIT4_(128, 32)};
 
 // Stream-K launchers of the same rungs (null: no stream-K form).
 #define SDT_STREAM4_(BM, BN)                                                                       \
@@ -51,7 +51,7 @@ static const LaunchFn kStreamLaunch[][4] = {
     SDT_STREAM4_(64, 64),   SDT_STREAM4_(64, 128),  SDT_STREAM4_(128, 64),  SDT_STREAM4_(128, 128),
     SDT_STREAM4_(128, 256), {nullptr, nullptr, nullptr, nullptr},       {nullptr, nullptr, nullptr, nullptr},
     {nullptr, nullptr, nullptr, nullptr},           {nullptr, nullptr, nullptr, nullptr},
-    SDT_STREAM4_(128, 16),  SDT_STREAM4_(128, 32)};
+    {nullptr, nullptr, nullptr, nullptr},           SDT_STREAM4_(128, 16),  SDT_STREAM4_(128, 32)};
 
 // One rung of the tile ladder.  kt_cycles / fixed_cycles feed pick_tile's cost
 // model: SM cycles one CTA of this tile spends per 64-deep k-tile when it has
@@ -123,6 +123,12 @@ static const LadderTile kLadder[] = {
     SDT_PTILE(256, 4, "p128x256", 11.265, 0.37733, 0.00000, true),
     SDT_PAIR(128, 8, "2cta_256x128", 12.888, 0.29877, 0.00000, false),
     SDT_PAIR(256, 6, "2cta_256x256", 13.532, 0.32647, 0.00000, true),
+    // 224 columns: divides shapes 256 does not (3584 = 16 x 224) and fills the pairs'
+    // rounds there (3584^2: 224 tiles = 2.95 rounds of 76 pairs instead of 196 = 2.58
+    // rounded up to 3 full-width rounds).  Its k-tile costs 0.96 of the 256-wide one's
+    // (measured at 3584^3 and 7168^3), not 224/256: the MMA time does not shrink in
+    // proportion to N.
+    SDT_PAIR(224, 6, "2cta_256x224", 13.532, 0.31340, 0.00000, true),
     // Skinny tiles for few-row problems (M up to a few tens, e.g. decode rows): the
     // operands are swapped so that the many output columns fill the 128 MMA rows and
     // the M rows become a 16- or 32-wide MMA N; the weights stream through a deep ring
@@ -410,6 +416,14 @@ static int tensor_map_2d(const void *ptr, int dtype, uint64_t inner, uint64_t ou
 // B is K x N (N contiguous) or, transposed, N x K.  A row-major A tile is one box
 // of a_rows (the rows one CTA stages) x 64; every other operand tile is loaded as
 // 64 x 64 boxes.
+// Rows of a K-major B box: the tile width for narrow tiles, 64 for the rest, and a
+// two-CTA tile's whole half width when that is not a multiple of 64 (256x224: 112).
+static int b_box_rows(const LadderTile &t) {
+    if (t.BN < 64) return t.BN;
+    if (t.cta_group == 2 && (t.BN / 2) % 64) return t.BN / 2;
+    return 64;
+}
+
 static int operand_maps(const void *A, int64_t lda, const void *B, int64_t ldb, int64_t M, int64_t N, int64_t K,
                         int dtype, int layout, int a_rows, CUtensorMap *tmA, CUtensorMap *tmB, int b_rows = 64) {
     const bool a_t = layout & SDT_LAYOUT_A_T, b_t = layout & SDT_LAYOUT_B_T;
@@ -550,7 +564,7 @@ static int run_tile_ex(int tile_id, int stagger_req, int64_t M0, int64_t N0, int
     const void *A = ex.A, *B = ex.B;
     const int layout = ex.layout;
     CUtensorMap tmA, tmB;
-    rc = operand_maps(A, lda, B, ldb, M, N, K, dtype, layout, t.BM / t.cta_group, &tmA, &tmB, t.BN < 64 ? t.BN : 64);
+    rc = operand_maps(A, lda, B, ldb, M, N, K, dtype, layout, t.BM / t.cta_group, &tmA, &tmB, b_box_rows(t));
     if (rc) return rc;
     int *status = nullptr;
     rc = status_word(&status);

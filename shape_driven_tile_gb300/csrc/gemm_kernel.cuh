@@ -76,7 +76,7 @@ struct OperandLayout {
 };
 
 // One operand tile of ROWS rows (M or N) x 64 K-elements for k-tile kt.
-// MN-major operand (rows contiguous in memory): ROWS/64 TMA boxes of 64 x 64, box c
+// MN-major operand (rows contiguous in memory): ceil(ROWS/64) TMA boxes of 64 x 64, box c
 // covering rows r0+64c .. +63 and landing at dst + 8 KB * c as 64 k-rows of 128 B
 // (canonical MN-major 128 B swizzle: 64-element chunks 8 KB apart).  K-major operand
 // (K contiguous): ROWS/KBOX boxes of 64 x KBOX (KBOX = ROWS when the whole tile is one
@@ -85,8 +85,10 @@ struct OperandLayout {
 template <bool PAIR, bool MN, int ROWS, int KBOX>
 __device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap *map, uint32_t bar, int kt, int r0) {
     if constexpr (MN) {
+        // (a width that is not a multiple of 64 takes a last whole box; its extra
+        // columns land in the unused part of the last 64-column block)
 #pragma unroll
-        for (int c = 0; c < ROWS / 64; ++c) {
+        for (int c = 0; c < (ROWS + 63) / 64; ++c) {
             if (PAIR) tma_load_2d_pair(dst + c * 8192, map, bar, r0 + 64 * c, kt * kBK);
             else tma_load_2d(dst + c * 8192, map, bar, r0 + 64 * c, kt * kBK);
         }

@@ -30,13 +30,23 @@ template <int BN>
 struct PairCfg {
     static constexpr int BM = 256;     // rows per pair tile
     static constexpr int CTA_M = 128;  // rows staged and accumulated per CTA
-    static constexpr int B_HALF = BN / 2;
+    static constexpr int B_HALF = BN / 2;  // B columns each CTA stages and supplies to the MMA
+    // MN-major B arrives in whole 64-column boxes (BN = 224: two boxes for 112 columns);
+    // K-major B in one box of B_HALF rows when B_HALF is not a multiple of 64
+    static constexpr int B_SMEM_COLS = (B_HALF + 63) / 64 * 64;
+    static constexpr int B_KBOX = B_HALF % 64 == 0 ? 64 : B_HALF;
     static constexpr int A_BYTES = CTA_M * kBK * 2;
-    static constexpr int B_BYTES = B_HALF * kBK * 2;
+    static constexpr int B_BYTES = B_SMEM_COLS * kBK * 2;  // shared memory per stage
     static constexpr int B_BOX_BYTES = 64 * kBK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // per CTA
     static constexpr int ACC_BUFS = 2;
-    static constexpr int TMEM_COLS = ACC_BUFS * BN;
+    // two accumulators of BN columns; the allocation is a power of two
+    static constexpr int TMEM_COLS = ACC_BUFS * BN <= 256 ? 256 : 512;
+    // bytes one CTA's TMA copies bring per k-tile (whole tile; B as it is staged)
+    template <bool B_MN>
+    __host__ __device__ static constexpr int load_bytes() {
+        return A_BYTES + (B_MN ? B_SMEM_COLS : B_HALF) * kBK * 2;
+    }
     static constexpr int THREADS = 192;
     static constexpr int EPI_WARPS = 4;
     static constexpr int ALIGN_SLACK = 1024;
@@ -44,8 +54,8 @@ struct PairCfg {
     __host__ __device__ static constexpr int smem_bytes(int stages) {
         return ALIGN_SLACK + stages * STAGE_BYTES + CTRL_BYTES;
     }
-    static_assert(BN == 128 || BN == 256, "pair tiles use BN 128 or 256");
-    static_assert(TMEM_COLS <= 512, "two accumulators must fit in TMEM");
+    static_assert(BN == 128 || BN == 224 || BN == 256, "pair tiles use BN 128, 224 or 256");
+    static_assert(ACC_BUFS * BN <= TMEM_COLS && TMEM_COLS <= 512, "two accumulators must fit in TMEM");
 };
 
 // Work item -> output tile, column offset and width.  When the last round of whole
@@ -138,8 +148,8 @@ __global__ void __launch_bounds__(192, 1)
                 const int m0 = m_tile * Cfg::BM + static_cast<int>(rank) * Cfg::CTA_M;
                 const int nb = n_tile * BN + n_off + static_cast<int>(rank) * (width / 2);
                 const bool whole = width == BN;  // whole tile, else a tail half (BN/4 B rows per CTA)
-                const uint32_t pair_bytes =
-                    2u * static_cast<uint32_t>(Cfg::A_BYTES + (whole ? Cfg::B_HALF : Cfg::B_HALF / 2) * kBK * 2);
+                const uint32_t pair_bytes = 2u * static_cast<uint32_t>(
+                    whole ? Cfg::template load_bytes<L::B_MN>() : Cfg::A_BYTES + (Cfg::B_HALF / 2) * kBK * 2);
                 const int start =
                     p.stagger ? static_cast<int>((static_cast<uint32_t>(tile) * static_cast<uint32_t>(p.stagger_stride)) &
                                                  static_cast<uint32_t>(nK - 1))
@@ -158,15 +168,16 @@ __global__ void __launch_bounds__(192, 1)
                     const uint32_t fb = mapa_shared(fb_local, 0);
                     load_operand<true, L::A_MN, Cfg::CTA_M, Cfg::CTA_M>(smem_u32(smA + s * Cfg::A_BYTES), &tmA, fb,
                                                                          kt, m0);
-                    if constexpr (Cfg::B_HALF >= 128) {
+                    if constexpr (Cfg::B_HALF == 128) {
                         if (whole)
                             load_operand<true, L::B_MN, Cfg::B_HALF, 64>(smem_u32(smB + s * Cfg::B_BYTES), &tmB, fb, kt,
                                                                          nb);
                         else
                             load_operand<true, L::B_MN, Cfg::B_HALF / 2, 64>(smem_u32(smB + s * Cfg::B_BYTES), &tmB, fb,
                                                                              kt, nb);
-                    } else {  // tail halves need B_HALF / 2 >= 64 (the host only splits BN = 256 tails)
-                        load_operand<true, L::B_MN, Cfg::B_HALF, 64>(smem_u32(smB + s * Cfg::B_BYTES), &tmB, fb, kt, nb);
+                    } else {  // tail halves only for BN = 256 (the host splits no other tail)
+                        load_operand<true, L::B_MN, Cfg::B_HALF, Cfg::B_KBOX>(smem_u32(smB + s * Cfg::B_BYTES), &tmB, fb,
+                                                                              kt, nb);
                     }
                     ctrl[2] = ++issued;
                     if (++s == S) { s = 0; phase ^= 1u; }

@@ -14,7 +14,7 @@ pytestmark = pytest.mark.gpu
 
 LAYOUTS = {"NN": (False, False), "NT": (False, True), "TN": (True, False), "TT": (True, True)}
 DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16}
-TILES = ["64x64", "128x128", "p128x256", "2cta_256x256", -1]
+TILES = ["64x64", "128x128", "p128x256", "2cta_256x256", "2cta_256x224", -1]
 
 
 def operand(rows, cols, trans, dtype, seed, integer, dev, pad=0):

@@ -28,7 +28,13 @@ def run(A, B, dev, tile=None, stagger=-1):
 
 
 def tile_ids():
-    return [t["id"] for t in sdt.tiles() if not t["skinny"]]  # skinny tiles: gemm_ex forms only
+    """Ladder tiles of power-of-two width (every shape below is a multiple of them); the
+    skinny tiles are gemm_ex forms only, the 224-wide pair tile has its own shapes."""
+    return [t["id"] for t in sdt.tiles() if not t["skinny"] and t["BN"] & (t["BN"] - 1) == 0]
+
+
+def odd_tile_ids():
+    return [t["id"] for t in sdt.tiles() if not t["skinny"] and t["BN"] & (t["BN"] - 1) != 0]
 
 
 def tile_name(i):
@@ -279,7 +285,7 @@ def test_nondefault_stream(cuda_device):
     assert_bit_exact_f16(C, oracle.gemm(u16(A), u16(B)), "side stream")
 
 
-@pytest.mark.parametrize("tile", tile_ids(), ids=tile_name)
+@pytest.mark.parametrize("tile", tile_ids() + odd_tile_ids(), ids=tile_name)
 def test_pipeline_phase_edges(cuda_device, tile):
     # k-tile counts around the ring depth: the first reuse of slot 0, the phase flip at
     # the ring's end, and one and two full turns of the ring, on one output tile
@@ -292,3 +298,27 @@ def test_pipeline_phase_edges(cuda_device, tile):
         B = inputs.integers((K, N), seed=inputs.seed_for(90 + nk, 1))
         C = run(A.to(cuda_device), B.to(cuda_device), cuda_device, tile=tile)
         assert_bit_exact_f16(C, oracle.gemm(u16(A), u16(B)), f"{tile_name(tile)} nK={nk}")
+
+
+# ---- the 224-wide two-CTA tile on shapes it divides -------------------------------------
+
+@pytest.mark.parametrize("tile", odd_tile_ids(), ids=tile_name)
+@pytest.mark.parametrize("M,N,K", [(256, 224, 256), (512, 672, 1024), (768, 448, 320), (256, 1344, 2112)])
+def test_odd_width_integer_bit_exact(cuda_device, tile, M, N, K):
+    A = inputs.integers((M, K), seed=inputs.seed_for(95, 0))
+    B = inputs.integers((K, N), seed=inputs.seed_for(95, 1))
+    ref = oracle.gemm(u16(A), u16(B))
+    for stagger in (0, 1):
+        C = run(A.to(cuda_device), B.to(cuda_device), cuda_device, tile, stagger)
+        assert_bit_exact_f16(C, ref, f"{M}x{N}x{K} {tile_name(tile)} stagger={stagger}")
+
+
+@pytest.mark.parametrize("tile", odd_tile_ids(), ids=tile_name)
+def test_odd_width_uniform_and_picked(cuda_device, tile):
+    M, N, K = 1024, 1792, 1536
+    A = inputs.uniform((M, K), seed=inputs.seed_for(96, 0))
+    B = inputs.uniform((K, N), seed=inputs.seed_for(96, 1))
+    C = run(A.to(cuda_device), B.to(cuda_device), cuda_device, tile)
+    rows = boundary_rows(M, step=64, extra=4)[::2]
+    assert_close(C.cpu().double().numpy()[rows], oracle.gemm(u16(A), u16(B), rows=rows), K, tile_name(tile))
+    assert tile in sdt.feasible_tiles(3584, 3584, 3584)
