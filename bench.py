@@ -340,36 +340,36 @@ def run_default(args):
     # The timed loop calls the C ABI directly with the operands' device pointers, so that
     # Python-side argument checks do not leave the GPU idle between the small GEMMs.
     L = sdt.lib()
-    sp = stream.cuda_stream
-    gemm_args = [(n, n, n, A[n].data_ptr(), B[n].data_ptr(), C[n].data_ptr(), sp) for n in SWEEP]
-    pb = [(DEC_K, DEC_N, x.data_ptr(), w.data_ptr(), yb.data_ptr(), sp) for w in Wb]
-    pq = [(DEC_K, DEC_N, x.data_ptr(), q.data_ptr(), s_.data_ptr(), yq.data_ptr(), sp) for q, s_ in zip(Wq, Sq)]
     gemm_c, gemv_b, gemv_q = L.gemm_f16, L.gemv_m1_bf16, L.gemv_m1_q8
 
+    def launch_args(sp):
+        return ([(n, n, n, A[n].data_ptr(), B[n].data_ptr(), C[n].data_ptr(), sp) for n in SWEEP],
+                [(DEC_K, DEC_N, x.data_ptr(), w.data_ptr(), yb.data_ptr(), sp) for w in Wb],
+                [(DEC_K, DEC_N, x.data_ptr(), q.data_ptr(), s_.data_ptr(), yq.data_ptr(), sp) for q, s_ in zip(Wq, Sq)])
+
+    args_on = {stream.cuda_stream: launch_args(stream.cuda_stream)}
     dom_j = len(SWEEP) - 1  # the 4096^3 launch: largest share of the step
 
-    def step(i, ev=None, dom=None):
-        # ev: events around every launch (instrumented step); dom: events around the
-        # dominant launch only.  Any event between two launches stops the second from
-        # overlapping its set-up with the first (programmatic dependent launch), so
-        # most timed steps carry only the two events around the dominant launch.
+    def step(i, ev=None, on=None):
+        # ev: events around every launch (instrumented step).  Any event between two
+        # launches stops the second from overlapping its set-up with the first
+        # (programmatic dependent launch), so most timed steps carry no events.
+        # on: the stream the launches go to (a capturing stream for the graphs).
+        on = on or stream
+        gemm_args, pb, pq = args_on.setdefault(on.cuda_stream, launch_args(on.cuda_stream))
         rc = 0
         for j, a in enumerate(gemm_args):
             if ev is not None:
-                ev[j].record(stream)
-            elif dom is not None and j == dom_j:
-                dom[0].record(stream)
+                ev[j].record(on)
             rc |= gemm_c(*a)
-            if ev is None and dom is not None and j == dom_j:
-                dom[1].record(stream)
         if ev is not None:
-            ev[len(SWEEP)].record(stream)
+            ev[len(SWEEP)].record(on)
         rc |= gemv_b(*pb[i % DEC_BUFFERS])
         if ev is not None:
-            ev[len(SWEEP) + 1].record(stream)
+            ev[len(SWEEP) + 1].record(on)
         rc |= gemv_q(*pq[i % DEC_BUFFERS])
         if ev is not None:
-            ev[len(SWEEP) + 2].record(stream)
+            ev[len(SWEEP) + 2].record(on)
         if rc:
             raise sdt.SdtError(rc, (L.sdt_last_error() or b"").decode())
 
@@ -401,16 +401,45 @@ def run_default(args):
     nev = launches_per_step + 1
     inst_idx = [i for i in range(args.steps) if i % INSTR == 0]
     events = {i: [torch.cuda.Event(enable_timing=True) for _ in range(nev)] for i in inst_idx}
-    dom_events = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for i in range(args.steps) if i not in events}
+    # The other nine steps in ten carry no events at all, so their launches overlap
+    # through programmatic dependent launch, and they run as one CUDA graph of nine
+    # steps (captured once per decode-buffer offset), so no host launch gap lands
+    # between them; the dominant kernel's duration comes from the instrumented steps.
+    graphs = {}
+    if not args.no_graph:
+        cap = torch.cuda.Stream(device=dev)
+        for i0 in inst_idx:
+            first = i0 + 1
+            if first + INSTR - 1 > args.steps or first % DEC_BUFFERS in graphs:
+                continue
+            g = torch.cuda.CUDAGraph()
+            cap.wait_stream(stream)
+            with torch.cuda.graph(g, stream=cap):
+                for j in range(INSTR - 1):
+                    step(first + j, on=cap)
+            stream.wait_stream(cap)
+            graphs[first % DEC_BUFFERS] = g
+        torch.cuda.synchronize()
+        for g in graphs.values():  # one untimed replay each
+            g.replay()
+        torch.cuda.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         start.record(stream)
-        for i in range(args.steps):
-            step(i, events.get(i), dom_events.get(i))
+        i = 0
+        while i < args.steps:
+            if i in events:
+                step(i, events[i])
+                i += 1
+            elif i + INSTR - 1 <= args.steps and i % DEC_BUFFERS in graphs and (i - 1) % INSTR == 0:
+                graphs[i % DEC_BUFFERS].replay()  # steps i .. i+8, same buffers as eager steps
+                i += INSTR - 1
+            else:
+                step(i)
+                i += 1
         stop.record(stream)
         torch.cuda.synchronize()
         barrier()
@@ -426,7 +455,7 @@ def run_default(args):
             per[n].append(ev[j].elapsed_time(ev[j + 1]))
         dec_b.append(ev[len(SWEEP)].elapsed_time(ev[len(SWEEP) + 1]))
         dec_q.append(ev[len(SWEEP) + 1].elapsed_time(ev[len(SWEEP) + 2]))
-    dom_ms = [e0.elapsed_time(e1) for e0, e1 in dom_events.values()] + per[SWEEP[dom_j]]
+    dom_ms = per[SWEEP[dom_j]]
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     e2e = run_e2e(args, dev, host, Wb_h, Q_h, stream)
@@ -473,7 +502,10 @@ def run_default(args):
                    % (step_working_set() / 1e6), "parallelism": f"replicas x{world}"},
         "timing": {"per_size_and_decode": f"instrumented steps (every {INSTR}th, events around every launch; "
                    "a decode launch there follows the GEMMs, so it cannot overlap a previous decode)",
-                   "roofline": "events around the 4096^3 launch in every timed step"},
+                   "roofline": f"events around the 4096^3 launch in the instrumented steps ({len(inst_idx)} of "
+                               f"{args.steps}); the other steps carry no events",
+                   "launch": "eager" if args.no_graph else "instrumented steps eager, the nine steps between "
+                             "two of them replayed as one CUDA graph"},
         "roofline": {"bound": "tensor", "kernel": f"gemm_f16 {dom}^3 ({tiles[dom]})",
                      "largest_share_in_step": f"gemm_f16 {largest_share}^3",
                      "achieved": round(achieved, 1), "peak": peaks["tflops"], "unit": "TFLOP/s",
@@ -1202,6 +1234,8 @@ def main(argv=None):
     ap.add_argument("--dtypes", nargs="*", choices=["f16", "bf16"], help="p4: operand types to run (default both)")
     ap.add_argument("--layouts", nargs="*", choices=["NN", "TN"], help="p4: layouts to run (default both)")
     ap.add_argument("--with-kscan", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="default run: launch every timed step eagerly instead of replaying nine-step CUDA graphs")
     ap.add_argument("--resume", help="sweep: append each shape's row to this file and skip shapes already in it")
     ap.add_argument("--shapes", nargs="*", help="extra GEMM shapes MxNxK for --mode sweep; shape names for --mode p4")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
