@@ -879,6 +879,43 @@ def append_resume(path, row):
             os.fsync(f.fileno())
 
 
+def run_ktile(args):
+    """The per-k-tile time of one CTA: every one-CTA tile on one output tile with a long K
+    (65536, 1024 k-tiles), ring depths 4, 8 and the tile's own, cold L2.  A time that does
+    not move with the ring depth or the bytes per k-tile is the tensor pipe's pace."""
+    import torch
+
+    import shape_driven_tile_gb300 as sdt
+
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    flush = L2Flush(dev)
+    K = 65536
+    rows = []
+    for t in sdt.tiles():
+        if t["cta_group"] != 1 or t["name"].startswith("p"):
+            continue
+        M, N = (t["BN"], t["BM"]) if t["skinny"] else (t["BM"], t["BN"])
+        A = (torch.rand((M, K), device=dev) * 2 - 1).bfloat16()
+        B = (torch.rand((N, K), device=dev) * 2 - 1).bfloat16().t()
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        row = {"tile": t["name"], "M": M, "N": N, "K": K,
+               "bytes_per_ktile": (t["BM"] + t["BN"]) * 64 * 2}
+        for depth in (4, 8, 0):
+            os.environ["SDT_STAGES"] = str(depth) if depth else ""
+            fn = lambda: sdt.gemm_ex(A, B, C, tile=t["name"])
+            fn()
+            mean = time_cold(fn, max(3, args.reps // 4), flush, stream)[0]
+            row[f"ns_per_ktile_depth{depth or t['stages']}"] = round(mean * 1e6 / (K // 64), 1)
+        os.environ.pop("SDT_STAGES", None)
+        rows.append(row)
+        print(json.dumps(row), flush=True)
+        del A, B, C
+    sdt.check_device_status()
+    print(json.dumps({"mode": "ktile", "rows": len(rows), "timing": "mean of cold launches, L2 flushed before each"}),
+          flush=True)
+
+
 def run_kscan(args):
     import torch
 
@@ -1220,7 +1257,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["sdt", "reference"], default="sdt")
     ap.add_argument("--mode", choices=["step", "sweep", "kscan", "decode", "large", "one", "splitk", "chain",
-                                       "record-traffic", "p4"], default="step")
+                                       "record-traffic", "p4", "ktile"], default="step")
     ap.add_argument("--tune", action="store_true", help="p4: run the coordinate-descent tuner per problem")
     ap.add_argument("--table-out", help="p4 --tune / sweep: write the winners as a gemm_f16 tune table")
     ap.add_argument("--ncu-csv", help="record-traffic: ncu --csv log of one launch")
@@ -1248,7 +1285,8 @@ def main(argv=None):
     if args.mode == "record-traffic":
         return record_traffic(args)
     {"step": run_default, "sweep": run_sweep, "kscan": run_kscan, "decode": run_decode,
-     "large": run_large, "one": run_one, "splitk": run_splitk, "chain": run_chain, "p4": run_p4}[args.mode](args)
+     "large": run_large, "one": run_one, "splitk": run_splitk, "chain": run_chain, "p4": run_p4,
+     "ktile": run_ktile}[args.mode](args)
 
 
 if __name__ == "__main__":
