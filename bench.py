@@ -1091,7 +1091,7 @@ def run_p4(args):
             out["table"] = write_tune_table(args.table_out, [
                 (r["M"], r["N"], r["K"], r["tuned"]) for r in rows
                 if r["dtype"] == "f16" and r["layout"] == "NN" and r["tuned"]["splits"] == 1
-                and r["tuned"]["algo"] != sdt.SPLITK_STREAM],
+                and r["tuned"]["algo"] not in (sdt.SPLITK_STREAM, sdt.SPLITK_STREAM_REDUCE)],
                 "coordinate descent, bench.py --mode p4 --tune")
     print(json.dumps(out), flush=True)
 
@@ -1267,7 +1267,8 @@ def main(argv=None):
     ap.add_argument("--sizes", type=int, nargs="*")
     ap.add_argument("--tile", help="one/kscan/sweep: the tile; p4: time this tile instead of the pick")
     ap.add_argument("--splits", type=int, default=1, help="p4 with --tile: split count (stream-K: CTA count, 0 = default)")
-    ap.add_argument("--algo", type=int, default=0, help="p4 with --tile: 0/1 split-K reduction, 2 stream-K")
+    ap.add_argument("--algo", type=int, default=0,
+                    help="p4 with --tile: 0/1 split-K reduction kernel / in-kernel, 2/3 stream-K fix-up in / after the kernel")
     ap.add_argument("--dtypes", nargs="*", choices=["f16", "bf16"], help="p4: operand types to run (default both)")
     ap.add_argument("--layouts", nargs="*", choices=["NN", "TN"], help="p4: layouts to run (default both)")
     ap.add_argument("--with-kscan", action="store_true")

@@ -262,7 +262,8 @@ int sdt_pick_tile_any_for(int64_t M, int64_t N, int64_t K, int sm_count, int sme
  */
 #define SDT_SPLITK_REDUCE_KERNEL 0
 #define SDT_SPLITK_IN_KERNEL 1
-#define SDT_SPLITK_STREAM 2 /* stream-K; see sdt_streamk_workspace_bytes */
+#define SDT_SPLITK_STREAM 2        /* stream-K, fix-up by the last CTA to arrive; see sdt_streamk_workspace_bytes */
+#define SDT_SPLITK_STREAM_REDUCE 3 /* stream-K, fix-up by a second kernel over the whole GPU */
 int gemm_f16_splitk(int64_t M, int64_t N, int64_t K, const void *A, const void *B, void *C,
                     void *workspace, size_t workspace_bytes, int tile_id, int splits, int algo,
                     sdt_stream_t stream);
@@ -311,7 +312,9 @@ size_t sdt_splitk_ex_workspace_bytes(int64_t M, int64_t N, int64_t K, int tile_i
  * first and last tile may be partial: it writes an fp32 partial tile to its
  * slots (2g, 2g+1) and counts its arrival on per-(tile, TMEM lane quarter)
  * counters; the last CTA to arrive sums the tile's partials in CTA order,
- * writes C and zeroes the counter.  Same tiles as split-K (the one-CTA rungs
+ * writes C and zeroes the counter (SDT_SPLITK_STREAM), or a second kernel sums
+ * every shared tile's partials in the same order (SDT_SPLITK_STREAM_REDUCE; the
+ * counters are not used).  Same tiles as split-K (the one-CTA rungs
  * and the skinny tiles), any shape and layout gemm_ex takes.
  * Workspace: the 1 MiB counter region shared with split-K (zero before the
  * first call, left zero by every completed call), then 2*G fp32 tiles of

@@ -20,7 +20,7 @@ __all__ = [
     "debug_timeout_probe", "device_sm_count", "lib", "gemm_f16_splitk", "splitk_workspace",
     "splitk_workspace_bytes", "pick_splitk", "pick_tile_any", "gemm_ex_splitk",
     "splitk_ex_workspace_bytes", "pick_splitk_any", "SPLITK_REDUCE_KERNEL", "SPLITK_IN_KERNEL", "gemm_ex",
-    "SPLITK_STREAM", "streamk_ctas", "streamk_workspace_bytes",
+    "SPLITK_STREAM", "SPLITK_STREAM_REDUCE", "streamk_ctas", "streamk_workspace_bytes",
 ]
 
 
@@ -168,7 +168,8 @@ def gemm_ex(A, B, C=None, *, tile=-1, stream=None):
 
 SPLITK_REDUCE_KERNEL = 0
 SPLITK_IN_KERNEL = 1
-SPLITK_STREAM = 2  # stream-K: `splits` is the CTA count (<= 0: one per SM slot)
+SPLITK_STREAM = 2  # stream-K: `splits` is the CTA count (<= 0: one per SM slot); fix-up in the kernel
+SPLITK_STREAM_REDUCE = 3  # stream-K with the fix-up in a second kernel
 
 
 def splitk_workspace_bytes(M: int, N: int, K: int, tile, splits: int) -> int:
@@ -210,8 +211,8 @@ def gemm_ex_splitk(A, B, C=None, *, workspace, tile=-1, splits: int = 0, algo: i
                    stream=None):
     """Split-K / Stream-K form of gemm_ex (same views); `workspace` as for gemm_f16_splitk,
     sized by splitk_ex_workspace_bytes (algo 0 and 1: `splits` k-slices per output tile) or
-    streamk_workspace_bytes (algo SPLITK_STREAM: `splits` is the CTA count, 0 = one per SM
-    slot)."""
+    streamk_workspace_bytes (algo SPLITK_STREAM or SPLITK_STREAM_REDUCE: `splits` is the CTA
+    count, 0 = one per SM slot)."""
     M, N, K, lda, ldb, ldc, layout, C = _ex_args(A, B, C)
     tid = tile_id(tile) if isinstance(tile, str) else int(tile)
     if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda:

@@ -868,6 +868,55 @@ static int splitk_launch_ex(int tile_id, int splits, int algo, int64_t M0, int64
 
 // ---- stream-K ---------------------------------------------------------------------
 
+// Tile index of output tile (m_tile, n_tile) in the banded raster order of
+// tile_coords (bands of `group` m-tiles, m fastest within a band).
+__device__ __forceinline__ int raster_index(int m_tile, int n_tile, int num_m, int num_n, int group) {
+    const int band = m_tile / group;
+    const int first_m = band * group;
+    const int band_m = min(num_m - first_m, group);
+    return band * group * num_n + n_tile * band_m + (m_tile - first_m);
+}
+
+// The separate fix-up of Stream-K: for every output tile that several CTAs share,
+// sums their fp32 partial tiles in CTA order (the in-kernel fix-up's order) and
+// writes C; tiles one CTA covered whole were stored by the GEMM kernel and are
+// skipped.  One thread per 8 consecutive columns of a row of the problem as the
+// kernel saw it (swapped for a skinny tile: c_trans writes C transposed).
+__global__ void streamk_reduce_kernel(const float *__restrict__ partials, uint16_t *__restrict__ C, int M, int N,
+                                      int64_t ldc, int BM, int BN, int num_m, int num_n, int nK, int G, int group,
+                                      int c_trans, int bf16) {
+    const int64_t chunks = (int64_t(N) + 7) / 8, total = int64_t(M) * chunks;
+    const long long U = static_cast<long long>(num_m) * num_n * nK;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
+        const int r = int(i / chunks), c0 = int(i % chunks) * 8;
+        const int m_tile = r / BM, n_tile = c0 / BN;
+        const int tile = raster_index(m_tile, n_tile, num_m, num_n, group);
+        const long long u0 = static_cast<long long>(tile) * nK;
+        const int g_lo = sk_owner(u0, G, U), g_hi = sk_owner(u0 + nK - 1, G, U);
+        if (g_lo == g_hi) continue;  // whole tile, already in C
+        const int lo_slot = 2 * g_lo + (sk_first_unit(g_lo, G, U) / nK == tile ? 0 : 1);
+        const size_t off = size_t(r - m_tile * BM) * BN + (c0 - n_tile * BN);
+        float v[8];
+        {
+            const float *src = partials + size_t(lo_slot) * BM * BN + off;
+            const float4 a = __ldg(reinterpret_cast<const float4 *>(src)), b = __ldg(reinterpret_cast<const float4 *>(src + 4));
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        }
+        for (int g = g_lo + 1; g <= g_hi; ++g) {
+            const float *src = partials + size_t(2 * g) * BM * BN + off;
+            const float4 a = __ldg(reinterpret_cast<const float4 *>(src)), b = __ldg(reinterpret_cast<const float4 *>(src + 4));
+            v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w; v[4] += b.x; v[5] += b.y; v[6] += b.z; v[7] += b.w;
+        }
+        if (c_trans) {
+            for (int t = 0; t < 8; ++t)
+                if (c0 + t < N) C[int64_t(c0 + t) * ldc + r] = f32_to_16(v[t], bf16 != 0);
+        } else if (c0 + 8 <= N) {  // N % 8 == 0 unless swapped
+            *reinterpret_cast<uint4 *>(C + int64_t(r) * ldc + c0) =
+                pack8_f32(make_float4(v[0], v[1], v[2], v[3]), make_float4(v[4], v[5], v[6], v[7]), bf16 != 0);
+        }
+    }
+}
+
 static constexpr int64_t kMaxStreamUnits = int64_t(1) << 40;  // keeps (u + 1) * G within 64 bits
 static constexpr int64_t kMaxStreamCtas = int64_t(1) << 20;
 
@@ -899,7 +948,7 @@ static size_t streamk_ws_bytes(const LadderTile &t, int64_t M, int64_t N, int64_
 // Launches stream-K with tile `tile_id` (which has a stream-K form and fits on chip) on
 // validated, non-empty operands with K > 0; ctas <= 0 takes one CTA per SM slot.  The
 // CTA count is lowered to the number of (tile, k-tile) units when it is larger.
-static int streamk_launch_ex(int tile_id, int64_t ctas, int64_t M0, int64_t N0, int64_t K0, const void *A0,
+static int streamk_launch_ex(int tile_id, int64_t ctas, int algo, int64_t M0, int64_t N0, int64_t K0, const void *A0,
                              int64_t lda0, const void *B0, int64_t ldb0, void *C, int64_t ldc, int dtype, int layout0,
                              void *ws, size_t ws_bytes, cudaStream_t stream, const DeviceInfo &dev) {
     const LadderTile &t = kLadder[tile_id];
@@ -946,6 +995,7 @@ static int streamk_launch_ex(int tile_id, int64_t ctas, int64_t M0, int64_t N0, 
     a.status = status;
     a.max_ctas = int(ctas);
     a.splits = int(ctas);
+    a.splitk_reduce_in_kernel = algo == SDT_SPLITK_STREAM ? 1 : 0;
     a.counters = static_cast<unsigned *>(ws);
     a.partials = reinterpret_cast<float *>(static_cast<char *>(ws) + kCounterRegionBytes);
     int e = kStreamLaunch[tile_id][ex.layout & 3](tmA, tmB, a, stream);
@@ -953,12 +1003,23 @@ static int streamk_launch_ex(int tile_id, int64_t ctas, int64_t M0, int64_t N0, 
         cudaGetLastError();
         return fail(SDT_ERR_LAUNCH, "stream-K launch of tile %s failed: %s", t.name, cudaGetErrorString(cudaError_t(e)));
     }
+    if (algo == SDT_SPLITK_STREAM_REDUCE) {
+        const int64_t total = M * ((N + 7) / 8);
+        const unsigned blocks = unsigned(std::min<int64_t>((total + 255) / 256, int64_t(dev.sm_count) * 8));
+        streamk_reduce_kernel<<<blocks, 256, 0, stream>>>(a.partials, static_cast<uint16_t *>(C), a.M, a.N, ldc, t.BM,
+                                                          t.BN, a.num_m_tiles, a.num_n_tiles, a.num_k_tiles, a.splits,
+                                                          a.raster_group, ex.c_trans, dtype == SDT_DTYPE_BF16 ? 1 : 0);
+        cudaError_t e2 = cudaGetLastError();
+        if (e2 != cudaSuccess) return fail(SDT_ERR_LAUNCH, "stream-K fix-up launch failed: %s", cudaGetErrorString(e2));
+    }
     return SDT_OK;
 }
 
 static bool splitk_algo_ok(int algo) {
-    return algo == SDT_SPLITK_REDUCE_KERNEL || algo == SDT_SPLITK_IN_KERNEL || algo == SDT_SPLITK_STREAM;
+    return algo == SDT_SPLITK_REDUCE_KERNEL || algo == SDT_SPLITK_IN_KERNEL || algo == SDT_SPLITK_STREAM ||
+           algo == SDT_SPLITK_STREAM_REDUCE;
 }
+static bool is_streamk(int algo) { return algo == SDT_SPLITK_STREAM || algo == SDT_SPLITK_STREAM_REDUCE; }
 
 // gemm_f16_splitk: tight row-major fp16, the tile must divide the shape.
 static int splitk_run(int64_t M, int64_t N, int64_t K, const void *A, const void *B, void *C, void *ws,
@@ -975,16 +1036,16 @@ static int splitk_run(int64_t M, int64_t N, int64_t K, const void *A, const void
         int sp = 1;
         rc = pick_splitk_for(M, N, K, dev.sm_count, dev.smem_optin, dev.smem_per_sm, &tile_id, &sp);
         if (rc) return rc;
-        if (splits <= 0 && algo != SDT_SPLITK_STREAM) splits = sp;
+        if (splits <= 0 && !is_streamk(algo)) splits = sp;
     }
     if (!splitk_tile_ok(tile_id)) return fail(SDT_ERR_TILE, "tile %d has no split-K form", tile_id);
     const LadderTile &t = kLadder[tile_id];
     if (!splitk_feasible(t, M, N, K, dev.smem_optin))
         return fail(SDT_ERR_TILE, "tile %s does not divide %lldx%lldx%lld", t.name, (long long)M, (long long)N,
                     (long long)K);
-    if (algo == SDT_SPLITK_STREAM)
-        return streamk_launch_ex(tile_id, splits, M, N, K, A, K, B, N, C, N, SDT_DTYPE_F16, 0, ws, ws_bytes, stream,
-                                 dev);
+    if (is_streamk(algo))
+        return streamk_launch_ex(tile_id, splits, algo, M, N, K, A, K, B, N, C, N, SDT_DTYPE_F16, 0, ws, ws_bytes,
+                                 stream, dev);
     return splitk_launch_ex(tile_id, splits, algo, M, N, K, A, K, B, N, C, N, SDT_DTYPE_F16, 0, ws, ws_bytes, stream,
                             dev);
 }
@@ -1078,12 +1139,12 @@ static int gemm_ex_splitk_impl(int64_t M, int64_t N, int64_t K, const void *A, i
         int sp = 1;
         rc = pick_splitk_any(M, N, K, dev.sm_count, dev.smem_optin, dev.smem_per_sm, &tile_id, &sp);
         if (rc) return rc;
-        if (splits <= 0 && algo != SDT_SPLITK_STREAM) splits = sp;
+        if (splits <= 0 && !is_streamk(algo)) splits = sp;
     }
     if (!splitk_tile_ok(tile_id)) return fail(SDT_ERR_TILE, "tile %d has no split-K form", tile_id);
     if (!fits_chip(kLadder[tile_id], dev.smem_optin)) return fail(SDT_ERR_TILE, "tile %d does not fit", tile_id);
-    if (algo == SDT_SPLITK_STREAM)
-        return streamk_launch_ex(tile_id, splits, M, N, K, A, lda, B, ldb, C, ldc, dtype, layout, ws, ws_bytes,
+    if (is_streamk(algo))
+        return streamk_launch_ex(tile_id, splits, algo, M, N, K, A, lda, B, ldb, C, ldc, dtype, layout, ws, ws_bytes,
                                  stream, dev);
     return splitk_launch_ex(tile_id, splits, algo, M, N, K, A, lda, B, ldb, C, ldc, dtype, layout, ws, ws_bytes,
                             stream, dev);

@@ -19,7 +19,9 @@
 // its arrival on the tile's counter; the warp that arrives last sums the
 // partials of all the tile's CTAs in CTA order (so the result does not depend on
 // the order of arrival), rounds once to fp16/bf16, writes C and resets the counter
-// to zero.  No CTA ever waits for another one.
+// to zero.  No CTA ever waits for another one.  Alternatively (splitk_reduce_in_kernel
+// = 0) the kernel only writes the partials and a second kernel sums every shared
+// tile with the whole GPU, in the same order (streamk_reduce_kernel).
 //
 // Roles (192 threads, as the persistent kernel):
 //   warp 0 lane 0 : TMA producer (ring slots: full/empty mbarriers)
@@ -288,7 +290,7 @@ __global__ void __launch_bounds__(192, 1)
             // A quarter with no row inside C takes no part in the fix-up (every CTA of
             // the tile skips it alike, so its counter stays untouched).
             const int row0 = BM == 128 ? q * 32 : q * 16;
-            if (!whole && m0 + row0 < p.M) {
+            if (!whole && m0 + row0 < p.M && p.splitk_reduce_in_kernel) {
                 // Publish this quarter's partial rows, then count the arrival on the
                 // (tile, quarter) counter; the last of the tile's CTAs to arrive sums.
                 __threadfence();

@@ -26,7 +26,8 @@ Groups for this library's kernels:
   4. ``tail``     -- the two-CTA 256x256 tile's tail as half-width items or not
   5. ``stream-K`` -- the page's terminal branch ("Stream-K"): the split count is
                      set aside and Stream-K opened instead, with one CTA per SM
-                     slot or one per SM, on the held tile (or, when it has no
+                     slot or one per SM and the fix-up in the kernel or in a
+                     second kernel, on the held tile (or, when it has no
                      stream-K form, on the tiles that have one); being a strict-
                      win round it keeps the split-K best when Stream-K loses,
                      which is the page's try-and-fallback
@@ -189,8 +190,9 @@ class GemmProblem:
 
     def launcher(self, cfg: dict):
         """A no-argument callable that launches cfg, or None when cfg is illegal here."""
-        if cfg["algo"] == sdt.SPLITK_STREAM or cfg["splits"] > 1:
-            if cfg["algo"] == sdt.SPLITK_STREAM:
+        streamk = cfg["algo"] in (sdt.SPLITK_STREAM, sdt.SPLITK_STREAM_REDUCE)
+        if streamk or cfg["splits"] > 1:
+            if streamk:
                 if sdt.lib().sdt_streamk_workspace_bytes(self.M, self.N, self.K, cfg["tile"], 1) == 0:
                     return None  # no stream-K form
                 nbytes = sdt.streamk_workspace_bytes(self.M, self.N, self.K, cfg["tile"], cfg["splits"] or None)
@@ -249,7 +251,7 @@ class GemmProblem:
             # opens the split-capable tiles with it; the held configuration stays a
             # candidate either way.  Candidates without a split-K form for the shape are
             # dropped by measure()'s legality check.
-            if held["splits"] > 1 or held["algo"] == sdt.SPLITK_STREAM:
+            if held["splits"] > 1 or held["algo"] in (sdt.SPLITK_STREAM, sdt.SPLITK_STREAM_REDUCE):
                 return
             own = sdt.splitk_ex_workspace_bytes(self.M, self.N, self.K, held["tile"], 2) > 0
             tiles = [held["tile"]] if own else range(self.ntiles)
@@ -277,7 +279,8 @@ class GemmProblem:
             sms = sdt.device_sm_count()
             for t in tiles:
                 for g in (0, sms):  # one CTA per SM slot (0), and one per SM
-                    yield dict(held, tile=t, splits=g, algo=sdt.SPLITK_STREAM, tail=1)
+                    for a in (sdt.SPLITK_STREAM, sdt.SPLITK_STREAM_REDUCE):  # fix-up in the kernel or after it
+                        yield dict(held, tile=t, splits=g, algo=a, tail=1)
 
         return [("tile", tiles), ("split-K", split), ("mapping", mapping), ("tail", tail), ("stream-K", stream)]
 

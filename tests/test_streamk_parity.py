@@ -18,12 +18,15 @@ def workspace(nbytes, dev):
     return ws[(-ws.data_ptr()) % 256:][:nbytes]
 
 
-def run(A, B, C, tile, ctas, ws=None):
+ALGOS = [sdt.SPLITK_STREAM, sdt.SPLITK_STREAM_REDUCE]
+
+
+def run(A, B, C, tile, ctas, ws=None, algo=sdt.SPLITK_STREAM):
     M, K = A.shape
     N = B.shape[1]
     if ws is None:
         ws = workspace(sdt.streamk_workspace_bytes(M, N, K, tile, ctas), A.device)
-    sdt.gemm_ex_splitk(A, B, C, workspace=ws, tile=tile, splits=ctas or 0, algo=sdt.SPLITK_STREAM)
+    sdt.gemm_ex_splitk(A, B, C, workspace=ws, tile=tile, splits=ctas or 0, algo=algo)
     sdt.check_device_status()
     return C
 
@@ -48,9 +51,10 @@ def test_layouts_integer_bit_exact(cuda_device, tile, dname, lname):
     A, Av = operand(M, K, ta, dt, 701, True, cuda_device)
     B, Bv = operand(K, N, tb, dt, 702, True, cuda_device)
     for ctas in (None, 5):
-        C = torch.full((M, N), float("nan"), dtype=dt, device=cuda_device)
-        run(A, B, C, tile, ctas)
-        check(C, Av, Bv, dt, K, True, f"{tile} {dname} {lname} ctas={ctas}")
+        for algo in ALGOS:
+            C = torch.full((M, N), float("nan"), dtype=dt, device=cuda_device)
+            run(A, B, C, tile, ctas, algo=algo)
+            check(C, Av, Bv, dt, K, True, f"{tile} {dname} {lname} ctas={ctas} algo={algo}")
 
 
 @pytest.mark.parametrize("tile", TILES)
@@ -60,9 +64,10 @@ def test_cta_counts(cuda_device, tile, ctas):
     M, N, K = 256, 384, 1024
     A, Av = operand(M, K, False, torch.float16, 711, True, cuda_device)
     B, Bv = operand(K, N, True, torch.float16, 712, True, cuda_device)
-    C = torch.full((M, N), float("nan"), dtype=torch.float16, device=cuda_device)
-    run(A, B, C, tile, ctas)
-    check(C, Av, Bv, torch.float16, K, True, f"{tile} ctas={ctas}")
+    for algo in ALGOS:
+        C = torch.full((M, N), float("nan"), dtype=torch.float16, device=cuda_device)
+        run(A, B, C, tile, ctas, algo=algo)
+        check(C, Av, Bv, torch.float16, K, True, f"{tile} ctas={ctas} algo={algo}")
 
 
 @pytest.mark.parametrize("tile", TILES)
@@ -72,9 +77,10 @@ def test_decode_and_tiny_shapes(cuda_device, tile, M, N, K):
     for dt in DTYPES.values():
         A, Av = operand(M, K, False, dt, 721, True, cuda_device)
         B, Bv = operand(K, N, True, dt, 722, True, cuda_device)
-        C = torch.full((M, N), float("nan"), dtype=dt, device=cuda_device)
-        run(A, B, C, tile, None)
-        check(C, Av, Bv, dt, K, True, f"{tile} {M}x{N}x{K} {dt}")
+        for algo in ALGOS:
+            C = torch.full((M, N), float("nan"), dtype=dt, device=cuda_device)
+            run(A, B, C, tile, None, algo=algo)
+            check(C, Av, Bv, dt, K, True, f"{tile} {M}x{N}x{K} {dt} algo={algo}")
 
 
 @pytest.mark.parametrize("tile", ["128x256", "s128x16", "64x64"])
@@ -89,6 +95,9 @@ def test_uniform_within_tolerance_and_deterministic(cuda_device, tile):
         for _ in range(3):  # partials are summed in CTA order, whatever the order of arrival
             C2 = run(A, B, torch.empty((M, N), dtype=dt, device=cuda_device), tile, None, ws)
             assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
+        # the second-kernel fix-up sums in the same order: the same bits
+        C3 = run(A, B, torch.empty((M, N), dtype=dt, device=cuda_device), tile, None, ws, algo=sdt.SPLITK_STREAM_REDUCE)
+        assert torch.equal(C1.view(torch.int16), C3.view(torch.int16))
 
 
 def test_padded_c_untouched(cuda_device):
@@ -111,8 +120,9 @@ def test_one_workspace_with_split_k(cuda_device):
     B, Bv = operand(K, N, False, torch.float16, 752, True, cuda_device)
     ref = ref_of(Av, Bv, torch.float16)
     cfgs = [("64x64", 152, sdt.SPLITK_STREAM), ("64x64", 3, sdt.SPLITK_IN_KERNEL), ("128x256", 4, sdt.SPLITK_REDUCE_KERNEL),
-            ("128x128", 77, sdt.SPLITK_STREAM), ("64x64", 2, sdt.SPLITK_IN_KERNEL), ("128x256", 300, sdt.SPLITK_STREAM)]
-    need = max(sdt.streamk_workspace_bytes(M, N, K, t, s) if a == sdt.SPLITK_STREAM
+            ("128x128", 77, sdt.SPLITK_STREAM), ("64x64", 2, sdt.SPLITK_IN_KERNEL), ("128x256", 300, sdt.SPLITK_STREAM),
+            ("64x128", 152, sdt.SPLITK_STREAM_REDUCE)]
+    need = max(sdt.streamk_workspace_bytes(M, N, K, t, s) if a in ALGOS
                else sdt.splitk_ex_workspace_bytes(M, N, K, t, s) for t, s, a in cfgs)
     ws = workspace(need, cuda_device)
     for rep in range(2):
