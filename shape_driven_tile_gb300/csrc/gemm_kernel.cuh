@@ -261,41 +261,53 @@ __global__ void __launch_bounds__(128, 1)
             : 0;
         int s = 0;
         uint32_t phase = 0;
-        for (int i = 0; i < nK; ++i) {
-            if (!mbar_wait(smem_u32(&empty[s]), phase ^ 1u, deadline)) {
+        // per-slot addresses are fixed offsets from slot 0: the loop adds instead of
+        // recomputing them, and reads the error flag only every eighth k-tile (this
+        // single thread's instruction count per k-tile sets the pace of small tiles)
+        const uint32_t empty0 = smem_u32(&empty[0]), full0 = smem_u32(&full[0]);
+        const uint32_t smA0 = smem_u32(smA), smB0 = smem_u32(smB);
+        int i = 0;
+        for (; i < nK; ++i) {
+            if (!mbar_wait(empty0 + 8u * s, phase ^ 1u, deadline)) {
                 record_status(p.status, kSiteProducer);
                 ctrl[1] = 1;
                 break;
             }
-            if (ctrl[1]) break;
+            if ((i & 7) == 0 && ctrl[1]) break;
             const int kt = k_first + (stagger ? ((start + i) & (nK - 1)) : i);
-            const uint32_t fb = smem_u32(&full[s]);
+            const uint32_t fb = full0 + 8u * s;
             mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
-            load_operand<false, L::A_MN, BM, BM>(smem_u32(smA + s * Cfg::A_BYTES), &tmA, fb, kt, m0);
+            load_operand<false, L::A_MN, BM, BM>(smA0 + static_cast<uint32_t>(s) * Cfg::A_BYTES, &tmA, fb, kt, m0);
             // (tiles narrower than 64 columns take K-major B only: boxes of BN rows)
-            load_operand<false, L::B_MN, BN, (BN < 64 ? BN : 64)>(smem_u32(smB + s * Cfg::B_BYTES), &tmB, fb, kt, n0);
-            ctrl[2] = i + 1;
+            load_operand<false, L::B_MN, BN, (BN < 64 ? BN : 64)>(smB0 + static_cast<uint32_t>(s) * Cfg::B_BYTES,
+                                                                 &tmB, fb, kt, n0);
             if (++s == S) { s = 0; phase ^= 1u; }
         }
+        ctrl[2] = i;  // k-tiles issued: read by the drain after an error
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer ----------------
         const uint32_t idesc = idesc_for(p.idesc_flags, BM, BN);
         constexpr uint64_t a_step = operand_k_step<L::A_MN>(), b_step = operand_k_step<L::B_MN>();
         int s = 0;
         uint32_t phase = 0;
+        // slot s's descriptors are slot 0's plus s stages (the start address field counts
+        // 16-byte units and shared memory stays below 2^18 bytes)
+        const uint64_t a_desc0 = operand_desc<L::A_MN>(smem_u32(smA));
+        const uint64_t b_desc0 = operand_desc<L::B_MN>(smem_u32(smB));
+        const uint32_t full0 = smem_u32(&full[0]), empty0 = smem_u32(&empty[0]);
         for (int i = 0; i < nK; ++i) {
-            if (!mbar_wait(smem_u32(&full[s]), phase, deadline)) {
+            if (!mbar_wait(full0 + 8u * s, phase, deadline)) {
                 record_status(p.status, kSiteMma);
                 ctrl[1] = 1;
                 break;
             }
             tc_fence_after();
-            const uint64_t a_desc = operand_desc<L::A_MN>(smem_u32(smA + s * Cfg::A_BYTES));
-            const uint64_t b_desc = operand_desc<L::B_MN>(smem_u32(smB + s * Cfg::B_BYTES));
+            const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(s) * (Cfg::A_BYTES >> 4);
+            const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(s) * (Cfg::B_BYTES >> 4);
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk)
                 umma_f16(tmem_d, a_desc + a_step * kk, b_desc + b_step * kk, idesc, (i > 0 || kk > 0) ? 1u : 0u);
-            umma_commit(smem_u32(&empty[s]));
+            umma_commit(empty0 + 8u * s);
             if (++s == S) { s = 0; phase ^= 1u; }
         }
         umma_commit(smem_u32(acc_full));

@@ -142,6 +142,11 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t phase = 0;
             int issued = 0;
             bool stop = false;
+            // per-slot addresses are fixed offsets from slot 0 (the leader's full barrier
+            // keeps its offset under mapa), so the loop adds instead of recomputing them
+            const uint32_t empty0 = smem_u32(&empty[0]), full0 = smem_u32(&full[0]);
+            const uint32_t full0_leader = mapa_shared(full0, 0);
+            const uint32_t smA0 = smem_u32(smA), smB0 = smem_u32(smB);
             for (int item = pair; item < num_items && !stop; item += num_pairs) {
                 int tile, m_tile, n_tile, n_off, width;
                 pair_item<BN>(item, p, tile, m_tile, n_tile, n_off, width);
@@ -155,34 +160,32 @@ __global__ void __launch_bounds__(192, 1)
                                                  static_cast<uint32_t>(nK - 1))
                               : 0;
                 for (int i = 0; i < nK; ++i) {
-                    if (!mbar_wait_for(smem_u32(&empty[s]), phase ^ 1u, lim)) {
+                    if (!mbar_wait_for(empty0 + 8u * s, phase ^ 1u, lim)) {
                         record_status(p.status, kSiteProducer | static_cast<int>(rank << 4) | (issued << 8));
                         ctrl[1] = 1;
                         stop = true;
                         break;
                     }
-                    if (ctrl[1]) { stop = true; break; }
+                    if ((i & 7) == 0 && ctrl[1]) { stop = true; break; }  // another role gave up
                     const int kt = p.stagger ? ((start + i) & (nK - 1)) : i;
-                    const uint32_t fb_local = smem_u32(&full[s]);
-                    if (leader) mbar_arrive_expect_tx(fb_local, pair_bytes);
-                    const uint32_t fb = mapa_shared(fb_local, 0);
-                    load_operand<true, L::A_MN, Cfg::CTA_M, Cfg::CTA_M>(smem_u32(smA + s * Cfg::A_BYTES), &tmA, fb,
-                                                                         kt, m0);
+                    if (leader) mbar_arrive_expect_tx(full0 + 8u * s, pair_bytes);
+                    const uint32_t fb = full0_leader + 8u * s;
+                    const uint32_t dA = smA0 + static_cast<uint32_t>(s) * Cfg::A_BYTES;
+                    const uint32_t dB = smB0 + static_cast<uint32_t>(s) * Cfg::B_BYTES;
+                    load_operand<true, L::A_MN, Cfg::CTA_M, Cfg::CTA_M>(dA, &tmA, fb, kt, m0);
                     if constexpr (Cfg::B_HALF == 128) {
                         if (whole)
-                            load_operand<true, L::B_MN, Cfg::B_HALF, 64>(smem_u32(smB + s * Cfg::B_BYTES), &tmB, fb, kt,
-                                                                         nb);
+                            load_operand<true, L::B_MN, Cfg::B_HALF, 64>(dB, &tmB, fb, kt, nb);
                         else
-                            load_operand<true, L::B_MN, Cfg::B_HALF / 2, 64>(smem_u32(smB + s * Cfg::B_BYTES), &tmB, fb,
-                                                                             kt, nb);
+                            load_operand<true, L::B_MN, Cfg::B_HALF / 2, 64>(dB, &tmB, fb, kt, nb);
                     } else {  // tail halves only for BN = 256 (the host splits no other tail)
-                        load_operand<true, L::B_MN, Cfg::B_HALF, Cfg::B_KBOX>(smem_u32(smB + s * Cfg::B_BYTES), &tmB, fb,
-                                                                              kt, nb);
+                        load_operand<true, L::B_MN, Cfg::B_HALF, Cfg::B_KBOX>(dB, &tmB, fb, kt, nb);
                     }
-                    ctrl[2] = ++issued;
+                    ++issued;
                     if (++s == S) { s = 0; phase ^= 1u; }
                 }
             }
+            ctrl[2] = issued;  // read by the drain after an error, once every role has stopped
         }
     } else if (warp == 1) {
         if (lane == 0 && leader) {
@@ -194,6 +197,11 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t phase = 0;
             int j = 0;
             bool stop = false;
+            // slot s's descriptors are slot 0's plus s stages (the start address field
+            // counts 16-byte units and shared memory stays below 2^18 bytes)
+            const uint64_t a_desc0 = operand_desc<L::A_MN>(smem_u32(smA));
+            const uint64_t b_desc0 = operand_desc<L::B_MN>(smem_u32(smB));
+            const uint32_t full0 = smem_u32(&full[0]), empty0 = smem_u32(&empty[0]);
             for (int item = pair; item < num_items && !stop; item += num_pairs, ++j) {
                 const uint32_t idesc = item < p.tail_start ? idesc_full : idesc_half;
                 const int b = j & 1;
@@ -206,20 +214,20 @@ __global__ void __launch_bounds__(192, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
                 for (int i = 0; i < nK; ++i) {
-                    if (!mbar_wait_for(smem_u32(&full[s]), phase, lim)) {
+                    if (!mbar_wait_for(full0 + 8u * s, phase, lim)) {
                         record_status(p.status, kSiteMma | (((j << 12) | i) << 8));
                         ctrl[1] = 1;
                         stop = true;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t a_desc = operand_desc<L::A_MN>(smem_u32(smA + s * Cfg::A_BYTES));
-                    const uint64_t b_desc = operand_desc<L::B_MN>(smem_u32(smB + s * Cfg::B_BYTES));
+                    const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(s) * (Cfg::A_BYTES >> 4);
+                    const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(s) * (Cfg::B_BYTES >> 4);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
                         umma_f16_pair(d_tmem, a_desc + a_step * kk, b_desc + b_step * kk, idesc,
                                       (i > 0 || kk > 0) ? 1u : 0u);
-                    umma_commit_pair(smem_u32(&empty[s]), 0x3);
+                    umma_commit_pair(empty0 + 8u * s, 0x3);
                     if (++s == S) { s = 0; phase ^= 1u; }
                 }
                 if (!stop) umma_commit_pair(smem_u32(&acc_full[b]), 0x3);

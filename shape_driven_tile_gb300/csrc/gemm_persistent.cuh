@@ -123,6 +123,9 @@ __global__ void __launch_bounds__(192, 1)
             int s = 0;
             uint32_t phase = 0;
             int issued = 0;
+            // per-slot addresses are fixed offsets from slot 0 (see gemm_kernel.cuh)
+            const uint32_t empty0 = smem_u32(&empty[0]), full0 = smem_u32(&full[0]);
+            const uint32_t smA0 = smem_u32(smA), smB0 = smem_u32(smB);
             for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
                 int m_tile, n_tile;
                 tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.raster_group, m_tile, n_tile);
@@ -133,23 +136,26 @@ __global__ void __launch_bounds__(192, 1)
                               : 0;
                 bool stop = false;
                 for (int i = 0; i < nK; ++i) {
-                    if (!mbar_wait_for(smem_u32(&empty[s]), phase ^ 1u, lim)) {
+                    if (!mbar_wait_for(empty0 + 8u * s, phase ^ 1u, lim)) {
                         record_status(p.status, kSiteProducer);
                         ctrl[1] = 1;
                         stop = true;
                         break;
                     }
-                    if (ctrl[1]) { stop = true; break; }
+                    if ((i & 7) == 0 && ctrl[1]) { stop = true; break; }
                     const int kt = p.stagger ? ((start + i) & (nK - 1)) : i;
-                    const uint32_t fb = smem_u32(&full[s]);
+                    const uint32_t fb = full0 + 8u * s;
                     mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
-                    load_operand<false, L::A_MN, Cfg::BM, Cfg::BM>(smem_u32(smA + s * Cfg::A_BYTES), &tmA, fb, kt, m0);
-                    load_operand<false, L::B_MN, BN, 64>(smem_u32(smB + s * Cfg::B_BYTES), &tmB, fb, kt, n0);
-                    ctrl[2] = ++issued;
+                    load_operand<false, L::A_MN, Cfg::BM, Cfg::BM>(smA0 + static_cast<uint32_t>(s) * Cfg::A_BYTES, &tmA,
+                                                                   fb, kt, m0);
+                    load_operand<false, L::B_MN, BN, 64>(smB0 + static_cast<uint32_t>(s) * Cfg::B_BYTES, &tmB, fb, kt,
+                                                         n0);
+                    ++issued;
                     if (++s == S) { s = 0; phase ^= 1u; }
                 }
                 if (stop) break;
             }
+            ctrl[2] = issued;  // read by the drain after an error, once every role has stopped
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -160,6 +166,9 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t phase = 0;
             int j = 0;
             bool stop = false;
+            const uint64_t a_desc0 = operand_desc<L::A_MN>(smem_u32(smA));
+            const uint64_t b_desc0 = operand_desc<L::B_MN>(smem_u32(smB));
+            const uint32_t full0 = smem_u32(&full[0]), empty0 = smem_u32(&empty[0]);
             for (int tile = blockIdx.x; tile < num_tiles && !stop; tile += gridDim.x, ++j) {
                 const int b = j & 1;
                 const uint32_t acc_phase = static_cast<uint32_t>((j >> 1) & 1);
@@ -171,20 +180,20 @@ __global__ void __launch_bounds__(192, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
                 for (int i = 0; i < nK; ++i) {
-                    if (!mbar_wait_for(smem_u32(&full[s]), phase, lim)) {
+                    if (!mbar_wait_for(full0 + 8u * s, phase, lim)) {
                         record_status(p.status, kSiteMma);
                         ctrl[1] = 1;
                         stop = true;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t a_desc = operand_desc<L::A_MN>(smem_u32(smA + s * Cfg::A_BYTES));
-                    const uint64_t b_desc = operand_desc<L::B_MN>(smem_u32(smB + s * Cfg::B_BYTES));
+                    const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(s) * (Cfg::A_BYTES >> 4);
+                    const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(s) * (Cfg::B_BYTES >> 4);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
                         umma_f16(d_tmem, a_desc + a_step * kk, b_desc + b_step * kk, idesc,
                                  (i > 0 || kk > 0) ? 1u : 0u);
-                    umma_commit(smem_u32(&empty[s]));
+                    umma_commit(empty0 + 8u * s);
                     if (++s == S) { s = 0; phase ^= 1u; }
                 }
                 if (!stop) umma_commit(smem_u32(&acc_full[b]));
