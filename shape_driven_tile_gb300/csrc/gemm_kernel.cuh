@@ -267,6 +267,9 @@ __global__ void __launch_bounds__(128, 1)
         const uint32_t empty0 = smem_u32(&empty[0]), full0 = smem_u32(&full[0]);
         const uint32_t smA0 = smem_u32(smA), smB0 = smem_u32(smB);
         int i = 0;
+// (the k-loops of the producer and MMA threads are unrolled by four: these single
+// threads set the pace of a k-tile, and the unrolled loop issues fewer instructions)
+#pragma unroll 4
         for (; i < nK; ++i) {
             if (!mbar_wait(empty0 + 8u * s, phase ^ 1u, deadline)) {
                 record_status(p.status, kSiteProducer);
@@ -295,6 +298,7 @@ __global__ void __launch_bounds__(128, 1)
         const uint64_t a_desc0 = operand_desc<L::A_MN>(smem_u32(smA));
         const uint64_t b_desc0 = operand_desc<L::B_MN>(smem_u32(smB));
         const uint32_t full0 = smem_u32(&full[0]), empty0 = smem_u32(&empty[0]);
+#pragma unroll 4
         for (int i = 0; i < nK; ++i) {
             if (!mbar_wait(full0 + 8u * s, phase, deadline)) {
                 record_status(p.status, kSiteMma);

@@ -159,6 +159,9 @@ __global__ void __launch_bounds__(192, 1)
                     p.stagger ? static_cast<int>((static_cast<uint32_t>(tile) * static_cast<uint32_t>(p.stagger_stride)) &
                                                  static_cast<uint32_t>(nK - 1))
                               : 0;
+// (the k-loops of the producer and MMA threads are unrolled by four: these single
+// threads set the pace of a k-tile, and the unrolled loop issues fewer instructions)
+#pragma unroll 4
                 for (int i = 0; i < nK; ++i) {
                     if (!mbar_wait_for(empty0 + 8u * s, phase ^ 1u, lim)) {
                         record_status(p.status, kSiteProducer | static_cast<int>(rank << 4) | (issued << 8));
@@ -213,6 +216,7 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
+#pragma unroll 4
                 for (int i = 0; i < nK; ++i) {
                     if (!mbar_wait_for(full0 + 8u * s, phase, lim)) {
                         record_status(p.status, kSiteMma | (((j << 12) | i) << 8));

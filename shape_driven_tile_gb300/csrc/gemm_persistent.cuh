@@ -135,6 +135,9 @@ __global__ void __launch_bounds__(192, 1)
                                                  static_cast<uint32_t>(nK - 1))
                               : 0;
                 bool stop = false;
+// (the k-loops of the producer and MMA threads are unrolled by four: these single
+// threads set the pace of a k-tile, and the unrolled loop issues fewer instructions)
+#pragma unroll 4
                 for (int i = 0; i < nK; ++i) {
                     if (!mbar_wait_for(empty0 + 8u * s, phase ^ 1u, lim)) {
                         record_status(p.status, kSiteProducer);
@@ -179,6 +182,7 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
+#pragma unroll 4
                 for (int i = 0; i < nK; ++i) {
                     if (!mbar_wait_for(full0 + 8u * s, phase, lim)) {
                         record_status(p.status, kSiteMma);

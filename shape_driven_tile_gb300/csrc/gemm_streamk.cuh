@@ -71,6 +71,20 @@ __host__ __device__ __forceinline__ int sk_owner(long long u, long long G, long 
     return static_cast<int>(((u + 1) * G - 1) / U);
 }
 
+// One segment of a CTA's units: output tile `tile`, k-tiles [kb, ke).  sk_next returns
+// the segment that starts at unit u and advances u past it (u_end: the CTA's end).
+struct SkSegment {
+    int tile, kb, ke;
+};
+__device__ __forceinline__ SkSegment sk_next(long long &u, long long u_end, long long nK) {
+    SkSegment sg;
+    sg.tile = static_cast<int>(u / nK);
+    sg.kb = static_cast<int>(u - static_cast<long long>(sg.tile) * nK);
+    sg.ke = static_cast<int>(nK - sg.kb < u_end - u ? nK : sg.kb + (u_end - u));
+    u += sg.ke - sg.kb;
+    return sg;
+}
+
 // Eight fp32 values of problem row `row`, columns n0+c .. n0+c+7, into C (fp16/bf16):
 // one 16-byte store into row `row` of C, or, for swapped operands, eight 2-byte
 // stores down column `row` of C.  Columns at or beyond N are skipped.
@@ -143,15 +157,8 @@ __global__ void __launch_bounds__(192, 1)
     griddep_launch_dependents();
     griddep_wait();  // the previous kernel's writes (A, B, C, counters) are visible from here on
 
-    // Segments of this CTA: (tile, k-tiles [kb, ke)); every role walks the same list.
-#define SDT_SK_SEGMENTS(...)                                                                      \
-    for (long long u_ = u_begin; u_ < u_end;) {                                                   \
-        const int tile = static_cast<int>(u_ / nK);                                               \
-        const int kb = static_cast<int>(u_ - static_cast<long long>(tile) * nK);                  \
-        const int ke = static_cast<int>(nK - kb < u_end - u_ ? nK : kb + (u_end - u_));           \
-        u_ += ke - kb;                                                                            \
-        __VA_ARGS__                                                                               \
-    }
+    // Segments of this CTA: (tile, k-tiles [kb, ke)); every role walks the same list
+    // with `for (long long u_ = u_begin; u_ < u_end;) { const SkSegment sg = sk_next(...)`.
 
     if (warp == 0) {
         if (lane == 0) {
@@ -165,11 +172,16 @@ __global__ void __launch_bounds__(192, 1)
             // per-slot addresses are fixed offsets from slot 0 (see gemm_kernel.cuh)
             const uint32_t empty0 = smem_u32(&empty[0]), full0 = smem_u32(&full[0]);
             const uint32_t smA0 = smem_u32(smA), smB0 = smem_u32(smB);
-            SDT_SK_SEGMENTS({
+            for (long long u_ = u_begin; u_ < u_end;) {
+                const SkSegment sg_ = sk_next(u_, u_end, nK);
+                const int tile = sg_.tile, kb = sg_.kb, ke = sg_.ke;
                 if (stop) break;
                 int m_tile, n_tile;
                 tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.raster_group, m_tile, n_tile);
                 const int m0 = m_tile * BM, n0 = n_tile * BN;
+// (the k-loops of the producer and MMA threads are unrolled by four: these single
+// threads set the pace of a k-tile, and the unrolled loop issues fewer instructions)
+#pragma unroll 4
                 for (int kt = kb; kt < ke; ++kt) {
                     if (!mbar_wait_for(empty0 + 8u * s, phase ^ 1u, lim)) {
                         record_status(p.status, kSiteProducer);
@@ -187,7 +199,7 @@ __global__ void __launch_bounds__(192, 1)
                     ++issued;
                     if (++s == S) { s = 0; phase ^= 1u; }
                 }
-            })
+            }
             ctrl[2] = issued;  // read by the drain after an error, once every role has stopped
         }
     } else if (warp == 1) {
@@ -202,7 +214,9 @@ __global__ void __launch_bounds__(192, 1)
             const uint64_t a_desc0 = operand_desc<L::A_MN>(smem_u32(smA));
             const uint64_t b_desc0 = operand_desc<L::B_MN>(smem_u32(smB));
             const uint32_t full0 = smem_u32(&full[0]), empty0 = smem_u32(&empty[0]);
-            SDT_SK_SEGMENTS({
+            for (long long u_ = u_begin; u_ < u_end;) {
+                const SkSegment sg_ = sk_next(u_, u_end, nK);
+                const int tile = sg_.tile, kb = sg_.kb, ke = sg_.ke;
                 if (stop) break;
                 (void)tile;
                 const int b = j & 1;
@@ -215,6 +229,7 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
+#pragma unroll 4
                 for (int kt = kb; kt < ke; ++kt) {
                     if (!mbar_wait_for(full0 + 8u * s, phase, lim)) {
                         record_status(p.status, kSiteMma);
@@ -233,7 +248,7 @@ __global__ void __launch_bounds__(192, 1)
                     if (++s == S) { s = 0; phase ^= 1u; }
                 }
                 if (!stop) umma_commit(smem_u32(&acc_full[b]));
-            })
+            }
             // all MMAs this thread issued have completed once mma_done flips
             umma_commit(smem_u32(mma_done));
             if (!mbar_wait_for(smem_u32(mma_done), 0, lim)) record_status(p.status, kSiteDrain);
@@ -248,7 +263,9 @@ __global__ void __launch_bounds__(192, 1)
         const bool bf16 = ((p.idesc_flags >> 7) & 7u) == 1u;
         constexpr int CH = BN < 32 ? BN : 32;  // accumulator columns per TMEM load
         int j = 0;
-        SDT_SK_SEGMENTS({
+        for (long long u_ = u_begin; u_ < u_end;) {
+                const SkSegment sg_ = sk_next(u_, u_end, nK);
+                const int tile = sg_.tile, kb = sg_.kb, ke = sg_.ke;
             const int b = j & 1;
             const uint32_t acc_phase = static_cast<uint32_t>((j >> 1) & 1);
             const int slot = 2 * static_cast<int>(blockIdx.x) + (j == 0 ? 0 : 1);
@@ -366,9 +383,8 @@ __global__ void __launch_bounds__(192, 1)
                     if (lane == 0) p.counters[static_cast<size_t>(tile) * 4 + q] = 0u;
                 }
             }
-        })
+        }
     }
-#undef SDT_SK_SEGMENTS
 
     tc_fence_before();
     __syncthreads();
