@@ -405,13 +405,11 @@ def run_default(args):
     # through programmatic dependent launch, and they run as one CUDA graph of nine
     # steps (captured once per decode-buffer offset), so no host launch gap lands
     # between them; the dominant kernel's duration comes from the instrumented steps.
+    plan = step_schedule(args.steps, INSTR, DEC_BUFFERS, graphed=not args.no_graph)
     graphs = {}
-    if not args.no_graph:
-        cap = torch.cuda.Stream(device=dev)
-        for i0 in inst_idx:
-            first = i0 + 1
-            if first + INSTR - 1 > args.steps or first % DEC_BUFFERS in graphs:
-                continue
+    for kind, first, _ in plan:
+        if kind == "graph" and first % DEC_BUFFERS not in graphs:
+            cap = torch.cuda.Stream(device=dev)
             g = torch.cuda.CUDAGraph()
             cap.wait_stream(stream)
             with torch.cuda.graph(g, stream=cap):
@@ -419,6 +417,7 @@ def run_default(args):
                     step(first + j, on=cap)
             stream.wait_stream(cap)
             graphs[first % DEC_BUFFERS] = g
+    if graphs:
         torch.cuda.synchronize()
         for g in graphs.values():  # one untimed replay each
             g.replay()
@@ -429,17 +428,13 @@ def run_default(args):
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         start.record(stream)
-        i = 0
-        while i < args.steps:
-            if i in events:
-                step(i, events[i])
-                i += 1
-            elif i + INSTR - 1 <= args.steps and i % DEC_BUFFERS in graphs and (i - 1) % INSTR == 0:
-                graphs[i % DEC_BUFFERS].replay()  # steps i .. i+8, same buffers as eager steps
-                i += INSTR - 1
+        for kind, first, count in plan:
+            if kind == "instrumented":
+                step(first, events[first])
+            elif kind == "graph":
+                graphs[first % DEC_BUFFERS].replay()  # steps first .. first+count-1, same buffers
             else:
-                step(i)
-                i += 1
+                step(first)
         stop.record(stream)
         torch.cuda.synchronize()
         barrier()
@@ -529,6 +524,26 @@ def run_default(args):
         "receipt": receipt(dev, warmup_s),
     }
     print(json.dumps(out), flush=True)
+
+
+def step_schedule(steps, instr, buffers, graphed=True):
+    """How the timed steps run: a list of (kind, first step, count) in step order.
+    Every `instr`-th step (0, instr, 2 instr, ...) is "instrumented" (events around each
+    launch); the instr-1 steps between two of them are one "graph" replay when they
+    all exist (a graph captured once per first-step decode buffer, first % buffers);
+    anything else is an "eager" step.  Each step index appears exactly once."""
+    plan, i = [], 0
+    while i < steps:
+        if i % instr == 0:
+            plan.append(("instrumented", i, 1))
+            i += 1
+        elif graphed and (i - 1) % instr == 0 and i + instr - 1 <= steps:
+            plan.append(("graph", i, instr - 1))
+            i += instr - 1
+        else:
+            plan.append(("eager", i, 1))
+            i += 1
+    return plan
 
 
 def receipt(dev, warmup_s):

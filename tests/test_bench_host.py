@@ -139,3 +139,19 @@ def test_sweep_resume_file(tmp_path):
     assert [r["shape"] for r in rows] == [[256, 256, 256]]
     assert bench.load_resume(str(tmp_path / "missing.jsonl"), [(256, 256, 256)]) == []
     assert bench.load_resume(None, [(256, 256, 256)]) == []
+
+
+@pytest.mark.parametrize("steps", [1, 9, 10, 11, 19, 20, 25, 2000])
+@pytest.mark.parametrize("graphed", [True, False])
+def test_step_schedule_covers_every_step_once(steps, graphed):
+    plan = bench.step_schedule(steps, 10, 8, graphed=graphed)
+    seen = [i for kind, first, count in plan for i in range(first, first + count)]
+    assert seen == list(range(steps))
+    assert [first for kind, first, _ in plan if kind == "instrumented"] == list(range(0, steps, 10))
+    for kind, first, count in plan:
+        if kind == "graph":
+            assert graphed and count == 9 and first % 10 == 1
+    if not graphed:
+        assert all(kind != "graph" for kind, _, _ in plan)
+    # graphs are keyed by their first step's decode buffer: at most four distinct keys
+    assert len({first % 8 for kind, first, _ in plan if kind == "graph"}) <= 4
