@@ -67,79 +67,83 @@ struct LadderTile {
     int threads;
     bool persistent;  // one CTA per SM walking tiles; accumulator double-buffered in TMEM
     // pick_tile cost model, fitted to the measured sweep of every feasible tile (us):
-    //   fixed  -- per launch (persistent) or per round of co-resident CTAs; it
-    //             covers the launch, the pipeline fill and the first `stages` k-tiles
-    //             (issued as one burst), and the exposed epilogue
-    //   kt     -- per further k-tile per round of tiles on one worker (CTA or pair)
-    //   per_mb -- per MB of operand tiles the whole grid streams from L2 (fits to 0
-    //             on GB300; kept so the model can express bandwidth-bound ladders)
+    //   fixed -- once per launch: the launch, the pipeline fill and the first
+    //            `stages` k-tiles (issued as one burst)
+    //   kt    -- per further k-tile on the busiest worker (CTA or CTA pair)
+    //   round -- per round of tiles on one worker (a wave of co-resident CTAs, or
+    //            a persistent worker's next tile): the exposed epilogue and refill
+    //   bw    -- per k-tile of the whole grid's work divided by the workers the
+    //            device holds: the share of the operand streaming that the L2
+    //            does not overlap with the MMAs (large for the wide pair tile)
     double fixed_us;
     double kt_us;
-    double per_mb_us;
+    double round_us;
+    double bw_us;
     bool candidate;   // considered by pick_tile (tiles dominated everywhere in the sweep are not)
     bool swap = false;  // skinny tile: runs C^T = op(B)^T . op(A)^T (gemm_ex forms only)
 };
 
 #define SDT_LAUNCH4_(FN, ...) {&FN<__VA_ARGS__, 0>, &FN<__VA_ARGS__, 1>, &FN<__VA_ARGS__, 2>, &FN<__VA_ARGS__, 3>}
 
-#define SDT_TILE(BM_, BN_, STAGES_, NAME_, FIX_, KT_, MB_, CAND_)                                  \
+#define SDT_TILE(BM_, BN_, STAGES_, NAME_, FIX_, KT_, RND_, BW_, CAND_)                                \
     LadderTile {                                                                                   \
         BM_, BN_, 1, STAGES_, NAME_, SDT_LAUNCH4_(launch_gemm_tile, BM_, BN_),                     \
             TileCfg<BM_, BN_>::STAGE_BYTES, TileCfg<BM_, BN_>::ALIGN_SLACK + TileCfg<BM_, BN_>::CTRL_BYTES, \
-            TileCfg<BM_, BN_>::TMEM_COLS, TileCfg<BM_, BN_>::THREADS, false, FIX_, KT_, MB_, CAND_ \
+            TileCfg<BM_, BN_>::TMEM_COLS, TileCfg<BM_, BN_>::THREADS, false, FIX_, KT_, RND_, BW_, CAND_ \
     }
 
-#define SDT_PTILE(BN_, STAGES_, NAME_, FIX_, KT_, MB_, CAND_)                                       \
+#define SDT_PTILE(BN_, STAGES_, NAME_, FIX_, KT_, RND_, BW_, CAND_)                                     \
     LadderTile {                                                                                   \
         128, BN_, 1, STAGES_, NAME_, SDT_LAUNCH4_(launch_gemm_persistent, BN_),                    \
             PersistentCfg<BN_>::STAGE_BYTES, PersistentCfg<BN_>::ALIGN_SLACK + PersistentCfg<BN_>::CTRL_BYTES, \
-            PersistentCfg<BN_>::TMEM_COLS, PersistentCfg<BN_>::THREADS, true, FIX_, KT_, MB_, CAND_ \
+            PersistentCfg<BN_>::TMEM_COLS, PersistentCfg<BN_>::THREADS, true, FIX_, KT_, RND_, BW_, CAND_ \
     }
 
-#define SDT_STILE(BN_, STAGES_, NAME_, FIX_, KT_, MB_)                                              \
+#define SDT_STILE(BN_, STAGES_, NAME_, FIX_, KT_)                                                    \
     LadderTile {                                                                                   \
         128, BN_, 1, STAGES_, NAME_, SDT_LAUNCH4_(launch_gemm_tile, 128, BN_),                     \
             TileCfg<128, BN_>::STAGE_BYTES, TileCfg<128, BN_>::ALIGN_SLACK + TileCfg<128, BN_>::CTRL_BYTES, \
-            TileCfg<128, BN_>::TMEM_COLS, TileCfg<128, BN_>::THREADS, false, FIX_, KT_, MB_, false, true \
+            TileCfg<128, BN_>::TMEM_COLS, TileCfg<128, BN_>::THREADS, false, FIX_, KT_, 0.0, 0.0, false, true \
     }
 
-#define SDT_PAIR(BN_, STAGES_, NAME_, FIX_, KT_, MB_, CAND_)                                        \
+#define SDT_PAIR(BN_, STAGES_, NAME_, FIX_, KT_, RND_, BW_, CAND_)                                      \
     LadderTile {                                                                                   \
         256, BN_, 2, STAGES_, NAME_, SDT_LAUNCH4_(launch_gemm_pair, BN_), PairCfg<BN_>::STAGE_BYTES, \
             PairCfg<BN_>::ALIGN_SLACK + PairCfg<BN_>::CTRL_BYTES, PairCfg<BN_>::TMEM_COLS,         \
-            PairCfg<BN_>::THREADS, true, FIX_, KT_, MB_, CAND_                                     \
+            PairCfg<BN_>::THREADS, true, FIX_, KT_, RND_, BW_, CAND_                                   \
     }
 
-// Cost-model constants fitted on GB300 (152 SMs) by one least-squares fit over
-// the cold-L2 sweep of every feasible tile on 43 shapes: the square sizes, the
-// K-scan, rectangular and deep-K shapes (bench.py --mode sweep).  The two-CTA
-// tiles' fixed cost is then raised from the fit's 13.53 to 14.0 us: a later sweep
-// measured p128x256 7 % faster than the pair at 2048x2048x2304, where the fitted
-// constants tied the two (one round of each; no other pick among the square, K-scan
-// and P4 shapes moves).
+// Cost-model constants fitted on GB300 (152 SMs) by one non-negative least-squares
+// fit, weighted by 1 / time, over two cold-L2 sweeps of every feasible tile
+// (bench.py --mode sweep): 43 shapes (the square sizes, the K-scan around 2048^2,
+// rectangular, skinny and deep-K shapes) and a second measurement of the 15 square and
+// K-scan ones.  The fitted model's pick is within 5.6 % of the best swept tile on
+// every one of those shapes (0.5 % on average), and stays there with each shape left
+// out of the fit in turn.
 static const LadderTile kLadder[] = {
-    SDT_TILE(64, 64, 6, "64x64", 6.174, 0.28066, 0.00000, true),
-    SDT_TILE(64, 128, 4, "64x128", 7.399, 0.32058, 0.00000, true),
-    SDT_TILE(128, 64, 4, "128x64", 7.378, 0.31033, 0.00000, true),
-    SDT_TILE(128, 128, 6, "128x128", 8.030, 0.30361, 0.00000, true),
-    SDT_TILE(128, 256, 4, "128x256", 9.910, 0.37718, 0.00000, false),
-    SDT_PTILE(128, 6, "p128x128", 10.442, 0.27964, 0.00000, true),
-    SDT_PTILE(256, 4, "p128x256", 11.265, 0.37733, 0.00000, true),
-    SDT_PAIR(128, 8, "2cta_256x128", 12.888, 0.29877, 0.00000, false),
-    SDT_PAIR(256, 6, "2cta_256x256", 14.000, 0.32647, 0.00000, true),
+    SDT_TILE(64, 64, 6, "64x64", 5.323, 0.21471, 3.548, 0.02879, true),
+    SDT_TILE(64, 128, 4, "64x128", 5.171, 0.23556, 3.615, 0.07831, true),
+    SDT_TILE(128, 64, 4, "128x64", 5.585, 0.23562, 3.147, 0.08161, true),
+    SDT_TILE(128, 128, 6, "128x128", 5.372, 0.21390, 4.557, 0.02838, true),
+    SDT_TILE(128, 256, 4, "128x256", 5.224, 0.31120, 5.706, 0.02606, false),
+    SDT_PTILE(128, 6, "p128x128", 9.242, 0.20692, 0.530, 0.02213, true),
+    SDT_PTILE(256, 4, "p128x256", 9.241, 0.31104, 1.679, 0.02061, true),
+    SDT_PAIR(128, 8, "2cta_256x128", 11.797, 0.23033, 0.171, 0.02098, false),
+    SDT_PAIR(256, 6, "2cta_256x256", 10.353, 0.21996, 1.328, 0.10876, true),
     // 224 columns: divides shapes 256 does not (3584 = 16 x 224) and fills the pairs'
     // rounds there (3584^2: 224 tiles = 2.95 rounds of 76 pairs instead of 196 = 2.58
-    // rounded up to 3 full-width rounds).  Its k-tile costs 0.96 of the 256-wide one's
-    // (measured at 3584^3 and 7168^3), not 224/256: the MMA time does not shrink in
-    // proportion to N.
-    SDT_PAIR(224, 6, "2cta_256x224", 14.000, 0.31340, 0.00000, true),
+    // rounded up to 3 full-width rounds).  It is feasible on few swept shapes, so its
+    // constants are the 256-wide tile's with the k-tile cost scaled by 0.96 (measured
+    // at 3584^3 and 7168^3: the MMA time does not shrink in proportion to N) and the
+    // streaming term by its operand bytes, 480 / 512.
+    SDT_PAIR(224, 6, "2cta_256x224", 10.353, 0.21116, 1.328, 0.10197, true),
     // Skinny tiles for few-row problems (M up to a few tens, e.g. decode rows): the
     // operands are swapped so that the many output columns fill the 128 MMA rows and
     // the M rows become a 16- or 32-wide MMA N; the weights stream through a deep ring
     // (18 / 20 KB per stage) and C is written transposed back.  gemm_ex and
     // gemm_ex_splitk only; A must be stored M x K (K contiguous).
-    SDT_STILE(16, 12, "s128x16", 7.0, 0.25, 0.00000),
-    SDT_STILE(32, 11, "s128x32", 7.0, 0.25, 0.00000),
+    SDT_STILE(16, 12, "s128x16", 7.0, 0.25),
+    SDT_STILE(32, 11, "s128x32", 7.0, 0.25),
 };
 static constexpr int kNumTiles = sizeof(kLadder) / sizeof(kLadder[0]);
 static_assert(sizeof(kSplitLaunch) / sizeof(kSplitLaunch[0]) == kNumTiles, "one split-K row per ladder tile");
@@ -184,30 +188,33 @@ static int ctas_per_sm(const LadderTile &t, int smem_per_sm) {
     return occ < 1 ? 1 : occ;
 }
 
+// Estimated run time (us) of `ctas` CTAs of non-persistent tile t, each walking
+// `kpc` k-tiles: whole waves of co-resident CTAs, a round cost per wave.
+static double wave_model_us(const LadderTile &t, double ctas, double kpc, int sm_count, int smem_per_sm) {
+    const double per_wave = double(sm_count) * ctas_per_sm(t, smem_per_sm);
+    const double waves = std::ceil(ctas / per_wave);
+    return t.fixed_us + waves * (t.round_us + std::max(0.0, kpc - t.stages) * t.kt_us) +
+           ctas * kpc / per_wave * t.bw_us;
+}
+
 // Estimated run time (us) of tile t on the shape.  Persistent tiles: one worker
-// (CTA or CTA pair) per SM (pair of SMs) walking ceil(tiles / workers) tiles,
-// fixed cost once.  Other tiles: whole waves of CTAs, fixed cost per round of
-// co-resident CTAs.  Both pay for the operand bytes the grid streams from L2.
+// (CTA or CTA pair) per SM (pair of SMs) walking ceil(tiles / workers) tiles.
+// Other tiles: whole waves of co-resident CTAs.
 static double model_us(const LadderTile &t, int64_t M, int64_t N, int64_t K, int sm_count, int smem_per_sm) {
     const double tiles = double((M + t.BM - 1) / t.BM) * double((N + t.BN - 1) / t.BN);
     const double nK = double((K + kBK - 1) / kBK);
-    const double mb = tiles * nK * double(t.BM + t.BN) * kBK * 2.0 / 1e6;
-    if (t.persistent) {
-        const double workers = t.cta_group == 2 ? double(sm_count / 2) : double(sm_count);
-        double rounds = std::ceil(tiles / workers);
-        if (t.cta_group == 2 && t.BN == 256 && tiles >= workers) {
-            // a tail of at most half the workers runs as half-width items in half a round
-            // (after at least one full round: a grid that is all tail keeps the full
-            // k-loop per item, which the fit does not cover)
-            const double tail = tiles - std::floor(tiles / workers) * workers;
-            if (tail > 0 && 2 * tail <= workers) rounds -= 0.5;
-        }
-        const double ktiles = std::max(0.0, rounds * nK - t.stages);
-        return t.fixed_us + ktiles * t.kt_us + mb * t.per_mb_us;
+    if (!t.persistent) return wave_model_us(t, tiles, nK, sm_count, smem_per_sm);
+    const double workers = t.cta_group == 2 ? double(sm_count / 2) : double(sm_count);
+    double rounds = std::ceil(tiles / workers);
+    if (t.cta_group == 2 && t.BN == 256 && tiles >= workers) {
+        // a tail of at most half the workers runs as half-width items in half a round
+        // (after at least one full round: a grid that is all tail keeps the full
+        // k-loop per item, which the fit does not cover)
+        const double tail = tiles - std::floor(tiles / workers) * workers;
+        if (tail > 0 && 2 * tail <= workers) rounds -= 0.5;
     }
-    const int occ = ctas_per_sm(t, smem_per_sm);
-    const double rounds = std::ceil(tiles / (double(sm_count) * occ));
-    return rounds * (t.fixed_us + std::max(0.0, nK - t.stages) * t.kt_us) + mb * t.per_mb_us;
+    return t.fixed_us + std::max(0.0, rounds * nK - t.stages) * t.kt_us + rounds * t.round_us +
+           tiles * nK / workers * t.bw_us;
 }
 
 static int pick_for(int64_t M, int64_t N, int64_t K, int sm_count, int smem_limit, int smem_per_sm) {
@@ -756,11 +763,9 @@ static bool splitk_feasible(const LadderTile &t, int64_t M, int64_t N, int64_t K
 // CTAs = tiles x splits, plus the reduction's fp32 traffic (written once, read once).
 static double splitk_model_us(const LadderTile &t, int64_t M, int64_t N, int64_t K, int splits, int sm_count,
                               int smem_per_sm) {
-    const double tiles = double(ceil_div(M, t.BM)) * double(ceil_div(N, t.BN)) * splits;
+    const double ctas = double(ceil_div(M, t.BM)) * double(ceil_div(N, t.BN)) * splits;
     const double kps = double(ceil_div(ceil_div(K, kBK), splits));
-    const int occ = ctas_per_sm(t, smem_per_sm);
-    const double rounds = std::ceil(tiles / (double(sm_count) * occ));
-    double us = rounds * (t.fixed_us + std::max(0.0, kps - t.stages) * t.kt_us);
+    double us = wave_model_us(t, ctas, kps, sm_count, smem_per_sm);
     if (splits > 1) us += 1.0 + double(M) * double(N) * (8.0 * splits + 2.0) / 4.0e6;  // ~4 TB/s through L2
     return us;
 }
