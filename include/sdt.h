@@ -267,7 +267,8 @@ int sdt_pick_tile_any_for(int64_t M, int64_t N, int64_t K, int sm_count, int sme
 int gemm_f16_splitk(int64_t M, int64_t N, int64_t K, const void *A, const void *B, void *C,
                     void *workspace, size_t workspace_bytes, int tile_id, int splits, int algo,
                     sdt_stream_t stream);
-/* Bytes of workspace gemm_f16_splitk needs (0 for an invalid combination). */
+/* Bytes of workspace gemm_f16_splitk needs (0 for an invalid combination, including a
+ * dimension above 2^30 or more than 2^30 - 1 output tiles, which the launch refuses). */
 size_t sdt_splitk_workspace_bytes(int64_t M, int64_t N, int64_t K, int tile_id, int splits);
 /* Zero a split-K workspace on `stream` (its counters must start at zero). */
 int sdt_splitk_workspace_init(void *workspace, size_t workspace_bytes, sdt_stream_t stream);
@@ -297,7 +298,8 @@ int gemm_ex_splitk(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, 
                    void *C, int64_t ldc, int dtype, int layout, void *workspace, size_t workspace_bytes,
                    int tile_id, int splits, int algo, sdt_stream_t stream);
 /* Bytes of workspace gemm_ex_splitk needs for any shape (0 for a tile without split-K form,
- * splits outside 1..ceil(K/64), or a non-positive dimension). */
+ * splits outside 1..ceil(K/64), a dimension outside 1..2^30, or more than 2^30 - 1 output
+ * tiles: the shapes the launch refuses). */
 size_t sdt_splitk_ex_workspace_bytes(int64_t M, int64_t N, int64_t K, int tile_id, int splits);
 /*
  * Stream-K [P4 "The Six Rounds", the last round "Stream-K": a fixed grid of
@@ -320,7 +322,7 @@ size_t sdt_splitk_ex_workspace_bytes(int64_t M, int64_t N, int64_t K, int tile_i
  * first call, left zero by every completed call), then 2*G fp32 tiles of
  * BM x BN: sdt_streamk_workspace_bytes(M,N,K,tile_id,G) bytes (G >= 1, taken
  * as at most the unit count; 0 for
- * a tile without stream-K form, a non-positive dimension, more than 65536
+ * a tile without stream-K form, a dimension outside 1..2^30, more than 65536
  * output tiles or more than 2^20 CTAs).
  */
 size_t sdt_streamk_workspace_bytes(int64_t M, int64_t N, int64_t K, int tile_id, int ctas);

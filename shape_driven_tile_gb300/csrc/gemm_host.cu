@@ -151,6 +151,7 @@ static_assert(sizeof(kStreamLaunch) / sizeof(kStreamLaunch[0]) == kNumTiles, "on
 static constexpr int kDefaultSmemLimit = 232448;  // opt-in shared memory per block on sm_100-class parts
 static constexpr int kMaxRing = 24;
 static constexpr int64_t kMaxDim = int64_t(1) << 30;
+static constexpr int64_t kMaxGridTiles = 0x3fffffff;  // output tiles of one launch
 
 // Ring depth of a launch: `req` when in 2..kMaxRing, else SDT_STAGES when set, else
 // the tile's own depth; lowered until the ring fits in shared memory.
@@ -601,7 +602,7 @@ static int run_tile_ex(int tile_id, int stagger_req, int64_t M0, int64_t N0, int
     a.ldc = int(ldc);
     a.idesc_flags = idesc_flags_for(dtype, layout);
     a.c_trans = ex.c_trans;
-    if (int64_t(a.num_m_tiles) * a.num_n_tiles > int64_t(0x3fffffff))
+    if (int64_t(a.num_m_tiles) * a.num_n_tiles > kMaxGridTiles)
         return fail(SDT_ERR_SHAPE, "grid too large");
     const int tiles = a.num_m_tiles * a.num_n_tiles;
     a.tail_start = tiles;
@@ -744,11 +745,19 @@ static bool splitk_tile_ok(int tile_id) {
     return tile_id >= 0 && tile_id < kNumTiles && kSplitLaunch[tile_id][0] != nullptr;
 }
 
+// Dimensions the launches take (they refuse the rest); the size queries apply the same
+// limits, so that their products stay far inside 64 bits.
+static bool dims_in_range(int64_t M, int64_t N, int64_t K) {
+    return M > 0 && N > 0 && K > 0 && M <= kMaxDim && N <= kMaxDim && K <= kMaxDim;
+}
+
 // Workspace bytes of split-K with tile t on any shape (0 for an invalid combination).
 static size_t splitk_ws_bytes(const LadderTile &t, int64_t M, int64_t N, int64_t K, int splits) {
+    if (!dims_in_range(M, N, K)) return 0;
     const int64_t nK = ceil_div(K, kBK);
-    if (M <= 0 || N <= 0 || K <= 0 || splits < 1 || splits > nK) return 0;
+    if (splits < 1 || splits > nK) return 0;
     const int64_t mt = ceil_div(M, t.BM), nt = ceil_div(N, t.BN);
+    if (mt * nt > kMaxGridTiles) return 0;
     return splitk_counter_bytes(mt * nt) + splitk_partials_bytes(mt * t.BM, nt * t.BN, splitk_effective(nK, splits));
 }
 
@@ -812,7 +821,7 @@ static int splitk_launch_ex(int tile_id, int splits, int algo, int64_t M0, int64
     if (splits < 1 || splits > nK) return fail(SDT_ERR_ARG, "splits must be in 1..%lld", (long long)nK);
     splits = splitk_effective(nK, splits);
     const int64_t mt = ceil_div(M, t.BM), nt = ceil_div(N, t.BN);
-    if (mt * nt > int64_t(0x3fffffff)) return fail(SDT_ERR_SHAPE, "grid too large");
+    if (mt * nt > kMaxGridTiles) return fail(SDT_ERR_SHAPE, "grid too large");
     if (algo == SDT_SPLITK_IN_KERNEL && mt * nt > kMaxCounters)
         return fail(SDT_ERR_SHAPE, "the in-kernel reduction counts at most %lld output tiles", (long long)kMaxCounters);
     const size_t need = splitk_ws_bytes(t, M, N, K, splits);
@@ -943,7 +952,7 @@ static int streamk_ctas_per_sm(const LadderTile &t, int smem_limit, int smem_per
 // on an M x N x K problem as the kernel sees it (swapped for a skinny tile), 0 for an
 // invalid combination: the counter region, then two fp32 BM x BN partial tiles per CTA.
 static size_t streamk_ws_bytes(const LadderTile &t, int64_t M, int64_t N, int64_t K, int64_t ctas) {
-    if (M <= 0 || N <= 0 || K <= 0 || ctas < 1 || ctas > kMaxStreamCtas) return 0;
+    if (!dims_in_range(M, N, K) || ctas < 1 || ctas > kMaxStreamCtas) return 0;
     const int64_t tiles = ceil_div(M, t.BM) * ceil_div(N, t.BN);
     const int64_t units = tiles * ceil_div(K, kBK);
     if (4 * tiles > kMaxCounters || units > kMaxStreamUnits) return 0;

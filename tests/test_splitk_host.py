@@ -172,3 +172,22 @@ def test_streamk_tiles_and_default_ctas():
         else:
             with pytest.raises(sdt.SdtError):
                 sdt.streamk_ctas(t["id"], sm_count=152)
+
+
+def test_workspace_queries_refuse_what_the_launches_refuse():
+    # Dimensions above 2^30, or a grid of more than 2^30 - 1 output tiles, are refused by
+    # the launches; the size queries return 0 for them instead of a product that wraps.
+    L = sdt.lib()
+    huge = 1 << 40
+    for name in SPLIT_TILES + ["s128x16"]:
+        tid = sdt.tile_id(name)
+        assert L.sdt_splitk_ex_workspace_bytes(huge, huge, 4096, tid, 32) == 0
+        assert L.sdt_splitk_ex_workspace_bytes(1 << 30, 1 << 30, 1 << 30, tid, 32) == 0   # too many tiles
+        assert L.sdt_streamk_workspace_bytes(huge, huge, 4096, tid, 152) == 0
+        assert L.sdt_streamk_workspace_bytes(64, 64, huge, tid, 152) == 0
+    # the largest dimension the launches take still sizes exactly (one tile column)
+    t = sdt.tile_info(sdt.tile_id("128x128"))
+    M = 1 << 30
+    want = COUNTER_REGION + 32 * M * t["BN"] * 4
+    assert L.sdt_splitk_ex_workspace_bytes(M, 128, 1 << 30, t["id"], 32) == want
+    assert L.sdt_splitk_workspace_bytes(M, 128, 1 << 30, t["id"], 32) == want
