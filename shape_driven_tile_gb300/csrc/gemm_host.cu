@@ -283,6 +283,18 @@ static int load_table_file(const char *path, std::map<ShapeKey, TuneEntry> *out)
     while (fgets(line, sizeof line, f)) {
         ++lineno;
         char *hash = strchr(line, '#');
+        if (!strchr(line, '\n') && !feof(f)) {
+            // a line longer than the buffer: its rest is read and dropped, which is
+            // only right when the cut falls inside a comment
+            int c;
+            while ((c = fgetc(f)) != EOF && c != '\n') {
+            }
+            if (!hash) {
+                fclose(f);
+                return fail(SDT_ERR_TABLE, "%s:%d: entry longer than %d characters", path, lineno,
+                            int(sizeof line) - 2);
+            }
+        }
         if (hash) *hash = 0;
         long long M, N, K;
         char name[64];

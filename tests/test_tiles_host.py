@@ -124,6 +124,7 @@ def test_tune_table_takes_raster_and_depth(tmp_path):
     ("256 256 256 64x64 0 -2\n", "raster"),
     ("256 256 256 64x64 0 4 1\n", "stages"),
     ("256 256 256 64x64 0 4 99\n", "stages"),
+    ("256 256 256 64x64" + " " * 600 + "0\n", "longer than"),
 ])
 def test_tune_table_rejects_bad_entries(tmp_path, body, needle):
     p = tmp_path / "bad.txt"
@@ -138,6 +139,20 @@ def test_tune_table_rejects_bad_entries(tmp_path, body, needle):
         assert needle in str(e.value)
         # a rejected table leaves the previous one in place
         assert sdt.lib().sdt_tune_table_size() == 1
+    finally:
+        sdt.clear_tune_table()
+
+
+def test_tune_table_long_comment_is_not_read_as_entries(tmp_path):
+    # a comment longer than the loader's line buffer: its tail (which here looks like an
+    # entry for another shape) must not be parsed
+    p = tmp_path / "table.txt"
+    p.write_text("256 256 256 64x64  # " + "x" * 600 + " 1024 1024 1024 128x128\n512 512 512 64x64\n")
+    sdt.load_tune_table(str(p))
+    try:
+        assert sdt.lib().sdt_tune_table_size() == 2
+        assert sdt.tune_table_lookup(1024, 1024, 1024) == -1
+        assert sdt.tile_info(sdt.tune_table_lookup(512, 512, 512))["name"] == "64x64"
     finally:
         sdt.clear_tune_table()
 
