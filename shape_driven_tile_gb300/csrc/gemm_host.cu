@@ -652,8 +652,13 @@ static int run_tile(int tile_id, int stagger_req, int64_t M, int64_t N, int64_t 
 static int autotune_shape(int64_t M, int64_t N, int64_t K, const void *A, const void *B, void *C,
                           cudaStream_t stream, const DeviceInfo &dev, TuneEntry *out) {
     cudaEvent_t e0, e1;
-    if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+    if (cudaEventCreate(&e0) != cudaSuccess) {
         cudaGetLastError();
+        return fail(SDT_ERR_CUDA, "cudaEventCreate failed during autotune");
+    }
+    if (cudaEventCreate(&e1) != cudaSuccess) {
+        cudaGetLastError();
+        cudaEventDestroy(e0);
         return fail(SDT_ERR_CUDA, "cudaEventCreate failed during autotune");
     }
     int best = -1;
@@ -661,7 +666,11 @@ static int autotune_shape(int64_t M, int64_t N, int64_t K, const void *A, const 
     for (int i = 0; i < kNumTiles; ++i) {
         if (!feasible(kLadder[i], M, N, K, dev.smem_optin)) continue;
         int rc = run_tile(i, -1, M, N, K, A, B, C, stream, dev);
-        if (rc) break;
+        if (rc) {  // the launch error of this tile, not a later "nothing feasible"
+            cudaEventDestroy(e0);
+            cudaEventDestroy(e1);
+            return rc;
+        }
         cudaEventRecord(e0, stream);
         for (int r = 0; r < 5 && rc == SDT_OK; ++r) rc = run_tile(i, -1, M, N, K, A, B, C, stream, dev);
         cudaEventRecord(e1, stream);

@@ -322,3 +322,28 @@ def test_odd_width_uniform_and_picked(cuda_device, tile):
     rows = boundary_rows(M, step=64, extra=4)[::2]
     assert_close(C.cpu().double().numpy()[rows], oracle.gemm(u16(A), u16(B), rows=rows), K, tile_name(tile))
     assert tile in sdt.feasible_tiles(3584, 3584, 3584)
+
+
+# ---- opt-in measured sweep (SDT_AUTOTUNE=1) ------------------------------------------
+
+
+def test_autotune_times_the_feasible_tiles_and_remembers_one(cuda_device, monkeypatch):
+    M, N, K = 512, 768, 1024
+    A = inputs.integers((M, K), seed=inputs.seed_for(9, 0))
+    B = inputs.integers((K, N), seed=inputs.seed_for(9, 1))
+    want = oracle.gemm(u16(A), u16(B))
+    Ad, Bd = A.to(cuda_device), B.to(cuda_device)
+    sdt.clear_tune_table()
+    try:
+        monkeypatch.setenv("SDT_AUTOTUNE", "1")
+        C = run(Ad, Bd, cuda_device)
+        tid = sdt.tune_table_lookup(M, N, K)
+        assert tid in sdt.feasible_tiles(M, N, K)
+        assert_bit_exact_f16(C, want, f"autotuned {tile_name(tid)}")
+        # the remembered tile serves the next call without the variable
+        monkeypatch.delenv("SDT_AUTOTUNE")
+        C2 = run(Ad, Bd, cuda_device)
+        assert sdt.tune_table_lookup(M, N, K) == tid
+        assert_bit_exact_f16(C2, want, "served from the table")
+    finally:
+        sdt.clear_tune_table()
