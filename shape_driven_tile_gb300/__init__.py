@@ -32,6 +32,29 @@ def _stream(stream):
     return ctypes.c_void_p(int(stream))
 
 
+def _one_device(**tensors):
+    """Every operand must be a CUDA tensor on the current device: the library launches on
+    the current device, so a host pointer or another GPU's memory would reach its kernels."""
+    current = None
+    for name, t in tensors.items():
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if current is None:
+            current = torch.cuda.current_device()
+        if t.device.index != current:
+            raise ValueError(f"{name} is on {t.device}, but the current device is cuda:{current}")
+
+
+def _workspace(workspace):
+    if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda:
+        raise TypeError("workspace must be a CUDA tensor")
+    if not workspace.is_contiguous():
+        raise ValueError("workspace must be contiguous")
+    return workspace.numel() * workspace.element_size()
+
+
 def _need(t, name, dtype, ndim):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
@@ -58,6 +81,7 @@ def _gemm_args(A, B, C):
         _need(C, "C", torch.float16, 2)
         if tuple(C.shape) != (M, N):
             raise ValueError(f"C must be {(M, N)}, got {tuple(C.shape)}")
+    _one_device(A=A, B=B, C=C)
     return M, N, K, C
 
 
@@ -89,6 +113,7 @@ def _gemv_args(x, W, y, wdtype):
         _need(y, "y", torch.float32, 1)
         if y.shape[0] != N:
             raise ValueError("y must have length N")
+    _one_device(x=x, W=W, y=y)
     return K, N, y
 
 
@@ -105,6 +130,7 @@ def gemv_m1_q8(x, q, scales, y=None, *, stream=None):
     _need(scales, "scales", torch.float16, 2)
     if K % 32 or tuple(scales.shape) != (N, K // 32):
         raise ValueError(f"scales must be {(N, K // 32)} with K % 32 == 0")
+    _one_device(x=x, scales=scales)
     check(lib().gemv_m1_q8(K, N, x.data_ptr(), q.data_ptr(), scales.data_ptr(), y.data_ptr(),
                            _stream(stream)))
     return y
@@ -137,10 +163,13 @@ def _layout_of(T, name):
 
 def _ex_args(A, B, C):
     """(M, N, K, lda, ldb, ldc, layout, C) of gemm_ex-style views."""
+    if not isinstance(A, torch.Tensor) or not isinstance(B, torch.Tensor):
+        raise TypeError("A and B must be torch.Tensors")
     if A.dtype not in DTYPE_CODES or B.dtype != A.dtype:
         raise TypeError("A and B must both be float16 or both bfloat16")
-    if not (A.is_cuda and B.is_cuda):
-        raise ValueError("A and B must be CUDA tensors")
+    _one_device(A=A, B=B)
+    if A.dim() != 2 or B.dim() != 2:
+        raise ValueError("A and B must be 2-D")
     M, K = A.shape
     K2, N = B.shape
     if K != K2:
@@ -149,8 +178,12 @@ def _ex_args(A, B, C):
     b_t, ldb = _layout_of(B, "B")
     if C is None:
         C = torch.empty((M, N), dtype=A.dtype, device=A.device)
-    elif C.dtype != A.dtype or tuple(C.shape) != (M, N) or (C.stride(1) != 1 and N > 1):
-        raise ValueError(f"C must be a row-major {A.dtype} [{M}, {N}] view")
+    else:
+        if not isinstance(C, torch.Tensor):
+            raise TypeError("C must be a torch.Tensor")
+        if C.dtype != A.dtype or C.dim() != 2 or tuple(C.shape) != (M, N) or (C.stride(1) != 1 and N > 1):
+            raise ValueError(f"C must be a row-major {A.dtype} [{M}, {N}] view")
+        _one_device(A=A, C=C)
     ldc = C.stride(0) if M > 1 else max(C.stride(0), N)
     layout = (LAYOUT_A_T if a_t else 0) | (LAYOUT_B_T if b_t else 0)
     return M, N, K, lda, ldb, ldc, layout, C
@@ -194,9 +227,8 @@ def gemm_f16_splitk(A, B, C=None, *, workspace, tile=-1, splits: int = 0,
     """Split-K GEMM with a caller-owned workspace (see sdt.h); tile -1 picks tile and splits."""
     M, N, K, C = _gemm_args(A, B, C)
     tid = tile_id(tile) if isinstance(tile, str) else int(tile)
-    if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda:
-        raise TypeError("workspace must be a CUDA tensor")
-    nbytes = workspace.numel() * workspace.element_size()
+    nbytes = _workspace(workspace)
+    _one_device(A=A, workspace=workspace)
     check(lib().gemm_f16_splitk(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(), workspace.data_ptr(), nbytes,
                                 tid, int(splits), int(algo), _stream(stream)))
     return C
@@ -215,9 +247,8 @@ def gemm_ex_splitk(A, B, C=None, *, workspace, tile=-1, splits: int = 0, algo: i
     count, 0 = one per SM slot)."""
     M, N, K, lda, ldb, ldc, layout, C = _ex_args(A, B, C)
     tid = tile_id(tile) if isinstance(tile, str) else int(tile)
-    if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda:
-        raise TypeError("workspace must be a CUDA tensor")
-    nbytes = workspace.numel() * workspace.element_size()
+    nbytes = _workspace(workspace)
+    _one_device(A=A, workspace=workspace)
     check(lib().gemm_ex_splitk(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, C.data_ptr(), ldc,
                                DTYPE_CODES[A.dtype], layout, workspace.data_ptr(), nbytes, tid, int(splits),
                                int(algo), _stream(stream)))
