@@ -1,0 +1,58 @@
+"""The cost-model constants in the library are the fit of the frozen sweep (host only).
+
+shape_driven_tile_gb300.costfit restates pick_tile's estimate over the library's tile
+geometry and fits its constants to a measured sweep; refitting the frozen GB300 sweep must
+give the ladder's printed constants, and the restated estimate must pick the library's tile.
+"""
+import os
+import re
+
+import pytest
+
+import shape_driven_tile_gb300 as sdt
+from shape_driven_tile_gb300 import costfit
+
+pytest.importorskip("scipy")
+
+PKG = os.path.dirname(sdt.__file__)
+TABLE = os.path.join(PKG, "tables", "gb300_tile_sweep.jsonl")
+HOST = os.path.join(PKG, "csrc", "gemm_host.cu")
+ROW = re.compile(r'SDT_(?:TILE|PTILE|PAIR)\([^"]*"([^"]+)",\s*([-\d.]+),\s*([-\d.]+),\s*([-\d.]+),\s*([-\d.]+),'
+                 r'\s*(true|false)\)')
+
+
+def ladder_source():
+    with open(HOST) as f:
+        return {m[0]: (tuple(float(v) for v in m[1:5]), m[5] == "true") for m in ROW.findall(f.read())}
+
+
+def test_source_rows_cover_the_ladder():
+    rows = ladder_source()
+    assert set(rows) == set(costfit.geometry())
+    for name, (_, candidate) in rows.items():
+        assert candidate == (name not in costfit.NOT_CANDIDATES), name
+
+
+def test_refit_reproduces_the_ladder_constants():
+    fitted = costfit.ladder_rows(costfit.fit(costfit.load(TABLE)))
+    for name, (consts, _) in ladder_source().items():
+        got = fitted[name]
+        for field, want, have, unit in zip(costfit.FIELDS, consts, got, (1e-3, 1e-5, 1e-3, 1e-5)):
+            assert abs(want - have) <= unit * 1.01, (name, field, want, have)
+
+
+def test_restated_estimate_picks_the_library_tile():
+    records = costfit.load(TABLE)
+    consts = {n: list(c) for n, c in costfit.ladder_rows(costfit.fit(records)).items()}
+    geo = costfit.geometry()
+    for r in records:
+        M, N, K = r["shape"]
+        lib_pick = sdt.tile_info(sdt.pick_tile(M, N, K, sm_count=152, smem_limit=232448))["name"]
+        assert costfit.pick(consts, r, geo=geo) == lib_pick, r["shape"]
+
+
+def test_each_fit_term_is_needed_somewhere():
+    # the fit is non-negative; a term that fits to zero on every tile would be dead weight
+    consts = costfit.fit(costfit.load(TABLE))
+    for i, field in enumerate(costfit.FIELDS):
+        assert any(c[i] > 0 for c in consts.values()), field
