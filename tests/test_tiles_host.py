@@ -173,3 +173,26 @@ def test_skinny_tiles_are_never_feasible_for_gemm_f16():
     for t in skinny:
         assert sdt.splitk_workspace_bytes(256, 32, 4096, t, 2) == 0        # not gemm_f16_splitk
         assert sdt.splitk_ex_workspace_bytes(16, 4096, 4096, t, 2) > 0     # gemm_ex_splitk
+
+
+def test_pick_tile_any_matches_pick_tile_where_the_tiles_divide():
+    # gemm_ex's picker lets tiles overhang ragged edges; on the measured configurations,
+    # where the tiles divide the shape, it must make gemm_f16's choice
+    shapes = [(n, n, n) for n in (256, 512, 768, 1024, 1536, 2048, 2560, 3072, 3584, 4096, 8192)]
+    shapes += [(2048, 2048, k) for k in (1920, 1984, 2048, 2112, 2176, 2304)]
+    for M, N, K in shapes:
+        assert sdt.pick_tile_any(M, N, K, sm_count=152, smem_limit=SMEM) == \
+            sdt.pick_tile(M, N, K, sm_count=152, smem_limit=SMEM), (M, N, K)
+
+
+def test_pick_tile_any_on_ragged_shapes():
+    candidates = {t["id"] for t in ladder() if t["name"] not in ("128x256", "2cta_256x128")}
+    for M, N, K in itertools.product([1, 7, 100, 1000, 4097], [8, 136, 1000, 16384], [1, 9, 70, 4096]):
+        tid = sdt.pick_tile_any(M, N, K, sm_count=152, smem_limit=SMEM)
+        assert tid in candidates, (M, N, K, tid)
+        assert sdt.tile_info(tid)["smem_bytes"] <= SMEM
+    for bad in [(0, 8, 8), (8, -1, 8), (8, 8, 0)]:
+        with pytest.raises(sdt.SdtError):
+            sdt.pick_tile_any(*bad, sm_count=152, smem_limit=SMEM)
+    with pytest.raises(sdt.SdtError):
+        sdt.pick_tile_any(8, 8, 8, sm_count=0, smem_limit=SMEM)
