@@ -1,11 +1,12 @@
 """Fit of pick_tile's cost-model constants to a measured tile sweep (host only, no GPU).
 
-pick_tile estimates each feasible tile's run time on a shape from four constants per
+pick_tile estimates each feasible tile's run time on a shape from five constants per
 tile (microseconds) and takes the smallest estimate; the estimate has the form of
 ``model_us`` in csrc/gemm_host.cu:
 
   one-CTA tiles, in waves of co-resident CTAs (waves = ceil(tiles / (SMs x CTAs per SM))):
       fixed + waves * (round + max(0, nK - stages) * kt) + tiles * nK / (SMs x CTAs per SM) * bw
+      + share * (CTAs beyond the first on the busiest SM, summed over the waves)
   persistent tiles, one worker per SM or per SM pair (rounds = ceil(tiles / workers), minus
   half a round when the two-CTA 256x256 tail runs as half-width items):
       fixed + max(0, rounds * nK - stages) * kt + rounds * round + tiles * nK / workers * bw
@@ -35,7 +36,7 @@ NOT_CANDIDATES = {"128x256", "2cta_256x128"}  # tiles that never won the sweep
 # name: (source tile, k-tile scale, streaming-term scale).  The 256x224 pair: an N = 224
 # MMA takes 0.96 of an N = 256 one (measured at 3584^3 and 7168^3); operand bytes 480 / 512.
 DERIVED = {"2cta_256x224": ("2cta_256x256", 0.96, 480 / 512)}
-FIELDS = ("fixed", "kt", "round", "bw")
+FIELDS = ("fixed", "kt", "round", "bw", "share")
 
 
 def load(path):
@@ -68,7 +69,7 @@ def geometry():
 
 
 def features(geo, M, N, K, sm_count=SM_COUNT):
-    """The four multipliers of (fixed, kt, round, bw) for one tile on one shape."""
+    """The multipliers of (fixed, kt, round, bw, share) for one tile on one shape."""
     BM, BN, persistent, pair, occ, stages = geo
     tiles = math.ceil(M / BM) * math.ceil(N / BN)
     nK = math.ceil(K / KB)
@@ -79,14 +80,16 @@ def features(geo, M, N, K, sm_count=SM_COUNT):
             tail = tiles - (tiles // workers) * workers
             if 0 < tail and 2 * tail <= workers:
                 rounds -= 0.5
-        return np.array([1.0, max(0.0, rounds * nK - stages), rounds, tiles * nK / workers])
+        return np.array([1.0, max(0.0, rounds * nK - stages), rounds, tiles * nK / workers, 0.0])
     per_wave = sm_count * occ
     waves = math.ceil(tiles / per_wave)
-    return np.array([1.0, waves * max(0, nK - stages), waves, tiles * nK / per_wave])
+    full, rest = divmod(tiles, per_wave)
+    extra = full * (occ - 1) + (min(occ, math.ceil(rest / sm_count)) - 1 if rest else 0)
+    return np.array([1.0, waves * max(0, nK - stages), waves, tiles * nK / per_wave, extra])
 
 
 def fit(records, sm_count=SM_COUNT):
-    """name -> array (fixed, kt, round, bw) fitted to the records."""
+    """name -> array (fixed, kt, round, bw, share) fitted to the records."""
     from scipy.optimize import nnls
 
     geo = geometry()
@@ -125,8 +128,9 @@ def pick(consts, record, sm_count=SM_COUNT, geo=None):
 
 
 def ladder_rows(consts):
-    """The constants as printed in the ladder (fixed and round to 3 decimals, kt and bw to 5)."""
-    return {name: (round(c[0], 3), round(c[1], 5), round(c[2], 3), round(c[3], 5)) for name, c in consts.items()}
+    """The constants as printed in the ladder (fixed, round and share to 3 decimals, kt and bw to 5)."""
+    return {name: (round(c[0], 3), round(c[1], 5), round(c[2], 3), round(c[3], 5), round(c[4], 3))
+            for name, c in consts.items()}
 
 
 def main(argv):
@@ -135,8 +139,8 @@ def main(argv):
         return 2
     records = load(argv[1])
     consts = fit(records)
-    for name, (f, kt, rnd, bw) in ladder_rows(consts).items():
-        print(f"{name:14s} fixed {f:.3f}  kt {kt:.5f}  round {rnd:.3f}  bw {bw:.5f}")
+    for name, (f, kt, rnd, bw, shr) in ladder_rows(consts).items():
+        print(f"{name:14s} fixed {f:.3f}  kt {kt:.5f}  round {rnd:.3f}  bw {bw:.5f}  share {shr:.3f}")
     slow = [r["us"][pick(consts, r)] / min(r["us"].values()) - 1 for r in records]
     print(f"pick slowdown over {len(records)} records: average {100 * sum(slow) / len(slow):.2f} %, "
           f"worst {100 * max(slow):.2f} %")

@@ -13,6 +13,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cerrno>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -75,57 +76,60 @@ struct LadderTile {
     //   bw    -- per k-tile of the whole grid's work divided by the workers the
     //            device holds: the share of the operand streaming that the L2
     //            does not overlap with the MMAs (large for the wide pair tile)
+    //   share -- per CTA beyond the first on the busiest SM of a wave (tiles that
+    //            fit two CTAs per SM)
     double fixed_us;
     double kt_us;
     double round_us;
     double bw_us;
+    double share_us;
     bool candidate;   // considered by pick_tile (tiles dominated everywhere in the sweep are not)
     bool swap = false;  // skinny tile: runs C^T = op(B)^T . op(A)^T (gemm_ex forms only)
 };
 
 #define SDT_LAUNCH4_(FN, ...) {&FN<__VA_ARGS__, 0>, &FN<__VA_ARGS__, 1>, &FN<__VA_ARGS__, 2>, &FN<__VA_ARGS__, 3>}
 
-#define SDT_TILE(BM_, BN_, STAGES_, NAME_, FIX_, KT_, RND_, BW_, CAND_)                                \
+#define SDT_TILE(BM_, BN_, STAGES_, NAME_, FIX_, KT_, RND_, BW_, SHR_, CAND_)                          \
     LadderTile {                                                                                   \
         BM_, BN_, 1, STAGES_, NAME_, SDT_LAUNCH4_(launch_gemm_tile, BM_, BN_),                     \
             TileCfg<BM_, BN_>::STAGE_BYTES, TileCfg<BM_, BN_>::ALIGN_SLACK + TileCfg<BM_, BN_>::CTRL_BYTES, \
-            TileCfg<BM_, BN_>::TMEM_COLS, TileCfg<BM_, BN_>::THREADS, false, FIX_, KT_, RND_, BW_, CAND_ \
+            TileCfg<BM_, BN_>::TMEM_COLS, TileCfg<BM_, BN_>::THREADS, false, FIX_, KT_, RND_, BW_, SHR_, CAND_ \
     }
 
 #define SDT_PTILE(BN_, STAGES_, NAME_, FIX_, KT_, RND_, BW_, CAND_)                                     \
     LadderTile {                                                                                   \
         128, BN_, 1, STAGES_, NAME_, SDT_LAUNCH4_(launch_gemm_persistent, BN_),                    \
             PersistentCfg<BN_>::STAGE_BYTES, PersistentCfg<BN_>::ALIGN_SLACK + PersistentCfg<BN_>::CTRL_BYTES, \
-            PersistentCfg<BN_>::TMEM_COLS, PersistentCfg<BN_>::THREADS, true, FIX_, KT_, RND_, BW_, CAND_ \
+            PersistentCfg<BN_>::TMEM_COLS, PersistentCfg<BN_>::THREADS, true, FIX_, KT_, RND_, BW_, 0.0, CAND_ \
     }
 
 #define SDT_STILE(BN_, STAGES_, NAME_, FIX_, KT_)                                                    \
     LadderTile {                                                                                   \
         128, BN_, 1, STAGES_, NAME_, SDT_LAUNCH4_(launch_gemm_tile, 128, BN_),                     \
             TileCfg<128, BN_>::STAGE_BYTES, TileCfg<128, BN_>::ALIGN_SLACK + TileCfg<128, BN_>::CTRL_BYTES, \
-            TileCfg<128, BN_>::TMEM_COLS, TileCfg<128, BN_>::THREADS, false, FIX_, KT_, 0.0, 0.0, false, true \
+            TileCfg<128, BN_>::TMEM_COLS, TileCfg<128, BN_>::THREADS, false, FIX_, KT_, 0.0, 0.0, 0.0, false, true \
     }
 
 #define SDT_PAIR(BN_, STAGES_, NAME_, FIX_, KT_, RND_, BW_, CAND_)                                      \
     LadderTile {                                                                                   \
         256, BN_, 2, STAGES_, NAME_, SDT_LAUNCH4_(launch_gemm_pair, BN_), PairCfg<BN_>::STAGE_BYTES, \
             PairCfg<BN_>::ALIGN_SLACK + PairCfg<BN_>::CTRL_BYTES, PairCfg<BN_>::TMEM_COLS,         \
-            PairCfg<BN_>::THREADS, true, FIX_, KT_, RND_, BW_, CAND_                                   \
+            PairCfg<BN_>::THREADS, true, FIX_, KT_, RND_, BW_, 0.0, CAND_                                  \
     }
 
 // Cost-model constants fitted on GB300 (152 SMs) by one non-negative least-squares
 // fit, weighted by 1 / time, over two cold-L2 sweeps of every feasible tile
 // (bench.py --mode sweep): 43 shapes (the square sizes, the K-scan around 2048^2,
 // rectangular, skinny and deep-K shapes) and a second measurement of the 15 square and
-// K-scan ones.  The fitted model's pick is within 5.6 % of the best swept tile on
-// every one of those shapes (0.5 % on average), and stays there with each shape left
-// out of the fit in turn.
+// K-scan ones.  The fitted model's pick is within 4.5 % of the best swept tile on
+// every one of those shapes (0.24 % on average), and stays there with each shape
+// left out of the fit in turn (python -m shape_driven_tile_gb300.costfit refits it).
 static const LadderTile kLadder[] = {
-    SDT_TILE(64, 64, 6, "64x64", 5.323, 0.21471, 3.548, 0.02879, true),
-    SDT_TILE(64, 128, 4, "64x128", 5.171, 0.23556, 3.615, 0.07831, true),
-    SDT_TILE(128, 64, 4, "128x64", 5.585, 0.23562, 3.147, 0.08161, true),
-    SDT_TILE(128, 128, 6, "128x128", 5.372, 0.21390, 4.557, 0.02838, true),
-    SDT_TILE(128, 256, 4, "128x256", 5.224, 0.31120, 5.706, 0.02606, false),
+    SDT_TILE(64, 64, 6, "64x64", 6.154, 0.22679, 2.362, 0.00893, 1.472, true),
+    SDT_TILE(64, 128, 4, "64x128", 6.272, 0.24633, 2.248, 0.05573, 1.436, true),
+    SDT_TILE(128, 64, 4, "128x64", 6.641, 0.24566, 1.839, 0.06036, 1.370, true),
+    SDT_TILE(128, 128, 6, "128x128", 5.372, 0.21390, 4.557, 0.02838, 0.000, true),
+    SDT_TILE(128, 256, 4, "128x256", 5.224, 0.31120, 5.706, 0.02606, 0.000, false),
     SDT_PTILE(128, 6, "p128x128", 9.242, 0.20692, 0.530, 0.02213, true),
     SDT_PTILE(256, 4, "p128x256", 9.241, 0.31104, 1.679, 0.02061, true),
     SDT_PAIR(128, 8, "2cta_256x128", 11.797, 0.23033, 0.171, 0.02098, false),
@@ -192,10 +196,16 @@ static int ctas_per_sm(const LadderTile &t, int smem_per_sm) {
 // Estimated run time (us) of `ctas` CTAs of non-persistent tile t, each walking
 // `kpc` k-tiles: whole waves of co-resident CTAs, a round cost per wave.
 static double wave_model_us(const LadderTile &t, double ctas, double kpc, int sm_count, int smem_per_sm) {
-    const double per_wave = double(sm_count) * ctas_per_sm(t, smem_per_sm);
+    const int occ = ctas_per_sm(t, smem_per_sm);
+    const double per_wave = double(sm_count) * occ;
     const double waves = std::ceil(ctas / per_wave);
+    // CTAs beyond the first on the busiest SM: occ - 1 in each full wave, and in the
+    // last wave as many as its CTAs need
+    const double full = std::floor(ctas / per_wave), rest = ctas - full * per_wave;
+    double extra = full * (occ - 1);
+    if (rest > 0) extra += std::min(double(occ), std::ceil(rest / sm_count)) - 1;
     return t.fixed_us + waves * (t.round_us + std::max(0.0, kpc - t.stages) * t.kt_us) +
-           ctas * kpc / per_wave * t.bw_us;
+           ctas * kpc / per_wave * t.bw_us + extra * t.share_us;
 }
 
 // Estimated run time (us) of tile t on the shape.  Persistent tiles: one worker
@@ -545,11 +555,16 @@ __global__ void zero_fill_f16(__half *C, size_t n) {
     for (; i < n; i += stride) C[i] = __ushort_as_half(0);
 }
 
+// A numeric knob: unset, empty or not a whole decimal number -> the default; else
+// clamped to [lo, hi].
 static int env_int(const char *name, int dflt, int lo, int hi) {
     const char *s = getenv(name);
     if (!s || !*s) return dflt;
-    int v = atoi(s);
-    return v < lo ? lo : (v > hi ? hi : v);
+    char *end = nullptr;
+    errno = 0;
+    const long v = strtol(s, &end, 10);
+    if (end == s || *end != '\0' || errno == ERANGE) return dflt;
+    return v < lo ? lo : (v > hi ? hi : int(v));
 }
 
 // SDT_STAGGER: "0"/"off", "1"/"on", or "auto" (default): on for the one-CTA tiles,

@@ -3,8 +3,8 @@
 The FlyDSL RDNA GEMM pull request checks the tile pick_tile returns for each
 measured shape; here the measurements themselves are frozen with the package
 (every feasible ladder tile timed cold on GB300) and the pick is held to them:
-on the square sweep and the K-scan within 5 % of the best tile, on every
-recorded shape within 6 %, and within 1 % on average.
+within 5 % of the best tile on every recorded shape (the square sweep, the
+K-scan, rectangular, skinny and deep-K shapes), and within 1 % on average.
 """
 import json
 import os
@@ -59,5 +59,5 @@ def test_pick_within_5_percent_on_the_configurations(rec):
 
 def test_pick_on_every_recorded_shape():
     s = [slowdown(r) for r in records()]
-    assert max(s) <= 0.06
+    assert max(s) <= 0.05
     assert sum(s) / len(s) <= 0.01
