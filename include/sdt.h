@@ -170,9 +170,12 @@ int sdt_feasible_tiles(int64_t M, int64_t N, int64_t K, int *ids, int cap);
 /*
  * pick_tile [P3 "Changes"; P1 "The part that actually mattered"]: the
  * heuristic tile for (M,N,K) on a GPU with `sm_count` SMs, chosen among the
- * feasible tiles by how many CTAs each grid yields against the SM count and a
- * per-tile throughput fitted to a measured sweep.  Needs no GPU and measures
- * nothing.  Returns a tile id, or SDT_ERR_SHAPE when no tile is feasible.
+ * feasible tiles by an estimate of each one's run time: the waves (or, for
+ * the persistent and two-CTA tiles, the rounds per worker) its grid makes on
+ * `sm_count` SMs, priced by per-tile launch, k-tile, per-round, operand
+ * streaming and co-residency costs fitted to a measured sweep.  Needs no GPU
+ * and measures nothing.  Returns a tile id, or SDT_ERR_SHAPE when no tile is
+ * feasible.
  * The plain form reads the current device's SM count and shared-memory limit.
  */
 int sdt_pick_tile_for(int64_t M, int64_t N, int64_t K, int sm_count, int smem_limit);
