@@ -505,7 +505,7 @@ def run_default(args):
                      "largest_share_in_step": f"gemm_f16 {largest_share}^3",
                      "achieved": round(achieved, 1), "peak": peaks["tflops"], "unit": "TFLOP/s",
                      "frac": round(achieved / peaks["tflops"], 4), "peak_source": peaks["source"] + " bf16 burst",
-                     "traffic": traffic},
+                     "traffic": traffic, **({"traffic_note": traffic_note(f"gemm_{dom}")} if traffic is None else {})},
         "cpu_baseline": baseline,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
@@ -606,6 +606,22 @@ def load_traffic(kernel_key):
     if not isinstance(e, dict) or kind not in SOURCES or e.get("source_digest") != kernel_source_digest(kind):
         return None
     return e.get("bytes")
+
+
+def traffic_note(kernel_key):
+    """Why load_traffic gave None: no record, or a record taken on other sources (its
+    digest beside the current one); None when the record is in use."""
+    if load_traffic(kernel_key) is not None:
+        return None
+    kind = kernel_key.split("_")[0]
+    e = None
+    if os.path.exists(TRAFFIC):
+        with open(TRAFFIC) as f:
+            e = json.load(f).get(kernel_key)
+    if not isinstance(e, dict):
+        return "no ncu record for this launch"
+    return (f"the ncu record ({e.get('bytes')} bytes) was taken on sources {e.get('source_digest')}; "
+            f"the current ones are {kernel_source_digest(kind)}")
 
 
 def record_traffic(args):

@@ -105,8 +105,12 @@ def test_record_traffic_and_staleness(tmp_path, monkeypatch):
     bench.record_traffic(types.SimpleNamespace(ncu_csv=str(csv_path), key="gemv_q8"))
     assert bench.load_traffic("gemv_q8") == 53510000 + 49150
     # a record taken on other sources is not used
+    assert bench.traffic_note("gemv_q8") is None
     monkeypatch.setattr(bench, "kernel_source_digest", lambda kind="gemm": "0" * 16)
     assert bench.load_traffic("gemv_q8") is None
+    note = bench.traffic_note("gemv_q8")
+    assert "53559150 bytes" in note and "0" * 16 in note
+    assert bench.traffic_note("gemm_4096") == "no ncu record for this launch"
 
 
 def test_tuned_configurations_freeze_into_a_loadable_table(tmp_path):
