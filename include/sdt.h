@@ -228,6 +228,13 @@ int gemm_ex(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const v
             void *C, int64_t ldc, int dtype, int layout, int tile_id, sdt_stream_t stream);
 /* pick_tile's cost model over every tile for any shape (tiles may overhang); needs no GPU. */
 int sdt_pick_tile_any_for(int64_t M, int64_t N, int64_t K, int sm_count, int smem_limit);
+/*
+ * The run-time estimate (microseconds) pick_tile gives tile `tile_id` on an M x N x K
+ * problem with `sm_count` SMs (228 KiB of shared memory per SM), whether or not the
+ * tile divides the shape or is a candidate; a negative status (SDT_ERR_TILE, SDT_ERR_ARG)
+ * for an unknown tile or a dimension outside 1..2^30.  Needs no GPU.
+ */
+double sdt_tile_estimate_us(int tile_id, int64_t M, int64_t N, int64_t K, int sm_count);
 
 /*
  * Split-K [P4 "The Six Rounds", the "Split-K" step: the contraction is split

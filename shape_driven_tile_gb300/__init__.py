@@ -15,7 +15,7 @@ from ._lib import SdtError, check, lib, sdt_tile_desc
 
 __all__ = [
     "SdtError", "gemm_f16", "gemm_f16_with_tile", "gemv_m1", "gemv_m1_bf16", "gemv_m1_q8",
-    "feasible_tiles", "pick_tile", "seed_tile", "tile_info", "tiles", "tile_id",
+    "feasible_tiles", "pick_tile", "tile_estimate_us", "seed_tile", "tile_info", "tiles", "tile_id",
     "load_tune_table", "clear_tune_table", "tune_table_lookup", "check_device_status",
     "debug_timeout_probe", "device_sm_count", "lib", "gemm_f16_splitk", "splitk_workspace",
     "splitk_workspace_bytes", "pick_splitk", "pick_tile_any", "gemm_ex_splitk",
@@ -332,6 +332,15 @@ def pick_tile_any(M: int, N: int, K: int, sm_count: int | None = None, smem_limi
         sm_count, smem_limit = device_sm_count(), lib().sdt_device_smem_optin()
     return check(lib().sdt_pick_tile_any_for(M, N, K, int(sm_count),
                                              int(smem_limit) if smem_limit is not None else 232448))
+
+
+def tile_estimate_us(tile, M: int, N: int, K: int, sm_count: int = 152) -> float:
+    """pick_tile's run-time estimate (microseconds) of a ladder tile (id or name) on the shape."""
+    tid = tile_id(tile) if isinstance(tile, str) else int(tile)
+    v = lib().sdt_tile_estimate_us(tid, M, N, K, int(sm_count))
+    if v < 0:
+        check(int(v))
+    return v
 
 
 def seed_tile(M: int, N: int, units: int) -> int:

@@ -57,6 +57,7 @@ SIGNATURES = {
     "gemm_f16_splitk_noalloc": (cint, [i64, i64, i64, vp, vp, vp, cint, cint, vp]),
     "gemm_ex": (cint, [i64, i64, i64, vp, i64, vp, i64, vp, i64, cint, cint, cint, vp]),
     "sdt_pick_tile_any_for": (cint, [i64, i64, i64, cint, cint]),
+    "sdt_tile_estimate_us": (ctypes.c_double, [cint, i64, i64, i64, cint]),
     "gemm_ex_splitk": (cint, [i64, i64, i64, vp, i64, vp, i64, vp, i64, cint, cint, vp, ctypes.c_size_t, cint, cint,
                               cint, vp]),
     "sdt_splitk_ex_workspace_bytes": (ctypes.c_size_t, [i64, i64, i64, cint, cint]),

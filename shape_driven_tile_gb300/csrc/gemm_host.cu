@@ -1271,6 +1271,14 @@ int sdt_feasible_tiles(int64_t M, int64_t N, int64_t K, int *ids, int cap) {
     return sdt_feasible_tiles_for(M, N, K, dev.smem_optin, ids, cap);
 }
 
+double sdt_tile_estimate_us(int tile_id, int64_t M, int64_t N, int64_t K, int sm_count) {
+    clear_error();
+    if (tile_id < 0 || tile_id >= kNumTiles) return fail(SDT_ERR_TILE, "unknown tile id %d", tile_id);
+    if (sm_count <= 0 || M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return fail(SDT_ERR_ARG, "dimensions must be in 1..2^30 and sm_count positive");
+    return model_us(kLadder[tile_id], M, N, K, sm_count, 233472);
+}
+
 int sdt_pick_tile_for(int64_t M, int64_t N, int64_t K, int sm_count, int smem_limit) {
     clear_error();
     if (sm_count <= 0) return fail(SDT_ERR_ARG, "sm_count must be positive");

@@ -63,3 +63,25 @@ def test_each_fit_term_is_needed_somewhere():
     consts = costfit.fit(costfit.load(TABLE))
     for i, field in enumerate(costfit.FIELDS):
         assert any(c[i] > 0 for c in consts.values()), field
+
+
+def test_restated_estimate_equals_the_library_estimate():
+    # the same numbers, not only the same picks: costfit's restatement with the printed
+    # constants against sdt_tile_estimate_us, over the recorded shapes and a ragged grid
+    consts = {n: list(c) for n, c in ladder_source_consts().items()}
+    geo = costfit.geometry()
+    shapes = [tuple(r["shape"]) for r in costfit.load(TABLE)]
+    shapes += [(m, n, k) for m in (1, 100, 1000, 5000) for n in (8, 300, 4096) for k in (1, 70, 4096)]
+    for M, N, K in shapes:
+        for name in geo:
+            want = costfit.estimate(consts, name, M, N, K, geo=geo)
+            have = sdt.tile_estimate_us(name, M, N, K, sm_count=152)
+            assert abs(have - want) <= 1e-9 * max(1.0, want), (name, M, N, K, have, want)
+    with pytest.raises(sdt.SdtError):
+        sdt.tile_estimate_us(99, 64, 64, 64)
+    with pytest.raises(sdt.SdtError):
+        sdt.tile_estimate_us("64x64", 0, 64, 64)
+
+
+def ladder_source_consts():
+    return {name: vals for name, (vals, _) in ladder_source().items()}
