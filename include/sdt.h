@@ -354,15 +354,21 @@ int sdt_pick_splitk_any_for(int64_t M, int64_t N, int64_t K, int sm_count, int s
  * budget and no allocator, latency-critical loops that forbid allocator calls.
  *
  * Arguments as gemm_f16_splitk, minus the workspace and the algorithm
- * (tile_id < 0 picks tile and splits).  Shapes whose partials
- * (sdt_splitk_workspace_bytes) exceed 16 MiB are rejected with SDT_ERR_ARG
- * and a message naming the sizes.  The first call on each device looks up the
- * array's device address (cudaGetSymbolAddress) with that device current;
- * make that first call before any stream capture.  Every GPU on which the
- * library's module holding the array is loaded keeps the 16 MiB until the
- * process exits.  All calls share the array: nothing in it has to start at
- * zero (each call overwrites the partials it reads), but calls that overlap
- * on the GPU race on it and corrupt each other's results.
+ * (tile_id < 0 picks tile and splits).  The array holds the workspace layout
+ * of gemm_f16_splitk: the 1 MiB counter region, then the fp32 partials, so
+ * the partials get 15 MiB (sdt_splitk_workspace_bytes must be at most 16 MiB:
+ * e.g. 1024x1024 with 3 splits, 512x512 with 15).  A given split count whose
+ * workspace exceeds that is rejected with SDT_ERR_ARG and a message naming
+ * the sizes; a split count the call picks itself (tile_id < 0, splits <= 0)
+ * is lowered until it fits, and only a shape that does not fit unsplit is
+ * rejected.  K == 0 writes C = 0 whatever tile and splits say.  The first
+ * call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every GPU on which the library's module holding
+ * the array is loaded keeps the 16 MiB until the process exits.  All calls
+ * share the array: nothing in it has to start at zero (each call overwrites
+ * the partials it reads), but calls that overlap on the GPU race on it and
+ * corrupt each other's results.
  */
 int gemm_f16_splitk_noalloc(int64_t M, int64_t N, int64_t K, const void *A, const void *B, void *C,
                             int tile_id, int splits, sdt_stream_t stream);

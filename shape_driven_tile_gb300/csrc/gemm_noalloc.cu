@@ -15,6 +15,15 @@
 // cached per device.  That first call should therefore come before any stream
 // capture.
 //
+// Size: the workspace layout of gemm_f16_splitk puts a fixed 1 MiB region of
+// arrival counters in front of the fp32 partials, so of the 16 MiB array
+// 15 MiB hold partials: sdt_splitk_workspace_bytes (counters + partials) must
+// be at most 16 MiB.  1024x1024 with 3 splits (12 MiB of partials), 512x512
+// with 15 (15 MiB) and 256x256 with 32 (8 MiB) fit; 1024x1024 with 4 splits
+// and 512x512 with 16 do not.  When the call picks the split count itself it
+// lowers it until the partials fit, and refuses only a shape whose unsplit
+// partials do not fit.
+//
 // Sharing: every call uses the same array and leaves its partials there.  The
 // reduction algorithm used here (a separate summing kernel) overwrites every
 // partial it later reads, so nothing in the array has to start at zero.  Calls
@@ -33,7 +42,8 @@ int splitk_launch(int64_t M, int64_t N, int64_t K, const void *A, const void *B,
 
 using namespace sdt;
 
-// 16 MiB: fp32 partials of e.g. 1024x1024 with 4 splits, 512x512 with 16, 256x256 with 64.
+// 16 MiB: the 1 MiB counter region of the split-K workspace layout plus 15 MiB of fp32
+// partials (e.g. 1024x1024 with 3 splits, 512x512 with 15).
 static constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -71,8 +81,16 @@ extern "C" int gemm_f16_splitk_noalloc(int64_t M, int64_t N, int64_t K, const vo
         return fail(SDT_ERR_SHAPE, "negative dimension (M=%lld N=%lld K=%lld)", (long long)M, (long long)N,
                     (long long)K);
     if (M == 0 || N == 0) return SDT_OK;
+    void *scratch = nullptr;
+    int rc = noalloc_scratch(&scratch);
+    if (rc) return rc;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // K == 0: the empty sum, C = 0, whatever the tile and split arguments (as gemm_f16_splitk)
+    if (K == 0)
+        return splitk_launch(M, N, K, A, B, C, scratch, kNoAllocScratchBytes, tile_id, splits,
+                             SDT_SPLITK_REDUCE_KERNEL, s);
     if (tile_id < 0) {
-        int rc = sdt_device_sm_count();
+        rc = sdt_device_sm_count();
         if (rc < 0) return rc;
         const int sm = rc;
         rc = sdt_device_smem_optin();
@@ -80,22 +98,23 @@ extern "C" int gemm_f16_splitk_noalloc(int64_t M, int64_t N, int64_t K, const vo
         int picked_splits = 1;
         rc = sdt_pick_splitk_for(M, N, K, sm, rc, &tile_id, &picked_splits);
         if (rc) return rc;
-        if (splits <= 0) splits = picked_splits;
+        if (splits <= 0) {
+            // a split count the call chose is lowered until its partials fit the array
+            splits = picked_splits;
+            while (splits > 1 && sdt_splitk_workspace_bytes(M, N, K, tile_id, splits) > kNoAllocScratchBytes)
+                --splits;
+        }
     }
-    if (K > 0) {
-        const size_t need = sdt_splitk_workspace_bytes(M, N, K, tile_id, splits);
-        if (need == 0)
-            return fail(SDT_ERR_ARG, "tile %d with %d splits is not a valid split-K configuration for %lldx%lldx%lld",
-                        tile_id, splits, (long long)M, (long long)N, (long long)K);
-        if (need > kNoAllocScratchBytes)
-            return fail(SDT_ERR_ARG,
-                        "%lldx%lldx%lld with %d splits needs %zu bytes of scratch; the fixed no-allocation scratch "
-                        "holds %zu bytes (use gemm_f16_splitk with a workspace, or fewer splits)",
-                        (long long)M, (long long)N, (long long)K, splits, need, kNoAllocScratchBytes);
-    }
-    void *scratch = nullptr;
-    int rc = noalloc_scratch(&scratch);
-    if (rc) return rc;
+    const size_t need = sdt_splitk_workspace_bytes(M, N, K, tile_id, splits);
+    if (need == 0)
+        return fail(SDT_ERR_ARG, "tile %d with %d splits is not a valid split-K configuration for %lldx%lldx%lld",
+                    tile_id, splits, (long long)M, (long long)N, (long long)K);
+    if (need > kNoAllocScratchBytes)
+        return fail(SDT_ERR_ARG,
+                    "%lldx%lldx%lld with %d splits needs %zu bytes of scratch (1 MiB of counters + fp32 partials); "
+                    "the fixed no-allocation scratch holds %zu bytes (use gemm_f16_splitk with a workspace, or "
+                    "fewer splits)",
+                    (long long)M, (long long)N, (long long)K, splits, need, kNoAllocScratchBytes);
     return splitk_launch(M, N, K, A, B, C, scratch, kNoAllocScratchBytes, tile_id, splits, SDT_SPLITK_REDUCE_KERNEL,
-                         reinterpret_cast<cudaStream_t>(stream));
+                         s);
 }
