@@ -15,6 +15,26 @@ Default run (`python bench.py [--gpus N] [--steps K] [--warmup W]`):
   wall time (CUDA events on the launching stream, barrier + synchronise on
   both sides), in TFLOP/s.  Rank 0 prints one JSON line.
 
+After the timed region rank 0 runs the configurations' own protocols, each
+after at least 1 s of warm-up and under its own clock sampler (--no-legs skips
+them).  Each answers one question with a prediction written before it was run:
+  decode_protocol  does the M=1 decode stream at >= 80 % of HBM?  200 graph-
+                   replayed launches x 10, 8 rotating buffers; predicted bf16
+                   93-98 %, q8 80-88 % of the measured copy bandwidth.
+  gemm_protocol    what fraction of the dense peak per square size?  200
+                   graph-replayed launches x 5 + one eager loop; predicted
+                   4096^3 78-86 %; falsified below 70 % or if graph and eager
+                   differ by > 5 % from 1536^3 up.
+  pick_check       is pick_tile within 5 % of the fastest feasible tile?
+                   every feasible tile cold, 5 shuffled passes x 8 launches;
+                   predicted average <= 1 %, worst <= 5 %.
+  kscan            does K = 2048 (32 k-tiles) camp memory channels on GB300?
+                   M=N=2048, K 1920..2304, 128x128, stagger off/on, cold and
+                   warm; predicted no dip at 2048 beyond 3 % and the stagger
+                   within +-3 %.
+  large            8192^3 / 12288^3 / 16384^3 with pick_tile, graph-replayed;
+                   predicted 80-90 / 78-90 / 72-86 % of the burst peak.
+
 Other modes (--mode): `sweep` times every feasible tile per square size and
 reports pick_tile's slowdown against the best; `kscan` the K-scan with the
 stagger on and off; `decode` the decode protocol (200 launches x 10
@@ -132,7 +152,8 @@ def aggregate_value(units_per_rank_per_step: float, steps: int, world: int, max_
 
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+                "temperature.gpu,utilization.gpu")
 
 
 class ClockSampler:
@@ -169,33 +190,67 @@ class ClockSampler:
         return parse_clock_csv(open(self.path).read() if self.path and os.path.exists(self.path) else "")
 
 
+def _num(v):
+    try:
+        return float(v)
+    except ValueError:
+        return None
+
+
 def parse_clock_csv(text: str):
+    """Summary of nvidia-smi samples (CLOCK_FIELDS, csv, no header, no units).  Samples
+    "under load" are those with GPU utilisation >= 50 % when the column is there, else
+    those with the SM clock above half its maximum."""
     rows = []
     for line in text.splitlines():
         parts = [p.strip() for p in line.split(",")]
         if len(parts) < 9:
             continue
         try:
-            rows.append(dict(sm=float(parts[1]), sm_max=float(parts[2]),
-                             power=float(parts[3]) if parts[3] not in ("[N/A]", "N/A") else None,
+            rows.append(dict(sm=float(parts[1]), sm_max=float(parts[2]), power=_num(parts[3]),
                              active=parts[4], hw=parts[5], hw_thermal=parts[6], sw_thermal=parts[7],
-                             sw_power=parts[8]))
+                             sw_power=parts[8], temp=_num(parts[9]) if len(parts) > 9 else None,
+                             util=_num(parts[10]) if len(parts) > 10 else None))
         except ValueError:
             continue
     if not rows:
         return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-    # samples "under load": the SM clock above half of its maximum
-    load = [r for r in rows if r["sm"] > 0.5 * r["sm_max"]] or rows
+    if any(r["util"] is not None for r in rows):
+        load = [r for r in rows if r["util"] is not None and r["util"] >= 50]
+    else:
+        load = [r for r in rows if r["sm"] > 0.5 * r["sm_max"]]
+    sel = load or rows
     reasons = set()
     for r in rows:
         for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
                           ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
             if r[key].lower() == "active":
                 reasons.add(name)
-    pw = [r["power"] for r in load if r["power"] is not None]
-    return {"sm_mhz": statistics.median(r["sm"] for r in load), "sm_max_mhz": max(r["sm_max"] for r in rows),
-            "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(load),
-            "power_w_max": max(pw) if pw else None}
+    pw = [r["power"] for r in sel if r["power"] is not None]
+    tp = [r["temp"] for r in rows if r["temp"] is not None]
+    out = {"sm_mhz": statistics.median(r["sm"] for r in sel), "sm_max_mhz": max(r["sm_max"] for r in rows),
+           "sm_mhz_min_under_load": min(r["sm"] for r in sel), "reasons": sorted(reasons), "samples": len(rows),
+           "samples_under_load": len(load), "power_w_max": max(pw) if pw else None,
+           "power_w_median_under_load": statistics.median(pw) if pw else None}
+    if tp:
+        out["temp_c_max"] = max(tp)
+    return out
+
+
+def gpu_state(gpu_index: int):
+    """One query of the GPU's temperature, power, clocks and utilisation (read only)."""
+    fields = "temperature.gpu,power.draw,clocks.sm,clocks.mem,pstate,utilization.gpu"
+    try:
+        r = subprocess.run(["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={fields}",
+                            "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=20)
+    except (OSError, subprocess.SubprocessError):
+        return None
+    parts = [p.strip() for p in r.stdout.strip().split(",")]
+    if r.returncode != 0 or len(parts) < 6:
+        return None
+    return {"temp_c": _num(parts[0]), "power_w": _num(parts[1]), "sm_mhz": _num(parts[2]),
+            "mem_mhz": _num(parts[3]), "pstate": parts[4], "util_pct": _num(parts[5]),
+            "t": round(time.time(), 1)}
 
 
 # ---------------------------------------------------------------------------------------------
@@ -324,6 +379,7 @@ def run_default(args):
     dev = torch.device("cuda", local)
     world, rank = dist_init("nccl")
     peaks = load_peaks()
+    state_before = gpu_state(local)
 
     host, x_h, Wb_h, Q_h = make_host_inputs(rank)
     A = {n: host[n][0].to(dev) for n in SWEEP}
@@ -424,9 +480,14 @@ def run_default(args):
         torch.cuda.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
+        # clock warm-up right before the timed region (the oracle leg above left the GPU
+        # idle): whole steps back to back for at least --clock-warmup-s seconds
+        warm_graph = graphs.get(0)
+        clock_warm_s = warm_for(args.clock_warmup_s, (lambda: warm_graph.replay()) if warm_graph is not None
+                                else (lambda: step(0)))
+        barrier()
+        torch.cuda.synchronize()
         start.record(stream)
         for kind, first, count in plan:
             if kind == "instrumented":
@@ -456,7 +517,17 @@ def run_default(args):
     e2e = run_e2e(args, dev, host, Wb_h, Q_h, stream)
 
     # the decode protocol (after the timed region): 200 back-to-back launches x 10 repeats
-    dec_proto = decode_protocol(x, Wb, Wq, Sq, yb, peaks, stream) if rank == 0 else None
+    dec_proto = None
+    if rank == 0:
+        with ClockSampler(local) as dclk:
+            dec_proto = decode_protocol(x, Wb, Wq, Sq, yb, peaks, stream)
+        dec_proto["clocks"] = dclk.summary()
+
+    # the configurations' own protocols (after the timed region, rank 0)
+    legs = run_legs(L, A, B, C, tiles, peaks, stream, dev, local) if rank == 0 and not args.no_legs else {}
+    if rank == 0:
+        sdt.check_device_status()
+    state_after = gpu_state(local)
 
     if rank != 0:
         return
@@ -495,12 +566,15 @@ def run_default(args):
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "l2": "inputs larger than L2 (step working set %.0f MB, L2 129 MB)"
                    % (step_working_set() / 1e6), "parallelism": f"replicas x{world}"},
-        "timing": {"per_size_and_decode": f"instrumented steps (every {INSTR}th, events around every launch; "
-                   "a decode launch there follows the GEMMs, so it cannot overlap a previous decode)",
+        "timing": {"per_size_and_decode": f"instrumented steps (every {INSTR}th, queued behind a graph replay, "
+                   "events around every launch; a decode launch there follows the GEMMs, so it cannot overlap a "
+                   "previous decode)",
                    "roofline": f"events around the 4096^3 launch in the instrumented steps ({len(inst_idx)} of "
                                f"{args.steps}); the other steps carry no events",
-                   "launch": "eager" if args.no_graph else "instrumented steps eager, the nine steps between "
-                             "two of them replayed as one CUDA graph"},
+                   "launch": "eager" if args.no_graph else "instrumented steps eager, the nine steps before "
+                             "each of them replayed as one CUDA graph",
+                   "clock_warmup": f"{clock_warm_s:.2f} s of whole steps right before the timed region",
+                   "clocks": "nvidia-smi every 50 ms over the clock warm-up and the timed region"},
         "roofline": {"bound": "tensor", "kernel": f"gemm_f16 {dom}^3 ({tiles[dom]})",
                      "largest_share_in_step": f"gemm_f16 {largest_share}^3",
                      "achieved": round(achieved, 1), "peak": peaks["tflops"], "unit": "TFLOP/s",
@@ -520,24 +594,28 @@ def run_default(args):
         "decode": dec,
         "decode_protocol": dict(dec_proto, protocol="1 s warm, 200 graph-replayed launches x 10 repeats, "
                                 "8 rotating buffers, after the timed region"),
+        **legs,
         "gate": gate,
-        "receipt": receipt(dev, warmup_s),
+        "receipt": receipt(dev, warmup_s, clock_warm_s, state_before, state_after),
     }
     print(json.dumps(out), flush=True)
 
 
 def step_schedule(steps, instr, buffers, graphed=True):
     """How the timed steps run: a list of (kind, first step, count) in step order.
-    Every `instr`-th step (0, instr, 2 instr, ...) is "instrumented" (events around each
-    launch); the instr-1 steps between two of them are one "graph" replay when they
-    all exist (a graph captured once per first-step decode buffer, first % buffers);
-    anything else is an "eager" step.  Each step index appears exactly once."""
+    Every `instr`-th step (instr-1, 2 instr-1, ...; the last step when there are fewer
+    than instr) is "instrumented" (events around each launch); the instr-1 steps before
+    each of them are one "graph" replay (a graph captured once per first-step decode
+    buffer, first % buffers), so an instrumented step is queued behind a replay and its
+    first launch does not wait for the host; anything else is an "eager" step.  Each
+    step index appears exactly once."""
+    inst = {i for i in range(steps) if i % instr == instr - 1} or ({steps - 1} if steps else set())
     plan, i = [], 0
     while i < steps:
-        if i % instr == 0:
+        if i in inst:
             plan.append(("instrumented", i, 1))
             i += 1
-        elif graphed and (i - 1) % instr == 0 and i + instr - 1 <= steps:
+        elif graphed and i % instr == 0 and i + instr - 1 in inst:
             plan.append(("graph", i, instr - 1))
             i += instr - 1
         else:
@@ -546,8 +624,9 @@ def step_schedule(steps, instr, buffers, graphed=True):
     return plan
 
 
-def receipt(dev, warmup_s):
-    """What the numbers were measured on: device, driver, runtime, library sources."""
+def receipt(dev, warmup_s, clock_warmup_s=None, before=None, after=None):
+    """What the numbers were measured on: device, driver, runtime, library sources, the
+    warm-up, and the GPU's temperature, power and clocks before and after the run."""
     import torch
 
     import shape_driven_tile_gb300 as sdt
@@ -563,7 +642,9 @@ def receipt(dev, warmup_s):
     return {"gpu": props.name, "sm_count": sdt.device_sm_count(), "driver": driver,
             "cuda_runtime": torch.version.cuda, "torch": torch.__version__,
             "kernel_sources": {k: kernel_source_digest(k) for k in SOURCES},
-            "warmup_s": round(warmup_s, 3), "host_cores": len(os.sched_getaffinity(0))}
+            "warmup_s": round(warmup_s, 3),
+            "clock_warmup_s": None if clock_warmup_s is None else round(clock_warmup_s, 3),
+            "gpu_before": before, "gpu_after": after, "host_cores": len(os.sched_getaffinity(0))}
 
 
 def step_working_set():
@@ -1023,6 +1104,261 @@ def decode_protocol(x, Wb, Wq, Sq, y, peaks, stream, warm_s=1.0, reps=10, launch
     return res
 
 
+# ---------------------------------------------------------------------------------------------
+# protocol legs: each configuration measured by the pages' own protocol, after the timed region
+# ---------------------------------------------------------------------------------------------
+
+
+def _chk(rc):
+    if rc:
+        import shape_driven_tile_gb300 as sdt
+
+        raise sdt.SdtError(rc, (sdt.lib().sdt_last_error() or b"").decode())
+
+
+def warm_for(seconds, fn):
+    """Runs fn() back to back until `seconds` of wall time have passed, synchronising
+    after every batch of eight (so the time is GPU time, not queued launches); returns
+    the wall time spent."""
+    import torch
+
+    t0 = time.perf_counter()
+    while True:
+        for _ in range(8):
+            fn()
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        if dt >= seconds:
+            return dt
+
+
+def graph_of(launch, count, dev):
+    """A CUDA graph of `count` calls launch(i, stream_handle), captured on a side stream."""
+    import torch
+
+    cap = torch.cuda.Stream(device=dev)
+    cap.wait_stream(torch.cuda.current_stream(dev))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        for i in range(count):
+            launch(i, cap.cuda_stream)
+    torch.cuda.current_stream(dev).wait_stream(cap)
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(g, count, reps, stream):
+    """Per-launch microseconds of each of `reps` replays of a graph of `count` launches
+    (CUDA events on `stream`, the stream the replay runs on)."""
+    import torch
+
+    out = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out.append(e0.elapsed_time(e1) * 1e3 / count)
+    return out
+
+
+def gemm_protocol_leg(L, A, B, C, tiles, peaks, stream, dev, launches=200, reps=5, warm_s=1.0):
+    """The square sweep by the pages' GEMM protocol ("Beating hipBLASLt on a Gaming GPU",
+    "Why these numbers should be trusted"; "mojo-baro", "Square fp16 GEMM vs hipBLASLt"):
+    a clock warm-up, then per size `launches` back-to-back launches of gemm_f16 replayed
+    from a CUDA graph, `reps` repeats in a shuffled size order, min-max per launch; plus
+    one host-issued loop of the same launches between two events (the plain-launch arm
+    of the FlyDSL pull request's "Performance")."""
+    import torch
+
+    def call(n, sp):
+        _chk(L.gemm_f16(n, n, n, A[n].data_ptr(), B[n].data_ptr(), C[n].data_ptr(), sp))
+
+    warm = warm_for(warm_s, lambda: [call(n, stream.cuda_stream) for n in SWEEP])
+    graphs = {n: graph_of(lambda i, sp, n=n: call(n, sp), launches, dev) for n in SWEEP}
+    times = {n: [] for n in SWEEP}
+    rng = random.Random(7)
+    for _ in range(reps):
+        order = list(SWEEP)
+        rng.shuffle(order)
+        for n in order:
+            times[n] += time_graph(graphs[n], launches, 1, stream)
+    eager = {}
+    for n in SWEEP:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(launches):
+            call(n, stream.cuda_stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        eager[n] = e0.elapsed_time(e1) * 1e3 / launches
+    del graphs
+    rows = []
+    for n in SWEEP:
+        best = min(times[n])
+        tf = gemm_flops(n, n, n) / (best / 1e6) / 1e12
+        rows.append({"size": n, "tile": tiles[n], "us_min": round(best, 2), "us_max": round(max(times[n]), 2),
+                     "tflops_best": round(tf, 1), "pct_peak_best": round(100 * tf / peaks["tflops"], 1),
+                     "eager_us": round(eager[n], 2)})
+    return {"rows": rows, "warmup_s": round(warm, 2),
+            "protocol": f"{warm_s:g} s warm-up; per size {launches} back-to-back launches replayed from a CUDA graph "
+                        f"(every size's operands fit in the 129 MB L2, as in a hot loop), {reps} repeats in shuffled size order, min-max per "
+                        f"launch; eager_us: {launches} host-issued launches between two events"}
+
+
+def large_leg(L, peaks, stream, dev, sizes=None, reps=3, warm_s=1.0):
+    """Large squares M=N=K in {8192, 12288, 16384} with pick_tile: a clock warm-up on the
+    first size, then per size a CUDA graph of back-to-back launches (about 20 ms) replayed
+    `reps` times; operands far larger than L2.  TFLOP/s against the measured burst and
+    sustained (power-capped) bf16 peaks."""
+    import torch
+
+    import shape_driven_tile_gb300 as sdt
+
+    rows, warm = [], 0.0
+    for idx, n in enumerate(sizes or LARGE):
+        g = torch.Generator(device=dev).manual_seed(50 + n)
+        A = torch.empty((n, n), dtype=torch.float16, device=dev).uniform_(-1, 1, generator=g)
+        B = torch.empty((n, n), dtype=torch.float16, device=dev).uniform_(-1, 1, generator=g)
+        C = torch.empty((n, n), dtype=torch.float16, device=dev)
+        fl = gemm_flops(n, n, n)
+        count = max(3, min(20, round(20e-3 / (fl / 1.5e15))))
+
+        def call(sp, n=n, A=A, B=B, C=C):
+            _chk(L.gemm_f16(n, n, n, A.data_ptr(), B.data_ptr(), C.data_ptr(), sp))
+
+        if idx == 0:
+            warm = warm_for(warm_s, lambda: call(stream.cuda_stream))
+        else:
+            for _ in range(2):
+                call(stream.cuda_stream)
+        gr = graph_of(lambda i, sp: call(sp), count, dev)
+        us = time_graph(gr, count, reps, stream)
+        best = min(us)
+        tf = fl / (best / 1e6) / 1e12
+        rows.append({"size": n, "tile": sdt.tile_info(sdt.pick_tile(n, n, n))["name"], "us_min": round(best, 1),
+                     "us_max": round(max(us), 1), "tflops_best": round(tf, 1),
+                     "pct_peak_best": round(100 * tf / peaks["tflops"], 1),
+                     "pct_sustained_peak_best": round(100 * tf / peaks["tflops_sustained"], 1),
+                     "launches_per_replay": count})
+        del gr, A, B, C
+        torch.cuda.empty_cache()
+    return {"rows": rows, "warmup_s": round(warm, 2),
+            "protocol": f"{warm_s:g} s warm-up, per size a graph of back-to-back launches (~20 ms) x {reps} "
+                        "repeats, min-max per launch; operands much larger than L2"}
+
+
+def kscan_leg(L, peaks, stream, dev, tile="128x128", passes=4, launches=8, graph_launches=50, warm_s=1.0):
+    """The K-scan of the FlyDSL pull request ("Motivation"; third commit message): M=N=2048,
+    K in {1920, 1984, 2048, 2112, 2176, 2304}, one fixed tile, the k-loop stagger off and
+    on.  Cold: each launch after an L2 flush, `passes` shuffled passes of `launches`
+    launches per setting, best pass mean.  Warm: `graph_launches` back-to-back launches
+    replayed from a CUDA graph, best of three."""
+    import torch
+
+    import shape_driven_tile_gb300 as sdt
+
+    tid = sdt.tile_id(tile)
+    M = N = 2048
+    g = torch.Generator(device=dev).manual_seed(31)
+    bufs = {}
+    for K in KSCAN:
+        bufs[K] = (torch.empty((M, K), dtype=torch.float16, device=dev).uniform_(-1, 1, generator=g),
+                   torch.empty((K, N), dtype=torch.float16, device=dev).uniform_(-1, 1, generator=g),
+                   torch.empty((M, N), dtype=torch.float16, device=dev))
+
+    def call(K, st, sp):
+        A, B, C = bufs[K]
+        _chk(L.gemm_f16_with_tile(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(), sp, tid, st))
+
+    warm = warm_for(warm_s, lambda: [call(K, 1, stream.cuda_stream) for K in KSCAN])
+    flush = L2Flush(dev)
+    configs = [(K, st) for K in KSCAN for st in (0, 1)]
+    cold = {}
+    rng = random.Random(11)
+    for _ in range(passes):
+        rng.shuffle(configs)
+        for K, st in configs:
+            mean = time_cold(lambda: call(K, st, stream.cuda_stream), launches, flush, stream)[0]
+            cold[(K, st)] = min(cold.get((K, st), mean), mean)
+    warm_t = {}
+    for K, st in configs:
+        gr = graph_of(lambda i, sp, K=K, st=st: call(K, st, sp), graph_launches, dev)
+        warm_t[(K, st)] = min(time_graph(gr, graph_launches, 3, stream)) / 1e3
+        del gr
+    rows = []
+    for K in KSCAN:
+        fl = gemm_flops(M, N, K)
+        nK = K // 64
+        rows.append({"K": K, "k_tiles": nK, "stagger_applies": nK & (nK - 1) == 0,
+                     "cold_tflops": {"off": round(fl / (cold[(K, 0)] / 1e3) / 1e12, 1),
+                                     "on": round(fl / (cold[(K, 1)] / 1e3) / 1e12, 1)},
+                     "warm_tflops": {"off": round(fl / (warm_t[(K, 0)] / 1e3) / 1e12, 1),
+                                     "on": round(fl / (warm_t[(K, 1)] / 1e3) / 1e12, 1)}})
+    del bufs, flush
+    torch.cuda.empty_cache()
+    return {"tile": tile, "rows": rows, "warmup_s": round(warm, 2),
+            "protocol": f"{warm_s:g} s warm-up; cold: L2 flushed (512 MB read) before each launch, {passes} shuffled "
+                        f"passes x {launches} launches per (K, stagger), best pass mean; warm: {graph_launches} "
+                        "graph-replayed launches, best of 3"}
+
+
+def pick_check_leg(L, A, B, C, tiles, peaks, stream, dev, passes=5, launches=8, warm_s=1.0):
+    """pick_tile against every feasible tile on each square size (the FlyDSL pull
+    request's check of pick_tile against the per-shape fastest, "Changes" and its first
+    commit message): every feasible tile timed cold (L2 flushed before each launch) in
+    `passes` passes of `launches` launches, each pass in a fresh shuffled tile order, a
+    tile's time its best pass mean; the pick's slowdown against the fastest."""
+    import shape_driven_tile_gb300 as sdt
+
+    warm = warm_for(warm_s, lambda: [_chk(L.gemm_f16(n, n, n, A[n].data_ptr(), B[n].data_ptr(), C[n].data_ptr(),
+                                                     stream.cuda_stream)) for n in SWEEP])
+    flush = L2Flush(dev)
+    rows = []
+    for n in SWEEP:
+        feas = sdt.feasible_tiles(n, n, n)
+        res = {}
+        rng = random.Random(1000 + n)
+        order = list(feas)
+        for _ in range(passes):
+            rng.shuffle(order)
+            for t in order:
+                fn = lambda t=t: _chk(L.gemm_f16_with_tile(n, n, n, A[n].data_ptr(), B[n].data_ptr(),
+                                                           C[n].data_ptr(), stream.cuda_stream, t, -1))
+                mean = time_cold(fn, launches, flush, stream)[0]
+                res[t] = min(res.get(t, mean), mean)
+        pick = sdt.pick_tile(n, n, n)
+        best = min(res, key=res.get)
+        name = lambda t: sdt.tile_info(t)["name"]
+        rows.append({"size": n, "pick": name(pick), "best": name(best),
+                     "slowdown": round(res[pick] / res[best] - 1, 4),
+                     "us": {name(t): round(v * 1e3, 2) for t, v in sorted(res.items(), key=lambda kv: kv[1])}})
+    del flush
+    slow = [r["slowdown"] for r in rows]
+    return {"rows": rows, "avg_slowdown": round(statistics.mean(slow), 4), "worst_slowdown": round(max(slow), 4),
+            "worst_size": rows[slow.index(max(slow))]["size"], "warmup_s": round(warm, 2),
+            "protocol": f"{warm_s:g} s warm-up; every feasible tile, L2 flushed (512 MB read) before each launch, "
+                        f"{passes} passes x {launches} launches in a fresh shuffled tile order per pass, "
+                        "best pass mean per tile"}
+
+
+def run_legs(L, A, B, C, tiles, peaks, stream, dev, gpu_index):
+    """The four protocol legs, each under its own nvidia-smi clock sampler."""
+    out = {}
+    for key, fn in (("gemm_protocol", lambda: gemm_protocol_leg(L, A, B, C, tiles, peaks, stream, dev)),
+                    ("pick_check", lambda: pick_check_leg(L, A, B, C, tiles, peaks, stream, dev)),
+                    ("kscan", lambda: kscan_leg(L, peaks, stream, dev)),
+                    ("large", lambda: large_leg(L, peaks, stream, dev))):
+        t0 = time.perf_counter()
+        with ClockSampler(gpu_index) as clk:
+            res = fn()
+        res["clocks"] = clk.summary()
+        res["wall_s"] = round(time.perf_counter() - t0, 2)
+        out[key] = res
+    return out
+
+
 def run_decode(args):
     """The decode protocol: 8 rotating buffers, warm-up, 200 timed launches, repeated 10 times."""
     import torch
@@ -1309,6 +1645,11 @@ def main(argv=None):
     ap.add_argument("--shapes", nargs="*", help="extra GEMM shapes MxNxK for --mode sweep; shape names for --mode p4")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--clock-warmup-s", type=float, default=1.0,
+                    help="default run: seconds of whole steps right before the timed region")
+    ap.add_argument("--no-legs", action="store_true",
+                    help="default run: skip the protocol legs after the timed region (gemm_protocol, pick_check, "
+                         "kscan, large)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -44,6 +44,19 @@ def test_parse_clock_csv():
     assert bench.parse_clock_csv("")["samples"] == 0
 
 
+def test_parse_clock_csv_with_utilisation_and_temperature():
+    # with the utilisation column, "under load" is utilisation >= 50 %, whatever the clock
+    text = ("0, 2070, 2070, 185.0, 0x0, Not Active, Not Active, Not Active, Not Active, 41, 0\n"
+            "0, 2070, 2070, 950.0, 0x0, Not Active, Not Active, Not Active, Not Active, 52, 100\n"
+            "0, 1920, 2070, 1398.0, 0x4, Not Active, Not Active, Not Active, Active, 58, 99\n"
+            "0, 2070, 2070, [N/A], 0x0, Not Active, Not Active, Not Active, Not Active, [N/A], 75\n")
+    s = bench.parse_clock_csv(text)
+    assert s["samples"] == 4 and s["samples_under_load"] == 3
+    assert s["sm_mhz"] == 2070 and s["sm_mhz_min_under_load"] == 1920
+    assert s["power_w_max"] == 1398.0 and s["power_w_median_under_load"] == (950.0 + 1398.0) / 2
+    assert s["temp_c_max"] == 58 and s["reasons"] == ["sw_power_cap"]
+
+
 def test_oracle_sample_plan_bounds():
     plan = bench.oracle_sample_plan(60e9)
     assert [n for n, _ in plan] == bench.SWEEP
@@ -151,10 +164,16 @@ def test_step_schedule_covers_every_step_once(steps, graphed):
     plan = bench.step_schedule(steps, 10, 8, graphed=graphed)
     seen = [i for kind, first, count in plan for i in range(first, first + count)]
     assert seen == list(range(steps))
-    assert [first for kind, first, _ in plan if kind == "instrumented"] == list(range(0, steps, 10))
+    inst = [first for kind, first, _ in plan if kind == "instrumented"]
+    assert inst == (list(range(9, steps, 10)) or [steps - 1])
     for kind, first, count in plan:
         if kind == "graph":
-            assert graphed and count == 9 and first % 10 == 1
+            # nine steps replayed right before an instrumented one
+            assert graphed and count == 9 and first % 10 == 0 and first + 9 in inst
+    if graphed and steps >= 10:
+        # every instrumented step is queued behind a graph replay
+        kinds = [k for k, _, _ in plan]
+        assert all(kinds[j - 1] == "graph" for j, k in enumerate(kinds) if k == "instrumented")
     if not graphed:
         assert all(kind != "graph" for kind, _, _ in plan)
     # graphs are keyed by their first step's decode buffer: at most four distinct keys
