@@ -813,32 +813,386 @@ __global__ void zero_fill_f32(float *y, int64_t n) {
         y[i] = 0.f;
 }
 
+// ---------------------------------------------------------------------------------
+// Ring kernels (SDT_GEMV_VARIANT=ring).  One CTA per SM owns a
+// balanced contiguous range of rows, which is one contiguous byte range of W (and
+// of the q8 scales).  A producer thread streams that range through a ring of S
+// shared-memory stages of RS rows with bulk copies (cp.async.bulk, completion on
+// an mbarrier), so within the first microsecond of a launch every SM has S stages
+// of its rows requested from HBM -- independently of the arithmetic and of any
+// round trip -- and each stage is requested again as soon as it is consumed (the
+// register kernels above keep at most two batches per thread in flight and refill
+// them after a CTA-wide barrier per batch).  Measured on GB300 at K = 4096,
+// N = 12288 it is the slower design: 17 us (q8) and 24 us (bf16) per launch back to
+// back, against 8.3 and 15.2 us for the row-range kernels, and the same for rings of
+// 60 to 200 KB -- one SM's bulk copies from HBM stay near 25 KB/us, below the
+// ~45 KB/us that an SM's share of the HBM bandwidth needs, while plain loads from
+// all of an SM's warps reach it.  It stays selectable for that comparison.
+//
+// Consumer thread t (of T) owns the 32-byte column slices t, t + T, ... of every row
+// and keeps their activations in registers, as the row-range kernels do (q8: group-
+// scaled int16 pairs for dp2a, bf16: packed fp32 pairs).  Per stage a warp sums its
+// lanes' partials per row with the transposed butterfly and leaves one value per
+// (row, warp) in shared memory, then every consumer lane arrives on the stage's
+// "empty" barrier.  The producer, once that barrier completes, requests the next
+// rows into the stage and then adds the stage's per-warp values in warp order (a
+// fixed order: results are deterministic) and writes y.  The per-warp values are
+// double-buffered by the stage's use count, so a refill cannot race the sum.
+// ---------------------------------------------------------------------------------
+
+struct RingArgs {
+    const uint4 *x;          // bf16 activations [K]
+    const uint8_t *W;        // [N][row_bytes]
+    const uint8_t *scales;   // q8: fp16 [N][K/32]
+    float *y;
+    int K, N;
+    int row_bytes;           // q8: K, bf16: 2K (a multiple of 32)
+    int scale_row_bytes;     // q8: K/16 (a multiple of 16), bf16: 0
+    int stages;
+    uint32_t pf_bytes;       // W bytes of the CTA's range asked of L2 before the dependency wait
+    int evict_first;         // weight copies marked evict-first in L2
+    unsigned long long timeout_ns;
+    int *status;
+};
+
+// cp.async.bulk global -> shared with an L2 eviction-priority policy (from createpolicy).
+__device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                               uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(pol)
+        : "memory");
+}
+
+template <bool Q8, int NCW, int GT, int RS>
+__global__ void __launch_bounds__((NCW + 1) * 32, 1) gemv_ring_kernel(const RingArgs a) {
+    constexpr int T = NCW * 32;  // consumer threads
+    static_assert(RS == 1 || RS == 2 || RS == 4 || RS == 8, "rows per stage: a power of two up to 8");
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw + 127u) & ~127u) - raw);
+    const int S = a.stages;
+    const int w_bytes = RS * a.row_bytes;
+    const int stage_bytes = w_bytes + RS * a.scale_row_bytes;  // a multiple of 16
+    float *part = reinterpret_cast<float *>(smem + S * stage_bytes);  // [2][S][NCW][RS] per-warp row sums
+    uint64_t *full = reinterpret_cast<uint64_t *>(part + 2 * S * NCW * RS);
+    uint64_t *empty = full + S;
+    volatile uint32_t *ctrl = reinterpret_cast<volatile uint32_t *>(empty + S);  // [0] gave up, [1] stages issued
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int r_begin = int(int64_t(a.N) * blockIdx.x / gridDim.x);
+    const int r_end = int(int64_t(a.N) * (blockIdx.x + 1) / gridDim.x);
+    const int n_st = (r_end - r_begin + RS - 1) / RS;
+    const uint64_t lim = a.timeout_ns;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(smem_u32(&full[i]), 1);
+            mbar_init(smem_u32(&empty[i]), T);
+        }
+        ctrl[0] = 0;
+        ctrl[1] = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    griddep_launch_dependents();
+    if (warp == NCW && lane == 0 && a.pf_bytes && r_end > r_begin) {
+        // Ask L2 for the first pf_bytes of this CTA's rows while the previous kernel in the
+        // stream may still run (L2 is the point of coherence: a line fetched now and written
+        // by that kernel later is updated in place, and the copies after the wait see it).
+        const size_t slice = size_t(r_end - r_begin) * a.row_bytes;
+        const size_t wb = slice < a.pf_bytes ? slice : size_t(a.pf_bytes);  // multiples of 16
+        const uint8_t *wp = a.W + size_t(r_begin) * a.row_bytes;
+        for (size_t o = 0; o < wb; o += 32768) bulk_prefetch_l2(wp + o, uint32_t(wb - o < 32768 ? wb - o : 32768));
+        if (Q8) {
+            const size_t rows = wb / a.row_bytes + 1 < size_t(r_end - r_begin) ? wb / a.row_bytes + 1 : size_t(r_end - r_begin);
+            bulk_prefetch_l2(a.scales + size_t(r_begin) * a.scale_row_bytes, uint32_t(rows * a.scale_row_bytes));
+        }
+    }
+    griddep_wait();  // x and W may come from the previous kernel
+
+    if (warp == NCW) {
+        if (lane == 0) {
+            // ---------------- producer: bulk copies into the ring, row sums out ----------------
+            uint64_t pol = 0;
+            if (a.evict_first) asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+            const uint32_t full0 = smem_u32(&full[0]), empty0 = smem_u32(&empty[0]);
+            const uint32_t ring0 = smem_u32(smem);
+            // y rows of stage st (in slot s): the warps' values added in warp order
+            auto finish = [&](int st, int s) {
+                const int r0 = r_begin + st * RS;
+                const int n = min(RS, r_end - r0);
+                const float *pp = part + ((st / S) & 1) * S * NCW * RS + s * NCW * RS;
+                for (int r = 0; r < n; ++r) {
+                    float t = 0.f;
+#pragma unroll
+                    for (int w = 0; w < NCW; ++w) t += pp[w * RS + r];
+                    a.y[r0 + r] = t;
+                }
+            };
+            bool stop = false;
+            for (int st = 0; st < n_st; ++st) {
+                const int s = st % S;
+                if (st >= S) {
+                    // slot s last held stage st - S: every consumer lane must be done with it
+                    if (!mbar_wait_for(empty0 + 8u * s, uint32_t((st / S - 1) & 1), lim)) {
+                        if (a.status) atomicCAS(a.status, 0, static_cast<int>(kSiteProducer));
+                        ctrl[0] = 1;
+                        stop = true;
+                        break;
+                    }
+                    if (ctrl[0]) { stop = true; break; }
+                }
+                const int r0 = r_begin + st * RS;
+                const int n = min(RS, r_end - r0);
+                const uint32_t fb = full0 + 8u * s;
+                const uint32_t dst = ring0 + uint32_t(s * stage_bytes);
+                mbar_arrive_expect_tx(fb, uint32_t(n * (a.row_bytes + a.scale_row_bytes)));
+                const uint8_t *src = a.W + size_t(r0) * a.row_bytes;
+                if (a.evict_first) bulk_load_hint(dst, src, uint32_t(n * a.row_bytes), fb, pol);
+                else bulk_load(dst, src, uint32_t(n * a.row_bytes), fb);
+                if (Q8)
+                    bulk_load(dst + uint32_t(w_bytes), a.scales + size_t(r0) * a.scale_row_bytes,
+                              uint32_t(n * a.scale_row_bytes), fb);
+                ctrl[1] = uint32_t(st + 1);
+                if (st >= S) finish(st - S, s);
+            }
+            // the stages still in the ring
+            for (int st = max(0, n_st - S); st < n_st && !stop; ++st) {
+                const int s = st % S;
+                if (!mbar_wait_for(empty0 + 8u * s, uint32_t((st / S) & 1), lim)) {
+                    if (a.status) atomicCAS(a.status, 0, static_cast<int>(kSiteProducer));
+                    ctrl[0] = 1;
+                    break;
+                }
+                finish(st, s);
+            }
+        }
+    } else {
+        // ---------------- consumers ----------------
+        const int G = Q8 ? (a.K >> 5) : (a.K >> 4);  // 32-byte slices per row
+        int g[GT];
+#pragma unroll
+        for (int i = 0; i < GT; ++i) g[i] = threadIdx.x + i * T;
+        // activations of this thread's slices
+        uint32_t xw[GT][Q8 ? 16 : 8];
+#pragma unroll
+        for (int i = 0; i < GT; ++i)
+#pragma unroll
+            for (int j = 0; j < (Q8 ? 4 : 2); ++j) {
+                const uint4 v = g[i] < G ? ld_nc_v4(a.x + size_t(g[i]) * (Q8 ? 4 : 2) + j) : make_uint4(0, 0, 0, 0);
+                xw[i][4 * j] = v.x;
+                xw[i][4 * j + 1] = v.y;
+                xw[i][4 * j + 2] = v.z;
+                xw[i][4 * j + 3] = v.w;
+            }
+        // q8: group-scaled int16 pairs and the factor undoing the scaling (as gemv_q8_dp2a_kernel);
+        // bf16: packed fp32 pairs
+        uint32_t xi[GT][Q8 ? 16 : 1];
+        float xf[GT];
+        uint64_t xp[GT][Q8 ? 1 : 8];
+#pragma unroll
+        for (int i = 0; i < GT; ++i) {
+            if constexpr (Q8) {
+                uint32_t e2 = 0;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) e2 = __vmaxu2(e2, xw[i][j] & 0x7F807F80u);
+                const uint32_t e_raw = max(e2 & 0xFFFFu, e2 >> 16) >> 7;
+                const uint32_t e = max(e_raw, 16u);
+                const float up = __uint_as_float((268u - e) << 23);
+                xf[i] = e_raw == 255u ? __uint_as_float(0x7FC00000u) : __uint_as_float((e - 14u) << 23);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int lo = __float2int_rn(__uint_as_float(xw[i][j] << 16) * up);
+                    const int hi = __float2int_rn(__uint_as_float(xw[i][j] & 0xFFFF0000u) * up);
+                    xi[i][j] = (uint32_t(lo) & 0xFFFFu) | (uint32_t(hi) << 16);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) xp[i][j] = bf16x2_to_f32x2(xw[i][j]);
+            }
+        }
+        const uint32_t full0 = smem_u32(&full[0]), empty0 = smem_u32(&empty[0]);
+        constexpr int kLanesPerRow = 32 / RS;
+        for (int st = 0; st < n_st; ++st) {
+            const int s = st % S;
+            if (!warp_wait(full0 + 8u * s, uint32_t((st / S) & 1), lim, lane)) {
+                if (lane == 0) {
+                    if (a.status) atomicCAS(a.status, 0, static_cast<int>(kSiteEpilogue));
+                    ctrl[0] = 1;
+                }
+                break;
+            }
+            const uint8_t *stage = smem + s * stage_bytes;
+            float p[RS];
+#pragma unroll
+            for (int r = 0; r < RS; ++r) {
+                const uint8_t *row = stage + r * a.row_bytes;
+                if constexpr (Q8) {
+                    const __half *sc = reinterpret_cast<const __half *>(stage + w_bytes + r * a.scale_row_bytes);
+                    float acc = 0.f;
+#pragma unroll
+                    for (int i = 0; i < GT; ++i) {
+                        if (g[i] < G) {
+                            const uint4 w0 = *reinterpret_cast<const uint4 *>(row + g[i] * 32);
+                            const uint4 w1 = *reinterpret_cast<const uint4 *>(row + g[i] * 32 + 16);
+                            const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                            int d = 0;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                d = dp2a_lo(xi[i][2 * j], w[j], d);
+                                d = dp2a_hi(xi[i][2 * j + 1], w[j], d);
+                            }
+                            acc = fmaf(float(d), __half2float(sc[g[i]]) * xf[i], acc);
+                        }
+                    }
+                    p[r] = acc;
+                } else {
+                    uint64_t acc = 0;
+#pragma unroll
+                    for (int i = 0; i < GT; ++i) {
+                        if (g[i] < G) {
+                            const uint4 w0 = *reinterpret_cast<const uint4 *>(row + g[i] * 32);
+                            const uint4 w1 = *reinterpret_cast<const uint4 *>(row + g[i] * 32 + 16);
+                            acc = fma2(bf16x2_to_f32x2(w0.x), xp[i][0], acc);
+                            acc = fma2(bf16x2_to_f32x2(w0.y), xp[i][1], acc);
+                            acc = fma2(bf16x2_to_f32x2(w0.z), xp[i][2], acc);
+                            acc = fma2(bf16x2_to_f32x2(w0.w), xp[i][3], acc);
+                            acc = fma2(bf16x2_to_f32x2(w1.x), xp[i][4], acc);
+                            acc = fma2(bf16x2_to_f32x2(w1.y), xp[i][5], acc);
+                            acc = fma2(bf16x2_to_f32x2(w1.z), xp[i][6], acc);
+                            acc = fma2(bf16x2_to_f32x2(w1.w), xp[i][7], acc);
+                        }
+                    }
+                    p[r] = sum2(acc);
+                }
+            }
+            const float v = reduce_rows<RS>(p, lane);
+            if (lane % kLanesPerRow == 0)
+                part[((st / S) & 1) * S * NCW * RS + s * NCW * RS + warp * RS + lane / kLanesPerRow] = v;
+            mbar_arrive(empty0 + 8u * s);  // this lane is done with the stage (and its row sums are written)
+        }
+    }
+
+    __syncthreads();
+    if (threadIdx.x == NCW * 32 && ctrl[0]) {
+        // drain: wait (bounded) for bulk copies this CTA issued and may not have seen land
+        const int issued = static_cast<int>(ctrl[1]);
+        for (int i = max(0, issued - S); i < issued; ++i)
+            if (!mbar_wait_for(smem_u32(&full[i % S]), static_cast<uint32_t>((i / S) & 1), lim)) {
+                if (a.status) atomicCAS(a.status, 0, static_cast<int>(kSiteDrain));
+                break;
+            }
+    }
+}
+
 struct GemvVariant {
     int rows, unroll;  // register-path kernel: rows per warp, chunks in flight per row
     int stream_h;      // > 0: streaming kernel with this many consumer warps per row
     int rr_rows;       // > 0: the row-range kernel (q8: integer dot products) with this many rows per batch
+    int ring;          // 1: the ring kernel first
 };
 
 // Variant selection.  Default: the row-range kernels with 2 rows per batch (q8 on
-// integer dot products, bf16 on packed fp32 FMA) where their conditions hold,
-// else the register kernel with 2 rows per warp and 4 chunks in flight per row
-// (fastest measured on GB300 at K=4096, N=12288).  SDT_GEMV_VARIANT overrides: "dp2" (row-range kernel, 2 rows per
-// batch, either format), "dp4" / "dp8" (q8 integer kernel, rows per batch),
-// "stream1" / "stream2" (streaming kernel, warps per row), "stream" (its default
-// split), or "R,U" for the register kernel.
+// integer dot products, bf16 on packed fp32 FMA) where their conditions hold, else
+// the register kernel with 2 rows per warp and 4 chunks in flight per row.
+// SDT_GEMV_VARIANT overrides: "ring" (the ring kernels first), "dp2" (row-range
+// kernel, 2 rows per batch, either format), "dp4" / "dp8" (q8 integer kernel, rows
+// per batch), "stream1" / "stream2" (streaming kernel, warps per row), "stream" (its
+// default split), or "R,U" for the register kernel.
 static GemvVariant gemv_variant(bool q8) {
-    GemvVariant v{2, 4, 0, 2};
+    GemvVariant v{2, 4, 0, 2, 0};
     if (const char *s = getenv("SDT_GEMV_VARIANT")) {
         int r = 0, u = 0;
-        if (!strcmp(s, "dp2")) v.rr_rows = 2;
-        else if (!strcmp(s, "dp4")) v.rr_rows = q8 ? 4 : 0;
-        else if (!strcmp(s, "dp8")) v.rr_rows = q8 ? 8 : 0;
-        else if (!strcmp(s, "stream1")) v = GemvVariant{2, 4, 1, 0};
-        else if (!strcmp(s, "stream2")) v = GemvVariant{2, 4, 2, 0};
-        else if (!strcmp(s, "stream")) v = GemvVariant{2, 4, q8 ? 1 : 2, 0};
-        else if (sscanf(s, "%d,%d", &r, &u) == 2) v = GemvVariant{r, u, 0, 0};
+        if (!strcmp(s, "ring")) v.ring = 1;
+        else if (!strcmp(s, "dp2")) v.ring = 0;
+        else if (!strcmp(s, "dp4")) v = GemvVariant{2, 4, 0, q8 ? 4 : 0, 0};
+        else if (!strcmp(s, "dp8")) v = GemvVariant{2, 4, 0, q8 ? 8 : 0, 0};
+        else if (!strcmp(s, "stream1")) v = GemvVariant{2, 4, 1, 0, 0};
+        else if (!strcmp(s, "stream2")) v = GemvVariant{2, 4, 2, 0, 0};
+        else if (!strcmp(s, "stream")) v = GemvVariant{2, 4, q8 ? 1 : 2, 0, 0};
+        else if (sscanf(s, "%d,%d", &r, &u) == 2) v = GemvVariant{r, u, 0, 0, 0};
     }
     return v;
+}
+
+// Shared memory the ring kernels give their ring (SDT_GEMV_RING_KB overrides), and
+// the bytes of its rows each CTA asks L2 for before waiting on the previous kernel
+// (SDT_GEMV_RING_PF_KB; 0 = none).
+static int64_t gemv_ring_budget(int64_t default_kb) {
+    int64_t kb = default_kb;
+    if (const char *s = getenv("SDT_GEMV_RING_KB")) kb = std::max<long>(16, std::min<long>(strtol(s, nullptr, 10), 1024));
+    return kb * 1024;
+}
+static uint32_t gemv_ring_prefetch(uint32_t default_kb) {
+    long kb = default_kb;
+    if (const char *s = getenv("SDT_GEMV_RING_PF_KB")) kb = std::max<long>(0, std::min<long>(strtol(s, nullptr, 10), 1 << 20));
+    return uint32_t(kb) * 1024u;
+}
+
+template <bool Q8, int NCW, int GT, int RS>
+static cudaError_t launch_ring(const RingArgs &a, int grid, int smem, cudaStream_t s, int device) {
+    auto kern = gemv_ring_kernel<Q8, NCW, GT, RS>;
+    static std::atomic<int> configured[64];
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    if (configured[device].load() < smem) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured[device].store(smem);
+    }
+    return launch_kernel(kern, dim3(grid), dim3((NCW + 1) * 32), size_t(smem), s, 1, a);
+}
+
+// The ring kernels take q8 with K % 256 == 0 (scale rows of whole 16-byte units),
+// bf16 with K % 16 == 0 (whole 32-byte slices), up to 4 slices per consumer thread
+// (K <= 16384), W and the scales 16-byte aligned (bulk copies), and a ring of at
+// least two stages; returns false to ask for another kernel.  One CTA per SM:
+// 4 consumer warps (q8, 4 rows per stage) or 8 (bf16, 2 rows per stage) and the
+// producer warp.
+static bool try_ring(bool q8, int64_t K, int64_t N, const void *x, const void *W, const void *scales, float *y,
+                     cudaStream_t s, const DeviceInfo &dev, int *status, cudaError_t *err) {
+    if (q8 ? (K % 256) : (K % 16)) return false;
+    if ((reinterpret_cast<uintptr_t>(W) & 15) || (q8 && (reinterpret_cast<uintptr_t>(scales) & 15))) return false;
+    const int ncw = q8 ? 4 : 8, rs = q8 ? 4 : 2;
+    const int64_t T = int64_t(ncw) * 32;
+    const int64_t slices = q8 ? K / 32 : K / 16;
+    const int gt = slices <= T ? 1 : slices <= 2 * T ? 2 : slices <= 4 * T ? 4 : 0;
+    if (gt == 0) return false;
+    const int64_t row_bytes = q8 ? K : 2 * K;
+    const int64_t scale_row_bytes = q8 ? K / 16 : 0;
+    const int64_t stage_bytes = rs * (row_bytes + scale_row_bytes);
+    const int64_t per_stage = stage_bytes + 8 * ncw * rs + 16;  // + the double-buffered row sums and two barriers
+    const int64_t fixed = 128 + 8;
+    const int64_t budget = std::min<int64_t>(gemv_ring_budget(200), dev.smem_optin);
+    const int64_t stages = std::min<int64_t>((budget - fixed) / per_stage, 64);
+    if (stages < 2) return false;
+    RingArgs a;
+    a.x = static_cast<const uint4 *>(x);
+    a.W = static_cast<const uint8_t *>(W);
+    a.scales = static_cast<const uint8_t *>(scales);
+    a.y = y;
+    a.K = int(K);
+    a.N = int(N);
+    a.row_bytes = int(row_bytes);
+    a.scale_row_bytes = int(scale_row_bytes);
+    a.stages = int(stages);
+    a.pf_bytes = gemv_ring_prefetch(q8 ? 16 : 32);
+    const char *ef_env = getenv("SDT_GEMV_EVICT_FIRST");
+    a.evict_first = (ef_env && (!strcmp(ef_env, "0") || !strcmp(ef_env, "off"))) ? 0 : 1;
+    a.timeout_ns = wait_timeout_ns();
+    a.status = status;
+    const int grid = int(std::min<int64_t>(dev.sm_count, N));
+    const int smem = int(fixed + stages * per_stage);
+    if (q8)
+        *err = gt == 1 ? launch_ring<true, 4, 1, 4>(a, grid, smem, s, dev.device)
+             : gt == 2 ? launch_ring<true, 4, 2, 4>(a, grid, smem, s, dev.device)
+                       : launch_ring<true, 4, 4, 4>(a, grid, smem, s, dev.device);
+    else
+        *err = gt == 1 ? launch_ring<false, 8, 1, 2>(a, grid, smem, s, dev.device)
+             : gt == 2 ? launch_ring<false, 8, 2, 2>(a, grid, smem, s, dev.device)
+                       : launch_ring<false, 8, 4, 2>(a, grid, smem, s, dev.device);
+    return true;
 }
 
 // Bytes of its weight rows each decode CTA asks L2 for before waiting on the
@@ -1080,7 +1434,8 @@ static int gemv_impl(int64_t K, int64_t N, const void *x, const void *W, const v
         int *status = nullptr;
         rc = status_word(&status);
         if (rc) return rc;
-        if (!(q8 && try_q8_dp(v.rr_rows, K, N, x, W, scales, y, s, dev, &e)) &&
+        if (!(v.ring && try_ring(q8, K, N, x, W, scales, y, s, dev, status, &e)) &&
+            !(q8 && try_q8_dp(v.rr_rows, K, N, x, W, scales, y, s, dev, &e)) &&
             !(!q8 && try_bf16_rows(v.rr_rows, K, N, x, W, y, s, dev, &e)) &&
             !try_stream(q8, v.stream_h, K, N, x, W, scales, y, s, dev, status, &e)) {
             if (!q8) SDT_GEMV_DISPATCH(e, launch_bf16, v, int(K / 8), int(N), x, W, y, s);

@@ -13,7 +13,7 @@ from _parity import assert_close, q8_rounding_bound, u16
 pytestmark = pytest.mark.gpu
 
 K_DEC, N_DEC = 4096, 12288
-VARIANTS = ["stream", "stream1", "stream2", "1,4", "2,4", "4,4", "dp2", "dp4", "dp8"]
+VARIANTS = ["ring", "stream", "stream1", "stream2", "1,4", "2,4", "4,4", "dp2", "dp4", "dp8"]
 
 
 @pytest.fixture
@@ -161,6 +161,60 @@ def test_q8_nonfinite_activation_gives_nan(cuda_device):
     q, s = inputs.q8_weights(N, K, seed=102)
     y = sdt.gemv_m1(x.to(cuda_device), q.to(cuda_device), s.to(cuda_device)).cpu().numpy()
     assert not np.isfinite(y).any()
+
+
+@pytest.mark.parametrize("variant", ["ring"], indirect=True)
+@pytest.mark.parametrize("K,N", [(256, 1), (256, 5), (512, 151), (4096, 12291), (8192, 153), (16384, 300),
+                                 (4352, 1000)])
+def test_ragged_q8_ring_kernel(cuda_device, variant, K, N):
+    # one row; fewer rows than SMs; one and two rows per CTA; a partial last stage; two and
+    # four 32-byte slices per consumer thread (K 8192, 16384); K a multiple of 256 only
+    x = inputs.uniform((K,), seed=121, dtype=torch.bfloat16)
+    q, s = inputs.q8_weights(N, K, seed=122)
+    y = sdt.gemv_m1(x.to(cuda_device), q.to(cuda_device), s.to(cuda_device)).cpu().numpy()
+    sdt.check_device_status()
+    assert_close(y, oracle.gemv_q8(u16(x), q.numpy(), u16(s)), K, f"q8 ring K={K} N={N}")
+
+
+@pytest.mark.parametrize("variant", ["ring"], indirect=True)
+@pytest.mark.parametrize("K,N", [(16, 3), (48, 1), (4096, 12291), (8192, 153), (16384, 77), (4112, 1000),
+                                 (6144, 152)])
+def test_ragged_bf16_ring_kernel(cuda_device, variant, K, N):
+    x, W = bf16_case(K, N, 131)
+    y = sdt.gemv_m1(x.to(cuda_device), W.to(cuda_device)).cpu().numpy()
+    sdt.check_device_status()
+    assert_close(y, oracle.gemv_bf16(u16(x), u16(W)), K, f"bf16 ring K={K} N={N}")
+
+
+@pytest.mark.parametrize("variant", ["ring"], indirect=True)
+def test_ring_integer_exact_and_repeatable(cuda_device, variant):
+    # exact in fp32 whatever the order (integer activations, power-of-two scales), and
+    # bit-identical from launch to launch (fixed summation order)
+    x = inputs.integers((K_DEC,), seed=141, dtype=torch.bfloat16)
+    q, s = inputs.q8_weights_exact(N_DEC, K_DEC, seed=142)
+    xd, qd, sd = x.to(cuda_device), q.to(cuda_device), s.to(cuda_device)
+    y1 = sdt.gemv_m1(xd, qd, sd)
+    y2 = sdt.gemv_m1(xd, qd, sd)
+    assert torch.equal(y1, y2)
+    assert np.array_equal(y1.cpu().double().numpy(), oracle.gemv_q8(u16(x), q.numpy(), u16(s)))
+    W = inputs.integers((N_DEC, K_DEC), seed=143, dtype=torch.bfloat16)
+    yb = sdt.gemv_m1(xd, W.to(cuda_device)).cpu().double().numpy()
+    assert np.array_equal(yb, oracle.gemv_bf16(u16(x), u16(W)))
+
+
+@pytest.mark.parametrize("variant", ["ring"], indirect=True)
+@pytest.mark.parametrize("ring_kb", ["36", "60", "100"])
+def test_ring_depths(cuda_device, variant, ring_kb, monkeypatch):
+    # rings of two stages up to the default depth (wraparound of the stage phases)
+    monkeypatch.setenv("SDT_GEMV_RING_KB", ring_kb)
+    x = inputs.uniform((K_DEC,), seed=151, dtype=torch.bfloat16)
+    q, s = inputs.q8_weights(2048, K_DEC, seed=152)
+    y = sdt.gemv_m1(x.to(cuda_device), q.to(cuda_device), s.to(cuda_device)).cpu().numpy()
+    assert_close(y, oracle.gemv_q8(u16(x), q.numpy(), u16(s)), K_DEC, f"q8 ring {ring_kb} KB")
+    W = inputs.uniform((2048, K_DEC), seed=153, dtype=torch.bfloat16)
+    y = sdt.gemv_m1(x.to(cuda_device), W.to(cuda_device)).cpu().numpy()
+    assert_close(y, oracle.gemv_bf16(u16(x), u16(W)), K_DEC, f"bf16 ring {ring_kb} KB")
+    sdt.check_device_status()
 
 
 @pytest.mark.parametrize("variant", ["dp2"], indirect=True)
