@@ -32,6 +32,9 @@
 namespace sdt {
 
 using LaunchFn = int (*)(const CUtensorMap &, const CUtensorMap &, const GemmArgs &, cudaStream_t);
+// The ladder's launchers also take the C map (TMA stores of the persistent and two-CTA kernels).
+using TileLaunchFn = int (*)(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const GemmArgs &,
+                             cudaStream_t);
 
 // Split-K launchers of the one-CTA-per-tile ladder rungs, in ladder order, per operand
 // layout (null: no split-K form).
@@ -61,7 +64,7 @@ static const LaunchFn kStreamLaunch[][4] = {
 struct LadderTile {
     int BM, BN, cta_group, stages;
     const char *name;
-    LaunchFn launch[4];  // per operand layout (bit 0: A transposed, bit 1: B transposed)
+    TileLaunchFn launch[4];  // per operand layout (bit 0: A transposed, bit 1: B transposed)
     int smem_per_stage;
     int smem_fixed;
     int tmem_cols;
@@ -99,7 +102,8 @@ struct LadderTile {
 #define SDT_PTILE(BN_, STAGES_, NAME_, FIX_, KT_, RND_, BW_, CAND_)                                     \
     LadderTile {                                                                                   \
         128, BN_, 1, STAGES_, NAME_, SDT_LAUNCH4_(launch_gemm_persistent, BN_),                    \
-            PersistentCfg<BN_>::STAGE_BYTES, PersistentCfg<BN_>::ALIGN_SLACK + PersistentCfg<BN_>::CTRL_BYTES, \
+            PersistentCfg<BN_>::STAGE_BYTES,                                                         \
+            PersistentCfg<BN_>::ALIGN_SLACK + PersistentCfg<BN_>::C_STAGE_BYTES + PersistentCfg<BN_>::CTRL_BYTES, \
             PersistentCfg<BN_>::TMEM_COLS, PersistentCfg<BN_>::THREADS, true, FIX_, KT_, RND_, BW_, 0.0, CAND_ \
     }
 
@@ -113,7 +117,8 @@ struct LadderTile {
 #define SDT_PAIR(BN_, STAGES_, NAME_, FIX_, KT_, RND_, BW_, CAND_)                                      \
     LadderTile {                                                                                   \
         256, BN_, 2, STAGES_, NAME_, SDT_LAUNCH4_(launch_gemm_pair, BN_), PairCfg<BN_>::STAGE_BYTES, \
-            PairCfg<BN_>::ALIGN_SLACK + PairCfg<BN_>::CTRL_BYTES, PairCfg<BN_>::TMEM_COLS,         \
+            PairCfg<BN_>::ALIGN_SLACK + PairCfg<BN_>::C_STAGE_BYTES + PairCfg<BN_>::CTRL_BYTES,    \
+            PairCfg<BN_>::TMEM_COLS,                                                               \
             PairCfg<BN_>::THREADS, true, FIX_, KT_, RND_, BW_, 0.0, CAND_                                  \
     }
 
@@ -395,29 +400,32 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 struct MapKey {
     uintptr_t ptr;
     uint64_t inner, outer, row_stride_bytes;
-    int dtype, box_outer;
+    int dtype, box_outer, box_inner, swizzle;
     bool operator<(const MapKey &o) const {
-        return std::tie(ptr, inner, outer, row_stride_bytes, dtype, box_outer) <
-               std::tie(o.ptr, o.inner, o.outer, o.row_stride_bytes, o.dtype, o.box_outer);
+        return std::tie(ptr, inner, outer, row_stride_bytes, dtype, box_outer, box_inner, swizzle) <
+               std::tie(o.ptr, o.inner, o.outer, o.row_stride_bytes, o.dtype, o.box_outer, o.box_inner, o.swizzle);
     }
 };
 
 static MapKey map_key(const void *ptr, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes, int dtype,
-                      int box_outer) {
-    return MapKey{reinterpret_cast<uintptr_t>(ptr), inner, outer, row_stride_bytes, dtype, box_outer};
+                      int box_outer, int box_inner, int swizzle) {
+    return MapKey{reinterpret_cast<uintptr_t>(ptr), inner, outer, row_stride_bytes, dtype, box_outer, box_inner,
+                  swizzle};
 }
 
 static std::mutex g_map_mu;
 static std::map<MapKey, CUtensorMap> g_maps;
 static uint64_t g_map_encodes = 0;
 
-// 2-D 16-bit tensor map (fp16 or bf16) with a box of 64 contiguous elements by
-// `box_outer` rows and 128-byte swizzle; `inner` is the contiguous dimension.
-// Elements outside [0, inner) x [0, outer) read as zero, which is what lets tiles
-// overhang ragged edges.
+// 2-D 16-bit tensor map (fp16 or bf16) with a box of `box_inner` contiguous elements
+// by `box_outer` rows; `inner` is the contiguous dimension.  Operand maps use 64 x
+// rows boxes with the 128-byte swizzle: elements outside [0, inner) x [0, outer) read
+// as zero, which is what lets tiles overhang ragged edges.  The C map of the TMA
+// stores uses 32 x 32 boxes with the 64-byte swizzle: elements outside are not written.
 static int tensor_map_2d(const void *ptr, int dtype, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
-                         int box_outer, CUtensorMap *out) {
-    const MapKey key = map_key(ptr, inner, outer, row_stride_bytes, dtype, box_outer);
+                         int box_outer, CUtensorMap *out, int box_inner = 64,
+                         CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+    const MapKey key = map_key(ptr, inner, outer, row_stride_bytes, dtype, box_outer, box_inner, int(swizzle));
     {
         std::lock_guard<std::mutex> lock(g_map_mu);
         auto it = g_maps.find(key);
@@ -431,12 +439,12 @@ static int tensor_map_2d(const void *ptr, int dtype, uint64_t inner, uint64_t ou
     CUtensorMap m;
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {row_stride_bytes};
-    cuuint32_t box[2] = {64, cuuint32_t(box_outer)};
+    cuuint32_t box[2] = {cuuint32_t(box_inner), cuuint32_t(box_outer)};
     cuuint32_t estr[2] = {1, 1};
     const CUtensorMapDataType dt =
         dtype == SDT_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUresult r = fn(&m, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(SDT_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", int(r));
     std::lock_guard<std::mutex> lock(g_map_mu);
     if (g_maps.size() >= 4096) g_maps.clear();
@@ -642,7 +650,14 @@ static int run_tile_ex(int tile_id, int stagger_req, int64_t M0, int64_t N0, int
             a.num_items = a.tail_start + 2 * tail;
         }
     }
-    int e = t.launch[layout & 3](tmA, tmB, a, stream);
+    // the persistent and two-CTA kernels write C with TMA stores (32 x 32 boxes)
+    CUtensorMap tmC = tmA;  // unused by the one-CTA kernel
+    if (t.persistent) {
+        rc = tensor_map_2d(C, dtype, uint64_t(N), uint64_t(M), uint64_t(ldc) * 2, 32, &tmC, 32,
+                           CU_TENSOR_MAP_SWIZZLE_64B);
+        if (rc) return rc;
+    }
+    int e = t.launch[layout & 3](tmA, tmB, tmC, a, stream);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return fail(SDT_ERR_LAUNCH, "launch of tile %s failed: %s", t.name, cudaGetErrorString(cudaError_t(e)));

@@ -140,6 +140,50 @@ __device__ __forceinline__ void store_row32(void *crow, const uint32_t (&r)[32],
         if (8 * v + 8 <= ncols) dst[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
 }
 
+// C through shared memory and TMA stores (persistent and two-CTA kernels).  Each
+// epilogue warp owns two staging buffers of 32 rows x 32 columns of 16-bit C (2 KB),
+// used alternately; a buffer holds the box of a C tensor map with a 32 x 32 box and
+// the 64-byte swizzle: row r's 16-byte chunk c sits at chunk c ^ ((r >> 1) & 3) of
+// its 64-byte row, so the warp's 16-byte writes of one chunk index reach 32 distinct
+// banks in every 8-lane phase.  The TMA writes whole 64-byte row pieces of C and
+// drops rows and columns outside C, so ragged edges need no masks.
+constexpr int kCStageBytes = 32 * 32 * 2;
+
+// Lane = row: its 32 fp32 accumulator columns -> fp16/bf16 -> staging buffer (nst & 1)
+// -> one TMA store of the warp's 32 x 32 box at (x, y).  Lane 0 issues the store and
+// first waits until the store that last used the buffer has read it.
+__device__ __forceinline__ void store_chunk_tma(const CUtensorMap *tmC, uint32_t buf0, int nst,
+                                                const uint32_t (&r)[32], bool bf16, int x, int y, int lane) {
+    uint32_t h[16];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+        const float lo = __uint_as_float(r[2 * t]), hi = __uint_as_float(r[2 * t + 1]);
+        if (bf16) {
+            __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+            h[t] = *reinterpret_cast<uint32_t *>(&v);
+        } else {
+            __half2 v = __floats2half2_rn(lo, hi);
+            h[t] = *reinterpret_cast<uint32_t *>(&v);
+        }
+    }
+    const uint32_t buf = buf0 + static_cast<uint32_t>(nst & 1) * kCStageBytes;
+    if (lane == 0) bulk_wait_group_read<1>();
+    __syncwarp();
+    const uint32_t row = buf + static_cast<uint32_t>(lane) * 64u;
+    const uint32_t sw = static_cast<uint32_t>((lane >> 1) & 3);
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((static_cast<uint32_t>(c) ^ sw) << 4)),
+                     "r"(h[4 * c]), "r"(h[4 * c + 1]), "r"(h[4 * c + 2]), "r"(h[4 * c + 3])
+                     : "memory");
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_2d(tmC, buf, x, y);
+        bulk_commit_group();
+    }
+}
+
 // One fp32 value -> fp16 or bf16 bits (round to nearest even).
 __device__ __forceinline__ uint16_t f32_to_16(float v, bool bf16) {
     return bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(v)) : __half_as_ushort(__float2half_rn(v));
@@ -471,9 +515,11 @@ __global__ void splitk_reduce_trans_kernel(const float *__restrict__ partials, u
                                            int64_t M, int64_t N, int64_t Mp, int64_t Np, int64_t ldc, int splits,
                                            int bf16);
 
-// Host-side launchers, instantiated per ladder tile and layout (gemm_t*.cu).
+// Host-side launchers, instantiated per ladder tile and layout (gemm_t*.cu).  The
+// ladder's launchers take the C map of the persistent and two-CTA kernels' TMA
+// stores; the one-CTA kernel stores C directly and ignores it.
 template <int BM, int BN, int LAYOUT>
-int launch_gemm_tile(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args,
+int launch_gemm_tile(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC, const GemmArgs &args,
                      cudaStream_t stream);
 template <int BM, int BN, int LAYOUT>
 int launch_gemm_tile_split(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args,

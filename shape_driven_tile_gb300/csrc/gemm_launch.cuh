@@ -31,7 +31,7 @@ int ensure_smem(Kern kern, int smem, std::atomic<int> *configured) {
 }
 
 template <int BM, int BN, int LAYOUT>
-int launch_gemm_tile(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args,
+int launch_gemm_tile(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &, const GemmArgs &args,
                      cudaStream_t stream) {
     using Cfg = TileCfg<BM, BN>;
     auto kern = gemm_f16_tile_kernel<BM, BN, false, LAYOUT>;
@@ -70,8 +70,8 @@ int launch_gemm_streamk(const CUtensorMap &tmA, const CUtensorMap &tmB, const Ge
 }
 
 template <int BN, int LAYOUT>
-int launch_gemm_persistent(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args,
-                           cudaStream_t stream) {
+int launch_gemm_persistent(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
+                           const GemmArgs &args, cudaStream_t stream) {
     using Cfg = PersistentCfg<BN>;
     auto kern = gemm_f16_persistent_kernel<BN, LAYOUT>;
     const int smem = Cfg::smem_bytes(args.stages);
@@ -79,11 +79,12 @@ int launch_gemm_persistent(const CUtensorMap &tmA, const CUtensorMap &tmB, const
     if (int e = ensure_smem(kern, smem, configured)) return e;
     const long long tiles = static_cast<long long>(args.num_m_tiles) * args.num_n_tiles;
     const unsigned grid = static_cast<unsigned>(tiles < args.max_ctas ? tiles : args.max_ctas);
-    return launch_kernel(kern, dim3(grid), dim3(Cfg::THREADS), size_t(smem), stream, 1, tmA, tmB, args);
+    return launch_kernel(kern, dim3(grid), dim3(Cfg::THREADS), size_t(smem), stream, 1, tmA, tmB, tmC, args);
 }
 
 template <int BN, int LAYOUT>
-int launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args, cudaStream_t stream) {
+int launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC, const GemmArgs &args,
+                     cudaStream_t stream) {
     using Cfg = PairCfg<BN>;
     auto kern = gemm_f16_pair_kernel<BN, LAYOUT>;
     const int smem = Cfg::smem_bytes(args.stages);
@@ -92,7 +93,7 @@ int launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmA
     const long long items = args.num_items;
     const long long pairs_cap = args.max_ctas / 2 > 0 ? args.max_ctas / 2 : 1;
     const unsigned pairs = static_cast<unsigned>(items < pairs_cap ? items : pairs_cap);
-    return launch_kernel(kern, dim3(2 * pairs), dim3(Cfg::THREADS), size_t(smem), stream, 2, tmA, tmB, args);
+    return launch_kernel(kern, dim3(2 * pairs), dim3(Cfg::THREADS), size_t(smem), stream, 2, tmA, tmB, tmC, args);
 }
 
 }  // namespace sdt
@@ -101,18 +102,18 @@ int launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmA
 #define SDT_LAYOUTS_(X, ...) X(__VA_ARGS__, 0) X(__VA_ARGS__, 1) X(__VA_ARGS__, 2) X(__VA_ARGS__, 3)
 
 #define SDT_PAIR_ONE_(BN, L)                                                                         \
-    template int sdt::launch_gemm_pair<BN, L>(const CUtensorMap &, const CUtensorMap &, const sdt::GemmArgs &, \
-                                              cudaStream_t);
+    template int sdt::launch_gemm_pair<BN, L>(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,   \
+                                              const sdt::GemmArgs &, cudaStream_t);
 #define SDT_INSTANTIATE_GEMM_PAIR(BN) SDT_LAYOUTS_(SDT_PAIR_ONE_, BN)
 
 #define SDT_PERSISTENT_ONE_(BN, L)                                                                   \
     template int sdt::launch_gemm_persistent<BN, L>(const CUtensorMap &, const CUtensorMap &,        \
-                                                    const sdt::GemmArgs &, cudaStream_t);
+                                                    const CUtensorMap &, const sdt::GemmArgs &, cudaStream_t);
 #define SDT_INSTANTIATE_GEMM_PERSISTENT(BN) SDT_LAYOUTS_(SDT_PERSISTENT_ONE_, BN)
 
 #define SDT_TILE_ONE_(BM, BN, L)                                                                     \
     template int sdt::launch_gemm_tile<BM, BN, L>(const CUtensorMap &, const CUtensorMap &,          \
-                                                  const sdt::GemmArgs &, cudaStream_t);
+                                                  const CUtensorMap &, const sdt::GemmArgs &, cudaStream_t);
 #define SDT_TILE_SPLIT_ONE_(BM, BN, L)                                                               \
     template int sdt::launch_gemm_tile_split<BM, BN, L>(const CUtensorMap &, const CUtensorMap &,    \
                                                         const sdt::GemmArgs &, cudaStream_t);

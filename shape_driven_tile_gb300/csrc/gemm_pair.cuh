@@ -51,8 +51,9 @@ struct PairCfg {
     static constexpr int EPI_WARPS = 4;
     static constexpr int ALIGN_SLACK = 1024;
     static constexpr int CTRL_BYTES = 512;
+    static constexpr int C_STAGE_BYTES = EPI_WARPS * 2 * kCStageBytes;  // C staging, two buffers per epilogue warp
     __host__ __device__ static constexpr int smem_bytes(int stages) {
-        return ALIGN_SLACK + stages * STAGE_BYTES + CTRL_BYTES;
+        return ALIGN_SLACK + stages * STAGE_BYTES + C_STAGE_BYTES + CTRL_BYTES;
     }
     static_assert(BN == 128 || BN == 224 || BN == 256, "pair tiles use BN 128, 224 or 256");
     static_assert(ACC_BUFS * BN <= TMEM_COLS && TMEM_COLS <= 512, "two accumulators must fit in TMEM");
@@ -80,7 +81,7 @@ __device__ __forceinline__ void pair_item(int item, const GemmArgs &p, int &tile
 template <int BN, int LAYOUT>
 __global__ void __launch_bounds__(192, 1)
     gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                         const GemmArgs p) {
+                         const __grid_constant__ CUtensorMap tmC, const GemmArgs p) {
     using Cfg = PairCfg<BN>;
     using L = OperandLayout<LAYOUT>;
     extern __shared__ uint8_t smem_raw[];
@@ -90,7 +91,8 @@ __global__ void __launch_bounds__(192, 1)
     const int S = p.stages;
     uint8_t *smA = smem;
     uint8_t *smB = smem + S * Cfg::A_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smB + S * Cfg::B_BYTES);
+    uint8_t *smC = smB + S * Cfg::B_BYTES;  // C staging (1024-byte aligned)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smC + Cfg::C_STAGE_BYTES);
     uint64_t *full = bars;
     uint64_t *empty = bars + S;
     uint64_t *acc_full = bars + 2 * S;
@@ -242,6 +244,8 @@ __global__ void __launch_bounds__(192, 1)
     } else {
         // ---------------- epilogue warps (both CTAs) ----------------
         const int q = warp & 3;
+        const uint32_t cbuf = smem_u32(smC) + static_cast<uint32_t>(q) * 2u * kCStageBytes;
+        int nst = 0;  // TMA stores this warp has issued (staging buffer parity)
         int j = 0;
         for (int item = pair; item < num_items; item += num_pairs, ++j) {
             const int b = j & 1;
@@ -256,11 +260,9 @@ __global__ void __launch_bounds__(192, 1)
             tc_fence_after();
             int tile, m_tile, n_tile, n_off, width;
             pair_item<BN>(item, p, tile, m_tile, n_tile, n_off, width);
-            const int row = m_tile * Cfg::BM + static_cast<int>(rank) * Cfg::CTA_M + q * 32 + lane;
+            const int row0 = m_tile * Cfg::BM + static_cast<int>(rank) * Cfg::CTA_M + q * 32;  // this warp's rows
             const int n0 = n_tile * BN + n_off;
-            const bool row_valid = row < p.M;
             const bool bf16 = ((p.idesc_flags >> 7) & 7u) == 1u;
-            uint16_t *crow = reinterpret_cast<uint16_t *>(p.C) + static_cast<size_t>(row) * p.ldc + n0;
             const uint32_t taddr =
                 tmem_base + static_cast<uint32_t>(b * BN) + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll 1
@@ -273,9 +275,11 @@ __global__ void __launch_bounds__(192, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[b]), 0));
                 }
-                if (row_valid) store_row32(crow + c, r, p.N - (n0 + c), bf16);
+                store_chunk_tma(&tmC, cbuf, nst++, r, bf16, n0 + c, row0, lane);
             }
         }
+        if (lane == 0) bulk_wait_group<0>();  // this warp's stores have landed (and read the staging)
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -297,6 +301,7 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 template <int BN, int LAYOUT>
-int launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args, cudaStream_t stream);
+int launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC, const GemmArgs &args,
+                     cudaStream_t stream);
 
 }  // namespace sdt

@@ -43,8 +43,9 @@ struct PersistentCfg {
     static constexpr int EPI_WARPS = 4;
     static constexpr int ALIGN_SLACK = 1024;
     static constexpr int CTRL_BYTES = 512;
+    static constexpr int C_STAGE_BYTES = EPI_WARPS * 2 * kCStageBytes;  // C staging, two buffers per epilogue warp
     __host__ __device__ static constexpr int smem_bytes(int stages) {
-        return ALIGN_SLACK + stages * STAGE_BYTES + CTRL_BYTES;
+        return ALIGN_SLACK + stages * STAGE_BYTES + C_STAGE_BYTES + CTRL_BYTES;
     }
     static_assert(BN == 128 || BN == 256, "persistent tiles use BN 128 or 256");
     static_assert(TMEM_COLS <= 512, "two accumulators must fit in TMEM");
@@ -65,7 +66,8 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int 
 template <int BN, int LAYOUT>
 __global__ void __launch_bounds__(192, 1)
     gemm_f16_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
-                               const __grid_constant__ CUtensorMap tmB, const GemmArgs p) {
+                               const __grid_constant__ CUtensorMap tmB,
+                               const __grid_constant__ CUtensorMap tmC, const GemmArgs p) {
     using Cfg = PersistentCfg<BN>;
     using L = OperandLayout<LAYOUT>;
     extern __shared__ uint8_t smem_raw[];
@@ -75,7 +77,8 @@ __global__ void __launch_bounds__(192, 1)
     const int S = p.stages;
     uint8_t *smA = smem;
     uint8_t *smB = smem + S * Cfg::A_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smB + S * Cfg::B_BYTES);
+    uint8_t *smC = smB + S * Cfg::B_BYTES;  // C staging (1024-byte aligned)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smC + Cfg::C_STAGE_BYTES);
     uint64_t *full = bars;
     uint64_t *empty = bars + S;
     uint64_t *acc_full = bars + 2 * S;       // [2]
@@ -209,6 +212,8 @@ __global__ void __launch_bounds__(192, 1)
     } else {
         // ---------------- epilogue warps ----------------
         const int q = warp & 3;
+        const uint32_t cbuf = smem_u32(smC) + static_cast<uint32_t>(q) * 2u * kCStageBytes;
+        int nst = 0;  // TMA stores this warp has issued (staging buffer parity)
         int j = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++j) {
             const int b = j & 1;
@@ -223,11 +228,9 @@ __global__ void __launch_bounds__(192, 1)
             tc_fence_after();
             int m_tile, n_tile;
             tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.raster_group, m_tile, n_tile);
-            const int row = m_tile * Cfg::BM + q * 32 + lane;
+            const int row0 = m_tile * Cfg::BM + q * 32;  // this warp's rows
             const int n0 = n_tile * BN;
-            const bool row_valid = row < p.M;
             const bool bf16 = ((p.idesc_flags >> 7) & 7u) == 1u;
-            uint16_t *crow = reinterpret_cast<uint16_t *>(p.C) + static_cast<size_t>(row) * p.ldc + n0;
             const uint32_t taddr = tmem_base + static_cast<uint32_t>(b * BN) + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll 1
             for (int c = 0; c < BN; c += 32) {
@@ -240,9 +243,11 @@ __global__ void __launch_bounds__(192, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&acc_empty[b]));
                 }
-                if (row_valid) store_row32(crow + c, r, p.N - (n0 + c), bf16);
+                store_chunk_tma(&tmC, cbuf, nst++, r, bf16, n0 + c, row0, lane);
             }
         }
+        if (lane == 0) bulk_wait_group<0>();  // this warp's stores have landed (and read the staging)
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -264,7 +269,7 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 template <int BN, int LAYOUT>
-int launch_gemm_persistent(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &args,
-                           cudaStream_t stream);
+int launch_gemm_persistent(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
+                           const GemmArgs &args, cudaStream_t stream);
 
 }  // namespace sdt
