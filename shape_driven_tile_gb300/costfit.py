@@ -12,8 +12,11 @@ tile (microseconds) and takes the smallest estimate; the estimate has the form o
       fixed + max(0, rounds * nK - stages) * kt + rounds * round + tiles * nK / workers * bw
 
 This module restates that form over the library's own tile geometry (``sdt.tiles()``), fits
-the constants of every tile to a sweep by non-negative least squares weighted by 1 / time
-(each tile's rows are independent, so the fit is one small problem per tile), and prints
+the constants of every tile to a sweep by non-negative least squares weighted by 1 / sqrt(time)
+(between absolute and relative error: a fit weighted by 1 / time let the few-microsecond
+shapes pull the wide tiles' constants off the long shapes, and picked 7.6 % off the best
+on the current sweep, against 2.7 % here; each tile's rows are independent, so the fit is
+one small problem per tile), and prints
 them as the ladder's rows.  A tile feasible on too few swept shapes takes a scaled copy of
 another tile's constants (``DERIVED``).  The sweep is the JSON-lines output of
 ``bench.py --mode sweep`` (one object per shape with ``"shape"`` and ``"us"``), e.g. the
@@ -103,7 +106,7 @@ def fit(records, sm_count=SM_COUNT):
         if not rows:
             continue
         X, y = np.array(rows), np.array(times)
-        w = 1.0 / y
+        w = 1.0 / np.sqrt(y)
         consts[name], _ = nnls(X * w[:, None], y * w)
     for name, (src, kt_scale, bw_scale) in DERIVED.items():
         if name in geo and src in consts:

@@ -123,29 +123,30 @@ struct LadderTile {
     }
 
 // Cost-model constants fitted on GB300 (152 SMs) by one non-negative least-squares
-// fit, weighted by 1 / time, over two cold-L2 sweeps of every feasible tile
-// (bench.py --mode sweep): 43 shapes (the square sizes, the K-scan around 2048^2,
+// fit, weighted by 1 / sqrt(time), over two cold-L2 sweeps of every feasible tile
+// (bench.py --mode sweep) of the current kernels (persistent and two-CTA kernels with
+// TMA stores of C): 43 shapes (the square sizes, the K-scan around 2048^2,
 // rectangular, skinny and deep-K shapes) and a second measurement of the 15 square and
-// K-scan ones.  The fitted model's pick is within 4.5 % of the best swept tile on
-// every one of those shapes (0.24 % on average), and stays there with each shape
+// K-scan ones.  The fitted model's pick is within 2.7 % of the best swept tile on
+// every one of those shapes (0.14 % on average), and stays there with each shape
 // left out of the fit in turn (python -m shape_driven_tile_gb300.costfit refits it).
 static const LadderTile kLadder[] = {
-    SDT_TILE(64, 64, 6, "64x64", 6.154, 0.22679, 2.362, 0.00893, 1.472, true),
-    SDT_TILE(64, 128, 4, "64x128", 6.272, 0.24633, 2.248, 0.05573, 1.436, true),
-    SDT_TILE(128, 64, 4, "128x64", 6.641, 0.24566, 1.839, 0.06036, 1.370, true),
-    SDT_TILE(128, 128, 6, "128x128", 5.372, 0.21390, 4.557, 0.02838, 0.000, true),
-    SDT_TILE(128, 256, 4, "128x256", 5.224, 0.31120, 5.706, 0.02606, 0.000, false),
-    SDT_PTILE(128, 6, "p128x128", 9.242, 0.20692, 0.530, 0.02213, true),
-    SDT_PTILE(256, 4, "p128x256", 9.241, 0.31104, 1.679, 0.02061, true),
-    SDT_PAIR(128, 8, "2cta_256x128", 11.797, 0.23033, 0.171, 0.02098, false),
-    SDT_PAIR(256, 6, "2cta_256x256", 10.353, 0.21996, 1.328, 0.10876, true),
+    SDT_TILE(64, 64, 6, "64x64", 6.293, 0.22299, 2.473, 0.01095, 1.323, true),
+    SDT_TILE(64, 128, 4, "64x128", 6.288, 0.24812, 2.152, 0.05457, 1.466, true),
+    SDT_TILE(128, 64, 4, "128x64", 6.654, 0.24589, 1.764, 0.06153, 1.353, true),
+    SDT_TILE(128, 128, 6, "128x128", 5.266, 0.21826, 4.685, 0.01681, 0.000, true),
+    SDT_TILE(128, 256, 4, "128x256", 5.328, 0.30875, 5.201, 0.04317, 0.000, false),
+    SDT_PTILE(128, 6, "p128x128", 9.292, 0.20648, 0.219, 0.01416, true),
+    SDT_PTILE(256, 4, "p128x256", 9.295, 0.31192, 0.158, 0.03885, true),
+    SDT_PAIR(128, 8, "2cta_256x128", 11.744, 0.23670, 0.275, 0.00779, false),
+    SDT_PAIR(256, 6, "2cta_256x256", 11.060, 0.22789, 0.000, 0.10519, true),
     // 224 columns: divides shapes 256 does not (3584 = 16 x 224) and fills the pairs'
     // rounds there (3584^2: 224 tiles = 2.95 rounds of 76 pairs instead of 196 = 2.58
     // rounded up to 3 full-width rounds).  It is feasible on few swept shapes, so its
     // constants are the 256-wide tile's with the k-tile cost scaled by 0.96 (measured
     // at 3584^3 and 7168^3: the MMA time does not shrink in proportion to N) and the
     // streaming term by its operand bytes, 480 / 512.
-    SDT_PAIR(224, 6, "2cta_256x224", 10.353, 0.21116, 1.328, 0.10197, true),
+    SDT_PAIR(224, 6, "2cta_256x224", 11.060, 0.21877, 0.000, 0.09862, true),
     // Skinny tiles for few-row problems (M up to a few tens, e.g. decode rows): the
     // operands are swapped so that the many output columns fill the 128 MMA rows and
     // the M rows become a 16- or 32-wide MMA N; the weights stream through a deep ring
