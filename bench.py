@@ -579,6 +579,8 @@ def run_default(args):
                      "largest_share_in_step": f"gemm_f16 {largest_share}^3",
                      "achieved": round(achieved, 1), "peak": peaks["tflops"], "unit": "TFLOP/s",
                      "frac": round(achieved / peaks["tflops"], 4), "peak_source": peaks["source"] + " bf16 burst",
+                     "peak_sustained": peaks["tflops_sustained"],
+                     "frac_sustained": round(achieved / peaks["tflops_sustained"], 4),
                      "traffic": traffic, **({"traffic_note": traffic_note(f"gemm_{dom}")} if traffic is None else {})},
         "cpu_baseline": baseline,
         "e2e": e2e,
