@@ -429,6 +429,39 @@ def run_default(args):
         if rc:
             raise sdt.SdtError(rc, (L.sdt_last_error() or b"").decode())
 
+    # Concurrent form of a step (graph-replayed steps, --concurrent-steps): the four small GEMMs
+    # (<= 1024^3, 8 to 144 CTAs each, launch-bound) on one side stream and the two
+    # decode GEMVs on another, beside the large GEMMs on the main stream -- a fork and
+    # a join per step.  The launches and buffers are the serial step's; only their
+    # order on the device changes (the problems are independent).
+    SMALL = [n for n in SWEEP if n <= 1024]
+    side_small = torch.cuda.Stream(device=dev)
+    side_dec = torch.cuda.Stream(device=dev)
+
+    def step_concurrent(i, on):
+        fork = torch.cuda.Event()
+        fork.record(on)
+        side_small.wait_event(fork)
+        side_dec.wait_event(fork)
+        g_main, _, _ = args_on.setdefault(on.cuda_stream, launch_args(on.cuda_stream))
+        g_small, _, _ = args_on.setdefault(side_small.cuda_stream, launch_args(side_small.cuda_stream))
+        _, pb, pq = args_on.setdefault(side_dec.cuda_stream, launch_args(side_dec.cuda_stream))
+        rc = 0
+        for j, n in enumerate(SWEEP):
+            if n in SMALL:
+                rc |= gemm_c(*g_small[j])
+        rc |= gemv_b(*pb[i % DEC_BUFFERS])
+        rc |= gemv_q(*pq[i % DEC_BUFFERS])
+        for j, n in enumerate(SWEEP):
+            if n not in SMALL:
+                rc |= gemm_c(*g_main[j])
+        for side in (side_small, side_dec):
+            join = torch.cuda.Event()
+            join.record(side)
+            on.wait_event(join)
+        if rc:
+            raise sdt.SdtError(rc, (L.sdt_last_error() or b"").decode())
+
     launches_per_step = len(SWEEP) + 2
     t_warm = time.perf_counter()
     for i in range(args.warmup):
@@ -470,7 +503,10 @@ def run_default(args):
             cap.wait_stream(stream)
             with torch.cuda.graph(g, stream=cap):
                 for j in range(INSTR - 1):
-                    step(first + j, on=cap)
+                    if args.concurrent_steps:
+                        step_concurrent(first + j, cap)
+                    else:
+                        step(first + j, on=cap)
             stream.wait_stream(cap)
             graphs[first % DEC_BUFFERS] = g
     if graphs:
@@ -573,6 +609,9 @@ def run_default(args):
                                f"{args.steps}); the other steps carry no events",
                    "launch": "eager" if args.no_graph else "instrumented steps eager, the nine steps before "
                              "each of them replayed as one CUDA graph",
+                   "concurrency": "serial" if (not args.concurrent_steps or args.no_graph) else
+                                  "graph-replayed steps: the GEMMs up to 1024^3 and the two decode GEMVs on two side "
+                                  "streams beside the larger GEMMs (fork and join per step); instrumented steps serial",
                    "clock_warmup": f"{clock_warm_s:.2f} s of whole steps right before the timed region",
                    "clocks": "nvidia-smi every 50 ms over the clock warm-up and the timed region"},
         "roofline": {"bound": "tensor", "kernel": f"gemm_f16 {dom}^3 ({tiles[dom]})",
@@ -1649,6 +1688,9 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--clock-warmup-s", type=float, default=1.0,
                     help="default run: seconds of whole steps right before the timed region")
+    ap.add_argument("--concurrent-steps", action="store_true",
+                    help="default run: graph-replayed steps issue the GEMMs up to 1024^3 and the decode GEMVs on two "
+                         "side streams beside the larger GEMMs (independent problems run at the same time)")
     ap.add_argument("--no-legs", action="store_true",
                     help="default run: skip the protocol legs after the timed region (gemm_protocol, pick_check, "
                          "kscan, large)")
