@@ -25,7 +25,8 @@ them).  Each answers one question with a prediction written before it was run:
                    graph-replayed launches x 5 + one eager loop; predicted
                    4096^3 78-86 %; falsified below 70 % or if graph and eager
                    differ by > 5 % from 1536^3 up.
-  pick_check       is pick_tile within 5 % of the fastest feasible tile?
+  pick_check       is pick_tile within 5 % of the fastest feasible tile (the
+                   square sizes and the K-scan shapes)?
                    every feasible tile cold, 5 shuffled passes x 8 launches;
                    predicted average <= 1 %, worst <= 5 %.
   kscan            does K = 2048 (32 k-tiles) camp memory channels on GB300?
@@ -1345,43 +1346,58 @@ def kscan_leg(L, peaks, stream, dev, tile="128x128", passes=4, launches=8, graph
                         "graph-replayed launches, best of 3"}
 
 
-def pick_check_leg(L, A, B, C, tiles, peaks, stream, dev, passes=5, launches=8, warm_s=1.0):
-    """pick_tile against every feasible tile on each square size (the FlyDSL pull
-    request's check of pick_tile against the per-shape fastest, "Changes" and its first
-    commit message): every feasible tile timed cold (L2 flushed before each launch) in
-    `passes` passes of `launches` launches, each pass in a fresh shuffled tile order, a
-    tile's time its best pass mean; the pick's slowdown against the fastest."""
+def pick_check_leg(L, A, B, C, tiles, peaks, stream, dev, passes=5, launches=8, warm_s=1.0, kscan=True):
+    """pick_tile against every feasible tile on each square size and on the K-scan
+    shapes (the FlyDSL pull request's check of pick_tile against the per-shape fastest,
+    "Changes" and its first commit message): every feasible tile timed cold (L2 flushed
+    before each launch) in `passes` passes of `launches` launches, each pass in a fresh
+    shuffled tile order, a tile's time its best pass mean; the pick's slowdown against
+    the fastest."""
+    import torch
+
     import shape_driven_tile_gb300 as sdt
 
     warm = warm_for(warm_s, lambda: [_chk(L.gemm_f16(n, n, n, A[n].data_ptr(), B[n].data_ptr(), C[n].data_ptr(),
                                                      stream.cuda_stream)) for n in SWEEP])
     flush = L2Flush(dev)
+    problems = [(n, n, n, A[n], B[n], C[n]) for n in SWEEP]
+    if kscan:
+        g = torch.Generator(device=dev).manual_seed(71)
+        for K in KSCAN:
+            if K != 2048:
+                problems.append((2048, 2048, K,
+                                 torch.empty((2048, K), dtype=torch.float16, device=dev).uniform_(-1, 1, generator=g),
+                                 torch.empty((K, 2048), dtype=torch.float16, device=dev).uniform_(-1, 1, generator=g),
+                                 torch.empty((2048, 2048), dtype=torch.float16, device=dev)))
     rows = []
-    for n in SWEEP:
-        feas = sdt.feasible_tiles(n, n, n)
+    for M, N, K, Am, Bm, Cm in problems:
+        feas = sdt.feasible_tiles(M, N, K)
         res = {}
-        rng = random.Random(1000 + n)
+        rng = random.Random(1000 * M + 7 * K)
         order = list(feas)
         for _ in range(passes):
             rng.shuffle(order)
             for t in order:
-                fn = lambda t=t: _chk(L.gemm_f16_with_tile(n, n, n, A[n].data_ptr(), B[n].data_ptr(),
-                                                           C[n].data_ptr(), stream.cuda_stream, t, -1))
+                fn = lambda t=t: _chk(L.gemm_f16_with_tile(M, N, K, Am.data_ptr(), Bm.data_ptr(), Cm.data_ptr(),
+                                                           stream.cuda_stream, t, -1))
                 mean = time_cold(fn, launches, flush, stream)[0]
                 res[t] = min(res.get(t, mean), mean)
-        pick = sdt.pick_tile(n, n, n)
+        pick = sdt.pick_tile(M, N, K)
         best = min(res, key=res.get)
         name = lambda t: sdt.tile_info(t)["name"]
-        rows.append({"size": n, "pick": name(pick), "best": name(best),
-                     "slowdown": round(res[pick] / res[best] - 1, 4),
-                     "us": {name(t): round(v * 1e3, 2) for t, v in sorted(res.items(), key=lambda kv: kv[1])}})
-    del flush
+        row = {"shape": [M, N, K], "pick": name(pick), "best": name(best),
+               "slowdown": round(res[pick] / res[best] - 1, 4),
+               "us": {name(t): round(v * 1e3, 2) for t, v in sorted(res.items(), key=lambda kv: kv[1])}}
+        if M == N == K:
+            row["size"] = M
+        rows.append(row)
+    del flush, problems
     slow = [r["slowdown"] for r in rows]
     return {"rows": rows, "avg_slowdown": round(statistics.mean(slow), 4), "worst_slowdown": round(max(slow), 4),
-            "worst_size": rows[slow.index(max(slow))]["size"], "warmup_s": round(warm, 2),
-            "protocol": f"{warm_s:g} s warm-up; every feasible tile, L2 flushed (512 MB read) before each launch, "
-                        f"{passes} passes x {launches} launches in a fresh shuffled tile order per pass, "
-                        "best pass mean per tile"}
+            "worst_shape": rows[slow.index(max(slow))]["shape"], "warmup_s": round(warm, 2),
+            "protocol": f"{warm_s:g} s warm-up; the square sizes and the K-scan shapes, every feasible tile, L2 "
+                        f"flushed (512 MB read) before each launch, {passes} passes x {launches} launches in a fresh "
+                        "shuffled tile order per pass, best pass mean per tile"}
 
 
 def run_legs(L, A, B, C, tiles, peaks, stream, dev, gpu_index):

@@ -36,10 +36,11 @@ def test_pick_check_leg(cuda_device, square_operands):
     A, B, C, tiles = square_operands
     out = bench.pick_check_leg(sdt.lib(), A, B, C, tiles, bench.load_peaks(), torch.cuda.current_stream(),
                                cuda_device, passes=1, launches=1, warm_s=0.05)
-    assert [r["size"] for r in out["rows"]] == bench.SWEEP
+    assert [r["shape"] for r in out["rows"]] == ([[n, n, n] for n in bench.SWEEP]
+                                                 + [[2048, 2048, k] for k in bench.KSCAN if k != 2048])
     for r in out["rows"]:
         assert r["pick"] in r["us"] and r["best"] in r["us"] and r["slowdown"] >= 0
-        assert set(r["us"]) == {sdt.tile_info(t)["name"] for t in sdt.feasible_tiles(r["size"], r["size"], r["size"])}
+        assert set(r["us"]) == {sdt.tile_info(t)["name"] for t in sdt.feasible_tiles(*r["shape"])}
     assert out["worst_slowdown"] == max(r["slowdown"] for r in out["rows"])
     sdt.check_device_status()
 
