@@ -145,3 +145,20 @@ def test_k_zero_and_errors(cuda_device):
     assert e.value.status == "SDT_ERR_SHAPE"
     with pytest.raises(TypeError):
         sdt.gemm_ex(A, B.to(torch.bfloat16))   # mixed types
+
+
+@pytest.mark.parametrize("tile", ["p128x128", "p128x256", "2cta_256x128", "2cta_256x256", "2cta_256x224"])
+@pytest.mark.parametrize("M,N,K", [(1, 8, 1), (3, 40, 70), (257, 264, 130), (130, 1000, 64)])
+def test_tma_store_tiles_on_tiny_ragged_shapes(cuda_device, tile, M, N, K):
+    # the persistent and two-CTA kernels store C through 32 x 32 TMA boxes: rows and
+    # columns past C (most of the tile here) must be dropped, the rest exact
+    for dname, dt in DTYPES.items():
+        A, Av = operand(M, K, False, dt, 451, True, cuda_device)
+        B, Bv = operand(K, N, True, dt, 452, True, cuda_device)
+        Cstore = torch.full((M + 2, N + 16), 3.0, dtype=dt, device=cuda_device)
+        C = Cstore[:M, :N]
+        sdt.gemm_ex(A, B, C, tile=tile)
+        sdt.check_device_status()
+        (assert_bit_exact_bf16 if dt == torch.bfloat16 else assert_bit_exact_f16)(C, ref_of(Av, Bv, dt),
+                                                                                   f"{tile} {M}x{N}x{K} {dname}")
+        assert bool((Cstore[:M, N:] == 3).all()) and bool((Cstore[M:] == 3).all()), f"{tile} wrote outside C"
