@@ -132,7 +132,6 @@ __global__ void __launch_bounds__(192, 1)
     cluster_sync();  // barriers of both CTAs initialised, TMEM allocated in both SMs
     tc_fence_after();
     const uint32_t tmem_base = ctrl[0];
-    griddep_launch_dependents();
     griddep_wait();  // the previous kernel's writes (A, B, C) are visible from here on
 
     if (warp == 0) {
@@ -155,6 +154,10 @@ __global__ void __launch_bounds__(192, 1)
                 const int m0 = m_tile * Cfg::BM + static_cast<int>(rank) * Cfg::CTA_M;
                 const int nb = n_tile * BN + n_off + static_cast<int>(rank) * (width / 2);
                 const bool whole = width == BN;  // whole tile, else a tail half (BN/4 B rows per CTA)
+                // the next kernel in the stream may be launched once every CTA starts its
+                // last item: a dependent that fits beside this kernel (a decode GEMV) then
+                // prefetches near the end of this launch instead of at its start
+                if (item + num_pairs >= num_items) griddep_launch_dependents();
                 const uint32_t pair_bytes = 2u * static_cast<uint32_t>(
                     whole ? Cfg::template load_bytes<L::B_MN>() : Cfg::A_BYTES + (Cfg::B_HALF / 2) * kBK * 2);
                 const int start =

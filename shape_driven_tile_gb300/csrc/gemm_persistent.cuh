@@ -115,7 +115,6 @@ __global__ void __launch_bounds__(192, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = ctrl[0];
-    griddep_launch_dependents();
     griddep_wait();  // the previous kernel's writes (A, B, C) are visible from here on
 
     if (warp == 0) {
@@ -130,6 +129,8 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t empty0 = smem_u32(&empty[0]), full0 = smem_u32(&full[0]);
             const uint32_t smA0 = smem_u32(smA), smB0 = smem_u32(smB);
             for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+                // dependents may launch once every CTA starts its last tile (see gemm_pair.cuh)
+                if (tile + static_cast<int>(gridDim.x) >= num_tiles) griddep_launch_dependents();
                 int m_tile, n_tile;
                 tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.raster_group, m_tile, n_tile);
                 const int m0 = m_tile * Cfg::BM, n0 = n_tile * BN;
