@@ -394,13 +394,22 @@ def run_default(args):
     yq = torch.empty(DEC_N, dtype=torch.float32, device=dev)
     tiles = {n: sdt.tile_info(sdt.pick_tile(n, n, n))["name"] for n in SWEEP}
     stream = torch.cuda.current_stream()
+    # The GEMMs are gemm_f16 calls; --gemm-ws on makes them gemm_f16_ws calls with one
+    # workspace (the two-CTA tiles may then split the contraction of a partly empty last
+    # round: at these sizes the plan keeps gemm_f16's form, at 8192^3 and 12288^3 of the
+    # large leg it splits).
+    gws = sdt.gemm_workspace(dev) if args.gemm_ws == "on" else None
     # The timed loop calls the C ABI directly with the operands' device pointers, so that
     # Python-side argument checks do not leave the GPU idle between the small GEMMs.
     L = sdt.lib()
-    gemm_c, gemv_b, gemv_q = L.gemm_f16, L.gemv_m1_bf16, L.gemv_m1_q8
+    gemv_b, gemv_q = L.gemv_m1_bf16, L.gemv_m1_q8
+    wsa = (gws.data_ptr(), gws.numel()) if gws is not None else None
+    gemm_c = L.gemm_f16_ws if gws is not None else L.gemm_f16
 
-    def launch_args(sp):
-        return ([(n, n, n, A[n].data_ptr(), B[n].data_ptr(), C[n].data_ptr(), sp) for n in SWEEP],
+    def launch_args(sp, ws=True):
+        # launches on a side stream get no workspace: calls that share one must not overlap
+        w = (wsa if ws else (None, 0)) if gws is not None else ()
+        return ([(n, n, n, A[n].data_ptr(), B[n].data_ptr(), C[n].data_ptr(), *w, sp) for n in SWEEP],
                 [(DEC_K, DEC_N, x.data_ptr(), w.data_ptr(), yb.data_ptr(), sp) for w in Wb],
                 [(DEC_K, DEC_N, x.data_ptr(), q.data_ptr(), s_.data_ptr(), yq.data_ptr(), sp) for q, s_ in zip(Wq, Sq)])
 
@@ -445,7 +454,7 @@ def run_default(args):
         side_small.wait_event(fork)
         side_dec.wait_event(fork)
         g_main, _, _ = args_on.setdefault(on.cuda_stream, launch_args(on.cuda_stream))
-        g_small, _, _ = args_on.setdefault(side_small.cuda_stream, launch_args(side_small.cuda_stream))
+        g_small, _, _ = args_on.setdefault(side_small.cuda_stream, launch_args(side_small.cuda_stream, ws=False))
         _, pb, pq = args_on.setdefault(side_dec.cuda_stream, launch_args(side_dec.cuda_stream))
         rc = 0
         for j, n in enumerate(SWEEP):
@@ -551,7 +560,7 @@ def run_default(args):
     dom_ms = per[SWEEP[dom_j]]
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
-    e2e = run_e2e(args, dev, host, Wb_h, Q_h, stream)
+    e2e = run_e2e(args, dev, host, Wb_h, Q_h, stream, gws)
 
     # the decode protocol (after the timed region): 200 back-to-back launches x 10 repeats
     dec_proto = None
@@ -561,7 +570,7 @@ def run_default(args):
         dec_proto["clocks"] = dclk.summary()
 
     # the configurations' own protocols (after the timed region, rank 0)
-    legs = run_legs(L, A, B, C, tiles, peaks, stream, dev, local) if rank == 0 and not args.no_legs else {}
+    legs = run_legs(L, A, B, C, tiles, peaks, stream, dev, local, wsa) if rank == 0 and not args.no_legs else {}
     if rank == 0:
         sdt.check_device_status()
     state_after = gpu_state(local)
@@ -588,6 +597,7 @@ def run_default(args):
     achieved = gemm_flops(dom, dom, dom) / (statistics.mean(dom_ms) / 1e3) / 1e12
     traffic = load_traffic(f"gemm_{dom}")
     clock = clocks.summary()
+    gemm_name = "gemm_f16_ws" if gws is not None else "gemm_f16"
     out = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -615,8 +625,8 @@ def run_default(args):
                                   "streams beside the larger GEMMs (fork and join per step); instrumented steps serial",
                    "clock_warmup": f"{clock_warm_s:.2f} s of whole steps right before the timed region",
                    "clocks": "nvidia-smi every 50 ms over the clock warm-up and the timed region"},
-        "roofline": {"bound": "tensor", "kernel": f"gemm_f16 {dom}^3 ({tiles[dom]})",
-                     "largest_share_in_step": f"gemm_f16 {largest_share}^3",
+        "roofline": {"bound": "tensor", "kernel": f"{gemm_name} {dom}^3 ({tiles[dom]}{last_round_note(dom, tiles[dom], gws)})",
+                     "largest_share_in_step": f"{gemm_name} {largest_share}^3",
                      "achieved": round(achieved, 1), "peak": peaks["tflops"], "unit": "TFLOP/s",
                      "frac": round(achieved / peaks["tflops"], 4), "peak_source": peaks["source"] + " bf16 burst",
                      "peak_sustained": peaks["tflops_sustained"],
@@ -779,7 +789,22 @@ def record_traffic(args):
     print(json.dumps({"mode": "record-traffic", args.key: t[args.key]}))
 
 
-def run_e2e(args, dev, host, Wb_h, Q_h, stream):
+def last_round_note(n, tile, gws):
+    """How a two-CTA tile runs the last round of an n^3 launch (empty for other tiles)."""
+    import shape_driven_tile_gb300 as sdt
+
+    if not tile.startswith("2cta"):
+        return ""
+    ts, items, sp, long_k = sdt.pair_tail_plan(n, n, n, tile, sdt.device_sm_count(),
+                                               sdt.lib().sdt_device_smem_optin(), workspace=gws is not None)
+    if items == ts:
+        return ""
+    if sp:
+        return f"; last round: {(items - ts) // sp} tiles x {sp} k-ranges (split 0: {long_k} k-tiles)"
+    return f"; last round: {(items - ts) // 2} tiles as half-width items"
+
+
+def run_e2e(args, dev, host, Wb_h, Q_h, stream, gws=None):
     """Same metric through the public API with pinned host buffers: every step copies its
     inputs host -> device, runs the step and copies every result device -> host, all inside
     the timed region.  The copies of neighbouring steps overlap the compute on three streams
@@ -834,7 +859,10 @@ def run_e2e(args, dev, host, Wb_h, Q_h, stream):
         s_c.wait_event(b["in"])
         s_c.wait_event(b["out"])  # step i-2's results have left this set's outputs
         for n in SWEEP:
-            sdt.gemm_f16(b["dA"][n], b["dB"][n], b["dC"][n], stream=s_c)
+            if gws is None:
+                sdt.gemm_f16(b["dA"][n], b["dB"][n], b["dC"][n], stream=s_c)
+            else:
+                sdt.gemm_f16_ws(b["dA"][n], b["dB"][n], b["dC"][n], workspace=gws, stream=s_c)
         sdt.gemv_m1(b["dx"], b["dW"], y=b["dyb"], stream=s_c)
         sdt.gemv_m1(b["dx"], b["dq"], b["ds"], y=b["dyq"], stream=s_c)
         b["comp"].record(s_c)
@@ -860,7 +888,10 @@ def run_e2e(args, dev, host, Wb_h, Q_h, stream):
     last = sets[(steps - 1) % 2]
     ref = {n: torch.empty((n, n), dtype=torch.float16, device=dev) for n in SWEEP}
     for n in SWEEP:
-        sdt.gemm_f16(last["dA"][n], last["dB"][n], ref[n])
+        if gws is None:
+            sdt.gemm_f16(last["dA"][n], last["dB"][n], ref[n])
+        else:
+            sdt.gemm_f16_ws(last["dA"][n], last["dB"][n], ref[n], workspace=gws)
     torch.cuda.synchronize()
     ok = all(torch.equal(last["hC"][n], ref[n].cpu()) for n in SWEEP)
     world = dist_env()[0]
@@ -1205,7 +1236,7 @@ def time_graph(g, count, reps, stream):
     return out
 
 
-def gemm_protocol_leg(L, A, B, C, tiles, peaks, stream, dev, launches=200, reps=5, warm_s=1.0):
+def gemm_protocol_leg(L, A, B, C, tiles, peaks, stream, dev, launches=200, reps=5, warm_s=1.0, wsa=None):
     """The square sweep by the pages' GEMM protocol ("Beating hipBLASLt on a Gaming GPU",
     "Why these numbers should be trusted"; "mojo-baro", "Square fp16 GEMM vs hipBLASLt"):
     a clock warm-up, then per size `launches` back-to-back launches of gemm_f16 replayed
@@ -1215,7 +1246,10 @@ def gemm_protocol_leg(L, A, B, C, tiles, peaks, stream, dev, launches=200, reps=
     import torch
 
     def call(n, sp):
-        _chk(L.gemm_f16(n, n, n, A[n].data_ptr(), B[n].data_ptr(), C[n].data_ptr(), sp))
+        if wsa is None:
+            _chk(L.gemm_f16(n, n, n, A[n].data_ptr(), B[n].data_ptr(), C[n].data_ptr(), sp))
+        else:
+            _chk(L.gemm_f16_ws(n, n, n, A[n].data_ptr(), B[n].data_ptr(), C[n].data_ptr(), *wsa, sp))
 
     warm = warm_for(warm_s, lambda: [call(n, stream.cuda_stream) for n in SWEEP])
     graphs = {n: graph_of(lambda i, sp, n=n: call(n, sp), launches, dev) for n in SWEEP}
@@ -1249,7 +1283,7 @@ def gemm_protocol_leg(L, A, B, C, tiles, peaks, stream, dev, launches=200, reps=
                         f"launch; eager_us: {launches} host-issued launches between two events"}
 
 
-def large_leg(L, peaks, stream, dev, sizes=None, reps=3, warm_s=1.0):
+def large_leg(L, peaks, stream, dev, sizes=None, reps=3, warm_s=1.0, wsa=None):
     """Large squares M=N=K in {8192, 12288, 16384} with pick_tile: a clock warm-up on the
     first size, then per size a CUDA graph of back-to-back launches (about 20 ms) replayed
     `reps` times; operands far larger than L2.  TFLOP/s against the measured burst and
@@ -1268,7 +1302,10 @@ def large_leg(L, peaks, stream, dev, sizes=None, reps=3, warm_s=1.0):
         count = max(3, min(20, round(20e-3 / (fl / 1.5e15))))
 
         def call(sp, n=n, A=A, B=B, C=C):
-            _chk(L.gemm_f16(n, n, n, A.data_ptr(), B.data_ptr(), C.data_ptr(), sp))
+            if wsa is None:
+                _chk(L.gemm_f16(n, n, n, A.data_ptr(), B.data_ptr(), C.data_ptr(), sp))
+            else:
+                _chk(L.gemm_f16_ws(n, n, n, A.data_ptr(), B.data_ptr(), C.data_ptr(), *wsa, sp))
 
         if idx == 0:
             warm = warm_for(warm_s, lambda: call(stream.cuda_stream))
@@ -1400,13 +1437,15 @@ def pick_check_leg(L, A, B, C, tiles, peaks, stream, dev, passes=5, launches=8, 
                         "shuffled tile order per pass, best pass mean per tile"}
 
 
-def run_legs(L, A, B, C, tiles, peaks, stream, dev, gpu_index):
-    """The four protocol legs, each under its own nvidia-smi clock sampler."""
+def run_legs(L, A, B, C, tiles, peaks, stream, dev, gpu_index, wsa=None):
+    """The four protocol legs, each under its own nvidia-smi clock sampler (the GEMM
+    protocol and the large squares through gemm_f16_ws with the step's workspace `wsa`
+    when one is given, else gemm_f16)."""
     out = {}
-    for key, fn in (("gemm_protocol", lambda: gemm_protocol_leg(L, A, B, C, tiles, peaks, stream, dev)),
+    for key, fn in (("gemm_protocol", lambda: gemm_protocol_leg(L, A, B, C, tiles, peaks, stream, dev, wsa=wsa)),
                     ("pick_check", lambda: pick_check_leg(L, A, B, C, tiles, peaks, stream, dev)),
                     ("kscan", lambda: kscan_leg(L, peaks, stream, dev)),
-                    ("large", lambda: large_leg(L, peaks, stream, dev))):
+                    ("large", lambda: large_leg(L, peaks, stream, dev, wsa=wsa))):
         t0 = time.perf_counter()
         with ClockSampler(gpu_index) as clk:
             res = fn()
@@ -1707,6 +1746,9 @@ def main(argv=None):
     ap.add_argument("--concurrent-steps", action="store_true",
                     help="default run: graph-replayed steps issue the GEMMs up to 1024^3 and the decode GEMVs on two "
                          "side streams beside the larger GEMMs (independent problems run at the same time)")
+    ap.add_argument("--gemm-ws", choices=["on", "off"], default="off",
+                    help="default run: the GEMMs as gemm_f16 calls (off) or as gemm_f16_ws calls with a workspace "
+                         "(on: a two-CTA tile may split its last round in K where the plan says it pays)")
     ap.add_argument("--no-legs", action="store_true",
                     help="default run: skip the protocol legs after the timed region (gemm_protocol, pick_check, "
                          "kscan, large)")

@@ -226,6 +226,65 @@ int gemm_f16_with_tile(int64_t M, int64_t N, int64_t K,
 #define SDT_LAYOUT_B_T 2
 int gemm_ex(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
             void *C, int64_t ldc, int dtype, int layout, int tile_id, sdt_stream_t stream);
+/*
+ * gemm_f16_ws / gemm_ex_ws -- gemm_f16 / gemm_ex with a caller workspace that lets
+ * the two-CTA tiles split the contraction of their last round [P3, third commit
+ * message: persistent workgroups and the grid tail when the tile count is not a
+ * multiple of the slot count; P4 "The Six Rounds": splitting the contraction, and
+ * Stream-K's decomposition of the iteration space, of which this is the special case
+ * "whole tiles, then the last partial wave split in K"].
+ *
+ * A two-CTA launch runs T output tiles on P = SMs/2 pairs.  When L = T mod P tiles
+ * are left for a last round (P - L pairs idle), each of them may run as S full-width
+ * items over consecutive k-ranges (L*S <= P, 2 <= S <= nK) instead of gemm_f16's form
+ * (whole, or two half-width items).  Split 0 takes the first k-tiles and is made
+ * longer than the others (sdt_pair_tail_plan's split0_ktiles) so that it normally
+ * finishes last.  An item that finishes while another split is still running writes
+ * its fp32 partial to the workspace and counts its arrival; the last to finish adds
+ * the S partials in split order (so the result does not depend on the order of
+ * arrival) and writes C.  The form is chosen per launch by a cost estimate (on GB300
+ * the split pays from about 100 k-tiles, e.g. 8192^3; at 4096^3 the half-width items
+ * are kept); gemm_ex_ws's tail_splits forces it: -1 estimate, 0 never split, 2..8
+ * that count (lowered to what L*S <= P, nK and the shared memory for the partials'
+ * copies allow: at most 7 with the current tiles; below 2 it is not split).
+ * Every other tile, and a launch with no partial last round, runs exactly as
+ * gemm_f16 / gemm_ex would.  Results may differ from gemm_f16's in the last bits
+ * (the split tiles add their k-ranges in another order); integer-valued products
+ * are identical.
+ *
+ * Workspace: NULL runs exactly gemm_f16 / gemm_ex.  Otherwise device memory owned
+ * by the caller, 256-byte aligned, at least sdt_gemm_workspace_bytes() bytes (the
+ * 1 MiB counter region of the split-K workspaces, then one 256 x 256 fp32 slot per
+ * SM pair: 20 MiB on a 152-SM GPU, for any shape).  Its counters must be zero before
+ * the first call (sdt_splitk_workspace_init); every completed call leaves them zero,
+ * so a workspace zeroed once serves any sequence of calls, and it may be shared with
+ * the split-K calls.  Calls that share a workspace must not overlap on the GPU.
+ * After a call that reported a device error (sdt_check_device_status), zero it again.
+ * Arguments and errors otherwise as gemm_f16 / gemm_ex, plus SDT_ERR_ALIGN and
+ * SDT_ERR_ARG for the workspace and SDT_ERR_ARG for tail_splits outside -1, 0, 2..8.
+ */
+int gemm_f16_ws(int64_t M, int64_t N, int64_t K, const void *A, const void *B, void *C, void *workspace,
+                size_t workspace_bytes, sdt_stream_t stream);
+int gemm_ex_ws(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
+               void *C, int64_t ldc, int dtype, int layout, int tile_id, int tail_splits, void *workspace,
+               size_t workspace_bytes, sdt_stream_t stream);
+/* Workspace bytes gemm_f16_ws / gemm_ex_ws accept on the current device (0 on error),
+ * and on a GPU with sm_count SMs (needs no GPU). */
+size_t sdt_gemm_workspace_bytes(void);
+size_t sdt_gemm_workspace_bytes_for(int sm_count);
+/*
+ * The last-round plan of two-CTA tile `tile_id` on M x N x K with sm_count SMs and
+ * smem_limit bytes of shared memory per block (needs no GPU): items [0, *tail_start)
+ * are whole tiles, items [*tail_start, *num_items) the last round's, as *splits
+ * k-ranges per tile (*splits >= 2; split 0 has *split0_ktiles k-tiles, the others
+ * share the rest evenly) or two half-width items per tile (*splits == 0,
+ * *num_items > *tail_start); *tail_start == *num_items means whole tiles throughout.
+ * with_workspace != 0 plans as gemm_ex_ws with `tail_splits`, 0 as gemm_ex.
+ * SDT_ERR_TILE for a tile that is not two-CTA, SDT_ERR_ARG for bad sizes.
+ */
+int sdt_pair_tail_plan(int64_t M, int64_t N, int64_t K, int tile_id, int sm_count, int smem_limit,
+                       int with_workspace, int tail_splits, int *tail_start, int *num_items, int *splits,
+                       int *split0_ktiles);
 /* pick_tile's cost model over every tile for any shape (tiles may overhang); needs no GPU. */
 int sdt_pick_tile_any_for(int64_t M, int64_t N, int64_t K, int sm_count, int smem_limit);
 /*

@@ -21,6 +21,7 @@ __all__ = [
     "splitk_workspace_bytes", "pick_splitk", "pick_tile_any", "gemm_ex_splitk",
     "splitk_ex_workspace_bytes", "pick_splitk_any", "SPLITK_REDUCE_KERNEL", "SPLITK_IN_KERNEL", "gemm_ex",
     "SPLITK_STREAM", "SPLITK_STREAM_REDUCE", "streamk_ctas", "streamk_workspace_bytes",
+    "gemm_f16_ws", "gemm_ex_ws", "gemm_workspace_bytes", "gemm_workspace", "pair_tail_plan",
 ]
 
 
@@ -197,6 +198,66 @@ def gemm_ex(A, B, C=None, *, tile=-1, stream=None):
     check(lib().gemm_ex(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, C.data_ptr(), ldc, DTYPE_CODES[A.dtype],
                         layout, tid, _stream(stream)))
     return C
+
+
+def gemm_workspace_bytes(sm_count: int | None = None) -> int:
+    """Bytes of workspace gemm_f16_ws / gemm_ex_ws take (current device when sm_count is None)."""
+    if sm_count is None:
+        return int(lib().sdt_gemm_workspace_bytes())
+    return int(lib().sdt_gemm_workspace_bytes_for(int(sm_count)))
+
+
+def gemm_workspace(device=None) -> torch.Tensor:
+    """A zeroed, 256-byte aligned workspace for gemm_f16_ws / gemm_ex_ws (owned by the caller)."""
+    nbytes = gemm_workspace_bytes()
+    if nbytes == 0:
+        raise SdtError(-9, "no CUDA device")
+    ws = torch.empty(nbytes + 256, dtype=torch.uint8, device=device or "cuda")
+    off = (-ws.data_ptr()) % 256
+    ws = ws[off:off + nbytes]
+    check(lib().sdt_splitk_workspace_init(ws.data_ptr(), nbytes, _stream(None)))
+    return ws
+
+
+def gemm_f16_ws(A, B, C=None, *, workspace, stream=None):
+    """gemm_f16 with a workspace (gemm_workspace()) in which a two-CTA tile's partly empty
+    last round may split its tiles in K; workspace None runs gemm_f16."""
+    M, N, K, C = _gemm_args(A, B, C)
+    if workspace is None:
+        check(lib().gemm_f16_ws(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(), None, 0, _stream(stream)))
+        return C
+    nbytes = _workspace(workspace)
+    _one_device(A=A, workspace=workspace)
+    check(lib().gemm_f16_ws(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(), workspace.data_ptr(), nbytes,
+                            _stream(stream)))
+    return C
+
+
+def gemm_ex_ws(A, B, C=None, *, workspace, tile=-1, tail_splits: int = -1, stream=None):
+    """gemm_ex with a gemm_f16_ws workspace; tail_splits -1 plans the last round, 0 never
+    splits it, 2..8 forces that many k-ranges per leftover tile."""
+    M, N, K, lda, ldb, ldc, layout, C = _ex_args(A, B, C)
+    tid = tile_id(tile) if isinstance(tile, str) else int(tile)
+    wptr, nbytes = None, 0
+    if workspace is not None:
+        nbytes = _workspace(workspace)
+        _one_device(A=A, workspace=workspace)
+        wptr = workspace.data_ptr()
+    check(lib().gemm_ex_ws(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, C.data_ptr(), ldc, DTYPE_CODES[A.dtype],
+                           layout, tid, int(tail_splits), wptr, nbytes, _stream(stream)))
+    return C
+
+
+def pair_tail_plan(M: int, N: int, K: int, tile, sm_count: int = 152, smem_limit: int = 232448, *,
+                   workspace: bool = True, tail_splits: int = -1) -> tuple[int, int, int, int]:
+    """(tail_start, num_items, splits, split0_ktiles) of a two-CTA tile's last round (see
+    sdt.h); no GPU needed."""
+    tid = tile_id(tile) if isinstance(tile, str) else int(tile)
+    a, b, c, d = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    check(lib().sdt_pair_tail_plan(M, N, K, tid, int(sm_count), int(smem_limit), 1 if workspace else 0,
+                                   int(tail_splits), ctypes.byref(a), ctypes.byref(b), ctypes.byref(c),
+                                   ctypes.byref(d)))
+    return a.value, b.value, c.value, d.value
 
 
 SPLITK_REDUCE_KERNEL = 0

@@ -65,6 +65,13 @@ SIGNATURES = {
     "sdt_streamk_workspace_bytes": (ctypes.c_size_t, [i64, i64, i64, cint, cint]),
     "sdt_streamk_ctas_for": (cint, [cint, cint, cint]),
     "sdt_streamk_ctas": (cint, [cint]),
+    "gemm_f16_ws": (cint, [i64, i64, i64, vp, vp, vp, vp, ctypes.c_size_t, vp]),
+    "gemm_ex_ws": (cint, [i64, i64, i64, vp, i64, vp, i64, vp, i64, cint, cint, cint, cint, vp, ctypes.c_size_t,
+                          vp]),
+    "sdt_gemm_workspace_bytes": (ctypes.c_size_t, []),
+    "sdt_gemm_workspace_bytes_for": (ctypes.c_size_t, [cint]),
+    "sdt_pair_tail_plan": (cint, [i64, i64, i64, cint, cint, cint, cint, cint, ctypes.POINTER(cint),
+                                  ctypes.POINTER(cint), ctypes.POINTER(cint), ctypes.POINTER(cint)]),
 }
 
 STATUS = {

@@ -599,11 +599,111 @@ static int validate_common(int64_t M, int64_t N, int64_t K, const void *A, const
     return SDT_OK;
 }
 
+// Workspaces of the split-K family and of the two-CTA tail begin with a fixed 1 MiB
+// region of u32 arrival counters; the fp32 partials follow it.
+static constexpr size_t kCounterRegionBytes = size_t(1) << 20;
+
+// ---- the last round of the two-CTA kernel -----------------------------------------
+//
+// T tiles on P pairs leave L = T mod P tiles (all T when T < P) for a last round in
+// which P - L pairs idle.  That round runs in one of three forms:
+//   whole   the L tiles as they are;
+//   halves  two half-width items per tile (BN = 256 and 2L <= P);
+//   k-split given a workspace, S full-width items per tile over consecutive k-ranges
+//           (L*S <= P) whose fp32 partials the last to finish sums.  Split 0 is made
+//           longer than the others by the time a partial takes to be published, so
+//           that it normally finishes last and sums without publishing its own.
+// The estimate of each form's last round uses GB300 timings of the 256 x 256 pair
+// kernel at 4096^3 (globaltimer stamps): a whole-width k-tile 0.297 us, a half-width
+// one 0.25 us; from the last MMA issue to the stores' completion 2.4 us for a plain
+// epilogue and 9.7 us for the summing split (its copies of the other partial 2.9 us,
+// the sums and stores 0.5 us per 32 columns; one more partial adds 2.5 us); a split's
+// partial is out and counted 5.0 us after its last MMA issue.  So half-width items win
+// up to nK ~ 100 (4096^3) and the split from there (8192^3: 31.4 against 34.4 us).
+// The cheapest form is planned; `req` forces the k-split count (>= 2) or disables it (0).
+struct PairTail {
+    int tail_start, num_items, splits, long_k;
+};
+
+static constexpr int kPairTailMaxSplits = 8;
+static constexpr double kTailKt = 0.297, kTailHalfKt = 0.25, kTailEpi = 2.4, kTailReduce = 9.7,
+                        kTailReduceExtra = 2.5, kTailPublish = 5.0;
+
+// The largest k-split count for L leftover tiles: L*S <= P, S <= nK, and the other
+// S-1 partials of a 64-column group must fit in an epilogue warp's quarter of the ring.
+static int pair_tail_max_splits(const LadderTile &t, int leftover, int pairs, int nK, int stages) {
+    if (leftover <= 0) return 1;
+    const int quarter = (stages * t.smem_per_stage / 4) & ~1023;
+    int s = std::min(std::min(pairs / leftover, nK), kPairTailMaxSplits);
+    while (s > 1 && (s - 1) * 64 * 32 * 4 > quarter) --s;
+    return std::max(s, 1);
+}
+
+// k-tiles of split 0 for an S-way split of nK k-tiles: the others' share plus the
+// publishing time, at most nK - (S-1) (every other split keeps at least one k-tile).
+static int pair_tail_long(int nK, int S) {
+    const double lead = kTailPublish / kTailKt;
+    const int want = int(std::ceil((nK + (S - 1) * lead) / S));
+    return std::max(std::min(want, nK - (S - 1)), (nK + S - 1) / S);
+}
+
+static PairTail pair_tail_plan(const LadderTile &t, int tiles, int nK, int pairs, int stages, bool have_ws,
+                               int req) {
+    PairTail pt{tiles, tiles, 0, 0};
+    if (t.cta_group != 2 || pairs <= 0 || tiles <= 0) return pt;
+    const int L = tiles % pairs;
+    if (L == 0) return pt;
+    double best = nK * kTailKt + kTailEpi;  // whole tiles
+    int form = 0;                           // 0 whole, 1 halves, >= 2 k-split count
+    if (t.BN == 256 && 2 * L <= pairs && env_int("SDT_TAIL_SPLIT", 1, 0, 1) && nK * kTailHalfKt + kTailEpi < best) {
+        best = nK * kTailHalfKt + kTailEpi;
+        form = 1;
+    }
+    const int smax = have_ws ? pair_tail_max_splits(t, L, pairs, nK, stages) : 1;
+    if (req >= 2 && smax >= 2) {
+        form = std::min(req, smax);
+    } else if (req != 0) {
+        for (int sp = 2; sp <= smax; ++sp) {
+            const double c = pair_tail_long(nK, sp) * kTailKt + kTailReduce + kTailReduceExtra * (sp - 2);
+            if (c < best) {
+                best = c;
+                form = sp;
+            }
+        }
+    }
+    pt.tail_start = tiles - L;
+    if (form == 1) {
+        pt.num_items = pt.tail_start + 2 * L;
+    } else if (form >= 2) {
+        pt.num_items = pt.tail_start + L * form;
+        pt.splits = form;
+        pt.long_k = pair_tail_long(nK, form);
+    } else {
+        pt.tail_start = tiles;
+    }
+    return pt;
+}
+
+// Workspace bytes a two-CTA launch with k-split tail items needs: the counter region
+// and one 256 x BN fp32 slot per item.
+static size_t pair_tail_ws_bytes(const LadderTile &t, int items) {
+    return kCounterRegionBytes + size_t(items) * 256 * size_t(t.BN) * 4;
+}
+
+// A caller workspace for the two-CTA tail (gemm_f16_ws / gemm_ex_ws); ws == nullptr
+// means none.  req: -1 plan the tail, 0 no k-split, >= 2 this k-split count.
+struct TailWs {
+    void *ws;
+    size_t bytes;
+    int req;
+};
+
 // Launches ladder tile `tile_id` on validated, non-empty arguments with K > 0
 // (any shape: tiles overhang ragged edges; layouts and type per the flags).
 static int run_tile_ex(int tile_id, int stagger_req, int64_t M0, int64_t N0, int64_t K0, const void *A0,
                        int64_t lda0, const void *B0, int64_t ldb0, void *C, int64_t ldc, int dtype, int layout0,
-                       cudaStream_t stream, const DeviceInfo &dev, int raster_req = 0, int stages_req = 0) {
+                       cudaStream_t stream, const DeviceInfo &dev, int raster_req = 0, int stages_req = 0,
+                       const TailWs *tw = nullptr) {
     const LadderTile &t = kLadder[tile_id];
     ExProblem ex;
     int rc = ex_problem(t, M0, N0, K0, A0, lda0, B0, ldb0, layout0, &ex);
@@ -641,15 +741,21 @@ static int run_tile_ex(int tile_id, int stagger_req, int64_t M0, int64_t N0, int
     if (int64_t(a.num_m_tiles) * a.num_n_tiles > kMaxGridTiles)
         return fail(SDT_ERR_SHAPE, "grid too large");
     const int tiles = a.num_m_tiles * a.num_n_tiles;
-    a.tail_start = tiles;
-    a.num_items = tiles;
-    if (t.cta_group == 2 && t.BN == 256 && env_int("SDT_TAIL_SPLIT", 1, 0, 1)) {
-        const int workers = std::max(1, a.max_ctas / 2);
-        const int tail = tiles % workers;
-        if (tail > 0 && 2 * tail <= workers) {
-            a.tail_start = tiles - tail;
-            a.num_items = a.tail_start + 2 * tail;
-        }
+    const bool have_ws = tw && tw->ws;
+    int tail_req = have_ws ? tw->req : 0;
+    if (have_ws && tail_req < 0) tail_req = env_int("SDT_TAIL_KSPLIT", -1, -1, kPairTailMaxSplits);
+    const PairTail pt = pair_tail_plan(t, tiles, a.num_k_tiles, std::max(1, a.max_ctas / 2), a.stages, have_ws,
+                                       tail_req);
+    a.tail_start = pt.tail_start;
+    a.num_items = pt.num_items;
+    a.tail_splits = pt.splits;
+    a.tail_long = pt.long_k;
+    if (pt.splits >= 2) {
+        if (pair_tail_ws_bytes(t, pt.num_items - pt.tail_start) > tw->bytes)
+            return fail(SDT_ERR_ARG, "workspace of %zu bytes is too small for the two-CTA tail (%zu)", tw->bytes,
+                        pair_tail_ws_bytes(t, pt.num_items - pt.tail_start));
+        a.counters = static_cast<unsigned *>(tw->ws);
+        a.partials = reinterpret_cast<float *>(static_cast<char *>(tw->ws) + kCounterRegionBytes);
     }
     // the persistent and two-CTA kernels write C with TMA stores (32 x 32 boxes)
     CUtensorMap tmC = tmA;  // unused by the one-CTA kernel
@@ -669,13 +775,13 @@ static int run_tile_ex(int tile_id, int stagger_req, int64_t M0, int64_t N0, int
 // gemm_f16's forced tile: tight row-major fp16, the tile must divide the shape.
 static int run_tile(int tile_id, int stagger_req, int64_t M, int64_t N, int64_t K, const void *A,
                     const void *B, void *C, cudaStream_t stream, const DeviceInfo &dev, int raster_req = 0,
-                    int stages_req = 0) {
+                    int stages_req = 0, const TailWs *tw = nullptr) {
     const LadderTile &t = kLadder[tile_id];
     if (!feasible(t, M, N, K, dev.smem_optin))
         return fail(SDT_ERR_TILE, "tile %s is infeasible for %lldx%lldx%lld", t.name, (long long)M,
                     (long long)N, (long long)K);
     return run_tile_ex(tile_id, stagger_req, M, N, K, A, K, B, N, C, N, SDT_DTYPE_F16, 0, stream, dev, raster_req,
-                       stages_req);
+                       stages_req, tw);
 }
 
 // SDT_AUTOTUNE=1: time every feasible tile on the caller's stream (synchronising
@@ -731,7 +837,7 @@ static int autotune_shape(int64_t M, int64_t N, int64_t K, const void *A, const 
 }
 
 static int gemm_dispatch(int64_t M, int64_t N, int64_t K, const void *A, const void *B, void *C,
-                         sdt_stream_t stream_h, int tile_id, int stagger) {
+                         sdt_stream_t stream_h, int tile_id, int stagger, const TailWs *tw = nullptr) {
     clear_error();
     int rc = validate_common(M, N, K, A, B, C);
     if (rc) return rc;
@@ -752,23 +858,23 @@ static int gemm_dispatch(int64_t M, int64_t N, int64_t K, const void *A, const v
         return e == cudaSuccess ? SDT_OK : fail(SDT_ERR_LAUNCH, "zero fill failed: %s", cudaGetErrorString(e));
     }
     if (N % 8 || K % 8) return fail(SDT_ERR_SHAPE, "N and K must be multiples of 8");
-    if (tile_id >= 0) return run_tile(tile_id, stagger, M, N, K, A, B, C, stream, dev);
+    if (tile_id >= 0) return run_tile(tile_id, stagger, M, N, K, A, B, C, stream, dev, 0, 0, tw);
 
     load_env_table();
     TuneEntry te;
     if (table_lookup(M, N, K, &te) && feasible(kLadder[te.tile], M, N, K, dev.smem_optin))
         return run_tile(te.tile, stagger >= 0 ? stagger : te.stagger, M, N, K, A, B, C, stream, dev, te.raster,
-                        te.stages);
+                        te.stages, tw);
     if (env_flag("SDT_AUTOTUNE")) {
         rc = autotune_shape(M, N, K, A, B, C, stream, dev, &te);
         if (rc) return rc;
-        return run_tile(te.tile, stagger, M, N, K, A, B, C, stream, dev);
+        return run_tile(te.tile, stagger, M, N, K, A, B, C, stream, dev, 0, 0, tw);
     }
     const int id = pick_for(M, N, K, dev.sm_count, dev.smem_optin, dev.smem_per_sm);
     if (id < 0)
         return fail(SDT_ERR_SHAPE, "no feasible tile for %lldx%lldx%lld (need M,N,K multiples of 64 and K >= 128)",
                     (long long)M, (long long)N, (long long)K);
-    return run_tile(id, stagger, M, N, K, A, B, C, stream, dev);
+    return run_tile(id, stagger, M, N, K, A, B, C, stream, dev, 0, 0, tw);
 }
 
 // ---- split-K ----------------------------------------------------------------------
@@ -781,7 +887,6 @@ static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // tile, split count and algorithm: a completed call leaves its counters at zero and
 // writes partials only past the region, so a workspace zeroed once serves any
 // sequence of calls that do not overlap on the GPU.
-static constexpr size_t kCounterRegionBytes = size_t(1) << 20;
 static constexpr int64_t kMaxCounters = int64_t(kCounterRegionBytes / 4);
 static size_t splitk_counter_bytes(int64_t) { return kCounterRegionBytes; }
 static size_t splitk_partials_bytes(int64_t Mp, int64_t Np, int splits) {
@@ -1176,7 +1281,8 @@ static int zero_c(int64_t M, int64_t N, void *C, int64_t ldc, cudaStream_t strea
 }
 
 static int gemm_ex_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
-                        void *C, int64_t ldc, int dtype, int layout, int tile_id, cudaStream_t stream) {
+                        void *C, int64_t ldc, int dtype, int layout, int tile_id, cudaStream_t stream,
+                        const TailWs *tw = nullptr) {
     int rc = validate_ex(M, N, K, A, lda, B, ldb, C, ldc, dtype, layout);
     if (rc || M == 0 || N == 0) return rc;
     if (tile_id < -1 || tile_id >= kNumTiles) return fail(SDT_ERR_TILE, "unknown tile id %d", tile_id);
@@ -1187,7 +1293,28 @@ static int gemm_ex_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t 
     if (tile_id < 0) tile_id = pick_any(M, N, K, dev.sm_count, dev.smem_optin, dev.smem_per_sm);
     if (tile_id < 0 || !fits_chip(kLadder[tile_id], dev.smem_optin))
         return fail(SDT_ERR_TILE, "no tile fits this device");
-    return run_tile_ex(tile_id, -1, M, N, K, A, lda, B, ldb, C, ldc, dtype, layout, stream, dev);
+    return run_tile_ex(tile_id, -1, M, N, K, A, lda, B, ldb, C, ldc, dtype, layout, stream, dev, 0, 0, tw);
+}
+
+// The workspace every gemm_f16_ws / gemm_ex_ws call accepts on a GPU with sm_count SMs:
+// the counter region and one 256 x 256 fp32 slot per SM pair (a last round has at most
+// one item per pair).
+static size_t gemm_ws_bytes(int sm_count) {
+    return kCounterRegionBytes + size_t(std::max(sm_count / 2, 1)) * 256 * 256 * 4;
+}
+
+// Checks a gemm_*_ws workspace (nullptr: none) and fills `tw`.
+static int tail_ws_arg(void *ws, size_t bytes, int req, const DeviceInfo &dev, TailWs *tw) {
+    *tw = TailWs{nullptr, 0, 0};
+    if (!ws) return SDT_OK;
+    if (reinterpret_cast<uintptr_t>(ws) & 255) return fail(SDT_ERR_ALIGN, "the workspace must be 256-byte aligned");
+    if (bytes < gemm_ws_bytes(dev.sm_count))
+        return fail(SDT_ERR_ARG, "workspace of %zu bytes; sdt_gemm_workspace_bytes() is %zu", bytes,
+                    gemm_ws_bytes(dev.sm_count));
+    if (req < -1 || req == 1 || req > kPairTailMaxSplits)
+        return fail(SDT_ERR_ARG, "tail_splits must be -1, 0 or 2..%d", kPairTailMaxSplits);
+    *tw = TailWs{ws, bytes, req};
+    return SDT_OK;
 }
 
 static int gemm_ex_splitk_impl(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
@@ -1240,6 +1367,68 @@ int gemm_f16_with_tile(int64_t M, int64_t N, int64_t K, const void *A, const voi
         return fail(SDT_ERR_TILE, "unknown tile id %d", tile_id);
     }
     return gemm_dispatch(M, N, K, A, B, C, stream, tile_id, stagger);
+}
+
+int gemm_f16_ws(int64_t M, int64_t N, int64_t K, const void *A, const void *B, void *C, void *workspace,
+                size_t workspace_bytes, sdt_stream_t stream) {
+    clear_error();
+    DeviceInfo dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    TailWs tw;
+    rc = tail_ws_arg(workspace, workspace_bytes, -1, dev, &tw);
+    if (rc) return rc;
+    return gemm_dispatch(M, N, K, A, B, C, stream, -1, -1, &tw);
+}
+
+int gemm_ex_ws(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb, void *C,
+               int64_t ldc, int dtype, int layout, int tile_id, int tail_splits, void *workspace,
+               size_t workspace_bytes, sdt_stream_t stream) {
+    clear_error();
+    DeviceInfo dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    TailWs tw;
+    rc = tail_ws_arg(workspace, workspace_bytes, tail_splits, dev, &tw);
+    if (rc) return rc;
+    return gemm_ex_impl(M, N, K, A, lda, B, ldb, C, ldc, dtype, layout, tile_id,
+                        reinterpret_cast<cudaStream_t>(stream), &tw);
+}
+
+size_t sdt_gemm_workspace_bytes_for(int sm_count) {
+    clear_error();
+    return sm_count > 0 ? gemm_ws_bytes(sm_count) : 0;
+}
+
+size_t sdt_gemm_workspace_bytes(void) {
+    DeviceInfo dev;
+    if (current_device(&dev)) return 0;
+    clear_error();
+    return gemm_ws_bytes(dev.sm_count);
+}
+
+int sdt_pair_tail_plan(int64_t M, int64_t N, int64_t K, int tile_id, int sm_count, int smem_limit,
+                       int with_workspace, int tail_splits, int *tail_start, int *num_items, int *splits,
+                       int *split0_ktiles) {
+    clear_error();
+    if (!tail_start || !num_items || !splits || !split0_ktiles)
+        return fail(SDT_ERR_NULL, "output pointers must not be NULL");
+    if (tile_id < 0 || tile_id >= kNumTiles || kLadder[tile_id].cta_group != 2)
+        return fail(SDT_ERR_TILE, "tile %d is not a two-CTA tile", tile_id);
+    if (!dims_in_range(M, N, K) || sm_count < 2 || smem_limit <= 0)
+        return fail(SDT_ERR_ARG, "dimensions and sm_count out of range");
+    if (tail_splits < -1 || tail_splits == 1 || tail_splits > kPairTailMaxSplits)
+        return fail(SDT_ERR_ARG, "tail_splits must be -1, 0 or 2..%d", kPairTailMaxSplits);
+    const LadderTile &t = kLadder[tile_id];
+    const int64_t tiles = ceil_div(M, t.BM) * ceil_div(N, t.BN);
+    if (tiles > kMaxGridTiles) return fail(SDT_ERR_SHAPE, "grid too large");
+    const PairTail pt = pair_tail_plan(t, int(tiles), int(ceil_div(K, kBK)), sm_count / 2,
+                                       tile_stages(t, smem_limit), with_workspace != 0, tail_splits);
+    *tail_start = pt.tail_start;
+    *num_items = pt.num_items;
+    *splits = pt.splits;
+    *split0_ktiles = pt.long_k;
+    return SDT_OK;
 }
 
 int sdt_num_tiles(void) { return kNumTiles; }

@@ -55,12 +55,16 @@ struct GemmArgs {
     int splits;
     int k_per_split;
     int splitk_reduce_in_kernel;  // 1: the last CTA of a tile sums the partials and writes C
-    float *partials;      // [splits][num_m_tiles*BM][num_n_tiles*BN] fp32
-    unsigned *counters;   // [num_m_tiles * num_n_tiles], zero between calls
-    // two-CTA tiles: work items [0, tail_start) are whole tiles, items
-    // [tail_start, num_items) are column halves of tiles tail_start ... (two per tile)
+    float *partials;      // [splits][num_m_tiles*BM][num_n_tiles*BN] fp32 (two-CTA tail: one slot per item)
+    unsigned *counters;   // [num_m_tiles * num_n_tiles], zero between calls (two-CTA tail: 8 per tile)
+    // two-CTA tiles: work items [0, tail_start) are whole tiles; items
+    // [tail_start, num_items) cover tiles tail_start ...: two column halves per tile
+    // (tail_splits == 0), or tail_splits k-ranges per tile whose fp32 partials go to
+    // `partials` and are counted on `counters` (tail_splits >= 2)
     int tail_start;
     int num_items;
+    int tail_splits;
+    int tail_long;          // k-split tail: k-tiles of split 0 (the others share the rest evenly); 0: all even
     int ldc;                // row stride of C in elements
     uint32_t idesc_flags;   // instruction-descriptor bits: accumulator, operand types, operand majors
     int c_trans;            // 1: element (r, c) of this problem is C[c * ldc + r] (operands swapped)

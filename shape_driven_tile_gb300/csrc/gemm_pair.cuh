@@ -16,6 +16,11 @@
 //     arrive on the leader's "acc_empty" barrier.
 // Everything else (tile walk, ring, epilogue, bounded waits) follows
 // gemm_persistent.cuh.
+//
+// The last round of a launch whose tiles do not fill every pair runs in one of two
+// forms, both planned on the host: each leftover tile as two half-width items, or,
+// given a workspace, each leftover tile as S full-width items over consecutive
+// k-ranges whose fp32 partials are summed by the last of them to finish (below).
 #pragma once
 
 #include <cuda_fp16.h>
@@ -59,16 +64,38 @@ struct PairCfg {
     static_assert(ACC_BUFS * BN <= TMEM_COLS && TMEM_COLS <= 512, "two accumulators must fit in TMEM");
 };
 
-// Work item -> output tile, column offset and width.  When the last round of whole
-// tiles would leave at least half of the pairs idle, the host makes each of those
-// tail tiles two half-width items instead, so the tail takes half a round.
+// Work item -> output tile, column offset, width and k-range.  Items [0, tail_start)
+// are whole tiles over all k-tiles.  The items after them cover the tiles left for a
+// last, partly empty round: with p.tail_splits == 0 two half-width items per tile;
+// with p.tail_splits = S >= 2, S full-width items per tile over consecutive k-ranges
+// (split >= 0 marks such an item): split 0 takes the first p.tail_long k-tiles and
+// the other S-1 share the rest evenly (p.tail_long == 0: all S share nK evenly).
+// A longer split 0 is meant to finish last, after the others' partials are out.
 template <int BN>
 __device__ __forceinline__ void pair_item(int item, const GemmArgs &p, int &tile, int &m_tile, int &n_tile,
-                                          int &n_off, int &width) {
+                                          int &n_off, int &width, int &k0, int &kn, int &split) {
+    const int nK = p.num_k_tiles;
+    n_off = 0;
+    width = BN;
+    k0 = 0;
+    kn = nK;
+    split = -1;
     if (item < p.tail_start) {
         tile = item;
-        n_off = 0;
-        width = BN;
+    } else if (p.tail_splits > 1) {
+        const int h = item - p.tail_start;
+        split = h % p.tail_splits;
+        tile = p.tail_start + h / p.tail_splits;
+        if (p.tail_long <= 0) {
+            k0 = split * nK / p.tail_splits;
+            kn = (split + 1) * nK / p.tail_splits - k0;
+        } else if (split == 0) {
+            kn = p.tail_long;
+        } else {
+            const int rest = nK - p.tail_long, others = p.tail_splits - 1;
+            k0 = p.tail_long + (split - 1) * rest / others;
+            kn = p.tail_long + split * rest / others - k0;
+        }
     } else {
         const int h = item - p.tail_start;
         tile = p.tail_start + (h >> 1);
@@ -76,6 +103,145 @@ __device__ __forceinline__ void pair_item(int item, const GemmArgs &p, int &tile
         width = BN / 2;
     }
     tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.raster_group, m_tile, n_tile);
+}
+
+// Workspace slot of a k-split tail item's partial: item h = item - tail_start, this CTA
+// (rank) and epilogue warp q own 32 rows x BN fp32 values.  Within the slot, columns
+// [c, c+32) of lane l (row l of the warp's 32) are the eight float4 at float offsets
+// c*32 + j*128 + l*4, j = 0..7: a warp's 16-byte stores and loads each cover 512
+// contiguous bytes, and any run of whole 32-column chunks is one contiguous range.
+// Copy buffers (and mbarriers) per epilogue warp for a k-split tail's partials.
+constexpr int kTailBufs = 4;
+
+template <int BN>
+__device__ __forceinline__ float *pair_tail_slot(const GemmArgs &p, int h, uint32_t rank, int q) {
+    return p.partials + ((static_cast<size_t>(h) * 2 + rank) * 4 + static_cast<size_t>(q)) * (32 * BN);
+}
+
+// Epilogue of one k-split tail item, for one warp's 32 rows (lane = row).  A warp
+// that finds the (tile, rank, warp) counter at S-1 -- every other split has already
+// published its partial -- is the last and skips publishing its own.  Otherwise it
+// writes its partial to its slot and then counts its arrival; the one whose count
+// makes S is the last.  The last warp -- whichever split it holds -- copies the other
+// splits' slots into the (now idle) operand ring with bulk copies, adds the splits in
+// split order (its own from TMEM), writes C and zeroes the counter.  No warp waits
+// for another one, and the sum does not depend on the order of arrival.
+// Returns false when the bulk copies did not complete in time (or could not fit).
+template <int BN>
+__device__ __forceinline__ bool pair_tail_epilogue(const GemmArgs &p, const CUtensorMap *tmC, uint32_t taddr,
+                                                   uint32_t stage_smem, uint32_t stage_bytes, uint32_t red_bar,
+                                                   int h, int split, uint32_t rank, int q, int lane, int x0,
+                                                   int row0, bool bf16, uint32_t cbuf, int &nst,
+                                                   uint32_t &red_phase, uint64_t lim) {
+    const int S = p.tail_splits;
+    const int tt = h / S;  // leftover tile
+    unsigned *ctr = p.counters + (static_cast<size_t>(tt) * 2 + rank) * 4 + static_cast<size_t>(q);
+    unsigned last = 0;
+    if (lane == 0) {
+        unsigned seen;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(seen) : "l"(ctr) : "memory");
+        last = seen + 1u == static_cast<unsigned>(S) ? 1u : 0u;
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) {
+        float *mine = pair_tail_slot<BN>(p, h, rank, q);
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + c, r);
+            tmem_ld_wait();
+            float4 *dst = reinterpret_cast<float4 *>(mine + c * 32) + lane;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                __stcg(dst + 32 * j, make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])));
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) last = atomicAdd(ctr, 1u) + 1u == static_cast<unsigned>(S) ? 1u : 0u;
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (!last) return true;
+    }
+    __threadfence();
+    if (lane == 0) *ctr = 0u;  // every split has arrived: ready for the next launch
+    asm volatile("fence.proxy.async.global;" ::: "memory");  // the other splits' stores, for the bulk copies
+    // The other splits' slots come in through a ring of buffers in this warp's quarter of
+    // the operand ring, 64 columns (32 KB / 4 of a 256-wide slot) at a time, one mbarrier
+    // per buffer: the sums of one group overlap the copies of the next ones.
+    const int others = S - 1;
+    constexpr uint32_t kGroupBytes = 64u * 128u;  // 64 columns x 32 rows of fp32
+    const uint32_t buf_bytes = static_cast<uint32_t>(others) * kGroupBytes;
+    int nbuf = static_cast<int>(stage_bytes / buf_bytes);
+    nbuf = nbuf > kTailBufs ? kTailBufs : nbuf;
+    if (nbuf < 1) return false;  // the host plans no split count whose copies do not fit
+    constexpr int kGroups = (BN + 63) / 64;
+    auto issue = [&](int g) {  // lane 0: the copies of group g into buffer g % nbuf
+        const int b = g % nbuf;
+        const int cols = BN - 64 * g < 64 ? BN - 64 * g : 64;
+        const uint32_t bytes = static_cast<uint32_t>(cols) * 128u;
+        mbar_arrive_expect_tx(red_bar + 8u * b, bytes * static_cast<uint32_t>(others));
+        int o = 0;
+        for (int s2 = 0; s2 < S; ++s2) {
+            if (s2 == split) continue;
+            const float *src = pair_tail_slot<BN>(p, tt * S + s2, rank, q) + 64 * 32 * g;
+            bulk_load(stage_smem + static_cast<uint32_t>(b) * buf_bytes + static_cast<uint32_t>(o++) * kGroupBytes,
+                      src, bytes, red_bar + 8u * b);
+        }
+    };
+    if (lane == 0)
+        for (int g = 0; g < nbuf && g < kGroups; ++g) issue(g);
+#pragma unroll 1
+    for (int g = 0; g < kGroups; ++g) {
+        const int b = g % nbuf;
+        if (!warp_wait(red_bar + 8u * b, (red_phase >> b) & 1u, lim, lane)) return false;
+        red_phase ^= 1u << b;
+        const uint32_t buf = stage_smem + static_cast<uint32_t>(b) * buf_bytes + static_cast<uint32_t>(lane) * 16u;
+        const int cols = BN - 64 * g < 64 ? BN - 64 * g : 64;
+#pragma unroll 1
+        for (int cc = 0; cc < cols; cc += 32) {
+            const int c = 64 * g + cc;
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + c, r);
+            tmem_ld_wait();
+            // the S terms in split order: this warp's own (r) at position `split`
+            float acc[32];
+            int o = 0;
+            auto add_other = [&](bool first) {
+                const uint32_t src = buf + static_cast<uint32_t>(o++) * kGroupBytes + static_cast<uint32_t>(cc) * 128u;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    float4 v;
+                    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                                 : "r"(src + static_cast<uint32_t>(j) * 512u));
+                    if (first) {
+                        acc[4 * j] = v.x; acc[4 * j + 1] = v.y; acc[4 * j + 2] = v.z; acc[4 * j + 3] = v.w;
+                    } else {
+                        acc[4 * j] += v.x; acc[4 * j + 1] += v.y; acc[4 * j + 2] += v.z; acc[4 * j + 3] += v.w;
+                    }
+                }
+            };
+            if (split == 0) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) acc[e] = __uint_as_float(r[e]);
+            } else {
+                add_other(true);
+                for (int s2 = 1; s2 < split; ++s2) add_other(false);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) acc[e] += __uint_as_float(r[e]);
+            }
+            for (int s2 = split + 1; s2 < S; ++s2) add_other(false);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(acc[e]);
+            store_chunk_tma(tmC, cbuf, nst++, r, bf16, x0 + c, row0, lane);
+        }
+        __syncwarp();  // every lane has read buffer b
+        if (lane == 0 && g + nbuf < kGroups) {
+            fence_proxy_async_smem();  // those shared-memory reads, before the copies overwrite them
+            issue(g + nbuf);
+        }
+    }
+    return true;
 }
 
 template <int BN, int LAYOUT>
@@ -98,7 +264,8 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t *acc_full = bars + 2 * S;
     uint64_t *acc_empty = bars + 2 * S + 2;
     uint64_t *mma_done = bars + 2 * S + 4;
-    volatile uint32_t *ctrl = reinterpret_cast<volatile uint32_t *>(bars + 2 * S + 5);
+    uint64_t *red_bar = bars + 2 * S + 5;  // kTailBufs per epilogue warp: bulk copies of a k-split tail's partials
+    volatile uint32_t *ctrl = reinterpret_cast<volatile uint32_t *>(bars + 2 * S + 5 + Cfg::EPI_WARPS * kTailBufs);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -120,6 +287,7 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(smem_u32(&acc_empty[b]), 2 * Cfg::EPI_WARPS);
         }
         mbar_init(smem_u32(mma_done), 1);
+        for (int w = 0; w < Cfg::EPI_WARPS * kTailBufs; ++w) mbar_init(smem_u32(&red_bar[w]), 1);
         ctrl[1] = 0;
         ctrl[2] = 0;
         fence_mbar_init();
@@ -149,8 +317,8 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t full0_leader = mapa_shared(full0, 0);
             const uint32_t smA0 = smem_u32(smA), smB0 = smem_u32(smB);
             for (int item = pair; item < num_items && !stop; item += num_pairs) {
-                int tile, m_tile, n_tile, n_off, width;
-                pair_item<BN>(item, p, tile, m_tile, n_tile, n_off, width);
+                int tile, m_tile, n_tile, n_off, width, k0, kn, split;
+                pair_item<BN>(item, p, tile, m_tile, n_tile, n_off, width, k0, kn, split);
                 const int m0 = m_tile * Cfg::BM + static_cast<int>(rank) * Cfg::CTA_M;
                 const int nb = n_tile * BN + n_off + static_cast<int>(rank) * (width / 2);
                 const bool whole = width == BN;  // whole tile, else a tail half (BN/4 B rows per CTA)
@@ -167,7 +335,7 @@ __global__ void __launch_bounds__(192, 1)
 // (the k-loops of the producer and MMA threads are unrolled by four: these single
 // threads set the pace of a k-tile, and the unrolled loop issues fewer instructions)
 #pragma unroll 4
-                for (int i = 0; i < nK; ++i) {
+                for (int i = 0; i < kn; ++i) {
                     if (!mbar_wait_for(empty0 + 8u * s, phase ^ 1u, lim)) {
                         record_status(p.status, kSiteProducer | static_cast<int>(rank << 4) | (issued << 8));
                         ctrl[1] = 1;
@@ -175,7 +343,7 @@ __global__ void __launch_bounds__(192, 1)
                         break;
                     }
                     if ((i & 7) == 0 && ctrl[1]) { stop = true; break; }  // another role gave up
-                    const int kt = p.stagger ? ((start + i) & (nK - 1)) : i;
+                    const int kt = (p.stagger && split < 0) ? ((start + i) & (nK - 1)) : k0 + i;
                     if (leader) mbar_arrive_expect_tx(full0 + 8u * s, pair_bytes);
                     const uint32_t fb = full0_leader + 8u * s;
                     const uint32_t dA = smA0 + static_cast<uint32_t>(s) * Cfg::A_BYTES;
@@ -211,7 +379,9 @@ __global__ void __launch_bounds__(192, 1)
             const uint64_t b_desc0 = operand_desc<L::B_MN>(smem_u32(smB));
             const uint32_t full0 = smem_u32(&full[0]), empty0 = smem_u32(&empty[0]);
             for (int item = pair; item < num_items && !stop; item += num_pairs, ++j) {
-                const uint32_t idesc = item < p.tail_start ? idesc_full : idesc_half;
+                const uint32_t idesc = (item < p.tail_start || p.tail_splits > 1) ? idesc_full : idesc_half;
+                int tile, m_tile, n_tile, n_off, width, k0, kn, split;
+                pair_item<BN>(item, p, tile, m_tile, n_tile, n_off, width, k0, kn, split);
                 const int b = j & 1;
                 const uint32_t acc_phase = static_cast<uint32_t>((j >> 1) & 1);
                 if (!mbar_wait_cluster_for(smem_u32(&acc_empty[b]), acc_phase ^ 1u, lim)) {
@@ -222,7 +392,7 @@ __global__ void __launch_bounds__(192, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
 #pragma unroll 4
-                for (int i = 0; i < nK; ++i) {
+                for (int i = 0; i < kn; ++i) {
                     if (!mbar_wait_for(full0 + 8u * s, phase, lim)) {
                         record_status(p.status, kSiteMma | (((j << 12) | i) << 8));
                         ctrl[1] = 1;
@@ -249,6 +419,11 @@ __global__ void __launch_bounds__(192, 1)
         const int q = warp & 3;
         const uint32_t cbuf = smem_u32(smC) + static_cast<uint32_t>(q) * 2u * kCStageBytes;
         int nst = 0;  // TMA stores this warp has issued (staging buffer parity)
+        uint32_t red_phase = 0;
+        // this warp's quarter of the operand ring, which a k-split tail item (always its
+        // pair's last item) reuses once its own MMAs have completed
+        const uint32_t ring_quarter = (static_cast<uint32_t>(S) * Cfg::STAGE_BYTES / Cfg::EPI_WARPS) & ~1023u;
+        const uint32_t stage_smem = smem_u32(smA) + static_cast<uint32_t>(q) * ring_quarter;
         int j = 0;
         for (int item = pair; item < num_items; item += num_pairs, ++j) {
             const int b = j & 1;
@@ -261,13 +436,30 @@ __global__ void __launch_bounds__(192, 1)
                 break;
             }
             tc_fence_after();
-            int tile, m_tile, n_tile, n_off, width;
-            pair_item<BN>(item, p, tile, m_tile, n_tile, n_off, width);
+            int tile, m_tile, n_tile, n_off, width, k0, kn, split;
+            pair_item<BN>(item, p, tile, m_tile, n_tile, n_off, width, k0, kn, split);
             const int row0 = m_tile * Cfg::BM + static_cast<int>(rank) * Cfg::CTA_M + q * 32;  // this warp's rows
             const int n0 = n_tile * BN + n_off;
             const bool bf16 = ((p.idesc_flags >> 7) & 7u) == 1u;
             const uint32_t taddr =
                 tmem_base + static_cast<uint32_t>(b * BN) + (static_cast<uint32_t>(q * 32) << 16);
+            if (split >= 0) {
+                const bool ok = pair_tail_epilogue<BN>(p, &tmC, taddr, stage_smem, ring_quarter,
+                                                       smem_u32(&red_bar[q * kTailBufs]), item - p.tail_start, split, rank, q,
+                                                       lane, n0, row0, bf16, cbuf, nst, red_phase, lim);
+                // the accumulator was read for the last time: hand it back
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[b]), 0));
+                    if (!ok) {
+                        record_status(p.status, kSiteEpilogue | 0x40 | static_cast<int>(rank << 4) | (j << 8));
+                        ctrl[1] = 1;
+                    }
+                }
+                if (!ok) break;
+                continue;
+            }
 #pragma unroll 1
             for (int c = 0; c < width; c += 32) {
                 uint32_t r[32];
