@@ -86,10 +86,12 @@ template <int BN, int LAYOUT>
 int launch_gemm_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC, const GemmArgs &args,
                      cudaStream_t stream) {
     using Cfg = PairCfg<BN>;
-    auto kern = gemm_f16_pair_kernel<BN, LAYOUT>;
+    // the form with the k-split last round only when the plan splits it
+    const bool ksplit = args.tail_splits >= 2;
+    auto kern = ksplit ? gemm_f16_pair_kernel<BN, LAYOUT, true> : gemm_f16_pair_kernel<BN, LAYOUT, false>;
     const int smem = Cfg::smem_bytes(args.stages);
-    static std::atomic<int> configured[64];
-    if (int e = ensure_smem(kern, smem, configured)) return e;
+    static std::atomic<int> configured[2][64];
+    if (int e = ensure_smem(kern, smem, configured[ksplit ? 1 : 0])) return e;
     const long long items = args.num_items;
     const long long pairs_cap = args.max_ctas / 2 > 0 ? args.max_ctas / 2 : 1;
     const unsigned pairs = static_cast<unsigned>(items < pairs_cap ? items : pairs_cap);

@@ -71,7 +71,7 @@ struct PairCfg {
 // (split >= 0 marks such an item): split 0 takes the first p.tail_long k-tiles and
 // the other S-1 share the rest evenly (p.tail_long == 0: all S share nK evenly).
 // A longer split 0 is meant to finish last, after the others' partials are out.
-template <int BN>
+template <int BN, bool KSPLIT>
 __device__ __forceinline__ void pair_item(int item, const GemmArgs &p, int &tile, int &m_tile, int &n_tile,
                                           int &n_off, int &width, int &k0, int &kn, int &split) {
     const int nK = p.num_k_tiles;
@@ -82,7 +82,7 @@ __device__ __forceinline__ void pair_item(int item, const GemmArgs &p, int &tile
     split = -1;
     if (item < p.tail_start) {
         tile = item;
-    } else if (p.tail_splits > 1) {
+    } else if (KSPLIT) {
         const int h = item - p.tail_start;
         split = h % p.tail_splits;
         tile = p.tail_start + h / p.tail_splits;
@@ -244,7 +244,9 @@ __device__ __forceinline__ bool pair_tail_epilogue(const GemmArgs &p, const CUte
     return true;
 }
 
-template <int BN, int LAYOUT>
+// KSPLIT: the launch's last round is split in K (p.tail_splits >= 2); the other form
+// of the kernel has none of that code.
+template <int BN, int LAYOUT, bool KSPLIT>
 __global__ void __launch_bounds__(192, 1)
     gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmC, const GemmArgs p) {
@@ -264,8 +266,10 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t *acc_full = bars + 2 * S;
     uint64_t *acc_empty = bars + 2 * S + 2;
     uint64_t *mma_done = bars + 2 * S + 4;
-    uint64_t *red_bar = bars + 2 * S + 5;  // kTailBufs per epilogue warp: bulk copies of a k-split tail's partials
-    volatile uint32_t *ctrl = reinterpret_cast<volatile uint32_t *>(bars + 2 * S + 5 + Cfg::EPI_WARPS * kTailBufs);
+    // kTailBufs per epilogue warp: bulk copies of a k-split tail's partials
+    constexpr int kRedBars = KSPLIT ? Cfg::EPI_WARPS * kTailBufs : 0;
+    uint64_t *red_bar = bars + 2 * S + 5;
+    volatile uint32_t *ctrl = reinterpret_cast<volatile uint32_t *>(bars + 2 * S + 5 + kRedBars);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -287,7 +291,7 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(smem_u32(&acc_empty[b]), 2 * Cfg::EPI_WARPS);
         }
         mbar_init(smem_u32(mma_done), 1);
-        for (int w = 0; w < Cfg::EPI_WARPS * kTailBufs; ++w) mbar_init(smem_u32(&red_bar[w]), 1);
+        for (int w = 0; w < kRedBars; ++w) mbar_init(smem_u32(&red_bar[w]), 1);
         ctrl[1] = 0;
         ctrl[2] = 0;
         fence_mbar_init();
@@ -318,7 +322,7 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t smA0 = smem_u32(smA), smB0 = smem_u32(smB);
             for (int item = pair; item < num_items && !stop; item += num_pairs) {
                 int tile, m_tile, n_tile, n_off, width, k0, kn, split;
-                pair_item<BN>(item, p, tile, m_tile, n_tile, n_off, width, k0, kn, split);
+                pair_item<BN, KSPLIT>(item, p, tile, m_tile, n_tile, n_off, width, k0, kn, split);
                 const int m0 = m_tile * Cfg::BM + static_cast<int>(rank) * Cfg::CTA_M;
                 const int nb = n_tile * BN + n_off + static_cast<int>(rank) * (width / 2);
                 const bool whole = width == BN;  // whole tile, else a tail half (BN/4 B rows per CTA)
@@ -379,9 +383,9 @@ __global__ void __launch_bounds__(192, 1)
             const uint64_t b_desc0 = operand_desc<L::B_MN>(smem_u32(smB));
             const uint32_t full0 = smem_u32(&full[0]), empty0 = smem_u32(&empty[0]);
             for (int item = pair; item < num_items && !stop; item += num_pairs, ++j) {
-                const uint32_t idesc = (item < p.tail_start || p.tail_splits > 1) ? idesc_full : idesc_half;
+                const uint32_t idesc = (item < p.tail_start || KSPLIT) ? idesc_full : idesc_half;
                 int tile, m_tile, n_tile, n_off, width, k0, kn, split;
-                pair_item<BN>(item, p, tile, m_tile, n_tile, n_off, width, k0, kn, split);
+                pair_item<BN, KSPLIT>(item, p, tile, m_tile, n_tile, n_off, width, k0, kn, split);
                 const int b = j & 1;
                 const uint32_t acc_phase = static_cast<uint32_t>((j >> 1) & 1);
                 if (!mbar_wait_cluster_for(smem_u32(&acc_empty[b]), acc_phase ^ 1u, lim)) {
@@ -437,28 +441,31 @@ __global__ void __launch_bounds__(192, 1)
             }
             tc_fence_after();
             int tile, m_tile, n_tile, n_off, width, k0, kn, split;
-            pair_item<BN>(item, p, tile, m_tile, n_tile, n_off, width, k0, kn, split);
+            pair_item<BN, KSPLIT>(item, p, tile, m_tile, n_tile, n_off, width, k0, kn, split);
             const int row0 = m_tile * Cfg::BM + static_cast<int>(rank) * Cfg::CTA_M + q * 32;  // this warp's rows
             const int n0 = n_tile * BN + n_off;
             const bool bf16 = ((p.idesc_flags >> 7) & 7u) == 1u;
             const uint32_t taddr =
                 tmem_base + static_cast<uint32_t>(b * BN) + (static_cast<uint32_t>(q * 32) << 16);
-            if (split >= 0) {
-                const bool ok = pair_tail_epilogue<BN>(p, &tmC, taddr, stage_smem, ring_quarter,
-                                                       smem_u32(&red_bar[q * kTailBufs]), item - p.tail_start, split, rank, q,
-                                                       lane, n0, row0, bf16, cbuf, nst, red_phase, lim);
-                // the accumulator was read for the last time: hand it back
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[b]), 0));
-                    if (!ok) {
-                        record_status(p.status, kSiteEpilogue | 0x40 | static_cast<int>(rank << 4) | (j << 8));
-                        ctrl[1] = 1;
+            if constexpr (KSPLIT) {
+                if (split >= 0) {
+                    const bool ok = pair_tail_epilogue<BN>(p, &tmC, taddr, stage_smem, ring_quarter,
+                                                           smem_u32(&red_bar[q * kTailBufs]), item - p.tail_start,
+                                                           split, rank, q, lane, n0, row0, bf16, cbuf, nst,
+                                                           red_phase, lim);
+                    // the accumulator was read for the last time: hand it back
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[b]), 0));
+                        if (!ok) {
+                            record_status(p.status, kSiteEpilogue | 0x40 | static_cast<int>(rank << 4) | (j << 8));
+                            ctrl[1] = 1;
+                        }
                     }
+                    if (!ok) break;
+                    continue;
                 }
-                if (!ok) break;
-                continue;
             }
 #pragma unroll 1
             for (int c = 0; c < width; c += 32) {
