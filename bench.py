@@ -342,6 +342,15 @@ def cpu_baseline_leg(host_inputs, gpu_outputs, budget_flops, check=True):
                 gate_ok = False
     baseline = {"value": flops / seconds / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                 "sample": "; ".join(parts) + f" ({flops / 1e9:.1f} GFLOP, {seconds:.1f} s, fp64 C oracle)"}
+    # the same oracle on one thread, on 32 evenly spaced rows of the 2048^3 product
+    n1 = 2048 if 2048 in host_inputs else max(k for k in host_inputs if isinstance(k, int))
+    A, B = host_inputs[n1]
+    sel = np.linspace(0, n1 - 1, 32).round().astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.gemm(_u16(A), _u16(B), rows=sel, threads=1)
+    t1 = time.perf_counter() - t0
+    baseline["one_thread"] = {"value": gemm_flops(32, n1, n1) / t1 / 1e12, "unit": "TFLOP/s",
+                              "sample": f"{n1}^3: 32 rows ({gemm_flops(32, n1, n1) / 1e9:.2f} GFLOP, {t1:.2f} s)"}
     gate = {"passed": gate_ok, "worst_err_over_bound": worst} if check else None
     return baseline, gate
 

@@ -202,3 +202,26 @@ def test_reference_arm_prints_the_contract_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_cpu_baseline_leg_reports_all_threads_and_one(monkeypatch):
+    # small sweep sizes stand in for the real ones: the leg's bookkeeping, not its scale
+    import torch
+
+    import bench
+    from shape_driven_tile_gb300 import inputs
+
+    monkeypatch.setattr(bench, "SWEEP", [64, 128])
+    monkeypatch.setattr(bench, "DEC_K", 64)
+    monkeypatch.setattr(bench, "DEC_N", 32)
+    host = {n: (inputs.uniform((n, n), seed=3 * n), inputs.uniform((n, n), seed=3 * n + 1)) for n in (64, 128)}
+    x = inputs.uniform((64,), seed=5, dtype=torch.bfloat16)
+    W = inputs.uniform((32, 64), seed=6, dtype=torch.bfloat16)
+    q, s = inputs.q8_weights(32, 64, seed=7)
+    host["dec_bf16"] = (x, W)
+    host["dec_q8"] = (x, q, s)
+    base, gate = bench.cpu_baseline_leg(host, None, budget_flops=1e6, check=False)
+    assert gate is None
+    assert base["kind"] == "oracle" and base["cores"] >= 1 and base["value"] > 0
+    one = base["one_thread"]
+    assert one["value"] > 0 and one["sample"].startswith("128^3: 32 rows")
