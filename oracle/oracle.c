@@ -170,8 +170,9 @@ int sdt_oracle_gemm_rows_t(int64_t M, int64_t N, int64_t K,
     for (int64_t t = 0; t < K * N; ++t) Bd[t] = sdt_oracle_decode(B[t], dtype);
     int bad = 0;
 #ifdef _OPENMP
-    if (threads > 0) omp_set_num_threads(threads);
-#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    /* the count applies to this loop only (no process-wide setting is changed) */
+    const int nt = threads > 0 ? threads : omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad) num_threads(nt)
 #endif
     for (int64_t r = 0; r < n_rows; ++r) {
         int64_t i = rows ? rows[r] : r;
@@ -215,8 +216,8 @@ int sdt_oracle_gemv_bf16(int64_t K, int64_t N, const uint16_t *x,
     if (!xd) return -1;
     for (int64_t k = 0; k < K; ++k) xd[k] = sdt_oracle_bf16_to_f64(x[k]);
 #ifdef _OPENMP
-    if (threads > 0) omp_set_num_threads(threads);
-#pragma omp parallel for schedule(static)
+    const int nt = threads > 0 ? threads : omp_get_max_threads();
+#pragma omp parallel for schedule(static) num_threads(nt)
 #endif
     for (int64_t n = 0; n < N; ++n) {
         double acc = 0.0;
@@ -241,8 +242,8 @@ int sdt_oracle_gemv_q8(int64_t K, int64_t N, const uint16_t *x,
     for (int64_t k = 0; k < K; ++k) xd[k] = sdt_oracle_bf16_to_f64(x[k]);
     const int64_t n_groups = K / G;
 #ifdef _OPENMP
-    if (threads > 0) omp_set_num_threads(threads);
-#pragma omp parallel for schedule(static)
+    const int nt = threads > 0 ? threads : omp_get_max_threads();
+#pragma omp parallel for schedule(static) num_threads(nt)
 #endif
     for (int64_t n = 0; n < N; ++n) {
         double acc = 0.0;

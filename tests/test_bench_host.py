@@ -220,8 +220,15 @@ def test_cpu_baseline_leg_reports_all_threads_and_one(monkeypatch):
     q, s = inputs.q8_weights(32, 64, seed=7)
     host["dec_bf16"] = (x, W)
     host["dec_q8"] = (x, q, s)
+    import oracle
+
+    before = oracle.max_threads()
     base, gate = bench.cpu_baseline_leg(host, None, budget_flops=1e6, check=False)
     assert gate is None
-    assert base["kind"] == "oracle" and base["cores"] >= 1 and base["value"] > 0
+    assert base["kind"] == "oracle" and base["cores"] == before and base["value"] > 0
     one = base["one_thread"]
     assert one["value"] > 0 and one["sample"].startswith("128^3: 32 rows")
+    # the one-thread figure leaves the oracle's thread count as it was: a second leg (the
+    # benchmark runs a calibration leg first) still uses every thread
+    assert oracle.max_threads() == before
+    assert bench.cpu_baseline_leg(host, None, budget_flops=1e6, check=False)[0]["cores"] == before
