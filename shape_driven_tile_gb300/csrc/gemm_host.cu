@@ -616,18 +616,19 @@ static constexpr size_t kCounterRegionBytes = size_t(1) << 20;
 // The estimate of each form's last round uses GB300 timings of the 256 x 256 pair
 // kernel at 4096^3 (globaltimer stamps): a whole-width k-tile 0.297 us, a half-width
 // one 0.25 us; from the last MMA issue to the stores' completion 2.4 us for a plain
-// epilogue and 9.7 us for the summing split (its copies of the other partial 2.9 us,
-// the sums and stores 0.5 us per 32 columns; one more partial adds 2.5 us); a split's
-// partial is out and counted 5.0 us after its last MMA issue.  So half-width items win
-// up to nK ~ 100 (4096^3) and the split from there (8192^3: 31.4 against 34.4 us).
+// epilogue and, for the summing split, 6.5 us with two splits (it reads the other
+// partial straight from L2) or 9.7 us + 2.5 us per split beyond two (it copies the
+// others through shared memory); a split's partial is out and counted 5.0 us after its
+// last MMA issue.  So half-width items win up to nK ~ 100 (4096^3: 18.4 against 18.7
+// us) and the split from there (8192^3: 28.2 against 34.4 us).
 // The cheapest form is planned; `req` forces the k-split count (>= 2) or disables it (0).
 struct PairTail {
     int tail_start, num_items, splits, long_k;
 };
 
 static constexpr int kPairTailMaxSplits = 8;
-static constexpr double kTailKt = 0.297, kTailHalfKt = 0.25, kTailEpi = 2.4, kTailReduce = 9.7,
-                        kTailReduceExtra = 2.5, kTailPublish = 5.0;
+static constexpr double kTailKt = 0.297, kTailHalfKt = 0.25, kTailEpi = 2.4, kTailReduce2 = 6.5,
+                        kTailReduceN = 9.7, kTailReduceExtra = 2.5, kTailPublish = 5.0;
 
 // The largest k-split count for L leftover tiles: L*S <= P, S <= nK, and the other
 // S-1 partials of a 64-column group must fit in an epilogue warp's quarter of the ring.
@@ -664,7 +665,8 @@ static PairTail pair_tail_plan(const LadderTile &t, int tiles, int nK, int pairs
         form = std::min(req, smax);
     } else if (req != 0) {
         for (int sp = 2; sp <= smax; ++sp) {
-            const double c = pair_tail_long(nK, sp) * kTailKt + kTailReduce + kTailReduceExtra * (sp - 2);
+            const double c = pair_tail_long(nK, sp) * kTailKt +
+                             (sp == 2 ? kTailReduce2 : kTailReduceN + kTailReduceExtra * (sp - 2));
             if (c < best) {
                 best = c;
                 form = sp;

@@ -110,8 +110,10 @@ __device__ __forceinline__ void pair_item(int item, const GemmArgs &p, int &tile
 // [c, c+32) of lane l (row l of the warp's 32) are the eight float4 at float offsets
 // c*32 + j*128 + l*4, j = 0..7: a warp's 16-byte stores and loads each cover 512
 // contiguous bytes, and any run of whole 32-column chunks is one contiguous range.
-// Copy buffers (and mbarriers) per epilogue warp for a k-split tail's partials.
+// Copy buffers (and mbarriers) per epilogue warp for a k-split tail's partials (S >= 3),
+// and the 32-column chunks of the other partial a warp keeps in flight when S == 2.
 constexpr int kTailBufs = 4;
+constexpr int kTailAhead = 3;
 
 template <int BN>
 __device__ __forceinline__ float *pair_tail_slot(const GemmArgs &p, int h, uint32_t rank, int q) {
@@ -122,9 +124,10 @@ __device__ __forceinline__ float *pair_tail_slot(const GemmArgs &p, int h, uint3
 // that finds the (tile, rank, warp) counter at S-1 -- every other split has already
 // published its partial -- is the last and skips publishing its own.  Otherwise it
 // writes its partial to its slot and then counts its arrival; the one whose count
-// makes S is the last.  The last warp -- whichever split it holds -- copies the other
-// splits' slots into the (now idle) operand ring with bulk copies, adds the splits in
-// split order (its own from TMEM), writes C and zeroes the counter.  No warp waits
+// makes S is the last.  The last warp -- whichever split it holds -- adds the splits in
+// split order (its own from TMEM; with two splits it reads the other's slot straight
+// from L2, with more it copies the other slots into the (now idle) operand ring with
+// bulk copies), writes C and zeroes the counter.  No warp waits
 // for another one, and the sum does not depend on the order of arrival.
 // Returns false when the bulk copies did not complete in time (or could not fit).
 template <int BN>
@@ -164,6 +167,39 @@ __device__ __forceinline__ bool pair_tail_epilogue(const GemmArgs &p, const CUte
     }
     __threadfence();
     if (lane == 0) *ctr = 0u;  // every split has arrived: ready for the next launch
+    if (S == 2) {
+        // One other partial: read it straight from L2, kTailAhead chunks ahead of the
+        // sums (the loop is unrolled, so the in-flight chunks stay in registers), and add
+        // it to this warp's own accumulator; own + other is the same sum whichever split
+        // this warp holds.
+        constexpr int kChunks = BN / 32;
+        const float4 *oth = reinterpret_cast<const float4 *>(pair_tail_slot<BN>(p, tt * 2 + (split ^ 1), rank, q)) + lane;
+        float4 ahead[kTailAhead][8];
+#pragma unroll
+        for (int d = 0; d < kTailAhead && d < kChunks; ++d)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) ahead[d][j] = __ldcg(oth + d * 256 + 32 * j);
+#pragma unroll
+        for (int ci = 0; ci < kChunks; ++ci) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + 32 * ci, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float4 o = ahead[ci % kTailAhead][j];
+                r[4 * j] = __float_as_uint(__uint_as_float(r[4 * j]) + o.x);
+                r[4 * j + 1] = __float_as_uint(__uint_as_float(r[4 * j + 1]) + o.y);
+                r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + o.z);
+                r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + o.w);
+            }
+            if (ci + kTailAhead < kChunks) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) ahead[ci % kTailAhead][j] = __ldcg(oth + (ci + kTailAhead) * 256 + 32 * j);
+            }
+            store_chunk_tma(tmC, cbuf, nst++, r, bf16, x0 + 32 * ci, row0, lane);
+        }
+        return true;
+    }
     asm volatile("fence.proxy.async.global;" ::: "memory");  // the other splits' stores, for the bulk copies
     // The other splits' slots come in through a ring of buffers in this warp's quarter of
     // the operand ring, 64 columns (32 KB / 4 of a 256-wide slot) at a time, one mbarrier

@@ -29,21 +29,21 @@ def test_workspace_bytes():
 def test_hand_worked_cases():
     # 4096^3: 256 tiles on 76 pairs -> 3 whole rounds (228) and 28 left.  The estimate: half-width
     # items 64 x 0.25 + 2.4 = 18.4 us; two k-ranges, split 0 of ceil((64 + 5.0 / 0.297) / 2) = 41
-    # k-tiles: 41 x 0.297 + 9.7 = 21.9 us -> half-width items, with or without a workspace
+    # k-tiles: 41 x 0.297 + 6.5 = 18.7 us -> half-width items, with or without a workspace
     assert plan(4096, 4096, 4096) == (228, 284, 0, 0)
     assert plan(4096, 4096, 4096, workspace=False) == (228, 284, 0, 0)
     # a forced count: 76 // 28 = 2 k-ranges, split 0 of 41 k-tiles, split 1 of 23
     assert plan(4096, 4096, 4096, tail_splits=2) == (228, 284, 2, 41)
     assert plan(4096, 4096, 4096, tail_splits=8) == (228, 284, 2, 41)
     # 8192^3: 1024 tiles -> 13 rounds (988) and 36 left (2 k-ranges at most); halves 128 x 0.25 + 2.4
-    # = 34.4 us against ceil((128 + 16.8) / 2) = 73 k-tiles: 73 x 0.297 + 9.7 = 31.4 us
+    # = 34.4 us against ceil((128 + 16.8) / 2) = 73 k-tiles: 73 x 0.297 + 6.5 = 28.2 us
     assert plan(8192, 8192, 8192) == (988, 1060, 2, 73)
     assert plan(8192, 8192, 8192, tail_splits=0) == (988, 1060, 0, 0)
     # 12288^3: 2304 tiles -> 30 rounds (2280) and 24 left; three k-ranges: split 0 of
-    # ceil((192 + 2 x 16.8) / 3) = 76 k-tiles: 22.6 + 9.7 + 2.5 = 34.8 us beats two (105: 40.9 us)
-    # and half-width items (50.4 us)
+    # ceil((192 + 2 x 16.8) / 3) = 76 k-tiles: 22.6 + 9.7 + 2.5 = 34.8 us beats two (105 k-tiles:
+    # 31.2 + 6.5 = 37.7 us) and half-width items (50.4 us)
     assert plan(12288, 12288, 12288) == (2280, 2352, 3, 76)
-    # 2560^3: 100 tiles -> 76 + 24: halves 12.4 us beat two (29: 18.3) and three k-ranges
+    # 2560^3: 100 tiles -> 76 + 24: halves 12.4 us beat two (29: 15.1) and three k-ranges
     assert plan(2560, 2560, 2560) == (76, 124, 0, 0)
     # 3072^3: 144 tiles -> 76 + 68: neither halves (136 > 76) nor a split (76 // 68 = 1)
     assert plan(3072, 3072, 3072) == (144, 144, 0, 0)
