@@ -403,10 +403,9 @@ def run_default(args):
     yq = torch.empty(DEC_N, dtype=torch.float32, device=dev)
     tiles = {n: sdt.tile_info(sdt.pick_tile(n, n, n))["name"] for n in SWEEP}
     stream = torch.cuda.current_stream()
-    # The GEMMs are gemm_f16 calls; --gemm-ws on makes them gemm_f16_ws calls with one
-    # workspace (the two-CTA tiles may then split the contraction of a partly empty last
-    # round: at these sizes the plan keeps gemm_f16's form, at 8192^3 and 12288^3 of the
-    # large leg it splits).
+    # The GEMMs are gemm_f16_ws calls with one workspace: a two-CTA tile may then split the
+    # contraction of a partly empty last round (here 4096^3, and 8192^3 and 12288^3 of the
+    # large leg); --gemm-ws off makes them plain gemm_f16 calls.
     gws = sdt.gemm_workspace(dev) if args.gemm_ws == "on" else None
     # The timed loop calls the C ABI directly with the operands' device pointers, so that
     # Python-side argument checks do not leave the GPU idle between the small GEMMs.
@@ -1688,8 +1687,9 @@ def run_chain(args):
 
 
 def run_one(args):
-    """A few launches of one kernel (for profiler captures): a square GEMM with pick_tile,
-    or the decode GEMV (--gemv bf16|q8)."""
+    """A few launches of one kernel (for profiler captures): a square GEMM with pick_tile
+    (through gemm_f16_ws unless --gemm-ws off, as in the benchmark step), or the decode
+    GEMV (--gemv bf16|q8)."""
     import torch
 
     import shape_driven_tile_gb300 as sdt
@@ -1711,6 +1711,9 @@ def run_one(args):
         C = torch.empty((n, n), device=dev, dtype=torch.float16)
         if args.tile:
             fn = lambda i: sdt.gemm_f16_with_tile(A, B, C, tile=args.tile)
+        elif args.gemm_ws == "on":  # as the benchmark step calls it
+            ws = sdt.gemm_workspace(dev)
+            fn = lambda i: sdt.gemm_f16_ws(A, B, C, workspace=ws)
         else:
             fn = lambda i: sdt.gemm_f16(A, B, C)
     for i in range(args.warmup + args.reps):
@@ -1755,9 +1758,9 @@ def main(argv=None):
     ap.add_argument("--concurrent-steps", action="store_true",
                     help="default run: graph-replayed steps issue the GEMMs up to 1024^3 and the decode GEMVs on two "
                          "side streams beside the larger GEMMs (independent problems run at the same time)")
-    ap.add_argument("--gemm-ws", choices=["on", "off"], default="off",
-                    help="default run: the GEMMs as gemm_f16 calls (off) or as gemm_f16_ws calls with a workspace "
-                         "(on: a two-CTA tile may split its last round in K where the plan says it pays)")
+    ap.add_argument("--gemm-ws", choices=["on", "off"], default="on",
+                    help="default run: the GEMMs as gemm_f16_ws calls with a workspace (on: a two-CTA tile may split "
+                         "its last round in K where the plan says it pays) or as plain gemm_f16 calls (off)")
     ap.add_argument("--no-legs", action="store_true",
                     help="default run: skip the protocol legs after the timed region (gemm_protocol, pick_check, "
                          "kscan, large)")

@@ -243,8 +243,9 @@ int gemm_ex(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const v
  * its fp32 partial to the workspace and counts its arrival; the last to finish adds
  * the S partials in split order (so the result does not depend on the order of
  * arrival) and writes C.  The form is chosen per launch by a cost estimate (on GB300
- * the split pays from about 100 k-tiles, e.g. 8192^3; at 4096^3 the half-width items
- * are kept); gemm_ex_ws's tail_splits forces it: -1 estimate, 0 never split, 2..8
+ * it splits at 4096^3 and above and keeps the half-width items at 2560^3, where 40
+ * k-tiles leave too little to hide the sum); gemm_ex_ws's tail_splits forces it: -1
+ * estimate, 0 never split, 2..8
  * that count (lowered to what L*S <= P, nK and the shared memory for the partials'
  * copies allow: at most 7 with the current tiles; below 2 it is not split).
  * Every other tile, and a launch with no partial last round, runs exactly as

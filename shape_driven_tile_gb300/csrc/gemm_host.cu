@@ -14,7 +14,6 @@
 
 #include <algorithm>
 #include <cerrno>
-#include <cmath>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -614,21 +613,25 @@ static constexpr size_t kCounterRegionBytes = size_t(1) << 20;
 //           longer than the others by the time a partial takes to be published, so
 //           that it normally finishes last and sums without publishing its own.
 // The estimate of each form's last round uses GB300 timings of the 256 x 256 pair
-// kernel at 4096^3 (globaltimer stamps): a whole-width k-tile 0.297 us, a half-width
-// one 0.25 us; from the last MMA issue to the stores' completion 2.4 us for a plain
-// epilogue and, for the summing split, 6.5 us with two splits (it reads the other
-// partial straight from L2) or 9.7 us + 2.5 us per split beyond two (it copies the
-// others through shared memory); a split's partial is out and counted 5.0 us after its
-// last MMA issue.  So half-width items win up to nK ~ 100 (4096^3: 18.4 against 18.7
-// us) and the split from there (8192^3: 28.2 against 34.4 us).
+// kernel at 4096^3 (globaltimer stamps, cold L2): a k-tile of the last round takes
+// 0.297 us in whole-width items, 0.272 us in half-width ones and 0.366 us in k-split
+// items (their partials' traffic shares L2 with the operand loads); from the last MMA
+// issue to the stores' completion 2.4 us for a plain epilogue; for the summing split
+// 4.1 us with two splits (it watched the other split's count during its last k-tiles
+// and read the other partial straight from L2) or 9.7 us + 2.5 us per split beyond
+// two (it copies the others through shared memory).  Split 0 leads the others by 12
+// k-tiles, the time a partial takes to be published.  So at 4096^3 two k-ranges
+// (39 x 0.366 + 4.1 = 18.4 us) beat half-width items (64 x 0.272 + 2.4 = 19.8 us), at
+// 2560^3 they do not (13.6 against 13.3 us).
 // The cheapest form is planned; `req` forces the k-split count (>= 2) or disables it (0).
 struct PairTail {
     int tail_start, num_items, splits, long_k;
 };
 
 static constexpr int kPairTailMaxSplits = 8;
-static constexpr double kTailKt = 0.297, kTailHalfKt = 0.25, kTailEpi = 2.4, kTailReduce2 = 6.5,
-                        kTailReduceN = 9.7, kTailReduceExtra = 2.5, kTailPublish = 5.0;
+static constexpr double kTailKt = 0.297, kTailHalfKt = 0.272, kTailSplitKt = 0.366, kTailEpi = 2.4,
+                        kTailReduce2 = 4.1, kTailReduceN = 9.7, kTailReduceExtra = 2.5;
+static constexpr int kTailLead = 12;  // k-tiles by which split 0 outlasts the others
 
 // The largest k-split count for L leftover tiles: L*S <= P, S <= nK, and the other
 // S-1 partials of a 64-column group must fit in an epilogue warp's quarter of the ring.
@@ -641,10 +644,9 @@ static int pair_tail_max_splits(const LadderTile &t, int leftover, int pairs, in
 }
 
 // k-tiles of split 0 for an S-way split of nK k-tiles: the others' share plus the
-// publishing time, at most nK - (S-1) (every other split keeps at least one k-tile).
+// lead, at most nK - (S-1) (every other split keeps at least one k-tile).
 static int pair_tail_long(int nK, int S) {
-    const double lead = kTailPublish / kTailKt;
-    const int want = int(std::ceil((nK + (S - 1) * lead) / S));
+    const int want = (nK + (S - 1) * kTailLead + S - 1) / S;
     return std::max(std::min(want, nK - (S - 1)), (nK + S - 1) / S);
 }
 
@@ -665,7 +667,7 @@ static PairTail pair_tail_plan(const LadderTile &t, int tiles, int nK, int pairs
         form = std::min(req, smax);
     } else if (req != 0) {
         for (int sp = 2; sp <= smax; ++sp) {
-            const double c = pair_tail_long(nK, sp) * kTailKt +
+            const double c = pair_tail_long(nK, sp) * kTailSplitKt +
                              (sp == 2 ? kTailReduce2 : kTailReduceN + kTailReduceExtra * (sp - 2));
             if (c < best) {
                 best = c;

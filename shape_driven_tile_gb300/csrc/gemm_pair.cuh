@@ -113,7 +113,41 @@ __device__ __forceinline__ void pair_item(int item, const GemmArgs &p, int &tile
 // Copy buffers (and mbarriers) per epilogue warp for a k-split tail's partials (S >= 3),
 // and the 32-column chunks of the other partial a warp keeps in flight when S == 2.
 constexpr int kTailBufs = 4;
-constexpr int kTailAhead = 3;
+constexpr int kTailAhead = 2;
+
+// Warp-uniform bounded wait for an mbarrier phase that also watches a u32 counter in
+// global memory: 1 once the phase has completed (every lane then observes it), 2 as
+// soon as lane 0 reads `want` from the counter first (acquire; the phase may still be
+// pending), 0 when `limit_ns` passes.
+__device__ __forceinline__ int warp_wait_or_count(uint32_t bar, uint32_t parity, const unsigned *ctr, unsigned want,
+                                                  uint64_t limit_ns, int lane) {
+    int st = 0;
+    if (lane == 0) {
+        if (mbar_try_wait(bar, parity)) {
+            st = 1;
+        } else {
+            const uint64_t deadline = global_timer_ns() + limit_ns;
+            for (uint32_t polls = 1;; ++polls) {
+                if (mbar_try_wait(bar, parity)) { st = 1; break; }
+                if ((polls & 7u) == 0) {
+                    unsigned seen;
+                    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(seen) : "l"(ctr) : "memory");
+                    if (seen == want) { st = 2; break; }
+                    if (global_timer_ns() > deadline) break;
+                }
+                __nanosleep(32);
+            }
+        }
+    }
+    st = __shfl_sync(0xffffffffu, st, 0);
+    if (st == 1 && lane != 0 && !mbar_wait_for(bar, parity, limit_ns)) st = 0;
+    return __all_sync(0xffffffffu, st != 0) ? st : 0;
+}
+
+// The (tile, CTA, epilogue warp) arrival counter of k-split tail item h.
+__device__ __forceinline__ unsigned *pair_tail_counter(const GemmArgs &p, int h, uint32_t rank, int q) {
+    return p.counters + (static_cast<size_t>(h / p.tail_splits) * 2 + rank) * 4 + static_cast<size_t>(q);
+}
 
 template <int BN>
 __device__ __forceinline__ float *pair_tail_slot(const GemmArgs &p, int h, uint32_t rank, int q) {
@@ -130,22 +164,37 @@ __device__ __forceinline__ float *pair_tail_slot(const GemmArgs &p, int h, uint3
 // bulk copies), writes C and zeroes the counter.  No warp waits
 // for another one, and the sum does not depend on the order of arrival.
 // Returns false when the bulk copies did not complete in time (or could not fit).
+// ahead / peeked: with S == 2, a warp that saw the other split's count while its own
+// accumulator was still being computed has the first kTailAhead chunks of the other
+// partial in `ahead` already and is the last (peeked).
+__device__ __forceinline__ void pair_tail_load_ahead(const float4 *oth, int chunks, float4 (&ahead)[kTailAhead][8]) {
+#pragma unroll
+    for (int d = 0; d < kTailAhead; ++d)
+        if (d < chunks) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) ahead[d][j] = __ldcg(oth + d * 256 + 32 * j);
+        }
+}
+
 template <int BN>
 __device__ __forceinline__ bool pair_tail_epilogue(const GemmArgs &p, const CUtensorMap *tmC, uint32_t taddr,
                                                    uint32_t stage_smem, uint32_t stage_bytes, uint32_t red_bar,
                                                    int h, int split, uint32_t rank, int q, int lane, int x0,
                                                    int row0, bool bf16, uint32_t cbuf, int &nst,
-                                                   uint32_t &red_phase, uint64_t lim) {
+                                                   uint32_t &red_phase, uint64_t lim, bool peeked,
+                                                   float4 (&ahead)[kTailAhead][8]) {
     const int S = p.tail_splits;
     const int tt = h / S;  // leftover tile
-    unsigned *ctr = p.counters + (static_cast<size_t>(tt) * 2 + rank) * 4 + static_cast<size_t>(q);
-    unsigned last = 0;
-    if (lane == 0) {
-        unsigned seen;
-        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(seen) : "l"(ctr) : "memory");
-        last = seen + 1u == static_cast<unsigned>(S) ? 1u : 0u;
+    unsigned *ctr = pair_tail_counter(p, h, rank, q);
+    unsigned last = peeked ? 1u : 0u;
+    if (!peeked) {
+        if (lane == 0) {
+            unsigned seen;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(seen) : "l"(ctr) : "memory");
+            last = seen + 1u == static_cast<unsigned>(S) ? 1u : 0u;
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
     }
-    last = __shfl_sync(0xffffffffu, last, 0);
     if (!last) {
         float *mine = pair_tail_slot<BN>(p, h, rank, q);
 #pragma unroll 1
@@ -174,11 +223,7 @@ __device__ __forceinline__ bool pair_tail_epilogue(const GemmArgs &p, const CUte
         // this warp holds.
         constexpr int kChunks = BN / 32;
         const float4 *oth = reinterpret_cast<const float4 *>(pair_tail_slot<BN>(p, tt * 2 + (split ^ 1), rank, q)) + lane;
-        float4 ahead[kTailAhead][8];
-#pragma unroll
-        for (int d = 0; d < kTailAhead && d < kChunks; ++d)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) ahead[d][j] = __ldcg(oth + d * 256 + 32 * j);
+        if (!peeked) pair_tail_load_ahead(oth, kChunks, ahead);
 #pragma unroll
         for (int ci = 0; ci < kChunks; ++ci) {
             uint32_t r[32];
@@ -468,6 +513,25 @@ __global__ void __launch_bounds__(192, 1)
         for (int item = pair; item < num_items; item += num_pairs, ++j) {
             const int b = j & 1;
             const uint32_t acc_phase = static_cast<uint32_t>((j >> 1) & 1);
+            bool peeked = false;
+            float4 ahead[kTailAhead][8];
+            if constexpr (KSPLIT) {
+                // a two-way split item: while its accumulator is being computed, watch the
+                // other split's count, and once that split has published its partial, start
+                // loading the partial's first chunks
+                if (p.tail_splits == 2 && item >= p.tail_start) {
+                    const int h = item - p.tail_start;
+                    const int st = warp_wait_or_count(smem_u32(&acc_full[b]), acc_phase,
+                                                      pair_tail_counter(p, h, rank, q), 1u, 4 * lim, lane);
+                    if (st == 2) {
+                        peeked = true;
+                        __threadfence();
+                        const float4 *oth = reinterpret_cast<const float4 *>(
+                                                pair_tail_slot<BN>(p, h ^ 1, rank, q)) + lane;
+                        pair_tail_load_ahead(oth, BN / 32, ahead);
+                    }
+                }
+            }
             if (!warp_wait(smem_u32(&acc_full[b]), acc_phase, 4 * lim, lane)) {
                 if (lane == 0) {
                     record_status(p.status, kSiteEpilogue | static_cast<int>(rank << 4) | (j << 8));
@@ -488,7 +552,7 @@ __global__ void __launch_bounds__(192, 1)
                     const bool ok = pair_tail_epilogue<BN>(p, &tmC, taddr, stage_smem, ring_quarter,
                                                            smem_u32(&red_bar[q * kTailBufs]), item - p.tail_start,
                                                            split, rank, q, lane, n0, row0, bf16, cbuf, nst,
-                                                           red_phase, lim);
+                                                           red_phase, lim, peeked, ahead);
                     // the accumulator was read for the last time: hand it back
                     tc_fence_before();
                     __syncwarp();

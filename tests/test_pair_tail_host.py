@@ -28,32 +28,34 @@ def test_workspace_bytes():
 
 def test_hand_worked_cases():
     # 4096^3: 256 tiles on 76 pairs -> 3 whole rounds (228) and 28 left.  The estimate: half-width
-    # items 64 x 0.25 + 2.4 = 18.4 us; two k-ranges, split 0 of ceil((64 + 5.0 / 0.297) / 2) = 41
-    # k-tiles: 41 x 0.297 + 6.5 = 18.7 us -> half-width items, with or without a workspace
-    assert plan(4096, 4096, 4096) == (228, 284, 0, 0)
+    # items 64 x 0.272 + 2.4 = 19.8 us; two k-ranges (76 // 28 = 2 at most), split 0 of
+    # (64 + 12) / 2 = 38 k-tiles: 38 x 0.366 + 4.1 = 18.0 us -> two k-ranges given a workspace
+    assert plan(4096, 4096, 4096) == (228, 284, 2, 38)
     assert plan(4096, 4096, 4096, workspace=False) == (228, 284, 0, 0)
-    # a forced count: 76 // 28 = 2 k-ranges, split 0 of 41 k-tiles, split 1 of 23
-    assert plan(4096, 4096, 4096, tail_splits=2) == (228, 284, 2, 41)
-    assert plan(4096, 4096, 4096, tail_splits=8) == (228, 284, 2, 41)
-    # 8192^3: 1024 tiles -> 13 rounds (988) and 36 left (2 k-ranges at most); halves 128 x 0.25 + 2.4
-    # = 34.4 us against ceil((128 + 16.8) / 2) = 73 k-tiles: 73 x 0.297 + 6.5 = 28.2 us
-    assert plan(8192, 8192, 8192) == (988, 1060, 2, 73)
+    assert plan(4096, 4096, 4096, tail_splits=0) == (228, 284, 0, 0)
+    assert plan(4096, 4096, 4096, tail_splits=2) == (228, 284, 2, 38)
+    assert plan(4096, 4096, 4096, tail_splits=8) == (228, 284, 2, 38)
+    # 8192^3: 1024 tiles -> 13 rounds (988) and 36 left; halves 128 x 0.272 + 2.4 = 37.2 us
+    # against split 0 of 70 k-tiles: 70 x 0.366 + 4.1 = 29.7 us
+    assert plan(8192, 8192, 8192) == (988, 1060, 2, 70)
     assert plan(8192, 8192, 8192, tail_splits=0) == (988, 1060, 0, 0)
-    # 12288^3: 2304 tiles -> 30 rounds (2280) and 24 left; three k-ranges: split 0 of
-    # ceil((192 + 2 x 16.8) / 3) = 76 k-tiles: 22.6 + 9.7 + 2.5 = 34.8 us beats two (105 k-tiles:
-    # 31.2 + 6.5 = 37.7 us) and half-width items (50.4 us)
-    assert plan(12288, 12288, 12288) == (2280, 2352, 3, 76)
-    # 2560^3: 100 tiles -> 76 + 24: halves 12.4 us beat two (29: 15.1) and three k-ranges
+    # 12288^3: 2304 tiles -> 30 rounds (2280) and 24 left; three k-ranges, split 0 of
+    # (192 + 24 + 2) // 3 = 72 k-tiles: 26.4 + 9.7 + 2.5 = 38.6 us beats two (102 k-tiles:
+    # 37.3 + 4.1 = 41.4 us) and half-width items (54.6 us)
+    assert plan(12288, 12288, 12288) == (2280, 2352, 3, 72)
+    # 2560^3: 100 tiles -> 76 + 24: halves 40 x 0.272 + 2.4 = 13.3 us beat two k-ranges
+    # (26 x 0.366 + 4.1 = 13.6 us)
     assert plan(2560, 2560, 2560) == (76, 124, 0, 0)
     # 3072^3: 144 tiles -> 76 + 68: neither halves (136 > 76) nor a split (76 // 68 = 1)
     assert plan(3072, 3072, 3072) == (144, 144, 0, 0)
     # tiles that fill every pair leave no last round
     assert plan(256 * 76, 256, 4096) == (76, 76, 0, 0)
+    # a short contraction: 8 k-tiles (halves 4.6 us against 7 x 0.366 + 4.1 = 6.7 us)
+    assert plan(4096, 4096, 512) == (228, 284, 0, 0)
     # fewer tiles than pairs: all of them are in the last round.  Eight k-ranges would need
     # 7 x 8 KB of copy buffers per epilogue warp, more than its 48 KB quarter of the ring: seven
-    # (4 tiles x 7 items; split 0 at most 33 - 6 = 27 k-tiles, the other six share the rest)
-    ts, items, sp, long_k = plan(512, 512, 2112, tail_splits=8)
-    assert (ts, items, sp) == (0, 28, 7) and 5 <= long_k <= 27
+    # (4 tiles x 7 items; split 0 of (33 + 6 x 12 + 6) // 7 = 15 k-tiles, the other six share 18)
+    assert plan(512, 512, 2112, tail_splits=8) == (0, 28, 7, 15)
     assert plan(512, 512, 2112, tail_splits=5)[:3] == (0, 20, 5)
     # ... and a split count is never above the k-tile count
     assert plan(512, 512, 128, tail_splits=8) == (0, 8, 2, 1)

@@ -112,10 +112,10 @@ def test_padded_c_outside_untouched(cuda_device, ws):
     assert bool((store[:M, N:] == 7.0).all()) and bool((store[M:] == 7.0).all())
 
 
-@pytest.mark.parametrize("n,splits", [(4096, 2), (2560, 3), (8192, -1)])
+@pytest.mark.parametrize("n,splits", [(4096, -1), (2560, 3), (8192, -1)])
 def test_planned_split_square(cuda_device, ws, n, splits):
-    # 4096^3 and 2560^3 with a forced count (the estimate keeps half-width items there),
-    # 8192^3 as planned (two k-ranges per leftover tile on a 152-SM GPU)
+    # 4096^3 and 8192^3 as planned (two k-ranges per leftover tile on a 152-SM GPU), 2560^3
+    # with a forced count (the estimate keeps half-width items there)
     tile = sdt.pick_tile(n, n, n)
     assert sdt.tile_info(tile)["name"] == "2cta_256x256"
     if splits < 0 and sdt.device_sm_count() != 152:
