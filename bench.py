@@ -812,74 +812,86 @@ def last_round_note(n, tile, gws):
     return f"; last round: {(items - ts) // 2} tiles as half-width items"
 
 
+def _packed(specs, make):
+    """One buffer (make(nbytes) -> uint8 tensor) holding tensors of the given shapes and
+    dtypes at 256-byte aligned offsets; returns the buffer and a view per key."""
+    import torch
+
+    offs, total = {}, 0
+    for key, shape, dtype in specs:
+        nbytes = math.prod(shape) * torch.empty((), dtype=dtype).element_size()
+        offs[key] = (total, nbytes, shape, dtype)
+        total += (nbytes + 255) // 256 * 256
+    buf = make(total)
+    return buf, {key: buf[o:o + nb].view(dtype).view(shape) for key, (o, nb, shape, dtype) in offs.items()}
+
+
 def run_e2e(args, dev, host, Wb_h, Q_h, stream, gws=None):
     """Same metric through the public API with pinned host buffers: every step copies its
     inputs host -> device, runs the step and copies every result device -> host, all inside
-    the timed region.  The copies of neighbouring steps overlap the compute on three streams
-    (inputs of step i+1 in, step i computed, results of step i-1 out), each with two buffer
-    sets ordered by events, as a serving loop would run it."""
+    the timed region.  A step's inputs sit in one pinned staging buffer and go over in one
+    copy, its results come back in one copy, as a serving loop that batches its transfers
+    would run it; the copies of neighbouring steps overlap the compute on three streams
+    (inputs of step i+1 in, step i computed, results of step i-1 out), each with two
+    buffer sets ordered by events."""
     import torch
 
     import shape_driven_tile_gb300 as sdt
 
     steps = max(3, min(args.steps, args.e2e_steps))
-    hA = {n: host[n][0].pin_memory() for n in SWEEP}
-    hB = {n: host[n][1].pin_memory() for n in SWEEP}
-    hx = host["dec_bf16"][0].pin_memory()
-    hW = [w.pin_memory() for w in Wb_h[:2]]
-    hQ = [(q.pin_memory(), s.pin_memory()) for q, s in Q_h[:2]]
+    x_h = host["dec_bf16"][0]
+    in_specs = ([(("A", n), (n, n), torch.float16) for n in SWEEP] + [(("B", n), (n, n), torch.float16) for n in SWEEP]
+                + [("x", tuple(x_h.shape), x_h.dtype), ("W", tuple(Wb_h[0].shape), Wb_h[0].dtype),
+                   ("q", tuple(Q_h[0][0].shape), Q_h[0][0].dtype), ("s", tuple(Q_h[0][1].shape), Q_h[0][1].dtype)])
+    out_specs = [(("C", n), (n, n), torch.float16) for n in SWEEP] + [("yb", (DEC_N,), torch.float32),
+                                                                      ("yq", (DEC_N,), torch.float32)]
+    pinned = lambda nbytes: torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    on_dev = lambda nbytes: torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    # host inputs: two staging buffers (the decode weights alternate between two sets)
+    hin = []
+    for k in range(2):
+        buf, v = _packed(in_specs, pinned)
+        for n in SWEEP:
+            v[("A", n)].copy_(host[n][0])
+            v[("B", n)].copy_(host[n][1])
+        v["x"].copy_(x_h)
+        v["W"].copy_(Wb_h[k])
+        v["q"].copy_(Q_h[k][0])
+        v["s"].copy_(Q_h[k][1])
+        hin.append(buf)
     sets = []
     for _ in range(2):
-        sets.append({
-            "hC": {n: torch.empty((n, n), dtype=torch.float16).pin_memory() for n in SWEEP},
-            "hyb": torch.empty(DEC_N, dtype=torch.float32).pin_memory(),
-            "hyq": torch.empty(DEC_N, dtype=torch.float32).pin_memory(),
-            "dA": {n: torch.empty_like(hA[n], device=dev) for n in SWEEP},
-            "dB": {n: torch.empty_like(hB[n], device=dev) for n in SWEEP},
-            "dC": {n: torch.empty((n, n), dtype=torch.float16, device=dev) for n in SWEEP},
-            "dx": torch.empty_like(hx, device=dev),
-            "dW": torch.empty_like(hW[0], device=dev),
-            "dq": torch.empty_like(hQ[0][0], device=dev),
-            "ds": torch.empty_like(hQ[0][1], device=dev),
-            "dyb": torch.empty(DEC_N, dtype=torch.float32, device=dev),
-            "dyq": torch.empty(DEC_N, dtype=torch.float32, device=dev),
-            # step i's input copies done / compute done / result copies done
-            "in": torch.cuda.Event(), "comp": torch.cuda.Event(), "out": torch.cuda.Event(),
-        })
-    h2d = sum(hA[n].numel() * 2 + hB[n].numel() * 2 for n in SWEEP) + hx.numel() * 2 + hW[0].numel() * 2 \
-        + hQ[0][0].numel() + hQ[0][1].numel() * 2
-    d2h = sum(n * n * 2 for n in SWEEP) + 2 * DEC_N * 4
+        din, dv = _packed(in_specs, on_dev)
+        dout, ov = _packed(out_specs, on_dev)
+        hout, hv = _packed(out_specs, pinned)
+        sets.append({"din": din, "dv": dv, "dout": dout, "ov": ov, "hout": hout, "hv": hv,
+                     # step i's input copy done / compute done / result copy done
+                     "in": torch.cuda.Event(), "comp": torch.cuda.Event(), "out": torch.cuda.Event()})
+    h2d = hin[0].numel()
+    d2h = sets[0]["dout"].numel()
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     s_c = stream
 
     def e2e_step(i):
         b = sets[i % 2]
+        dv, ov = b["dv"], b["ov"]
         with torch.cuda.stream(s_in):
             s_in.wait_event(b["comp"])  # step i-2 no longer reads this set's inputs
-            for n in SWEEP:
-                b["dA"][n].copy_(hA[n], non_blocking=True)
-                b["dB"][n].copy_(hB[n], non_blocking=True)
-            b["dx"].copy_(hx, non_blocking=True)
-            b["dW"].copy_(hW[i % 2], non_blocking=True)
-            b["dq"].copy_(hQ[i % 2][0], non_blocking=True)
-            b["ds"].copy_(hQ[i % 2][1], non_blocking=True)
+            b["din"].copy_(hin[i % 2], non_blocking=True)
             b["in"].record(s_in)
         s_c.wait_event(b["in"])
         s_c.wait_event(b["out"])  # step i-2's results have left this set's outputs
         for n in SWEEP:
             if gws is None:
-                sdt.gemm_f16(b["dA"][n], b["dB"][n], b["dC"][n], stream=s_c)
+                sdt.gemm_f16(dv[("A", n)], dv[("B", n)], ov[("C", n)], stream=s_c)
             else:
-                sdt.gemm_f16_ws(b["dA"][n], b["dB"][n], b["dC"][n], workspace=gws, stream=s_c)
-        sdt.gemv_m1(b["dx"], b["dW"], y=b["dyb"], stream=s_c)
-        sdt.gemv_m1(b["dx"], b["dq"], b["ds"], y=b["dyq"], stream=s_c)
+                sdt.gemm_f16_ws(dv[("A", n)], dv[("B", n)], ov[("C", n)], workspace=gws, stream=s_c)
+        sdt.gemv_m1(dv["x"], dv["W"], y=ov["yb"], stream=s_c)
+        sdt.gemv_m1(dv["x"], dv["q"], dv["s"], y=ov["yq"], stream=s_c)
         b["comp"].record(s_c)
         with torch.cuda.stream(s_out):
             s_out.wait_event(b["comp"])
-            for n in SWEEP:
-                b["hC"][n].copy_(b["dC"][n], non_blocking=True)
-            b["hyb"].copy_(b["dyb"], non_blocking=True)
-            b["hyq"].copy_(b["dyq"], non_blocking=True)
+            b["hout"].copy_(b["dout"], non_blocking=True)
             b["out"].record(s_out)
 
     for i in range(2):
@@ -897,17 +909,18 @@ def run_e2e(args, dev, host, Wb_h, Q_h, stream, gws=None):
     ref = {n: torch.empty((n, n), dtype=torch.float16, device=dev) for n in SWEEP}
     for n in SWEEP:
         if gws is None:
-            sdt.gemm_f16(last["dA"][n], last["dB"][n], ref[n])
+            sdt.gemm_f16(last["dv"][("A", n)], last["dv"][("B", n)], ref[n])
         else:
-            sdt.gemm_f16_ws(last["dA"][n], last["dB"][n], ref[n], workspace=gws)
+            sdt.gemm_f16_ws(last["dv"][("A", n)], last["dv"][("B", n)], ref[n], workspace=gws)
     torch.cuda.synchronize()
-    ok = all(torch.equal(last["hC"][n], ref[n].cpu()) for n in SWEEP)
+    ok = all(torch.equal(last["hv"][("C", n)], ref[n].cpu()) for n in SWEEP)
     world = dist_env()[0]
     max_s = max_over_ranks(secs, device=dev)
     return {"value": round(aggregate_value(step_flops(), steps, world, max_s) / 1e12, 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
             "ms_per_step": round(max_s * 1e3 / steps, 3), "results_match_device_run": ok,
-            "overlap": "inputs of step i+1 in, step i computed, results of step i-1 out, on three streams"}
+            "overlap": "inputs of step i+1 in, step i computed, results of step i-1 out, on three streams; one "
+                       "copy each way per step (the step's inputs and results in one pinned staging buffer each)"}
 
 
 # ---------------------------------------------------------------------------------------------

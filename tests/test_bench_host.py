@@ -232,3 +232,19 @@ def test_cpu_baseline_leg_reports_all_threads_and_one(monkeypatch):
     # benchmark runs a calibration leg first) still uses every thread
     assert oracle.max_threads() == before
     assert bench.cpu_baseline_leg(host, None, budget_flops=1e6, check=False)[0]["cores"] == before
+
+
+def test_packed_staging_buffer_views():
+    # the end-to-end leg's staging buffers: 256-byte aligned views that alias one buffer
+    import torch
+
+    import bench
+
+    specs = [("a", (3, 5), torch.float16), ("b", (7,), torch.float32), ("c", (2, 2, 2), torch.int8)]
+    buf, v = bench._packed(specs, lambda n: torch.zeros(n, dtype=torch.uint8))
+    assert buf.numel() == 768
+    offs = {k: t.data_ptr() - buf.data_ptr() for k, t in v.items()}
+    assert offs == {"a": 0, "b": 256, "c": 512}
+    assert all(tuple(v[k].shape) == shape and v[k].dtype == dt for k, shape, dt in specs)
+    v["b"].fill_(2.0)
+    assert torch.equal(buf[256:284].view(torch.float32), torch.full((7,), 2.0))
