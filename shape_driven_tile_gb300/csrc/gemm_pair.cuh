@@ -105,11 +105,6 @@ __device__ __forceinline__ void pair_item(int item, const GemmArgs &p, int &tile
     tile_coords(tile, p.num_m_tiles, p.num_n_tiles, p.raster_group, m_tile, n_tile);
 }
 
-// Workspace slot of a k-split tail item's partial: item h = item - tail_start, this CTA
-// (rank) and epilogue warp q own 32 rows x BN fp32 values.  Within the slot, columns
-// [c, c+32) of lane l (row l of the warp's 32) are the eight float4 at float offsets
-// c*32 + j*128 + l*4, j = 0..7: a warp's 16-byte stores and loads each cover 512
-// contiguous bytes, and any run of whole 32-column chunks is one contiguous range.
 // Copy buffers (and mbarriers) per epilogue warp for a k-split tail's partials (S >= 3),
 // and the 32-column chunks of the other partial a warp keeps in flight when S == 2.
 constexpr int kTailBufs = 4;
@@ -149,9 +144,24 @@ __device__ __forceinline__ unsigned *pair_tail_counter(const GemmArgs &p, int h,
     return p.counters + (static_cast<size_t>(h / p.tail_splits) * 2 + rank) * 4 + static_cast<size_t>(q);
 }
 
+// Workspace slot of a k-split tail item's partial: item h = item - tail_start, this CTA
+// (rank) and epilogue warp q own 32 rows x BN fp32 values.  Within the slot, columns
+// [c, c+32) of lane l (row l of the warp's 32) are the eight float4 at float offsets
+// c*32 + j*128 + l*4, j = 0..7: a warp's 16-byte stores and loads each cover 512
+// contiguous bytes, and any run of whole 32-column chunks is one contiguous range.
 template <int BN>
 __device__ __forceinline__ float *pair_tail_slot(const GemmArgs &p, int h, uint32_t rank, int q) {
     return p.partials + ((static_cast<size_t>(h) * 2 + rank) * 4 + static_cast<size_t>(q)) * (32 * BN);
+}
+
+// The first `chunks` (at most kTailAhead) 32-column chunks of a partial, lane's row.
+__device__ __forceinline__ void pair_tail_load_ahead(const float4 *oth, int chunks, float4 (&ahead)[kTailAhead][8]) {
+#pragma unroll
+    for (int d = 0; d < kTailAhead; ++d)
+        if (d < chunks) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) ahead[d][j] = __ldcg(oth + d * 256 + 32 * j);
+        }
 }
 
 // Epilogue of one k-split tail item, for one warp's 32 rows (lane = row).  A warp
@@ -167,15 +177,6 @@ __device__ __forceinline__ float *pair_tail_slot(const GemmArgs &p, int h, uint3
 // ahead / peeked: with S == 2, a warp that saw the other split's count while its own
 // accumulator was still being computed has the first kTailAhead chunks of the other
 // partial in `ahead` already and is the last (peeked).
-__device__ __forceinline__ void pair_tail_load_ahead(const float4 *oth, int chunks, float4 (&ahead)[kTailAhead][8]) {
-#pragma unroll
-    for (int d = 0; d < kTailAhead; ++d)
-        if (d < chunks) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) ahead[d][j] = __ldcg(oth + d * 256 + 32 * j);
-        }
-}
-
 template <int BN>
 __device__ __forceinline__ bool pair_tail_epilogue(const GemmArgs &p, const CUtensorMap *tmC, uint32_t taddr,
                                                    uint32_t stage_smem, uint32_t stage_bytes, uint32_t red_bar,
