@@ -513,8 +513,17 @@ __device__ __forceinline__ float reduce_rows(float (&v)[RB], int lane) {
 template <int GT, int RB>
 struct DpBatch {
     uint32_t w[RB][GT][8];  // 32 int8 weights per (row, group)
-    float s[RB][GT];        // that group's scale
+    uint16_t s[RB][GT];     // that group's scale (fp16 bits, converted where it is used)
 };
+
+// Read-only 2-byte load kept in program order with the weight loads, so that a
+// batch's scales are requested with its weights and waited for only where they are
+// used (a plain load converted on arrival would wait for its data where it is issued).
+__device__ __forceinline__ uint16_t ld_nc_u16(const __half *p) {
+    uint16_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.b16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
 
 template <bool EF, int GT, int RB>
 __device__ __forceinline__ void dp_load(DpBatch<GT, RB> &b, int n0, int r_end, int K, int G, const int (&g)[GT],
@@ -529,11 +538,11 @@ __device__ __forceinline__ void dp_load(DpBatch<GT, RB> &b, int n0, int r_end, i
                 // (a run-time choice here would merge the two loads' registers and wait for each)
                 if (EF) ld_stream_v8_hint(W + size_t(n) * K + size_t(g[i]) * 32, pol, b.w[r][i]);
                 else ld_stream_v8(W + size_t(n) * K + size_t(g[i]) * 32, b.w[r][i]);
-                b.s[r][i] = __half2float(scales[size_t(n) * G + g[i]]);
+                b.s[r][i] = ld_nc_u16(scales + size_t(n) * G + g[i]);
             } else {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) b.w[r][i][j] = 0u;
-                b.s[r][i] = 0.f;
+                b.s[r][i] = 0;
             }
         }
     }
@@ -559,9 +568,8 @@ __device__ __forceinline__ void dp_prefetch_rows(int r0, int r1, int K, int G, c
 // sums added in warp order by threads 0..RB-1 (one barrier; `red` alternates
 // between two buffers by batch, so the next batch's writes cannot race the reads).
 template <int RB>
-__device__ __forceinline__ void store_rows(float (&p)[RB], int n0, int r_end, float *red, float *__restrict__ y) {
+__device__ __forceinline__ void store_warp_sums(float v, int n0, int r_end, float *red, float *__restrict__ y) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const float v = reduce_rows<RB>(p, lane);
     constexpr int kLanesPerRow = 32 / RB;
     if (lane % kLanesPerRow == 0) red[warp * RB + lane / kLanesPerRow] = v;
     __syncthreads();
@@ -572,10 +580,14 @@ __device__ __forceinline__ void store_rows(float (&p)[RB], int n0, int r_end, fl
     }
 }
 
+template <int RB>
+__device__ __forceinline__ void store_rows(float (&p)[RB], int n0, int r_end, float *red, float *__restrict__ y) {
+    store_warp_sums<RB>(reduce_rows<RB>(p, threadIdx.x & 31), n0, r_end, red, y);
+}
+
 template <int GT, int RB>
-__device__ __forceinline__ void dp_finish(const DpBatch<GT, RB> &b, int n0, int r_end, const uint32_t (&xi)[GT][16],
-                                          const float (&xf)[GT], float *red, float *__restrict__ y) {
-    float p[RB];
+__device__ __forceinline__ void dp_dot(const DpBatch<GT, RB> &b, const uint32_t (&xi)[GT][16], const float (&xf)[GT],
+                                       float (&p)[RB]) {
 #pragma unroll
     for (int r = 0; r < RB; ++r) {
         p[r] = 0.f;
@@ -587,10 +599,9 @@ __device__ __forceinline__ void dp_finish(const DpBatch<GT, RB> &b, int n0, int 
                 acc = dp2a_lo(xi[i][2 * j], b.w[r][i][j], acc);
                 acc = dp2a_hi(xi[i][2 * j + 1], b.w[r][i][j], acc);
             }
-            p[r] = fmaf(float(acc), b.s[r][i] * xf[i], p[r]);
+            p[r] = fmaf(float(acc), __half2float(__ushort_as_half(b.s[r][i])) * xf[i], p[r]);
         }
     }
-    store_rows<RB>(p, n0, r_end, red, y);
 }
 
 template <int GT, int RB, bool EF, int MINB = 1>
@@ -670,22 +681,30 @@ __global__ void __launch_bounds__(kDpMaxThreads, MINB)
         }
     }
 
-    // batch pipeline: while one register set is summed, the other is in flight
+    // batch pipeline: while one register set is summed, the other is in flight.  A
+    // set's next rows are requested once its dot products are formed and summed within
+    // the warp (one register per thread then holds them), before the cross-warp sum and
+    // its barrier, so that two batches stay in flight through the sum.
     int n0 = r_begin, parity = 0;
     while (n0 < r_end) {
-        dp_finish(ba, n0, r_end, xi, xf, red[parity], y);
-        parity ^= 1;
+        float p[RB];
+        dp_dot(ba, xi, xf, p);
+        float v = reduce_rows<RB>(p, threadIdx.x & 31);
         if (n0 + 2 * RB < r_end) {
             dp_load<EF>(ba, n0 + 2 * RB, r_end, K, G, g, W, scales, pol);
             if (ahead) dp_prefetch_rows(n0 + 2 * RB + ahead, min(n0 + 3 * RB + ahead, r_end), K, G, W, scales);
         }
-        if (n0 + RB >= r_end) break;
-        dp_finish(bb, n0 + RB, r_end, xi, xf, red[parity], y);
+        store_warp_sums<RB>(v, n0, r_end, red[parity], y);
         parity ^= 1;
+        if (n0 + RB >= r_end) break;
+        dp_dot(bb, xi, xf, p);
+        v = reduce_rows<RB>(p, threadIdx.x & 31);
         if (n0 + 3 * RB < r_end) {
             dp_load<EF>(bb, n0 + 3 * RB, r_end, K, G, g, W, scales, pol);
             if (ahead) dp_prefetch_rows(n0 + 3 * RB + ahead, min(n0 + 4 * RB + ahead, r_end), K, G, W, scales);
         }
+        store_warp_sums<RB>(v, n0 + RB, r_end, red[parity], y);
+        parity ^= 1;
         n0 += 2 * RB;
     }
 }
@@ -790,7 +809,8 @@ __global__ void __launch_bounds__(kDpMaxThreads, MINB)
     // A register set's next rows are requested as soon as its dot products are formed,
     // before the cross-warp sum and its barrier, so that two batches stay in flight
     // through the sum (2 % faster back to back on GB300 at K = 4096, N = 12288; the q8
-    // kernel, at its 64-register cap, measured no gain from the same order).
+    // kernel, at its 64-register cap, issues them after the warp's butterfly instead,
+    // where its per-row partials have shrunk to one register).
     int n0 = r_begin, parity = 0;
     while (n0 < r_end) {
         float p[RB];
@@ -1202,7 +1222,7 @@ static bool try_ring(bool q8, int64_t K, int64_t N, const void *x, const void *W
 
 // Bytes of its weight rows each decode CTA asks L2 for before waiting on the
 // previous kernel (SDT_GEMV_L2_PREFETCH_KB overrides; 0 turns the prefetch off).
-// Measured best on GB300 at K=4096, N=12288: 8 KB (two rows) for q8, 32 KB (four
+// Measured best on GB300 at K=4096, N=12288: 12 KB (three rows) for q8, 32 KB (four
 // rows) for bf16; larger prefetches compete with the previous kernel's last loads.
 static uint32_t gemv_l2_prefetch_bytes(uint32_t default_kb) {
     if (const char *s = getenv("SDT_GEMV_L2_PREFETCH_KB")) {
@@ -1243,7 +1263,7 @@ static cudaError_t launch_q8_dp(int K, int N, const void *x, const void *W, cons
     const int grid = int(std::min<int64_t>(int64_t(occ) * dev.sm_count, N));
     return launch_kernel(kern, dim3(grid), dim3(T), 0, s, 1, K, N, static_cast<const uint4 *>(x),
                          static_cast<const uint8_t *>(W), static_cast<const __half *>(sc), y,
-                         gemv_l2_prefetch_bytes(8), gemv_l2_ahead_rows(RB));
+                         gemv_l2_prefetch_bytes(12), gemv_l2_ahead_rows(RB));
 }
 
 // Launches the bf16 row-range kernel: T = ceil(U / GT) threads (U = K/16 units of
