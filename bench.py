@@ -572,6 +572,7 @@ def run_default(args):
 
     # the decode protocol (after the timed region): 200 back-to-back launches x 10 repeats
     dec_proto = None
+    ev_cost = event_pair_cost(stream, dev) if rank == 0 else None
     if rank == 0:
         with ClockSampler(local) as dclk:
             dec_proto = decode_protocol(x, Wb, Wq, Sq, yb, peaks, stream)
@@ -632,7 +633,8 @@ def run_default(args):
                                   "graph-replayed steps: the GEMMs up to 1024^3 and the two decode GEMVs on two side "
                                   "streams beside the larger GEMMs (fork and join per step); instrumented steps serial",
                    "clock_warmup": f"{clock_warm_s:.2f} s of whole steps right before the timed region",
-                   "clocks": "nvidia-smi every 50 ms over the clock warm-up and the timed region"},
+                   "clocks": "nvidia-smi every 50 ms over the clock warm-up and the timed region",
+                   "event_pair_around_one_element_fill_us": ev_cost},
         "roofline": {"bound": "tensor", "kernel": f"{gemm_name} {dom}^3 ({tiles[dom]}{last_round_note(dom, tiles[dom], gws)})",
                      "largest_share_in_step": f"{gemm_name} {largest_share}^3",
                      "achieved": round(achieved, 1), "peak": peaks["tflops"], "unit": "TFLOP/s",
@@ -659,6 +661,27 @@ def run_default(args):
         "receipt": receipt(dev, warmup_s, clock_warm_s, state_before, state_after),
     }
     print(json.dumps(out), flush=True)
+
+
+def event_pair_cost(stream, dev, reps=50):
+    """What an event pair costs around a launch on this GPU: min and median of `reps` pairs
+    of timing events around a one-element fill kernel (after the timed region).  Every
+    launch of an instrumented step carries such a pair, so this is the part of the per-size
+    and decode figures there that is launch and event latency rather than the kernel."""
+    import torch
+
+    t = torch.empty(1, device=dev)
+    for _ in range(5):
+        t.fill_(1.0)
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    torch.cuda.synchronize()
+    for e0, e1 in pairs:
+        e0.record(stream)
+        t.fill_(1.0)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us = sorted(e0.elapsed_time(e1) * 1e3 for e0, e1 in pairs)
+    return {"min": round(us[0], 2), "median": round(us[len(us) // 2], 2)}
 
 
 def step_schedule(steps, instr, buffers, graphed=True):
