@@ -65,14 +65,14 @@ def bf16_ulp(x) -> np.ndarray:
 def assert_close_bf16(got, ref, K, what=""):
     """bf16 output against want = the oracle's value rounded to bf16 (nearest even):
       * |got - want| <= 1 bf16 ulp + 1e-3*sqrt(K) per element: the fp32 sum may sit on
-        the other side of a rounding boundary of want, by at most the benchmark spec's
-        accumulation bound;
+        the other side of a rounding boundary of want, by at most the stated
+        accumulation bound (max error 1e-3*sqrt(K));
       * at most 2 % of the results (at least 8) off want: the tensor cores' fp32
         accumulation error is far below half a bf16 ulp almost everywhere (measured on
         GB300 for these kernels and for cuBLAS on the same inputs: 0.02-0.43 % off), so
         nearly every result is the correctly rounded value;
       * ||got - C_ref||_F <= ||want - C_ref||_F + 1e-3 ||C_ref||_F: beyond what rounding
-        the exact product to bf16 costs, the benchmark spec's relative Frobenius bound."""
+        the exact product to bf16 costs, the stated relative Frobenius bound (1e-3)."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (got.shape, ref.shape)

@@ -137,7 +137,7 @@ def test_q8_wide_dynamic_range(cuda_device):
     err = np.abs(y - ref)
     assert (err <= bound).all(), f"worst error / stated bound {np.max(err / bound):.3f}"
     assert np.linalg.norm(y - ref) <= 1e-3 * np.linalg.norm(ref)
-    # the bound is tight enough to mean something: far inside the benchmark spec's absolute bound
+    # the bound is tight enough to mean something: far inside the stated absolute bound (1e-3*sqrt(K))
     assert bound.max() <= 1e-3 * np.sqrt(K) * np.abs(ref).max()
 
 
