@@ -154,6 +154,23 @@ def test_q8_weights_16_byte_aligned(cuda_device):
     assert_close(y, oracle.gemv_q8(u16(x), q.numpy(), u16(s)), K, "q8 16-byte aligned W")
 
 
+@pytest.mark.parametrize("N", [12288, 1217])
+def test_q8_scales_2_byte_aligned(cuda_device, N):
+    # scales at an address that is 2- but not 4-byte aligned: the integer kernel loads each
+    # scale's fp16 bits on their own and asks L2 for no scale rows (that needs 16 bytes);
+    # integer inputs, so the result is exact.  N = 1217 leaves one CTA with two rows.
+    K = 4096
+    x = inputs.integers((K,), seed=103, dtype=torch.bfloat16)
+    q, s = inputs.q8_weights_exact(N, K, seed=104)
+    buf = torch.empty(N * (K // 32) + 1, dtype=torch.float16, device=cuda_device)
+    sd = buf[1:].view(N, K // 32)
+    sd.copy_(s.to(cuda_device))
+    assert sd.data_ptr() % 4 == 2
+    y = sdt.gemv_m1(x.to(cuda_device), q.to(cuda_device), sd).cpu().double().numpy()
+    sdt.check_device_status()
+    assert np.array_equal(y, oracle.gemv_q8(u16(x), q.numpy(), u16(s)))
+
+
 def test_q8_nonfinite_activation_gives_nan(cuda_device):
     K, N = 4096, 64
     x = inputs.uniform((K,), seed=101, dtype=torch.bfloat16)
