@@ -58,3 +58,9 @@ def test_kscan_and_large_legs(cuda_device):
     assert r["size"] == 8192 and r["tile"] == sdt.tile_info(sdt.pick_tile(8192, 8192, 8192))["name"]
     assert 0 < r["pct_peak_best"] < 120
     sdt.check_device_status()
+
+
+def test_event_pair_cost(cuda_device):
+    cost = bench.event_pair_cost(torch.cuda.current_stream(), cuda_device, reps=8)
+    assert set(cost) == {"min", "median"}
+    assert 0 < cost["min"] <= cost["median"] < 1e4  # microseconds
